@@ -1,0 +1,330 @@
+"""Pins of the CPU oracle to things other than itself (closed forms, invariants,
+brute force, library routines, the pages' printed constants).  CPU only."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+import synth
+from tests import _seqref
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def small_shape(**kw):
+    base = synth.TINY.replace(window=8, max_slots=3)
+    return base.replace(**kw)
+
+
+@pytest.fixture(scope="module")
+def tiny_w8():
+    s = small_shape()
+    w = synth.make_weights(s, seed=3, gain_std=0.1)
+    return s, w
+
+
+# ----------------------------------------------------------------------------- RMSNorm
+
+def test_rmsnorm_constant_vector_closed_form():
+    n, c, eps = 64, -0.37, 1e-8
+    g = synth.normal_f32(5, 0, n, 1.0, 0.2)
+    out = oracle.rmsnorm(np.full(n, c), g, eps)
+    expect = c / np.sqrt(c * c + eps) * g.astype(np.float64)
+    np.testing.assert_allclose(out, expect, rtol=1e-14, atol=0)
+    # sign of the constant times the gain, to within eps
+    np.testing.assert_allclose(out, -g.astype(np.float64), rtol=1e-6)
+
+
+def test_rmsnorm_scale_invariance_and_library():
+    x = synth.normal_f32(6, 0, 300).astype(np.float64)
+    g = synth.normal_f32(6, 1, 300, 1.0, 0.3)
+    a = oracle.rmsnorm(x, g, 1e-8)
+    b = oracle.rmsnorm(17.0 * x, g, 1e-8)
+    np.testing.assert_allclose(a, b, rtol=1e-8)   # differs by ~eps/2 relative
+    ref = F.rms_norm(torch.from_numpy(x), (300,), torch.from_numpy(g.astype(np.float64)), 1e-8)
+    np.testing.assert_allclose(a, ref.numpy(), rtol=1e-13, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------- RoPE
+
+@pytest.mark.parametrize("hd", [64, 128])
+def test_rope_complex_closed_form(hd):
+    v = synth.normal_f32(7, hd, hd).astype(np.float64)
+    for p in (0, 1, 5, 257, 2999, 8191):
+        out = oracle.rope(v, p)
+        z = v[0::2] + 1j * v[1::2]
+        i = np.arange(hd // 2)
+        z = z * np.exp(1j * p * 10000.0 ** (-2.0 * i / hd))
+        np.testing.assert_allclose(out[0::2], z.real, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(out[1::2], z.imag, rtol=0, atol=1e-12)
+
+
+def test_rope_invariants():
+    hd = 128
+    q = synth.normal_f32(8, 0, hd).astype(np.float64)
+    k = synth.normal_f32(8, 1, hd).astype(np.float64)
+    np.testing.assert_array_equal(oracle.rope(q, 0), q)                      # R(0) = I
+    for p in (3, 100, 4000):
+        assert abs(np.linalg.norm(oracle.rope(q, p)) - np.linalg.norm(q)) < 1e-12  # rotation
+    # <R(p) q, R(p') k> depends only on p - p'
+    a = oracle.rope(q, 1000) @ oracle.rope(k, 990)
+    b = oracle.rope(q, 10) @ oracle.rope(k, 0)
+    c = oracle.rope(q, 7010) @ oracle.rope(k, 7000)
+    assert abs(a - b) < 1e-9 and abs(c - b) < 1e-9
+
+
+# ----------------------------------------------------------------------------- attention
+
+def test_attention_single_key_returns_value():
+    q = synth.normal_f32(9, 0, 64).astype(np.float64)
+    K = synth.normal_f32(9, 1, 64).astype(np.float64).reshape(1, 64)
+    V = synth.normal_f32(9, 2, 64).astype(np.float64).reshape(1, 64)
+    np.testing.assert_allclose(oracle.attention(q, K, V), V[0], rtol=0, atol=1e-15)
+
+
+def test_attention_equal_keys_average_values():
+    q = synth.normal_f32(10, 0, 64).astype(np.float64)
+    K = np.tile(synth.normal_f32(10, 1, 64).astype(np.float64), (7, 1))
+    V = synth.normal_f32(10, 2, 7 * 64).astype(np.float64).reshape(7, 64)
+    np.testing.assert_allclose(oracle.attention(q, K, V), V.mean(0), rtol=1e-13, atol=1e-15)
+
+
+def test_attention_matches_library_sdpa():
+    for n in (1, 2, 16, 300):
+        q = synth.normal_f32(11, n, 128, 0.0, 2.0).astype(np.float64)
+        K = synth.normal_f32(12, n, n * 128, 0.0, 2.0).astype(np.float64).reshape(n, 128)
+        V = synth.normal_f32(13, n, n * 128).astype(np.float64).reshape(n, 128)
+        ref = F.scaled_dot_product_attention(torch.from_numpy(q)[None, None, None],
+                                             torch.from_numpy(K)[None, None],
+                                             torch.from_numpy(V)[None, None])[0, 0, 0].numpy()
+        np.testing.assert_allclose(oracle.attention(q, K, V), ref, rtol=1e-11, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- stream layout
+
+def test_golden_stream_layout_matches_workload_constants():
+    g = json.load(open(os.path.join(GOLDEN, "stream_layout.json")))
+    assert tuple(g["delays"]) == synth.DELAYS
+    assert g["n_streams"] == synth.N_STREAMS == 1 + synth.FULL.n_q
+    assert [synth.DELAYS[k] for k in g["semantic_rows"]] == [0, 0]
+    assert g["frame_ms"] * (1 + g["acoustic_delay_frames"]) == g["theoretical_latency_ms"]
+
+
+def test_golden_bitrate_closed_form():
+    g = json.load(open(os.path.join(GOLDEN, "mimi_bitrate.json")))
+    bits = g["frame_rate_hz"] * g["codebooks_per_side"] * np.log2(g["card"])
+    assert bits == pytest.approx(g["bitrate_kbps"] * 1000)
+    assert g["sample_rate_hz"] / g["frame_rate_hz"] == g["samples_per_frame"]
+    assert synth.FULL.card == g["card"] and synth.FULL.n_q == 2 * g["codebooks_per_side"]
+
+
+# ----------------------------------------------------------------------------- delay schedule
+
+def expected_rows(s, chosen):
+    """brute force: row read by stream k at step p is chosen[p-1-delay[k]][k] or INIT."""
+    T = chosen.shape[0]
+    X = np.empty((T, 17), np.int64)
+    for p in range(T):
+        for k in range(17):
+            f = p - 1 - s.delays[k]
+            X[p, k] = chosen[f, k] if f >= 0 else (s.text_vocab if k == 0 else s.card)
+    return X
+
+
+def test_delay_schedule_forced_bit_exact(tiny_w8):
+    s, w = tiny_w8
+    T = 12
+    z = synth.forced_frames(s, 21, synth.STREAM_FORCED, T, 1)[:, 0]
+    o = oracle.Oracle(s, w)
+    rows, outs = [], []
+    for p in range(T):
+        r = o.step([0], z[p:p + 1], want_tokens=True)
+        rows.append(r["x_tokens"][0])
+        outs.append(r)
+    np.testing.assert_array_equal(np.array(rows), expected_rows(s, z))
+    # every (stream, frame) comes out exactly once, at step frame + delay
+    for p, r in enumerate(outs):
+        assert r["text"][0] == z[p, 0]
+        for k in range(1, 17):
+            f = p - s.delays[k]
+            assert r["codes"][0, k - 1] == (z[f, k] if f >= 0 else -1)
+
+
+def test_delay_schedule_free_running(tiny_w8):
+    """Generated rows: the input column at step p is the column chosen at earlier steps."""
+    s, w = tiny_w8
+    T = 10
+    inp = synth.user_frames(s, 22, T, 1)[:, 0]
+    o = oracle.Oracle(s, w)
+    res = [o.step([0], inp[p:p + 1], want_tokens=True) for p in range(T)]
+    chosen = np.full((T, 17), -7, np.int64)
+    for p, r in enumerate(res):
+        chosen[p, 0] = r["text"][0]
+        for k in range(1, 17):
+            f = p - s.delays[k]
+            if f >= 0:
+                chosen[f, k] = r["codes"][0, k - 1]
+    # user rows come out as supplied
+    for p in range(T):
+        for k in range(9, 17):
+            f = p - s.delays[k]
+            if f >= 0:
+                assert chosen[f, k] == inp[f, k]
+    X = np.array([r["x_tokens"][0] for r in res])
+    exp = expected_rows(s, chosen)
+    np.testing.assert_array_equal(X, exp)
+    assert (X >= 0).all()
+
+
+# ----------------------------------------------------------------------------- model
+
+@pytest.mark.parametrize("T", [20])
+def test_oracle_matches_whole_sequence_library_forward(tiny_w8, T):
+    """Step-by-step oracle (ring of W=8) == whole-sequence masked forward, in fp64."""
+    s, w = tiny_w8
+    z = synth.forced_frames(s, 31, synth.STREAM_FORCED, T, 1)[:, 0]
+    o = oracle.Oracle(s, w)
+    tl, dl = [], []
+    for p in range(T):
+        r = o.step([0], z[p:p + 1], want_logits=True)
+        tl.append(r["text_logits"][0])
+        dl.append(r["dep_logits"][0])
+    ref_t, ref_d = _seqref.forward(s, w, z)
+    tl, dl = np.array(tl), np.array(dl)
+    np.testing.assert_allclose(tl, ref_t, rtol=0, atol=1e-10 * np.abs(ref_t).max())
+    np.testing.assert_allclose(dl, ref_d, rtol=0, atol=1e-10 * np.abs(ref_d).max())
+
+
+def test_oracle_matches_library_forward_bf16_weights():
+    s = small_shape(weight_dtype="bf16", kv_dtype="bf16", window=5)
+    w = synth.make_weights(s, seed=4, gain_std=0.1)
+    T = 9
+    z = synth.forced_frames(s, 32, synth.STREAM_FORCED, T, 1)[:, 0]
+    o = oracle.Oracle(s, w)
+    res = [o.step([0], z[p:p + 1], want_logits=True) for p in range(T)]
+    ref_t, ref_d = _seqref.forward(s, w, z)
+    tl = np.array([r["text_logits"][0] for r in res])
+    dl = np.array([r["dep_logits"][0] for r in res])
+    np.testing.assert_allclose(tl, ref_t, rtol=0, atol=1e-10 * np.abs(ref_t).max())
+    np.testing.assert_allclose(dl, ref_d, rtol=0, atol=1e-10 * np.abs(ref_d).max())
+
+
+def test_ring_equals_brute_force_history(tiny_w8):
+    """Ring storage at position mod W == every position kept and masked to the last W."""
+    s, w = tiny_w8
+    T = 40
+    inp = synth.user_frames(s, 23, T, 1)[:, 0]
+    a, b = oracle.Oracle(s, w), oracle.Oracle(s, w, brute_force=True)
+    for p in range(T):
+        ra = a.step([0], inp[p:p + 1], want_logits=True)
+        rb = b.step([0], inp[p:p + 1], want_logits=True)
+        for key in ra:
+            np.testing.assert_array_equal(ra[key], rb[key])
+
+
+def test_window_actually_limits_context(tiny_w8):
+    """Tokens older than the window (through every layer) cannot change the output."""
+    s, w = tiny_w8
+    reach = 2 + s.n_layers * (s.window - 1)   # frame 0 enters positions 1..2; each layer
+    T = reach + 4                             # widens the receptive field by W - 1
+    z1 = synth.forced_frames(s, 41, synth.STREAM_FORCED, T, 1)[:, 0]
+    z2 = z1.copy()
+    z2[0] = synth.forced_frames(s, 42, synth.STREAM_FORCED, 1, 1)[0, 0]   # change frame 0 only
+    outs = []
+    for z in (z1, z2):
+        o = oracle.Oracle(s, w)
+        outs.append([o.step([0], z[p:p + 1], want_logits=True)["text_logits"][0] for p in range(T)])
+    assert not np.array_equal(outs[0][3], outs[1][3])
+    assert not np.array_equal(outs[0][reach], outs[1][reach])
+    for p in range(reach + 1, T):
+        np.testing.assert_array_equal(outs[0][p], outs[1][p])
+
+
+def test_depformer_causality(tiny_w8):
+    """Changing the supplied code of stream j changes substeps >= j only."""
+    s, w = tiny_w8
+    z = synth.forced_frames(s, 43, synth.STREAM_FORCED, 3, 1)[:, 0]
+    base = oracle.Oracle(s, w)
+    for p in range(2):
+        base.step([0], z[p:p + 1])
+    ref = base.step([0], z[2:3], want_logits=True)["dep_logits"][0]
+    j = 9                                 # user semantic stream, delay 0: read by substep 9
+    z2 = z.copy()
+    z2[2, j] = (z2[2, j] + 1) % s.card
+    o = oracle.Oracle(s, w)
+    for p in range(2):
+        o.step([0], z2[p:p + 1])
+    alt = o.step([0], z2[2:3], want_logits=True)["dep_logits"][0]
+    np.testing.assert_array_equal(alt[:j], ref[:j])
+    assert not np.array_equal(alt[j], ref[j])
+
+
+def test_argmax_lowest_index_on_ties():
+    s = small_shape()
+    w = synth.make_weights(s, seed=5)
+    head = np.zeros_like(w["text_head"])
+    r = synth.normal_f32(44, 0, s.d, 0.0, 0.02)
+    head[5], head[9], head[2] = r, r, -r
+    w["text_head"] = head
+    o = oracle.Oracle(s, w)
+    res = o.step([0], synth.user_frames(s, 45, 1, 1)[0], want_logits=True)
+    lg = res["text_logits"][0]
+    a = lg[5]
+    assert lg[9] == a and lg[2] == -a
+    assert res["text_argmax"][0] == (5 if a > 0 else 2 if a < 0 else 0)
+    w["text_head"] = np.zeros_like(head)              # all logits 0 -> index 0
+    o = oracle.Oracle(s, w)
+    assert o.step([0], synth.user_frames(s, 45, 1, 1)[0])["text_argmax"][0] == 0
+
+
+def test_slot_isolation_and_reset(tiny_w8):
+    s, w = tiny_w8
+    T = 6
+    a = synth.user_frames(s, 46, T, 3)
+    solo, multi = oracle.Oracle(s, w), oracle.Oracle(s, w)
+    for p in range(T):
+        r1 = solo.step([1], a[p, 1:2], want_logits=True)
+        r3 = multi.step([2, 1, 0], a[p, [2, 1, 0]], want_logits=True)
+        for key in r1:
+            np.testing.assert_array_equal(r1[key][0], r3[key][1])
+    # a reset slot behaves as a fresh one
+    multi.reset_slot(1)
+    fresh = oracle.Oracle(s, w)
+    for p in range(3):
+        ra = multi.step([1], a[p, 1:2], want_logits=True)
+        rb = fresh.step([1], a[p, 1:2], want_logits=True)
+        for key in ra:
+            np.testing.assert_array_equal(ra[key], rb[key])
+
+
+def test_prefill_equals_forced_steps(tiny_w8):
+    s, w = tiny_w8
+    T = 11
+    z = synth.forced_frames(s, 47, synth.STREAM_FORCED, T, 1)[:, 0]
+    nxt = synth.user_frames(s, 48, 3, 1)[:, 0]
+    a, b = oracle.Oracle(s, w), oracle.Oracle(s, w)
+    a.prefill(0, z)
+    for p in range(T):
+        b.step([0], z[p:p + 1])
+    assert a.position(0) == b.position(0) == T
+    for p in range(3):
+        ra = a.step([0], nxt[p:p + 1], want_logits=True)
+        rb = b.step([0], nxt[p:p + 1], want_logits=True)
+        for key in ra:
+            np.testing.assert_array_equal(ra[key], rb[key])
+
+
+def test_oracle_rejects_bad_input(tiny_w8):
+    s, w = tiny_w8
+    o = oracle.Oracle(s, w)
+    bad = synth.user_frames(s, 49, 1, 1)[0]
+    bad[0, 3] = s.card
+    with pytest.raises(ValueError):
+        o.step([0], bad)
+    with pytest.raises(ValueError):
+        o.step([3], synth.user_frames(s, 49, 1, 1)[0])
+    assert o.position(0) == 0
