@@ -1,0 +1,327 @@
+"""Frame-step benchmark: aggregate frames/s and step latency of the full PersonaPlex
+shape at B = 1 (250-frame forced prompt, then decode frames), against the HBM roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+One JSON line on rank 0.  With torchrun (N > 1) every rank runs the same
+workload on its own GPU (independent replicas: slots never interact), and the
+value is all ranks' frames over the slowest rank's time.
+
+--impl reference times the CPU oracle (the plain fp64 definition) on this
+machine's host cores over a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WORKLOAD = synth.WORKLOADS["full_b1"]
+PROMPT = 250
+METRIC = "aggregate frames/s (B=1 full PersonaPlex frame step)"
+UNIT = "frames/s"
+
+
+def algorithmic_bytes(s, lens):
+    """Bytes one step must move: every streamed weight once, the embedding rows
+    read, and per slot the keys/values of its window plus this frame's writes."""
+    wb = 2 if s.weight_dtype == "bf16" else 4
+    kvb = 2 if s.kv_dtype == "bf16" else 4
+    d, F, V, C, S, L = s.d, s.ffn, s.text_vocab, s.card, s.dep_steps, s.n_layers
+    dd, dF, dL = s.dep_d, s.dep_ffn, s.dep_layers
+    weights = L * (4 * d * d + 3 * F * d) * wb + (V + S * dd) * d * wb
+    weights += S * (dL * (4 * dd * dd + 3 * dd * dF) + C * dd) * wb
+    per_slot_rows = 17 * d * wb + S * dd * wb
+    kv_pos = L * 2 * d * kvb
+    return weights + sum(per_slot_rows + ln * kv_pos + kv_pos for ln in lens)
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "full_duplex_speech_frame_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None if the kernel source changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", f"step_kernel_{workload}.txt")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_digest") != kernel_source_digest():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo")
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_sample(frames=6, prompt=8):
+    """Time the CPU oracle on a bounded sample of the workload: a short forced
+    prompt (untimed), then `frames` decode frames (timed)."""
+    import oracle
+    s = WORKLOAD.shape
+    w = synth.make_weights(s, WORKLOAD.weight_seed)
+    orc = oracle.Oracle(s, w)
+    orc.prefill(0, synth.forced_frames(s, WORKLOAD.input_seed, synth.STREAM_PROMPT, prompt, 1)[:, 0])
+    u = synth.user_frames(s, WORKLOAD.input_seed, frames, 1)
+    t0 = time.perf_counter()
+    for p in range(frames):
+        orc.step([0], u[p])
+    dt = time.perf_counter() - t0
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": frames / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{frames} decode frames of the full shape at B=1 after a {prompt}-frame prompt "
+                      f"(fp64 oracle, OpenMP over output rows); {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    frames = max(1, min(args.steps, 6))
+    cb = cpu_oracle_sample(frames=frames)
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": args.gpus,
+            "steps": frames, "warmup": 0, "ms_per_step": 1000.0 / cb["value"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "full_b1: full PersonaPlex shape, bf16 weights N(0,0.02) seed 0, B=1, "
+                                   "forced prompt then decode frames, greedy", "batch": 1},
+            "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, rank, world):
+    import torch
+    from full_duplex_speech_frame_gb300 import mfs
+    from tests import _harness as H
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    s = WORKLOAD.shape
+    n = WORKLOAD.batch
+    need = args.warmup + 2 * args.steps
+    if PROMPT + need > s.max_pos:
+        raise SystemExit("too many steps for the position range")
+    w = synth.make_weights(s, WORKLOAD.weight_seed)
+    ctx = H.gpu_context(s, w)
+    del w
+    prompt = synth.forced_frames(s, WORKLOAD.input_seed, synth.STREAM_PROMPT, PROMPT, n)
+    mfs.mfs_prefill(ctx, list(range(n)), prompt.transpose(1, 0, 2))
+    frames = synth.user_frames(s, WORKLOAD.input_seed, need, n)
+    slots = list(range(n))
+    d_codes = torch.from_numpy(frames).cuda()
+    d_text = torch.empty(n, dtype=torch.int32, device="cuda")
+    d_out = torch.empty(n, 16, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    # warm-up
+    for p in range(args.warmup):
+        mfs.mfs_step_device(ctx, slots, d_codes[p], d_text, d_out)
+    mfs.mfs_sync(ctx)
+    base = args.warmup
+
+    # device-resident timed region (the value)
+    lens = []
+    for k in range(args.steps):
+        lens += [min(PROMPT + base + k + 1, s.window)] * n
+    mfs.mfs_set_timing(ctx, True)
+    mfs.mfs_kernel_time(ctx)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for k in range(args.steps):
+            mfs.mfs_step_device(ctx, slots, d_codes[base + k], d_text, d_out)
+        e1.record(stream)
+        mfs.mfs_sync(ctx)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    kms, ksteps = mfs.mfs_kernel_time(ctx)
+    mfs.mfs_set_timing(ctx, False)
+    launches = mfs.mfs_launches_per_step(ctx) * args.steps
+    ms_max = max_over_ranks(ms, world)
+    value = n * args.steps * world / (ms_max / 1000.0)
+
+    # end to end through the public host-buffer call
+    base2 = base + args.steps
+    pinned = torch.from_numpy(frames[base2:base2 + args.steps]).pin_memory().numpy()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        text, codes = mfs.mfs_step(ctx, slots, pinned[k])
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    barrier(world)
+
+    if rank != 0:
+        return
+    hbm, peak_kind = read_peaks()
+    bytes_step = algorithmic_bytes(s, lens) / args.steps
+    kernel_ms = kms / max(ksteps, 1)
+    achieved = bytes_step / (kernel_ms / 1000.0) / 1e9
+    traffic = recorded_traffic("full_b1")
+    desc_bytes = 16 + 64 * 4 * 2 + 64 * 17 * 4
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "full_b1: full PersonaPlex shape (4096-d/32-layer temporal, 1024-d/6-layer "
+                               "16-substep depformer), bf16 weights N(0,0.02) seed 0, B=1, ring prompt 250 "
+                               "forced frames, then decode frames with user rows supplied, greedy",
+                   "batch": n, "prompt_frames": PROMPT, "positions": [PROMPT + base, PROMPT + base + args.steps],
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: every step streams 16.1 GB of weights"},
+        "latency_ms_per_step": ms_max / args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": traffic, "peak_kind": f"{peak_kind} hbm_gbs",
+                     "kernel": "step_kernel (one persistent launch per step)",
+                     "kernel_ms": kernel_ms, "algorithmic_bytes_per_launch": bytes_step},
+        "e2e": {"value": n * args.steps * world / e2e_s, "unit": UNIT, "h2d_bytes_per_step": desc_bytes,
+                "d2h_bytes_per_step": n * 4 + n * 16 * 4 + 8},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_sample(frames=3)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    rank, world = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_gpu(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,788 @@
+// Host side of the C ABI declared in include/mfs.h.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <map>
+#include <new>
+#include <cstddef>
+#include <string>
+#include <vector>
+
+#include "mfs_internal.h"
+
+using namespace mfs;
+
+namespace {
+
+constexpr int SCRATCH_FLOATS = 4096;  // must match the kernels' shared-memory map
+constexpr int PREF_CHUNK = 256;       // prompt frames staged per copy
+constexpr int DESC_RING = 8;          // pinned step descriptors in flight
+
+struct CopyOp {
+    size_t dst_off;    // bytes from the region base
+    size_t src_off;    // bytes from the caller's pointer
+    size_t width;      // bytes per row
+    size_t rows;       // rows (1 = plain copy)
+    size_t dst_pitch;  // bytes between destination rows
+    size_t src_pitch;
+};
+
+struct TensorInfo {
+    int region;        // 0 = weight arena, 1 = gain arena
+    size_t bytes;
+    std::vector<CopyOp> ops;
+    bool loaded = false;
+};
+
+struct Pending {
+    int seq;
+    std::vector<int> slots;
+    std::vector<int> old_pos;
+};
+
+}  // namespace
+
+struct mfs_ctx {
+    mfs_config cfg;
+    cudaStream_t stream = nullptr;
+    bool own_stream = false;
+    int device = 0, G = 0;
+    size_t wb = 2, kvb = 2;
+    // device memory
+    char* arena = nullptr;
+    size_t arena_bytes = 0;
+    float* gains = nullptr;
+    size_t gain_bytes = 0;
+    void* kc = nullptr;
+    void* vc = nullptr;
+    int* hist = nullptr;
+    char* act = nullptr;
+    float2* rope = nullptr;
+    Phase* d_phases = nullptr;
+    StepDesc* d_desc = nullptr;
+    StepDesc* d_pref = nullptr;
+    unsigned* d_bar = nullptr;
+    int* d_err = nullptr;
+    // pinned host memory
+    StepDesc* h_desc = nullptr;  // DESC_RING entries
+    cudaEvent_t desc_ev[DESC_RING] = {};
+    int desc_next = 0;
+    StepDesc* h_pref = nullptr;
+    int* h_out = nullptr;        // text [MS] | codes [MS*16] | err | err_seq
+    // state
+    Params P;
+    int nphase = 0, nphase_prefill = 0;
+    int maxrows = 0;
+    size_t smem[3] = {0, 0, 0};
+    const void* kfn[3] = {nullptr, nullptr, nullptr};
+    std::vector<int> pos;
+    std::map<std::string, TensorInfo> tensors;
+    int mode = 0;
+    int launches = 0;
+    int seq = 0;
+    int last_n = 0;
+    bool last_full = false;
+    std::vector<Pending> pending;
+    std::string err;
+    // kernel timing
+    bool timing = false;
+    std::vector<cudaEvent_t> ev_pool;
+    size_t ev_used = 0;
+};
+
+static int fail(mfs_ctx* c, int code, const char* fmt, ...)
+{
+    if (c) {
+        char buf[512];
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(buf, sizeof buf, fmt, ap);
+        va_end(ap);
+        c->err = buf;
+    }
+    return code;
+}
+
+#define CK(call)                                                                                 \
+    do {                                                                                         \
+        cudaError_t e_ = (call);                                                                 \
+        if (e_ != cudaSuccess) return fail(c, MFS_E_CUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+    } while (0)
+
+namespace mfs {
+const void* kernel_f32_1();
+const void* kernel_f32_2();
+const void* kernel_f32_4();
+const void* kernel_bf16_1();
+const void* kernel_bf16_2();
+const void* kernel_bf16_4();
+const void* kernel_f32(int bg) { return bg == 1 ? kernel_f32_1() : bg == 2 ? kernel_f32_2() : kernel_f32_4(); }
+const void* kernel_bf16(int bg) { return bg == 1 ? kernel_bf16_1() : bg == 2 ? kernel_bf16_2() : kernel_bf16_4(); }
+}  // namespace mfs
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static int bg_index(int n) { return n <= 1 ? 0 : (n == 2 ? 1 : 2); }
+static int bg_value(int idx) { return idx == 0 ? 1 : (idx == 1 ? 2 : 4); }
+
+// ------------------------------------------------------------------ create
+
+static int check_config(mfs_ctx* c, const mfs_config& g)
+{
+    if (g.d <= 0 || g.n_layers <= 0 || g.n_heads <= 0 || g.ffn <= 0 || g.text_vocab <= 0 || g.card <= 0 ||
+        g.window <= 0 || g.max_pos <= 0 || g.dep_d <= 0 || g.dep_layers <= 0 || g.dep_heads <= 0 ||
+        g.dep_ffn <= 0)
+        return fail(c, MFS_E_ARG, "config: non-positive dimension");
+    if (g.n_q != 16 || g.dep_steps != 16) return fail(c, MFS_E_ARG, "config: n_q and dep_steps must be 16");
+    if (g.head_dim != 64 && g.head_dim != 128) return fail(c, MFS_E_ARG, "config: head_dim must be 64 or 128");
+    if (g.n_heads * g.head_dim != g.d) return fail(c, MFS_E_ARG, "config: n_heads * head_dim != d");
+    if (g.dep_head_dim != 64 || g.dep_heads * g.dep_head_dim != g.dep_d)
+        return fail(c, MFS_E_ARG, "config: dep_head_dim must be 64 and dep_heads * 64 == dep_d");
+    const int Ks[4] = {g.d, g.ffn, g.dep_d, g.dep_ffn};
+    for (int K : Ks)
+        if (K % 8 != 0 || K > 12288) return fail(c, MFS_E_ARG, "config: K dimension %d not a multiple of 8 or > 12288", K);
+    if (g.text_vocab % 2 || g.card % 2) return fail(c, MFS_E_ARG, "config: vocabularies must be even");
+    if (g.max_slots < 1 || g.max_slots > MFS_MAX_SLOTS) return fail(c, MFS_E_ARG, "config: max_slots out of range");
+    if (g.weight_dtype != MFS_DTYPE_F32 && g.weight_dtype != MFS_DTYPE_BF16) return fail(c, MFS_E_ARG, "config: weight_dtype");
+    if (g.kv_dtype != g.weight_dtype) return fail(c, MFS_E_ARG, "config: kv_dtype must equal weight_dtype");
+    for (int k = 0; k < NSTREAM; ++k)
+        if (g.delays[k] < 0 || g.delays[k] > 1) return fail(c, MFS_E_ARG, "config: delays must be 0 or 1");
+    if (g.eps <= 0 || g.rope_theta <= 0) return fail(c, MFS_E_ARG, "config: eps and rope_theta must be positive");
+    return MFS_OK;
+}
+
+static void add_tensor(mfs_ctx* c, const std::string& name, int region, size_t bytes, std::vector<CopyOp> ops)
+{
+    TensorInfo t;
+    t.region = region;
+    t.bytes = bytes;
+    t.ops = std::move(ops);
+    c->tensors[name] = t;
+}
+
+static CopyOp plain(size_t dst, size_t src, size_t bytes) { return CopyOp{dst, src, bytes, 1, bytes, bytes}; }
+
+// Gate rows go to even destination rows, up rows to odd ones.
+static void interleave(std::vector<CopyOp>& ops, size_t dst, size_t src, size_t rows_half, size_t row_bytes)
+{
+    ops.push_back(CopyOp{dst, src, row_bytes, rows_half, 2 * row_bytes, row_bytes});
+    ops.push_back(CopyOp{dst + row_bytes, src + rows_half * row_bytes, row_bytes, rows_half, 2 * row_bytes, row_bytes});
+}
+
+static int build_layout(mfs_ctx* c)
+{
+    const mfs_config& g = c->cfg;
+    const size_t wb = c->wb;
+    const size_t d = g.d, F = g.ffn, V = g.text_vocab, C = g.card, S = g.dep_steps, L = g.n_layers;
+    const size_t dd = g.dep_d, dF = g.dep_ffn, dL = g.dep_layers;
+    size_t off = 0;
+    auto region = [&](size_t elems) {
+        size_t o = off;
+        off = align_up(off + elems * wb, 256);
+        return o;
+    };
+    const size_t o_emb_text = region((V + 1) * d);
+    const size_t o_emb_audio = region(16 * (C + 1) * d);
+    const size_t o_dep_emb_text = region(V * dd);
+    const size_t o_dep_emb_audio = region((S - 1) * C * dd);
+    const size_t t_layer = 4 * d * d + 3 * F * d;
+    const size_t o_tw = region(L * t_layer);
+    const size_t o_head = region((V + S * dd) * d);
+    const size_t d_layer = 4 * dd * dd + 3 * dd * dF;
+    const size_t d_sub = dL * d_layer + C * dd;
+    const size_t o_dw = region(S * d_sub);
+    c->arena_bytes = off;
+
+    // gains (fp32)
+    size_t go = 0;
+    auto gregion = [&](size_t elems) {
+        size_t o = go;
+        go = align_up(go + elems * 4, 256);
+        return o;
+    };
+    const size_t g_attn = gregion(L * d), g_ffn = gregion(L * d), g_out = gregion(d);
+    const size_t g_dattn = gregion(dL * dd), g_dffn = gregion(dL * dd), g_dout = gregion(dd);
+    c->gain_bytes = go;
+
+    add_tensor(c, "emb.text", 0, (V + 1) * d * wb, {plain(o_emb_text, 0, (V + 1) * d * wb)});
+    add_tensor(c, "emb.audio", 0, 16 * (C + 1) * d * wb, {plain(o_emb_audio, 0, 16 * (C + 1) * d * wb)});
+    add_tensor(c, "dep.emb.text", 0, V * dd * wb, {plain(o_dep_emb_text, 0, V * dd * wb)});
+    add_tensor(c, "dep.emb.audio", 0, (S - 1) * C * dd * wb, {plain(o_dep_emb_audio, 0, (S - 1) * C * dd * wb)});
+    for (size_t l = 0; l < L; ++l) {
+        const size_t base = o_tw + l * t_layer * wb;
+        const std::string p = "layers." + std::to_string(l) + ".";
+        add_tensor(c, p + "wqkv", 0, 3 * d * d * wb, {plain(base, 0, 3 * d * d * wb)});
+        add_tensor(c, p + "wo", 0, d * d * wb, {plain(base + 3 * d * d * wb, 0, d * d * wb)});
+        std::vector<CopyOp> gu;
+        interleave(gu, base + 4 * d * d * wb, 0, F, d * wb);
+        add_tensor(c, p + "wgu", 0, 2 * F * d * wb, gu);
+        add_tensor(c, p + "wdown", 0, d * F * wb, {plain(base + (4 * d * d + 2 * F * d) * wb, 0, d * F * wb)});
+        add_tensor(c, p + "attn_norm", 1, d * 4, {plain(g_attn + l * d * 4, 0, d * 4)});
+        add_tensor(c, p + "ffn_norm", 1, d * 4, {plain(g_ffn + l * d * 4, 0, d * 4)});
+    }
+    add_tensor(c, "out_norm", 1, d * 4, {plain(g_out, 0, d * 4)});
+    add_tensor(c, "text_head", 0, V * d * wb, {plain(o_head, 0, V * d * wb)});
+    add_tensor(c, "dep.in", 0, S * dd * d * wb, {plain(o_head + V * d * wb, 0, S * dd * d * wb)});
+    for (size_t l = 0; l < dL; ++l) {
+        const std::string p = "dep.layers." + std::to_string(l) + ".";
+        std::vector<CopyOp> qkv, wo, gu, down;
+        for (size_t s = 0; s < S; ++s) {
+            const size_t base = o_dw + (s * d_sub + l * d_layer) * wb;
+            qkv.push_back(plain(base, s * 3 * dd * dd * wb, 3 * dd * dd * wb));
+            wo.push_back(plain(base + 3 * dd * dd * wb, s * dd * dd * wb, dd * dd * wb));
+            interleave(gu, base + 4 * dd * dd * wb, s * 2 * dF * dd * wb, dF, dd * wb);
+            down.push_back(plain(base + (4 * dd * dd + 2 * dF * dd) * wb, s * dd * dF * wb, dd * dF * wb));
+        }
+        add_tensor(c, p + "wqkv", 0, S * 3 * dd * dd * wb, qkv);
+        add_tensor(c, p + "wo", 0, S * dd * dd * wb, wo);
+        add_tensor(c, p + "wgu", 0, S * 2 * dF * dd * wb, gu);
+        add_tensor(c, p + "wdown", 0, S * dd * dF * wb, down);
+        add_tensor(c, p + "attn_norm", 1, dd * 4, {plain(g_dattn + l * dd * 4, 0, dd * 4)});
+        add_tensor(c, p + "ffn_norm", 1, dd * 4, {plain(g_dffn + l * dd * 4, 0, dd * 4)});
+    }
+    add_tensor(c, "dep.out_norm", 1, dd * 4, {plain(g_dout, 0, dd * 4)});
+    {
+        std::vector<CopyOp> hd;
+        for (size_t s = 0; s < S; ++s) hd.push_back(plain(o_dw + (s * d_sub + dL * d_layer) * wb, s * C * dd * wb, C * dd * wb));
+        add_tensor(c, "dep.head", 0, S * C * dd * wb, hd);
+    }
+
+    // device pointers (filled once the arenas exist)
+    Params& P = c->P;
+    P.emb_text = (void*)o_emb_text;
+    P.emb_audio = (void*)o_emb_audio;
+    P.dep_emb_text = (void*)o_dep_emb_text;
+    P.dep_emb_audio = (void*)o_dep_emb_audio;
+    P.tw = (void*)o_tw;
+    P.t_layer = (long long)t_layer;
+    P.head = (void*)o_head;
+    P.dw = (void*)o_dw;
+    P.d_layer = (long long)d_layer;
+    P.d_sub = (long long)d_sub;
+    P.attn_norm = (float*)g_attn;
+    P.ffn_norm = (float*)g_ffn;
+    P.out_norm = (float*)g_out;
+    P.dep_attn_norm = (float*)g_dattn;
+    P.dep_ffn_norm = (float*)g_dffn;
+    P.dep_out_norm = (float*)g_dout;
+    return MFS_OK;
+}
+
+static void rebase(const void*& p, char* base) { p = base + (size_t)p; }
+static void rebasef(const float*& p, float* base) { p = (const float*)((char*)base + (size_t)p); }
+
+static int max_rows(const mfs_config& g, int G)
+{
+    const long long npairs[] = {3LL * g.d / 2, g.d / 2, g.ffn, g.d / 2, (g.text_vocab + 16LL * g.dep_d) / 2,
+                                3LL * g.dep_d / 2, g.dep_d / 2, g.dep_ffn, g.dep_d / 2, g.card / 2};
+    long long m = 0;
+    for (long long np : npairs) m = (np + G - 1) / G > m ? (np + G - 1) / G : m;
+    return (int)(2 * m);
+}
+
+static thread_local std::string g_create_error;
+
+static int create_impl(mfs_ctx* c, void* cuda_stream)
+{
+    int rc = check_config(c, c->cfg);
+    if (rc != MFS_OK) return rc;
+    const mfs_config& g = c->cfg;
+    c->wb = g.weight_dtype == MFS_DTYPE_BF16 ? 2 : 4;
+    c->kvb = g.kv_dtype == MFS_DTYPE_BF16 ? 2 : 4;
+    CK(cudaGetDevice(&c->device));
+    int nsm = 0;
+    CK(cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, c->device));
+    int coop = 0;
+    CK(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, c->device));
+    if (!coop) return fail(c, MFS_E_CUDA, "device lacks cooperative launch");
+    c->G = nsm;
+    if (cuda_stream) c->stream = (cudaStream_t)cuda_stream;
+    else {
+        CK(cudaStreamCreateWithFlags(&c->stream, cudaStreamNonBlocking));
+        c->own_stream = true;
+    }
+
+    build_layout(c);
+    const size_t MS = g.max_slots, d = g.d, F = g.ffn, V = g.text_vocab, C = g.card, S = g.dep_steps;
+    const size_t dd = g.dep_d, dF = g.dep_ffn, dL = g.dep_layers, H = g.n_heads, hd = g.head_dim;
+
+    CK(cudaMalloc((void**)&c->arena, c->arena_bytes));
+    CK(cudaMalloc((void**)&c->gains, c->gain_bytes));
+    CK(cudaMemset(c->gains, 0, c->gain_bytes));
+    const size_t kv = MS * g.n_layers * (size_t)g.window * d * c->kvb;
+    CK(cudaMalloc(&c->kc, kv));
+    CK(cudaMalloc(&c->vc, kv));
+    CK(cudaMalloc((void**)&c->hist, MS * NSTREAM * HIST * sizeof(int)));
+    CK(cudaMemset(c->hist, 0xFF, MS * NSTREAM * HIST * sizeof(int)));
+
+    // activations
+    size_t ao = 0;
+    auto areg = [&](size_t bytes) {
+        size_t o = ao;
+        ao = align_up(ao + bytes, 256);
+        return o;
+    };
+    const size_t a_x = areg(MS * d * 4), a_q = areg(MS * d * 4), a_o = areg(MS * d * 4), a_s = areg(MS * F * 4);
+    const size_t a_lg = areg(MS * V * 4), a_yin = areg(MS * S * dd * 4), a_u = areg(MS * dd * 4);
+    const size_t a_dq = areg(MS * dd * 4), a_dkv = areg(MS * dL * S * 2 * dd * 4), a_dat = areg(MS * dd * 4);
+    const size_t a_ds = areg(MS * dF * 4), a_dlg = areg(MS * S * C * 4);
+    const size_t a_ap = areg(MS * H * NCHUNK_MAX * (hd + 4) * 4), a_ac = areg(MS * H * 4);
+    const size_t a_amv = areg(MS * c->G * 4), a_ami = areg(MS * c->G * 4), a_ch = areg(MS * NSTREAM * 4);
+    const size_t a_to = areg(MS * 4), a_co = areg(MS * 16 * 4), a_ta = areg(MS * 4), a_ca = areg(MS * 16 * 4);
+    CK(cudaMalloc((void**)&c->act, ao));
+    CK(cudaMemset(c->act, 0, ao));
+
+    // RoPE table: angle p * theta^(-2i/hd), in double, rounded to fp32
+    {
+        const size_t half = hd / 2;
+        std::vector<float2> tab((size_t)g.max_pos * half);
+        for (size_t p = 0; p < (size_t)g.max_pos; ++p)
+            for (size_t i = 0; i < half; ++i) {
+                const double a = (double)p * pow(g.rope_theta, -2.0 * (double)i / (double)hd);
+                tab[p * half + i] = make_float2((float)cos(a), (float)sin(a));
+            }
+        CK(cudaMalloc((void**)&c->rope, tab.size() * sizeof(float2)));
+        CK(cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice));
+    }
+
+    // phase list: embed, L x 5, head, S x (dL x 5 + 1), final
+    std::vector<Phase> ph;
+    ph.push_back({PH_EMBED, 0, 0, 0});
+    for (int l = 0; l < g.n_layers; ++l) {
+        ph.push_back({PH_QKV, l, 0, 0});
+        ph.push_back({PH_ATTN, l, 0, 0});
+        ph.push_back({PH_O, l, 0, 0});
+        ph.push_back({PH_GU, l, 0, 0});
+        ph.push_back({PH_DOWN, l, 0, 0});
+    }
+    c->nphase_prefill = (int)ph.size();
+    ph.push_back({PH_HEAD, 0, 0, 0});
+    for (int j = 0; j < g.dep_steps; ++j) {
+        for (int l = 0; l < g.dep_layers; ++l) {
+            ph.push_back({PH_DQKV, l, j, 0});
+            ph.push_back({PH_DATTN, l, j, 0});
+            ph.push_back({PH_DO, l, j, 0});
+            ph.push_back({PH_DGU, l, j, 0});
+            ph.push_back({PH_DDOWN, l, j, 0});
+        }
+        ph.push_back({PH_DHEAD, 0, j, 0});
+    }
+    ph.push_back({PH_FINAL, 0, 0, 0});
+    c->nphase = (int)ph.size();
+    CK(cudaMalloc((void**)&c->d_phases, ph.size() * sizeof(Phase)));
+    CK(cudaMemcpy(c->d_phases, ph.data(), ph.size() * sizeof(Phase), cudaMemcpyHostToDevice));
+
+    CK(cudaMalloc((void**)&c->d_desc, sizeof(StepDesc)));
+    CK(cudaMemset(c->d_desc, 0, sizeof(StepDesc)));
+    CK(cudaMalloc((void**)&c->d_pref, PREF_CHUNK * sizeof(StepDesc)));
+    CK(cudaMalloc((void**)&c->d_bar, 256));
+    CK(cudaMemset(c->d_bar, 0, 256));
+    c->d_err = (int*)((char*)c->d_bar + 64);
+    CK(cudaHostAlloc((void**)&c->h_desc, DESC_RING * sizeof(StepDesc), cudaHostAllocDefault));
+    for (int i = 0; i < DESC_RING; ++i) CK(cudaEventCreateWithFlags(&c->desc_ev[i], cudaEventDisableTiming));
+    CK(cudaHostAlloc((void**)&c->h_pref, PREF_CHUNK * sizeof(StepDesc), cudaHostAllocDefault));
+    CK(cudaHostAlloc((void**)&c->h_out, (MFS_MAX_SLOTS * 17 + 2) * sizeof(int), cudaHostAllocDefault));
+
+    Params& P = c->P;
+    P.d = g.d; P.L = g.n_layers; P.H = g.n_heads; P.hd = g.head_dim; P.F = g.ffn; P.V = g.text_vocab;
+    P.C = g.card; P.W = g.window; P.dd = g.dep_d; P.dL = g.dep_layers; P.dH = g.dep_heads;
+    P.dhd = g.dep_head_dim; P.dF = g.dep_ffn; P.S = g.dep_steps;
+    for (int k = 0; k < NSTREAM; ++k) P.delays[k] = g.delays[k];
+    P.eps = (float)g.eps;
+    P.G = c->G;
+    rebase(P.emb_text, c->arena); rebase(P.emb_audio, c->arena);
+    rebase(P.dep_emb_text, c->arena); rebase(P.dep_emb_audio, c->arena);
+    rebase(P.tw, c->arena); rebase(P.head, c->arena); rebase(P.dw, c->arena);
+    rebasef(P.attn_norm, c->gains); rebasef(P.ffn_norm, c->gains); rebasef(P.out_norm, c->gains);
+    rebasef(P.dep_attn_norm, c->gains); rebasef(P.dep_ffn_norm, c->gains); rebasef(P.dep_out_norm, c->gains);
+    P.rope = c->rope;
+    P.kc = c->kc; P.vc = c->vc; P.hist = c->hist; P.desc = c->d_desc;
+    char* A = c->act;
+    P.x = (float*)(A + a_x); P.q = (float*)(A + a_q); P.o = (float*)(A + a_o); P.s = (float*)(A + a_s);
+    P.logits = (float*)(A + a_lg); P.yin = (float*)(A + a_yin); P.u = (float*)(A + a_u);
+    P.dq = (float*)(A + a_dq); P.dkv = (float*)(A + a_dkv); P.dat = (float*)(A + a_dat);
+    P.ds = (float*)(A + a_ds); P.dlogits = (float*)(A + a_dlg); P.apart = (float*)(A + a_ap);
+    P.acnt = (int*)(A + a_ac); P.amax_v = (float*)(A + a_amv); P.amax_i = (int*)(A + a_ami);
+    P.chosen = (int*)(A + a_ch); P.text_out = (int*)(A + a_to); P.codes_out = (int*)(A + a_co);
+    P.text_argmax = (int*)(A + a_ta); P.code_argmax = (int*)(A + a_ca);
+    P.bar = c->d_bar; P.err = c->d_err; P.err_seq = c->d_err + 1;
+    P.phases = c->d_phases;
+
+    // kernels: one per batch group; shared memory for the largest row block
+    c->maxrows = max_rows(g, c->G);
+    for (int i = 0; i < 3; ++i) {
+        const int bg = bg_value(i);
+        c->kfn[i] = g.weight_dtype == MFS_DTYPE_BF16 ? kernel_bf16(bg) : kernel_f32(bg);
+        c->smem[i] = ((size_t)c->maxrows * bg * 17 + SCRATCH_FLOATS) * sizeof(float);
+        if (c->smem[i] > 227 * 1024) return fail(c, MFS_E_ARG, "shape needs %zu B of shared memory", c->smem[i]);
+        CK(cudaFuncSetAttribute(c->kfn[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c->smem[i]));
+        int per_sm = 0;
+        CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, c->kfn[i], NT, c->smem[i]));
+        if (per_sm < 1) return fail(c, MFS_E_CUDA, "kernel does not fit on an SM");
+    }
+    c->pos.assign(MS, 0);
+    return MFS_OK;
+}
+
+extern "C" int mfs_create(const mfs_config* cfg, void* cuda_stream, mfs_ctx** out)
+{
+    if (!out) return MFS_E_ARG;
+    *out = nullptr;
+    if (!cfg) {
+        g_create_error = "null config";
+        return MFS_E_ARG;
+    }
+    mfs_ctx* c = new (std::nothrow) mfs_ctx();
+    if (!c) {
+        g_create_error = "out of host memory";
+        return MFS_E_NOMEM;
+    }
+    c->cfg = *cfg;
+    const int rc = create_impl(c, cuda_stream);
+    if (rc != MFS_OK) {
+        g_create_error = c->err;
+        mfs_destroy(c);
+        return rc;
+    }
+    *out = c;
+    return MFS_OK;
+}
+
+extern "C" void mfs_destroy(mfs_ctx* c)
+{
+    if (!c) return;
+    if (c->stream) cudaStreamSynchronize(c->stream);
+    cudaFree(c->arena); cudaFree(c->gains); cudaFree(c->kc); cudaFree(c->vc); cudaFree(c->hist);
+    cudaFree(c->act); cudaFree(c->rope); cudaFree(c->d_phases); cudaFree(c->d_desc); cudaFree(c->d_pref);
+    cudaFree(c->d_bar);
+    for (int i = 0; i < DESC_RING; ++i)
+        if (c->desc_ev[i]) cudaEventDestroy(c->desc_ev[i]);
+    for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
+    cudaFreeHost(c->h_desc); cudaFreeHost(c->h_pref); cudaFreeHost(c->h_out);
+    if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
+    delete c;
+}
+
+extern "C" const char* mfs_last_error(const mfs_ctx* c)
+{
+    if (!c) return g_create_error.c_str();
+    return c->err.c_str();
+}
+
+// ------------------------------------------------------------------ weights
+
+extern "C" int mfs_load_weights(mfs_ctx* c, const char* name, const void* src, size_t bytes, int on_device)
+{
+    if (!c || !name || !src) return fail(c, MFS_E_ARG, "null argument");
+    if (!c->arena) return fail(c, MFS_E_STATE, "context not created");
+    auto it = c->tensors.find(name);
+    if (it == c->tensors.end()) return fail(c, MFS_E_STATE, "unknown tensor %s", name);
+    TensorInfo& t = it->second;
+    if (bytes != t.bytes) return fail(c, MFS_E_STATE, "%s: %zu bytes, expected %zu", name, bytes, t.bytes);
+    CK(cudaStreamSynchronize(c->stream));
+    char* base = t.region == 0 ? c->arena : (char*)c->gains;
+    const cudaMemcpyKind kind = on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+    for (const CopyOp& op : t.ops) {
+        if (op.rows == 1) CK(cudaMemcpy(base + op.dst_off, (const char*)src + op.src_off, op.width, kind));
+        else CK(cudaMemcpy2D(base + op.dst_off, op.dst_pitch, (const char*)src + op.src_off, op.src_pitch, op.width, op.rows, kind));
+    }
+    t.loaded = true;
+    return MFS_OK;
+}
+
+static int weights_ready(mfs_ctx* c)
+{
+    for (auto& kv : c->tensors)
+        if (!kv.second.loaded) return fail(c, MFS_E_STATE, "tensor %s not loaded", kv.first.c_str());
+    return MFS_OK;
+}
+
+// ------------------------------------------------------------------ steps
+
+static int check_slots(mfs_ctx* c, int n, const int32_t* slots, int advance)
+{
+    if (n < 1 || n > c->cfg.max_slots) return fail(c, MFS_E_ARG, "n = %d outside [1, %d]", n, c->cfg.max_slots);
+    if (!slots) return fail(c, MFS_E_ARG, "null slots");
+    std::vector<char> seen(c->cfg.max_slots, 0);
+    for (int i = 0; i < n; ++i) {
+        const int s = slots[i];
+        if (s < 0 || s >= c->cfg.max_slots) return fail(c, MFS_E_SLOT, "slot %d outside [0, %d)", s, c->cfg.max_slots);
+        if (seen[s]) return fail(c, MFS_E_ARG, "slot %d listed twice", s);
+        seen[s] = 1;
+        if (c->pos[s] + advance > c->cfg.max_pos)
+            return fail(c, MFS_E_RANGE, "slot %d at frame %d would pass max_pos %d", s, c->pos[s], c->cfg.max_pos);
+    }
+    return MFS_OK;
+}
+
+static int check_tokens(mfs_ctx* c, const int32_t* codes, int rows, int lo)
+{
+    for (int r = 0; r < rows; ++r)
+        for (int k = 0; k < NSTREAM; ++k) {
+            const int t = codes[(size_t)r * NSTREAM + k];
+            const int hi = k == 0 ? c->cfg.text_vocab : c->cfg.card;
+            if (t < lo || t >= hi) return fail(c, MFS_E_TOKEN, "token %d of stream %d outside [%d, %d)", t, k, lo, hi);
+        }
+    return MFS_OK;
+}
+
+// Enqueue the kernel(s) for phases [0, nph) of the step described by desc.
+static int launch(mfs_ctx* c, int n, int nph, const StepDesc* desc)
+{
+    Params P = c->P;
+    P.desc = desc;
+    const int bi = bg_index(n);
+    int maxrows = c->maxrows;
+    CK(cudaMemsetAsync(c->d_bar, 0, 4, c->stream));
+    cudaEvent_t ev1 = nullptr;
+    if (c->timing) {
+        if (c->ev_used + 2 > c->ev_pool.size()) {
+            for (int k = 0; k < 64; ++k) {
+                cudaEvent_t e;
+                CK(cudaEventCreate(&e));
+                c->ev_pool.push_back(e);
+            }
+        }
+        CK(cudaEventRecord(c->ev_pool[c->ev_used], c->stream));
+        ev1 = c->ev_pool[c->ev_used + 1];
+        c->ev_used += 2;
+    }
+    if (c->mode == 0) {
+        int ph0 = 0, ph1 = nph, coop = 1;
+        void* args[] = {&P, &ph0, &ph1, &coop, &maxrows};
+        CK(cudaLaunchCooperativeKernel(c->kfn[bi], dim3(c->G), dim3(NT), args, c->smem[bi], c->stream));
+        c->launches = 1;
+    } else {
+        for (int ph = 0; ph < nph; ++ph) {
+            int ph0 = ph, ph1 = ph + 1, coop = 0;
+            void* args[] = {&P, &ph0, &ph1, &coop, &maxrows};
+            CK(cudaLaunchKernel(c->kfn[bi], dim3(c->G), dim3(NT), args, c->smem[bi], c->stream));
+        }
+        c->launches = nph;
+    }
+    if (ev1) CK(cudaEventRecord(ev1, c->stream));
+    return MFS_OK;
+}
+
+static StepDesc* next_desc(mfs_ctx* c, int* idx)
+{
+    const int i = c->desc_next;
+    c->desc_next = (i + 1) % DESC_RING;
+    cudaEventSynchronize(c->desc_ev[i]);
+    *idx = i;
+    return &c->h_desc[i];
+}
+
+// Read the device error flag (stream must be idle); rolls back positions of
+// steps that a device-side token check turned into no-ops.
+static int collect_device_error(mfs_ctx* c)
+{
+    int e[2] = {0, 0};
+    CK(cudaMemcpy(e, c->d_err, sizeof e, cudaMemcpyDeviceToHost));
+    int rc = MFS_OK;
+    if (e[0] != 0) {
+        if (e[0] == DERR_TOKEN) {
+            for (auto it = c->pending.rbegin(); it != c->pending.rend(); ++it)
+                if (it->seq >= e[1])
+                    for (size_t k = 0; k < it->slots.size(); ++k) c->pos[it->slots[k]] = it->old_pos[k];
+            rc = fail(c, MFS_E_TOKEN, "a device-side token was out of range (step %d); those steps did nothing", e[1]);
+        } else {
+            rc = fail(c, MFS_E_DEVICE, "device wait gave up (code %d); slot state is undefined", e[0]);
+        }
+        CK(cudaMemset(c->d_err, 0, sizeof e));
+    }
+    c->pending.clear();
+    return rc;
+}
+
+extern "C" int mfs_sync(mfs_ctx* c)
+{
+    if (!c) return MFS_E_ARG;
+    CK(cudaStreamSynchronize(c->stream));
+    return collect_device_error(c);
+}
+
+static int fill_desc(mfs_ctx* c, StepDesc* h, int n, const int32_t* slots, const int32_t* codes, int frame_off)
+{
+    h->n = n;
+    h->seq = ++c->seq;
+    for (int i = 0; i < n; ++i) {
+        h->slot[i] = slots[i];
+        h->pos[i] = c->pos[slots[i]] + frame_off;
+        if (codes) memcpy(h->codes[i], codes + (size_t)i * NSTREAM, NSTREAM * sizeof(int));
+    }
+    return MFS_OK;
+}
+
+extern "C" int mfs_step(mfs_ctx* c, int n, const int32_t* slots, const int32_t* in_codes, int32_t* text_tok,
+                        int32_t* codes)
+{
+    if (!c) return MFS_E_ARG;
+    if (!c->pending.empty()) {
+        int rc = mfs_sync(c);
+        if (rc != MFS_OK) return rc;
+    }
+    int rc = weights_ready(c);
+    if (rc) return rc;
+    if ((rc = check_slots(c, n, slots, 1))) return rc;
+    if (!in_codes || !text_tok || !codes) return fail(c, MFS_E_ARG, "null buffer");
+    if ((rc = check_tokens(c, in_codes, n, -1))) return rc;
+    int di;
+    StepDesc* h = next_desc(c, &di);
+    fill_desc(c, h, n, slots, in_codes, 0);
+    CK(cudaMemcpyAsync(c->d_desc, h, sizeof(StepDesc), cudaMemcpyHostToDevice, c->stream));
+    CK(cudaEventRecord(c->desc_ev[di], c->stream));
+    if ((rc = launch(c, n, c->nphase, c->d_desc))) return rc;
+    int* ho = c->h_out;
+    CK(cudaMemcpyAsync(ho, c->P.text_out, n * sizeof(int), cudaMemcpyDeviceToHost, c->stream));
+    CK(cudaMemcpyAsync(ho + MFS_MAX_SLOTS, c->P.codes_out, n * 16 * sizeof(int), cudaMemcpyDeviceToHost, c->stream));
+    CK(cudaMemcpyAsync(ho + MFS_MAX_SLOTS * 17, c->d_err, 2 * sizeof(int), cudaMemcpyDeviceToHost, c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+    if (ho[MFS_MAX_SLOTS * 17] != 0) return collect_device_error(c);
+    memcpy(text_tok, ho, n * sizeof(int));
+    memcpy(codes, ho + MFS_MAX_SLOTS, n * 16 * sizeof(int));
+    for (int i = 0; i < n; ++i) c->pos[slots[i]] += 1;
+    c->last_n = n;
+    c->last_full = true;
+    return MFS_OK;
+}
+
+extern "C" int mfs_step_device(mfs_ctx* c, int n, const int32_t* slots, const int32_t* d_in_codes,
+                               int32_t* d_text_tok, int32_t* d_codes)
+{
+    if (!c) return MFS_E_ARG;
+    int rc = weights_ready(c);
+    if (rc) return rc;
+    if ((rc = check_slots(c, n, slots, 1))) return rc;
+    if (!d_in_codes) return fail(c, MFS_E_ARG, "null device codes");
+    int di;
+    StepDesc* h = next_desc(c, &di);
+    fill_desc(c, h, n, slots, nullptr, 0);
+    const size_t head = offsetof(StepDesc, codes);
+    CK(cudaMemcpyAsync(c->d_desc, h, head, cudaMemcpyHostToDevice, c->stream));
+    CK(cudaEventRecord(c->desc_ev[di], c->stream));
+    CK(cudaMemcpyAsync(c->d_desc->codes, d_in_codes, (size_t)n * NSTREAM * sizeof(int), cudaMemcpyDeviceToDevice, c->stream));
+    if ((rc = launch(c, n, c->nphase, c->d_desc))) return rc;
+    if (d_text_tok) CK(cudaMemcpyAsync(d_text_tok, c->P.text_out, n * sizeof(int), cudaMemcpyDeviceToDevice, c->stream));
+    if (d_codes) CK(cudaMemcpyAsync(d_codes, c->P.codes_out, n * 16 * sizeof(int), cudaMemcpyDeviceToDevice, c->stream));
+    Pending pd;
+    pd.seq = h->seq;
+    for (int i = 0; i < n; ++i) {
+        pd.slots.push_back(slots[i]);
+        pd.old_pos.push_back(c->pos[slots[i]]);
+        c->pos[slots[i]] += 1;
+    }
+    c->pending.push_back(pd);
+    c->last_n = n;
+    c->last_full = true;
+    return MFS_OK;
+}
+
+extern "C" int mfs_prefill(mfs_ctx* c, int n, const int32_t* slots, int T, const int32_t* codes)
+{
+    if (!c) return MFS_E_ARG;
+    if (!c->pending.empty()) {
+        int rc = mfs_sync(c);
+        if (rc != MFS_OK) return rc;
+    }
+    int rc = weights_ready(c);
+    if (rc) return rc;
+    if (T < 0) return fail(c, MFS_E_ARG, "T < 0");
+    if ((rc = check_slots(c, n, slots, T))) return rc;
+    if (T == 0) return MFS_OK;
+    if (!codes) return fail(c, MFS_E_ARG, "null codes");
+    if ((rc = check_tokens(c, codes, n * T, 0))) return rc;
+    std::vector<int32_t> col((size_t)n * NSTREAM);
+    for (int t0 = 0; t0 < T; t0 += PREF_CHUNK) {
+        const int tn = T - t0 < PREF_CHUNK ? T - t0 : PREF_CHUNK;
+        CK(cudaStreamSynchronize(c->stream));  // the pinned staging is reused
+        for (int t = 0; t < tn; ++t) {
+            for (int i = 0; i < n; ++i)
+                memcpy(&col[(size_t)i * NSTREAM], codes + ((size_t)i * T + t0 + t) * NSTREAM, NSTREAM * sizeof(int));
+            fill_desc(c, &c->h_pref[t], n, slots, col.data(), t0 + t);
+        }
+        CK(cudaMemcpyAsync(c->d_pref, c->h_pref, tn * sizeof(StepDesc), cudaMemcpyHostToDevice, c->stream));
+        for (int t = 0; t < tn; ++t)
+            if ((rc = launch(c, n, c->nphase_prefill, c->d_pref + t))) return rc;
+    }
+    CK(cudaMemcpyAsync(c->h_out + MFS_MAX_SLOTS * 17, c->d_err, 2 * sizeof(int), cudaMemcpyDeviceToHost, c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+    if (c->h_out[MFS_MAX_SLOTS * 17] != 0) return collect_device_error(c);
+    for (int i = 0; i < n; ++i) c->pos[slots[i]] += T;
+    c->last_full = false;
+    return MFS_OK;
+}
+
+extern "C" int mfs_reset_slot(mfs_ctx* c, int slot)
+{
+    if (!c) return MFS_E_ARG;
+    if (!c->pending.empty()) {
+        int rc = mfs_sync(c);
+        if (rc != MFS_OK) return rc;
+    }
+    if (slot < 0 || slot >= c->cfg.max_slots) return fail(c, MFS_E_SLOT, "slot %d outside [0, %d)", slot, c->cfg.max_slots);
+    CK(cudaMemsetAsync(c->hist + (size_t)slot * NSTREAM * HIST, 0xFF, NSTREAM * HIST * sizeof(int), c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+    c->pos[slot] = 0;
+    return MFS_OK;
+}
+
+extern "C" int mfs_position(const mfs_ctx* c, int slot)
+{
+    if (!c) return MFS_E_ARG;
+    if (slot < 0 || slot >= c->cfg.max_slots) return MFS_E_SLOT;
+    return c->pos[slot];
+}
+
+extern "C" int mfs_read_debug(mfs_ctx* c, float* text_logits, float* dep_logits, int32_t* text_argmax,
+                              int32_t* code_argmax)
+{
+    if (!c) return MFS_E_ARG;
+    if (!c->last_full || c->last_n == 0) return fail(c, MFS_E_STATE, "no full step to report");
+    CK(cudaStreamSynchronize(c->stream));
+    const size_t n = c->last_n;
+    if (text_logits) CK(cudaMemcpy(text_logits, c->P.logits, n * c->cfg.text_vocab * 4, cudaMemcpyDeviceToHost));
+    if (dep_logits) CK(cudaMemcpy(dep_logits, c->P.dlogits, n * 16 * c->cfg.card * 4, cudaMemcpyDeviceToHost));
+    if (text_argmax) CK(cudaMemcpy(text_argmax, c->P.text_argmax, n * 4, cudaMemcpyDeviceToHost));
+    if (code_argmax) CK(cudaMemcpy(code_argmax, c->P.code_argmax, n * 16 * 4, cudaMemcpyDeviceToHost));
+    return MFS_OK;
+}
+
+extern "C" int mfs_set_mode(mfs_ctx* c, int mode)
+{
+    if (!c) return MFS_E_ARG;
+    if (mode != 0 && mode != 1) return fail(c, MFS_E_ARG, "mode must be 0 or 1");
+    c->mode = mode;
+    return MFS_OK;
+}
+
+extern "C" int mfs_launches_per_step(const mfs_ctx* c)
+{
+    if (!c) return MFS_E_ARG;
+    return c->launches;
+}
+
+extern "C" int mfs_set_timing(mfs_ctx* c, int enable)
+{
+    if (!c) return MFS_E_ARG;
+    c->timing = enable != 0;
+    return MFS_OK;
+}
+
+extern "C" int mfs_kernel_time(mfs_ctx* c, double* total_ms, int* steps)
+{
+    if (!c || !total_ms || !steps) return MFS_E_ARG;
+    CK(cudaStreamSynchronize(c->stream));
+    double tot = 0.0;
+    for (size_t k = 0; k + 1 < c->ev_used; k += 2) {
+        float ms = 0.f;
+        CK(cudaEventElapsedTime(&ms, c->ev_pool[k], c->ev_pool[k + 1]));
+        tot += ms;
+    }
+    *total_ms = tot;
+    *steps = (int)(c->ev_used / 2);
+    c->ev_used = 0;
+    return MFS_OK;
+}

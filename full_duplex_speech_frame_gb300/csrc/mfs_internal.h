@@ -1,0 +1,109 @@
+// Internal layout shared by the host side of the library and its kernels.
+#pragma once
+#include <stdint.h>
+#include <cuda_runtime.h>
+
+#include "../../include/mfs.h"
+
+namespace mfs {
+
+constexpr int NT = 512;          // threads per CTA (16 warps)
+constexpr int NWARP = NT / 32;
+constexpr int NSTREAM = MFS_N_STREAMS;
+constexpr int NCHUNK_MAX = 32;   // attention split over the window, per (slot, head)
+constexpr int HIST = 3;          // frames of token history per stream
+
+enum PhaseType : int {
+    PH_EMBED = 0,  // S0 + S1: record frame p's tokens, delayed embedding sum
+    PH_QKV,        // S2: RMSNorm + QKV + RoPE + ring write
+    PH_ATTN,       // S5: split flash-decode over the ring window + merge
+    PH_O,          // S6: out projection + residual
+    PH_GU,         // S7: RMSNorm + gate/up + SwiGLU
+    PH_DOWN,       // S8: down projection + residual
+    PH_HEAD,       // S4: final norm + text logits (+ argmax partials) + depformer in-projections
+    PH_DQKV,       // S9: depformer layer QKV (layer 0 also forms u = in-proj + embedding)
+    PH_DATTN,      // S9: depformer attention over substeps 0..j
+    PH_DO,
+    PH_DGU,
+    PH_DDOWN,
+    PH_DHEAD,      // S9: depformer head + argmax partials
+    PH_FINAL,      // S10: last argmax, history write-back, outputs
+};
+
+struct Phase {
+    int type, l, j, pad;
+};
+
+// Written by the host before each launch.
+struct StepDesc {
+    int n, seq, pad0, pad1;
+    int slot[MFS_MAX_SLOTS];
+    int pos[MFS_MAX_SLOTS];
+    int codes[MFS_MAX_SLOTS][NSTREAM];
+};
+
+enum DeviceError : int { DERR_NONE = 0, DERR_TOKEN = 1, DERR_BARRIER = 2 };
+
+struct Params {
+    // shape
+    int d, L, H, hd, F, V, C, W, dd, dL, dH, dhd, dF, S;
+    int delays[NSTREAM];
+    float eps;
+    int G;  // CTAs in the grid
+    // weights (element pointers into the arena; "W" = weight dtype)
+    const void* emb_text;       // [V+1][d]
+    const void* emb_audio;      // [16][C+1][d]
+    const void* dep_emb_text;   // [V][dd]
+    const void* dep_emb_audio;  // [S-1][C][dd]
+    const void* tw;             // per layer: wqkv [3d][d] | wo [d][d] | wgu [2F][d] (gate/up rows interleaved) | wdown [d][F]
+    long long t_layer;          // elements per temporal layer block
+    const void* head;           // text head [V][d] then depformer in-proj [S*dd][d]
+    const void* dw;             // per substep j: per layer l': dqkv | dwo | dgu (interleaved) | ddown; then head [C][dd]
+    long long d_layer, d_sub;   // elements per depformer layer block / per substep block
+    const float* attn_norm;     // [L][d]
+    const float* ffn_norm;      // [L][d]
+    const float* out_norm;      // [d]
+    const float* dep_attn_norm; // [dL][dd]
+    const float* dep_ffn_norm;  // [dL][dd]
+    const float* dep_out_norm;  // [dd]
+    const float2* rope;         // [max_pos][hd/2] (cos, sin)
+    // per-slot state
+    void* kc;                   // [MS][L][W][d] keys (kv dtype)
+    void* vc;                   // [MS][L][W][d] values
+    int* hist;                  // [MS][17][3]
+    const StepDesc* desc;
+    // activations, row = position in the step's slot list
+    float* x;        // [MS][d]  residual stream
+    float* q;        // [MS][d]  rotated queries
+    float* o;        // [MS][d]  attention output
+    float* s;        // [MS][F]  SwiGLU output
+    float* logits;   // [MS][V]
+    float* yin;      // [MS][S][dd]  depformer in-projections
+    float* u;        // [MS][dd] depformer residual stream
+    float* dq;       // [MS][dd]
+    float* dkv;      // [MS][dL][S][2][dd]
+    float* dat;      // [MS][dd] depformer attention output
+    float* ds;       // [MS][dF]
+    float* dlogits;  // [MS][S][C]
+    float* apart;    // [MS][H][NCHUNK_MAX][hd+4] attention partials (m, l, pad, pad, acc[hd])
+    int* acnt;       // [MS][H] arrival counters (zero between uses)
+    float* amax_v;   // [MS][G] per-CTA argmax partials
+    int* amax_i;
+    int* chosen;     // [MS][17] tokens chosen this step
+    int* text_out;   // [MS]
+    int* codes_out;  // [MS][16]
+    int* text_argmax;  // [MS]
+    int* code_argmax;  // [MS][16]
+    // control
+    unsigned* bar;   // grid barrier counter (zeroed before each launch)
+    int* err;        // sticky device error (DeviceError)
+    int* err_seq;    // step sequence number that raised it
+    const Phase* phases;
+};
+
+// Kernel entry points, one per (weight dtype, batch group).  Defined in the
+// per-instantiation translation units.
+const void* kernel_f32(int bg);
+const void* kernel_bf16(int bg);
+
+}  // namespace mfs

@@ -1,0 +1,6 @@
+// Kernel instantiation: bf16 weights and key/value ring, batch group of 2.
+#include "mfs_kernels.cuh"
+
+namespace mfs {
+const void* kernel_bf16_2() { return (const void*)&step_kernel<__nv_bfloat16, __nv_bfloat16, 2>; }
+}  // namespace mfs

@@ -1,0 +1,236 @@
+"""Python binding of the C ABI in include/mfs.h (ctypes; argument marshalling only).
+
+Every step of the frame step runs in the CUDA library ``libmfs.so``; this module
+only converts arguments.  There is no fallback: if the library is missing the
+import fails with the command that builds it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmfs.so")
+
+MFS_OK = 0
+STATUS = {-1: "MFS_E_ARG", -2: "MFS_E_SLOT", -3: "MFS_E_TOKEN", -4: "MFS_E_RANGE", -5: "MFS_E_STATE",
+          -6: "MFS_E_CUDA", -7: "MFS_E_DEVICE", -8: "MFS_E_NOMEM"}
+MFS_DTYPE_F32, MFS_DTYPE_BF16 = 0, 1
+MFS_MAX_SLOTS = 64
+
+
+class MfsError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"{STATUS.get(code, code)}: {message}")
+        self.code = code
+        self.status = STATUS.get(code, str(code))
+
+
+class mfs_config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in (
+        "d", "n_layers", "n_heads", "head_dim", "ffn", "text_vocab", "card", "n_q", "window", "max_pos",
+        "dep_d", "dep_layers", "dep_heads", "dep_head_dim", "dep_ffn", "dep_steps")] + [
+        ("delays", ctypes.c_int * 17), ("rope_theta", ctypes.c_double), ("eps", ctypes.c_double),
+        ("weight_dtype", ctypes.c_int), ("kv_dtype", ctypes.c_int), ("max_slots", ctypes.c_int)]
+
+
+def _load_library():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'` "
+                          "(or python full_duplex_speech_frame_gb300/build.py)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, ci, i32p = ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p
+    sig = {
+        "mfs_create": (ci, [ctypes.POINTER(mfs_config), vp, ctypes.POINTER(vp)]),
+        "mfs_destroy": (None, [vp]),
+        "mfs_last_error": (ctypes.c_char_p, [vp]),
+        "mfs_load_weights": (ci, [vp, ctypes.c_char_p, vp, ctypes.c_size_t, ci]),
+        "mfs_step": (ci, [vp, ci, i32p, i32p, i32p, i32p]),
+        "mfs_step_device": (ci, [vp, ci, i32p, vp, vp, vp]),
+        "mfs_sync": (ci, [vp]),
+        "mfs_prefill": (ci, [vp, ci, i32p, ci, i32p]),
+        "mfs_reset_slot": (ci, [vp, ci]),
+        "mfs_position": (ci, [vp, ci]),
+        "mfs_read_debug": (ci, [vp, vp, vp, vp, vp]),
+        "mfs_set_mode": (ci, [vp, ci]),
+        "mfs_launches_per_step": (ci, [vp]),
+        "mfs_set_timing": (ci, [vp, ci]),
+        "mfs_kernel_time": (ci, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    return lib
+
+
+_lib = _load_library()
+
+
+def exported_symbols() -> Sequence[str]:
+    return [n for n in dir(_lib) if n.startswith("mfs_")]
+
+
+class Ctx:
+    """Owner of an ``mfs_ctx*``; destroyed with ``mfs_destroy``."""
+
+    def __init__(self, handle: int, cfg: mfs_config):
+        self.handle = ctypes.c_void_p(handle)
+        self.cfg = cfg
+        self.last_n = 0
+
+    def __del__(self):
+        if getattr(self, "handle", None) and self.handle.value:
+            _lib.mfs_destroy(self.handle)
+            self.handle = ctypes.c_void_p(None)
+
+
+def _check(ctx: Optional[Ctx], rc: int) -> None:
+    if rc != MFS_OK:
+        h = ctx.handle if ctx is not None else None
+        raise MfsError(rc, (_lib.mfs_last_error(h) or b"").decode())
+
+
+def make_config(d, n_layers, n_heads, head_dim, ffn, text_vocab, card, window, max_pos, dep_d, dep_layers,
+                dep_heads, dep_head_dim, dep_ffn, delays, rope_theta=10000.0, eps=1e-8,
+                weight_dtype="bf16", kv_dtype="bf16", max_slots=1, n_q=16, dep_steps=16) -> mfs_config:
+    c = mfs_config()
+    for k, v in dict(d=d, n_layers=n_layers, n_heads=n_heads, head_dim=head_dim, ffn=ffn, text_vocab=text_vocab,
+                     card=card, n_q=n_q, window=window, max_pos=max_pos, dep_d=dep_d, dep_layers=dep_layers,
+                     dep_heads=dep_heads, dep_head_dim=dep_head_dim, dep_ffn=dep_ffn, dep_steps=dep_steps,
+                     max_slots=max_slots).items():
+        setattr(c, k, int(v))
+    c.delays[:] = [int(x) for x in delays]
+    c.rope_theta = float(rope_theta)
+    c.eps = float(eps)
+    c.weight_dtype = MFS_DTYPE_BF16 if weight_dtype == "bf16" else MFS_DTYPE_F32
+    c.kv_dtype = MFS_DTYPE_BF16 if kv_dtype == "bf16" else MFS_DTYPE_F32
+    return c
+
+
+def _current_stream():
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    except ImportError:
+        pass
+    return None
+
+
+def mfs_create(cfg: mfs_config, stream=None) -> Ctx:
+    out = ctypes.c_void_p()
+    st = _current_stream() if stream is None else ctypes.c_void_p(stream)
+    rc = _lib.mfs_create(ctypes.byref(cfg), st, ctypes.byref(out))
+    _check(None, rc)
+    return Ctx(out.value, cfg)
+
+
+def mfs_destroy(ctx: Ctx) -> None:
+    if ctx.handle.value:
+        _lib.mfs_destroy(ctx.handle)
+        ctx.handle = ctypes.c_void_p(None)
+
+
+def mfs_last_error(ctx: Optional[Ctx]) -> str:
+    return (_lib.mfs_last_error(ctx.handle if ctx else None) or b"").decode()
+
+
+def mfs_load_weights(ctx: Ctx, name: str, src) -> None:
+    """src: a C-contiguous numpy array (host) or a contiguous CUDA torch tensor."""
+    if isinstance(src, np.ndarray):
+        src = np.ascontiguousarray(src)
+        rc = _lib.mfs_load_weights(ctx.handle, name.encode(), src.ctypes.data, src.nbytes, 0)
+    else:
+        assert src.is_cuda and src.is_contiguous()
+        rc = _lib.mfs_load_weights(ctx.handle, name.encode(), src.data_ptr(),
+                                   src.numel() * src.element_size(), 1)
+    _check(ctx, rc)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def mfs_step(ctx: Ctx, slots, in_codes):
+    """Returns (text_tok [n], codes [n, 16]) as int32 numpy arrays."""
+    slots = _i32(slots).reshape(-1)
+    n = slots.size
+    codes_in = _i32(in_codes).reshape(n, 17)
+    text = np.empty(n, np.int32)
+    codes = np.empty((n, 16), np.int32)
+    rc = _lib.mfs_step(ctx.handle, n, slots.ctypes.data, codes_in.ctypes.data, text.ctypes.data, codes.ctypes.data)
+    _check(ctx, rc)
+    ctx.last_n = n
+    return text, codes
+
+
+def mfs_step_device(ctx: Ctx, slots, d_in_codes, d_text=None, d_codes=None) -> None:
+    """d_* are contiguous int32 CUDA tensors; returns without waiting."""
+    slots = _i32(slots).reshape(-1)
+    n = slots.size
+    rc = _lib.mfs_step_device(ctx.handle, n, slots.ctypes.data, d_in_codes.data_ptr(),
+                              d_text.data_ptr() if d_text is not None else None,
+                              d_codes.data_ptr() if d_codes is not None else None)
+    _check(ctx, rc)
+    ctx.last_n = n
+
+
+def mfs_sync(ctx: Ctx) -> None:
+    _check(ctx, _lib.mfs_sync(ctx.handle))
+
+
+def mfs_prefill(ctx: Ctx, slots, codes) -> None:
+    """codes [n, T, 17] int, every entry >= 0."""
+    slots = _i32(slots).reshape(-1)
+    n = slots.size
+    codes = _i32(codes)
+    T = codes.shape[1] if codes.ndim == 3 else codes.size // (17 * n)
+    codes = codes.reshape(n, T, 17)
+    _check(ctx, _lib.mfs_prefill(ctx.handle, n, slots.ctypes.data, T, codes.ctypes.data))
+
+
+def mfs_reset_slot(ctx: Ctx, slot: int) -> None:
+    _check(ctx, _lib.mfs_reset_slot(ctx.handle, int(slot)))
+
+
+def mfs_position(ctx: Ctx, slot: int) -> int:
+    rc = _lib.mfs_position(ctx.handle, int(slot))
+    if rc < 0:
+        _check(ctx, rc)
+    return rc
+
+
+def mfs_read_debug(ctx: Ctx, n: Optional[int] = None) -> dict:
+    n = ctx.last_n if n is None else n
+    c = ctx.cfg
+    out = {"text_logits": np.empty((n, c.text_vocab), np.float32),
+           "dep_logits": np.empty((n, 16, c.card), np.float32),
+           "text_argmax": np.empty(n, np.int32), "code_argmax": np.empty((n, 16), np.int32)}
+    rc = _lib.mfs_read_debug(ctx.handle, out["text_logits"].ctypes.data, out["dep_logits"].ctypes.data,
+                             out["text_argmax"].ctypes.data, out["code_argmax"].ctypes.data)
+    _check(ctx, rc)
+    return out
+
+
+def mfs_set_mode(ctx: Ctx, mode: int) -> None:
+    _check(ctx, _lib.mfs_set_mode(ctx.handle, int(mode)))
+
+
+def mfs_launches_per_step(ctx: Ctx) -> int:
+    return _lib.mfs_launches_per_step(ctx.handle)
+
+
+def mfs_set_timing(ctx: Ctx, enable: bool) -> None:
+    _check(ctx, _lib.mfs_set_timing(ctx.handle, 1 if enable else 0))
+
+
+def mfs_kernel_time(ctx: Ctx):
+    """(summed kernel milliseconds, steps timed) since the previous call."""
+    ms, n = ctypes.c_double(), ctypes.c_int()
+    _check(ctx, _lib.mfs_kernel_time(ctx.handle, ctypes.byref(ms), ctypes.byref(n)))
+    return ms.value, n.value

@@ -1,0 +1,167 @@
+/*
+ * mfs.h -- C ABI of the GB300 lockstep frame step of a Moshi-class
+ * full-duplex speech model (PersonaPlex / Moshi RQ-Transformer).
+ *
+ * One frame step (80 ms of audio per session) for B concurrent sessions
+ * ("slots") runs, on one GPU:
+ *   - the 17-stream delayed embedding sum (1 text row + 16 audio codebooks,
+ *     delays [0, 0, 1 x 7, 0, 1 x 7]: mobius PR #368 "Add PersonaPlex / Moshi
+ *     full-duplex S2S support", section "P3 - ONNX Runtime example"; token
+ *     column layout: vLLM-Omni PersonaPlex recipe, section "Architecture");
+ *   - one decode step of the temporal transformer (RMSNorm, RoPE, sliding-
+ *     window causal attention over a per-slot ring of keys/values, SwiGLU:
+ *     mobius PR #368, "P2 - Moshi LM"; 3000-frame ring window: vLLM-Omni
+ *     PersonaPlex recipe, "Architecture" and "Notes") and a greedy text argmax;
+ *   - the 16-substep autoregressive depformer with per-substep weights and a
+ *     greedy code argmax per substep (mobius PR #368, "P2 - Moshi LM").
+ *
+ * Conventions for every entry point:
+ *   - Return value: MFS_OK (0) or a negative MFS_E_* status.  An argument
+ *     error is detected on the host before anything is launched and leaves
+ *     every slot's state unchanged; mfs_last_error() gives a one-line reason.
+ *   - Host pointers are read or written only during the call; the library
+ *     keeps no reference to them.  Device pointers must be device memory of
+ *     the context's GPU.
+ *   - All GPU work runs on the stream given to mfs_create().
+ *   - A context is not thread-safe: one host thread at a time.
+ */
+#ifndef MFS_H
+#define MFS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MFS_OK 0
+#define MFS_E_ARG (-1)     /* null pointer, n out of range, duplicate slot, bad config */
+#define MFS_E_SLOT (-2)    /* slot id outside [0, max_slots) */
+#define MFS_E_TOKEN (-3)   /* token outside [-1, vocab) (text) or [-1, card) (audio) */
+#define MFS_E_RANGE (-4)   /* a slot would pass max_pos frames (context limit) */
+#define MFS_E_STATE (-5)   /* weights missing, unknown tensor name or wrong size */
+#define MFS_E_CUDA (-6)    /* a CUDA runtime call failed */
+#define MFS_E_DEVICE (-7)  /* a device-side wait gave up (bounded spin); state undefined */
+#define MFS_E_NOMEM (-8)   /* device or host allocation failed */
+
+#define MFS_DTYPE_F32 0
+#define MFS_DTYPE_BF16 1
+
+#define MFS_MAX_SLOTS 64
+#define MFS_N_STREAMS 17
+
+typedef struct mfs_ctx mfs_ctx;
+
+/* Model shape and limits.  Stream 0 is the text row; streams 1..16 are the
+ * audio codebooks (1..8 agent, 9..16 user); delays[k] is stream k's delay in
+ * frames.  window = ring length W (keys of positions p-W+1..p are attended);
+ * max_pos = largest frame count a slot may reach (RoPE range).  n_q and
+ * dep_steps must be 16.  Limits: head_dim in {64, 128}, dep_head_dim = 64,
+ * every K dimension (d, ffn, dep_d, dep_ffn) a multiple of 8 and at most
+ * 12288, max_slots <= MFS_MAX_SLOTS. */
+typedef struct {
+    int d, n_layers, n_heads, head_dim, ffn, text_vocab, card, n_q, window, max_pos;
+    int dep_d, dep_layers, dep_heads, dep_head_dim, dep_ffn, dep_steps;
+    int delays[MFS_N_STREAMS];
+    double rope_theta, eps;
+    int weight_dtype; /* MFS_DTYPE_F32 | MFS_DTYPE_BF16: linears and embedding tables */
+    int kv_dtype;     /* MFS_DTYPE_F32 | MFS_DTYPE_BF16: the ring of keys/values */
+    int max_slots;
+} mfs_config;
+
+/* Create a context on the current CUDA device: allocates the weight arena,
+ * the per-slot key/value rings (max_slots x n_layers x window x d, for keys
+ * and for values), the token histories and the activations.  cuda_stream is a
+ * cudaStream_t (NULL: the library creates its own).  Every slot starts fresh
+ * (position 0, empty history).  On success *out owns all of it. */
+int mfs_create(const mfs_config* cfg, void* cuda_stream, mfs_ctx** out);
+
+/* Synchronize and free everything the context owns. NULL is accepted. */
+void mfs_destroy(mfs_ctx* ctx);
+
+/* Reason for the last non-OK status of this context (never NULL); with a
+ * NULL context, the reason the last mfs_create() on this thread failed. */
+const char* mfs_last_error(const mfs_ctx* ctx);
+
+/* Copy one named tensor into the weight arena (the caller keeps ownership).
+ * src: host memory (on_device = 0) or device memory (on_device = 1); bytes
+ * must equal the tensor's size.  Names and row-major shapes (W = weight
+ * dtype, gains always fp32; V = text_vocab, C = card, S = dep_steps,
+ * d' = dep_d, F' = dep_ffn):
+ *   emb.text [V+1, d] W        emb.audio [16, C+1, d] W   (row V / C = INIT)
+ *   layers.{l}.attn_norm [d]   layers.{l}.wqkv [3d, d] W   (rows q | k | v)
+ *   layers.{l}.wo [d, d] W     layers.{l}.ffn_norm [d]
+ *   layers.{l}.wgu [2F, d] W   (rows: gate then up)      layers.{l}.wdown [d, F] W
+ *   out_norm [d]               text_head [V, d] W
+ *   dep.in [S, d', d] W        dep.emb.text [V, d'] W      dep.emb.audio [S-1, C, d'] W
+ *   dep.layers.{l}.attn_norm [d']   dep.layers.{l}.wqkv [S, 3d', d'] W
+ *   dep.layers.{l}.wo [S, d', d'] W dep.layers.{l}.ffn_norm [d']
+ *   dep.layers.{l}.wgu [S, 2F', d'] W   dep.layers.{l}.wdown [S, d', F'] W
+ *   dep.out_norm [d']          dep.head [S, C, d'] W
+ * Blocking.  Returns MFS_E_STATE for an unknown name or a size mismatch. */
+int mfs_load_weights(mfs_ctx* ctx, const char* name, const void* src, size_t bytes, int on_device);
+
+/* One frame step for n slots (1 <= n <= max_slots).
+ *   slots    [n]      distinct slot ids (host)
+ *   in_codes [n, 17]  frame p's tokens for each slot (host): -1 = generate,
+ *                     else the token is forced (text < text_vocab, audio < card)
+ *   text_tok [n]      out (host): text token of frame p
+ *   codes    [n, 16]  out (host): code of stream k (k = 1..16) for frame
+ *                     p - delays[k], or -1 when that frame is before 0
+ * Slots not listed are untouched.  Each listed slot advances by one frame.
+ * Blocks until the results are on the host. */
+int mfs_step(mfs_ctx* ctx, int n, const int32_t* slots, const int32_t* in_codes,
+             int32_t* text_tok, int32_t* codes);
+
+/* Same step with device-resident tokens; returns without waiting.
+ *   slots (host) [n]; d_in_codes [n, 17], d_text_tok [n], d_codes [n, 16]
+ *   (device; may be NULL for outputs that are not wanted).
+ * Token ranges are checked on the device: a bad token makes the whole step
+ * (and any later step enqueued before the next mfs_sync) a no-op, and the
+ * next mfs_sync (or blocking call) returns MFS_E_TOKEN with the positions of
+ * those steps rolled back. */
+int mfs_step_device(mfs_ctx* ctx, int n, const int32_t* slots, const int32_t* d_in_codes,
+                    int32_t* d_text_tok, int32_t* d_codes);
+
+/* Wait for enqueued steps; report a deferred device-side error (see above). */
+int mfs_sync(mfs_ctx* ctx);
+
+/* Teacher-forced prompt of T frames for n slots: codes [n, T, 17] (host), every
+ * token >= 0.  Runs the temporal stack only (the text head and depformer
+ * cannot change a slot whose every stream is supplied) and advances each slot
+ * by T frames.  Blocking. */
+int mfs_prefill(mfs_ctx* ctx, int n, const int32_t* slots, int T, const int32_t* codes);
+
+/* Return a slot to the fresh state: position 0, empty history.  Its ring is
+ * not cleared: positions are only ever read after being rewritten. */
+int mfs_reset_slot(mfs_ctx* ctx, int slot);
+
+/* Frame count of a slot (its next position), or a negative status. */
+int mfs_position(const mfs_ctx* ctx, int slot);
+
+/* Diagnostics of the last step, rows in that step's slot order (any pointer
+ * may be NULL): text logits [n, V], depformer logits [n, 16, C] (fp32), and
+ * the raw argmaxes before forcing, text [n] and per substep [n, 16]. */
+int mfs_read_debug(mfs_ctx* ctx, float* text_logits, float* dep_logits,
+                   int32_t* text_argmax, int32_t* code_argmax);
+
+/* Execution mode: 0 (default) = one persistent cooperative launch per step
+ * with grid-wide barriers between phases; 1 = one launch per phase (same
+ * arithmetic, for diagnosis). */
+int mfs_set_mode(mfs_ctx* ctx, int mode);
+
+/* Kernel launches made by the last step (for accounting). */
+int mfs_launches_per_step(const mfs_ctx* ctx);
+
+/* Kernel timing.  While enabled, every step records a CUDA event pair on the
+ * context's stream around its kernel launch(es).  mfs_kernel_time waits for
+ * the stream, returns the summed device time (ms) and the number of steps
+ * timed since the previous call, and starts a new sum. */
+int mfs_set_timing(mfs_ctx* ctx, int enable);
+int mfs_kernel_time(mfs_ctx* ctx, double* total_ms, int* steps);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MFS_H */

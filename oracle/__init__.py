@@ -34,7 +34,7 @@ _lib = None
 def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + ".tmp"
-        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c11",
+        subprocess.check_call(["gcc", "-O3", "-fPIC", "-shared", "-fopenmp", "-std=c11",
                                _SRC, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB

@@ -141,6 +141,37 @@ static void matvec(const orc* o, const void* W, size_t row0, int N, int K,
     }
 }
 
+/* Y[t][n] = sum_k W[n][k] X[t][k] for T frames (prompt path).  Every entry
+ * is the same ascending-k sum as matvec(); rows are taken 32 at a time with
+ * the frames innermost only so that one pass over W serves all T frames. */
+static void matmul_frames(const orc* o, const void* W, int N, int K, const double* X, int T, double* Y)
+{
+    double* XT = (double*)malloc(sizeof(double) * (size_t)K * (size_t)T);
+    for (int t = 0; t < T; ++t)
+        for (int k = 0; k < K; ++k) XT[(size_t)k * T + t] = X[(size_t)t * K + k];
+#pragma omp parallel
+    {
+        double* acc = (double*)malloc(sizeof(double) * 32 * (size_t)T);
+#pragma omp for schedule(dynamic)
+        for (int n0 = 0; n0 < N; n0 += 32) {
+            int m = N - n0 < 32 ? N - n0 : 32;
+            for (size_t i = 0; i < (size_t)m * T; ++i) acc[i] = 0.0;
+            for (int k = 0; k < K; ++k) {
+                const double* x = XT + (size_t)k * T;
+                for (int r = 0; r < m; ++r) {
+                    double w = w_at(o, W, (size_t)(n0 + r) * (size_t)K + (size_t)k);
+                    double* a = acc + (size_t)r * T;
+                    for (int t = 0; t < T; ++t) a[t] += w * x[t];
+                }
+            }
+            for (int r = 0; r < m; ++r)
+                for (int t = 0; t < T; ++t) Y[(size_t)t * N + n0 + r] = acc[(size_t)r * T + t];
+        }
+        free(acc);
+    }
+    free(XT);
+}
+
 /* RMSNorm: out = x / sqrt(mean(x^2) + eps) * g  (g fp32) */
 void orc_rmsnorm(const double* x, const float* g, int n, double eps, double* out)
 {
@@ -327,49 +358,54 @@ static int input_token(const orc* o, const orc_slot* s, int k, int p)
     return s->hist[k][mod(f, ORC_HIST)];
 }
 
+/* Rotate q and k of one position, store k and v at the ring row of position p,
+ * and attend over the window of p (keys in ascending absolute position). */
+static void attend(orc* o, orc_slot* s, int l, int p, double* q, double* k, const double* v, double* att)
+{
+    const orc_config* c = &o->c;
+    int d = c->d, H = c->n_heads, hd = c->head_dim, W = c->window;
+    int len = p + 1 < W ? p + 1 : W;
+    int start = p - len + 1;
+    size_t layer_stride = (size_t)o->cap * (size_t)d;
+    for (int hh = 0; hh < H; ++hh) {
+        orc_rope(q + hh * hd, hd, p, c->rope_theta);
+        orc_rope(k + hh * hd, hd, p, c->rope_theta);
+    }
+    int row = c->brute_force ? p : mod(p, W);
+    double* Kl = s->K + (size_t)l * layer_stride;
+    double* Vl = s->V + (size_t)l * layer_stride;
+    memcpy(Kl + (size_t)row * d, k, sizeof(double) * (size_t)d);
+    memcpy(Vl + (size_t)row * d, v, sizeof(double) * (size_t)d);
+    double* Kw = (double*)malloc(sizeof(double) * (size_t)len * (size_t)d);
+    double* Vw = (double*)malloc(sizeof(double) * (size_t)len * (size_t)d);
+    for (int j = 0; j < len; ++j) {
+        int pos = start + j;
+        int r = c->brute_force ? pos : mod(pos, W);
+        memcpy(Kw + (size_t)j * d, Kl + (size_t)r * d, sizeof(double) * (size_t)d);
+        memcpy(Vw + (size_t)j * d, Vl + (size_t)r * d, sizeof(double) * (size_t)d);
+    }
+    for (int hh = 0; hh < H; ++hh)
+        orc_attention(q + hh * hd, Kw + hh * hd, Vw + hh * hd, len, hd, d, att + hh * hd);
+    free(Kw); free(Vw);
+}
+
 /* temporal stack for one slot at position p; x[d] in, h[d] (post final norm) out
  * when h != NULL. */
 static void temporal(orc* o, orc_slot* s, int p, double* x, double* h)
 {
     const orc_config* c = &o->c;
-    int d = c->d, H = c->n_heads, hd = c->head_dim, F = c->ffn, W = c->window;
+    int d = c->d, F = c->ffn;
     double* a = (double*)malloc(sizeof(double) * (size_t)d);
     double* qkv = (double*)malloc(sizeof(double) * (size_t)(3 * d));
     double* att = (double*)malloc(sizeof(double) * (size_t)d);
     double* y = (double*)malloc(sizeof(double) * (size_t)d);
     double* gu = (double*)malloc(sizeof(double) * (size_t)(2 * F));
     double* act = (double*)malloc(sizeof(double) * (size_t)F);
-    int len = p + 1 < W ? p + 1 : W;
-    int start = p - len + 1;
-    size_t layer_stride = (size_t)o->cap * (size_t)d;
     for (int l = 0; l < c->n_layers; ++l) {
         const orc_layer* Ly = &o->L[l];
         orc_rmsnorm(x, (const float*)Ly->attn_norm, d, c->eps, a);
         matvec(o, Ly->wqkv, 0, 3 * d, d, a, qkv);
-        double* q = qkv;
-        double* k = qkv + d;
-        double* v = qkv + 2 * d;
-        for (int hh = 0; hh < H; ++hh) {
-            orc_rope(q + hh * hd, hd, p, c->rope_theta);
-            orc_rope(k + hh * hd, hd, p, c->rope_theta);
-        }
-        int row = c->brute_force ? p : mod(p, W);
-        double* Kl = s->K + (size_t)l * layer_stride;
-        double* Vl = s->V + (size_t)l * layer_stride;
-        memcpy(Kl + (size_t)row * d, k, sizeof(double) * (size_t)d);
-        memcpy(Vl + (size_t)row * d, v, sizeof(double) * (size_t)d);
-        /* gather the window's keys in ascending absolute position */
-        double* Kw = (double*)malloc(sizeof(double) * (size_t)len * (size_t)d);
-        double* Vw = (double*)malloc(sizeof(double) * (size_t)len * (size_t)d);
-        for (int j = 0; j < len; ++j) {
-            int pos = start + j;
-            int r = c->brute_force ? pos : mod(pos, W);
-            memcpy(Kw + (size_t)j * d, Kl + (size_t)r * d, sizeof(double) * (size_t)d);
-            memcpy(Vw + (size_t)j * d, Vl + (size_t)r * d, sizeof(double) * (size_t)d);
-        }
-        for (int hh = 0; hh < H; ++hh)
-            orc_attention(q + hh * hd, Kw + hh * hd, Vw + hh * hd, len, hd, d, att + hh * hd);
-        free(Kw); free(Vw);
+        attend(o, s, l, p, qkv, qkv + d, qkv + 2 * d, att);
         matvec(o, Ly->wo, 0, d, d, att, y);
         for (int i = 0; i < d; ++i) x[i] += y[i];
         orc_rmsnorm(x, (const float*)Ly->ffn_norm, d, c->eps, a);
@@ -519,7 +555,11 @@ int orc_step(orc* o, int n, const int* slots, const int* codes, int* text_out, i
 
 /* T frames of one slot with every token supplied: the temporal stack only.
  * With all 17 rows forced the text head and the depformer change nothing in
- * the slot's state, so they are not run. */
+ * the slot's state, so they are not run.  Frames are taken layer by layer
+ * (each layer's products for a block of frames at once, then the frames'
+ * attention in frame order, so a frame only sees keys of earlier positions);
+ * the arithmetic of every frame is that of orc_step. */
+#define ORC_PREFILL_BLOCK 256
 int orc_prefill(orc* o, int slot, int T, const int* codes)
 {
     const orc_config* c = &o->c;
@@ -530,12 +570,43 @@ int orc_prefill(orc* o, int slot, int T, const int* codes)
     for (int t = 0; t < T; ++t)
         if (check_tokens(o, codes + (size_t)t * ORC_STREAMS, 0)) { snprintf(o->err, sizeof o->err, "bad token"); return -4; }
     if (ensure_kv(o, s)) return -6;
-    double* x = (double*)malloc(sizeof(double) * (size_t)c->d);
-    for (int t = 0; t < T; ++t) {
-        embed(o, s, codes + (size_t)t * ORC_STREAMS, x, NULL);
-        temporal(o, s, s->pos, x, NULL);
-        s->pos += 1;
+    int d = c->d, F = c->ffn;
+    for (int t0 = 0; t0 < T; t0 += ORC_PREFILL_BLOCK) {
+        int nt = T - t0 < ORC_PREFILL_BLOCK ? T - t0 : ORC_PREFILL_BLOCK;
+        int p0 = s->pos;
+        double* X = (double*)malloc(sizeof(double) * (size_t)nt * d);
+        double* A = (double*)malloc(sizeof(double) * (size_t)nt * d);
+        double* QKV = (double*)malloc(sizeof(double) * (size_t)nt * 3 * d);
+        double* ATT = (double*)malloc(sizeof(double) * (size_t)nt * d);
+        double* Y = (double*)malloc(sizeof(double) * (size_t)nt * d);
+        double* GU = (double*)malloc(sizeof(double) * (size_t)nt * 2 * F);
+        double* ACT = (double*)malloc(sizeof(double) * (size_t)nt * F);
+        for (int t = 0; t < nt; ++t) {
+            s->pos = p0 + t;
+            embed(o, s, codes + (size_t)(t0 + t) * ORC_STREAMS, X + (size_t)t * d, NULL);
+        }
+        for (int l = 0; l < c->n_layers; ++l) {
+            const orc_layer* Ly = &o->L[l];
+            for (int t = 0; t < nt; ++t)
+                orc_rmsnorm(X + (size_t)t * d, (const float*)Ly->attn_norm, d, c->eps, A + (size_t)t * d);
+            matmul_frames(o, Ly->wqkv, 3 * d, d, A, nt, QKV);
+            for (int t = 0; t < nt; ++t) {
+                double* q = QKV + (size_t)t * 3 * d;
+                attend(o, s, l, p0 + t, q, q + d, q + 2 * d, ATT + (size_t)t * d);
+            }
+            matmul_frames(o, Ly->wo, d, d, ATT, nt, Y);
+            for (size_t i = 0; i < (size_t)nt * d; ++i) X[i] += Y[i];
+            for (int t = 0; t < nt; ++t)
+                orc_rmsnorm(X + (size_t)t * d, (const float*)Ly->ffn_norm, d, c->eps, A + (size_t)t * d);
+            matmul_frames(o, Ly->wgu, 2 * F, d, A, nt, GU);
+            for (int t = 0; t < nt; ++t)
+                for (int i = 0; i < F; ++i)
+                    ACT[(size_t)t * F + i] = silu(GU[(size_t)t * 2 * F + i]) * GU[(size_t)t * 2 * F + F + i];
+            matmul_frames(o, Ly->wdown, d, F, ACT, nt, Y);
+            for (size_t i = 0; i < (size_t)nt * d; ++i) X[i] += Y[i];
+        }
+        s->pos = p0 + nt;
+        free(X); free(A); free(QKV); free(ATT); free(Y); free(GU); free(ACT);
     }
-    free(x);
     return 0;
 }

@@ -1,0 +1,62 @@
+"""Shared helpers for the GPU tests: contexts from synth shapes, and the
+acceptance rules of the frame step against the oracle.
+
+Acceptance (floating point): each logit vector within 2e-2 x its RMS of the
+oracle's, elementwise; greedy tokens equal unless the oracle's top-2 margin is
+below 0.1 (a legal flip).  Integer work is compared bit for bit.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import synth
+
+LOGIT_RTOL = 2e-2       # x rms(oracle logits), elementwise
+FLIP_MARGIN = 0.1       # argmax may differ only below this top-2 margin
+
+
+def config_of(shape):
+    from full_duplex_speech_frame_gb300 import mfs
+    s = shape
+    return mfs.make_config(d=s.d, n_layers=s.n_layers, n_heads=s.n_heads, head_dim=s.head_dim, ffn=s.ffn,
+                           text_vocab=s.text_vocab, card=s.card, window=s.window, max_pos=s.max_pos,
+                           dep_d=s.dep_d, dep_layers=s.dep_layers, dep_heads=s.dep_heads,
+                           dep_head_dim=s.dep_head_dim, dep_ffn=s.dep_ffn, delays=s.delays,
+                           rope_theta=s.rope_theta, eps=s.eps, weight_dtype=s.weight_dtype,
+                           kv_dtype=s.kv_dtype, max_slots=s.max_slots, n_q=s.n_q, dep_steps=s.dep_steps)
+
+
+def gpu_context(shape, weights):
+    from full_duplex_speech_frame_gb300 import mfs
+    ctx = mfs.mfs_create(config_of(shape))
+    for name, arr in weights.items():
+        mfs.mfs_load_weights(ctx, name, arr)
+    return ctx
+
+
+def check_logits(gpu: np.ndarray, ref: np.ndarray, what: str) -> float:
+    """Elementwise |gpu - ref| <= 2e-2 * rms(ref) per vector (last axis).  Returns the worst ratio."""
+    ref = np.asarray(ref, np.float64)
+    gpu = np.asarray(gpu, np.float64)
+    rms = np.sqrt(np.mean(ref * ref, axis=-1, keepdims=True))
+    ratio = np.abs(gpu - ref) / rms
+    worst = float(ratio.max())
+    assert worst <= LOGIT_RTOL, f"{what}: |gpu-ref|/rms = {worst:.3e} > {LOGIT_RTOL}"
+    return worst
+
+
+def top2_margin(logits: np.ndarray) -> np.ndarray:
+    part = np.sort(logits, axis=-1)
+    return part[..., -1] - part[..., -2]
+
+
+def argmax_agrees(gpu_am: np.ndarray, ref_logits: np.ndarray) -> np.ndarray:
+    """Boolean mask: equal argmax, or the oracle's top-2 margin < 0.1."""
+    ref_am = np.argmax(ref_logits, axis=-1)
+    return (gpu_am == ref_am) | (top2_margin(ref_logits) < FLIP_MARGIN)
+
+
+def check_argmax(gpu_am, ref_logits, what: str) -> int:
+    ok = argmax_agrees(np.asarray(gpu_am), np.asarray(ref_logits))
+    assert ok.all(), f"{what}: greedy token differs with top-2 margin >= {FLIP_MARGIN} at {np.argwhere(~ok)[:5]}"
+    return int((np.asarray(gpu_am) != np.argmax(ref_logits, axis=-1)).sum())
