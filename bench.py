@@ -37,7 +37,8 @@ UNIT = "frames/s"
 
 def algorithmic_bytes(s, lens):
     """Bytes one step must move: every streamed weight once, the embedding rows
-    read, and per slot the keys/values of its window plus this frame's writes."""
+    read, and per slot (lens = window length of each slot in the step) the
+    keys/values of its window plus this frame's writes."""
     wb = 2 if s.weight_dtype == "bf16" else 4
     kvb = 2 if s.kv_dtype == "bf16" else 4
     d, F, V, C, S, L = s.d, s.ffn, s.text_vocab, s.card, s.dep_steps, s.n_layers
@@ -211,6 +212,9 @@ def run_gpu(args, rank, world):
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
+    # a stream of our own: the library enqueues on it and the events below time it
+    side = torch.cuda.Stream()
+    torch.cuda.set_stream(side)
     s = WORKLOAD.shape
     n = WORKLOAD.batch
     need = args.warmup + 2 * args.steps
@@ -235,10 +239,8 @@ def run_gpu(args, rank, world):
     base = args.warmup
 
     # device-resident timed region (the value)
-    lens = []
-    for k in range(args.steps):
-        lens += [min(PROMPT + base + k + 1, s.window)] * n
-    mfs.mfs_set_timing(ctx, True)
+    lens = [[min(PROMPT + base + k + 1, s.window)] * n for k in range(args.steps)]
+    mfs.mfs_set_timing(ctx, 1)
     mfs.mfs_kernel_time(ctx)
     barrier(world)
     torch.cuda.synchronize()
@@ -253,7 +255,7 @@ def run_gpu(args, rank, world):
     barrier(world)
     ms = e0.elapsed_time(e1)
     kms, ksteps = mfs.mfs_kernel_time(ctx)
-    mfs.mfs_set_timing(ctx, False)
+    mfs.mfs_set_timing(ctx, 0)
     launches = mfs.mfs_launches_per_step(ctx) * args.steps
     ms_max = max_over_ranks(ms, world)
     value = n * args.steps * world / (ms_max / 1000.0)
@@ -273,7 +275,7 @@ def run_gpu(args, rank, world):
     if rank != 0:
         return
     hbm, peak_kind = read_peaks()
-    bytes_step = algorithmic_bytes(s, lens) / args.steps
+    bytes_step = sum(algorithmic_bytes(s, l) for l in lens) / args.steps
     kernel_ms = kms / max(ksteps, 1)
     achieved = bytes_step / (kernel_ms / 1000.0) / 1e9
     traffic = recorded_traffic("full_b1")

@@ -88,6 +88,9 @@ struct mfs_ctx {
     std::string err;
     // kernel timing
     bool timing = false;
+    bool stamps = false;
+    unsigned long long* d_ptime = nullptr;
+    int last_nph = 0;
     std::vector<cudaEvent_t> ev_pool;
     size_t ev_used = 0;
 };
@@ -457,6 +460,7 @@ extern "C" void mfs_destroy(mfs_ctx* c)
     cudaFree(c->arena); cudaFree(c->gains); cudaFree(c->kc); cudaFree(c->vc); cudaFree(c->hist);
     cudaFree(c->act); cudaFree(c->rope); cudaFree(c->d_phases); cudaFree(c->d_desc); cudaFree(c->d_pref);
     cudaFree(c->d_bar);
+    cudaFree(c->d_ptime);
     for (int i = 0; i < DESC_RING; ++i)
         if (c->desc_ev[i]) cudaEventDestroy(c->desc_ev[i]);
     for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
@@ -533,6 +537,8 @@ static int launch(mfs_ctx* c, int n, int nph, const StepDesc* desc)
 {
     Params P = c->P;
     P.desc = desc;
+    P.ptime = c->stamps ? c->d_ptime : nullptr;
+    c->last_nph = nph;
     const int bi = bg_index(n);
     int maxrows = c->maxrows;
     CK(cudaMemsetAsync(c->d_bar, 0, 4, c->stream));
@@ -764,11 +770,27 @@ extern "C" int mfs_launches_per_step(const mfs_ctx* c)
     return c->launches;
 }
 
-extern "C" int mfs_set_timing(mfs_ctx* c, int enable)
+extern "C" int mfs_set_timing(mfs_ctx* c, int flags)
 {
     if (!c) return MFS_E_ARG;
-    c->timing = enable != 0;
+    c->timing = (flags & 1) != 0;
+    c->stamps = (flags & 2) != 0;
+    if (c->stamps && !c->d_ptime) {
+        CK(cudaMalloc((void**)&c->d_ptime, (size_t)(c->nphase + 1) * sizeof(unsigned long long)));
+        CK(cudaMemset(c->d_ptime, 0, (size_t)(c->nphase + 1) * sizeof(unsigned long long)));
+    }
     return MFS_OK;
+}
+
+extern "C" int mfs_phase_times(mfs_ctx* c, uint64_t* ns, int cap)
+{
+    if (!c || !ns) return MFS_E_ARG;
+    if (!c->d_ptime) return fail(c, MFS_E_STATE, "phase stamps were never enabled");
+    CK(cudaStreamSynchronize(c->stream));
+    const int cnt = c->last_nph + 1;
+    if (cap < cnt) return fail(c, MFS_E_ARG, "need room for %d stamps", cnt);
+    CK(cudaMemcpy(ns, c->d_ptime, (size_t)cnt * sizeof(uint64_t), cudaMemcpyDeviceToHost));
+    return cnt;
 }
 
 extern "C" int mfs_kernel_time(mfs_ctx* c, double* total_ms, int* steps)

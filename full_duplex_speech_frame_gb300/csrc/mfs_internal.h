@@ -99,6 +99,7 @@ struct Params {
     int* err;        // sticky device error (DeviceError)
     int* err_seq;    // step sequence number that raised it
     const Phase* phases;
+    unsigned long long* ptime;  // optional: globaltimer at each phase start (CTA 0), [nphase + 1]
 };
 
 // Kernel entry points, one per (weight dtype, batch group).  Defined in the

@@ -511,16 +511,19 @@ __device__ void epi_logits(const Params& P, float* lg, long long lg_stride, int 
     }
 }
 
-// Reduce the per-CTA argmax partials of batch row i (same result in every thread).
-__device__ __forceinline__ int argmax_partials(const Params& P, int i)
+// Reduce the per-CTA argmax partials of batch row i with one warp (every lane
+// gets the same result; the tie rule makes the combine order irrelevant).
+__device__ __forceinline__ int argmax_partials_warp(const Params& P, int i)
 {
+    const int lane = threadIdx.x & 31;
     float v = -INFINITY;
     int ix = 0x7fffffff;
-    for (int c = 0; c < P.G; ++c) {
+    for (int c = lane; c < P.G; c += 32) {
         const float v2 = ld_cg_f(P.amax_v + (size_t)i * P.G + c);
         const int i2 = ld_cg_int(P.amax_i + (size_t)i * P.G + c);
         if (am_better(v2, i2, v, ix)) { v = v2; ix = i2; }
     }
+    warp_argmax(v, ix);
     return ix == 0x7fffffff ? 0 : ix;
 }
 
@@ -532,23 +535,24 @@ __device__ __forceinline__ int argmax_partials(const Params& P, int i)
 __device__ void dep_select_inputs(const Params& P, int j, int b0, int nb, const Smem& sm)
 {
     const StepDesc* D = P.desc;
-    if (threadIdx.x < nb) {
-        const int i = b0 + threadIdx.x;
-        const int a = argmax_partials(P, i);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < nb) {
+        const int i = b0 + warp;
+        const int a = argmax_partials_warp(P, i);
         int chosen;
         if (j == 0) {
             const int forced = D->codes[i][0];
             chosen = forced >= 0 ? forced : a;
-            if (blockIdx.x == 0) { P.text_argmax[i] = a; P.chosen[i * NSTREAM + 0] = chosen; }
+            if (blockIdx.x == 0 && lane == 0) { P.text_argmax[i] = a; P.chosen[i * NSTREAM + 0] = chosen; }
         } else {
             const int p = D->pos[i], f = p - P.delays[j];
             const int forced =
                 f >= 0 ? ld_cg_int(P.hist + ((size_t)D->slot[i] * NSTREAM + j) * HIST + f % HIST) : -1;
             chosen = forced >= 0 ? forced : a;
-            if (blockIdx.x == 0) { P.code_argmax[i * 16 + (j - 1)] = a; P.chosen[i * NSTREAM + j] = chosen; }
+            if (blockIdx.x == 0 && lane == 0) { P.code_argmax[i * 16 + (j - 1)] = a; P.chosen[i * NSTREAM + j] = chosen; }
         }
         const int lim = j == 0 ? P.V : P.C;
-        sm.prev[threadIdx.x] = (chosen >= 0 && chosen < lim) ? chosen : 0;  // keeps the embedding read in range
+        if (lane == 0) sm.prev[warp] = (chosen >= 0 && chosen < lim) ? chosen : 0;  // keeps the embedding read in range
     }
     __syncthreads();
 }
@@ -754,19 +758,17 @@ __device__ void phase_attn(const Params& P, int l, int n, const Smem& sm)
         if (old == nc - 1) {
             __threadfence();
             const float* pb = P.apart + ((size_t)i * H + h) * NCHUNK_MAX * pstride;
-            float M = -INFINITY;
-            for (int cc = 0; cc < nc; ++cc) M = fmaxf(M, ld_cg_f(pb + (size_t)cc * pstride));
-            float L = 0.f;
-            for (int cc = 0; cc < nc; ++cc) {
-                const float mc = ld_cg_f(pb + (size_t)cc * pstride);
-                if (mc != -INFINITY) L += ld_cg_f(pb + (size_t)cc * pstride + 1) * expf(mc - M);
-            }
-            const float invL = 1.f / L;
+            const float mc = lane < nc ? ld_cg_f(pb + (size_t)lane * pstride) : -INFINITY;
+            const float lc = lane < nc ? ld_cg_f(pb + (size_t)lane * pstride + 1) : 0.f;
+            const float M = warp_max(mc);
+            const float wc = mc == -INFINITY ? 0.f : expf(mc - M);
+            const float invL = 1.f / warp_sum(lc * wc);
             for (int e = lane; e < hd; e += 32) {
                 float a = 0.f;
+#pragma unroll 4
                 for (int cc = 0; cc < nc; ++cc) {
-                    const float mc = ld_cg_f(pb + (size_t)cc * pstride);
-                    if (mc != -INFINITY) a += ld_cg_f(pb + (size_t)cc * pstride + 4 + e) * expf(mc - M);
+                    const float wcc = __shfl_sync(0xffffffffu, wc, cc);
+                    a = fmaf(wcc, ld_cg_f(pb + (size_t)cc * pstride + 4 + e), a);
                 }
                 P.o[(size_t)i * d + h * hd + e] = a * invL;
             }
@@ -817,10 +819,11 @@ __device__ void phase_final(const Params& P, int n)
 {
     if (blockIdx.x != 0) return;
     const StepDesc* D = P.desc;
-    if (threadIdx.x < n) {
-        const int i = threadIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = warp; i < n; i += NWARP) {
         const int S = P.S;
-        const int a = argmax_partials(P, i);
+        const int a = argmax_partials_warp(P, i);
+        if (lane != 0) continue;
         const int p = D->pos[i], slot = D->slot[i];
         {
             const int f = p - P.delays[S];
@@ -961,6 +964,7 @@ __global__ void __launch_bounds__(NT, 1) step_kernel(Params P, int ph0, int ph1,
     }
     unsigned target = 0;
     for (int ph = ph0; ph < ph1; ++ph) {
+        if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) P.ptime[ph] = globaltimer_ns();
         const Phase phs = P.phases[ph];
         run_phase<TW, TKV, BG>(P, phs, n, sm);
         if (coop && ph + 1 < ph1) {
@@ -968,6 +972,7 @@ __global__ void __launch_bounds__(NT, 1) step_kernel(Params P, int ph0, int ph1,
             if (!grid_barrier(P.bar, target, P.err)) return;
         }
     }
+    if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) P.ptime[ph1] = globaltimer_ns();
 }
 
 }  // namespace

@@ -60,6 +60,7 @@ def _load_library():
         "mfs_launches_per_step": (ci, [vp]),
         "mfs_set_timing": (ci, [vp, ci]),
         "mfs_kernel_time": (ci, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
+        "mfs_phase_times": (ci, [vp, vp, ci]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -225,8 +226,18 @@ def mfs_launches_per_step(ctx: Ctx) -> int:
     return _lib.mfs_launches_per_step(ctx.handle)
 
 
-def mfs_set_timing(ctx: Ctx, enable: bool) -> None:
-    _check(ctx, _lib.mfs_set_timing(ctx.handle, 1 if enable else 0))
+def mfs_set_timing(ctx: Ctx, flags) -> None:
+    """flags: bit 0 = event timing of each step's kernel, bit 1 = per-phase timer stamps."""
+    _check(ctx, _lib.mfs_set_timing(ctx.handle, int(flags)))
+
+
+def mfs_phase_times(ctx: Ctx) -> np.ndarray:
+    """Global-timer stamps (ns) at the start of each phase of the last step, plus its end."""
+    buf = np.zeros(4096, np.uint64)
+    rc = _lib.mfs_phase_times(ctx.handle, buf.ctypes.data, buf.size)
+    if rc < 0:
+        _check(ctx, rc)
+    return buf[:rc].copy()
 
 
 def mfs_kernel_time(ctx: Ctx):

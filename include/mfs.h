@@ -154,12 +154,16 @@ int mfs_set_mode(mfs_ctx* ctx, int mode);
 /* Kernel launches made by the last step (for accounting). */
 int mfs_launches_per_step(const mfs_ctx* ctx);
 
-/* Kernel timing.  While enabled, every step records a CUDA event pair on the
- * context's stream around its kernel launch(es).  mfs_kernel_time waits for
+/* Kernel timing.  flags bit 0: every step records a CUDA event pair on the
+ * context's stream around its kernel launch(es); mfs_kernel_time waits for
  * the stream, returns the summed device time (ms) and the number of steps
- * timed since the previous call, and starts a new sum. */
-int mfs_set_timing(mfs_ctx* ctx, int enable);
+ * timed since the previous call, and starts a new sum.  flags bit 1: the
+ * kernel stamps the GPU's global timer at the start of every phase (and at
+ * the end); mfs_phase_times copies the stamps (ns) of the last step into
+ * ns[0..count) and returns count (phases + 1), or a negative status. */
+int mfs_set_timing(mfs_ctx* ctx, int flags);
 int mfs_kernel_time(mfs_ctx* ctx, double* total_ms, int* steps);
+int mfs_phase_times(mfs_ctx* ctx, uint64_t* ns, int cap);
 
 #ifdef __cplusplus
 }
