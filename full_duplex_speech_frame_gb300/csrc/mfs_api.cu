@@ -16,7 +16,6 @@ using namespace mfs;
 
 namespace {
 
-constexpr int SCRATCH_FLOATS = 4096;  // must match the kernels' shared-memory map
 constexpr int PREF_CHUNK = 256;       // prompt frames staged per copy
 constexpr int DESC_RING = 8;          // pinned step descriptors in flight
 
@@ -144,8 +143,10 @@ static int check_config(mfs_ctx* c, const mfs_config& g)
     if (g.dep_head_dim != 64 || g.dep_heads * g.dep_head_dim != g.dep_d)
         return fail(c, MFS_E_ARG, "config: dep_head_dim must be 64 and dep_heads * 64 == dep_d");
     const int Ks[4] = {g.d, g.ffn, g.dep_d, g.dep_ffn};
+    const int wbytes = g.weight_dtype == MFS_DTYPE_BF16 ? 2 : 4;
     for (int K : Ks)
-        if (K % 8 != 0 || K > 12288) return fail(c, MFS_E_ARG, "config: K dimension %d not a multiple of 8 or > 12288", K);
+        if (K % 8 != 0 || K > 12288 || K * wbytes > STAGE_BYTES)
+            return fail(c, MFS_E_ARG, "config: K dimension %d not a multiple of 8, or a row exceeds %d bytes", K, STAGE_BYTES);
     if (g.text_vocab % 2 || g.card % 2) return fail(c, MFS_E_ARG, "config: vocabularies must be even");
     if (g.max_slots < 1 || g.max_slots > MFS_MAX_SLOTS) return fail(c, MFS_E_ARG, "config: max_slots out of range");
     if (g.weight_dtype != MFS_DTYPE_F32 && g.weight_dtype != MFS_DTYPE_BF16) return fail(c, MFS_E_ARG, "config: weight_dtype");
@@ -418,11 +419,18 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
     for (int i = 0; i < 3; ++i) {
         const int bg = bg_value(i);
         c->kfn[i] = g.weight_dtype == MFS_DTYPE_BF16 ? kernel_bf16(bg) : kernel_f32(bg);
-        c->smem[i] = ((size_t)c->maxrows * bg * 17 + SCRATCH_FLOATS) * sizeof(float);
+        // ring, then one region used as GEMV partials + row values, attention
+        // partials, or the step's embedding rows, whichever phase runs
+        const size_t gemv = ((size_t)2 * RPS_MAX * bg * 16 + (size_t)c->maxrows * bg) * sizeof(float);
+        const size_t attn = (size_t)NWARP * (g.head_dim + 4) * sizeof(float);
+        const size_t emb = (size_t)MFS_MAX_SLOTS * NSTREAM * sizeof(int);
+        size_t region = gemv > attn ? gemv : attn;
+        region = region > emb ? region : emb;
+        c->smem[i] = SMEM_HEAD + (size_t)NSTAGE * STAGE_BYTES + region;
         if (c->smem[i] > 227 * 1024) return fail(c, MFS_E_ARG, "shape needs %zu B of shared memory", c->smem[i]);
         CK(cudaFuncSetAttribute(c->kfn[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c->smem[i]));
         int per_sm = 0;
-        CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, c->kfn[i], NT, c->smem[i]));
+        CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, c->kfn[i], NT + 32, c->smem[i]));
         if (per_sm < 1) return fail(c, MFS_E_CUDA, "kernel does not fit on an SM");
     }
     c->pos.assign(MS, 0);
@@ -558,13 +566,13 @@ static int launch(mfs_ctx* c, int n, int nph, const StepDesc* desc)
     if (c->mode == 0) {
         int ph0 = 0, ph1 = nph, coop = 1;
         void* args[] = {&P, &ph0, &ph1, &coop, &maxrows};
-        CK(cudaLaunchCooperativeKernel(c->kfn[bi], dim3(c->G), dim3(NT), args, c->smem[bi], c->stream));
+        CK(cudaLaunchCooperativeKernel(c->kfn[bi], dim3(c->G), dim3(NT + 32), args, c->smem[bi], c->stream));
         c->launches = 1;
     } else {
         for (int ph = 0; ph < nph; ++ph) {
             int ph0 = ph, ph1 = ph + 1, coop = 0;
             void* args[] = {&P, &ph0, &ph1, &coop, &maxrows};
-            CK(cudaLaunchKernel(c->kfn[bi], dim3(c->G), dim3(NT), args, c->smem[bi], c->stream));
+            CK(cudaLaunchKernel(c->kfn[bi], dim3(c->G), dim3(NT + 32), args, c->smem[bi], c->stream));
         }
         c->launches = nph;
     }

@@ -7,8 +7,12 @@
 
 namespace mfs {
 
-constexpr int NT = 512;          // threads per CTA (16 warps)
+constexpr int NT = 512;          // consumer threads per CTA (16 warps); one more warp produces
 constexpr int NWARP = NT / 32;
+constexpr int NSTAGE = 8;        // weight ring stages per CTA
+constexpr int STAGE_BYTES = 24576;
+constexpr int RPS_MAX = 16;      // rows per stage at most
+constexpr int SMEM_HEAD = 1024;  // mbarriers and scalars before the ring
 constexpr int NSTREAM = MFS_N_STREAMS;
 constexpr int NCHUNK_MAX = 32;   // attention split over the window, per (slot, head)
 constexpr int HIST = 3;          // frames of token history per stream

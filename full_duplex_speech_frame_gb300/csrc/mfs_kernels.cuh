@@ -3,15 +3,20 @@
 // One persistent cooperative kernel runs every phase of a step (embedding sum,
 // 32 temporal layers, text head, 16 depformer substeps, write-back) with a
 // grid-wide barrier between phases; the same kernel can also be launched once
-// per phase (no barriers) for diagnosis.  One CTA per SM, 16 warps.
+// per phase (no barriers) for diagnosis.  One CTA per SM: 16 consumer warps
+// and one producer warp.
 //
-// Matrix-vector phases stream bf16 (or fp32) weight rows with 128-bit
-// non-allocating loads.  A CTA owns a contiguous block of row pairs; its 16
-// warps split K into contiguous slices so that each warp keeps its slice of
-// the (normalised) activations in registers for the whole phase.  Partial dot
-// products are reduced lane-wise with a fixed shuffle tree, then across the
-// K-slices in slice order: the arithmetic of one slot never depends on the
-// other slots of the batch, on the batch size or on the CTA that owns a row.
+// Weights move by TMA bulk copies (cp.async.bulk) into a ring of shared-memory
+// stages guarded by mbarriers.  The producer walks the same phase schedule as
+// the consumers and copies each phase's weight rows as soon as a stage is
+// free, so it runs ahead across the grid barriers and HBM keeps streaming while
+// the consumers synchronise.  A CTA owns a contiguous block of row pairs of
+// every matrix; its 16 consumer warps split K into contiguous slices and keep
+// their slice of the (normalised) activations in registers for the whole
+// phase.  Partial dot products are reduced lane-wise with a fixed shuffle
+// tree, then across K-slices in slice order: the arithmetic of one slot never
+// depends on the other slots of the batch, on the batch size or on the CTA
+// that owns a row.
 #pragma once
 #include <cuda_bf16.h>
 #include <math.h>
@@ -161,13 +166,18 @@ __device__ __forceinline__ float block_sum(float v, float* scratch)
     return t;
 }
 
-// ------------------------------------------------------------------ grid barrier
+// ------------------------------------------------------------------ synchronisation
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p)
 {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned long long globaltimer_ns()
@@ -177,68 +187,119 @@ __device__ __forceinline__ unsigned long long globaltimer_ns()
     return t;
 }
 
-// All CTAs arrive; returns false (and leaves the error flag set) if the wait
-// gave up after 2 s or another CTA reported an error.
-__device__ bool grid_barrier(unsigned* bar, unsigned target, int* err)
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // every spin gives up after 2 s
+
+// Barrier over the 16 consumer warps of the CTA (the producer warp never joins).
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+
+// All CTAs' consumers arrive; false (error flag set) if the wait gave up or
+// another CTA reported an error.
+__device__ bool grid_barrier(unsigned* bar, unsigned target, int* err, int* s_ok)
 {
-    __shared__ int s_ok;
-    __syncthreads();
+    csync();
     if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(bar, 1u);
+        red_release_add(bar, 1u);
         int ok = 1;
-        const unsigned long long t0 = globaltimer_ns();
+        unsigned long long t0 = 0;
         unsigned spins = 0;
         while (ld_acquire_u32(bar) < target) {
             if ((++spins & 63u) == 0u) {
                 if (*(volatile int*)err != 0) { ok = 0; break; }
-                if (globaltimer_ns() - t0 > 2000000000ull) {
-                    atomicCAS(err, 0, (int)DERR_BARRIER);
-                    ok = 0;
-                    break;
-                }
+                const unsigned long long t = globaltimer_ns();
+                if (t0 == 0) t0 = t;
+                else if (t - t0 > WAIT_LIMIT_NS) { atomicCAS(err, 0, (int)DERR_BARRIER); ok = 0; break; }
             }
         }
-        __threadfence();
-        s_ok = ok;
+        *s_ok = ok;
     }
-    __syncthreads();
-    return s_ok != 0;
+    csync();
+    return *(volatile int*)s_ok != 0;
+}
+
+__device__ __forceinline__ unsigned smem_u32(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, unsigned count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, unsigned bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(b)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* b)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint64_t* b, unsigned parity)
+{
+    unsigned ok;
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(b)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of parity `parity` to complete.
+__device__ bool mbar_wait(uint64_t* b, unsigned parity, int* err)
+{
+    unsigned long long t0 = 0;
+    for (unsigned i = 0;; ++i) {
+        if (mbar_try(b, parity)) return true;
+        if ((i & 255u) == 255u) {
+            if (*(volatile int*)err != 0) return false;
+            const unsigned long long t = globaltimer_ns();
+            if (t0 == 0) t0 = t;
+            else if (t - t0 > WAIT_LIMIT_NS) { atomicCAS(err, 0, (int)DERR_BARRIER); return false; }
+        }
+    }
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
 // ------------------------------------------------------------------ shared memory map
 
 struct Smem {
-    float* red;    // [maxrows][BG][16]  per-K-slice partial sums
-    float* yf;     // [maxrows][BG]      final row values of the CTA
-    float* r;      // [BG] RMSNorm factors
-    int* prev;     // [BG] depformer input token per batch row
-    float* sred;   // [NWARP * 4] block-reduction scratch
-    float* amv;    // [NWARP]
-    int* ami;      // [NWARP]
-    int* X;        // [MFS_MAX_SLOTS][17] embedding rows of this step
-    int* att;      // [MFS_MAX_SLOTS][4]  len, chunks, prefix, pad
+    uint64_t* full;   // [NSTAGE] stage filled
+    uint64_t* empty;  // [NSTAGE] stage released
+    float* r;         // [4] RMSNorm factors of the batch group
+    int* prev;        // [4] depformer input token per batch row
+    float* ssq;       // [4][16] per-K-slice sums of squares
+    float* amv;       // [NWARP]
+    int* ami;         // [NWARP]
+    int* ok;          // grid-barrier verdict
+    char* ring;       // [NSTAGE][STAGE_BYTES]
+    float* red;       // [2][RPS_MAX][BG][16] per-K-slice partial sums of a stage
+    float* yf;        // [maxrows][BG] final row values of the CTA
+    int* X;           // embedding rows of this step (aliases red)
+    float* wbuf;      // attention partials of the 16 warps (aliases red)
 };
 
-constexpr int SCRATCH_FLOATS = 4096;
-
-__device__ __forceinline__ Smem smem_map(float* base, int maxrows, int BG)
+__device__ __forceinline__ Smem smem_map(char* base, int maxrows, int BG)
 {
     Smem s;
-    s.red = base;
-    s.yf = s.red + (size_t)maxrows * BG * 16;
-    float* sc = s.yf + (size_t)maxrows * BG;
-    s.r = sc;
-    s.prev = (int*)(sc + 16);
-    s.sred = sc + 64;
-    s.amv = sc + 128;
-    s.ami = (int*)(sc + 160);
-    s.X = (int*)(sc + 256);
-    s.att = (int*)(sc + 256 + MFS_MAX_SLOTS * NSTREAM);
+    s.full = (uint64_t*)base;
+    s.empty = s.full + NSTAGE;
+    s.r = (float*)(base + 256);
+    s.prev = (int*)(base + 272);
+    s.ssq = (float*)(base + 288);
+    s.amv = (float*)(base + 544);
+    s.ami = (int*)(base + 608);
+    s.ok = (int*)(base + 672);
+    s.ring = base + SMEM_HEAD;
+    s.red = (float*)(s.ring + (size_t)NSTAGE * STAGE_BYTES);
+    s.yf = s.red + 2 * RPS_MAX * BG * 16;
+    s.X = (int*)s.red;
+    s.wbuf = s.red;
     return s;
 }
 
-// ------------------------------------------------------------------ GEMV engine
+// ------------------------------------------------------------------ GEMV schedule (producer and consumers)
 
 struct GemvCfg {
     int nwk, nwr, nvw, vpl;
@@ -259,6 +320,87 @@ __device__ __forceinline__ GemvCfg gemv_cfg(int K)
     return c;
 }
 
+template <int BG>
+__device__ __forceinline__ int group_size(int K)
+{
+    return gemv_cfg(K).vpl == 3 ? (BG < 2 ? BG : 2) : BG;
+}
+
+// The weight matrix a phase streams, or false if it streams none.
+template <typename TW>
+__device__ __forceinline__ bool phase_matrix(const Params& P, const Phase& ph, const TW*& W, int& N, int& K)
+{
+    const long long d = P.d, F = P.F, dd = P.dd, dF = P.dF;
+    const TW* tl = (const TW*)P.tw + (size_t)ph.l * P.t_layer;
+    const TW* dl = (const TW*)P.dw + (size_t)ph.j * P.d_sub + (size_t)ph.l * P.d_layer;
+    switch (ph.type) {
+        case PH_QKV: W = tl; N = 3 * d; K = d; return true;
+        case PH_O: W = tl + 3 * d * d; N = d; K = d; return true;
+        case PH_GU: W = tl + 4 * d * d; N = 2 * F; K = d; return true;
+        case PH_DOWN: W = tl + 4 * d * d + 2 * F * d; N = d; K = F; return true;
+        case PH_HEAD: W = (const TW*)P.head; N = P.V + P.S * dd; K = d; return true;
+        case PH_DQKV: W = dl; N = 3 * dd; K = dd; return true;
+        case PH_DO: W = dl + 3 * dd * dd; N = dd; K = dd; return true;
+        case PH_DGU: W = dl + 4 * dd * dd; N = 2 * dF; K = dd; return true;
+        case PH_DDOWN: W = dl + 4 * dd * dd + 2 * dF * dd; N = dd; K = dF; return true;
+        case PH_DHEAD: W = (const TW*)P.dw + (size_t)ph.j * P.d_sub + (size_t)P.dL * P.d_layer; N = P.C; K = dd; return true;
+        default: return false;
+    }
+}
+
+__device__ __forceinline__ void cta_rows(int N, int G, int& r0, int& r1)
+{
+    const int npairs = N / 2;
+    r0 = 2 * (int)((long long)npairs * blockIdx.x / G);
+    r1 = 2 * (int)((long long)npairs * (blockIdx.x + 1) / G);
+}
+
+template <typename TW>
+__device__ __forceinline__ int rows_per_stage(int K)
+{
+    const int r = STAGE_BYTES / (K * (int)sizeof(TW));
+    return r < RPS_MAX ? r : RPS_MAX;
+}
+
+// Producer: copy, for every phase of the launch, every batch group's pass over
+// this CTA's rows, stage by stage, in the order the consumers use them.
+template <typename TW, int BG>
+__device__ void producer(const Params& P, int ph0, int ph1, int n, const Smem& sm)
+{
+    unsigned s = 0;
+    bool ok = true;
+    for (int ph = ph0; ph < ph1 && ok; ++ph) {
+        const TW* W;
+        int N, K;
+        if (!phase_matrix<TW>(P, P.phases[ph], W, N, K)) continue;
+        int r0, r1;
+        cta_rows(N, P.G, r0, r1);
+        const int rps = rows_per_stage<TW>(K);
+        const int bgv = group_size<BG>(K);
+        for (int b0 = 0; b0 < n && ok; b0 += bgv) {
+            for (int r = r0; r < r1; r += rps, ++s) {
+                const int rows = min(rps, r1 - r);
+                const unsigned bytes = (unsigned)(rows * K * (int)sizeof(TW));
+                const int slot = (int)(s % NSTAGE);
+                if (!mbar_wait(&sm.empty[slot], ((s / NSTAGE) & 1u) ^ 1u, P.err)) { ok = false; break; }
+                mbar_expect_tx(&sm.full[slot], bytes);
+                bulk_g2s(sm.ring + (size_t)slot * STAGE_BYTES, W + (size_t)r * K, bytes, &sm.full[slot]);
+            }
+        }
+    }
+    if (!ok) {
+        // the consumers stopped early: wait (bounded) until every issued copy has landed
+        for (unsigned k = s > NSTAGE ? s - NSTAGE : 0; k < s; ++k) {
+            uint64_t* b = &sm.full[k % NSTAGE];
+            const unsigned long long t0 = globaltimer_ns();
+            while (!mbar_try(b, (k / NSTAGE) & 1u))
+                if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ GEMV consumers
+
 // Where the input vector of a matrix-vector phase comes from.
 struct XSrc {
     const float* base;    // batch row i at base + i * stride
@@ -269,70 +411,11 @@ struct XSrc {
     float* store;         // CTA 0 stores base + add here (depformer residual), or nullptr
 };
 
-template <typename TW, int VPL, int BGV, int UP>
-__device__ __forceinline__ void gemv_rows(const TW* __restrict__ W, int K, const GemvCfg& c, int kw, int rw,
-                                          int lane, int pair_lo, int pair_hi, const float (&xr)[VPL][BGV][8],
-                                          float* red)
-{
-    using V = WV<TW>;
-    const int NV = K / 8;
-    const int v_begin = kw * c.nvw;
-    const int v_end = min(NV, v_begin + c.nvw);
-    for (int pp0 = pair_lo + rw; pp0 < pair_hi; pp0 += c.nwr * UP) {
-        typename V::raw wv[UP][2][VPL];
-#pragma unroll
-        for (int u = 0; u < UP; ++u) {
-            const int pp = pp0 + u * c.nwr;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const TW* row = W + (size_t)(2 * pp + h) * (size_t)K;
-#pragma unroll
-                for (int t = 0; t < VPL; ++t) {
-                    const int v = v_begin + lane + 32 * t;
-                    wv[u][h][t] = (pp < pair_hi && v < v_end) ? V::load(row + (size_t)v * 8) : V::zero();
-                }
-            }
-        }
-        float acc[UP][2][BGV];
-#pragma unroll
-        for (int u = 0; u < UP; ++u)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int b = 0; b < BGV; ++b) acc[u][h][b] = 0.f;
-#pragma unroll
-        for (int u = 0; u < UP; ++u)
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int t = 0; t < VPL; ++t) {
-                    float f[8];
-                    V::cvt(wv[u][h][t], f);
-#pragma unroll
-                    for (int b = 0; b < BGV; ++b)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[u][h][b] = fmaf(f[e], xr[t][b][e], acc[u][h][b]);
-                }
-#pragma unroll
-        for (int u = 0; u < UP; ++u) {
-            const int pp = pp0 + u * c.nwr;
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int b = 0; b < BGV; ++b) {
-                    const float s = warp_sum(acc[u][h][b]);
-                    if (lane == 0 && pp < pair_hi)
-                        red[((size_t)((pp - pair_lo) * 2 + h) * BGV + b) * 16 + kw] = s;
-                }
-        }
-    }
-}
-
-// Runs one batch group [b0, b0+nb) of a matrix-vector phase and leaves the
-// CTA's row results in sm.yf[row_local][b] (layout stride BGV).
-template <typename TW, int VPL, int BGV, int UP>
-__device__ void gemv_group(const Params& P, const TW* __restrict__ W, int K, const GemvCfg& c, int pair_lo,
-                           int pair_hi, const XSrc& xs, int b0, int nb, const Smem& sm)
+// Consume one batch group [b0, b0+nb) of a matrix-vector phase: leaves the
+// CTA's row values in sm.yf[(r - r0) * bgv + b].  `stage` counts ring stages.
+template <typename TW, int VPL, int BGV>
+__device__ bool gemv_group(const Params& P, int K, const GemvCfg& c, int r0, int r1, const XSrc& xs, int b0,
+                           int nb, const Smem& sm, unsigned& stage)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kw = warp % c.nwk, rw = warp / c.nwk;
@@ -341,92 +424,144 @@ __device__ void gemv_group(const Params& P, const TW* __restrict__ W, int K, con
     for (int b = 0; b < BGV; ++b)
         add_rows[b] = (xs.add && b < nb) ? (const TW*)xs.add + (size_t)sm.prev[b] * (size_t)xs.add_stride : nullptr;
 
-    // RMSNorm factors (every CTA computes the same bits)
-    if (xs.g) {
-#pragma unroll
-        for (int b = 0; b < BGV; ++b) {
-            if (b >= nb) break;
-            const float* xb = xs.base + (size_t)(b0 + b) * xs.stride;
-            float ss = 0.f;
-            for (int k = tid; k < K; k += NT) {
-                float v = ld_cg_f(xb + k);
-                if (add_rows[b]) v += WV<TW>::at(add_rows[b], k);
-                ss = fmaf(v, v, ss);
-            }
-            const float tot = block_sum(ss, sm.sred);
-            if (tid == 0) sm.r[b] = rsqrtf(tot / (float)K + P.eps);
-        }
-        __syncthreads();
-    }
-    // the depformer residual u = in-projection + embedding, written once
-    if (xs.store && blockIdx.x == 0) {
-        for (int b = 0; b < nb; ++b) {
-            const float* xb = xs.base + (size_t)(b0 + b) * xs.stride;
-            float* ub = xs.store + (size_t)(b0 + b) * K;
-            for (int k = tid; k < K; k += NT) {
-                float v = ld_cg_f(xb + k);
-                if (add_rows[b]) v += WV<TW>::at(add_rows[b], k);
-                ub[k] = v;
-            }
-        }
-    }
-    // this warp's K-slice of the input, normalised, in registers
-    float xr[VPL][BGV][8];
+    // this warp's K-slice of the input, in registers; sums of squares per slice
     const int NV = K / 8;
     const int v_begin = kw * c.nvw;
     const int v_end = min(NV, v_begin + c.nvw);
+    float xr[VPL][BGV][8];
+    float ssq[BGV];
+#pragma unroll
+    for (int b = 0; b < BGV; ++b) ssq[b] = 0.f;
 #pragma unroll
     for (int t = 0; t < VPL; ++t) {
         const int v = v_begin + lane + 32 * t;
 #pragma unroll
         for (int b = 0; b < BGV; ++b) {
-            const bool ok = v < v_end && b < nb;
-            float rb = 1.f;
-            if (xs.g && ok) rb = sm.r[b];
+            const bool okv = v < v_end && b < nb;
+            float f[8];
+            if (okv) {
+                const float4* src = reinterpret_cast<const float4*>(xs.base + (size_t)(b0 + b) * xs.stride + v * 8);
+                const float4 a0 = __ldcg(src), a1 = __ldcg(src + 1);
+                f[0] = a0.x; f[1] = a0.y; f[2] = a0.z; f[3] = a0.w; f[4] = a1.x; f[5] = a1.y; f[6] = a1.z; f[7] = a1.w;
+                if (add_rows[b]) {
+                    float e8[8];
+                    WV<TW>::cvt(WV<TW>::load(add_rows[b] + v * 8), e8);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] += e8[e];
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = 0.f;
+            }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                float val = 0.f;
-                if (ok) {
-                    const int k = v * 8 + e;
-                    val = ld_cg_f(xs.base + (size_t)(b0 + b) * xs.stride + k);
-                    if (add_rows[b]) val += WV<TW>::at(add_rows[b], k);
-                    if (xs.g) val = val * rb * xs.g[k];
-                }
-                xr[t][b][e] = val;
+                xr[t][b][e] = f[e];
+                ssq[b] = fmaf(f[e], f[e], ssq[b]);
+            }
+            if (okv && xs.store && blockIdx.x == 0 && rw == 0) {
+                float4* dst = reinterpret_cast<float4*>(xs.store + (size_t)(b0 + b) * K + v * 8);
+                dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+                dst[1] = make_float4(f[4], f[5], f[6], f[7]);
             }
         }
     }
-    gemv_rows<TW, VPL, BGV, UP>(W, K, c, kw, rw, lane, pair_lo, pair_hi, xr, sm.red);
-    __syncthreads();
-    // sum the K-slices in slice order
-    const int rows = (pair_hi - pair_lo) * 2;
-    for (int it = tid; it < rows * nb; it += NT) {
-        const int r = it / nb, b = it % nb;
-        const float* rp = sm.red + ((size_t)r * BGV + b) * 16;
-        float y = 0.f;
-        for (int k = 0; k < c.nwk; ++k) y += rp[k];
-        sm.yf[(size_t)r * BGV + b] = y;
+    if (xs.g) {
+#pragma unroll
+        for (int b = 0; b < BGV; ++b) {
+            const float t = warp_sum(ssq[b]);
+            if (lane == 0 && rw == 0) sm.ssq[b * 16 + kw] = t;
+        }
+        csync();
+#pragma unroll
+        for (int b = 0; b < BGV; ++b) {
+            float tot = 0.f;
+            for (int k = 0; k < c.nwk; ++k) tot += sm.ssq[b * 16 + k];
+            const float rb = rsqrtf(tot / (float)K + P.eps);
+#pragma unroll
+            for (int t = 0; t < VPL; ++t) {
+                const int v = v_begin + lane + 32 * t;
+                if (v < v_end) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xr[t][b][e] = xr[t][b][e] * rb * xs.g[v * 8 + e];
+                }
+            }
+        }
     }
-    __syncthreads();
+
+    // stream the CTA's rows through the ring
+    using Vt = WV<TW>;
+    const int rps = rows_per_stage<TW>(K);
+    for (int ra = r0; ra < r1; ra += rps, ++stage) {
+        const int nr = min(rps, r1 - ra);
+        const int slot = (int)(stage % NSTAGE);
+        if (!mbar_wait(&sm.full[slot], (stage / NSTAGE) & 1u, P.err)) return false;
+        const TW* ring = (const TW*)(sm.ring + (size_t)slot * STAGE_BYTES);
+        float* red = sm.red + (size_t)(stage & 1u) * RPS_MAX * BGV * 16;
+        for (int rr = rw; rr < nr; rr += c.nwr) {
+            float acc[BGV];
+#pragma unroll
+            for (int b = 0; b < BGV; ++b) acc[b] = 0.f;
+#pragma unroll
+            for (int t = 0; t < VPL; ++t) {
+                const int v = v_begin + lane + 32 * t;
+                if (v < v_end) {
+                    float f[8];
+                    const TW* wp = ring + (size_t)rr * K + (size_t)v * 8;
+                    if (sizeof(TW) == 2) {
+                        const uint4 q = *reinterpret_cast<const uint4*>(wp);
+                        typename Vt::raw rq;
+                        memcpy(&rq, &q, sizeof(q));
+                        Vt::cvt(rq, f);
+                    } else {
+                        const uint4 q0 = *reinterpret_cast<const uint4*>(wp);
+                        const uint4 q1 = *reinterpret_cast<const uint4*>((const float*)wp + 4);
+                        f[0] = __uint_as_float(q0.x); f[1] = __uint_as_float(q0.y); f[2] = __uint_as_float(q0.z); f[3] = __uint_as_float(q0.w);
+                        f[4] = __uint_as_float(q1.x); f[5] = __uint_as_float(q1.y); f[6] = __uint_as_float(q1.z); f[7] = __uint_as_float(q1.w);
+                    }
+#pragma unroll
+                    for (int b = 0; b < BGV; ++b)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[b] = fmaf(f[e], xr[t][b][e], acc[b]);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < BGV; ++b) {
+                const float sum = warp_sum(acc[b]);
+                if (lane == 0) red[((size_t)rr * BGV + b) * 16 + kw] = sum;
+            }
+        }
+        csync();
+        if (tid == 0) mbar_arrive(&sm.empty[slot]);
+        // sum the K-slices in slice order
+        for (int it = tid; it < nr * nb; it += NT) {
+            const int rr = it / nb, b = it % nb;
+            const float* rp = red + ((size_t)rr * BGV + b) * 16;
+            float y = 0.f;
+            for (int k = 0; k < c.nwk; ++k) y += rp[k];
+            sm.yf[(size_t)(ra - r0 + rr) * BGV + b] = y;
+        }
+    }
+    csync();
+    return true;
 }
 
 // ------------------------------------------------------------------ epilogues
 
-// Each epilogue sees the CTA's rows [2*pair_lo, 2*pair_hi) for batch rows
-// b0..b0+nb-1, values in sm.yf[(row - 2*pair_lo) * bgv + b].
+// Each epilogue sees the CTA's rows [r0, r1) for batch rows b0..b0+nb-1,
+// values in sm.yf[(row - r0) * bgv + b].
 
 __device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
 
 template <typename TKV>
-__device__ void epi_qkv(const Params& P, int l, int pair_lo, int pair_hi, int b0, int nb, int bgv, const Smem& sm)
+__device__ void epi_qkv(const Params& P, int l, int r0, int r1, int b0, int nb, int bgv, const Smem& sm)
 {
     const StepDesc* D = P.desc;
     const int d = P.d, hd = P.hd;
-    const int npair = pair_hi - pair_lo;
+    const int npair = (r1 - r0) / 2;
     for (int it = threadIdx.x; it < npair * nb; it += NT) {
         const int pl = it / nb, b = it % nb;
         const int i = b0 + b;
-        const int r = 2 * (pair_lo + pl);
+        const int r = r0 + 2 * pl;
         float y0 = sm.yf[(size_t)(2 * pl) * bgv + b], y1 = sm.yf[(size_t)(2 * pl + 1) * bgv + b];
         const int part = r / d, e = r - part * d;
         const int p = D->pos[i];
@@ -447,38 +582,31 @@ __device__ void epi_qkv(const Params& P, int l, int pair_lo, int pair_hi, int b0
     }
 }
 
-__device__ void epi_resid(float* dst, long long stride, int pair_lo, int pair_hi, int b0, int nb, int bgv,
-                          const Smem& sm)
+__device__ void epi_resid(float* dst, long long stride, int r0, int r1, int b0, int nb, int bgv, const Smem& sm)
 {
-    const int npair = pair_hi - pair_lo;
-    for (int it = threadIdx.x; it < npair * nb; it += NT) {
-        const int pl = it / nb, b = it % nb;
-        float* row = dst + (size_t)(b0 + b) * stride + 2 * (pair_lo + pl);
-        row[0] += sm.yf[(size_t)(2 * pl) * bgv + b];
-        row[1] += sm.yf[(size_t)(2 * pl + 1) * bgv + b];
+    for (int it = threadIdx.x; it < (r1 - r0) * nb; it += NT) {
+        const int rl = it / nb, b = it % nb;
+        dst[(size_t)(b0 + b) * stride + r0 + rl] += sm.yf[(size_t)rl * bgv + b];
     }
 }
 
 // rows are (gate m, up m) pairs
-__device__ void epi_swiglu(float* dst, long long stride, int pair_lo, int pair_hi, int b0, int nb, int bgv,
-                           const Smem& sm)
+__device__ void epi_swiglu(float* dst, long long stride, int r0, int r1, int b0, int nb, int bgv, const Smem& sm)
 {
-    const int npair = pair_hi - pair_lo;
+    const int npair = (r1 - r0) / 2;
     for (int it = threadIdx.x; it < npair * nb; it += NT) {
         const int pl = it / nb, b = it % nb;
         const float g = sm.yf[(size_t)(2 * pl) * bgv + b], u = sm.yf[(size_t)(2 * pl + 1) * bgv + b];
-        dst[(size_t)(b0 + b) * stride + pair_lo + pl] = silu(g) * u;
+        dst[(size_t)(b0 + b) * stride + r0 / 2 + pl] = silu(g) * u;
     }
 }
 
 // Rows [0, nlog) are logits (stored, and the CTA's argmax per batch row goes
 // to amax_*[i][cta]); rows >= nlog go to extra[i][row - nlog] (may be null).
 __device__ void epi_logits(const Params& P, float* lg, long long lg_stride, int nlog, float* extra,
-                           long long extra_stride, int pair_lo, int pair_hi, int b0, int nb, int bgv,
-                           const Smem& sm)
+                           long long extra_stride, int r0, int r1, int b0, int nb, int bgv, const Smem& sm)
 {
-    const int npair = pair_hi - pair_lo;
-    const int rows = 2 * npair, r0 = 2 * pair_lo;
+    const int rows = r1 - r0;
     for (int it = threadIdx.x; it < rows * nb; it += NT) {
         const int rl = it / nb, b = it % nb;
         const int r = r0 + rl;
@@ -497,9 +625,9 @@ __device__ void epi_logits(const Params& P, float* lg, long long lg_stride, int 
             if (am_better(y, r, bv, bi)) { bv = y; bi = r; }
         }
         warp_argmax(bv, bi);
-        __syncthreads();
+        csync();
         if (lane == 0) { sm.amv[warp] = bv; sm.ami[warp] = bi; }
-        __syncthreads();
+        csync();
         if (threadIdx.x == 0) {
             float v = sm.amv[0];
             int ix = sm.ami[0];
@@ -527,8 +655,6 @@ __device__ __forceinline__ int argmax_partials_warp(const Params& P, int i)
     return ix == 0x7fffffff ? 0 : ix;
 }
 
-// ------------------------------------------------------------------ GEMV phase driver
-
 // Picks, for depformer substep j, each batch row's input token (the text token
 // for j = 0, else the code chosen for stream j), from the previous head's
 // argmax partials unless the token was supplied.  CTA 0 records it.
@@ -554,34 +680,38 @@ __device__ void dep_select_inputs(const Params& P, int j, int b0, int nb, const 
         const int lim = j == 0 ? P.V : P.C;
         if (lane == 0) sm.prev[warp] = (chosen >= 0 && chosen < lim) ? chosen : 0;  // keeps the embedding read in range
     }
-    __syncthreads();
+    csync();
 }
 
-// One matrix-vector phase: rows [0, N) of W [N][K] times the input vector of
-// each batch row; epi(pair_lo, pair_hi, b0, nb, bgv) consumes the CTA's rows.
+// One matrix-vector phase; epi(r0, r1, b0, nb, bgv) consumes the CTA's rows.
 // dep_j >= 0 selects the depformer layer-0 input tokens first.
 template <typename TW, int BG, class Epi>
-__device__ void gemv_phase(const Params& P, const TW* W, int N, int K, const XSrc& xs, int dep_j, int n,
-                           const Smem& sm, Epi epi)
+__device__ bool gemv_phase(const Params& P, const Phase& ph, const XSrc& xs, int dep_j, int n, const Smem& sm,
+                           unsigned& stage, Epi epi)
 {
-    const int npairs = N / 2;
-    const int pair_lo = (int)((long long)npairs * blockIdx.x / P.G);
-    const int pair_hi = (int)((long long)npairs * (blockIdx.x + 1) / P.G);
+    const TW* W;
+    int N, K;
+    phase_matrix<TW>(P, ph, W, N, K);
+    int r0, r1;
+    cta_rows(N, P.G, r0, r1);
     const GemvCfg c = gemv_cfg(K);
-    const int bgv = c.vpl == 3 ? (BG < 2 ? BG : 2) : BG;
+    const int bgv = group_size<BG>(K);
     for (int b0 = 0; b0 < n; b0 += bgv) {
         const int nb = min(bgv, n - b0);
         if (dep_j >= 0) dep_select_inputs(P, dep_j, b0, nb, sm);
-        if (pair_hi > pair_lo || xs.store) {
+        if (r1 > r0 || xs.store) {
+            bool ok;
             switch (c.vpl) {
-                case 1: gemv_group<TW, 1, BG, 4>(P, W, K, c, pair_lo, pair_hi, xs, b0, nb, sm); break;
-                case 2: gemv_group<TW, 2, BG, 2>(P, W, K, c, pair_lo, pair_hi, xs, b0, nb, sm); break;
-                default: gemv_group<TW, 3, (BG < 2 ? BG : 2), 2>(P, W, K, c, pair_lo, pair_hi, xs, b0, nb, sm); break;
+                case 1: ok = gemv_group<TW, 1, BG>(P, K, c, r0, r1, xs, b0, nb, sm, stage); break;
+                case 2: ok = gemv_group<TW, 2, BG>(P, K, c, r0, r1, xs, b0, nb, sm, stage); break;
+                default: ok = gemv_group<TW, 3, (BG < 2 ? BG : 2)>(P, K, c, r0, r1, xs, b0, nb, sm, stage); break;
             }
+            if (!ok) return false;
         }
-        epi(pair_lo, pair_hi, b0, nb, bgv);
-        __syncthreads();
+        epi(r0, r1, b0, nb, bgv);
+        csync();
     }
+    return true;
 }
 
 // ------------------------------------------------------------------ S0 + S1
@@ -600,7 +730,7 @@ __device__ void phase_embed(const Params& P, int n, const Smem& sm)
         if (tok < 0 || tok > init) tok = init;  // never taken for a consistent history; keeps reads in the table
         sm.X[it] = tok;
     }
-    __syncthreads();
+    csync();
     // frame p's tokens into the history (column p mod 3, disjoint from the reads above)
     if (blockIdx.x == 0) {
         for (int it = threadIdx.x; it < n * NSTREAM; it += NT) {
@@ -628,57 +758,38 @@ __device__ void phase_embed(const Params& P, int n, const Smem& sm)
         dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
         dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
+    csync();
 }
 
 // ------------------------------------------------------------------ S5 attention
 
-// Chunks of the window of a slot of window length len: depends on len only.
-__device__ __forceinline__ int attn_chunks(int len)
-{
-    const int c = (len + 15) / 16;
-    return c < NCHUNK_MAX ? c : NCHUNK_MAX;
-}
-
+// One CTA per (batch row, head); its 16 warps split the window into 16
+// contiguous runs of keys (a split that depends on the window length only),
+// and the partial softmax states are merged in shared memory in warp order.
 template <typename TKV>
 __device__ void phase_attn(const Params& P, int l, int n, const Smem& sm)
 {
     const StepDesc* D = P.desc;
     const int H = P.H, hd = P.hd, d = P.d, W = P.W;
-    if (threadIdx.x == 0) {
-        int pref = 0;
-        for (int i = 0; i < n; ++i) {
-            const int p = D->pos[i];
-            const int len = p + 1 < W ? p + 1 : W;
-            const int nc = attn_chunks(len);
-            sm.att[i * 4 + 0] = len;
-            sm.att[i * 4 + 1] = nc;
-            sm.att[i * 4 + 2] = pref;
-            pref += nc * H;
-        }
-        sm.att[n * 4 + 2] = pref;
-    }
-    __syncthreads();
-    const int total = sm.att[n * 4 + 2];
-    const int lane = threadIdx.x & 31;
-    const int gwarp = blockIdx.x * NWARP + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int LPP = hd / 8;            // lanes per key
     const int PPI = 32 / LPP;          // keys per warp iteration
     const int grp = lane / LPP, gl = lane % LPP;
     const float scale = rsqrtf((float)hd);
-    const int pstride = hd + 4;
-    for (int item = gwarp; item < total; item += P.G * NWARP) {
-        int i = 0;
-        while (i + 1 < n && sm.att[(i + 1) * 4 + 2] <= item) ++i;
-        const int len = sm.att[i * 4 + 0], nc = sm.att[i * 4 + 1];
-        const int rem = item - sm.att[i * 4 + 2];
-        const int h = rem / nc, c = rem % nc;
+    const int wstride = hd + 4;
+    for (int item = blockIdx.x; item < n * H; item += P.G) {
+        const int i = item / H, h = item % H;
         const int p = D->pos[i], slot = D->slot[i];
-        const int CH = (len + nc - 1) / nc;
-        const int j0 = c * CH, j1 = min(len, j0 + CH);
+        const int len = p + 1 < W ? p + 1 : W;
         const int start = p - len + 1;
+        const int j0 = (int)((long long)len * warp / NWARP), j1 = (int)((long long)len * (warp + 1) / NWARP);
         float qv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qv[e] = ld_cg_f(P.q + (size_t)i * d + h * hd + gl * 8 + e) * scale;
+        {
+            const float4* qs = reinterpret_cast<const float4*>(P.q + (size_t)i * d + h * hd + gl * 8);
+            const float4 a0 = __ldcg(qs), a1 = __ldcg(qs + 1);
+            qv[0] = a0.x * scale; qv[1] = a0.y * scale; qv[2] = a0.z * scale; qv[3] = a0.w * scale;
+            qv[4] = a1.x * scale; qv[5] = a1.y * scale; qv[6] = a1.z * scale; qv[7] = a1.w * scale;
+        }
         const long long kvbase = ((long long)slot * P.L + l) * (long long)W * d + h * hd + gl * 8;
         float m = -INFINITY, lsum = 0.f, acc[8];
 #pragma unroll
@@ -740,76 +851,74 @@ __device__ void phase_attn(const Params& P, int l, int n, const Smem& sm)
             for (int e = 0; e < 8; ++e) acc[e] = acc[e] * c1 + a2[e] * c2;
             m = M;
         }
-        float* part = P.apart + (((size_t)i * H + h) * NCHUNK_MAX + c) * pstride;
+        float* wb = sm.wbuf + (size_t)warp * wstride;
         if (lane < LPP) {
-            if (lane == 0) { part[0] = m; part[1] = lsum; }
-            float4* dst = reinterpret_cast<float4*>(part + 4 + gl * 8);
-            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            if (lane == 0) { wb[0] = m; wb[1] = lsum; }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) wb[4 + gl * 8 + e] = acc[e];
         }
-        // the warp that completes (i, h) merges its chunks in chunk order
-        __syncwarp();
-        int old = 0;
-        if (lane == 0) {
-            __threadfence();
-            old = atomicAdd(P.acnt + i * H + h, 1);
-        }
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old == nc - 1) {
-            __threadfence();
-            const float* pb = P.apart + ((size_t)i * H + h) * NCHUNK_MAX * pstride;
-            const float mc = lane < nc ? ld_cg_f(pb + (size_t)lane * pstride) : -INFINITY;
-            const float lc = lane < nc ? ld_cg_f(pb + (size_t)lane * pstride + 1) : 0.f;
-            const float M = warp_max(mc);
-            const float wc = mc == -INFINITY ? 0.f : expf(mc - M);
-            const float invL = 1.f / warp_sum(lc * wc);
-            for (int e = lane; e < hd; e += 32) {
-                float a = 0.f;
-#pragma unroll 4
-                for (int cc = 0; cc < nc; ++cc) {
-                    const float wcc = __shfl_sync(0xffffffffu, wc, cc);
-                    a = fmaf(wcc, ld_cg_f(pb + (size_t)cc * pstride + 4 + e), a);
-                }
-                P.o[(size_t)i * d + h * hd + e] = a * invL;
+        csync();
+        // merge the 16 warps in warp order
+        for (int e = threadIdx.x; e < hd; e += NT) {
+            float M = -INFINITY;
+            for (int w = 0; w < NWARP; ++w) M = fmaxf(M, sm.wbuf[(size_t)w * wstride]);
+            float L = 0.f, a = 0.f;
+            for (int w = 0; w < NWARP; ++w) {
+                const float mw = sm.wbuf[(size_t)w * wstride];
+                if (mw == -INFINITY) continue;
+                const float f = expf(mw - M);
+                L += sm.wbuf[(size_t)w * wstride + 1] * f;
+                a += sm.wbuf[(size_t)w * wstride + 4 + e] * f;
             }
-            if (lane == 0) P.acnt[i * H + h] = 0;
+            P.o[(size_t)i * d + h * hd + e] = a / L;
         }
+        csync();
     }
 }
 
 // ------------------------------------------------------------------ S9 depformer attention
 
+// One warp per (batch row, head): keys of substeps 0..j, no rotation.
 __device__ void phase_dattn(const Params& P, int l, int j, int n)
 {
-    const int dd = P.dd, dH = P.dH, dhd = P.dhd, S = P.S;
+    const int dd = P.dd, dH = P.dH, S = P.S;  // head dim is 64
     const int lane = threadIdx.x & 31;
     const int gwarp = blockIdx.x * NWARP + (threadIdx.x >> 5);
     const int npos = j + 1;
-    const float scale = rsqrtf((float)dhd);
+    const float scale = 0.125f;  // 1 / sqrt(64)
     for (int item = gwarp; item < n * dH; item += P.G * NWARP) {
         const int i = item / dH, h = item % dH;
-        const float* q = P.dq + (size_t)i * dd + h * dhd;
-        const float* kv = P.dkv + ((size_t)i * P.dL + l) * S * 2 * dd;
+        const float* q = P.dq + (size_t)i * dd + h * 64;
+        const float* kv = P.dkv + ((size_t)i * P.dL + l) * S * 2 * dd + h * 64;
+        // lane covers dims 2*lane, 2*lane+1; all key loads first, then one warp sum per key
+        const float2 qq = __ldcg(reinterpret_cast<const float2*>(q) + lane);
+        float2 k2[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+            k2[t] = t < npos ? __ldcg(reinterpret_cast<const float2*>(kv + (size_t)t * 2 * dd) + lane) : make_float2(0.f, 0.f);
         float s = -INFINITY;
-        if (lane < npos) {
-            const float* kr = kv + (size_t)lane * 2 * dd + h * dhd;
-            float t = 0.f;
-            for (int e = 0; e < dhd; ++e) t = fmaf(ld_cg_f(q + e), ld_cg_f(kr + e), t);
-            s = t * scale;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            const float part = warp_sum(fmaf(qq.x, k2[t].x, qq.y * k2[t].y));
+            if (t == lane && t < npos) s = part * scale;
         }
         const float M = warp_max(s);
         const float pe = lane < npos ? expf(s - M) : 0.f;
-        const float Z = warp_sum(pe);
-        const float inv = 1.f / Z;
-        for (int e = lane; e < dhd; e += 32) {
-            float a = 0.f;
-            for (int t = 0; t < npos; ++t) {
-                const float pt = __shfl_sync(0xffffffffu, pe, t);
-                a = fmaf(pt, ld_cg_f(kv + ((size_t)t * 2 + 1) * dd + h * dhd + e), a);
-            }
-            P.dat[(size_t)i * dd + h * dhd + e] = a * inv;
+        const float inv = 1.f / warp_sum(pe);
+        // this lane's two output dims: all value loads first, then the sum in key order
+        float2 v[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t)
+            v[t] = t < npos ? __ldcg(reinterpret_cast<const float2*>(kv + ((size_t)t * 2 + 1) * dd) + lane)
+                            : make_float2(0.f, 0.f);
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            const float pt = __shfl_sync(0xffffffffu, pe, t);
+            a0 = fmaf(pt, v[t].x, a0);
+            a1 = fmaf(pt, v[t].y, a1);
         }
-        // lanes >= 32 of dhd handled by the loop above; all lanes shuffle uniformly
+        reinterpret_cast<float2*>(P.dat + (size_t)i * dd + h * 64)[lane] = make_float2(a0 * inv, a1 * inv);
     }
 }
 
@@ -844,44 +953,34 @@ __device__ void phase_final(const Params& P, int n)
 // ------------------------------------------------------------------ phase dispatch
 
 template <typename TW, typename TKV, int BG>
-__device__ void run_phase(const Params& P, const Phase ph, int n, const Smem& sm)
+__device__ bool run_phase(const Params& P, const Phase ph, int n, const Smem& sm, unsigned& stage)
 {
     const int d = P.d, F = P.F, dd = P.dd, dF = P.dF;
-    const TW* tl = (const TW*)P.tw + (size_t)ph.l * P.t_layer;
-    const TW* dl = (const TW*)P.dw + (size_t)ph.j * P.d_sub + (size_t)ph.l * P.d_layer;
-    XSrc xs{nullptr, 0, nullptr, nullptr, 0, nullptr};
     switch (ph.type) {
-        case PH_EMBED: phase_embed<TW>(P, n, sm); break;
+        case PH_EMBED: phase_embed<TW>(P, n, sm); return true;
         case PH_QKV:
-            xs = XSrc{P.x, d, P.attn_norm + (size_t)ph.l * d, nullptr, 0, nullptr};
-            gemv_phase<TW, BG>(P, tl, 3 * d, d, xs, -1, n, sm, [&](int lo, int hi, int b0, int nb, int bgv) {
-                epi_qkv<TKV>(P, ph.l, lo, hi, b0, nb, bgv, sm);
-            });
-            break;
-        case PH_ATTN: phase_attn<TKV>(P, ph.l, n, sm); break;
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, P.attn_norm + (size_t)ph.l * d, nullptr, 0, nullptr}, -1, n,
+                                      sm, stage, [&](int r0, int r1, int b0, int nb, int bgv) {
+                                          epi_qkv<TKV>(P, ph.l, r0, r1, b0, nb, bgv, sm);
+                                      });
+        case PH_ATTN: phase_attn<TKV>(P, ph.l, n, sm); return true;
         case PH_O:
-            xs = XSrc{P.o, d, nullptr, nullptr, 0, nullptr};
-            gemv_phase<TW, BG>(P, tl + (size_t)3 * d * d, d, d, xs, -1, n, sm,
-                               [&](int lo, int hi, int b0, int nb, int bgv) { epi_resid(P.x, d, lo, hi, b0, nb, bgv, sm); });
-            break;
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.o, d, nullptr, nullptr, 0, nullptr}, -1, n, sm, stage,
+                                      [&](int r0, int r1, int b0, int nb, int bgv) { epi_resid(P.x, d, r0, r1, b0, nb, bgv, sm); });
         case PH_GU:
-            xs = XSrc{P.x, d, P.ffn_norm + (size_t)ph.l * d, nullptr, 0, nullptr};
-            gemv_phase<TW, BG>(P, tl + (size_t)4 * d * d, 2 * F, d, xs, -1, n, sm,
-                               [&](int lo, int hi, int b0, int nb, int bgv) { epi_swiglu(P.s, F, lo, hi, b0, nb, bgv, sm); });
-            break;
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, P.ffn_norm + (size_t)ph.l * d, nullptr, 0, nullptr}, -1, n,
+                                      sm, stage,
+                                      [&](int r0, int r1, int b0, int nb, int bgv) { epi_swiglu(P.s, F, r0, r1, b0, nb, bgv, sm); });
         case PH_DOWN:
-            xs = XSrc{P.s, F, nullptr, nullptr, 0, nullptr};
-            gemv_phase<TW, BG>(P, tl + (size_t)4 * d * d + (size_t)2 * F * d, d, F, xs, -1, n, sm,
-                               [&](int lo, int hi, int b0, int nb, int bgv) { epi_resid(P.x, d, lo, hi, b0, nb, bgv, sm); });
-            break;
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.s, F, nullptr, nullptr, 0, nullptr}, -1, n, sm, stage,
+                                      [&](int r0, int r1, int b0, int nb, int bgv) { epi_resid(P.x, d, r0, r1, b0, nb, bgv, sm); });
         case PH_HEAD:
-            xs = XSrc{P.x, d, P.out_norm, nullptr, 0, nullptr};
-            gemv_phase<TW, BG>(P, (const TW*)P.head, P.V + P.S * dd, d, xs, -1, n, sm,
-                               [&](int lo, int hi, int b0, int nb, int bgv) {
-                                   epi_logits(P, P.logits, P.V, P.V, P.yin, (long long)P.S * dd, lo, hi, b0, nb, bgv, sm);
-                               });
-            break;
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, P.out_norm, nullptr, 0, nullptr}, -1, n, sm, stage,
+                                      [&](int r0, int r1, int b0, int nb, int bgv) {
+                                          epi_logits(P, P.logits, P.V, P.V, P.yin, (long long)P.S * dd, r0, r1, b0, nb, bgv, sm);
+                                      });
         case PH_DQKV: {
+            XSrc xs;
             if (ph.l == 0) {
                 const void* add = ph.j == 0 ? P.dep_emb_text
                                             : (const void*)((const TW*)P.dep_emb_audio + (size_t)(ph.j - 1) * P.C * dd);
@@ -889,49 +988,41 @@ __device__ void run_phase(const Params& P, const Phase ph, int n, const Smem& sm
             } else {
                 xs = XSrc{P.u, dd, P.dep_attn_norm + (size_t)ph.l * dd, nullptr, 0, nullptr};
             }
-            gemv_phase<TW, BG>(P, dl, 3 * dd, dd, xs, ph.l == 0 ? ph.j : -1, n, sm,
-                               [&](int lo, int hi, int b0, int nb, int bgv) {
-                                   const int npair = hi - lo;
-                                   for (int it = threadIdx.x; it < npair * nb; it += NT) {
-                                       const int pl = it / nb, b = it % nb, i = b0 + b;
-                                       const int r = 2 * (lo + pl);
-                                       const int part = r / dd, e = r - part * dd;
-                                       const float y0 = sm.yf[(size_t)(2 * pl) * bgv + b];
-                                       const float y1 = sm.yf[(size_t)(2 * pl + 1) * bgv + b];
-                                       float* dst = part == 0 ? P.dq + (size_t)i * dd + e
-                                                              : P.dkv + ((((size_t)i * P.dL + ph.l) * P.S + ph.j) * 2 + (part - 1)) * dd + e;
-                                       dst[0] = y0;
-                                       dst[1] = y1;
-                                   }
-                               });
-            break;
+            return gemv_phase<TW, BG>(P, ph, xs, ph.l == 0 ? ph.j : -1, n, sm, stage,
+                                      [&](int r0, int r1, int b0, int nb, int bgv) {
+                                          const int npair = (r1 - r0) / 2;
+                                          for (int it = threadIdx.x; it < npair * nb; it += NT) {
+                                              const int pl = it / nb, b = it % nb, i = b0 + b;
+                                              const int r = r0 + 2 * pl;
+                                              const int part = r / dd, e = r - part * dd;
+                                              const float y0 = sm.yf[(size_t)(2 * pl) * bgv + b];
+                                              const float y1 = sm.yf[(size_t)(2 * pl + 1) * bgv + b];
+                                              float* dst = part == 0 ? P.dq + (size_t)i * dd + e
+                                                                     : P.dkv + ((((size_t)i * P.dL + ph.l) * P.S + ph.j) * 2 + (part - 1)) * dd + e;
+                                              dst[0] = y0;
+                                              dst[1] = y1;
+                                          }
+                                      });
         }
-        case PH_DATTN: phase_dattn(P, ph.l, ph.j, n); break;
+        case PH_DATTN: phase_dattn(P, ph.l, ph.j, n); return true;
         case PH_DO:
-            xs = XSrc{P.dat, dd, nullptr, nullptr, 0, nullptr};
-            gemv_phase<TW, BG>(P, dl + (size_t)3 * dd * dd, dd, dd, xs, -1, n, sm,
-                               [&](int lo, int hi, int b0, int nb, int bgv) { epi_resid(P.u, dd, lo, hi, b0, nb, bgv, sm); });
-            break;
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.dat, dd, nullptr, nullptr, 0, nullptr}, -1, n, sm, stage,
+                                      [&](int r0, int r1, int b0, int nb, int bgv) { epi_resid(P.u, dd, r0, r1, b0, nb, bgv, sm); });
         case PH_DGU:
-            xs = XSrc{P.u, dd, P.dep_ffn_norm + (size_t)ph.l * dd, nullptr, 0, nullptr};
-            gemv_phase<TW, BG>(P, dl + (size_t)4 * dd * dd, 2 * dF, dd, xs, -1, n, sm,
-                               [&](int lo, int hi, int b0, int nb, int bgv) { epi_swiglu(P.ds, dF, lo, hi, b0, nb, bgv, sm); });
-            break;
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.u, dd, P.dep_ffn_norm + (size_t)ph.l * dd, nullptr, 0, nullptr}, -1,
+                                      n, sm, stage,
+                                      [&](int r0, int r1, int b0, int nb, int bgv) { epi_swiglu(P.ds, dF, r0, r1, b0, nb, bgv, sm); });
         case PH_DDOWN:
-            xs = XSrc{P.ds, dF, nullptr, nullptr, 0, nullptr};
-            gemv_phase<TW, BG>(P, dl + (size_t)4 * dd * dd + (size_t)2 * dF * dd, dd, dF, xs, -1, n, sm,
-                               [&](int lo, int hi, int b0, int nb, int bgv) { epi_resid(P.u, dd, lo, hi, b0, nb, bgv, sm); });
-            break;
-        case PH_DHEAD: {
-            xs = XSrc{P.u, dd, P.dep_out_norm, nullptr, 0, nullptr};
-            const TW* hw = (const TW*)P.dw + (size_t)ph.j * P.d_sub + (size_t)P.dL * P.d_layer;
-            gemv_phase<TW, BG>(P, hw, P.C, dd, xs, -1, n, sm, [&](int lo, int hi, int b0, int nb, int bgv) {
-                epi_logits(P, P.dlogits + (size_t)ph.j * P.C, (long long)P.S * P.C, P.C, nullptr, 0, lo, hi, b0, nb, bgv, sm);
-            });
-            break;
-        }
-        case PH_FINAL: phase_final(P, n); break;
-        default: break;
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.ds, dF, nullptr, nullptr, 0, nullptr}, -1, n, sm, stage,
+                                      [&](int r0, int r1, int b0, int nb, int bgv) { epi_resid(P.u, dd, r0, r1, b0, nb, bgv, sm); });
+        case PH_DHEAD:
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.u, dd, P.dep_out_norm, nullptr, 0, nullptr}, -1, n, sm, stage,
+                                      [&](int r0, int r1, int b0, int nb, int bgv) {
+                                          epi_logits(P, P.dlogits + (size_t)ph.j * P.C, (long long)P.S * P.C, P.C, nullptr, 0,
+                                                     r0, r1, b0, nb, bgv, sm);
+                                      });
+        case PH_FINAL: phase_final(P, n); return true;
+        default: return true;
     }
 }
 
@@ -940,36 +1031,49 @@ __device__ void run_phase(const Params& P, const Phase ph, int n, const Smem& sm
 // Phases [ph0, ph1) of one step.  coop != 0: cooperative launch, grid barrier
 // between phases.  maxrows sizes the dynamic shared memory (host computes it).
 template <typename TW, typename TKV, int BG>
-__global__ void __launch_bounds__(NT, 1) step_kernel(Params P, int ph0, int ph1, int coop, int maxrows)
+__global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int ph1, int coop, int maxrows)
 {
-    extern __shared__ __align__(16) float smem_raw[];
+    extern __shared__ __align__(1024) char smem_raw[];
     const Smem sm = smem_map(smem_raw, maxrows, BG);
-    if (*(volatile int*)P.err != 0) return;
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < NSTAGE; ++k) {
+            mbar_init(&sm.full[k], 1);
+            mbar_init(&sm.empty[k], 1);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
     const StepDesc* D = P.desc;
     const int n = D->n;
-    if (ph0 == 0) {
+    int bad = *(volatile int*)P.err != 0;
+    if (ph0 == 0 && !bad) {
         // token ranges (device-resident inputs are only checked here)
-        int bad = 0;
-        for (int it = threadIdx.x; it < n * NSTREAM; it += NT) {
+        int tb = 0;
+        for (int it = threadIdx.x; it < n * NSTREAM; it += blockDim.x) {
             const int k = it % NSTREAM;
             const int t = D->codes[it / NSTREAM][k];
-            if (t < -1 || t >= (k == 0 ? P.V : P.C)) bad = 1;
+            if (t < -1 || t >= (k == 0 ? P.V : P.C)) tb = 1;
         }
-        if (__syncthreads_or(bad)) {
+        if (__syncthreads_or(tb)) {
             if (blockIdx.x == 0 && threadIdx.x == 0) {
                 if (atomicCAS(P.err, 0, (int)DERR_TOKEN) == 0) *P.err_seq = D->seq;
             }
-            return;
+            bad = 1;
         }
     }
-    unsigned target = 0;
+    __syncthreads();  // barrier init visible to every thread; all threads agree on `bad`
+    if (bad) return;
+    if ((threadIdx.x >> 5) == NWARP) {
+        if ((threadIdx.x & 31) == 0) producer<TW, BG>(P, ph0, ph1, n, sm);
+        return;
+    }
+    unsigned target = 0, stage = 0;
     for (int ph = ph0; ph < ph1; ++ph) {
         if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) P.ptime[ph] = globaltimer_ns();
         const Phase phs = P.phases[ph];
-        run_phase<TW, TKV, BG>(P, phs, n, sm);
+        if (!run_phase<TW, TKV, BG>(P, phs, n, sm, stage)) return;
         if (coop && ph + 1 < ph1) {
             target += (unsigned)P.G;
-            if (!grid_barrier(P.bar, target, P.err)) return;
+            if (!grid_barrier(P.bar, target, P.err, sm.ok)) return;
         }
     }
     if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) P.ptime[ph1] = globaltimer_ns();
