@@ -421,12 +421,12 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
         c->kfn[i] = g.weight_dtype == MFS_DTYPE_BF16 ? kernel_bf16(bg) : kernel_f32(bg);
         // ring, then one region used as GEMV partials + row values, attention
         // partials, or the step's embedding rows, whichever phase runs
-        const size_t gemv = ((size_t)2 * RPS_MAX * bg * 16 + (size_t)c->maxrows * bg) * sizeof(float);
+        const size_t gemv = (size_t)c->maxrows * bg * 17 * sizeof(float);
         const size_t attn = (size_t)NWARP * (g.head_dim + 4) * sizeof(float);
         const size_t emb = (size_t)MFS_MAX_SLOTS * NSTREAM * sizeof(int);
         size_t region = gemv > attn ? gemv : attn;
         region = region > emb ? region : emb;
-        c->smem[i] = SMEM_HEAD + (size_t)NSTAGE * STAGE_BYTES + region;
+        c->smem[i] = SMEM_HEAD + (size_t)nstage_for(bg) * STAGE_BYTES + region;
         if (c->smem[i] > 227 * 1024) return fail(c, MFS_E_ARG, "shape needs %zu B of shared memory", c->smem[i]);
         CK(cudaFuncSetAttribute(c->kfn[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c->smem[i]));
         int per_sm = 0;

@@ -265,16 +265,16 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
 // ------------------------------------------------------------------ shared memory map
 
 struct Smem {
-    uint64_t* full;   // [NSTAGE] stage filled
-    uint64_t* empty;  // [NSTAGE] stage released
+    uint64_t* full;   // [nstage] stage filled
+    uint64_t* empty;  // [nstage] stage released
     float* r;         // [4] RMSNorm factors of the batch group
     int* prev;        // [4] depformer input token per batch row
     float* ssq;       // [4][16] per-K-slice sums of squares
     float* amv;       // [NWARP]
     int* ami;         // [NWARP]
     int* ok;          // grid-barrier verdict
-    char* ring;       // [NSTAGE][STAGE_BYTES]
-    float* red;       // [2][RPS_MAX][BG][16] per-K-slice partial sums of a stage
+    char* ring;       // [nstage][STAGE_BYTES]
+    float* red;       // [maxrows][BG][16] per-K-slice partial sums of the CTA's rows
     float* yf;        // [maxrows][BG] final row values of the CTA
     int* X;           // embedding rows of this step (aliases red)
     float* wbuf;      // attention partials of the 16 warps (aliases red)
@@ -284,7 +284,7 @@ __device__ __forceinline__ Smem smem_map(char* base, int maxrows, int BG)
 {
     Smem s;
     s.full = (uint64_t*)base;
-    s.empty = s.full + NSTAGE;
+    s.empty = s.full + 8;
     s.r = (float*)(base + 256);
     s.prev = (int*)(base + 272);
     s.ssq = (float*)(base + 288);
@@ -292,8 +292,8 @@ __device__ __forceinline__ Smem smem_map(char* base, int maxrows, int BG)
     s.ami = (int*)(base + 608);
     s.ok = (int*)(base + 672);
     s.ring = base + SMEM_HEAD;
-    s.red = (float*)(s.ring + (size_t)NSTAGE * STAGE_BYTES);
-    s.yf = s.red + 2 * RPS_MAX * BG * 16;
+    s.red = (float*)(s.ring + (size_t)nstage_for(BG) * STAGE_BYTES);
+    s.yf = s.red + (size_t)maxrows * BG * 16;
     s.X = (int*)s.red;
     s.wbuf = s.red;
     return s;
@@ -367,6 +367,7 @@ __device__ __forceinline__ int rows_per_stage(int K)
 template <typename TW, int BG>
 __device__ void producer(const Params& P, int ph0, int ph1, int n, const Smem& sm)
 {
+    constexpr unsigned NS = nstage_for(BG);
     unsigned s = 0;
     bool ok = true;
     for (int ph = ph0; ph < ph1 && ok; ++ph) {
@@ -381,8 +382,8 @@ __device__ void producer(const Params& P, int ph0, int ph1, int n, const Smem& s
             for (int r = r0; r < r1; r += rps, ++s) {
                 const int rows = min(rps, r1 - r);
                 const unsigned bytes = (unsigned)(rows * K * (int)sizeof(TW));
-                const int slot = (int)(s % NSTAGE);
-                if (!mbar_wait(&sm.empty[slot], ((s / NSTAGE) & 1u) ^ 1u, P.err)) { ok = false; break; }
+                const int slot = (int)(s % NS);
+                if (!mbar_wait(&sm.empty[slot], ((s / NS) & 1u) ^ 1u, P.err)) { ok = false; break; }
                 mbar_expect_tx(&sm.full[slot], bytes);
                 bulk_g2s(sm.ring + (size_t)slot * STAGE_BYTES, W + (size_t)r * K, bytes, &sm.full[slot]);
             }
@@ -390,10 +391,10 @@ __device__ void producer(const Params& P, int ph0, int ph1, int n, const Smem& s
     }
     if (!ok) {
         // the consumers stopped early: wait (bounded) until every issued copy has landed
-        for (unsigned k = s > NSTAGE ? s - NSTAGE : 0; k < s; ++k) {
-            uint64_t* b = &sm.full[k % NSTAGE];
+        for (unsigned k = s > NS ? s - NS : 0; k < s; ++k) {
+            uint64_t* b = &sm.full[k % NS];
             const unsigned long long t0 = globaltimer_ns();
-            while (!mbar_try(b, (k / NSTAGE) & 1u))
+            while (!mbar_try(b, (k / NS) & 1u))
                 if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
         }
     }
@@ -413,7 +414,7 @@ struct XSrc {
 
 // Consume one batch group [b0, b0+nb) of a matrix-vector phase: leaves the
 // CTA's row values in sm.yf[(r - r0) * bgv + b].  `stage` counts ring stages.
-template <typename TW, int VPL, int BGV>
+template <typename TW, int VPL, int BGV, int BG_OF_STAGES>
 __device__ bool gemv_group(const Params& P, int K, const GemvCfg& c, int r0, int r1, const XSrc& xs, int b0,
                            int nb, const Smem& sm, unsigned& stage)
 {
@@ -488,58 +489,82 @@ __device__ bool gemv_group(const Params& P, int K, const GemvCfg& c, int r0, int
         }
     }
 
-    // stream the CTA's rows through the ring
+    // stream the CTA's rows through the ring: each warp takes rows rw, rw+nwr, ...
+    // of a stage, four at a time, and releases the stage on its own
     using Vt = WV<TW>;
+    constexpr unsigned NS = nstage_for(BG_OF_STAGES);
     const int rps = rows_per_stage<TW>(K);
     for (int ra = r0; ra < r1; ra += rps, ++stage) {
         const int nr = min(rps, r1 - ra);
-        const int slot = (int)(stage % NSTAGE);
-        if (!mbar_wait(&sm.full[slot], (stage / NSTAGE) & 1u, P.err)) return false;
+        const int slot = (int)(stage % NS);
+        if (!mbar_wait(&sm.full[slot], (stage / NS) & 1u, P.err)) return false;
         const TW* ring = (const TW*)(sm.ring + (size_t)slot * STAGE_BYTES);
-        float* red = sm.red + (size_t)(stage & 1u) * RPS_MAX * BGV * 16;
-        for (int rr = rw; rr < nr; rr += c.nwr) {
-            float acc[BGV];
+        for (int c0 = rw; c0 < nr; c0 += 4 * c.nwr) {
+            float acc[4][BGV];
 #pragma unroll
-            for (int b = 0; b < BGV; ++b) acc[b] = 0.f;
+            for (int q = 0; q < 4; ++q)
 #pragma unroll
-            for (int t = 0; t < VPL; ++t) {
-                const int v = v_begin + lane + 32 * t;
-                if (v < v_end) {
-                    float f[8];
-                    const TW* wp = ring + (size_t)rr * K + (size_t)v * 8;
-                    if (sizeof(TW) == 2) {
-                        const uint4 q = *reinterpret_cast<const uint4*>(wp);
-                        typename Vt::raw rq;
-                        memcpy(&rq, &q, sizeof(q));
-                        Vt::cvt(rq, f);
-                    } else {
-                        const uint4 q0 = *reinterpret_cast<const uint4*>(wp);
-                        const uint4 q1 = *reinterpret_cast<const uint4*>((const float*)wp + 4);
-                        f[0] = __uint_as_float(q0.x); f[1] = __uint_as_float(q0.y); f[2] = __uint_as_float(q0.z); f[3] = __uint_as_float(q0.w);
-                        f[4] = __uint_as_float(q1.x); f[5] = __uint_as_float(q1.y); f[6] = __uint_as_float(q1.z); f[7] = __uint_as_float(q1.w);
+                for (int b = 0; b < BGV; ++b) acc[q][b] = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int rr = c0 + q * c.nwr;
+                if (rr < nr) {
+#pragma unroll
+                    for (int t = 0; t < VPL; ++t) {
+                        const int v = v_begin + lane + 32 * t;
+                        if (v < v_end) {
+                            float f[8];
+                            const TW* wp = ring + (size_t)rr * K + (size_t)v * 8;
+                            if (sizeof(TW) == 2) {
+                                const uint4 w4 = *reinterpret_cast<const uint4*>(wp);
+                                f[0] = bf_lo(w4.x); f[1] = bf_hi(w4.x); f[2] = bf_lo(w4.y); f[3] = bf_hi(w4.y);
+                                f[4] = bf_lo(w4.z); f[5] = bf_hi(w4.z); f[6] = bf_lo(w4.w); f[7] = bf_hi(w4.w);
+                            } else {
+                                const uint4 q0 = *reinterpret_cast<const uint4*>(wp);
+                                const uint4 q1 = *reinterpret_cast<const uint4*>((const float*)wp + 4);
+                                f[0] = __uint_as_float(q0.x); f[1] = __uint_as_float(q0.y); f[2] = __uint_as_float(q0.z); f[3] = __uint_as_float(q0.w);
+                                f[4] = __uint_as_float(q1.x); f[5] = __uint_as_float(q1.y); f[6] = __uint_as_float(q1.z); f[7] = __uint_as_float(q1.w);
+                            }
+#pragma unroll
+                            for (int b = 0; b < BGV; ++b)
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) acc[q][b] = fmaf(f[e], xr[t][b][e], acc[q][b]);
+                        }
                     }
-#pragma unroll
-                    for (int b = 0; b < BGV; ++b)
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[b] = fmaf(f[e], xr[t][b][e], acc[b]);
                 }
             }
+            // transposed butterfly: lanes 0, 8, 16, 24 end with the sums of rows 0..3
+            const int myq = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
+            const int rr = c0 + myq * c.nwr;
 #pragma unroll
             for (int b = 0; b < BGV; ++b) {
-                const float sum = warp_sum(acc[b]);
-                if (lane == 0) red[((size_t)rr * BGV + b) * 16 + kw] = sum;
+                const bool hi16 = (lane & 16) != 0;
+                float s0 = hi16 ? acc[2][b] : acc[0][b], s1 = hi16 ? acc[3][b] : acc[1][b];
+                const float o0 = hi16 ? acc[0][b] : acc[2][b], o1 = hi16 ? acc[1][b] : acc[3][b];
+                s0 += __shfl_xor_sync(0xffffffffu, o0, 16);
+                s1 += __shfl_xor_sync(0xffffffffu, o1, 16);
+                const bool hi8 = (lane & 8) != 0;
+                float t = hi8 ? s1 : s0;
+                const float u = hi8 ? s0 : s1;
+                t += __shfl_xor_sync(0xffffffffu, u, 8);
+                t += __shfl_xor_sync(0xffffffffu, t, 4);
+                t += __shfl_xor_sync(0xffffffffu, t, 2);
+                t += __shfl_xor_sync(0xffffffffu, t, 1);
+                if ((lane & 7) == 0 && rr < nr)
+                    sm.red[((size_t)(ra - r0 + rr) * BGV + b) * 16 + kw] = t;
             }
         }
-        csync();
-        if (tid == 0) mbar_arrive(&sm.empty[slot]);
-        // sum the K-slices in slice order
-        for (int it = tid; it < nr * nb; it += NT) {
-            const int rr = it / nb, b = it % nb;
-            const float* rp = red + ((size_t)rr * BGV + b) * 16;
-            float y = 0.f;
-            for (int k = 0; k < c.nwk; ++k) y += rp[k];
-            sm.yf[(size_t)(ra - r0 + rr) * BGV + b] = y;
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[slot]);
+    }
+    csync();
+    // sum the K-slices in slice order
+    for (int it = tid; it < (r1 - r0) * nb; it += NT) {
+        const int rl = it / nb, b = it % nb;
+        const float* rp = sm.red + ((size_t)rl * BGV + b) * 16;
+        float y = 0.f;
+        for (int k = 0; k < c.nwk; ++k) y += rp[k];
+        sm.yf[(size_t)rl * BGV + b] = y;
     }
     csync();
     return true;
@@ -702,9 +727,9 @@ __device__ bool gemv_phase(const Params& P, const Phase& ph, const XSrc& xs, int
         if (r1 > r0 || xs.store) {
             bool ok;
             switch (c.vpl) {
-                case 1: ok = gemv_group<TW, 1, BG>(P, K, c, r0, r1, xs, b0, nb, sm, stage); break;
-                case 2: ok = gemv_group<TW, 2, BG>(P, K, c, r0, r1, xs, b0, nb, sm, stage); break;
-                default: ok = gemv_group<TW, 3, (BG < 2 ? BG : 2)>(P, K, c, r0, r1, xs, b0, nb, sm, stage); break;
+                case 1: ok = gemv_group<TW, 1, BG, BG>(P, K, c, r0, r1, xs, b0, nb, sm, stage); break;
+                case 2: ok = gemv_group<TW, 2, BG, BG>(P, K, c, r0, r1, xs, b0, nb, sm, stage); break;
+                default: ok = gemv_group<TW, 3, (BG < 2 ? BG : 2), BG>(P, K, c, r0, r1, xs, b0, nb, sm, stage); break;
             }
             if (!ok) return false;
         }
@@ -1036,9 +1061,9 @@ __global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int
     extern __shared__ __align__(1024) char smem_raw[];
     const Smem sm = smem_map(smem_raw, maxrows, BG);
     if (threadIdx.x == 0) {
-        for (int k = 0; k < NSTAGE; ++k) {
+        for (int k = 0; k < (int)nstage_for(BG); ++k) {
             mbar_init(&sm.full[k], 1);
-            mbar_init(&sm.empty[k], 1);
+            mbar_init(&sm.empty[k], NWARP);  // every consumer warp releases every stage
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
