@@ -262,6 +262,16 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
+// Diagnostic timer stamps of CTA 0: slot k of phase ph (0 start, 1 inputs
+// ready, 2 last weight stage consumed, 3 before the grid barrier).
+__device__ __forceinline__ void stamp(const Params& P, int ph, int k)
+{
+    if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) P.ptime[(size_t)ph * 4 + k] = globaltimer_ns();
+}
+
+// phase index for stamps taken inside a phase (thread 0 writes and reads it)
+
+
 // ------------------------------------------------------------------ shared memory map
 
 struct Smem {
@@ -272,7 +282,7 @@ struct Smem {
     float* ssq;       // [4][16] per-K-slice sums of squares
     float* amv;       // [NWARP]
     int* ami;         // [NWARP]
-    int* ok;          // grid-barrier verdict
+    int* ok;          // [0] grid-barrier verdict, [1] phase index (stamps)
     char* ring;       // [nstage][STAGE_BYTES]
     float* red;       // [maxrows][BG][16] per-K-slice partial sums of the CTA's rows
     float* yf;        // [maxrows][BG] final row values of the CTA
@@ -414,63 +424,110 @@ struct XSrc {
 
 // Consume one batch group [b0, b0+nb) of a matrix-vector phase: leaves the
 // CTA's row values in sm.yf[(r - r0) * bgv + b].  `stage` counts ring stages.
+__device__ __forceinline__ void dep_select_inputs(const Params& P, int j, int b0, int nb, const Smem& sm);
+
 template <typename TW, int VPL, int BGV, int BG_OF_STAGES>
-__device__ bool gemv_group(const Params& P, int K, const GemvCfg& c, int r0, int r1, const XSrc& xs, int b0,
-                           int nb, const Smem& sm, unsigned& stage)
+__device__ __forceinline__ bool gemv_group(const Params& P, int K, const GemvCfg& c, int r0, int r1, const XSrc& xs, int b0,
+                           int nb, int dep_j, const Smem& sm, unsigned& stage)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kw = warp % c.nwk, rw = warp / c.nwk;
-    const TW* add_rows[BGV];
-#pragma unroll
-    for (int b = 0; b < BGV; ++b)
-        add_rows[b] = (xs.add && b < nb) ? (const TW*)xs.add + (size_t)sm.prev[b] * (size_t)xs.add_stride : nullptr;
-
-    // this warp's K-slice of the input, in registers; sums of squares per slice
     const int NV = K / 8;
     const int v_begin = kw * c.nvw;
     const int v_end = min(NV, v_begin + c.nvw);
+    // this warp's K-slice of the input in registers, already multiplied by the
+    // norm gain (loaded in the same round trip); sums of squares of the raw input
     float xr[VPL][BGV][8];
     float ssq[BGV];
 #pragma unroll
     for (int b = 0; b < BGV; ++b) ssq[b] = 0.f;
+    const bool gain_now = xs.g && !xs.add;
 #pragma unroll
     for (int t = 0; t < VPL; ++t) {
         const int v = v_begin + lane + 32 * t;
+        float4 g0 = make_float4(1.f, 1.f, 1.f, 1.f), g1 = g0;
+        if (gain_now && v < v_end) {
+            const float4* gs = reinterpret_cast<const float4*>(xs.g + v * 8);
+            g0 = __ldg(gs);
+            g1 = __ldg(gs + 1);
+        }
 #pragma unroll
         for (int b = 0; b < BGV; ++b) {
-            const bool okv = v < v_end && b < nb;
-            float f[8];
-            if (okv) {
+            if (v < v_end && b < nb) {
                 const float4* src = reinterpret_cast<const float4*>(xs.base + (size_t)(b0 + b) * xs.stride + v * 8);
                 const float4 a0 = __ldcg(src), a1 = __ldcg(src + 1);
-                f[0] = a0.x; f[1] = a0.y; f[2] = a0.z; f[3] = a0.w; f[4] = a1.x; f[5] = a1.y; f[6] = a1.z; f[7] = a1.w;
-                if (add_rows[b]) {
-                    float e8[8];
-                    WV<TW>::cvt(WV<TW>::load(add_rows[b] + v * 8), e8);
+                const float f[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] += e8[e];
+                for (int e = 0; e < 8; ++e) {
+                    ssq[b] = fmaf(f[e], f[e], ssq[b]);
+                    xr[t][b][e] = f[e] * gg[e];
                 }
             } else {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = 0.f;
+                for (int e = 0; e < 8; ++e) xr[t][b][e] = 0.f;
             }
+        }
+    }
+    // depformer layer 0: the input adds the embedding of the token chosen by the
+    // previous head (its selection overlaps the loads above); then the gain
+    if (xs.add) {
+        dep_select_inputs(P, dep_j, b0, nb, sm);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                xr[t][b][e] = f[e];
-                ssq[b] = fmaf(f[e], f[e], ssq[b]);
+        for (int b = 0; b < BGV; ++b) ssq[b] = 0.f;
+#pragma unroll
+        for (int b = 0; b < BGV; ++b) {
+            if (b >= nb) break;
+            const TW* row = (const TW*)xs.add + (size_t)sm.prev[b] * (size_t)xs.add_stride;
+#pragma unroll
+            for (int t = 0; t < VPL; ++t) {
+                const int v = v_begin + lane + 32 * t;
+                if (v < v_end) {
+                    float e8[8];
+                    WV<TW>::cvt(WV<TW>::load(row + v * 8), e8);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        xr[t][b][e] += e8[e];
+                        ssq[b] = fmaf(xr[t][b][e], xr[t][b][e], ssq[b]);
+                    }
+                }
             }
-            if (okv && xs.store && blockIdx.x == 0 && rw == 0) {
-                float4* dst = reinterpret_cast<float4*>(xs.store + (size_t)(b0 + b) * K + v * 8);
-                dst[0] = make_float4(f[0], f[1], f[2], f[3]);
-                dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+        }
+        if (xs.store && blockIdx.x == 0 && rw == 0) {
+#pragma unroll
+            for (int t = 0; t < VPL; ++t) {
+                const int v = v_begin + lane + 32 * t;
+#pragma unroll
+                for (int b = 0; b < BGV; ++b) {
+                    if (v < v_end && b < nb) {
+                        float4* dst = reinterpret_cast<float4*>(xs.store + (size_t)(b0 + b) * K + v * 8);
+                        dst[0] = make_float4(xr[t][b][0], xr[t][b][1], xr[t][b][2], xr[t][b][3]);
+                        dst[1] = make_float4(xr[t][b][4], xr[t][b][5], xr[t][b][6], xr[t][b][7]);
+                    }
+                }
+            }
+        }
+        if (xs.g) {
+#pragma unroll
+            for (int t = 0; t < VPL; ++t) {
+                const int v = v_begin + lane + 32 * t;
+                if (v < v_end) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float ge = __ldg(xs.g + v * 8 + e);
+#pragma unroll
+                        for (int b = 0; b < BGV; ++b) xr[t][b][e] *= ge;
+                    }
+                }
             }
         }
     }
     if (xs.g) {
+        // RMSNorm factor: sums of squares per K-slice, combined in slice order
 #pragma unroll
         for (int b = 0; b < BGV; ++b) {
-            const float t = warp_sum(ssq[b]);
-            if (lane == 0 && rw == 0) sm.ssq[b * 16 + kw] = t;
+            const float q = warp_sum(ssq[b]);
+            if (lane == 0 && rw == 0) sm.ssq[b * 16 + kw] = q;
         }
         csync();
 #pragma unroll
@@ -479,16 +536,12 @@ __device__ bool gemv_group(const Params& P, int K, const GemvCfg& c, int r0, int
             for (int k = 0; k < c.nwk; ++k) tot += sm.ssq[b * 16 + k];
             const float rb = rsqrtf(tot / (float)K + P.eps);
 #pragma unroll
-            for (int t = 0; t < VPL; ++t) {
-                const int v = v_begin + lane + 32 * t;
-                if (v < v_end) {
+            for (int t = 0; t < VPL; ++t)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) xr[t][b][e] = xr[t][b][e] * rb * xs.g[v * 8 + e];
-                }
-            }
+                for (int e = 0; e < 8; ++e) xr[t][b][e] *= rb;
         }
     }
-
+    if (P.ptime) stamp(P, *(volatile int*)(sm.ok + 1), 1);
     // stream the CTA's rows through the ring: each warp takes rows rw, rw+nwr, ...
     // of a stage, four at a time, and releases the stage on its own
     using Vt = WV<TW>;
@@ -557,6 +610,7 @@ __device__ bool gemv_group(const Params& P, int K, const GemvCfg& c, int r0, int
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
+    if (P.ptime) stamp(P, *(volatile int*)(sm.ok + 1), 2);
     csync();
     // sum the K-slices in slice order
     for (int it = tid; it < (r1 - r0) * nb; it += NT) {
@@ -572,97 +626,174 @@ __device__ bool gemv_group(const Params& P, int K, const GemvCfg& c, int r0, int
 
 // ------------------------------------------------------------------ epilogues
 
-// Each epilogue sees the CTA's rows [r0, r1) for batch rows b0..b0+nb-1,
-// values in sm.yf[(row - r0) * bgv + b].
+// An epilogue sees the CTA's rows [r0, r1) for batch rows b0..b0+nb-1, values
+// in sm.yf[(row - r0) * bgv + b].  pre() runs before the weight stages and
+// loads what apply() needs from memory (up to two items per thread), so the
+// epilogue itself does not wait on a round trip.
+struct Pre {
+    float a[2], b[2];
+};
 
 __device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
 
 template <typename TKV>
-__device__ void epi_qkv(const Params& P, int l, int r0, int r1, int b0, int nb, int bgv, const Smem& sm)
-{
-    const StepDesc* D = P.desc;
-    const int d = P.d, hd = P.hd;
-    const int npair = (r1 - r0) / 2;
-    for (int it = threadIdx.x; it < npair * nb; it += NT) {
-        const int pl = it / nb, b = it % nb;
-        const int i = b0 + b;
-        const int r = r0 + 2 * pl;
-        float y0 = sm.yf[(size_t)(2 * pl) * bgv + b], y1 = sm.yf[(size_t)(2 * pl + 1) * bgv + b];
-        const int part = r / d, e = r - part * d;
-        const int p = D->pos[i];
-        if (part < 2) {
-            const float2 cs = P.rope[(size_t)p * (hd / 2) + (e % hd) / 2];
-            const float a = y0, c = y1;
-            y0 = a * cs.x - c * cs.y;
-            y1 = a * cs.y + c * cs.x;
+struct EpiQKV {
+    int l;
+    __device__ Pre pre(const Params& P, int r0, int r1, int b0, int nb) const
+    {
+        Pre q{{0.f, 0.f}, {0.f, 0.f}};
+        const int npair = (r1 - r0) / 2;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int it = threadIdx.x + k * NT;
+            if (it < npair * nb) {
+                const int pl = it / nb, b = it % nb;
+                const int r = r0 + 2 * pl, part = r / P.d, e = r - part * P.d;
+                if (part < 2) {
+                    const float2 cs = __ldg(P.rope + (size_t)P.desc->pos[b0 + b] * (P.hd / 2) + (e % P.hd) / 2);
+                    q.a[k] = cs.x;
+                    q.b[k] = cs.y;
+                }
+            }
         }
-        if (part == 0) {
-            P.q[(size_t)i * d + e] = y0;
-            P.q[(size_t)i * d + e + 1] = y1;
-        } else {
-            const int slot = D->slot[i];
-            const long long idx = (((long long)slot * P.L + l) * P.W + (p % P.W)) * (long long)d + e;
-            KV<TKV>::store2(part == 1 ? P.kc : P.vc, idx, y0, y1);
+        return q;
+    }
+    __device__ void apply(const Params& P, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre& q) const
+    {
+        const StepDesc* D = P.desc;
+        const int d = P.d, hd = P.hd;
+        const int npair = (r1 - r0) / 2;
+        for (int it = threadIdx.x; it < npair * nb; it += NT) {
+            const int pl = it / nb, b = it % nb;
+            const int i = b0 + b;
+            const int r = r0 + 2 * pl;
+            float y0 = sm.yf[(size_t)(2 * pl) * bgv + b], y1 = sm.yf[(size_t)(2 * pl + 1) * bgv + b];
+            const int part = r / d, e = r - part * d;
+            const int p = D->pos[i];
+            if (part < 2) {
+                const int k = it / NT;
+                const float2 cs = k < 2 ? make_float2(q.a[k], q.b[k]) : __ldg(P.rope + (size_t)p * (hd / 2) + (e % hd) / 2);
+                const float a = y0, c = y1;
+                y0 = a * cs.x - c * cs.y;
+                y1 = a * cs.y + c * cs.x;
+            }
+            if (part == 0) {
+                *reinterpret_cast<float2*>(P.q + (size_t)i * d + e) = make_float2(y0, y1);
+            } else {
+                const int slot = D->slot[i];
+                const long long idx = (((long long)slot * P.L + l) * P.W + (p % P.W)) * (long long)d + e;
+                KV<TKV>::store2(part == 1 ? P.kc : P.vc, idx, y0, y1);
+            }
         }
     }
-}
+};
 
-__device__ void epi_resid(float* dst, long long stride, int r0, int r1, int b0, int nb, int bgv, const Smem& sm)
-{
-    for (int it = threadIdx.x; it < (r1 - r0) * nb; it += NT) {
-        const int rl = it / nb, b = it % nb;
-        dst[(size_t)(b0 + b) * stride + r0 + rl] += sm.yf[(size_t)rl * bgv + b];
+// dst[row] = residual + row value; the residual is read in pre()
+struct EpiResid {
+    float* dst;
+    long long stride;
+    __device__ Pre pre(const Params&, int r0, int r1, int b0, int nb) const
+    {
+        Pre q{{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int it = threadIdx.x + k * NT;
+            if (it < (r1 - r0) * nb) q.a[k] = __ldcg(dst + (size_t)(b0 + it % nb) * stride + r0 + it / nb);
+        }
+        return q;
     }
-}
+    __device__ void apply(const Params&, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre& q) const
+    {
+        for (int it = threadIdx.x; it < (r1 - r0) * nb; it += NT) {
+            const int rl = it / nb, b = it % nb;
+            float* p = dst + (size_t)(b0 + b) * stride + r0 + rl;
+            const int k = it / NT;
+            *p = (k < 2 ? q.a[k] : __ldcg(p)) + sm.yf[(size_t)rl * bgv + b];
+        }
+    }
+};
 
 // rows are (gate m, up m) pairs
-__device__ void epi_swiglu(float* dst, long long stride, int r0, int r1, int b0, int nb, int bgv, const Smem& sm)
-{
-    const int npair = (r1 - r0) / 2;
-    for (int it = threadIdx.x; it < npair * nb; it += NT) {
-        const int pl = it / nb, b = it % nb;
-        const float g = sm.yf[(size_t)(2 * pl) * bgv + b], u = sm.yf[(size_t)(2 * pl + 1) * bgv + b];
-        dst[(size_t)(b0 + b) * stride + r0 / 2 + pl] = silu(g) * u;
+struct EpiSwiglu {
+    float* dst;
+    long long stride;
+    __device__ Pre pre(const Params&, int, int, int, int) const { return Pre{{0.f, 0.f}, {0.f, 0.f}}; }
+    __device__ void apply(const Params&, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre&) const
+    {
+        const int npair = (r1 - r0) / 2;
+        for (int it = threadIdx.x; it < npair * nb; it += NT) {
+            const int pl = it / nb, b = it % nb;
+            const float g = sm.yf[(size_t)(2 * pl) * bgv + b], u = sm.yf[(size_t)(2 * pl + 1) * bgv + b];
+            dst[(size_t)(b0 + b) * stride + r0 / 2 + pl] = silu(g) * u;
+        }
     }
-}
+};
 
 // Rows [0, nlog) are logits (stored, and the CTA's argmax per batch row goes
 // to amax_*[i][cta]); rows >= nlog go to extra[i][row - nlog] (may be null).
-__device__ void epi_logits(const Params& P, float* lg, long long lg_stride, int nlog, float* extra,
-                           long long extra_stride, int r0, int r1, int b0, int nb, int bgv, const Smem& sm)
-{
-    const int rows = r1 - r0;
-    for (int it = threadIdx.x; it < rows * nb; it += NT) {
-        const int rl = it / nb, b = it % nb;
-        const int r = r0 + rl;
-        const float y = sm.yf[(size_t)rl * bgv + b];
-        if (r < nlog) lg[(size_t)(b0 + b) * lg_stride + r] = y;
-        else if (extra) extra[(size_t)(b0 + b) * extra_stride + (r - nlog)] = y;
-    }
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int b = 0; b < nb; ++b) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-        for (int rl = threadIdx.x; rl < rows; rl += NT) {
+struct EpiLogits {
+    float* lg;
+    long long lg_stride;
+    int nlog;
+    float* extra;
+    long long extra_stride;
+    __device__ Pre pre(const Params&, int, int, int, int) const { return Pre{{0.f, 0.f}, {0.f, 0.f}}; }
+    __device__ void apply(const Params& P, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre&) const
+    {
+        const int rows = r1 - r0;
+        for (int it = threadIdx.x; it < rows * nb; it += NT) {
+            const int rl = it / nb, b = it % nb;
             const int r = r0 + rl;
-            if (r >= nlog) break;
             const float y = sm.yf[(size_t)rl * bgv + b];
-            if (am_better(y, r, bv, bi)) { bv = y; bi = r; }
+            if (r < nlog) lg[(size_t)(b0 + b) * lg_stride + r] = y;
+            else if (extra) extra[(size_t)(b0 + b) * extra_stride + (r - nlog)] = y;
         }
-        warp_argmax(bv, bi);
-        csync();
-        if (lane == 0) { sm.amv[warp] = bv; sm.ami[warp] = bi; }
-        csync();
-        if (threadIdx.x == 0) {
-            float v = sm.amv[0];
-            int ix = sm.ami[0];
-            for (int k = 1; k < NWARP; ++k)
-                if (am_better(sm.amv[k], sm.ami[k], v, ix)) { v = sm.amv[k]; ix = sm.ami[k]; }
-            P.amax_v[(size_t)(b0 + b) * P.G + blockIdx.x] = v;
-            P.amax_i[(size_t)(b0 + b) * P.G + blockIdx.x] = ix;
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        for (int b = 0; b < nb; ++b) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+            for (int rl = threadIdx.x; rl < rows; rl += NT) {
+                const int r = r0 + rl;
+                if (r >= nlog) break;
+                const float y = sm.yf[(size_t)rl * bgv + b];
+                if (am_better(y, r, bv, bi)) { bv = y; bi = r; }
+            }
+            warp_argmax(bv, bi);
+            csync();
+            if (lane == 0) { sm.amv[warp] = bv; sm.ami[warp] = bi; }
+            csync();
+            if (threadIdx.x == 0) {
+                float v = sm.amv[0];
+                int ix = sm.ami[0];
+                for (int k = 1; k < NWARP; ++k)
+                    if (am_better(sm.amv[k], sm.ami[k], v, ix)) { v = sm.amv[k]; ix = sm.ami[k]; }
+                P.amax_v[(size_t)(b0 + b) * P.G + blockIdx.x] = v;
+                P.amax_i[(size_t)(b0 + b) * P.G + blockIdx.x] = ix;
+            }
         }
     }
-}
+};
+
+// depformer q to dq, k and v of substep j to the layer's substep cache
+struct EpiDQKV {
+    int l, j;
+    __device__ Pre pre(const Params&, int, int, int, int) const { return Pre{{0.f, 0.f}, {0.f, 0.f}}; }
+    __device__ void apply(const Params& P, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre&) const
+    {
+        const int dd = P.dd;
+        const int npair = (r1 - r0) / 2;
+        for (int it = threadIdx.x; it < npair * nb; it += NT) {
+            const int pl = it / nb, b = it % nb, i = b0 + b;
+            const int r = r0 + 2 * pl;
+            const int part = r / dd, e = r - part * dd;
+            const float y0 = sm.yf[(size_t)(2 * pl) * bgv + b];
+            const float y1 = sm.yf[(size_t)(2 * pl + 1) * bgv + b];
+            float* dst = part == 0 ? P.dq + (size_t)i * dd + e
+                                   : P.dkv + ((((size_t)i * P.dL + l) * P.S + j) * 2 + (part - 1)) * dd + e;
+            *reinterpret_cast<float2*>(dst) = make_float2(y0, y1);
+        }
+    }
+};
 
 // Reduce the per-CTA argmax partials of batch row i with one warp (every lane
 // gets the same result; the tie rule makes the combine order irrelevant).
@@ -683,7 +814,7 @@ __device__ __forceinline__ int argmax_partials_warp(const Params& P, int i)
 // Picks, for depformer substep j, each batch row's input token (the text token
 // for j = 0, else the code chosen for stream j), from the previous head's
 // argmax partials unless the token was supplied.  CTA 0 records it.
-__device__ void dep_select_inputs(const Params& P, int j, int b0, int nb, const Smem& sm)
+__device__ __forceinline__ void dep_select_inputs(const Params& P, int j, int b0, int nb, const Smem& sm)
 {
     const StepDesc* D = P.desc;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -708,11 +839,11 @@ __device__ void dep_select_inputs(const Params& P, int j, int b0, int nb, const 
     csync();
 }
 
-// One matrix-vector phase; epi(r0, r1, b0, nb, bgv) consumes the CTA's rows.
-// dep_j >= 0 selects the depformer layer-0 input tokens first.
+// One matrix-vector phase; the epilogue consumes the CTA's rows.  dep_j >= 0
+// selects the depformer layer-0 input tokens (xs.add set).
 template <typename TW, int BG, class Epi>
 __device__ bool gemv_phase(const Params& P, const Phase& ph, const XSrc& xs, int dep_j, int n, const Smem& sm,
-                           unsigned& stage, Epi epi)
+                           unsigned& stage, const Epi& epi)
 {
     const TW* W;
     int N, K;
@@ -723,17 +854,19 @@ __device__ bool gemv_phase(const Params& P, const Phase& ph, const XSrc& xs, int
     const int bgv = group_size<BG>(K);
     for (int b0 = 0; b0 < n; b0 += bgv) {
         const int nb = min(bgv, n - b0);
-        if (dep_j >= 0) dep_select_inputs(P, dep_j, b0, nb, sm);
         if (r1 > r0 || xs.store) {
+            const Pre pre = epi.pre(P, r0, r1, b0, nb);
             bool ok;
             switch (c.vpl) {
-                case 1: ok = gemv_group<TW, 1, BG, BG>(P, K, c, r0, r1, xs, b0, nb, sm, stage); break;
-                case 2: ok = gemv_group<TW, 2, BG, BG>(P, K, c, r0, r1, xs, b0, nb, sm, stage); break;
-                default: ok = gemv_group<TW, 3, (BG < 2 ? BG : 2), BG>(P, K, c, r0, r1, xs, b0, nb, sm, stage); break;
+                case 1: ok = gemv_group<TW, 1, BG, BG>(P, K, c, r0, r1, xs, b0, nb, dep_j, sm, stage); break;
+                case 2: ok = gemv_group<TW, 2, BG, BG>(P, K, c, r0, r1, xs, b0, nb, dep_j, sm, stage); break;
+                default: ok = gemv_group<TW, 3, (BG < 2 ? BG : 2), BG>(P, K, c, r0, r1, xs, b0, nb, dep_j, sm, stage); break;
             }
             if (!ok) return false;
+            epi.apply(P, sm, r0, r1, b0, nb, bgv, pre);
+        } else if (dep_j >= 0) {
+            dep_select_inputs(P, dep_j, b0, nb, sm);  // keeps the CTA's records consistent
         }
-        epi(r0, r1, b0, nb, bgv);
         csync();
     }
     return true;
@@ -770,14 +903,29 @@ __device__ void phase_embed(const Params& P, int n, const Smem& sm)
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        for (int k = 0; k < NSTREAM; ++k) {
-            const int tok = sm.X[i * NSTREAM + k];
-            const TW* row = k == 0 ? (const TW*)P.emb_text + (size_t)tok * d
-                                   : (const TW*)P.emb_audio + ((size_t)(k - 1) * (P.C + 1) + tok) * d;
-            float f[8];
-            WV<TW>::cvt(WV<TW>::load(row + e0), f);
+        // loads in batches of 6 rows (in flight together), summed in stream order
 #pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] += f[e];
+        for (int k0 = 0; k0 < NSTREAM; k0 += 6) {
+            typename WV<TW>::raw rows[6];
+#pragma unroll
+            for (int q = 0; q < 6; ++q) {
+                const int k = k0 + q;
+                if (k < NSTREAM) {
+                    const int tok = sm.X[i * NSTREAM + k];
+                    const TW* row = k == 0 ? (const TW*)P.emb_text + (size_t)tok * d
+                                           : (const TW*)P.emb_audio + ((size_t)(k - 1) * (P.C + 1) + tok) * d;
+                    rows[q] = WV<TW>::load(row + e0);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 6; ++q) {
+                if (k0 + q < NSTREAM) {
+                    float f[8];
+                    WV<TW>::cvt(rows[q], f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[e] += f[e];
+                }
+            }
         }
         float4* dst = reinterpret_cast<float4*>(P.x + (size_t)i * d + e0);
         dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
@@ -954,20 +1102,21 @@ __device__ void phase_final(const Params& P, int n)
     if (blockIdx.x != 0) return;
     const StepDesc* D = P.desc;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = P.S;
     for (int i = warp; i < n; i += NWARP) {
-        const int S = P.S;
         const int a = argmax_partials_warp(P, i);
-        if (lane != 0) continue;
         const int p = D->pos[i], slot = D->slot[i];
-        {
-            const int f = p - P.delays[S];
-            const int forced = f >= 0 ? ld_cg_int(P.hist + ((size_t)slot * NSTREAM + S) * HIST + f % HIST) : -1;
-            P.code_argmax[i * 16 + (S - 1)] = a;
-            P.chosen[i * NSTREAM + S] = forced >= 0 ? forced : a;
-        }
-        for (int k = 0; k < NSTREAM; ++k) {
+        if (lane < NSTREAM) {
+            const int k = lane;
             const int f = p - P.delays[k];
-            const int c = P.chosen[i * NSTREAM + k];
+            int c;
+            if (k == S) {
+                const int forced = f >= 0 ? ld_cg_int(P.hist + ((size_t)slot * NSTREAM + S) * HIST + f % HIST) : -1;
+                c = forced >= 0 ? forced : a;
+                P.code_argmax[i * 16 + (S - 1)] = a;
+            } else {
+                c = P.chosen[i * NSTREAM + k];
+            }
             if (f >= 0) P.hist[((size_t)slot * NSTREAM + k) * HIST + f % HIST] = c;
             if (k == 0) P.text_out[i] = c;
             else P.codes_out[i * 16 + (k - 1)] = f >= 0 ? c : -1;
@@ -985,25 +1134,20 @@ __device__ bool run_phase(const Params& P, const Phase ph, int n, const Smem& sm
         case PH_EMBED: phase_embed<TW>(P, n, sm); return true;
         case PH_QKV:
             return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, P.attn_norm + (size_t)ph.l * d, nullptr, 0, nullptr}, -1, n,
-                                      sm, stage, [&](int r0, int r1, int b0, int nb, int bgv) {
-                                          epi_qkv<TKV>(P, ph.l, r0, r1, b0, nb, bgv, sm);
-                                      });
+                                      sm, stage, EpiQKV<TKV>{ph.l});
         case PH_ATTN: phase_attn<TKV>(P, ph.l, n, sm); return true;
         case PH_O:
             return gemv_phase<TW, BG>(P, ph, XSrc{P.o, d, nullptr, nullptr, 0, nullptr}, -1, n, sm, stage,
-                                      [&](int r0, int r1, int b0, int nb, int bgv) { epi_resid(P.x, d, r0, r1, b0, nb, bgv, sm); });
+                                      EpiResid{P.x, d});
         case PH_GU:
             return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, P.ffn_norm + (size_t)ph.l * d, nullptr, 0, nullptr}, -1, n,
-                                      sm, stage,
-                                      [&](int r0, int r1, int b0, int nb, int bgv) { epi_swiglu(P.s, F, r0, r1, b0, nb, bgv, sm); });
+                                      sm, stage, EpiSwiglu{P.s, F});
         case PH_DOWN:
             return gemv_phase<TW, BG>(P, ph, XSrc{P.s, F, nullptr, nullptr, 0, nullptr}, -1, n, sm, stage,
-                                      [&](int r0, int r1, int b0, int nb, int bgv) { epi_resid(P.x, d, r0, r1, b0, nb, bgv, sm); });
+                                      EpiResid{P.x, d});
         case PH_HEAD:
             return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, P.out_norm, nullptr, 0, nullptr}, -1, n, sm, stage,
-                                      [&](int r0, int r1, int b0, int nb, int bgv) {
-                                          epi_logits(P, P.logits, P.V, P.V, P.yin, (long long)P.S * dd, r0, r1, b0, nb, bgv, sm);
-                                      });
+                                      EpiLogits{P.logits, P.V, P.V, P.yin, (long long)P.S * dd});
         case PH_DQKV: {
             XSrc xs;
             if (ph.l == 0) {
@@ -1013,39 +1157,21 @@ __device__ bool run_phase(const Params& P, const Phase ph, int n, const Smem& sm
             } else {
                 xs = XSrc{P.u, dd, P.dep_attn_norm + (size_t)ph.l * dd, nullptr, 0, nullptr};
             }
-            return gemv_phase<TW, BG>(P, ph, xs, ph.l == 0 ? ph.j : -1, n, sm, stage,
-                                      [&](int r0, int r1, int b0, int nb, int bgv) {
-                                          const int npair = (r1 - r0) / 2;
-                                          for (int it = threadIdx.x; it < npair * nb; it += NT) {
-                                              const int pl = it / nb, b = it % nb, i = b0 + b;
-                                              const int r = r0 + 2 * pl;
-                                              const int part = r / dd, e = r - part * dd;
-                                              const float y0 = sm.yf[(size_t)(2 * pl) * bgv + b];
-                                              const float y1 = sm.yf[(size_t)(2 * pl + 1) * bgv + b];
-                                              float* dst = part == 0 ? P.dq + (size_t)i * dd + e
-                                                                     : P.dkv + ((((size_t)i * P.dL + ph.l) * P.S + ph.j) * 2 + (part - 1)) * dd + e;
-                                              dst[0] = y0;
-                                              dst[1] = y1;
-                                          }
-                                      });
+            return gemv_phase<TW, BG>(P, ph, xs, ph.l == 0 ? ph.j : -1, n, sm, stage, EpiDQKV{ph.l, ph.j});
         }
         case PH_DATTN: phase_dattn(P, ph.l, ph.j, n); return true;
         case PH_DO:
             return gemv_phase<TW, BG>(P, ph, XSrc{P.dat, dd, nullptr, nullptr, 0, nullptr}, -1, n, sm, stage,
-                                      [&](int r0, int r1, int b0, int nb, int bgv) { epi_resid(P.u, dd, r0, r1, b0, nb, bgv, sm); });
+                                      EpiResid{P.u, dd});
         case PH_DGU:
             return gemv_phase<TW, BG>(P, ph, XSrc{P.u, dd, P.dep_ffn_norm + (size_t)ph.l * dd, nullptr, 0, nullptr}, -1,
-                                      n, sm, stage,
-                                      [&](int r0, int r1, int b0, int nb, int bgv) { epi_swiglu(P.ds, dF, r0, r1, b0, nb, bgv, sm); });
+                                      n, sm, stage, EpiSwiglu{P.ds, dF});
         case PH_DDOWN:
             return gemv_phase<TW, BG>(P, ph, XSrc{P.ds, dF, nullptr, nullptr, 0, nullptr}, -1, n, sm, stage,
-                                      [&](int r0, int r1, int b0, int nb, int bgv) { epi_resid(P.u, dd, r0, r1, b0, nb, bgv, sm); });
+                                      EpiResid{P.u, dd});
         case PH_DHEAD:
             return gemv_phase<TW, BG>(P, ph, XSrc{P.u, dd, P.dep_out_norm, nullptr, 0, nullptr}, -1, n, sm, stage,
-                                      [&](int r0, int r1, int b0, int nb, int bgv) {
-                                          epi_logits(P, P.dlogits + (size_t)ph.j * P.C, (long long)P.S * P.C, P.C, nullptr, 0,
-                                                     r0, r1, b0, nb, bgv, sm);
-                                      });
+                                      EpiLogits{P.dlogits + (size_t)ph.j * P.C, (long long)P.S * P.C, P.C, nullptr, 0});
         case PH_FINAL: phase_final(P, n); return true;
         default: return true;
     }
@@ -1093,15 +1219,17 @@ __global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int
     }
     unsigned target = 0, stage = 0;
     for (int ph = ph0; ph < ph1; ++ph) {
-        if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) P.ptime[ph] = globaltimer_ns();
+        if (threadIdx.x == 0) sm.ok[1] = ph;  // phase index for the in-phase stamps
+        stamp(P, ph, 0);
         const Phase phs = P.phases[ph];
         if (!run_phase<TW, TKV, BG>(P, phs, n, sm, stage)) return;
+        stamp(P, ph, 3);
         if (coop && ph + 1 < ph1) {
             target += (unsigned)P.G;
             if (!grid_barrier(P.bar, target, P.err, sm.ok)) return;
         }
     }
-    if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) P.ptime[ph1] = globaltimer_ns();
+    stamp(P, ph1, 0);
 }
 
 }  // namespace

@@ -232,12 +232,12 @@ def mfs_set_timing(ctx: Ctx, flags) -> None:
 
 
 def mfs_phase_times(ctx: Ctx) -> np.ndarray:
-    """Global-timer stamps (ns) at the start of each phase of the last step, plus its end."""
-    buf = np.zeros(4096, np.uint64)
+    """Global-timer stamps (ns) of the last step, [phases + 1, 4] (see include/mfs.h)."""
+    buf = np.zeros(16384, np.uint64)
     rc = _lib.mfs_phase_times(ctx.handle, buf.ctypes.data, buf.size)
     if rc < 0:
         _check(ctx, rc)
-    return buf[:rc].copy()
+    return buf[:rc].reshape(-1, 4).copy()
 
 
 def mfs_kernel_time(ctx: Ctx):

@@ -158,9 +158,11 @@ int mfs_launches_per_step(const mfs_ctx* ctx);
  * context's stream around its kernel launch(es); mfs_kernel_time waits for
  * the stream, returns the summed device time (ms) and the number of steps
  * timed since the previous call, and starts a new sum.  flags bit 1: the
- * kernel stamps the GPU's global timer at the start of every phase (and at
- * the end); mfs_phase_times copies the stamps (ns) of the last step into
- * ns[0..count) and returns count (phases + 1), or a negative status. */
+ * kernel stamps the GPU's global timer four times per phase (start, inputs
+ * ready, weights consumed, before the grid barrier; 0 where a point does not
+ * apply) and once at the end; mfs_phase_times copies the stamps (ns) of the
+ * last step into ns[0..count) as [phases + 1][4] and returns count, or a
+ * negative status. */
 int mfs_set_timing(mfs_ctx* ctx, int flags);
 int mfs_kernel_time(mfs_ctx* ctx, double* total_ms, int* steps);
 int mfs_phase_times(mfs_ctx* ctx, uint64_t* ns, int cap);
