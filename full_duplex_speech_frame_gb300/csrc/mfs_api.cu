@@ -62,7 +62,6 @@ struct mfs_ctx {
     Phase* d_phases = nullptr;
     StepDesc* d_desc = nullptr;
     StepDesc* d_pref = nullptr;
-    unsigned* d_bar = nullptr;
     int* d_err = nullptr;
     // pinned host memory
     StepDesc* h_desc = nullptr;  // DESC_RING entries
@@ -328,13 +327,16 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
         ao = align_up(ao + bytes, 256);
         return o;
     };
-    const size_t a_x = areg(MS * d * 4), a_q = areg(MS * d * 4), a_o = areg(MS * d * 4), a_s = areg(MS * F * 4);
-    const size_t a_lg = areg(MS * V * 4), a_yin = areg(MS * S * dd * 4), a_u = areg(MS * dd * 4);
-    const size_t a_dq = areg(MS * dd * 4), a_dkv = areg(MS * dL * S * 2 * dd * 4), a_dat = areg(MS * dd * 4);
-    const size_t a_ds = areg(MS * dF * 4), a_dlg = areg(MS * S * C * 4);
-    const size_t a_ap = areg(MS * H * NCHUNK_MAX * (hd + 4) * 4), a_ac = areg(MS * H * 4);
-    const size_t a_amv = areg(MS * c->G * 4), a_ami = areg(MS * c->G * 4), a_ch = areg(MS * NSTREAM * 4);
+    const size_t T8 = sizeof(uint2);  // tagged element
+    const size_t a_x = areg(MS * d * T8), a_q = areg(MS * d * T8), a_kc = areg(MS * d * T8), a_vc = areg(MS * d * T8);
+    const size_t a_o = areg(MS * d * T8), a_s = areg(MS * F * T8);
+    const size_t a_lg = areg(MS * V * 4), a_yin = areg(MS * S * dd * T8), a_u = areg(MS * dd * T8);
+    const size_t a_dq = areg(MS * dd * T8), a_dkv = areg(MS * dL * S * 2 * dd * T8), a_dat = areg(MS * dd * T8);
+    const size_t a_ds = areg(MS * dF * T8), a_dlg = areg(MS * S * C * 4);
+    const size_t a_am = areg(MS * c->G * 2 * T8), a_ch = areg(MS * NSTREAM * 4);
     const size_t a_to = areg(MS * 4), a_co = areg(MS * 16 * 4), a_ta = areg(MS * 4), a_ca = areg(MS * 16 * 4);
+    (void)H;
+    (void)hd;
     CK(cudaMalloc((void**)&c->act, ao));
     CK(cudaMemset(c->act, 0, ao));
 
@@ -351,39 +353,49 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
         CK(cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice));
     }
 
-    // phase list: embed, L x 5, head, S x (dL x 5 + 1), final
+    // phase list: embed, L x 5, head, S x (dL x 5 + 1), final; each phase names
+    // the phases whose tagged outputs it consumes
     std::vector<Phase> ph;
-    ph.push_back({PH_EMBED, 0, 0, 0});
+    auto add = [&](int type, int l, int j, int in, int res, int am) {
+        ph.push_back(Phase{type, l, j, in, res, am, 0, 0});
+        return (int)ph.size() - 1;
+    };
+    int x_ph = add(PH_EMBED, 0, 0, -1, -1, -1);  // last writer of the residual stream
     for (int l = 0; l < g.n_layers; ++l) {
-        ph.push_back({PH_QKV, l, 0, 0});
-        ph.push_back({PH_ATTN, l, 0, 0});
-        ph.push_back({PH_O, l, 0, 0});
-        ph.push_back({PH_GU, l, 0, 0});
-        ph.push_back({PH_DOWN, l, 0, 0});
+        const int qkv = add(PH_QKV, l, 0, x_ph, -1, -1);
+        const int att = add(PH_ATTN, l, 0, qkv, -1, -1);
+        const int o = add(PH_O, l, 0, att, x_ph, -1);
+        const int gu = add(PH_GU, l, 0, o, -1, -1);
+        x_ph = add(PH_DOWN, l, 0, gu, o, -1);
     }
     c->nphase_prefill = (int)ph.size();
-    ph.push_back({PH_HEAD, 0, 0, 0});
+    const int head = add(PH_HEAD, 0, 0, x_ph, -1, -1);
+    int am_ph = head;
+    c->P.dep_ph0 = (int)ph.size();
+    c->P.dep_ph_stride = 5 * g.dep_layers + 1;
     for (int j = 0; j < g.dep_steps; ++j) {
+        int u_ph = -1;  // last writer of the depformer residual
         for (int l = 0; l < g.dep_layers; ++l) {
-            ph.push_back({PH_DQKV, l, j, 0});
-            ph.push_back({PH_DATTN, l, j, 0});
-            ph.push_back({PH_DO, l, j, 0});
-            ph.push_back({PH_DGU, l, j, 0});
-            ph.push_back({PH_DDOWN, l, j, 0});
+            const int qkv = add(PH_DQKV, l, j, l == 0 ? head : u_ph, -1, l == 0 ? am_ph : -1);
+            if (l == 0) u_ph = qkv;  // layer 0 also writes the residual (in-projection + embedding)
+            const int att = add(PH_DATTN, l, j, qkv, -1, -1);
+            const int o = add(PH_DO, l, j, att, u_ph, -1);
+            const int gu = add(PH_DGU, l, j, o, -1, -1);
+            u_ph = add(PH_DDOWN, l, j, gu, o, -1);
         }
-        ph.push_back({PH_DHEAD, 0, j, 0});
+        am_ph = add(PH_DHEAD, 0, j, u_ph, -1, -1);
     }
-    ph.push_back({PH_FINAL, 0, 0, 0});
+    add(PH_FINAL, 0, 0, -1, -1, am_ph);
     c->nphase = (int)ph.size();
+    if (c->nphase >= 1024) return fail(c, MFS_E_ARG, "config: %d phases per step (at most 1023)", c->nphase);
     CK(cudaMalloc((void**)&c->d_phases, ph.size() * sizeof(Phase)));
     CK(cudaMemcpy(c->d_phases, ph.data(), ph.size() * sizeof(Phase), cudaMemcpyHostToDevice));
 
     CK(cudaMalloc((void**)&c->d_desc, sizeof(StepDesc)));
     CK(cudaMemset(c->d_desc, 0, sizeof(StepDesc)));
     CK(cudaMalloc((void**)&c->d_pref, PREF_CHUNK * sizeof(StepDesc)));
-    CK(cudaMalloc((void**)&c->d_bar, 256));
-    CK(cudaMemset(c->d_bar, 0, 256));
-    c->d_err = (int*)((char*)c->d_bar + 64);
+    CK(cudaMalloc((void**)&c->d_err, 256));
+    CK(cudaMemset(c->d_err, 0, 256));
     CK(cudaHostAlloc((void**)&c->h_desc, DESC_RING * sizeof(StepDesc), cudaHostAllocDefault));
     for (int i = 0; i < DESC_RING; ++i) CK(cudaEventCreateWithFlags(&c->desc_ev[i], cudaEventDisableTiming));
     CK(cudaHostAlloc((void**)&c->h_pref, PREF_CHUNK * sizeof(StepDesc), cudaHostAllocDefault));
@@ -404,14 +416,14 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
     P.rope = c->rope;
     P.kc = c->kc; P.vc = c->vc; P.hist = c->hist; P.desc = c->d_desc;
     char* A = c->act;
-    P.x = (float*)(A + a_x); P.q = (float*)(A + a_q); P.o = (float*)(A + a_o); P.s = (float*)(A + a_s);
-    P.logits = (float*)(A + a_lg); P.yin = (float*)(A + a_yin); P.u = (float*)(A + a_u);
-    P.dq = (float*)(A + a_dq); P.dkv = (float*)(A + a_dkv); P.dat = (float*)(A + a_dat);
-    P.ds = (float*)(A + a_ds); P.dlogits = (float*)(A + a_dlg); P.apart = (float*)(A + a_ap);
-    P.acnt = (int*)(A + a_ac); P.amax_v = (float*)(A + a_amv); P.amax_i = (int*)(A + a_ami);
+    P.x = (uint2*)(A + a_x); P.q = (uint2*)(A + a_q); P.kcur = (uint2*)(A + a_kc); P.vcur = (uint2*)(A + a_vc);
+    P.o = (uint2*)(A + a_o); P.s = (uint2*)(A + a_s);
+    P.logits = (float*)(A + a_lg); P.yin = (uint2*)(A + a_yin); P.u = (uint2*)(A + a_u);
+    P.dq = (uint2*)(A + a_dq); P.dkv = (uint2*)(A + a_dkv); P.dat = (uint2*)(A + a_dat);
+    P.ds = (uint2*)(A + a_ds); P.dlogits = (float*)(A + a_dlg); P.amax = (uint2*)(A + a_am);
     P.chosen = (int*)(A + a_ch); P.text_out = (int*)(A + a_to); P.codes_out = (int*)(A + a_co);
     P.text_argmax = (int*)(A + a_ta); P.code_argmax = (int*)(A + a_ca);
-    P.bar = c->d_bar; P.err = c->d_err; P.err_seq = c->d_err + 1;
+    P.err = c->d_err; P.err_seq = c->d_err + 1;
     P.phases = c->d_phases;
 
     // kernels: one per batch group; shared memory for the largest row block
@@ -467,7 +479,7 @@ extern "C" void mfs_destroy(mfs_ctx* c)
     if (c->stream) cudaStreamSynchronize(c->stream);
     cudaFree(c->arena); cudaFree(c->gains); cudaFree(c->kc); cudaFree(c->vc); cudaFree(c->hist);
     cudaFree(c->act); cudaFree(c->rope); cudaFree(c->d_phases); cudaFree(c->d_desc); cudaFree(c->d_pref);
-    cudaFree(c->d_bar);
+    cudaFree(c->d_err);
     cudaFree(c->d_ptime);
     for (int i = 0; i < DESC_RING; ++i)
         if (c->desc_ev[i]) cudaEventDestroy(c->desc_ev[i]);
@@ -549,7 +561,6 @@ static int launch(mfs_ctx* c, int n, int nph, const StepDesc* desc)
     c->last_nph = nph;
     const int bi = bg_index(n);
     int maxrows = c->maxrows;
-    CK(cudaMemsetAsync(c->d_bar, 0, 4, c->stream));
     cudaEvent_t ev1 = nullptr;
     if (c->timing) {
         if (c->ev_used + 2 > c->ev_pool.size()) {
@@ -564,14 +575,14 @@ static int launch(mfs_ctx* c, int n, int nph, const StepDesc* desc)
         c->ev_used += 2;
     }
     if (c->mode == 0) {
-        int ph0 = 0, ph1 = nph, coop = 1;
-        void* args[] = {&P, &ph0, &ph1, &coop, &maxrows};
+        int ph0 = 0, ph1 = nph;
+        void* args[] = {&P, &ph0, &ph1, &maxrows};
         CK(cudaLaunchCooperativeKernel(c->kfn[bi], dim3(c->G), dim3(NT + 32), args, c->smem[bi], c->stream));
         c->launches = 1;
     } else {
         for (int ph = 0; ph < nph; ++ph) {
-            int ph0 = ph, ph1 = ph + 1, coop = 0;
-            void* args[] = {&P, &ph0, &ph1, &coop, &maxrows};
+            int ph0 = ph, ph1 = ph + 1;
+            void* args[] = {&P, &ph0, &ph1, &maxrows};
             CK(cudaLaunchKernel(c->kfn[bi], dim3(c->G), dim3(NT + 32), args, c->smem[bi], c->stream));
         }
         c->launches = nph;

@@ -35,8 +35,11 @@ enum PhaseType : int {
     PH_FINAL,      // S10: last argmax, history write-back, outputs
 };
 
+// One phase of the step.  in_ph / res_ph / am_ph: index of the phase that
+// writes this phase's input vector / residual / argmax partials (-1: none);
+// the consumer waits for that phase's tag.
 struct Phase {
-    int type, l, j, pad;
+    int type, l, j, in_ph, res_ph, am_ph, pad0, pad1;
 };
 
 // Written by the host before each launch.
@@ -47,7 +50,7 @@ struct StepDesc {
     int codes[MFS_MAX_SLOTS][NSTREAM];
 };
 
-enum DeviceError : int { DERR_NONE = 0, DERR_TOKEN = 1, DERR_BARRIER = 2 };
+enum DeviceError : int { DERR_NONE = 0, DERR_TOKEN = 1, DERR_WAIT = 2 };
 
 struct Params {
     // shape
@@ -77,30 +80,31 @@ struct Params {
     void* vc;                   // [MS][L][W][d] values
     int* hist;                  // [MS][17][3]
     const StepDesc* desc;
-    // activations, row = position in the step's slot list
-    float* x;        // [MS][d]  residual stream
-    float* q;        // [MS][d]  rotated queries
-    float* o;        // [MS][d]  attention output
-    float* s;        // [MS][F]  SwiGLU output
-    float* logits;   // [MS][V]
-    float* yin;      // [MS][S][dd]  depformer in-projections
-    float* u;        // [MS][dd] depformer residual stream
-    float* dq;       // [MS][dd]
-    float* dkv;      // [MS][dL][S][2][dd]
-    float* dat;      // [MS][dd] depformer attention output
-    float* ds;       // [MS][dF]
-    float* dlogits;  // [MS][S][C]
-    float* apart;    // [MS][H][NCHUNK_MAX][hd+4] attention partials (m, l, pad, pad, acc[hd])
-    int* acnt;       // [MS][H] arrival counters (zero between uses)
-    float* amax_v;   // [MS][G] per-CTA argmax partials
-    int* amax_i;
-    int* chosen;     // [MS][17] tokens chosen this step
+    // activations, row = position in the step's slot list.  Elements that cross
+    // CTAs are tagged 64-bit words {float bits, tag}.
+    uint2* x;        // [MS][d]  residual stream
+    uint2* q;        // [MS][d]  rotated queries
+    uint2* kcur;     // [MS][d]  this step's rotated keys (rounded to the ring's type)
+    uint2* vcur;     // [MS][d]  this step's values (rounded to the ring's type)
+    uint2* o;        // [MS][d]  attention output
+    uint2* s;        // [MS][F]  SwiGLU output
+    float* logits;   // [MS][V]  (diagnostics)
+    uint2* yin;      // [MS][S][dd]  depformer in-projections
+    uint2* u;        // [MS][dd] depformer residual stream
+    uint2* dq;       // [MS][dd]
+    uint2* dkv;      // [MS][dL][S][2][dd]
+    uint2* dat;      // [MS][dd] depformer attention output
+    uint2* ds;       // [MS][dF]
+    float* dlogits;  // [MS][S][C]  (diagnostics)
+    uint2* amax;     // [MS][G][2] per-CTA argmax partials: {value, tag}, {index, tag}
+    int* chosen;     // [MS][17] tokens chosen this step (CTA 0)
     int* text_out;   // [MS]
     int* codes_out;  // [MS][16]
     int* text_argmax;  // [MS]
     int* code_argmax;  // [MS][16]
+    int dep_ph0;       // index of the first depformer phase
+    int dep_ph_stride; // phases per depformer substep
     // control
-    unsigned* bar;   // grid barrier counter (zeroed before each launch)
     int* err;        // sticky device error (DeviceError)
     int* err_seq;    // step sequence number that raised it
     const Phase* phases;

@@ -1,22 +1,30 @@
 // Device code of the lockstep frame step.
 //
 // One persistent cooperative kernel runs every phase of a step (embedding sum,
-// 32 temporal layers, text head, 16 depformer substeps, write-back) with a
-// grid-wide barrier between phases; the same kernel can also be launched once
-// per phase (no barriers) for diagnosis.  One CTA per SM: 16 consumer warps
-// and one producer warp.
+// 32 temporal layers, text head, 16 depformer substeps, write-back); the same
+// kernel can also be launched once per phase for diagnosis.  One CTA per SM:
+// 16 consumer warps and one producer warp.
 //
 // Weights move by TMA bulk copies (cp.async.bulk) into a ring of shared-memory
 // stages guarded by mbarriers.  The producer walks the same phase schedule as
 // the consumers and copies each phase's weight rows as soon as a stage is
-// free, so it runs ahead across the grid barriers and HBM keeps streaming while
-// the consumers synchronise.  A CTA owns a contiguous block of row pairs of
-// every matrix; its 16 consumer warps split K into contiguous slices and keep
-// their slice of the (normalised) activations in registers for the whole
-// phase.  Partial dot products are reduced lane-wise with a fixed shuffle
-// tree, then across K-slices in slice order: the arithmetic of one slot never
-// depends on the other slots of the batch, on the batch size or on the CTA
-// that owns a row.
+// free, so HBM keeps streaming while the consumers wait for their inputs.
+//
+// Phases do not meet at grid barriers.  Every activation element that crosses
+// CTAs is a 64-bit word {value, tag} written with one single-copy-atomic
+// store; the tag is (step sequence << 10 | writer phase).  A consumer reads
+// exactly the elements it needs and re-reads until the tags match, so a phase
+// starts as soon as its inputs exist, and a stale value can never be consumed
+// (a wait that cannot complete gives up after 2 s and sets the error flag).
+// Buffers are reused only after every reader of the previous value has
+// produced an output that the next writer itself waits for.
+//
+// A CTA owns a contiguous block of row pairs of every matrix; its 16 consumer
+// warps split K into contiguous slices and keep their slice of the
+// (normalised) activations in registers for the whole phase.  Partial dot
+// products are reduced with a fixed shuffle tree, then across K-slices in
+// slice order: the arithmetic of one slot never depends on the other slots of
+// the batch, on the batch size or on the CTA that owns a row.
 #pragma once
 #include <cuda_bf16.h>
 #include <math.h>
@@ -37,7 +45,7 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p)
     return r;
 }
 
-// L2-only load for data written by other CTAs during the same launch.
+// L2-only load (keys/values written by earlier steps).
 __device__ __forceinline__ uint4 ld_cg16(const void* p)
 {
     uint4 r;
@@ -47,7 +55,6 @@ __device__ __forceinline__ uint4 ld_cg16(const void* p)
 }
 
 __device__ __forceinline__ int ld_cg_int(const int* p) { return __ldcg(p); }
-__device__ __forceinline__ float ld_cg_f(const float* p) { return __ldcg(p); }
 
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
@@ -60,15 +67,17 @@ template <>
 struct WV<__nv_bfloat16> {
     struct raw { uint4 a; };
     static __device__ __forceinline__ raw load(const __nv_bfloat16* p) { return {ld_stream16(p)}; }
-    static __device__ __forceinline__ raw zero() { return {make_uint4(0u, 0u, 0u, 0u)}; }
     static __device__ __forceinline__ void cvt(const raw& r, float f[8])
     {
         f[0] = bf_lo(r.a.x); f[1] = bf_hi(r.a.x); f[2] = bf_lo(r.a.y); f[3] = bf_hi(r.a.y);
         f[4] = bf_lo(r.a.z); f[5] = bf_hi(r.a.z); f[6] = bf_lo(r.a.w); f[7] = bf_hi(r.a.w);
     }
-    static __device__ __forceinline__ float at(const void* base, long long i)
+    // 8 weights from shared memory
+    static __device__ __forceinline__ void lds8(const __nv_bfloat16* p, float f[8])
     {
-        return __uint_as_float((uint32_t)((const unsigned short*)base)[i] << 16);
+        const uint4 w = *reinterpret_cast<const uint4*>(p);
+        f[0] = bf_lo(w.x); f[1] = bf_hi(w.x); f[2] = bf_lo(w.y); f[3] = bf_hi(w.y);
+        f[4] = bf_lo(w.z); f[5] = bf_hi(w.z); f[6] = bf_lo(w.w); f[7] = bf_hi(w.w);
     }
 };
 
@@ -76,7 +85,6 @@ template <>
 struct WV<float> {
     struct raw { uint4 a, b; };
     static __device__ __forceinline__ raw load(const float* p) { return {ld_stream16(p), ld_stream16(p + 4)}; }
-    static __device__ __forceinline__ raw zero() { return {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)}; }
     static __device__ __forceinline__ void cvt(const raw& r, float f[8])
     {
         f[0] = __uint_as_float(r.a.x); f[1] = __uint_as_float(r.a.y);
@@ -84,7 +92,11 @@ struct WV<float> {
         f[4] = __uint_as_float(r.b.x); f[5] = __uint_as_float(r.b.y);
         f[6] = __uint_as_float(r.b.z); f[7] = __uint_as_float(r.b.w);
     }
-    static __device__ __forceinline__ float at(const void* base, long long i) { return ((const float*)base)[i]; }
+    static __device__ __forceinline__ void lds8(const float* p, float f[8])
+    {
+        const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
 };
 
 // Key/value ring element type.
@@ -93,14 +105,14 @@ struct KV;
 
 template <>
 struct KV<__nv_bfloat16> {
+    static __device__ __forceinline__ float round(float a) { return __bfloat162float(__float2bfloat16_rn(a)); }
     static __device__ __forceinline__ void store2(void* base, long long i, float a, float b)
     {
-        __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-        *reinterpret_cast<__nv_bfloat162*>((__nv_bfloat16*)base + i) = v;
+        *reinterpret_cast<__nv_bfloat162*>((__nv_bfloat16*)base + i) = __floats2bfloat162_rn(a, b);
     }
     static __device__ __forceinline__ void load8(const void* base, long long i, float f[8])
     {
-        uint4 r = ld_cg16((const __nv_bfloat16*)base + i);
+        const uint4 r = ld_cg16((const __nv_bfloat16*)base + i);
         f[0] = bf_lo(r.x); f[1] = bf_hi(r.x); f[2] = bf_lo(r.y); f[3] = bf_hi(r.y);
         f[4] = bf_lo(r.z); f[5] = bf_hi(r.z); f[6] = bf_lo(r.w); f[7] = bf_hi(r.w);
     }
@@ -108,17 +120,114 @@ struct KV<__nv_bfloat16> {
 
 template <>
 struct KV<float> {
+    static __device__ __forceinline__ float round(float a) { return a; }
     static __device__ __forceinline__ void store2(void* base, long long i, float a, float b)
     {
         *reinterpret_cast<float2*>((float*)base + i) = make_float2(a, b);
     }
     static __device__ __forceinline__ void load8(const void* base, long long i, float f[8])
     {
-        uint4 r0 = ld_cg16((const float*)base + i), r1 = ld_cg16((const float*)base + i + 4);
+        const uint4 r0 = ld_cg16((const float*)base + i), r1 = ld_cg16((const float*)base + i + 4);
         f[0] = __uint_as_float(r0.x); f[1] = __uint_as_float(r0.y); f[2] = __uint_as_float(r0.z); f[3] = __uint_as_float(r0.w);
         f[4] = __uint_as_float(r1.x); f[5] = __uint_as_float(r1.y); f[6] = __uint_as_float(r1.z); f[7] = __uint_as_float(r1.w);
     }
 };
+
+// ------------------------------------------------------------------ timers, errors
+
+__device__ __forceinline__ unsigned long long globaltimer_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // every wait gives up after 2 s
+
+// Spin bookkeeping: every 64 spins look at the clock and the error flag.
+// false: give up (error flag set).
+struct Spin {
+    unsigned n = 0;
+    unsigned long long t0 = 0;
+    __device__ __forceinline__ bool ok(int* err)
+    {
+        if ((++n & 63u) != 0u) return true;
+        if (*(volatile int*)err != 0) return false;
+        const unsigned long long t = globaltimer_ns();
+        if (t0 == 0) { t0 = t; return true; }
+        if (t - t0 > WAIT_LIMIT_NS) { atomicCAS(err, 0, (int)DERR_WAIT); return false; }
+        return true;
+    }
+};
+
+// ------------------------------------------------------------------ tagged values
+
+__device__ __forceinline__ unsigned phase_tag(const StepDesc* D, int ph)
+{
+    return ((unsigned)D->seq << 10) | (unsigned)ph;
+}
+
+// two tagged elements (16 bytes; each 64-bit half is read atomically)
+__device__ __forceinline__ void ld_tag2(const uint2* p, uint2& a, uint2& b)
+{
+    unsigned long long x, y;
+    asm volatile("ld.global.cg.v2.u64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "l"(p) : "memory");
+    a = make_uint2((unsigned)x, (unsigned)(x >> 32));
+    b = make_uint2((unsigned)y, (unsigned)(y >> 32));
+}
+
+__device__ __forceinline__ uint2 ld_tag1(const uint2* p)
+{
+    unsigned long long x;
+    asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(x) : "l"(p) : "memory");
+    return make_uint2((unsigned)x, (unsigned)(x >> 32));
+}
+
+__device__ __forceinline__ void st_tag2(uint2* p, float a, float b, unsigned tag)
+{
+    const unsigned long long x = ((unsigned long long)tag << 32) | __float_as_uint(a);
+    const unsigned long long y = ((unsigned long long)tag << 32) | __float_as_uint(b);
+    asm volatile("st.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(x), "l"(y) : "memory");
+}
+
+__device__ __forceinline__ void st_tag1(uint2* p, unsigned bits, unsigned tag)
+{
+    const unsigned long long x = ((unsigned long long)tag << 32) | bits;
+    asm volatile("st.global.u64 [%0], %1;" ::"l"(p), "l"(x) : "memory");
+}
+
+// one element, waiting for its tag
+__device__ __forceinline__ bool wait_tag1(const uint2* p, unsigned tag, unsigned& bits, int* err)
+{
+    Spin sp;
+    for (;;) {
+        const uint2 e = ld_tag1(p);
+        if (e.y == tag) { bits = e.x; return true; }
+        if (!sp.ok(err)) return false;
+    }
+}
+
+// 8 consecutive elements, waiting for their tags
+__device__ __forceinline__ bool wait_tag8(const uint2* p, unsigned tag, float f[8], int* err)
+{
+    Spin sp;
+    for (;;) {
+        uint2 e[8];
+        ld_tag2(p, e[0], e[1]);
+        ld_tag2(p + 2, e[2], e[3]);
+        ld_tag2(p + 4, e[4], e[5]);
+        ld_tag2(p + 6, e[6], e[7]);
+        bool ok = true;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ok = ok && e[k].y == tag;
+        if (ok) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(e[k].x);
+            return true;
+        }
+        if (!sp.ok(err)) return false;
+    }
+}
 
 // ------------------------------------------------------------------ reductions
 
@@ -146,74 +255,24 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        float v2 = __shfl_xor_sync(0xffffffffu, v, o);
-        int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+        const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
         if (am_better(v2, i2, v, i)) { v = v2; i = i2; }
     }
 }
 
-// Sum over the block, same bits in every thread (fixed order).  scratch >= NWARP floats.
-__device__ __forceinline__ float block_sum(float v, float* scratch)
-{
-    v = warp_sum(v);
-    const int w = threadIdx.x >> 5;
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) scratch[w] = v;
-    __syncthreads();
-    float t = 0.f;
-#pragma unroll
-    for (int k = 0; k < NWARP; ++k) t += scratch[k];
-    return t;
-}
-
 // ------------------------------------------------------------------ synchronisation
-
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v)
-{
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ unsigned long long globaltimer_ns()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // every spin gives up after 2 s
 
 // Barrier over the 16 consumer warps of the CTA (the producer warp never joins).
 __device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
-// All CTAs' consumers arrive; false (error flag set) if the wait gave up or
-// another CTA reported an error.
-__device__ bool grid_barrier(unsigned* bar, unsigned target, int* err, int* s_ok)
+// Same barrier, returning whether the predicate held in every consumer thread.
+__device__ __forceinline__ bool csync_and(int pred)
 {
-    csync();
-    if (threadIdx.x == 0) {
-        red_release_add(bar, 1u);
-        int ok = 1;
-        unsigned long long t0 = 0;
-        unsigned spins = 0;
-        while (ld_acquire_u32(bar) < target) {
-            if ((++spins & 63u) == 0u) {
-                if (*(volatile int*)err != 0) { ok = 0; break; }
-                const unsigned long long t = globaltimer_ns();
-                if (t0 == 0) t0 = t;
-                else if (t - t0 > WAIT_LIMIT_NS) { atomicCAS(err, 0, (int)DERR_BARRIER); ok = 0; break; }
-            }
-        }
-        *s_ok = ok;
-    }
-    csync();
-    return *(volatile int*)s_ok != 0;
+    int r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.and.pred q, 1, 512, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r) : "r"(pred) : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ unsigned smem_u32(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
@@ -242,17 +301,12 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, unsigned parity)
 }
 
 // Bounded wait for the phase of parity `parity` to complete.
-__device__ bool mbar_wait(uint64_t* b, unsigned parity, int* err)
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, int* err)
 {
-    unsigned long long t0 = 0;
-    for (unsigned i = 0;; ++i) {
+    Spin sp;
+    for (;;) {
         if (mbar_try(b, parity)) return true;
-        if ((i & 255u) == 255u) {
-            if (*(volatile int*)err != 0) return false;
-            const unsigned long long t = globaltimer_ns();
-            if (t0 == 0) t0 = t;
-            else if (t - t0 > WAIT_LIMIT_NS) { atomicCAS(err, 0, (int)DERR_BARRIER); return false; }
-        }
+        if (!sp.ok(err)) return false;
     }
 }
 
@@ -262,27 +316,16 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
 }
 
-// Diagnostic timer stamps of CTA 0: slot k of phase ph (0 start, 1 inputs
-// ready, 2 last weight stage consumed, 3 before the grid barrier).
-__device__ __forceinline__ void stamp(const Params& P, int ph, int k)
-{
-    if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) P.ptime[(size_t)ph * 4 + k] = globaltimer_ns();
-}
-
-// phase index for stamps taken inside a phase (thread 0 writes and reads it)
-
-
 // ------------------------------------------------------------------ shared memory map
 
 struct Smem {
     uint64_t* full;   // [nstage] stage filled
     uint64_t* empty;  // [nstage] stage released
-    float* r;         // [4] RMSNorm factors of the batch group
-    int* prev;        // [4] depformer input token per batch row
     float* ssq;       // [4][16] per-K-slice sums of squares
+    int* prev;        // [4] depformer input token per batch row
     float* amv;       // [NWARP]
     int* ami;         // [NWARP]
-    int* ok;          // [0] grid-barrier verdict, [1] phase index (stamps)
+    int* misc;        // [0] phase index (diagnostic stamps)
     char* ring;       // [nstage][STAGE_BYTES]
     float* red;       // [maxrows][BG][16] per-K-slice partial sums of the CTA's rows
     float* yf;        // [maxrows][BG] final row values of the CTA
@@ -295,18 +338,24 @@ __device__ __forceinline__ Smem smem_map(char* base, int maxrows, int BG)
     Smem s;
     s.full = (uint64_t*)base;
     s.empty = s.full + 8;
-    s.r = (float*)(base + 256);
-    s.prev = (int*)(base + 272);
-    s.ssq = (float*)(base + 288);
+    s.ssq = (float*)(base + 256);
+    s.prev = (int*)(base + 512);
     s.amv = (float*)(base + 544);
     s.ami = (int*)(base + 608);
-    s.ok = (int*)(base + 672);
+    s.misc = (int*)(base + 672);
     s.ring = base + SMEM_HEAD;
     s.red = (float*)(s.ring + (size_t)nstage_for(BG) * STAGE_BYTES);
     s.yf = s.red + (size_t)maxrows * BG * 16;
     s.X = (int*)s.red;
     s.wbuf = s.red;
     return s;
+}
+
+// Diagnostic timer stamps of CTA 0: slot k of phase ph (0 start, 1 inputs
+// ready, 2 last weight stage consumed, 3 end of the phase).
+__device__ __forceinline__ void stamp(const Params& P, int ph, int k)
+{
+    if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) P.ptime[(size_t)ph * 4 + k] = globaltimer_ns();
 }
 
 // ------------------------------------------------------------------ GEMV schedule (producer and consumers)
@@ -375,7 +424,7 @@ __device__ __forceinline__ int rows_per_stage(int K)
 // Producer: copy, for every phase of the launch, every batch group's pass over
 // this CTA's rows, stage by stage, in the order the consumers use them.
 template <typename TW, int BG>
-__device__ void producer(const Params& P, int ph0, int ph1, int n, const Smem& sm)
+__device__ __forceinline__ void producer(const Params& P, int ph0, int ph1, int n, const Smem& sm)
 {
     constexpr unsigned NS = nstage_for(BG);
     unsigned s = 0;
@@ -414,65 +463,114 @@ __device__ void producer(const Params& P, int ph0, int ph1, int n, const Smem& s
 
 // Where the input vector of a matrix-vector phase comes from.
 struct XSrc {
-    const float* base;    // batch row i at base + i * stride
+    const uint2* base;    // batch row i at base + i * stride (tagged)
     long long stride;
+    unsigned tag;         // tag the input must carry
     const float* g;       // RMSNorm gain, or nullptr for no norm
     const void* add;      // depformer embedding table (weight dtype) or nullptr
     long long add_stride; // row length of that table (elements)
-    float* store;         // CTA 0 stores base + add here (depformer residual), or nullptr
+    uint2* store;         // CTA 0 stores base + add here (depformer residual), or nullptr
+    unsigned store_tag;
 };
+
+// argmax partials of batch row i from every CTA (one warp; every lane gets the
+// same result; the tie rule makes the combine order irrelevant).  -1: gave up.
+__device__ __forceinline__ int argmax_partials_warp(const Params& P, int i, unsigned tag)
+{
+    const int lane = threadIdx.x & 31;
+    float v = -INFINITY;
+    int ix = 0x7fffffff;
+    bool ok = true;
+    for (int c = lane; c < P.G && ok; c += 32) {
+        const uint2* e = P.amax + ((size_t)i * P.G + c) * 2;
+        unsigned vb = 0, ib = 0;
+        ok = wait_tag1(e, tag, vb, P.err) && wait_tag1(e + 1, tag, ib, P.err);
+        if (ok && am_better(__uint_as_float(vb), (int)ib, v, ix)) { v = __uint_as_float(vb); ix = (int)ib; }
+    }
+    if (!__all_sync(0xffffffffu, ok)) return -1;
+    warp_argmax(v, ix);
+    return ix == 0x7fffffff ? 0 : ix;
+}
+
+// Picks, for depformer substep j, each batch row's input token (the text token
+// for j = 0, else the code chosen for stream j): the token the caller supplied
+// for that frame if any, else the previous head's argmax.  CTA 0 records it.
+// Every consumer thread calls it; false if a wait gave up.
+__device__ __forceinline__ bool dep_select_inputs(const Params& P, int j, unsigned am_tag, int b0, int nb, const Smem& sm)
+{
+    const StepDesc* D = P.desc;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int ok = 1;
+    if (warp < nb) {
+        const int i = b0 + warp;
+        const int a = argmax_partials_warp(P, i, am_tag);
+        ok = a >= 0;
+        int chosen = 0;
+        if (ok) {
+            const int p = D->pos[i], f = p - P.delays[j];
+            int forced = -1;
+            if (f == p) forced = D->codes[i][j];  // frame p: this step's input
+            else if (f >= 0) forced = ld_cg_int(P.hist + ((size_t)D->slot[i] * NSTREAM + j) * HIST + f % HIST);
+            chosen = forced >= 0 ? forced : a;
+            if (blockIdx.x == 0 && lane == 0) {
+                if (j == 0) P.text_argmax[i] = a;
+                else P.code_argmax[i * 16 + (j - 1)] = a;
+                P.chosen[i * NSTREAM + j] = chosen;
+            }
+        }
+        const int lim = j == 0 ? P.V : P.C;
+        if (lane == 0) sm.prev[warp] = (chosen >= 0 && chosen < lim) ? chosen : 0;  // keeps the embedding read in range
+    }
+    return csync_and(ok);
+}
 
 // Consume one batch group [b0, b0+nb) of a matrix-vector phase: leaves the
 // CTA's row values in sm.yf[(r - r0) * bgv + b].  `stage` counts ring stages.
-__device__ __forceinline__ void dep_select_inputs(const Params& P, int j, int b0, int nb, const Smem& sm);
-
 template <typename TW, int VPL, int BGV, int BG_OF_STAGES>
-__device__ __forceinline__ bool gemv_group(const Params& P, int K, const GemvCfg& c, int r0, int r1, const XSrc& xs, int b0,
-                           int nb, int dep_j, const Smem& sm, unsigned& stage)
+__device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int K, const GemvCfg& c, int r0, int r1,
+                                           const XSrc& xs, int b0, int nb, const Smem& sm, unsigned& stage)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kw = warp % c.nwk, rw = warp / c.nwk;
     const int NV = K / 8;
     const int v_begin = kw * c.nvw;
     const int v_end = min(NV, v_begin + c.nvw);
-    // this warp's K-slice of the input in registers, already multiplied by the
-    // norm gain (loaded in the same round trip); sums of squares of the raw input
+    // this warp's K-slice of the input in registers, waiting for its tags and
+    // multiplied by the norm gain; sums of squares of the raw input
     float xr[VPL][BGV][8];
     float ssq[BGV];
 #pragma unroll
     for (int b = 0; b < BGV; ++b) ssq[b] = 0.f;
     const bool gain_now = xs.g && !xs.add;
+    int ok = 1;
 #pragma unroll
     for (int t = 0; t < VPL; ++t) {
         const int v = v_begin + lane + 32 * t;
-        float4 g0 = make_float4(1.f, 1.f, 1.f, 1.f), g1 = g0;
+        float gg[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) gg[e] = 1.f;
         if (gain_now && v < v_end) {
             const float4* gs = reinterpret_cast<const float4*>(xs.g + v * 8);
-            g0 = __ldg(gs);
-            g1 = __ldg(gs + 1);
+            const float4 g0 = __ldg(gs), g1 = __ldg(gs + 1);
+            gg[0] = g0.x; gg[1] = g0.y; gg[2] = g0.z; gg[3] = g0.w; gg[4] = g1.x; gg[5] = g1.y; gg[6] = g1.z; gg[7] = g1.w;
         }
 #pragma unroll
         for (int b = 0; b < BGV; ++b) {
-            if (v < v_end && b < nb) {
-                const float4* src = reinterpret_cast<const float4*>(xs.base + (size_t)(b0 + b) * xs.stride + v * 8);
-                const float4 a0 = __ldcg(src), a1 = __ldcg(src + 1);
-                const float f[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-                const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            float f[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    ssq[b] = fmaf(f[e], f[e], ssq[b]);
-                    xr[t][b][e] = f[e] * gg[e];
-                }
-            } else {
+            for (int e = 0; e < 8; ++e) f[e] = 0.f;
+            if (v < v_end && b < nb && ok) ok = wait_tag8(xs.base + (size_t)(b0 + b) * xs.stride + v * 8, xs.tag, f, P.err);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) xr[t][b][e] = 0.f;
+            for (int e = 0; e < 8; ++e) {
+                ssq[b] = fmaf(f[e], f[e], ssq[b]);
+                xr[t][b][e] = f[e] * gg[e];
             }
         }
     }
     // depformer layer 0: the input adds the embedding of the token chosen by the
-    // previous head (its selection overlaps the loads above); then the gain
+    // previous head; then the gain
     if (xs.add) {
-        dep_select_inputs(P, dep_j, b0, nb, sm);
+        if (!dep_select_inputs(P, ph.j, phase_tag(P.desc, ph.am_ph), b0, nb, sm)) ok = 0;
 #pragma unroll
         for (int b = 0; b < BGV; ++b) ssq[b] = 0.f;
 #pragma unroll
@@ -500,9 +598,9 @@ __device__ __forceinline__ bool gemv_group(const Params& P, int K, const GemvCfg
 #pragma unroll
                 for (int b = 0; b < BGV; ++b) {
                     if (v < v_end && b < nb) {
-                        float4* dst = reinterpret_cast<float4*>(xs.store + (size_t)(b0 + b) * K + v * 8);
-                        dst[0] = make_float4(xr[t][b][0], xr[t][b][1], xr[t][b][2], xr[t][b][3]);
-                        dst[1] = make_float4(xr[t][b][4], xr[t][b][5], xr[t][b][6], xr[t][b][7]);
+                        uint2* dst = xs.store + (size_t)(b0 + b) * K + v * 8;
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) st_tag2(dst + e, xr[t][b][e], xr[t][b][e + 1], xs.store_tag);
                     }
                 }
             }
@@ -529,7 +627,7 @@ __device__ __forceinline__ bool gemv_group(const Params& P, int K, const GemvCfg
             const float q = warp_sum(ssq[b]);
             if (lane == 0 && rw == 0) sm.ssq[b * 16 + kw] = q;
         }
-        csync();
+        if (!csync_and(ok)) return false;
 #pragma unroll
         for (int b = 0; b < BGV; ++b) {
             float tot = 0.f;
@@ -540,11 +638,13 @@ __device__ __forceinline__ bool gemv_group(const Params& P, int K, const GemvCfg
 #pragma unroll
                 for (int e = 0; e < 8; ++e) xr[t][b][e] *= rb;
         }
+    } else if (!csync_and(ok)) {
+        return false;
     }
-    if (P.ptime) stamp(P, *(volatile int*)(sm.ok + 1), 1);
+    if (P.ptime) stamp(P, sm.misc[0], 1);
+
     // stream the CTA's rows through the ring: each warp takes rows rw, rw+nwr, ...
     // of a stage, four at a time, and releases the stage on its own
-    using Vt = WV<TW>;
     constexpr unsigned NS = nstage_for(BG_OF_STAGES);
     const int rps = rows_per_stage<TW>(K);
     for (int ra = r0; ra < r1; ra += rps, ++stage) {
@@ -567,17 +667,7 @@ __device__ __forceinline__ bool gemv_group(const Params& P, int K, const GemvCfg
                         const int v = v_begin + lane + 32 * t;
                         if (v < v_end) {
                             float f[8];
-                            const TW* wp = ring + (size_t)rr * K + (size_t)v * 8;
-                            if (sizeof(TW) == 2) {
-                                const uint4 w4 = *reinterpret_cast<const uint4*>(wp);
-                                f[0] = bf_lo(w4.x); f[1] = bf_hi(w4.x); f[2] = bf_lo(w4.y); f[3] = bf_hi(w4.y);
-                                f[4] = bf_lo(w4.z); f[5] = bf_hi(w4.z); f[6] = bf_lo(w4.w); f[7] = bf_hi(w4.w);
-                            } else {
-                                const uint4 q0 = *reinterpret_cast<const uint4*>(wp);
-                                const uint4 q1 = *reinterpret_cast<const uint4*>((const float*)wp + 4);
-                                f[0] = __uint_as_float(q0.x); f[1] = __uint_as_float(q0.y); f[2] = __uint_as_float(q0.z); f[3] = __uint_as_float(q0.w);
-                                f[4] = __uint_as_float(q1.x); f[5] = __uint_as_float(q1.y); f[6] = __uint_as_float(q1.z); f[7] = __uint_as_float(q1.w);
-                            }
+                            WV<TW>::lds8(ring + (size_t)rr * K + (size_t)v * 8, f);
 #pragma unroll
                             for (int b = 0; b < BGV; ++b)
 #pragma unroll
@@ -603,14 +693,13 @@ __device__ __forceinline__ bool gemv_group(const Params& P, int K, const GemvCfg
                 t += __shfl_xor_sync(0xffffffffu, t, 4);
                 t += __shfl_xor_sync(0xffffffffu, t, 2);
                 t += __shfl_xor_sync(0xffffffffu, t, 1);
-                if ((lane & 7) == 0 && rr < nr)
-                    sm.red[((size_t)(ra - r0 + rr) * BGV + b) * 16 + kw] = t;
+                if ((lane & 7) == 0 && rr < nr) sm.red[((size_t)(ra - r0 + rr) * BGV + b) * 16 + kw] = t;
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
-    if (P.ptime) stamp(P, *(volatile int*)(sm.ok + 1), 2);
+    if (P.ptime) stamp(P, sm.misc[0], 2);
     csync();
     // sum the K-slices in slice order
     for (int it = tid; it < (r1 - r0) * nb; it += NT) {
@@ -628,10 +717,11 @@ __device__ __forceinline__ bool gemv_group(const Params& P, int K, const GemvCfg
 
 // An epilogue sees the CTA's rows [r0, r1) for batch rows b0..b0+nb-1, values
 // in sm.yf[(row - r0) * bgv + b].  pre() runs before the weight stages and
-// loads what apply() needs from memory (up to two items per thread), so the
-// epilogue itself does not wait on a round trip.
+// loads what apply() needs (up to two items per thread) so that the epilogue
+// rarely waits on memory; empty() publishes what a CTA without rows owes.
 struct Pre {
     float a[2], b[2];
+    int ok;
 };
 
 __device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
@@ -639,9 +729,10 @@ __device__ __forceinline__ float silu(float g) { return g / (1.f + expf(-g)); }
 template <typename TKV>
 struct EpiQKV {
     int l;
+    unsigned tag;
     __device__ Pre pre(const Params& P, int r0, int r1, int b0, int nb) const
     {
-        Pre q{{0.f, 0.f}, {0.f, 0.f}};
+        Pre q{{0.f, 0.f}, {0.f, 0.f}, 1};
         const int npair = (r1 - r0) / 2;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
@@ -658,7 +749,8 @@ struct EpiQKV {
         }
         return q;
     }
-    __device__ void apply(const Params& P, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre& q) const
+    __device__ void empty(const Params&, int, int) const {}
+    __device__ bool apply(const Params& P, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre& q) const
     {
         const StepDesc* D = P.desc;
         const int d = P.d, hd = P.hd;
@@ -678,67 +770,99 @@ struct EpiQKV {
                 y1 = a * cs.y + c * cs.x;
             }
             if (part == 0) {
-                *reinterpret_cast<float2*>(P.q + (size_t)i * d + e) = make_float2(y0, y1);
+                st_tag2(P.q + (size_t)i * d + e, y0, y1, tag);
             } else {
+                // the ring keeps the key/value for later steps; this step's attention reads
+                // the same (rounded) numbers from the tagged copy
                 const int slot = D->slot[i];
                 const long long idx = (((long long)slot * P.L + l) * P.W + (p % P.W)) * (long long)d + e;
                 KV<TKV>::store2(part == 1 ? P.kc : P.vc, idx, y0, y1);
+                st_tag2((part == 1 ? P.kcur : P.vcur) + (size_t)i * d + e, KV<TKV>::round(y0), KV<TKV>::round(y1), tag);
             }
         }
+        return true;
     }
 };
 
-// dst[row] = residual + row value; the residual is read in pre()
+// dst[row] = residual + row value; the residual (tag res_tag) is read in pre()
 struct EpiResid {
-    float* dst;
+    uint2* dst;
     long long stride;
-    __device__ Pre pre(const Params&, int r0, int r1, int b0, int nb) const
+    unsigned res_tag, tag;
+    __device__ Pre pre(const Params& P, int r0, int r1, int b0, int nb) const
     {
-        Pre q{{0.f, 0.f}, {0.f, 0.f}};
+        Pre q{{0.f, 0.f}, {0.f, 0.f}, 1};
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int it = threadIdx.x + k * NT;
-            if (it < (r1 - r0) * nb) q.a[k] = __ldcg(dst + (size_t)(b0 + it % nb) * stride + r0 + it / nb);
+            if (it < (r1 - r0) * nb && q.ok) {
+                unsigned bits = 0;
+                q.ok = wait_tag1(dst + (size_t)(b0 + it % nb) * stride + r0 + it / nb, res_tag, bits, P.err);
+                q.a[k] = __uint_as_float(bits);
+            }
         }
         return q;
     }
-    __device__ void apply(const Params&, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre& q) const
+    __device__ void empty(const Params&, int, int) const {}
+    __device__ bool apply(const Params& P, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre& q) const
     {
-        for (int it = threadIdx.x; it < (r1 - r0) * nb; it += NT) {
+        bool ok = true;
+        for (int it = threadIdx.x; it < (r1 - r0) * nb && ok; it += NT) {
             const int rl = it / nb, b = it % nb;
-            float* p = dst + (size_t)(b0 + b) * stride + r0 + rl;
+            uint2* p = dst + (size_t)(b0 + b) * stride + r0 + rl;
             const int k = it / NT;
-            *p = (k < 2 ? q.a[k] : __ldcg(p)) + sm.yf[(size_t)rl * bgv + b];
+            float res = q.a[k < 2 ? k : 0];
+            if (k >= 2) {
+                unsigned bits = 0;
+                ok = wait_tag1(p, res_tag, bits, P.err);
+                res = __uint_as_float(bits);
+            }
+            st_tag1(p, __float_as_uint(res + sm.yf[(size_t)rl * bgv + b]), tag);
         }
+        return ok;
     }
 };
 
 // rows are (gate m, up m) pairs
 struct EpiSwiglu {
-    float* dst;
+    uint2* dst;
     long long stride;
-    __device__ Pre pre(const Params&, int, int, int, int) const { return Pre{{0.f, 0.f}, {0.f, 0.f}}; }
-    __device__ void apply(const Params&, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre&) const
+    unsigned tag;
+    __device__ Pre pre(const Params&, int, int, int, int) const { return Pre{{0.f, 0.f}, {0.f, 0.f}, 1}; }
+    __device__ void empty(const Params&, int, int) const {}
+    __device__ bool apply(const Params&, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre&) const
     {
         const int npair = (r1 - r0) / 2;
         for (int it = threadIdx.x; it < npair * nb; it += NT) {
             const int pl = it / nb, b = it % nb;
             const float g = sm.yf[(size_t)(2 * pl) * bgv + b], u = sm.yf[(size_t)(2 * pl + 1) * bgv + b];
-            dst[(size_t)(b0 + b) * stride + r0 / 2 + pl] = silu(g) * u;
+            st_tag1(dst + (size_t)(b0 + b) * stride + r0 / 2 + pl, __float_as_uint(silu(g) * u), tag);
         }
+        return true;
     }
 };
 
-// Rows [0, nlog) are logits (stored, and the CTA's argmax per batch row goes
-// to amax_*[i][cta]); rows >= nlog go to extra[i][row - nlog] (may be null).
+// Rows [0, nlog) are logits (stored for diagnostics; the CTA's argmax per
+// batch row goes to amax[i][cta], tagged); rows >= nlog go to extra[i][row - nlog].
 struct EpiLogits {
     float* lg;
     long long lg_stride;
     int nlog;
-    float* extra;
+    uint2* extra;
     long long extra_stride;
-    __device__ Pre pre(const Params&, int, int, int, int) const { return Pre{{0.f, 0.f}, {0.f, 0.f}}; }
-    __device__ void apply(const Params& P, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre&) const
+    unsigned tag;
+    __device__ Pre pre(const Params&, int, int, int, int) const { return Pre{{0.f, 0.f}, {0.f, 0.f}, 1}; }
+    __device__ void publish(const Params& P, int i, float v, int ix) const
+    {
+        uint2* e = P.amax + ((size_t)i * P.G + blockIdx.x) * 2;
+        st_tag1(e, __float_as_uint(v), tag);
+        st_tag1(e + 1, (unsigned)ix, tag);
+    }
+    __device__ void empty(const Params& P, int b0, int nb) const
+    {
+        if (threadIdx.x < nb) publish(P, b0 + threadIdx.x, -INFINITY, 0x7fffffff);
+    }
+    __device__ bool apply(const Params& P, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre&) const
     {
         const int rows = r1 - r0;
         for (int it = threadIdx.x; it < rows * nb; it += NT) {
@@ -746,7 +870,7 @@ struct EpiLogits {
             const int r = r0 + rl;
             const float y = sm.yf[(size_t)rl * bgv + b];
             if (r < nlog) lg[(size_t)(b0 + b) * lg_stride + r] = y;
-            else if (extra) extra[(size_t)(b0 + b) * extra_stride + (r - nlog)] = y;
+            else if (extra) st_tag1(extra + (size_t)(b0 + b) * extra_stride + (r - nlog), __float_as_uint(y), tag);
         }
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
         for (int b = 0; b < nb; ++b) {
@@ -767,18 +891,20 @@ struct EpiLogits {
                 int ix = sm.ami[0];
                 for (int k = 1; k < NWARP; ++k)
                     if (am_better(sm.amv[k], sm.ami[k], v, ix)) { v = sm.amv[k]; ix = sm.ami[k]; }
-                P.amax_v[(size_t)(b0 + b) * P.G + blockIdx.x] = v;
-                P.amax_i[(size_t)(b0 + b) * P.G + blockIdx.x] = ix;
+                publish(P, b0 + b, v, ix);
             }
         }
+        return true;
     }
 };
 
 // depformer q to dq, k and v of substep j to the layer's substep cache
 struct EpiDQKV {
     int l, j;
-    __device__ Pre pre(const Params&, int, int, int, int) const { return Pre{{0.f, 0.f}, {0.f, 0.f}}; }
-    __device__ void apply(const Params& P, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre&) const
+    unsigned tag;
+    __device__ Pre pre(const Params&, int, int, int, int) const { return Pre{{0.f, 0.f}, {0.f, 0.f}, 1}; }
+    __device__ void empty(const Params&, int, int) const {}
+    __device__ bool apply(const Params& P, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre&) const
     {
         const int dd = P.dd;
         const int npair = (r1 - r0) / 2;
@@ -788,62 +914,18 @@ struct EpiDQKV {
             const int part = r / dd, e = r - part * dd;
             const float y0 = sm.yf[(size_t)(2 * pl) * bgv + b];
             const float y1 = sm.yf[(size_t)(2 * pl + 1) * bgv + b];
-            float* dst = part == 0 ? P.dq + (size_t)i * dd + e
+            uint2* dst = part == 0 ? P.dq + (size_t)i * dd + e
                                    : P.dkv + ((((size_t)i * P.dL + l) * P.S + j) * 2 + (part - 1)) * dd + e;
-            *reinterpret_cast<float2*>(dst) = make_float2(y0, y1);
+            st_tag2(dst, y0, y1, tag);
         }
+        return true;
     }
 };
 
-// Reduce the per-CTA argmax partials of batch row i with one warp (every lane
-// gets the same result; the tie rule makes the combine order irrelevant).
-__device__ __forceinline__ int argmax_partials_warp(const Params& P, int i)
-{
-    const int lane = threadIdx.x & 31;
-    float v = -INFINITY;
-    int ix = 0x7fffffff;
-    for (int c = lane; c < P.G; c += 32) {
-        const float v2 = ld_cg_f(P.amax_v + (size_t)i * P.G + c);
-        const int i2 = ld_cg_int(P.amax_i + (size_t)i * P.G + c);
-        if (am_better(v2, i2, v, ix)) { v = v2; ix = i2; }
-    }
-    warp_argmax(v, ix);
-    return ix == 0x7fffffff ? 0 : ix;
-}
-
-// Picks, for depformer substep j, each batch row's input token (the text token
-// for j = 0, else the code chosen for stream j), from the previous head's
-// argmax partials unless the token was supplied.  CTA 0 records it.
-__device__ __forceinline__ void dep_select_inputs(const Params& P, int j, int b0, int nb, const Smem& sm)
-{
-    const StepDesc* D = P.desc;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (warp < nb) {
-        const int i = b0 + warp;
-        const int a = argmax_partials_warp(P, i);
-        int chosen;
-        if (j == 0) {
-            const int forced = D->codes[i][0];
-            chosen = forced >= 0 ? forced : a;
-            if (blockIdx.x == 0 && lane == 0) { P.text_argmax[i] = a; P.chosen[i * NSTREAM + 0] = chosen; }
-        } else {
-            const int p = D->pos[i], f = p - P.delays[j];
-            const int forced =
-                f >= 0 ? ld_cg_int(P.hist + ((size_t)D->slot[i] * NSTREAM + j) * HIST + f % HIST) : -1;
-            chosen = forced >= 0 ? forced : a;
-            if (blockIdx.x == 0 && lane == 0) { P.code_argmax[i * 16 + (j - 1)] = a; P.chosen[i * NSTREAM + j] = chosen; }
-        }
-        const int lim = j == 0 ? P.V : P.C;
-        if (lane == 0) sm.prev[warp] = (chosen >= 0 && chosen < lim) ? chosen : 0;  // keeps the embedding read in range
-    }
-    csync();
-}
-
-// One matrix-vector phase; the epilogue consumes the CTA's rows.  dep_j >= 0
-// selects the depformer layer-0 input tokens (xs.add set).
+// One matrix-vector phase; the epilogue consumes the CTA's rows.
 template <typename TW, int BG, class Epi>
-__device__ bool gemv_phase(const Params& P, const Phase& ph, const XSrc& xs, int dep_j, int n, const Smem& sm,
-                           unsigned& stage, const Epi& epi)
+__device__ __forceinline__ bool gemv_phase(const Params& P, const Phase& ph, const XSrc& xs, int n, const Smem& sm, unsigned& stage,
+                           const Epi& epi)
 {
     const TW* W;
     int N, K;
@@ -854,20 +936,19 @@ __device__ bool gemv_phase(const Params& P, const Phase& ph, const XSrc& xs, int
     const int bgv = group_size<BG>(K);
     for (int b0 = 0; b0 < n; b0 += bgv) {
         const int nb = min(bgv, n - b0);
-        if (r1 > r0 || xs.store) {
+        if (r1 > r0 || (xs.store && blockIdx.x == 0)) {
             const Pre pre = epi.pre(P, r0, r1, b0, nb);
             bool ok;
             switch (c.vpl) {
-                case 1: ok = gemv_group<TW, 1, BG, BG>(P, K, c, r0, r1, xs, b0, nb, dep_j, sm, stage); break;
-                case 2: ok = gemv_group<TW, 2, BG, BG>(P, K, c, r0, r1, xs, b0, nb, dep_j, sm, stage); break;
-                default: ok = gemv_group<TW, 3, (BG < 2 ? BG : 2), BG>(P, K, c, r0, r1, xs, b0, nb, dep_j, sm, stage); break;
+                case 1: ok = gemv_group<TW, 1, BG, BG>(P, ph, K, c, r0, r1, xs, b0, nb, sm, stage); break;
+                case 2: ok = gemv_group<TW, 2, BG, BG>(P, ph, K, c, r0, r1, xs, b0, nb, sm, stage); break;
+                default: ok = gemv_group<TW, 3, (BG < 2 ? BG : 2), BG>(P, ph, K, c, r0, r1, xs, b0, nb, sm, stage); break;
             }
-            if (!ok) return false;
-            epi.apply(P, sm, r0, r1, b0, nb, bgv, pre);
-        } else if (dep_j >= 0) {
-            dep_select_inputs(P, dep_j, b0, nb, sm);  // keeps the CTA's records consistent
+            if (!csync_and(ok && pre.ok)) return false;
+            if (!csync_and(epi.apply(P, sm, r0, r1, b0, nb, bgv, pre))) return false;
+        } else {
+            epi.empty(P, b0, nb);
         }
-        csync();
     }
     return true;
 }
@@ -875,7 +956,7 @@ __device__ bool gemv_phase(const Params& P, const Phase& ph, const XSrc& xs, int
 // ------------------------------------------------------------------ S0 + S1
 
 template <typename TW>
-__device__ void phase_embed(const Params& P, int n, const Smem& sm)
+__device__ __forceinline__ void phase_embed(const Params& P, int n, unsigned tag, const Smem& sm)
 {
     const StepDesc* D = P.desc;
     const int d = P.d;
@@ -896,14 +977,13 @@ __device__ void phase_embed(const Params& P, int n, const Smem& sm)
             P.hist[((size_t)D->slot[i] * NSTREAM + k) * HIST + D->pos[i] % HIST] = D->codes[i][k];
         }
     }
-    // x[i] = sum over streams in stream order
+    // x[i] = sum over streams in stream order; rows loaded 6 at a time
     const int per = d / 8;
     for (int it = blockIdx.x * NT + threadIdx.x; it < n * per; it += P.G * NT) {
         const int i = it / per, e0 = (it % per) * 8;
         float acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        // loads in batches of 6 rows (in flight together), summed in stream order
 #pragma unroll
         for (int k0 = 0; k0 < NSTREAM; k0 += 6) {
             typename WV<TW>::raw rows[6];
@@ -927,9 +1007,9 @@ __device__ void phase_embed(const Params& P, int n, const Smem& sm)
                 }
             }
         }
-        float4* dst = reinterpret_cast<float4*>(P.x + (size_t)i * d + e0);
-        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        uint2* dst = P.x + (size_t)i * d + e0;
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) st_tag2(dst + e, acc[e], acc[e + 1], tag);
     }
     csync();
 }
@@ -939,8 +1019,9 @@ __device__ void phase_embed(const Params& P, int n, const Smem& sm)
 // One CTA per (batch row, head); its 16 warps split the window into 16
 // contiguous runs of keys (a split that depends on the window length only),
 // and the partial softmax states are merged in shared memory in warp order.
+// The newest key/value (this step's) comes from the tagged copy.
 template <typename TKV>
-__device__ void phase_attn(const Params& P, int l, int n, const Smem& sm)
+__device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsigned in_tag, unsigned tag, const Smem& sm)
 {
     const StepDesc* D = P.desc;
     const int H = P.H, hd = P.hd, d = P.d, W = P.W;
@@ -957,12 +1038,9 @@ __device__ void phase_attn(const Params& P, int l, int n, const Smem& sm)
         const int start = p - len + 1;
         const int j0 = (int)((long long)len * warp / NWARP), j1 = (int)((long long)len * (warp + 1) / NWARP);
         float qv[8];
-        {
-            const float4* qs = reinterpret_cast<const float4*>(P.q + (size_t)i * d + h * hd + gl * 8);
-            const float4 a0 = __ldcg(qs), a1 = __ldcg(qs + 1);
-            qv[0] = a0.x * scale; qv[1] = a0.y * scale; qv[2] = a0.z * scale; qv[3] = a0.w * scale;
-            qv[4] = a1.x * scale; qv[5] = a1.y * scale; qv[6] = a1.z * scale; qv[7] = a1.w * scale;
-        }
+        int ok = wait_tag8(P.q + (size_t)i * d + h * hd + gl * 8, in_tag, qv, P.err);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qv[e] *= scale;
         const long long kvbase = ((long long)slot * P.L + l) * (long long)W * d + h * hd + gl * 8;
         float m = -INFINITY, lsum = 0.f, acc[8];
 #pragma unroll
@@ -975,13 +1053,15 @@ __device__ void phase_attn(const Params& P, int l, int n, const Smem& sm)
 #pragma unroll
             for (int u = 0; u < UNR; ++u) {
                 const int j = jj + u * PPI;
-                if (j < j1) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { kf[u][e] = 0.f; vf[u][e] = 0.f; }
+                if (j < j1 && j != len - 1) {
                     const long long row = (long long)((start + j) % W) * d;
                     KV<TKV>::load8(P.kc, kvbase + row, kf[u]);
                     KV<TKV>::load8(P.vc, kvbase + row, vf[u]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) { kf[u][e] = 0.f; vf[u][e] = 0.f; }
+                } else if (j == len - 1 && ok) {
+                    ok = wait_tag8(P.kcur + (size_t)i * d + h * hd + gl * 8, in_tag, kf[u], P.err) &&
+                         wait_tag8(P.vcur + (size_t)i * d + h * hd + gl * 8, in_tag, vf[u], P.err);
                 }
             }
 #pragma unroll
@@ -1030,7 +1110,7 @@ __device__ void phase_attn(const Params& P, int l, int n, const Smem& sm)
 #pragma unroll
             for (int e = 0; e < 8; ++e) wb[4 + gl * 8 + e] = acc[e];
         }
-        csync();
+        if (!csync_and(ok)) return false;
         // merge the 16 warps in warp order
         for (int e = threadIdx.x; e < hd; e += NT) {
             float M = -INFINITY;
@@ -1043,17 +1123,20 @@ __device__ void phase_attn(const Params& P, int l, int n, const Smem& sm)
                 L += sm.wbuf[(size_t)w * wstride + 1] * f;
                 a += sm.wbuf[(size_t)w * wstride + 4 + e] * f;
             }
-            P.o[(size_t)i * d + h * hd + e] = a / L;
+            st_tag1(P.o + (size_t)i * d + h * hd + e, __float_as_uint(a / L), tag);
         }
         csync();
     }
+    return true;
 }
 
 // ------------------------------------------------------------------ S9 depformer attention
 
-// One warp per (batch row, head): keys of substeps 0..j, no rotation.
-__device__ void phase_dattn(const Params& P, int l, int j, int n)
+// One warp per (batch row, head): keys of substeps 0..j, no rotation.  The key
+// and value of substep t carry the tag of that substep's QKV phase.
+__device__ __forceinline__ bool phase_dattn(const Params& P, int l, int j, int n, unsigned in_tag, unsigned tag)
 {
+    const StepDesc* D = P.desc;
     const int dd = P.dd, dH = P.dH, S = P.S;  // head dim is 64
     const int lane = threadIdx.x & 31;
     const int gwarp = blockIdx.x * NWARP + (threadIdx.x >> 5);
@@ -1061,14 +1144,42 @@ __device__ void phase_dattn(const Params& P, int l, int j, int n)
     const float scale = 0.125f;  // 1 / sqrt(64)
     for (int item = gwarp; item < n * dH; item += P.G * NWARP) {
         const int i = item / dH, h = item % dH;
-        const float* q = P.dq + (size_t)i * dd + h * 64;
-        const float* kv = P.dkv + ((size_t)i * P.dL + l) * S * 2 * dd + h * 64;
-        // lane covers dims 2*lane, 2*lane+1; all key loads first, then one warp sum per key
-        const float2 qq = __ldcg(reinterpret_cast<const float2*>(q) + lane);
-        float2 k2[16];
+        const uint2* q = P.dq + (size_t)i * dd + h * 64;
+        const uint2* kv = P.dkv + ((size_t)i * P.dL + l) * S * 2 * dd + h * 64;
+        int ok = 1;
+        // lane covers dims 2*lane, 2*lane+1; all loads first, then one warp sum per key
+        uint2 qa, qb;
+        {
+            Spin sp;
+            for (;;) {
+                ld_tag2(q + 2 * lane, qa, qb);
+                if (qa.y == in_tag && qb.y == in_tag) break;
+                if (!sp.ok(P.err)) { ok = 0; break; }
+            }
+        }
+        const float2 qq = make_float2(__uint_as_float(qa.x), __uint_as_float(qb.x));
+        float2 k2[16], v2[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t)
-            k2[t] = t < npos ? __ldcg(reinterpret_cast<const float2*>(kv + (size_t)t * 2 * dd) + lane) : make_float2(0.f, 0.f);
+        for (int t = 0; t < 16; ++t) {
+            k2[t] = make_float2(0.f, 0.f);
+            v2[t] = make_float2(0.f, 0.f);
+            if (t < npos && ok) {
+                const unsigned tt = phase_tag(D, P.dep_ph0 + t * P.dep_ph_stride + l * 5);
+                Spin sp;
+                for (;;) {
+                    uint2 a, b, c, e;
+                    ld_tag2(kv + (size_t)t * 2 * dd + 2 * lane, a, b);
+                    ld_tag2(kv + ((size_t)t * 2 + 1) * dd + 2 * lane, c, e);
+                    if (a.y == tt && b.y == tt && c.y == tt && e.y == tt) {
+                        k2[t] = make_float2(__uint_as_float(a.x), __uint_as_float(b.x));
+                        v2[t] = make_float2(__uint_as_float(c.x), __uint_as_float(e.x));
+                        break;
+                    }
+                    if (!sp.ok(P.err)) { ok = 0; break; }
+                }
+            }
+        }
+        if (!__all_sync(0xffffffffu, ok)) return false;
         float s = -INFINITY;
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
@@ -1078,40 +1189,38 @@ __device__ void phase_dattn(const Params& P, int l, int j, int n)
         const float M = warp_max(s);
         const float pe = lane < npos ? expf(s - M) : 0.f;
         const float inv = 1.f / warp_sum(pe);
-        // this lane's two output dims: all value loads first, then the sum in key order
-        float2 v[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t)
-            v[t] = t < npos ? __ldcg(reinterpret_cast<const float2*>(kv + ((size_t)t * 2 + 1) * dd) + lane)
-                            : make_float2(0.f, 0.f);
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
             const float pt = __shfl_sync(0xffffffffu, pe, t);
-            a0 = fmaf(pt, v[t].x, a0);
-            a1 = fmaf(pt, v[t].y, a1);
+            a0 = fmaf(pt, v2[t].x, a0);
+            a1 = fmaf(pt, v2[t].y, a1);
         }
-        reinterpret_cast<float2*>(P.dat + (size_t)i * dd + h * 64)[lane] = make_float2(a0 * inv, a1 * inv);
+        st_tag2(P.dat + (size_t)i * dd + h * 64 + 2 * lane, a0 * inv, a1 * inv, tag);
     }
+    return true;
 }
 
 // ------------------------------------------------------------------ S10
 
-__device__ void phase_final(const Params& P, int n)
+__device__ __forceinline__ bool phase_final(const Params& P, int n, unsigned am_tag)
 {
-    if (blockIdx.x != 0) return;
+    if (blockIdx.x != 0) return true;
     const StepDesc* D = P.desc;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = P.S;
     for (int i = warp; i < n; i += NWARP) {
-        const int a = argmax_partials_warp(P, i);
+        const int a = argmax_partials_warp(P, i, am_tag);
+        if (a < 0) return false;
         const int p = D->pos[i], slot = D->slot[i];
         if (lane < NSTREAM) {
             const int k = lane;
             const int f = p - P.delays[k];
             int c;
             if (k == S) {
-                const int forced = f >= 0 ? ld_cg_int(P.hist + ((size_t)slot * NSTREAM + S) * HIST + f % HIST) : -1;
+                int forced = -1;
+                if (f == p) forced = D->codes[i][S];
+                else if (f >= 0) forced = ld_cg_int(P.hist + ((size_t)slot * NSTREAM + S) * HIST + f % HIST);
                 c = forced >= 0 ? forced : a;
                 P.code_argmax[i * 16 + (S - 1)] = a;
             } else {
@@ -1122,67 +1231,73 @@ __device__ void phase_final(const Params& P, int n)
             else P.codes_out[i * 16 + (k - 1)] = f >= 0 ? c : -1;
         }
     }
+    return true;
 }
 
 // ------------------------------------------------------------------ phase dispatch
 
 template <typename TW, typename TKV, int BG>
-__device__ bool run_phase(const Params& P, const Phase ph, int n, const Smem& sm, unsigned& stage)
+__device__ __forceinline__ bool run_phase(const Params& P, const Phase ph, int phi, int n, const Smem& sm, unsigned& stage)
 {
     const int d = P.d, F = P.F, dd = P.dd, dF = P.dF;
+    const StepDesc* D = P.desc;
+    const unsigned tag = phase_tag(D, phi);
+    const unsigned in_tag = ph.in_ph >= 0 ? phase_tag(D, ph.in_ph) : 0u;
+    const unsigned res_tag = ph.res_ph >= 0 ? phase_tag(D, ph.res_ph) : 0u;
     switch (ph.type) {
-        case PH_EMBED: phase_embed<TW>(P, n, sm); return true;
+        case PH_EMBED: phase_embed<TW>(P, n, tag, sm); return true;
         case PH_QKV:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, P.attn_norm + (size_t)ph.l * d, nullptr, 0, nullptr}, -1, n,
-                                      sm, stage, EpiQKV<TKV>{ph.l});
-        case PH_ATTN: phase_attn<TKV>(P, ph.l, n, sm); return true;
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, in_tag, P.attn_norm + (size_t)ph.l * d, nullptr, 0, nullptr, 0},
+                                      n, sm, stage, EpiQKV<TKV>{ph.l, tag});
+        case PH_ATTN: return phase_attn<TKV>(P, ph.l, n, in_tag, tag, sm);
         case PH_O:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.o, d, nullptr, nullptr, 0, nullptr}, -1, n, sm, stage,
-                                      EpiResid{P.x, d});
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.o, d, in_tag, nullptr, nullptr, 0, nullptr, 0}, n, sm, stage,
+                                      EpiResid{P.x, d, res_tag, tag});
         case PH_GU:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, P.ffn_norm + (size_t)ph.l * d, nullptr, 0, nullptr}, -1, n,
-                                      sm, stage, EpiSwiglu{P.s, F});
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, in_tag, P.ffn_norm + (size_t)ph.l * d, nullptr, 0, nullptr, 0},
+                                      n, sm, stage, EpiSwiglu{P.s, F, tag});
         case PH_DOWN:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.s, F, nullptr, nullptr, 0, nullptr}, -1, n, sm, stage,
-                                      EpiResid{P.x, d});
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.s, F, in_tag, nullptr, nullptr, 0, nullptr, 0}, n, sm, stage,
+                                      EpiResid{P.x, d, res_tag, tag});
         case PH_HEAD:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, P.out_norm, nullptr, 0, nullptr}, -1, n, sm, stage,
-                                      EpiLogits{P.logits, P.V, P.V, P.yin, (long long)P.S * dd});
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, in_tag, P.out_norm, nullptr, 0, nullptr, 0}, n, sm, stage,
+                                      EpiLogits{P.logits, P.V, P.V, P.yin, (long long)P.S * dd, tag});
         case PH_DQKV: {
             XSrc xs;
             if (ph.l == 0) {
                 const void* add = ph.j == 0 ? P.dep_emb_text
                                             : (const void*)((const TW*)P.dep_emb_audio + (size_t)(ph.j - 1) * P.C * dd);
-                xs = XSrc{P.yin + (size_t)ph.j * dd, (long long)P.S * dd, P.dep_attn_norm, add, dd, P.u};
+                xs = XSrc{P.yin + (size_t)ph.j * dd, (long long)P.S * dd, in_tag, P.dep_attn_norm, add, dd, P.u, tag};
             } else {
-                xs = XSrc{P.u, dd, P.dep_attn_norm + (size_t)ph.l * dd, nullptr, 0, nullptr};
+                xs = XSrc{P.u, dd, in_tag, P.dep_attn_norm + (size_t)ph.l * dd, nullptr, 0, nullptr, 0};
             }
-            return gemv_phase<TW, BG>(P, ph, xs, ph.l == 0 ? ph.j : -1, n, sm, stage, EpiDQKV{ph.l, ph.j});
+            return gemv_phase<TW, BG>(P, ph, xs, n, sm, stage, EpiDQKV{ph.l, ph.j, tag});
         }
-        case PH_DATTN: phase_dattn(P, ph.l, ph.j, n); return true;
+        case PH_DATTN: return phase_dattn(P, ph.l, ph.j, n, in_tag, tag);
         case PH_DO:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.dat, dd, nullptr, nullptr, 0, nullptr}, -1, n, sm, stage,
-                                      EpiResid{P.u, dd});
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.dat, dd, in_tag, nullptr, nullptr, 0, nullptr, 0}, n, sm, stage,
+                                      EpiResid{P.u, dd, res_tag, tag});
         case PH_DGU:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.u, dd, P.dep_ffn_norm + (size_t)ph.l * dd, nullptr, 0, nullptr}, -1,
-                                      n, sm, stage, EpiSwiglu{P.ds, dF});
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.u, dd, in_tag, P.dep_ffn_norm + (size_t)ph.l * dd, nullptr, 0, nullptr, 0},
+                                      n, sm, stage, EpiSwiglu{P.ds, dF, tag});
         case PH_DDOWN:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.ds, dF, nullptr, nullptr, 0, nullptr}, -1, n, sm, stage,
-                                      EpiResid{P.u, dd});
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.ds, dF, in_tag, nullptr, nullptr, 0, nullptr, 0}, n, sm, stage,
+                                      EpiResid{P.u, dd, res_tag, tag});
         case PH_DHEAD:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.u, dd, P.dep_out_norm, nullptr, 0, nullptr}, -1, n, sm, stage,
-                                      EpiLogits{P.dlogits + (size_t)ph.j * P.C, (long long)P.S * P.C, P.C, nullptr, 0});
-        case PH_FINAL: phase_final(P, n); return true;
+            return gemv_phase<TW, BG>(P, ph, XSrc{P.u, dd, in_tag, P.dep_out_norm, nullptr, 0, nullptr, 0}, n, sm, stage,
+                                      EpiLogits{P.dlogits + (size_t)ph.j * P.C, (long long)P.S * P.C, P.C, nullptr, 0, tag});
+        case PH_FINAL: return phase_final(P, n, phase_tag(D, ph.am_ph));
         default: return true;
     }
 }
 
 // ------------------------------------------------------------------ the kernel
 
-// Phases [ph0, ph1) of one step.  coop != 0: cooperative launch, grid barrier
-// between phases.  maxrows sizes the dynamic shared memory (host computes it).
+// Phases [ph0, ph1) of one step.  When the launch spans more than one phase,
+// every CTA must be resident at once (cooperative launch), because CTAs wait
+// for each other's tagged outputs.  maxrows sizes the shared memory.
 template <typename TW, typename TKV, int BG>
-__global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int ph1, int coop, int maxrows)
+__global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int ph1, int maxrows)
 {
     extern __shared__ __align__(1024) char smem_raw[];
     const Smem sm = smem_map(smem_raw, maxrows, BG);
@@ -1217,17 +1332,13 @@ __global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int
         if ((threadIdx.x & 31) == 0) producer<TW, BG>(P, ph0, ph1, n, sm);
         return;
     }
-    unsigned target = 0, stage = 0;
+    unsigned stage = 0;
     for (int ph = ph0; ph < ph1; ++ph) {
-        if (threadIdx.x == 0) sm.ok[1] = ph;  // phase index for the in-phase stamps
+        if (threadIdx.x == 0) sm.misc[0] = ph;  // phase index for the in-phase stamps
         stamp(P, ph, 0);
         const Phase phs = P.phases[ph];
-        if (!run_phase<TW, TKV, BG>(P, phs, n, sm, stage)) return;
+        if (!run_phase<TW, TKV, BG>(P, phs, ph, n, sm, stage)) return;
         stamp(P, ph, 3);
-        if (coop && ph + 1 < ph1) {
-            target += (unsigned)P.G;
-            if (!grid_barrier(P.bar, target, P.err, sm.ok)) return;
-        }
     }
     stamp(P, ph1, 0);
 }
