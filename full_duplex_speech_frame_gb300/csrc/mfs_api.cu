@@ -604,7 +604,7 @@ static StepDesc* next_desc(mfs_ctx* c, int* idx)
 // steps that a device-side token check turned into no-ops.
 static int collect_device_error(mfs_ctx* c)
 {
-    int e[2] = {0, 0};
+    int e[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     CK(cudaMemcpy(e, c->d_err, sizeof e, cudaMemcpyDeviceToHost));
     int rc = MFS_OK;
     if (e[0] != 0) {
@@ -614,7 +614,14 @@ static int collect_device_error(mfs_ctx* c)
                     for (size_t k = 0; k < it->slots.size(); ++k) c->pos[it->slots[k]] = it->old_pos[k];
             rc = fail(c, MFS_E_TOKEN, "a device-side token was out of range (step %d); those steps did nothing", e[1]);
         } else {
-            rc = fail(c, MFS_E_DEVICE, "device wait gave up (code %d); slot state is undefined", e[0]);
+            static const char* sites[] = {"?", "tagged element", "tagged vector", "weight stage", "ring slot release",
+                                          "depformer query", "depformer key/value"};
+            const unsigned want = (unsigned)e[3], seen = (unsigned)e[4];
+            rc = fail(c, MFS_E_DEVICE,
+                      "device wait gave up at %s (expected step %u phase %u, saw step %u phase %u; CTA %d thread %d); "
+                      "slot state is undefined",
+                      sites[e[2] >= 1 && e[2] <= 6 ? e[2] : 0], want >> 10, want & 1023u, seen >> 10, seen & 1023u,
+                      e[5], e[6]);
         }
         CK(cudaMemset(c->d_err, 0, sizeof e));
     }

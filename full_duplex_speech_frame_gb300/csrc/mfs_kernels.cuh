@@ -145,17 +145,29 @@ __device__ __forceinline__ unsigned long long globaltimer_ns()
 constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // every wait gives up after 2 s
 
 // Spin bookkeeping: every 64 spins look at the clock and the error flag.
-// false: give up (error flag set).
+// false: give up.  The first waiter to give up records where (err[2..6]:
+// wait site, expected and observed tag or parity, CTA, thread).
+enum WaitSite : int { WS_TAG1 = 1, WS_TAG8 = 2, WS_FULL = 3, WS_EMPTY = 4, WS_DQ = 5, WS_DKV = 6 };
+
 struct Spin {
     unsigned n = 0;
     unsigned long long t0 = 0;
-    __device__ __forceinline__ bool ok(int* err)
+    __device__ __forceinline__ bool ok(int* err, int site, unsigned want, unsigned seen)
     {
         if ((++n & 63u) != 0u) return true;
         if (*(volatile int*)err != 0) return false;
         const unsigned long long t = globaltimer_ns();
         if (t0 == 0) { t0 = t; return true; }
-        if (t - t0 > WAIT_LIMIT_NS) { atomicCAS(err, 0, (int)DERR_WAIT); return false; }
+        if (t - t0 > WAIT_LIMIT_NS) {
+            if (atomicCAS(err, 0, (int)DERR_WAIT) == 0) {
+                err[2] = site;
+                err[3] = (int)want;
+                err[4] = (int)seen;
+                err[5] = (int)blockIdx.x;
+                err[6] = (int)threadIdx.x;
+            }
+            return false;
+        }
         return true;
     }
 };
@@ -167,11 +179,14 @@ __device__ __forceinline__ unsigned phase_tag(const StepDesc* D, int ph)
     return ((unsigned)D->seq << 10) | (unsigned)ph;
 }
 
-// two tagged elements (16 bytes; each 64-bit half is read atomically)
+// Tagged elements are read and written with relaxed gpu-scope (morally strong)
+// operations: weak loads may keep returning a stale copy of a line written by
+// another SM, strong ones observe the coherent value.
+// Two tagged elements (16 bytes; each 64-bit half is single-copy atomic).
 __device__ __forceinline__ void ld_tag2(const uint2* p, uint2& a, uint2& b)
 {
     unsigned long long x, y;
-    asm volatile("ld.global.cg.v2.u64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(x), "=l"(y) : "l"(p) : "memory");
     a = make_uint2((unsigned)x, (unsigned)(x >> 32));
     b = make_uint2((unsigned)y, (unsigned)(y >> 32));
 }
@@ -179,7 +194,7 @@ __device__ __forceinline__ void ld_tag2(const uint2* p, uint2& a, uint2& b)
 __device__ __forceinline__ uint2 ld_tag1(const uint2* p)
 {
     unsigned long long x;
-    asm volatile("ld.global.cg.u64 %0, [%1];" : "=l"(x) : "l"(p) : "memory");
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(x) : "l"(p) : "memory");
     return make_uint2((unsigned)x, (unsigned)(x >> 32));
 }
 
@@ -187,13 +202,13 @@ __device__ __forceinline__ void st_tag2(uint2* p, float a, float b, unsigned tag
 {
     const unsigned long long x = ((unsigned long long)tag << 32) | __float_as_uint(a);
     const unsigned long long y = ((unsigned long long)tag << 32) | __float_as_uint(b);
-    asm volatile("st.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(x), "l"(y) : "memory");
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(x), "l"(y) : "memory");
 }
 
 __device__ __forceinline__ void st_tag1(uint2* p, unsigned bits, unsigned tag)
 {
     const unsigned long long x = ((unsigned long long)tag << 32) | bits;
-    asm volatile("st.global.u64 [%0], %1;" ::"l"(p), "l"(x) : "memory");
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(x) : "memory");
 }
 
 // one element, waiting for its tag
@@ -203,7 +218,7 @@ __device__ __forceinline__ bool wait_tag1(const uint2* p, unsigned tag, unsigned
     for (;;) {
         const uint2 e = ld_tag1(p);
         if (e.y == tag) { bits = e.x; return true; }
-        if (!sp.ok(err)) return false;
+        if (!sp.ok(err, WS_TAG1, tag, e.y)) return false;
     }
 }
 
@@ -218,15 +233,42 @@ __device__ __forceinline__ bool wait_tag8(const uint2* p, unsigned tag, float f[
         ld_tag2(p + 4, e[4], e[5]);
         ld_tag2(p + 6, e[6], e[7]);
         bool ok = true;
+        unsigned seen = tag;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) ok = ok && e[k].y == tag;
+        for (int k = 0; k < 8; ++k) {
+            ok = ok && e[k].y == tag;
+            if (e[k].y != tag) seen = e[k].y;
+        }
         if (ok) {
 #pragma unroll
             for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(e[k].x);
             return true;
         }
-        if (!sp.ok(err)) return false;
+        if (!sp.ok(err, WS_TAG8, tag, seen)) return false;
     }
+}
+
+// Issue the loads of 8 tagged elements without waiting (values and tags land
+// in e[]); tag8_take() checks them and falls back to wait_tag8 if needed.
+__device__ __forceinline__ void tag8_issue(const uint2* p, uint2 (&e)[8])
+{
+    ld_tag2(p, e[0], e[1]);
+    ld_tag2(p + 2, e[2], e[3]);
+    ld_tag2(p + 4, e[4], e[5]);
+    ld_tag2(p + 6, e[6], e[7]);
+}
+
+__device__ __forceinline__ bool tag8_take(const uint2 (&e)[8], const uint2* p, unsigned tag, float f[8], int* err)
+{
+    bool ok = true;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ok = ok && e[k].y == tag;
+    if (ok) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] = __uint_as_float(e[k].x);
+        return true;
+    }
+    return wait_tag8(p, tag, f, err);
 }
 
 // ------------------------------------------------------------------ reductions
@@ -301,12 +343,12 @@ __device__ __forceinline__ bool mbar_try(uint64_t* b, unsigned parity)
 }
 
 // Bounded wait for the phase of parity `parity` to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, int* err)
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, int* err, int site)
 {
     Spin sp;
     for (;;) {
         if (mbar_try(b, parity)) return true;
-        if (!sp.ok(err)) return false;
+        if (!sp.ok(err, site, parity, 0)) return false;
     }
 }
 
@@ -442,7 +484,7 @@ __device__ __forceinline__ void producer(const Params& P, int ph0, int ph1, int 
                 const int rows = min(rps, r1 - r);
                 const unsigned bytes = (unsigned)(rows * K * (int)sizeof(TW));
                 const int slot = (int)(s % NS);
-                if (!mbar_wait(&sm.empty[slot], ((s / NS) & 1u) ^ 1u, P.err)) { ok = false; break; }
+                if (!mbar_wait(&sm.empty[slot], ((s / NS) & 1u) ^ 1u, P.err, WS_EMPTY)) { ok = false; break; }
                 mbar_expect_tx(&sm.full[slot], bytes);
                 bulk_g2s(sm.ring + (size_t)slot * STAGE_BYTES, W + (size_t)r * K, bytes, &sm.full[slot]);
             }
@@ -543,23 +585,37 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
     for (int b = 0; b < BGV; ++b) ssq[b] = 0.f;
     const bool gain_now = xs.g && !xs.add;
     int ok = 1;
+    // first pass issues every vector's loads (in chunks of 4 vectors), then checks
+    constexpr int NVEC = VPL * BGV;
+    constexpr int CH = NVEC < 4 ? NVEC : 4;
 #pragma unroll
-    for (int t = 0; t < VPL; ++t) {
-        const int v = v_begin + lane + 32 * t;
-        float gg[8];
+    for (int c0 = 0; c0 < NVEC; c0 += CH) {
+        uint2 pend[CH][8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) gg[e] = 1.f;
-        if (gain_now && v < v_end) {
-            const float4* gs = reinterpret_cast<const float4*>(xs.g + v * 8);
-            const float4 g0 = __ldg(gs), g1 = __ldg(gs + 1);
-            gg[0] = g0.x; gg[1] = g0.y; gg[2] = g0.z; gg[3] = g0.w; gg[4] = g1.x; gg[5] = g1.y; gg[6] = g1.z; gg[7] = g1.w;
+        for (int q = 0; q < CH; ++q) {
+            const int t = (c0 + q) / BGV, b = (c0 + q) % BGV;
+            const int v = v_begin + lane + 32 * t;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) pend[q][k] = make_uint2(0u, 0u);
+            if (c0 + q < NVEC && v < v_end && b < nb) tag8_issue(xs.base + (size_t)(b0 + b) * xs.stride + v * 8, pend[q]);
         }
 #pragma unroll
-        for (int b = 0; b < BGV; ++b) {
+        for (int q = 0; q < CH; ++q) {
+            if (c0 + q >= NVEC) break;
+            const int t = (c0 + q) / BGV, b = (c0 + q) % BGV;
+            const int v = v_begin + lane + 32 * t;
             float f[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) f[e] = 0.f;
-            if (v < v_end && b < nb && ok) ok = wait_tag8(xs.base + (size_t)(b0 + b) * xs.stride + v * 8, xs.tag, f, P.err);
+            if (v < v_end && b < nb && ok) ok = tag8_take(pend[q], xs.base + (size_t)(b0 + b) * xs.stride + v * 8, xs.tag, f, P.err);
+            float gg[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) gg[e] = 1.f;
+            if (gain_now && v < v_end) {
+                const float4* gs = reinterpret_cast<const float4*>(xs.g + v * 8);
+                const float4 g0 = __ldg(gs), g1 = __ldg(gs + 1);
+                gg[0] = g0.x; gg[1] = g0.y; gg[2] = g0.z; gg[3] = g0.w; gg[4] = g1.x; gg[5] = g1.y; gg[6] = g1.z; gg[7] = g1.w;
+            }
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 ssq[b] = fmaf(f[e], f[e], ssq[b]);
@@ -650,7 +706,7 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
     for (int ra = r0; ra < r1; ra += rps, ++stage) {
         const int nr = min(rps, r1 - ra);
         const int slot = (int)(stage % NS);
-        if (!mbar_wait(&sm.full[slot], (stage / NS) & 1u, P.err)) return false;
+        if (!mbar_wait(&sm.full[slot], (stage / NS) & 1u, P.err, WS_FULL)) return false;
         const TW* ring = (const TW*)(sm.ring + (size_t)slot * STAGE_BYTES);
         for (int c0 = rw; c0 < nr; c0 += 4 * c.nwr) {
             float acc[4][BGV];
@@ -792,14 +848,19 @@ struct EpiResid {
     __device__ Pre pre(const Params& P, int r0, int r1, int b0, int nb) const
     {
         Pre q{{0.f, 0.f}, {0.f, 0.f}, 1};
+        uint2 e[2] = {make_uint2(0u, res_tag), make_uint2(0u, res_tag)};
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int it = threadIdx.x + k * NT;
-            if (it < (r1 - r0) * nb && q.ok) {
-                unsigned bits = 0;
+            if (it < (r1 - r0) * nb) e[k] = ld_tag1(dst + (size_t)(b0 + it % nb) * stride + r0 + it / nb);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int it = threadIdx.x + k * NT;
+            unsigned bits = e[k].x;
+            if (it < (r1 - r0) * nb && e[k].y != res_tag && q.ok)
                 q.ok = wait_tag1(dst + (size_t)(b0 + it % nb) * stride + r0 + it / nb, res_tag, bits, P.err);
-                q.a[k] = __uint_as_float(bits);
-            }
+            q.a[k] = __uint_as_float(bits);
         }
         return q;
     }
@@ -1037,11 +1098,24 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
         const int len = p + 1 < W ? p + 1 : W;
         const int start = p - len + 1;
         const int j0 = (int)((long long)len * warp / NWARP), j1 = (int)((long long)len * (warp + 1) / NWARP);
-        float qv[8];
-        int ok = wait_tag8(P.q + (size_t)i * d + h * hd + gl * 8, in_tag, qv, P.err);
+        const long long kvbase = ((long long)slot * P.L + l) * (long long)W * d + h * hd + gl * 8;
+        // the query and this step's key/value are polled while the first ring loads are in flight
+        uint2 qt[8], kt[8], vt[8];
+        tag8_issue(P.q + (size_t)i * d + h * hd + gl * 8, qt);
+        const bool has_cur = len - 1 >= j0 && len - 1 < j1;
+        if (has_cur) {
+            tag8_issue(P.kcur + (size_t)i * d + h * hd + gl * 8, kt);
+            tag8_issue(P.vcur + (size_t)i * d + h * hd + gl * 8, vt);
+        }
+        float qv[8], kcur[8], vcur[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { kcur[e] = 0.f; vcur[e] = 0.f; }
+        int ok = tag8_take(qt, P.q + (size_t)i * d + h * hd + gl * 8, in_tag, qv, P.err);
+        if (has_cur && ok)
+            ok = tag8_take(kt, P.kcur + (size_t)i * d + h * hd + gl * 8, in_tag, kcur, P.err) &&
+                 tag8_take(vt, P.vcur + (size_t)i * d + h * hd + gl * 8, in_tag, vcur, P.err);
 #pragma unroll
         for (int e = 0; e < 8; ++e) qv[e] *= scale;
-        const long long kvbase = ((long long)slot * P.L + l) * (long long)W * d + h * hd + gl * 8;
         float m = -INFINITY, lsum = 0.f, acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
@@ -1059,9 +1133,9 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
                     const long long row = (long long)((start + j) % W) * d;
                     KV<TKV>::load8(P.kc, kvbase + row, kf[u]);
                     KV<TKV>::load8(P.vc, kvbase + row, vf[u]);
-                } else if (j == len - 1 && ok) {
-                    ok = wait_tag8(P.kcur + (size_t)i * d + h * hd + gl * 8, in_tag, kf[u], P.err) &&
-                         wait_tag8(P.vcur + (size_t)i * d + h * hd + gl * 8, in_tag, vf[u], P.err);
+                } else if (j == len - 1) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) { kf[u][e] = kcur[e]; vf[u][e] = vcur[e]; }
                 }
             }
 #pragma unroll
@@ -1132,71 +1206,71 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
 
 // ------------------------------------------------------------------ S9 depformer attention
 
-// One warp per (batch row, head): keys of substeps 0..j, no rotation.  The key
-// and value of substep t carry the tag of that substep's QKV phase.
-__device__ __forceinline__ bool phase_dattn(const Params& P, int l, int j, int n, unsigned in_tag, unsigned tag)
+// One CTA per (batch row, head): keys of substeps 0..j, no rotation.  Warp t
+// loads key/value t (tag of that substep's QKV phase) together with the
+// query, so every load of the item is in flight at once; the softmax and the
+// weighted sum run in key order in shared memory.
+__device__ __forceinline__ bool phase_dattn(const Params& P, int l, int j, int n, unsigned in_tag, unsigned tag,
+                                            const Smem& sm)
 {
     const StepDesc* D = P.desc;
     const int dd = P.dd, dH = P.dH, S = P.S;  // head dim is 64
-    const int lane = threadIdx.x & 31;
-    const int gwarp = blockIdx.x * NWARP + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int npos = j + 1;
     const float scale = 0.125f;  // 1 / sqrt(64)
-    for (int item = gwarp; item < n * dH; item += P.G * NWARP) {
+    float* sc = sm.wbuf;         // [16] scores
+    float* pv = sm.wbuf + 16;    // [16][64] p_t * v_t
+    for (int item = blockIdx.x; item < n * dH; item += P.G) {
         const int i = item / dH, h = item % dH;
-        const uint2* q = P.dq + (size_t)i * dd + h * 64;
-        const uint2* kv = P.dkv + ((size_t)i * P.dL + l) * S * 2 * dd + h * 64;
+        const uint2* q = P.dq + (size_t)i * dd + h * 64 + 2 * lane;
+        const uint2* kv = P.dkv + ((size_t)i * P.dL + l) * S * 2 * dd + h * 64 + 2 * lane;
+        const int t = warp;
         int ok = 1;
-        // lane covers dims 2*lane, 2*lane+1; all loads first, then one warp sum per key
-        uint2 qa, qb;
-        {
+        float2 vt = make_float2(0.f, 0.f);
+        if (t < npos) {
+            const unsigned tt = phase_tag(D, P.dep_ph0 + t * P.dep_ph_stride + l * 5);
+            const uint2* kp = kv + (size_t)t * 2 * dd;
+            const uint2* vp = kv + ((size_t)t * 2 + 1) * dd;
+            uint2 qa, qb, ka, kb, va, vb;
+            ld_tag2(q, qa, qb);
+            ld_tag2(kp, ka, kb);
+            ld_tag2(vp, va, vb);
             Spin sp;
-            for (;;) {
-                ld_tag2(q + 2 * lane, qa, qb);
-                if (qa.y == in_tag && qb.y == in_tag) break;
-                if (!sp.ok(P.err)) { ok = 0; break; }
+            while (!(qa.y == in_tag && qb.y == in_tag)) {
+                if (!sp.ok(P.err, WS_DQ, in_tag, qa.y)) { ok = 0; break; }
+                ld_tag2(q, qa, qb);
             }
-        }
-        const float2 qq = make_float2(__uint_as_float(qa.x), __uint_as_float(qb.x));
-        float2 k2[16], v2[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            k2[t] = make_float2(0.f, 0.f);
-            v2[t] = make_float2(0.f, 0.f);
-            if (t < npos && ok) {
-                const unsigned tt = phase_tag(D, P.dep_ph0 + t * P.dep_ph_stride + l * 5);
-                Spin sp;
-                for (;;) {
-                    uint2 a, b, c, e;
-                    ld_tag2(kv + (size_t)t * 2 * dd + 2 * lane, a, b);
-                    ld_tag2(kv + ((size_t)t * 2 + 1) * dd + 2 * lane, c, e);
-                    if (a.y == tt && b.y == tt && c.y == tt && e.y == tt) {
-                        k2[t] = make_float2(__uint_as_float(a.x), __uint_as_float(b.x));
-                        v2[t] = make_float2(__uint_as_float(c.x), __uint_as_float(e.x));
-                        break;
-                    }
-                    if (!sp.ok(P.err)) { ok = 0; break; }
-                }
+            while (ok && !(ka.y == tt && kb.y == tt && va.y == tt && vb.y == tt)) {
+                if (!sp.ok(P.err, WS_DKV, tt, ka.y)) { ok = 0; break; }
+                ld_tag2(kp, ka, kb);
+                ld_tag2(vp, va, vb);
             }
+            const float part = warp_sum(fmaf(__uint_as_float(qa.x), __uint_as_float(ka.x),
+                                             __uint_as_float(qb.x) * __uint_as_float(kb.x)));
+            if (lane == 0) sc[t] = part * scale;
+            vt = make_float2(__uint_as_float(va.x), __uint_as_float(vb.x));
         }
-        if (!__all_sync(0xffffffffu, ok)) return false;
-        float s = -INFINITY;
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            const float part = warp_sum(fmaf(qq.x, k2[t].x, qq.y * k2[t].y));
-            if (t == lane && t < npos) s = part * scale;
+        if (!csync_and(ok)) return false;
+        if (t < npos) {
+            float M = -INFINITY;
+            for (int u = 0; u < npos; ++u) M = fmaxf(M, sc[u]);
+            const float pt = expf(sc[t] - M);
+            pv[t * 64 + 2 * lane] = pt * vt.x;
+            pv[t * 64 + 2 * lane + 1] = pt * vt.y;
         }
-        const float M = warp_max(s);
-        const float pe = lane < npos ? expf(s - M) : 0.f;
-        const float inv = 1.f / warp_sum(pe);
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int t = 0; t < 16; ++t) {
-            const float pt = __shfl_sync(0xffffffffu, pe, t);
-            a0 = fmaf(pt, v2[t].x, a0);
-            a1 = fmaf(pt, v2[t].y, a1);
+        csync();
+        if (threadIdx.x < 64) {
+            const int e = threadIdx.x;
+            float M = -INFINITY;
+            for (int u = 0; u < npos; ++u) M = fmaxf(M, sc[u]);
+            float Z = 0.f, a = 0.f;
+            for (int u = 0; u < npos; ++u) {
+                Z += expf(sc[u] - M);
+                a += pv[u * 64 + e];
+            }
+            st_tag1(P.dat + (size_t)i * dd + h * 64 + e, __float_as_uint(a / Z), tag);
         }
-        st_tag2(P.dat + (size_t)i * dd + h * 64 + 2 * lane, a0 * inv, a1 * inv, tag);
+        csync();
     }
     return true;
 }
@@ -1273,7 +1347,7 @@ __device__ __forceinline__ bool run_phase(const Params& P, const Phase ph, int p
             }
             return gemv_phase<TW, BG>(P, ph, xs, n, sm, stage, EpiDQKV{ph.l, ph.j, tag});
         }
-        case PH_DATTN: return phase_dattn(P, ph.l, ph.j, n, in_tag, tag);
+        case PH_DATTN: return phase_dattn(P, ph.l, ph.j, n, in_tag, tag, sm);
         case PH_DO:
             return gemv_phase<TW, BG>(P, ph, XSrc{P.dat, dd, in_tag, nullptr, nullptr, 0, nullptr, 0}, n, sm, stage,
                                       EpiResid{P.u, dd, res_tag, tag});
