@@ -433,7 +433,7 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
         c->kfn[i] = g.weight_dtype == MFS_DTYPE_BF16 ? kernel_bf16(bg) : kernel_f32(bg);
         // ring, then one region used as GEMV partials + row values, attention
         // partials, or the step's embedding rows, whichever phase runs
-        const size_t gemv = (size_t)c->maxrows * bg * 17 * sizeof(float);
+        const size_t gemv = (size_t)c->maxrows * bg * (NWARP + 1) * sizeof(float);
         const size_t attn = (size_t)NWARP * (g.head_dim + 4) * sizeof(float);
         const size_t emb = (size_t)MFS_MAX_SLOTS * NSTREAM * sizeof(int);
         size_t region = gemv > attn ? gemv : attn;

@@ -7,12 +7,12 @@
 
 namespace mfs {
 
-constexpr int NT = 512;          // consumer threads per CTA (16 warps); one more warp produces
+constexpr int NT = 256;          // consumer threads per CTA (8 warps); one more warp produces
 constexpr int NWARP = NT / 32;
 constexpr int STAGE_BYTES = 24576;  // one weight ring stage
 constexpr int RPS_MAX = 16;      // rows per stage at most
 // Ring depth per batch group: the per-row partial sums grow with the group, the ring shrinks.
-__host__ __device__ constexpr unsigned nstage_for(int bg) { return bg <= 1 ? 8u : (bg == 2 ? 7u : 5u); }
+__host__ __device__ constexpr unsigned nstage_for(int bg) { return bg <= 2 ? 8u : 7u; }
 constexpr int SMEM_HEAD = 1024;  // mbarriers and scalars before the ring
 constexpr int NSTREAM = MFS_N_STREAMS;
 constexpr int NCHUNK_MAX = 32;   // attention split over the window, per (slot, head)

@@ -305,15 +305,15 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i)
 
 // ------------------------------------------------------------------ synchronisation
 
-// Barrier over the 16 consumer warps of the CTA (the producer warp never joins).
-__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+// Barrier over the consumer warps of the CTA (the producer warp never joins).
+__device__ __forceinline__ void csync() { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); }
 
 // Same barrier, returning whether the predicate held in every consumer thread.
 __device__ __forceinline__ bool csync_and(int pred)
 {
     int r;
-    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.and.pred q, 1, 512, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
-                 : "=r"(r) : "r"(pred) : "memory");
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\tbar.red.and.pred q, 1, %2, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r) : "r"(pred), "n"(NT) : "memory");
     return r != 0;
 }
 
@@ -369,7 +369,7 @@ struct Smem {
     int* ami;         // [NWARP]
     int* misc;        // [0] phase index (diagnostic stamps)
     char* ring;       // [nstage][STAGE_BYTES]
-    float* red;       // [maxrows][BG][16] per-K-slice partial sums of the CTA's rows
+    float* red;       // [maxrows][BG][NWARP] per-K-slice partial sums of the CTA's rows
     float* yf;        // [maxrows][BG] final row values of the CTA
     int* X;           // embedding rows of this step (aliases red)
     float* wbuf;      // attention partials of the 16 warps (aliases red)
@@ -387,7 +387,7 @@ __device__ __forceinline__ Smem smem_map(char* base, int maxrows, int BG)
     s.misc = (int*)(base + 672);
     s.ring = base + SMEM_HEAD;
     s.red = (float*)(s.ring + (size_t)nstage_for(BG) * STAGE_BYTES);
-    s.yf = s.red + (size_t)maxrows * BG * 16;
+    s.yf = s.red + (size_t)maxrows * BG * NWARP;
     s.X = (int*)s.red;
     s.wbuf = s.red;
     return s;
@@ -406,12 +406,12 @@ struct GemvCfg {
     int nwk, nwr, nvw, vpl;
 };
 
-// K-slices per row: the largest power of two <= 16 that leaves >= 32 vectors
-// (of 8 weights) per slice.
+// K-slices per row: the largest power of two <= NWARP that leaves >= 32
+// vectors (of 8 weights) per slice.
 __device__ __forceinline__ GemvCfg gemv_cfg(int K)
 {
     const int NV = K / 8;
-    int nwk = 16;
+    int nwk = NWARP;
     while (nwk > 1 && NV / nwk < 32) nwk >>= 1;
     GemvCfg c;
     c.nwk = nwk;
@@ -421,10 +421,14 @@ __device__ __forceinline__ GemvCfg gemv_cfg(int K)
     return c;
 }
 
+// vectors per lane, rounded up to an instantiated width
+__device__ __forceinline__ int vpl_class(int vpl) { return vpl <= 1 ? 1 : (vpl == 2 ? 2 : 6); }
+
+// batch rows per pass: the input slice (8 * vpl * rows floats) stays in registers
 template <int BG>
 __device__ __forceinline__ int group_size(int K)
 {
-    return gemv_cfg(K).vpl == 3 ? (BG < 2 ? BG : 2) : BG;
+    return vpl_class(gemv_cfg(K).vpl) <= 2 ? BG : (BG < 2 ? BG : 2);
 }
 
 // The weight matrix a phase streams, or false if it streams none.
@@ -749,7 +753,7 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
                 t += __shfl_xor_sync(0xffffffffu, t, 4);
                 t += __shfl_xor_sync(0xffffffffu, t, 2);
                 t += __shfl_xor_sync(0xffffffffu, t, 1);
-                if ((lane & 7) == 0 && rr < nr) sm.red[((size_t)(ra - r0 + rr) * BGV + b) * 16 + kw] = t;
+                if ((lane & 7) == 0 && rr < nr) sm.red[((size_t)(ra - r0 + rr) * BGV + b) * NWARP + kw] = t;
             }
         }
         __syncwarp();
@@ -760,7 +764,7 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
     // sum the K-slices in slice order
     for (int it = tid; it < (r1 - r0) * nb; it += NT) {
         const int rl = it / nb, b = it % nb;
-        const float* rp = sm.red + ((size_t)rl * BGV + b) * 16;
+        const float* rp = sm.red + ((size_t)rl * BGV + b) * NWARP;
         float y = 0.f;
         for (int k = 0; k < c.nwk; ++k) y += rp[k];
         sm.yf[(size_t)rl * BGV + b] = y;
@@ -1000,10 +1004,10 @@ __device__ __forceinline__ bool gemv_phase(const Params& P, const Phase& ph, con
         if (r1 > r0 || (xs.store && blockIdx.x == 0)) {
             const Pre pre = epi.pre(P, r0, r1, b0, nb);
             bool ok;
-            switch (c.vpl) {
+            switch (vpl_class(c.vpl)) {
                 case 1: ok = gemv_group<TW, 1, BG, BG>(P, ph, K, c, r0, r1, xs, b0, nb, sm, stage); break;
                 case 2: ok = gemv_group<TW, 2, BG, BG>(P, ph, K, c, r0, r1, xs, b0, nb, sm, stage); break;
-                default: ok = gemv_group<TW, 3, (BG < 2 ? BG : 2), BG>(P, ph, K, c, r0, r1, xs, b0, nb, sm, stage); break;
+                default: ok = gemv_group<TW, 6, (BG < 2 ? BG : 2), BG>(P, ph, K, c, r0, r1, xs, b0, nb, sm, stage); break;
             }
             if (!csync_and(ok && pre.ok)) return false;
             if (!csync_and(epi.apply(P, sm, r0, r1, b0, nb, bgv, pre))) return false;
@@ -1076,6 +1080,37 @@ __device__ __forceinline__ void phase_embed(const Params& P, int n, unsigned tag
 }
 
 // ------------------------------------------------------------------ S5 attention
+
+__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// While the QKV phase of layer l runs, the CTAs that will run that layer's
+// attention pull the older keys/values of their (row, head) windows into L2,
+// so the attention reads hit L2 instead of queueing behind the weight stream.
+// Only for windows small enough to sit in L2 (at most 32 MB per layer).
+template <typename TKV>
+__device__ __forceinline__ void prefetch_kv_windows(const Params& P, int l, int n)
+{
+    const StepDesc* D = P.desc;
+    const int H = P.H, hd = P.hd, d = P.d, W = P.W;
+    long long total = 0;
+    for (int i = 0; i < n; ++i) total += (long long)(D->pos[i] + 1 < W ? D->pos[i] + 1 : W);
+    if (total * H * hd * (long long)sizeof(TKV) * 2 > (32ll << 20)) return;
+    for (int item = blockIdx.x; item < n * H; item += P.G) {
+        const int i = item / H, h = item % H;
+        const int p = D->pos[i], slot = D->slot[i];
+        const int len = p + 1 < W ? p + 1 : W;
+        const int start = p - len + 1;
+        const long long base = ((long long)slot * P.L + l) * (long long)W * d + h * hd;
+        for (int k = threadIdx.x; k < 2 * (len - 1); k += NT) {
+            const int j = k >> 1;
+            const long long off = base + (long long)((start + j) % W) * d;
+            prefetch_l2((const TKV*)((k & 1) ? P.vc : P.kc) + off, (unsigned)(hd * sizeof(TKV)));
+        }
+    }
+}
 
 // One CTA per (batch row, head); its 16 warps split the window into 16
 // contiguous runs of keys (a split that depends on the window length only),
@@ -1206,9 +1241,9 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
 
 // ------------------------------------------------------------------ S9 depformer attention
 
-// One CTA per (batch row, head): keys of substeps 0..j, no rotation.  Warp t
-// loads key/value t (tag of that substep's QKV phase) together with the
-// query, so every load of the item is in flight at once; the softmax and the
+// One CTA per (batch row, head): keys of substeps 0..j, no rotation.  Warp w
+// loads keys/values w and w + NWARP (tag of that substep's QKV phase) with the
+// query, so the loads of the item are in flight together; the softmax and the
 // weighted sum run in key order in shared memory.
 __device__ __forceinline__ bool phase_dattn(const Params& P, int l, int j, int n, unsigned in_tag, unsigned tag,
                                             const Smem& sm)
@@ -1224,39 +1259,48 @@ __device__ __forceinline__ bool phase_dattn(const Params& P, int l, int j, int n
         const int i = item / dH, h = item % dH;
         const uint2* q = P.dq + (size_t)i * dd + h * 64 + 2 * lane;
         const uint2* kv = P.dkv + ((size_t)i * P.dL + l) * S * 2 * dd + h * 64 + 2 * lane;
-        const int t = warp;
         int ok = 1;
-        float2 vt = make_float2(0.f, 0.f);
-        if (t < npos) {
-            const unsigned tt = phase_tag(D, P.dep_ph0 + t * P.dep_ph_stride + l * 5);
-            const uint2* kp = kv + (size_t)t * 2 * dd;
-            const uint2* vp = kv + ((size_t)t * 2 + 1) * dd;
-            uint2 qa, qb, ka, kb, va, vb;
-            ld_tag2(q, qa, qb);
-            ld_tag2(kp, ka, kb);
-            ld_tag2(vp, va, vb);
-            Spin sp;
-            while (!(qa.y == in_tag && qb.y == in_tag)) {
-                if (!sp.ok(P.err, WS_DQ, in_tag, qa.y)) { ok = 0; break; }
+        constexpr int TPW = 16 / NWARP;  // keys per warp
+        float2 vt[TPW];
+#pragma unroll
+        for (int k = 0; k < TPW; ++k) {
+            const int t = warp + k * NWARP;
+            vt[k] = make_float2(0.f, 0.f);
+            if (t < npos && ok) {
+                const unsigned tt = phase_tag(D, P.dep_ph0 + t * P.dep_ph_stride + l * 5);
+                const uint2* kp = kv + (size_t)t * 2 * dd;
+                const uint2* vp = kv + ((size_t)t * 2 + 1) * dd;
+                uint2 qa, qb, ka, kb, va, vb;
                 ld_tag2(q, qa, qb);
-            }
-            while (ok && !(ka.y == tt && kb.y == tt && va.y == tt && vb.y == tt)) {
-                if (!sp.ok(P.err, WS_DKV, tt, ka.y)) { ok = 0; break; }
                 ld_tag2(kp, ka, kb);
                 ld_tag2(vp, va, vb);
+                Spin sp;
+                while (!(qa.y == in_tag && qb.y == in_tag)) {
+                    if (!sp.ok(P.err, WS_DQ, in_tag, qa.y)) { ok = 0; break; }
+                    ld_tag2(q, qa, qb);
+                }
+                while (ok && !(ka.y == tt && kb.y == tt && va.y == tt && vb.y == tt)) {
+                    if (!sp.ok(P.err, WS_DKV, tt, ka.y)) { ok = 0; break; }
+                    ld_tag2(kp, ka, kb);
+                    ld_tag2(vp, va, vb);
+                }
+                const float part = warp_sum(fmaf(__uint_as_float(qa.x), __uint_as_float(ka.x),
+                                                 __uint_as_float(qb.x) * __uint_as_float(kb.x)));
+                if (lane == 0) sc[t] = part * scale;
+                vt[k] = make_float2(__uint_as_float(va.x), __uint_as_float(vb.x));
             }
-            const float part = warp_sum(fmaf(__uint_as_float(qa.x), __uint_as_float(ka.x),
-                                             __uint_as_float(qb.x) * __uint_as_float(kb.x)));
-            if (lane == 0) sc[t] = part * scale;
-            vt = make_float2(__uint_as_float(va.x), __uint_as_float(vb.x));
         }
         if (!csync_and(ok)) return false;
-        if (t < npos) {
-            float M = -INFINITY;
-            for (int u = 0; u < npos; ++u) M = fmaxf(M, sc[u]);
-            const float pt = expf(sc[t] - M);
-            pv[t * 64 + 2 * lane] = pt * vt.x;
-            pv[t * 64 + 2 * lane + 1] = pt * vt.y;
+#pragma unroll
+        for (int k = 0; k < TPW; ++k) {
+            const int t = warp + k * NWARP;
+            if (t < npos) {
+                float M = -INFINITY;
+                for (int u = 0; u < npos; ++u) M = fmaxf(M, sc[u]);
+                const float pt = expf(sc[t] - M);
+                pv[t * 64 + 2 * lane] = pt * vt[k].x;
+                pv[t * 64 + 2 * lane + 1] = pt * vt[k].y;
+            }
         }
         csync();
         if (threadIdx.x < 64) {
@@ -1321,6 +1365,7 @@ __device__ __forceinline__ bool run_phase(const Params& P, const Phase ph, int p
     switch (ph.type) {
         case PH_EMBED: phase_embed<TW>(P, n, tag, sm); return true;
         case PH_QKV:
+            prefetch_kv_windows<TKV>(P, ph.l, n);
             return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, in_tag, P.attn_norm + (size_t)ph.l * d, nullptr, 0, nullptr, 0},
                                       n, sm, stage, EpiQKV<TKV>{ph.l, tag});
         case PH_ATTN: return phase_attn<TKV>(P, ph.l, n, in_tag, tag, sm);
