@@ -45,14 +45,9 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p)
     return r;
 }
 
-// L2-only load (keys/values written by earlier steps).
-__device__ __forceinline__ uint4 ld_cg16(const void* p)
-{
-    uint4 r;
-    asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p) : "memory");
-    return r;
-}
+// L2-only load of keys/values written by earlier launches (no ordering
+// constraint, so the compiler keeps many of these in flight).
+__device__ __forceinline__ uint4 ld_cg16(const void* p) { return __ldcg(reinterpret_cast<const uint4*>(p)); }
 
 __device__ __forceinline__ int ld_cg_int(const int* p) { return __ldcg(p); }
 
@@ -1151,6 +1146,7 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
                  tag8_take(vt, P.vcur + (size_t)i * d + h * hd + gl * 8, in_tag, vcur, P.err);
 #pragma unroll
         for (int e = 0; e < 8; ++e) qv[e] *= scale;
+        if (P.ptime && item == blockIdx.x) stamp(P, sm.misc[0], 1);
         float m = -INFINITY, lsum = 0.f, acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
@@ -1213,6 +1209,7 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
             for (int e = 0; e < 8; ++e) acc[e] = acc[e] * c1 + a2[e] * c2;
             m = M;
         }
+        if (P.ptime && item == blockIdx.x) stamp(P, sm.misc[0], 2);
         float* wb = sm.wbuf + (size_t)warp * wstride;
         if (lane < LPP) {
             if (lane == 0) { wb[0] = m; wb[1] = lsum; }

@@ -13,7 +13,8 @@ from typing import Optional, Sequence
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmfs.so")
+# MFS_LIBRARY selects another build of the same library (same ABI).
+LIB_PATH = os.environ.get("MFS_LIBRARY") or os.path.join(_HERE, "libmfs.so")
 
 MFS_OK = 0
 STATUS = {-1: "MFS_E_ARG", -2: "MFS_E_SLOT", -3: "MFS_E_TOKEN", -4: "MFS_E_RANGE", -5: "MFS_E_STATE",
