@@ -266,6 +266,17 @@ __device__ __forceinline__ bool tag8_take(const uint2 (&e)[8], const uint2* p, u
     return wait_tag8(p, tag, f, err);
 }
 
+// Two IEEE fp32 FMAs in one instruction: c = a * b + c lane by lane.
+__device__ __forceinline__ void ffma2(float2& c, float a0, float a1, float b0, float b1)
+{
+    unsigned long long ra, rb, rc;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b0), "f"(b1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(rc) : "l"(ra), "l"(rb));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(c.x), "=f"(c.y) : "l"(rc));
+}
+
 // ------------------------------------------------------------------ reductions
 
 __device__ __forceinline__ float warp_sum(float v)
@@ -347,10 +358,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* b, unsigned parity, int* err
     }
 }
 
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar)
+// L2 policies: streamed weights are evicted first, so that activations and
+// prefetched keys/values stay resident.
+__device__ __forceinline__ uint64_t l2_evict_first()
 {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar, uint64_t pol)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol) : "memory");
 }
 
 // ------------------------------------------------------------------ shared memory map
@@ -468,6 +495,7 @@ template <typename TW, int BG>
 __device__ __forceinline__ void producer(const Params& P, int ph0, int ph1, int n, const Smem& sm)
 {
     constexpr unsigned NS = nstage_for(BG);
+    const uint64_t pol = l2_evict_first();
     unsigned s = 0;
     bool ok = true;
     for (int ph = ph0; ph < ph1 && ok; ++ph) {
@@ -485,7 +513,7 @@ __device__ __forceinline__ void producer(const Params& P, int ph0, int ph1, int 
                 const int slot = (int)(s % NS);
                 if (!mbar_wait(&sm.empty[slot], ((s / NS) & 1u) ^ 1u, P.err, WS_EMPTY)) { ok = false; break; }
                 mbar_expect_tx(&sm.full[slot], bytes);
-                bulk_g2s(sm.ring + (size_t)slot * STAGE_BYTES, W + (size_t)r * K, bytes, &sm.full[slot]);
+                bulk_g2s(sm.ring + (size_t)slot * STAGE_BYTES, W + (size_t)r * K, bytes, &sm.full[slot], pol);
             }
         }
     }
@@ -708,11 +736,12 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
         if (!mbar_wait(&sm.full[slot], (stage / NS) & 1u, P.err, WS_FULL)) return false;
         const TW* ring = (const TW*)(sm.ring + (size_t)slot * STAGE_BYTES);
         for (int c0 = rw; c0 < nr; c0 += 4 * c.nwr) {
-            float acc[4][BGV];
+            // even and odd elements accumulate separately (packed fp32 FMAs)
+            float2 acc2[4][BGV];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int b = 0; b < BGV; ++b) acc[q][b] = 0.f;
+                for (int b = 0; b < BGV; ++b) acc2[q][b] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int rr = c0 + q * c.nwr;
@@ -726,11 +755,16 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
 #pragma unroll
                             for (int b = 0; b < BGV; ++b)
 #pragma unroll
-                                for (int e = 0; e < 8; ++e) acc[q][b] = fmaf(f[e], xr[t][b][e], acc[q][b]);
+                                for (int e = 0; e < 8; e += 2) ffma2(acc2[q][b], f[e], f[e + 1], xr[t][b][e], xr[t][b][e + 1]);
                         }
                     }
                 }
             }
+            float acc[4][BGV];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int b = 0; b < BGV; ++b) acc[q][b] = acc2[q][b].x + acc2[q][b].y;
             // transposed butterfly: lanes 0, 8, 16, 24 end with the sums of rows 0..3
             const int myq = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
             const int rr = c0 + myq * c.nwr;
@@ -1076,9 +1110,9 @@ __device__ __forceinline__ void phase_embed(const Params& P, int n, unsigned tag
 
 // ------------------------------------------------------------------ S5 attention
 
-__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes)
+__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes, uint64_t pol)
 {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes), "l"(pol) : "memory");
 }
 
 // While the QKV phase of layer l runs, the CTAs that will run that layer's
@@ -1093,6 +1127,7 @@ __device__ __forceinline__ void prefetch_kv_windows(const Params& P, int l, int 
     long long total = 0;
     for (int i = 0; i < n; ++i) total += (long long)(D->pos[i] + 1 < W ? D->pos[i] + 1 : W);
     if (total * H * hd * (long long)sizeof(TKV) * 2 > (32ll << 20)) return;
+    const uint64_t pol = l2_evict_last();
     for (int item = blockIdx.x; item < n * H; item += P.G) {
         const int i = item / H, h = item % H;
         const int p = D->pos[i], slot = D->slot[i];
@@ -1102,7 +1137,7 @@ __device__ __forceinline__ void prefetch_kv_windows(const Params& P, int l, int 
         for (int k = threadIdx.x; k < 2 * (len - 1); k += NT) {
             const int j = k >> 1;
             const long long off = base + (long long)((start + j) % W) * d;
-            prefetch_l2((const TKV*)((k & 1) ? P.vc : P.kc) + off, (unsigned)(hd * sizeof(TKV)));
+            prefetch_l2((const TKV*)((k & 1) ? P.vc : P.kc) + off, (unsigned)(hd * sizeof(TKV)), pol);
         }
     }
 }
