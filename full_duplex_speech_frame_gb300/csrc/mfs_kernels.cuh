@@ -735,7 +735,30 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
         const int slot = (int)(stage % NS);
         if (!mbar_wait(&sm.full[slot], (stage / NS) & 1u, P.err, WS_FULL)) return false;
         const TW* ring = (const TW*)(sm.ring + (size_t)slot * STAGE_BYTES);
-        for (int c0 = rw; c0 < nr; c0 += 4 * c.nwr) {
+        // copy this warp's rows of the stage into registers, release the stage at
+        // once (the producer refills it while the arithmetic runs), then compute
+        constexpr int RW = VPL <= 2 ? 8 : 2;   // rows per warp per stage, at most
+        constexpr int U4 = sizeof(TW) == 2 ? 1 : 2;  // 16-byte words per vector of 8 weights
+        uint4 wv[RW][VPL][U4];
+#pragma unroll
+        for (int q = 0; q < RW; ++q) {
+            const int rr = rw + q * c.nwr;
+#pragma unroll
+            for (int t = 0; t < VPL; ++t) {
+                const int v = v_begin + lane + 32 * t;
+#pragma unroll
+                for (int h = 0; h < U4; ++h) {
+                    wv[q][t][h] = make_uint4(0u, 0u, 0u, 0u);
+                    if (rr < nr && v < v_end)
+                        wv[q][t][h] = *reinterpret_cast<const uint4*>(ring + (size_t)rr * K + (size_t)v * 8 + h * 4);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[slot]);
+#pragma unroll
+        for (int q0 = 0; q0 < RW; q0 += 4) {
+            if (rw + q0 * c.nwr < nr) {  // warp-uniform
             // even and odd elements accumulate separately (packed fp32 FMAs)
             float2 acc2[4][BGV];
 #pragma unroll
@@ -744,14 +767,22 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
                 for (int b = 0; b < BGV; ++b) acc2[q][b] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const int rr = c0 + q * c.nwr;
+                const int rr = rw + (q0 + q) * c.nwr;
                 if (rr < nr) {
 #pragma unroll
                     for (int t = 0; t < VPL; ++t) {
                         const int v = v_begin + lane + 32 * t;
                         if (v < v_end) {
                             float f[8];
-                            WV<TW>::lds8(ring + (size_t)rr * K + (size_t)v * 8, f);
+                            if (U4 == 1) {
+                                const uint4 w4 = wv[q0 + q][t][0];
+                                f[0] = bf_lo(w4.x); f[1] = bf_hi(w4.x); f[2] = bf_lo(w4.y); f[3] = bf_hi(w4.y);
+                                f[4] = bf_lo(w4.z); f[5] = bf_hi(w4.z); f[6] = bf_lo(w4.w); f[7] = bf_hi(w4.w);
+                            } else {
+                                const uint4 a = wv[q0 + q][t][0], b4 = wv[q0 + q][t][U4 - 1];
+                                f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y); f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
+                                f[4] = __uint_as_float(b4.x); f[5] = __uint_as_float(b4.y); f[6] = __uint_as_float(b4.z); f[7] = __uint_as_float(b4.w);
+                            }
 #pragma unroll
                             for (int b = 0; b < BGV; ++b)
 #pragma unroll
@@ -765,9 +796,9 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
             for (int q = 0; q < 4; ++q)
 #pragma unroll
                 for (int b = 0; b < BGV; ++b) acc[q][b] = acc2[q][b].x + acc2[q][b].y;
-            // transposed butterfly: lanes 0, 8, 16, 24 end with the sums of rows 0..3
+            // transposed butterfly: lanes 0, 8, 16, 24 end with the sums of rows q0..q0+3
             const int myq = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
-            const int rr = c0 + myq * c.nwr;
+            const int rr = rw + (q0 + myq) * c.nwr;
 #pragma unroll
             for (int b = 0; b < BGV; ++b) {
                 const bool hi16 = (lane & 16) != 0;
@@ -784,9 +815,8 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
                 t += __shfl_xor_sync(0xffffffffu, t, 1);
                 if ((lane & 7) == 0 && rr < nr) sm.red[((size_t)(ra - r0 + rr) * BGV + b) * NWARP + kw] = t;
             }
+            }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
     if (P.ptime) stamp(P, sm.misc[0], 2);
     csync();
