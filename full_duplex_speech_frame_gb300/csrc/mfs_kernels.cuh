@@ -759,12 +759,15 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
 #pragma unroll
         for (int q0 = 0; q0 < RW; q0 += 4) {
             if (rw + q0 * c.nwr < nr) {  // warp-uniform
-            // even and odd elements accumulate separately (packed fp32 FMAs)
-            float2 acc2[4][BGV];
+            // independent packed accumulators per (row, vector): even and odd
+            // elements of each vector accumulate separately, combined in fixed order
+            float2 acc2[4][BGV][VPL];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int b = 0; b < BGV; ++b) acc2[q][b] = make_float2(0.f, 0.f);
+                for (int b = 0; b < BGV; ++b)
+#pragma unroll
+                    for (int t = 0; t < VPL; ++t) acc2[q][b][t] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int rr = rw + (q0 + q) * c.nwr;
@@ -786,7 +789,7 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
 #pragma unroll
                             for (int b = 0; b < BGV; ++b)
 #pragma unroll
-                                for (int e = 0; e < 8; e += 2) ffma2(acc2[q][b], f[e], f[e + 1], xr[t][b][e], xr[t][b][e + 1]);
+                                for (int e = 0; e < 8; e += 2) ffma2(acc2[q][b][t], f[e], f[e + 1], xr[t][b][e], xr[t][b][e + 1]);
                         }
                     }
                 }
@@ -795,7 +798,12 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int b = 0; b < BGV; ++b) acc[q][b] = acc2[q][b].x + acc2[q][b].y;
+                for (int b = 0; b < BGV; ++b) {
+                    float a = 0.f;
+#pragma unroll
+                    for (int t = 0; t < VPL; ++t) a += acc2[q][b][t].x + acc2[q][b][t].y;
+                    acc[q][b] = a;
+                }
             // transposed butterfly: lanes 0, 8, 16, 24 end with the sums of rows q0..q0+3
             const int myq = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
             const int rr = rw + (q0 + myq) * c.nwr;
