@@ -419,7 +419,7 @@ __device__ __forceinline__ Smem smem_map(char* base, int maxrows, int BG)
 // ready, 2 last weight stage consumed, 3 end of the phase).
 __device__ __forceinline__ void stamp(const Params& P, int ph, int k)
 {
-    if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) P.ptime[(size_t)ph * 8 + k] = globaltimer_ns();
+    if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) P.ptime[(size_t)ph * 4 + k] = globaltimer_ns();
 }
 
 // ------------------------------------------------------------------ GEMV schedule (producer and consumers)
@@ -595,11 +595,9 @@ __device__ __forceinline__ bool dep_select_inputs(const Params& P, int j, unsign
 
 // Consume one batch group [b0, b0+nb) of a matrix-vector phase: leaves the
 // CTA's row values in sm.yf[(r - r0) * bgv + b].  `stage` counts ring stages.
-// Not inlined: every matrix-vector phase type shares this code, which keeps
-// the hot loop resident in the instruction caches.
 template <typename TW, int VPL, int BGV, int BG_OF_STAGES>
-__device__ __noinline__ bool gemv_group(const Params& P, const Phase& ph, int K, const GemvCfg& c, int r0, int r1,
-                                        const XSrc& xs, int b0, int nb, const Smem& sm, unsigned& stage)
+__device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int K, const GemvCfg& c, int r0, int r1,
+                                           const XSrc& xs, int b0, int nb, const Smem& sm, unsigned& stage)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int kw = warp % c.nwk, rw = warp / c.nwk;
@@ -735,49 +733,85 @@ __device__ __noinline__ bool gemv_group(const Params& P, const Phase& ph, int K,
     for (int ra = r0; ra < r1; ra += rps, ++stage) {
         const int nr = min(rps, r1 - ra);
         const int slot = (int)(stage % NS);
-        const unsigned long long tw0 = P.ptime ? globaltimer_ns() : 0ull;
         if (!mbar_wait(&sm.full[slot], (stage / NS) & 1u, P.err, WS_FULL)) return false;
-        if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) {
-            // diagnostics: time CTA 0 spent waiting for weight stages, and their count
-            P.ptime[(size_t)sm.misc[0] * 8 + 4] += globaltimer_ns() - tw0;
-            P.ptime[(size_t)sm.misc[0] * 8 + 5] += 1;
-        }
         const TW* ring = (const TW*)(sm.ring + (size_t)slot * STAGE_BYTES);
-        // this warp takes rows rw, rw + nwr, ... of the stage, four at a time
-        for (int c0 = rw; c0 < nr; c0 += 4 * c.nwr) {
-            float2 acc2[4][BGV];  // even and odd elements accumulate separately
+        // copy this warp's rows of the stage into registers, release the stage at
+        // once (the producer refills it while the arithmetic runs), then compute
+        constexpr int RW = VPL <= 2 ? 8 : 2;   // rows per warp per stage, at most
+        constexpr int U4 = sizeof(TW) == 2 ? 1 : 2;  // 16-byte words per vector of 8 weights
+        uint4 wv[RW][VPL][U4];
+#pragma unroll
+        for (int q = 0; q < RW; ++q) {
+            const int rr = rw + q * c.nwr;
+#pragma unroll
+            for (int t = 0; t < VPL; ++t) {
+                const int v = v_begin + lane + 32 * t;
+#pragma unroll
+                for (int h = 0; h < U4; ++h) {
+                    wv[q][t][h] = make_uint4(0u, 0u, 0u, 0u);
+                    if (rr < nr && v < v_end)
+                        wv[q][t][h] = *reinterpret_cast<const uint4*>(ring + (size_t)rr * K + (size_t)v * 8 + h * 4);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[slot]);
+#pragma unroll
+        for (int q0 = 0; q0 < RW; q0 += 4) {
+            if (rw + q0 * c.nwr < nr) {  // warp-uniform
+            // independent packed accumulators per (row, vector): even and odd
+            // elements of each vector accumulate separately, combined in fixed order
+            float2 acc2[4][BGV][VPL];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int b = 0; b < BGV; ++b) acc2[q][b] = make_float2(0.f, 0.f);
+                for (int b = 0; b < BGV; ++b)
+#pragma unroll
+                    for (int t = 0; t < VPL; ++t) acc2[q][b][t] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const int rr = c0 + q * c.nwr;
+                const int rr = rw + (q0 + q) * c.nwr;
                 if (rr < nr) {
 #pragma unroll
                     for (int t = 0; t < VPL; ++t) {
                         const int v = v_begin + lane + 32 * t;
                         if (v < v_end) {
                             float f[8];
-                            WV<TW>::lds8(ring + (size_t)rr * K + (size_t)v * 8, f);
+                            if (U4 == 1) {
+                                const uint4 w4 = wv[q0 + q][t][0];
+                                f[0] = bf_lo(w4.x); f[1] = bf_hi(w4.x); f[2] = bf_lo(w4.y); f[3] = bf_hi(w4.y);
+                                f[4] = bf_lo(w4.z); f[5] = bf_hi(w4.z); f[6] = bf_lo(w4.w); f[7] = bf_hi(w4.w);
+                            } else {
+                                const uint4 a = wv[q0 + q][t][0], b4 = wv[q0 + q][t][U4 - 1];
+                                f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y); f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
+                                f[4] = __uint_as_float(b4.x); f[5] = __uint_as_float(b4.y); f[6] = __uint_as_float(b4.z); f[7] = __uint_as_float(b4.w);
+                            }
 #pragma unroll
                             for (int b = 0; b < BGV; ++b)
 #pragma unroll
-                                for (int e = 0; e < 8; e += 2) ffma2(acc2[q][b], f[e], f[e + 1], xr[t][b][e], xr[t][b][e + 1]);
+                                for (int e = 0; e < 8; e += 2) ffma2(acc2[q][b][t], f[e], f[e + 1], xr[t][b][e], xr[t][b][e + 1]);
                         }
                     }
                 }
             }
-            // transposed butterfly: lanes 0, 8, 16, 24 end with the sums of rows 0..3
+            float acc[4][BGV];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int b = 0; b < BGV; ++b) {
+                    float a = 0.f;
+#pragma unroll
+                    for (int t = 0; t < VPL; ++t) a += acc2[q][b][t].x + acc2[q][b][t].y;
+                    acc[q][b] = a;
+                }
+            // transposed butterfly: lanes 0, 8, 16, 24 end with the sums of rows q0..q0+3
             const int myq = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
-            const int rr = c0 + myq * c.nwr;
+            const int rr = rw + (q0 + myq) * c.nwr;
 #pragma unroll
             for (int b = 0; b < BGV; ++b) {
                 const bool hi16 = (lane & 16) != 0;
-                const float a0 = acc2[0][b].x + acc2[0][b].y, a1 = acc2[1][b].x + acc2[1][b].y;
-                const float a2 = acc2[2][b].x + acc2[2][b].y, a3 = acc2[3][b].x + acc2[3][b].y;
-                float s0 = hi16 ? a2 : a0, s1 = hi16 ? a3 : a1;
-                const float o0 = hi16 ? a0 : a2, o1 = hi16 ? a1 : a3;
+                float s0 = hi16 ? acc[2][b] : acc[0][b], s1 = hi16 ? acc[3][b] : acc[1][b];
+                const float o0 = hi16 ? acc[0][b] : acc[2][b], o1 = hi16 ? acc[1][b] : acc[3][b];
                 s0 += __shfl_xor_sync(0xffffffffu, o0, 16);
                 s1 += __shfl_xor_sync(0xffffffffu, o1, 16);
                 const bool hi8 = (lane & 8) != 0;
@@ -789,9 +823,8 @@ __device__ __noinline__ bool gemv_group(const Params& P, const Phase& ph, int K,
                 t += __shfl_xor_sync(0xffffffffu, t, 1);
                 if ((lane & 7) == 0 && rr < nr) sm.red[((size_t)(ra - r0 + rr) * BGV + b) * NWARP + kw] = t;
             }
+            }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
     if (P.ptime) stamp(P, sm.misc[0], 2);
     csync();
