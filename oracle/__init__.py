@@ -45,7 +45,8 @@ class _Cfg(ctypes.Structure):
         "d", "n_layers", "n_heads", "head_dim", "ffn", "text_vocab", "card", "n_q", "window",
         "max_pos", "dep_d", "dep_layers", "dep_heads", "dep_head_dim", "dep_ffn", "dep_steps")] + [
         ("delays", ctypes.c_int * 17), ("rope_theta", ctypes.c_double), ("eps", ctypes.c_double),
-        ("weight_dtype", ctypes.c_int), ("max_slots", ctypes.c_int), ("brute_force", ctypes.c_int)]
+        ("weight_dtype", ctypes.c_int), ("max_slots", ctypes.c_int), ("brute_force", ctypes.c_int),
+        ("kv_dtype", ctypes.c_int)]
 
 
 def _load():
@@ -115,6 +116,7 @@ class Oracle:
         c.eps = float(s.eps)
         c.weight_dtype = 1 if s.weight_dtype == "bf16" else 0
         c.brute_force = 1 if brute_force else 0
+        c.kv_dtype = 1 if s.kv_dtype == "bf16" else 0
         self.shape = s
         self._lib = _load()
         self._h = self._lib.orc_create(ctypes.byref(c))

@@ -36,6 +36,11 @@
  *  S10 outputs: the text token of frame p and, per audio stream, the code of
  *      frame p-delay[k] (-1 for frames before 0); p advances by one.
  *
+ * Keys (after rotation) and values are cached in the cache's dtype: fp64, or
+ * bf16 (round to nearest even) as the model's own KV cache is held
+ * (SGLang-Omni PersonaPlex pipeline, "Windowed KV": BF16 KV per request);
+ * every key, the current position's included, is read back from the cache.
+ *
  * The ring of keys/values is kept two ways: storage at position mod W (the
  * default), or a full history of every position masked to the last W
  * (brute_force = 1).  Both read keys in ascending absolute position.
@@ -57,6 +62,7 @@ typedef struct {
     int weight_dtype; /* 0 = fp32, 1 = bf16 */
     int max_slots;
     int brute_force;  /* 1: keep every position, mask to the last W */
+    int kv_dtype;     /* 0 = fp64 cache, 1 = keys and values rounded to bf16 when cached */
 } orc_config;
 
 typedef struct {
@@ -91,6 +97,17 @@ static double bf16_bits_to_double(uint16_t b)
     float f;
     memcpy(&f, &u, 4);
     return (double)f;
+}
+
+/* x rounded to the nearest bfloat16 (8 significant bits, ties to even), as a
+ * double.  Only normal bf16 magnitudes occur in a key or value cache. */
+static double round_bf16(double x)
+{
+    if (x == 0.0 || !isfinite(x)) return x;
+    int e;
+    double m = frexp(x, &e);          /* x = m * 2^e, 0.5 <= |m| < 1 */
+    double r = nearbyint(ldexp(m, 8)); /* default rounding mode: to nearest, ties to even */
+    return ldexp(r, e - 8);
 }
 
 /* element i of a weight tensor stored in the model's weight dtype */
@@ -371,11 +388,18 @@ static void attend(orc* o, orc_slot* s, int l, int p, double* q, double* k, cons
         orc_rope(q + hh * hd, hd, p, c->rope_theta);
         orc_rope(k + hh * hd, hd, p, c->rope_theta);
     }
+    if (c->kv_dtype == 1) {
+        /* the cache holds keys and values in bf16: the current position is read
+         * back from it like every other */
+        for (int i = 0; i < d; ++i) { k[i] = round_bf16(k[i]); }
+    }
     int row = c->brute_force ? p : mod(p, W);
     double* Kl = s->K + (size_t)l * layer_stride;
     double* Vl = s->V + (size_t)l * layer_stride;
     memcpy(Kl + (size_t)row * d, k, sizeof(double) * (size_t)d);
     memcpy(Vl + (size_t)row * d, v, sizeof(double) * (size_t)d);
+    if (c->kv_dtype == 1)
+        for (int i = 0; i < d; ++i) Vl[(size_t)row * d + i] = round_bf16(Vl[(size_t)row * d + i]);
     double* Kw = (double*)malloc(sizeof(double) * (size_t)len * (size_t)d);
     double* Vw = (double*)malloc(sizeof(double) * (size_t)len * (size_t)d);
     for (int j = 0; j < len; ++j) {

@@ -63,6 +63,9 @@ def forward(s, w, tokens: np.ndarray):
         q = rotate(q.reshape(T, H, hd), s.rope_theta).transpose(0, 1)
         k = rotate(k.reshape(T, H, hd), s.rope_theta).transpose(0, 1)
         v = v.reshape(T, H, hd).transpose(0, 1)
+        if s.kv_dtype == "bf16":  # the cache holds rotated keys and values in bf16
+            k = k.to(torch.bfloat16).to(torch.float64)
+            v = v.to(torch.bfloat16).to(torch.float64)
         o = F.scaled_dot_product_attention(q, k, v, attn_mask=mask)
         x = x + F.linear(o.transpose(0, 1).reshape(T, d), W[f"layers.{l}.wo"])
         a = F.rms_norm(x, (d,), W[f"layers.{l}.ffn_norm"], s.eps)
