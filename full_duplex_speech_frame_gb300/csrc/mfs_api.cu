@@ -802,8 +802,8 @@ extern "C" int mfs_set_timing(mfs_ctx* c, int flags)
     c->timing = (flags & 1) != 0;
     c->stamps = (flags & 2) != 0;
     if (c->stamps && !c->d_ptime) {
-        CK(cudaMalloc((void**)&c->d_ptime, (size_t)(c->nphase + 1) * 4 * sizeof(unsigned long long)));
-        CK(cudaMemset(c->d_ptime, 0, (size_t)(c->nphase + 1) * 4 * sizeof(unsigned long long)));
+        CK(cudaMalloc((void**)&c->d_ptime, (size_t)(c->nphase + 1) * 8 * sizeof(unsigned long long)));
+        CK(cudaMemset(c->d_ptime, 0, (size_t)(c->nphase + 1) * 8 * sizeof(unsigned long long)));
     }
     return MFS_OK;
 }
@@ -813,9 +813,10 @@ extern "C" int mfs_phase_times(mfs_ctx* c, uint64_t* ns, int cap)
     if (!c || !ns) return MFS_E_ARG;
     if (!c->d_ptime) return fail(c, MFS_E_STATE, "phase stamps were never enabled");
     CK(cudaStreamSynchronize(c->stream));
-    const int cnt = (c->last_nph + 1) * 4;
+    const int cnt = (c->last_nph + 1) * 8;
     if (cap < cnt) return fail(c, MFS_E_ARG, "need room for %d stamps", cnt);
     CK(cudaMemcpy(ns, c->d_ptime, (size_t)cnt * sizeof(uint64_t), cudaMemcpyDeviceToHost));
+    CK(cudaMemset(c->d_ptime, 0, (size_t)cnt * sizeof(uint64_t)));  // the wait totals restart
     return cnt;
 }
 

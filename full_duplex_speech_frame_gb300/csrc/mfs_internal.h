@@ -108,7 +108,7 @@ struct Params {
     int* err;        // sticky device error (DeviceError)
     int* err_seq;    // step sequence number that raised it
     const Phase* phases;
-    unsigned long long* ptime;  // optional: CTA 0 timer stamps, [nphase + 1][4]
+    unsigned long long* ptime;  // optional: CTA 0 timer stamps and stage-wait sums, [nphase + 1][8]
 };
 
 // Kernel entry points, one per (weight dtype, batch group).  Defined in the

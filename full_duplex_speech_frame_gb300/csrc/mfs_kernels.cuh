@@ -419,7 +419,7 @@ __device__ __forceinline__ Smem smem_map(char* base, int maxrows, int BG)
 // ready, 2 last weight stage consumed, 3 end of the phase).
 __device__ __forceinline__ void stamp(const Params& P, int ph, int k)
 {
-    if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) P.ptime[(size_t)ph * 4 + k] = globaltimer_ns();
+    if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) P.ptime[(size_t)ph * 8 + k] = globaltimer_ns();
 }
 
 // ------------------------------------------------------------------ GEMV schedule (producer and consumers)
@@ -733,7 +733,13 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
     for (int ra = r0; ra < r1; ra += rps, ++stage) {
         const int nr = min(rps, r1 - ra);
         const int slot = (int)(stage % NS);
+        const unsigned long long tw0 = P.ptime ? globaltimer_ns() : 0ull;
         if (!mbar_wait(&sm.full[slot], (stage / NS) & 1u, P.err, WS_FULL)) return false;
+        if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) {
+            // diagnostics: time CTA 0 spent waiting for weight stages, and their count
+            P.ptime[(size_t)sm.misc[0] * 8 + 4] += globaltimer_ns() - tw0;
+            P.ptime[(size_t)sm.misc[0] * 8 + 5] += 1;
+        }
         const TW* ring = (const TW*)(sm.ring + (size_t)slot * STAGE_BYTES);
         // copy this warp's rows of the stage into registers, release the stage at
         // once (the producer refills it while the arithmetic runs), then compute

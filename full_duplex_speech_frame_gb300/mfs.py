@@ -233,12 +233,12 @@ def mfs_set_timing(ctx: Ctx, flags) -> None:
 
 
 def mfs_phase_times(ctx: Ctx) -> np.ndarray:
-    """Global-timer stamps (ns) of the last step, [phases + 1, 4] (see include/mfs.h)."""
+    """Diagnostic timer values of the last step(s), [phases + 1, 8] (see include/mfs.h)."""
     buf = np.zeros(16384, np.uint64)
     rc = _lib.mfs_phase_times(ctx.handle, buf.ctypes.data, buf.size)
     if rc < 0:
         _check(ctx, rc)
-    return buf[:rc].reshape(-1, 4).copy()
+    return buf[:rc].reshape(-1, 8).copy()
 
 
 def mfs_kernel_time(ctx: Ctx):

@@ -157,12 +157,13 @@ int mfs_launches_per_step(const mfs_ctx* ctx);
 /* Kernel timing.  flags bit 0: every step records a CUDA event pair on the
  * context's stream around its kernel launch(es); mfs_kernel_time waits for
  * the stream, returns the summed device time (ms) and the number of steps
- * timed since the previous call, and starts a new sum.  flags bit 1: the
- * kernel stamps the GPU's global timer four times per phase (start, inputs
- * ready, weights consumed, before the grid barrier; 0 where a point does not
- * apply) and once at the end; mfs_phase_times copies the stamps (ns) of the
- * last step into ns[0..count) as [phases + 1][4] and returns count, or a
- * negative status. */
+ * timed since the previous call, and starts a new sum.  flags bit 1: CTA 0
+ * records, per phase, 8 values: GPU timer stamps (ns) at the start, when the
+ * inputs are ready, when the last weight stage is consumed, at the end (0
+ * where a point does not apply), then the ns spent waiting for weight stages
+ * and the number of stages, summed since the last read; mfs_phase_times
+ * copies [phases + 1][8] values into ns, restarts the sums and returns the
+ * count, or a negative status. */
 int mfs_set_timing(mfs_ctx* ctx, int flags);
 int mfs_kernel_time(mfs_ctx* ctx, double* total_ms, int* steps);
 int mfs_phase_times(mfs_ctx* ctx, uint64_t* ns, int cap);
