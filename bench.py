@@ -193,7 +193,7 @@ def cpu_oracle_sample(frames=6, prompt=8):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    frames = max(1, min(args.steps, 6))
+    frames = max(1, min(args.steps, 30))
     cb = cpu_oracle_sample(frames=frames)
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": args.gpus,
             "steps": frames, "warmup": 0, "ms_per_step": 1000.0 / cb["value"], "higher_is_better": True,
@@ -301,7 +301,7 @@ def run_gpu(args, rank, world):
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_sample(frames=3)
+        line["cpu_baseline"] = cpu_oracle_sample(frames=40)
     print(json.dumps(line), flush=True)
 
 
