@@ -60,10 +60,12 @@ def read_peaks():
 
 
 def kernel_source_digest():
+    """Digest of the step kernel's device sources (its template, internal layout
+    and the instantiation units), which decide its DRAM traffic."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "full_duplex_speech_frame_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name in ("mfs_kernels.cuh", "mfs_internal.h") or (name.startswith("mfs_k_") and name.endswith(".cu")):
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode())
                 h.update(f.read())
@@ -81,10 +83,10 @@ def recorded_traffic(workload):
         if ":" in line:
             k, v = line.split(":", 1)
             vals[k.strip()] = v.strip()
-    if vals.get("kernel_source_digest") != kernel_source_digest():
+    if (vals.get("kernel_source_digest") or "?").split()[0] != kernel_source_digest():
         return None
     try:
-        return float(vals["dram_bytes_per_launch"])
+        return float(vals["dram_bytes_per_launch"].split()[0])
     except (KeyError, ValueError):
         return None
 
