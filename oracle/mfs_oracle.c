@@ -38,7 +38,7 @@
  *
  * Keys (after rotation) and values are cached in the cache's dtype: fp64, or
  * bf16 (round to nearest even) as the model's own KV cache is held
- * (SGLang-Omni PersonaPlex pipeline, "Windowed KV": BF16 KV per request);
+ * (SGLang-Omni cookbook, PersonaPlex, "Known limitations": BF16 KV per request);
  * every key, the current position's included, is read back from the cache.
  *
  * The ring of keys/values is kept two ways: storage at position mod W (the
