@@ -489,6 +489,11 @@ extern "C" void mfs_destroy(mfs_ctx* c)
     delete c;
 }
 
+namespace mfs {
+// Message for mfs_last_error(NULL) from an entry point that takes no context.
+void set_thread_error(const char* msg) { g_create_error = msg ? msg : ""; }
+}  // namespace mfs
+
 extern "C" const char* mfs_last_error(const mfs_ctx* c)
 {
     if (!c) return g_create_error.c_str();

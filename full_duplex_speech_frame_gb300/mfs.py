@@ -62,6 +62,7 @@ def _load_library():
         "mfs_set_timing": (ci, [vp, ci]),
         "mfs_kernel_time": (ci, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
         "mfs_phase_times": (ci, [vp, vp, ci]),
+        "mfs_argmax_rows_noalloc": (ci, [vp, ci, ci, ctypes.c_longlong, vp, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -246,3 +247,16 @@ def mfs_kernel_time(ctx: Ctx):
     ms, n = ctypes.c_double(), ctypes.c_int()
     _check(ctx, _lib.mfs_kernel_time(ctx.handle, ctypes.byref(ms), ctypes.byref(n)))
     return ms.value, n.value
+
+
+def mfs_argmax_rows_noalloc(logits, out, stream=None) -> None:
+    """Greedy argmax of each row of a 2-D fp32 CUDA tensor into an int32 CUDA tensor,
+    with no device allocation (see include/mfs.h); enqueued on `stream` (default:
+    torch's current stream)."""
+    import torch
+    assert logits.is_cuda and logits.dtype == torch.float32 and logits.dim() == 2 and logits.stride(1) == 1
+    assert out.is_cuda and out.dtype == torch.int32 and out.is_contiguous() and out.numel() >= logits.shape[0]
+    rows, cols = logits.shape
+    st = _current_stream() if stream is None else ctypes.c_void_p(stream)
+    rc = _lib.mfs_argmax_rows_noalloc(logits.data_ptr(), rows, cols, logits.stride(0), out.data_ptr(), st)
+    _check(None, rc)

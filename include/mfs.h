@@ -168,6 +168,46 @@ int mfs_set_timing(mfs_ctx* ctx, int flags);
 int mfs_kernel_time(mfs_ctx* ctx, double* total_ms, int* steps);
 int mfs_phase_times(mfs_ctx* ctx, uint64_t* ns, int cap);
 
+/* ---------------------------------------------------------------- no-alloc
+ * Greedy argmax over rows of fp32 logits that allocates no device memory.
+ * The pages describe no such call: it exists for callers that cannot call
+ * cudaMalloc at the point where they pick tokens, for example code running
+ * inside a serving engine whose allocator has already reserved all free
+ * device memory (a cudaMalloc there fails or takes memory the engine counts
+ * on), or a real-time loop that must not block on the allocator.
+ *
+ * It is the frame step's argmax stage as a stand-alone kernel: blocks of 4096
+ * columns leave partial maxima in scratch memory and the last block of each
+ * row reduces them.  That scratch is a fixed static array of
+ * MFS_ARGMAX_SCRATCH_BYTES (528 KiB) inside this library, held on every GPU
+ * that loads the library until the process exits.
+ *
+ *   logits  device pointer, row r at logits + r * ld (fp32, read only)
+ *   rows    0 .. MFS_ARGMAX_MAX_ROWS; 0 returns MFS_OK and launches nothing
+ *   cols    >= 1, with rows * ceil(cols / 4096) <= MFS_ARGMAX_MAX_PARTIALS
+ *   ld      row stride in elements, >= cols
+ *   out     device pointer to rows int32: the lowest column holding the
+ *           row's maximum (NaN never wins; a row of only NaN gives 0), the
+ *           same rule as the step's text and code argmax
+ *   stream  cudaStream_t (NULL = legacy default stream); the call only
+ *           enqueues work and returns without waiting
+ * Returns MFS_OK, MFS_E_ARG (bad sizes or NULL pointers), MFS_E_RANGE (sizes
+ * beyond the fixed scratch), or MFS_E_CUDA; mfs_last_error(NULL) then gives
+ * the reason.  Nothing is launched when an error is returned.
+ *
+ * The first call on each device looks up the device address of the scratch
+ * array (cudaGetSymbolAddress) with that device current: make that first call
+ * before any stream capture on the device.  Every call on a device shares the
+ * one array; each call first clears the per-row counters that must start at
+ * zero.  Calls whose work overlaps on the GPU (other streams, other host
+ * threads) race on the array and may return wrong indices: order them on one
+ * stream or synchronise between them. */
+#define MFS_ARGMAX_MAX_ROWS 4096
+#define MFS_ARGMAX_MAX_PARTIALS 65536
+#define MFS_ARGMAX_SCRATCH_BYTES (MFS_ARGMAX_MAX_ROWS * 4 + MFS_ARGMAX_MAX_PARTIALS * 8)
+int mfs_argmax_rows_noalloc(const float* logits, int rows, int cols, long long ld, int32_t* out,
+                            void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif
