@@ -766,6 +766,73 @@ extern "C" int mfs_reset_slot(mfs_ctx* c, int slot)
     return MFS_OK;
 }
 
+// ------------------------------------------------------------------ slot state
+
+static size_t ring_bytes(const mfs_ctx* c)
+{
+    return (size_t)c->cfg.n_layers * c->cfg.window * c->cfg.d * c->kvb;
+}
+
+extern "C" size_t mfs_slot_state_bytes(const mfs_ctx* c)
+{
+    if (!c) return 0;
+    return MFS_SLOT_HEADER_BYTES + 2 * ring_bytes(c);
+}
+
+extern "C" int mfs_export_slot(mfs_ctx* c, int slot, void* buf, size_t bytes)
+{
+    if (!c || !buf) return MFS_E_ARG;
+    if (slot < 0 || slot >= c->cfg.max_slots) return fail(c, MFS_E_SLOT, "slot %d outside [0, %d)", slot, c->cfg.max_slots);
+    if (bytes != mfs_slot_state_bytes(c)) return fail(c, MFS_E_ARG, "slot state is %zu bytes, not %zu", mfs_slot_state_bytes(c), bytes);
+    if (!c->pending.empty()) {
+        int rc = mfs_sync(c);
+        if (rc != MFS_OK) return rc;
+    }
+    CK(cudaStreamSynchronize(c->stream));
+    char* out = (char*)buf;
+    memset(out, 0, MFS_SLOT_HEADER_BYTES);
+    int32_t head[4] = {1, c->pos[slot], c->cfg.window, c->cfg.kv_dtype};
+    memcpy(out, head, sizeof head);
+    CK(cudaMemcpy(out + sizeof head, c->hist + (size_t)slot * NSTREAM * HIST, NSTREAM * HIST * sizeof(int),
+                  cudaMemcpyDeviceToHost));
+    const size_t rb = ring_bytes(c);
+    CK(cudaMemcpy(out + MFS_SLOT_HEADER_BYTES, (const char*)c->kc + slot * rb, rb, cudaMemcpyDeviceToHost));
+    CK(cudaMemcpy(out + MFS_SLOT_HEADER_BYTES + rb, (const char*)c->vc + slot * rb, rb, cudaMemcpyDeviceToHost));
+    return MFS_OK;
+}
+
+extern "C" int mfs_import_slot(mfs_ctx* c, int slot, const void* buf, size_t bytes)
+{
+    if (!c || !buf) return MFS_E_ARG;
+    if (slot < 0 || slot >= c->cfg.max_slots) return fail(c, MFS_E_SLOT, "slot %d outside [0, %d)", slot, c->cfg.max_slots);
+    if (bytes != mfs_slot_state_bytes(c)) return fail(c, MFS_E_ARG, "slot state is %zu bytes, not %zu", mfs_slot_state_bytes(c), bytes);
+    const char* in = (const char*)buf;
+    int32_t head[4];
+    memcpy(head, in, sizeof head);
+    if (head[0] != 1 || head[2] != c->cfg.window || head[3] != c->cfg.kv_dtype)
+        return fail(c, MFS_E_ARG, "slot state header (version %d, window %d, kv dtype %d) does not match this context",
+                    head[0], head[2], head[3]);
+    if (head[1] < 0 || head[1] > c->cfg.max_pos) return fail(c, MFS_E_ARG, "slot state position %d outside [0, %d]", head[1], c->cfg.max_pos);
+    int32_t hist[NSTREAM * HIST];
+    memcpy(hist, in + sizeof head, sizeof hist);
+    for (int k = 0; k < NSTREAM; ++k)
+        for (int t = 0; t < HIST; ++t) {
+            const int v = hist[k * HIST + t], lim = k == 0 ? c->cfg.text_vocab : c->cfg.card;
+            if (v < -1 || v >= lim) return fail(c, MFS_E_ARG, "slot state history: stream %d holds token %d", k, v);
+        }
+    if (!c->pending.empty()) {
+        int rc = mfs_sync(c);
+        if (rc != MFS_OK) return rc;
+    }
+    CK(cudaStreamSynchronize(c->stream));
+    const size_t rb = ring_bytes(c);
+    CK(cudaMemcpy(c->hist + (size_t)slot * NSTREAM * HIST, hist, sizeof hist, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy((char*)c->kc + slot * rb, in + MFS_SLOT_HEADER_BYTES, rb, cudaMemcpyHostToDevice));
+    CK(cudaMemcpy((char*)c->vc + slot * rb, in + MFS_SLOT_HEADER_BYTES + rb, rb, cudaMemcpyHostToDevice));
+    c->pos[slot] = head[1];
+    return MFS_OK;
+}
+
 extern "C" int mfs_position(const mfs_ctx* c, int slot)
 {
     if (!c) return MFS_E_ARG;

@@ -737,8 +737,9 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
         if (!mbar_wait(&sm.full[slot], (stage / NS) & 1u, P.err, WS_FULL)) return false;
         if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) {
             // diagnostics: time CTA 0 spent waiting for weight stages, and their count
-            P.ptime[(size_t)sm.misc[0] * 8 + 4] += globaltimer_ns() - tw0;
-            P.ptime[(size_t)sm.misc[0] * 8 + 5] += 1;
+            // (fire-and-forget reductions: the warp does not wait on them)
+            atomicAdd(P.ptime + (size_t)sm.misc[0] * 8 + 4, globaltimer_ns() - tw0);
+            atomicAdd(P.ptime + (size_t)sm.misc[0] * 8 + 5, 1ull);
         }
         const TW* ring = (const TW*)(sm.ring + (size_t)slot * STAGE_BYTES);
         // copy this warp's rows of the stage into registers, release the stage at
@@ -767,13 +768,11 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
             if (rw + q0 * c.nwr < nr) {  // warp-uniform
             // independent packed accumulators per (row, vector): even and odd
             // elements of each vector accumulate separately, combined in fixed order
-            float2 acc2[4][BGV][VPL];
+            float2 acc2[4][BGV];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int b = 0; b < BGV; ++b)
-#pragma unroll
-                    for (int t = 0; t < VPL; ++t) acc2[q][b][t] = make_float2(0.f, 0.f);
+                for (int b = 0; b < BGV; ++b) acc2[q][b] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const int rr = rw + (q0 + q) * c.nwr;
@@ -795,7 +794,7 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
 #pragma unroll
                             for (int b = 0; b < BGV; ++b)
 #pragma unroll
-                                for (int e = 0; e < 8; e += 2) ffma2(acc2[q][b][t], f[e], f[e + 1], xr[t][b][e], xr[t][b][e + 1]);
+                                for (int e = 0; e < 8; e += 2) ffma2(acc2[q][b], f[e], f[e + 1], xr[t][b][e], xr[t][b][e + 1]);
                         }
                     }
                 }
@@ -805,10 +804,7 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
             for (int q = 0; q < 4; ++q)
 #pragma unroll
                 for (int b = 0; b < BGV; ++b) {
-                    float a = 0.f;
-#pragma unroll
-                    for (int t = 0; t < VPL; ++t) a += acc2[q][b][t].x + acc2[q][b][t].y;
-                    acc[q][b] = a;
+                    acc[q][b] = acc2[q][b].x + acc2[q][b].y;
                 }
             // transposed butterfly: lanes 0, 8, 16, 24 end with the sums of rows q0..q0+3
             const int myq = ((lane >> 4) & 1) * 2 + ((lane >> 3) & 1);
@@ -1534,6 +1530,8 @@ __global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int
         const Phase phs = P.phases[ph];
         if (!run_phase<TW, TKV, BG>(P, phs, ph, n, sm, stage)) return;
         stamp(P, ph, 3);
+        // diagnostics: the latest end of this phase over all CTAs
+        if (P.ptime && threadIdx.x == 0) atomicMax(P.ptime + (size_t)ph * 8 + 6, globaltimer_ns());
     }
     stamp(P, ph1, 0);
 }

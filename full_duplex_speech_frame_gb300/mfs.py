@@ -63,6 +63,9 @@ def _load_library():
         "mfs_kernel_time": (ci, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
         "mfs_phase_times": (ci, [vp, vp, ci]),
         "mfs_argmax_rows_noalloc": (ci, [vp, ci, ci, ctypes.c_longlong, vp, vp]),
+        "mfs_slot_state_bytes": (ctypes.c_size_t, [vp]),
+        "mfs_export_slot": (ci, [vp, ci, vp, ctypes.c_size_t]),
+        "mfs_import_slot": (ci, [vp, ci, vp, ctypes.c_size_t]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -206,6 +209,18 @@ def mfs_position(ctx: Ctx, slot: int) -> int:
     if rc < 0:
         _check(ctx, rc)
     return rc
+
+
+def mfs_export_slot(ctx: Ctx, slot: int) -> np.ndarray:
+    """The slot's state as a uint8 buffer (layout in include/mfs.h)."""
+    buf = np.empty(_lib.mfs_slot_state_bytes(ctx.handle), np.uint8)
+    _check(ctx, _lib.mfs_export_slot(ctx.handle, int(slot), buf.ctypes.data, buf.nbytes))
+    return buf
+
+
+def mfs_import_slot(ctx: Ctx, slot: int, buf: np.ndarray) -> None:
+    buf = np.ascontiguousarray(buf, dtype=np.uint8)
+    _check(ctx, _lib.mfs_import_slot(ctx.handle, int(slot), buf.ctypes.data, buf.nbytes))
 
 
 def mfs_read_debug(ctx: Ctx, n: Optional[int] = None) -> dict:

@@ -140,6 +140,27 @@ int mfs_reset_slot(mfs_ctx* ctx, int slot);
 /* Frame count of a slot (its next position), or a negative status. */
 int mfs_position(const mfs_ctx* ctx, int slot);
 
+/* ---------------------------------------------------------------- slot state
+ * A slot's whole decode state as one host buffer, so that a session can be
+ * checkpointed, moved to another context, or checked against an independent
+ * implementation without replaying its history (SGLang-Omni cookbook,
+ * PersonaPlex, "Known limitations": decode states are resident per request).
+ * Layout, little-endian, MFS_SLOT_HEADER_BYTES of header then the ring:
+ *   int32 version (1), position p, window W, kv dtype (MFS_DTYPE_*),
+ *   int32 hist[17][3]: token of stream k for frame f at [k][f mod 3], -1 = none,
+ *   zero padding to MFS_SLOT_HEADER_BYTES,
+ *   keys [n_layers][W][d] then values [n_layers][W][d] in the kv dtype; row r
+ *   holds the position q < p with q mod W == r among the last W positions
+ *   (rows of positions never written are unspecified).
+ * mfs_slot_state_bytes: the buffer size for this context.  Export copies the
+ * slot's state out (waits for the stream); import replaces it after checking
+ * the header (version, window, dtype, 0 <= p <= max_pos, every history token
+ * -1 or inside its stream's vocabulary), else MFS_E_ARG and nothing changes. */
+#define MFS_SLOT_HEADER_BYTES 256
+size_t mfs_slot_state_bytes(const mfs_ctx* ctx);
+int mfs_export_slot(mfs_ctx* ctx, int slot, void* buf, size_t bytes);
+int mfs_import_slot(mfs_ctx* ctx, int slot, const void* buf, size_t bytes);
+
 /* Diagnostics of the last step, rows in that step's slot order (any pointer
  * may be NULL): text logits [n, V], depformer logits [n, 16, C] (fp32), and
  * the raw argmaxes before forcing, text [n] and per substep [n, 16]. */
@@ -161,7 +182,8 @@ int mfs_launches_per_step(const mfs_ctx* ctx);
  * records, per phase, 8 values: GPU timer stamps (ns) at the start, when the
  * inputs are ready, when the last weight stage is consumed, at the end (0
  * where a point does not apply), then the ns spent waiting for weight stages
- * and the number of stages, summed since the last read; mfs_phase_times
+ * and the number of stages, summed since the last read, then the latest end
+ * of the phase over all CTAs (timer ns, the maximum since the last read); mfs_phase_times
  * copies [phases + 1][8] values into ns, restarts the sums and returns the
  * count, or a negative status. */
 int mfs_set_timing(mfs_ctx* ctx, int flags);

@@ -65,6 +65,8 @@ def _load():
         lib.orc_position.argtypes = [vp, ci]
         lib.orc_step.argtypes = [vp, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.orc_prefill.argtypes = [vp, ci, ci, vp]
+        lib.orc_import_slot.argtypes = [vp, ci, vp, ctypes.c_longlong]
+        lib.orc_export_slot.argtypes = [vp, ci, vp, ctypes.c_longlong]
         lib.orc_rmsnorm.argtypes = [vp, vp, ci, ctypes.c_double, vp]
         lib.orc_rope.argtypes = [vp, ci, ci, ctypes.c_double]
         lib.orc_attention.argtypes = [vp, vp, vp, ci, ci, ctypes.c_long, vp]
@@ -137,6 +139,23 @@ class Oracle:
 
     def position(self, slot: int) -> int:
         return self._lib.orc_position(self._h, slot)
+
+    def import_slot(self, slot: int, buf: np.ndarray) -> None:
+        """Replace a slot's state with a buffer in the slot-state layout (position,
+        history, key/value ring rows in the cache dtype)."""
+        buf = np.ascontiguousarray(buf, dtype=np.uint8)
+        if self._lib.orc_import_slot(self._h, slot, buf.ctypes.data, buf.nbytes) != 0:
+            raise ValueError("slot state rejected")
+
+    def state_bytes(self) -> int:
+        s = self.shape
+        return 256 + 2 * s.n_layers * s.window * s.d * (2 if s.kv_dtype == "bf16" else 4)
+
+    def export_slot(self, slot: int) -> np.ndarray:
+        buf = np.empty(self.state_bytes(), np.uint8)
+        if self._lib.orc_export_slot(self._h, slot, buf.ctypes.data, buf.nbytes) != 0:
+            raise ValueError("export failed")
+        return buf
 
     def reset_slot(self, slot: int) -> None:
         if self._lib.orc_reset_slot(self._h, slot) != 0:

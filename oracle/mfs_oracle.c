@@ -288,6 +288,89 @@ int orc_reset_slot(orc* o, int slot)
     return 0;
 }
 
+/* Replace a slot's state with a buffer in the CUDA library's slot-state layout
+ * (its header documents it): 256 bytes of header (int32 version 1, position,
+ * window, kv dtype, then history [17][3]), then keys and values
+ * [n_layers][W][d] in the kv dtype, row r holding the position q with
+ * q mod W == r.  Ring storage only (not brute_force).  Returns 0 or -1. */
+static int ensure_kv(orc* o, orc_slot* s);
+
+int orc_import_slot(orc* o, int slot, const void* buf, long long nbytes)
+{
+    const orc_config* c = &o->c;
+    if (slot < 0 || slot >= c->max_slots || c->brute_force) return -1;
+    size_t kvb = c->kv_dtype == 1 ? 2 : 4;
+    size_t ring = (size_t)c->n_layers * (size_t)c->window * (size_t)c->d;
+    if (nbytes != (long long)(256 + 2 * ring * kvb)) return -1;
+    const unsigned char* in = (const unsigned char*)buf;
+    int32_t head[4 + ORC_STREAMS * ORC_HIST];
+    memcpy(head, in, sizeof head);
+    if (head[0] != 1 || head[2] != c->window || head[3] != c->kv_dtype || head[1] < 0 || head[1] > c->max_pos) return -1;
+    orc_slot* s = &o->slots[slot];
+    if (ensure_kv(o, s) != 0) return -1;
+    s->pos = head[1];
+    for (int k = 0; k < ORC_STREAMS; ++k)
+        for (int t = 0; t < ORC_HIST; ++t) s->hist[k][t] = head[4 + k * ORC_HIST + t];
+    const unsigned char* kin = in + 256;
+    const unsigned char* vin = kin + ring * kvb;
+    for (size_t i = 0; i < ring; ++i) {
+        if (kvb == 2) {
+            uint16_t kb, vb;
+            memcpy(&kb, kin + 2 * i, 2);
+            memcpy(&vb, vin + 2 * i, 2);
+            s->K[i] = bf16_bits_to_double(kb);
+            s->V[i] = bf16_bits_to_double(vb);
+        } else {
+            float kf, vf;
+            memcpy(&kf, kin + 4 * i, 4);
+            memcpy(&vf, vin + 4 * i, 4);
+            s->K[i] = kf;
+            s->V[i] = vf;
+        }
+    }
+    return 0;
+}
+
+/* The slot's state in the same layout (ring storage only); keys and values
+ * are converted to the kv dtype (exact for a bf16 cache, which holds bf16
+ * values already).  Returns 0 or -1. */
+int orc_export_slot(orc* o, int slot, void* buf, long long nbytes)
+{
+    const orc_config* c = &o->c;
+    if (slot < 0 || slot >= c->max_slots || c->brute_force) return -1;
+    size_t kvb = c->kv_dtype == 1 ? 2 : 4;
+    size_t ring = (size_t)c->n_layers * (size_t)c->window * (size_t)c->d;
+    if (nbytes != (long long)(256 + 2 * ring * kvb)) return -1;
+    orc_slot* s = &o->slots[slot];
+    if (ensure_kv(o, s) != 0) return -1;
+    unsigned char* out = (unsigned char*)buf;
+    memset(out, 0, 256);
+    int32_t head[4 + ORC_STREAMS * ORC_HIST];
+    head[0] = 1; head[1] = s->pos; head[2] = c->window; head[3] = c->kv_dtype;
+    for (int k = 0; k < ORC_STREAMS; ++k)
+        for (int t = 0; t < ORC_HIST; ++t) head[4 + k * ORC_HIST + t] = s->hist[k][t];
+    memcpy(out, head, sizeof head);
+    unsigned char* kout = out + 256;
+    unsigned char* vout = kout + ring * kvb;
+    for (size_t i = 0; i < ring; ++i) {
+        if (kvb == 2) {
+            /* the cache values are bf16 already: keep the top 16 bits of the float */
+            float kf = (float)s->K[i], vf = (float)s->V[i];
+            uint32_t ku, vu;
+            memcpy(&ku, &kf, 4);
+            memcpy(&vu, &vf, 4);
+            uint16_t kb = (uint16_t)(ku >> 16), vb = (uint16_t)(vu >> 16);
+            memcpy(kout + 2 * i, &kb, 2);
+            memcpy(vout + 2 * i, &vb, 2);
+        } else {
+            float kf = (float)s->K[i], vf = (float)s->V[i];
+            memcpy(kout + 4 * i, &kf, 4);
+            memcpy(vout + 4 * i, &vf, 4);
+        }
+    }
+    return 0;
+}
+
 /* Borrow a host tensor by name; size must match the shape the config implies. */
 int orc_set_weight(orc* o, const char* name, const void* data, long long nbytes)
 {

@@ -264,6 +264,33 @@ def user_frames(s: Shape, seed: int, T: int, B: int, stream: int = STREAM_USER) 
     return out
 
 
+STREAM_STATE = 6 << 20       # synthetic slot states (history and key/value rings)
+
+
+def slot_state(s: Shape, seed: int, tag: int, pos: int, kv_std: float = 1.0) -> np.ndarray:
+    """A synthetic slot state in the slot-state buffer layout (256-byte header:
+    int32 version 1, position, window, kv dtype 1 (bf16), history [17][3];
+    then keys and values [n_layers][W][d] as bf16).  History holds uniform
+    tokens for frames pos-3 .. pos-1 that exist (-1 elsewhere); every ring row
+    holds N(0, kv_std) draws.  ``tag`` selects independent draws."""
+    assert s.kv_dtype == "bf16"
+    ring = s.n_layers * s.window * s.d
+    buf = np.zeros(256 + 4 * ring, np.uint8)
+    head = np.zeros(4 + 17 * 3, np.int32)
+    head[:4] = [1, pos, s.window, 1]
+    hist = np.full((17, 3), -1, np.int32)
+    toks = uniform_int(seed, STREAM_STATE + 8 * tag, 17 * 3, 0, 1 << 30).reshape(17, 3)
+    for f in range(max(0, pos - 3), pos):
+        lim = np.array([s.text_vocab] + [s.card] * 16)
+        hist[:, f % 3] = toks[:, f % 3] % lim
+    head[4:] = hist.reshape(-1)
+    buf[:head.nbytes] = np.frombuffer(head.tobytes(), np.uint8)
+    kv = buf[256:].view(np.uint16)
+    normal_bf16(seed, STREAM_STATE + 8 * tag + 1, ring, 0.0, kv_std, out=kv[:ring])
+    normal_bf16(seed, STREAM_STATE + 8 * tag + 2, ring, 0.0, kv_std, out=kv[ring:])
+    return buf
+
+
 def prefill_lengths(seed: int, B: int, lo: int, hi: int) -> np.ndarray:
     """Per-slot prompt lengths uniform in [lo, hi] (inclusive)."""
     return uniform_int(seed, STREAM_LENGTHS, B, lo, hi + 1)

@@ -331,3 +331,26 @@ def test_oracle_rejects_bad_input(tiny_w8):
     with pytest.raises(ValueError):
         o.step([3], synth.user_frames(s, 49, 1, 1)[0])
     assert o.position(0) == 0
+
+
+def test_slot_state_import_continues_exactly():
+    """A bf16-cache slot exported after some steps and imported into another slot of a
+    fresh oracle continues bit for bit like the original (position, history and every
+    ring row carried over; the ring wraps at W = 5 within the run)."""
+    s = small_shape(weight_dtype="bf16", kv_dtype="bf16", window=5)
+    w = synth.make_weights(s, seed=8, gain_std=0.1)
+    z = synth.user_frames(s, 41, 14, 1)
+    a, b = oracle.Oracle(s, w), oracle.Oracle(s, w)
+    for p in range(9):
+        a.step([0], z[p])
+    b.import_slot(2, a.export_slot(0))
+    assert b.position(2) == a.position(0) == 9
+    for p in range(9, 14):
+        ra = a.step([0], z[p], want_logits=True)
+        rb = b.step([2], z[p], want_logits=True)
+        for key in ra:
+            np.testing.assert_array_equal(ra[key], rb[key], err_msg=key)
+    bad = a.export_slot(0)
+    bad[4:8] = np.frombuffer(np.int32(s.max_pos + 1).tobytes(), np.uint8)
+    with pytest.raises(ValueError):
+        b.import_slot(1, bad)
