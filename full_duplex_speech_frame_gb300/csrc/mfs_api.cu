@@ -278,10 +278,14 @@ static void rebasef(const float*& p, float* base) { p = (const float*)((char*)ba
 
 static int max_rows(const mfs_config& g, int G)
 {
-    const long long npairs[] = {3LL * g.d / 2, g.d / 2, g.ffn, g.d / 2, (g.text_vocab + 16LL * g.dep_d) / 2,
-                                3LL * g.dep_d / 2, g.dep_d / 2, g.dep_ffn, g.dep_d / 2, g.card / 2};
+    // temporal matrices are shared by all G CTAs; a depformer matrix by at
+    // least G / MAXGW of them (a group of up to MAXGW substeps splits the grid)
+    const long long tpairs[] = {3LL * g.d / 2, g.d / 2, g.ffn, g.d / 2, (g.text_vocab + 16LL * g.dep_d) / 2};
+    const long long dpairs[] = {3LL * g.dep_d / 2, g.dep_d / 2, g.dep_ffn, g.dep_d / 2, g.card / 2};
+    const long long Gd = G / MAXGW;
     long long m = 0;
-    for (long long np : npairs) m = (np + G - 1) / G > m ? (np + G - 1) / G : m;
+    for (long long np : tpairs) m = (np + G - 1) / G > m ? (np + G - 1) / G : m;
+    for (long long np : dpairs) m = (np + Gd - 1) / Gd > m ? (np + Gd - 1) / Gd : m;
     return (int)(2 * m);
 }
 
@@ -330,10 +334,10 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
     const size_t T8 = sizeof(uint2);  // tagged element
     const size_t a_x = areg(MS * d * T8), a_q = areg(MS * d * T8), a_kc = areg(MS * d * T8), a_vc = areg(MS * d * T8);
     const size_t a_o = areg(MS * d * T8), a_s = areg(MS * F * T8);
-    const size_t a_lg = areg(MS * V * 4), a_yin = areg(MS * S * dd * T8), a_u = areg(MS * dd * T8);
-    const size_t a_dq = areg(MS * dd * T8), a_dkv = areg(MS * dL * S * 2 * dd * T8), a_dat = areg(MS * dd * T8);
-    const size_t a_ds = areg(MS * dF * T8), a_dlg = areg(MS * S * C * 4);
-    const size_t a_am = areg(MS * c->G * 2 * T8), a_ch = areg(MS * NSTREAM * 4);
+    const size_t a_lg = areg(MS * V * 4), a_yin = areg(MS * S * dd * T8), a_u = areg(MS * S * dd * T8);
+    const size_t a_dq = areg(MS * S * dd * T8), a_dkv = areg(MS * dL * S * 2 * dd * T8), a_dat = areg(MS * S * dd * T8);
+    const size_t a_ds = areg(MS * S * dF * T8), a_dlg = areg(MS * S * C * 4);
+    const size_t a_am = areg(MS * c->G * 2 * T8), a_dam = areg(MS * S * c->G * 2 * T8);
     const size_t a_to = areg(MS * 4), a_co = areg(MS * 16 * 4), a_ta = areg(MS * 4), a_ca = areg(MS * 16 * 4);
     (void)H;
     (void)hd;
@@ -421,7 +425,7 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
     P.logits = (float*)(A + a_lg); P.yin = (uint2*)(A + a_yin); P.u = (uint2*)(A + a_u);
     P.dq = (uint2*)(A + a_dq); P.dkv = (uint2*)(A + a_dkv); P.dat = (uint2*)(A + a_dat);
     P.ds = (uint2*)(A + a_ds); P.dlogits = (float*)(A + a_dlg); P.amax = (uint2*)(A + a_am);
-    P.chosen = (int*)(A + a_ch); P.text_out = (int*)(A + a_to); P.codes_out = (int*)(A + a_co);
+    P.damax = (uint2*)(A + a_dam); P.text_out = (int*)(A + a_to); P.codes_out = (int*)(A + a_co);
     P.text_argmax = (int*)(A + a_ta); P.code_argmax = (int*)(A + a_ca);
     P.err = c->d_err; P.err_seq = c->d_err + 1;
     P.phases = c->d_phases;

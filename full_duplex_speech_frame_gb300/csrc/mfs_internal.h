@@ -17,6 +17,7 @@ constexpr int SMEM_HEAD = 1024;  // mbarriers and scalars before the ring
 constexpr int NSTREAM = MFS_N_STREAMS;
 constexpr int NCHUNK_MAX = 32;   // attention split over the window, per (slot, head)
 constexpr int HIST = 3;          // frames of token history per stream
+constexpr int MAXGW = 8;         // depformer substeps run together as one group, at most
 
 enum PhaseType : int {
     PH_EMBED = 0,  // S0 + S1: record frame p's tokens, delayed embedding sum
@@ -90,20 +91,20 @@ struct Params {
     uint2* s;        // [MS][F]  SwiGLU output
     float* logits;   // [MS][V]  (diagnostics)
     uint2* yin;      // [MS][S][dd]  depformer in-projections
-    uint2* u;        // [MS][dd] depformer residual stream
-    uint2* dq;       // [MS][dd]
+    uint2* u;        // [MS][S][dd] depformer residual stream, per substep
+    uint2* dq;       // [MS][S][dd]
     uint2* dkv;      // [MS][dL][S][2][dd]
-    uint2* dat;      // [MS][dd] depformer attention output
-    uint2* ds;       // [MS][dF]
+    uint2* dat;      // [MS][S][dd] depformer attention output
+    uint2* ds;       // [MS][S][dF]
     float* dlogits;  // [MS][S][C]  (diagnostics)
-    uint2* amax;     // [MS][G][2] per-CTA argmax partials: {value, tag}, {index, tag}
-    int* chosen;     // [MS][17] tokens chosen this step (CTA 0)
+    uint2* amax;     // [MS][G][2] text head argmax partials per CTA: {value, tag}, {index, tag}
+    uint2* damax;    // [MS][S][G][2] depformer head argmax partials per substep and CTA
     int* text_out;   // [MS]
     int* codes_out;  // [MS][16]
     int* text_argmax;  // [MS]
     int* code_argmax;  // [MS][16]
     int dep_ph0;       // index of the first depformer phase
-    int dep_ph_stride; // phases per depformer substep
+    int dep_ph_stride; // phases per depformer group (dL x 5 + head)
     // control
     int* err;        // sticky device error (DeviceError)
     int* err_seq;    // step sequence number that raised it

@@ -475,11 +475,77 @@ __device__ __forceinline__ bool phase_matrix(const Params& P, const Phase& ph, c
     }
 }
 
-__device__ __forceinline__ void cta_rows(int N, int G, int& r0, int& r1)
+// Rows [r0, r1) of an N-row matrix for CTA c of the cnt that share it (row pairs stay together).
+__device__ __forceinline__ void cta_rows(int N, int cnt, int c, int& r0, int& r1)
 {
     const int npairs = N / 2;
-    r0 = 2 * (int)((long long)npairs * blockIdx.x / G);
-    r1 = 2 * (int)((long long)npairs * (blockIdx.x + 1) / G);
+    r0 = 2 * (int)((long long)npairs * c / cnt);
+    r1 = 2 * (int)((long long)npairs * (c + 1) / cnt);
+}
+
+// ------------------------------------------------------------------ depformer substep groups
+// A substep whose input token is supplied for every slot of the step (forced
+// this frame, or the frame before for a delayed stream) needs nothing from the
+// substep before it except that layer's keys and values, so it runs with that
+// substep in one wide pass per layer; at most MAXGW substeps form a group.
+// `starts` has bit j set where a group begins (always bit 0).
+
+// Token of stream k for frame p - delay[k] supplied by the caller, or -1.
+__device__ __forceinline__ int supplied_token(const Params& P, int i, int k)
+{
+    const StepDesc* D = P.desc;
+    const int p = D->pos[i], f = p - P.delays[k];
+    if (f == p) return D->codes[i][k];
+    if (f >= 0) return __ldcg(P.hist + ((size_t)D->slot[i] * NSTREAM + k) * HIST + f % HIST);
+    return -1;
+}
+
+__device__ __forceinline__ int n_groups(unsigned starts) { return __popc(starts); }
+__device__ __forceinline__ int group_of(unsigned starts, int t) { return __popc(starts & ((2u << t) - 1u)) - 1; }
+
+// first substep j0 and width nj of group g
+__device__ __forceinline__ void group_bounds(unsigned starts, int S, int g, int& j0, int& nj)
+{
+    unsigned m = starts;
+    for (int k = 0; k < g; ++k) m &= m - 1u;
+    j0 = __ffs(m) - 1;
+    m &= m - 1u;
+    nj = (m ? __ffs(m) - 1 : S) - j0;
+}
+
+// CTAs [b0, b1) of the G work on substep s of an nj-wide group
+__device__ __forceinline__ void substep_ctas(int G, int nj, int s, int& b0, int& b1)
+{
+    b0 = (int)(((long long)s * G + nj - 1) / nj);
+    b1 = (int)(((long long)(s + 1) * G + nj - 1) / nj);
+}
+
+__device__ __forceinline__ bool is_dep_gemv(int type) { return type == PH_DQKV || type == PH_DO || type == PH_DGU || type == PH_DDOWN || type == PH_DHEAD; }
+
+// This CTA's share of a phase: CTA c of the cnt that share its matrix.  A
+// depformer phase's Phase.j names its group; resolve() turns it into this
+// CTA's substep (q.j) and records the group's first substep (q.pad0) and
+// width (q.pad1).  False when the group does not exist this step.
+__device__ __forceinline__ bool resolve(const Params& P, unsigned starts, Phase& q, int& c, int& cnt)
+{
+    c = blockIdx.x;
+    cnt = P.G;
+    if (q.type >= PH_DQKV && q.type <= PH_DHEAD) {
+        if (q.j >= n_groups(starts)) return false;
+        int j0, nj;
+        group_bounds(starts, P.S, q.j, j0, nj);
+        q.pad0 = j0;
+        q.pad1 = nj;
+        if (is_dep_gemv(q.type)) {
+            const int s = (int)((long long)blockIdx.x * nj / P.G);
+            int b0, b1;
+            substep_ctas(P.G, nj, s, b0, b1);
+            c = blockIdx.x - b0;
+            cnt = b1 - b0;
+            q.j = j0 + s;
+        }
+    }
+    return true;
 }
 
 template <typename TW>
@@ -492,7 +558,7 @@ __device__ __forceinline__ int rows_per_stage(int K)
 // Producer: copy, for every phase of the launch, every batch group's pass over
 // this CTA's rows, stage by stage, in the order the consumers use them.
 template <typename TW, int BG>
-__device__ __forceinline__ void producer(const Params& P, int ph0, int ph1, int n, const Smem& sm)
+__device__ __forceinline__ void producer(const Params& P, int ph0, int ph1, int n, unsigned starts, const Smem& sm)
 {
     constexpr unsigned NS = nstage_for(BG);
     const uint64_t pol = l2_evict_first();
@@ -500,10 +566,12 @@ __device__ __forceinline__ void producer(const Params& P, int ph0, int ph1, int 
     bool ok = true;
     for (int ph = ph0; ph < ph1 && ok; ++ph) {
         const TW* W;
-        int N, K;
-        if (!phase_matrix<TW>(P, P.phases[ph], W, N, K)) continue;
+        int N, K, c, cnt;
+        Phase q = P.phases[ph];
+        if (!resolve(P, starts, q, c, cnt)) continue;
+        if (!phase_matrix<TW>(P, q, W, N, K)) continue;
         int r0, r1;
-        cta_rows(N, P.G, r0, r1);
+        cta_rows(N, cnt, c, r0, r1);
         const int rps = rows_per_stage<TW>(K);
         const int bgv = group_size<BG>(K);
         for (int b0 = 0; b0 < n && ok; b0 += bgv) {
@@ -538,20 +606,24 @@ struct XSrc {
     const float* g;       // RMSNorm gain, or nullptr for no norm
     const void* add;      // depformer embedding table (weight dtype) or nullptr
     long long add_stride; // row length of that table (elements)
-    uint2* store;         // CTA 0 stores base + add here (depformer residual), or nullptr
+    uint2* store;         // stores base + add here (depformer residual; one CTA per substep), or nullptr
     unsigned store_tag;
+    long long store_stride;
+    int dj, dj0;          // depformer substep and its group's first substep (when add != nullptr)
+    unsigned am_tag;      // tag of the argmax partials the group's first substep reads
+    int am_cnt;           // and their count
 };
 
 // argmax partials of batch row i from every CTA (one warp; every lane gets the
 // same result; the tie rule makes the combine order irrelevant).  -1: gave up.
-__device__ __forceinline__ int argmax_partials_warp(const Params& P, int i, unsigned tag)
+__device__ __forceinline__ int argmax_partials_warp(const Params& P, const uint2* parts, int cnt, unsigned tag)
 {
     const int lane = threadIdx.x & 31;
     float v = -INFINITY;
     int ix = 0x7fffffff;
     bool ok = true;
-    for (int c = lane; c < P.G && ok; c += 32) {
-        const uint2* e = P.amax + ((size_t)i * P.G + c) * 2;
+    for (int c = lane; c < cnt && ok; c += 32) {
+        const uint2* e = parts + (size_t)c * 2;
         unsigned vb = 0, ib = 0;
         ok = wait_tag1(e, tag, vb, P.err) && wait_tag1(e + 1, tag, ib, P.err);
         if (ok && am_better(__uint_as_float(vb), (int)ib, v, ix)) { v = __uint_as_float(vb); ix = (int)ib; }
@@ -561,31 +633,22 @@ __device__ __forceinline__ int argmax_partials_warp(const Params& P, int i, unsi
     return ix == 0x7fffffff ? 0 : ix;
 }
 
-// Picks, for depformer substep j, each batch row's input token (the text token
-// for j = 0, else the code chosen for stream j): the token the caller supplied
-// for that frame if any, else the previous head's argmax.  CTA 0 records it.
-// Every consumer thread calls it; false if a wait gave up.
-__device__ __forceinline__ bool dep_select_inputs(const Params& P, int j, unsigned am_tag, int b0, int nb, const Smem& sm)
+// Input token of depformer substep j for each batch row: the token supplied
+// for stream j (this frame, or the frame before for a delayed stream) if any,
+// else, at a group's first substep only, the argmax of the head before it (the
+// text head for j = 0).  Every consumer thread calls it; false if a wait gave up.
+__device__ __forceinline__ bool dep_select_inputs(const Params& P, const XSrc& xs, int b0, int nb, const Smem& sm)
 {
-    const StepDesc* D = P.desc;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j = xs.dj;
     int ok = 1;
     if (warp < nb) {
         const int i = b0 + warp;
-        const int a = argmax_partials_warp(P, i, am_tag);
-        ok = a >= 0;
-        int chosen = 0;
-        if (ok) {
-            const int p = D->pos[i], f = p - P.delays[j];
-            int forced = -1;
-            if (f == p) forced = D->codes[i][j];  // frame p: this step's input
-            else if (f >= 0) forced = ld_cg_int(P.hist + ((size_t)D->slot[i] * NSTREAM + j) * HIST + f % HIST);
-            chosen = forced >= 0 ? forced : a;
-            if (blockIdx.x == 0 && lane == 0) {
-                if (j == 0) P.text_argmax[i] = a;
-                else P.code_argmax[i * 16 + (j - 1)] = a;
-                P.chosen[i * NSTREAM + j] = chosen;
-            }
+        int chosen = supplied_token(P, i, j);
+        if (chosen < 0 && j == xs.dj0) {
+            const uint2* parts = j == 0 ? P.amax + (size_t)i * P.G * 2 : P.damax + ((size_t)i * P.S + (j - 1)) * P.G * 2;
+            chosen = argmax_partials_warp(P, parts, xs.am_cnt, xs.am_tag);
+            ok = chosen >= 0;
         }
         const int lim = j == 0 ? P.V : P.C;
         if (lane == 0) sm.prev[warp] = (chosen >= 0 && chosen < lim) ? chosen : 0;  // keeps the embedding read in range
@@ -653,7 +716,7 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
     // depformer layer 0: the input adds the embedding of the token chosen by the
     // previous head; then the gain
     if (xs.add) {
-        if (!dep_select_inputs(P, ph.j, phase_tag(P.desc, ph.am_ph), b0, nb, sm)) ok = 0;
+        if (!dep_select_inputs(P, xs, b0, nb, sm)) ok = 0;
 #pragma unroll
         for (int b = 0; b < BGV; ++b) ssq[b] = 0.f;
 #pragma unroll
@@ -674,14 +737,14 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
                 }
             }
         }
-        if (xs.store && blockIdx.x == 0 && rw == 0) {
+        if (xs.store && rw == 0) {
 #pragma unroll
             for (int t = 0; t < VPL; ++t) {
                 const int v = v_begin + lane + 32 * t;
 #pragma unroll
                 for (int b = 0; b < BGV; ++b) {
                     if (v < v_end && b < nb) {
-                        uint2* dst = xs.store + (size_t)(b0 + b) * K + v * 8;
+                        uint2* dst = xs.store + (size_t)(b0 + b) * xs.store_stride + v * 8;
 #pragma unroll
                         for (int e = 0; e < 8; e += 2) st_tag2(dst + e, xr[t][b][e], xr[t][b][e + 1], xs.store_tag);
                     }
@@ -985,10 +1048,13 @@ struct EpiLogits {
     uint2* extra;
     long long extra_stride;
     unsigned tag;
+    uint2* am;            // argmax partials: batch row i, this CTA at am + i * am_stride + am_idx * 2
+    long long am_stride;
+    int am_idx;
     __device__ Pre pre(const Params&, int, int, int, int) const { return Pre{{0.f, 0.f}, {0.f, 0.f}, 1}; }
     __device__ void publish(const Params& P, int i, float v, int ix) const
     {
-        uint2* e = P.amax + ((size_t)i * P.G + blockIdx.x) * 2;
+        uint2* e = am + (size_t)i * am_stride + (size_t)am_idx * 2;
         st_tag1(e, __float_as_uint(v), tag);
         st_tag1(e + 1, (unsigned)ix, tag);
     }
@@ -1048,7 +1114,7 @@ struct EpiDQKV {
             const int part = r / dd, e = r - part * dd;
             const float y0 = sm.yf[(size_t)(2 * pl) * bgv + b];
             const float y1 = sm.yf[(size_t)(2 * pl + 1) * bgv + b];
-            uint2* dst = part == 0 ? P.dq + (size_t)i * dd + e
+            uint2* dst = part == 0 ? P.dq + ((size_t)i * P.S + j) * dd + e
                                    : P.dkv + ((((size_t)i * P.dL + l) * P.S + j) * 2 + (part - 1)) * dd + e;
             st_tag2(dst, y0, y1, tag);
         }
@@ -1058,19 +1124,19 @@ struct EpiDQKV {
 
 // One matrix-vector phase; the epilogue consumes the CTA's rows.
 template <typename TW, int BG, class Epi>
-__device__ __forceinline__ bool gemv_phase(const Params& P, const Phase& ph, const XSrc& xs, int n, const Smem& sm, unsigned& stage,
-                           const Epi& epi)
+__device__ __forceinline__ bool gemv_phase(const Params& P, const Phase& ph, int cta, int cnt, const XSrc& xs, int n,
+                                           const Smem& sm, unsigned& stage, const Epi& epi)
 {
     const TW* W;
     int N, K;
     phase_matrix<TW>(P, ph, W, N, K);
     int r0, r1;
-    cta_rows(N, P.G, r0, r1);
+    cta_rows(N, cnt, cta, r0, r1);
     const GemvCfg c = gemv_cfg(K);
     const int bgv = group_size<BG>(K);
     for (int b0 = 0; b0 < n; b0 += bgv) {
         const int nb = min(bgv, n - b0);
-        if (r1 > r0 || (xs.store && blockIdx.x == 0)) {
+        if (r1 > r0 || xs.store) {
             const Pre pre = epi.pre(P, r0, r1, b0, nb);
             bool ok;
             switch (vpl_class(c.vpl)) {
@@ -1317,19 +1383,20 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
 // loads keys/values w and w + NWARP (tag of that substep's QKV phase) with the
 // query, so the loads of the item are in flight together; the softmax and the
 // weighted sum run in key order in shared memory.
-__device__ __forceinline__ bool phase_dattn(const Params& P, int l, int j, int n, unsigned in_tag, unsigned tag,
-                                            const Smem& sm)
+__device__ __forceinline__ bool phase_dattn(const Params& P, int l, int j0, int nj, unsigned starts, int n, unsigned in_tag,
+                                            unsigned tag, const Smem& sm)
 {
     const StepDesc* D = P.desc;
     const int dd = P.dd, dH = P.dH, S = P.S;  // head dim is 64
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int npos = j + 1;
     const float scale = 0.125f;  // 1 / sqrt(64)
     float* sc = sm.wbuf;         // [16] scores
     float* pv = sm.wbuf + 16;    // [16][64] p_t * v_t
-    for (int item = blockIdx.x; item < n * dH; item += P.G) {
-        const int i = item / dH, h = item % dH;
-        const uint2* q = P.dq + (size_t)i * dd + h * 64 + 2 * lane;
+    // items: (batch row, substep of the group, head)
+    for (int item = blockIdx.x; item < n * nj * dH; item += P.G) {
+        const int i = item / (nj * dH), j = j0 + (item / dH) % nj, h = item % dH;
+        const int npos = j + 1;
+        const uint2* q = P.dq + ((size_t)i * S + j) * dd + h * 64 + 2 * lane;
         const uint2* kv = P.dkv + ((size_t)i * P.dL + l) * S * 2 * dd + h * 64 + 2 * lane;
         int ok = 1;
         constexpr int TPW = 16 / NWARP;  // keys per warp
@@ -1339,7 +1406,7 @@ __device__ __forceinline__ bool phase_dattn(const Params& P, int l, int j, int n
             const int t = warp + k * NWARP;
             vt[k] = make_float2(0.f, 0.f);
             if (t < npos && ok) {
-                const unsigned tt = phase_tag(D, P.dep_ph0 + t * P.dep_ph_stride + l * 5);
+                const unsigned tt = phase_tag(D, P.dep_ph0 + group_of(starts, t) * P.dep_ph_stride + l * 5);
                 const uint2* kp = kv + (size_t)t * 2 * dd;
                 const uint2* vp = kv + ((size_t)t * 2 + 1) * dd;
                 uint2 qa, qb, ka, kb, va, vb;
@@ -1384,7 +1451,7 @@ __device__ __forceinline__ bool phase_dattn(const Params& P, int l, int j, int n
                 Z += expf(sc[u] - M);
                 a += pv[u * 64 + e];
             }
-            st_tag1(P.dat + (size_t)i * dd + h * 64 + e, __float_as_uint(a / Z), tag);
+            st_tag1(P.dat + ((size_t)i * S + j) * dd + h * 64 + e, __float_as_uint(a / Z), tag);
         }
         csync();
     }
@@ -1393,33 +1460,46 @@ __device__ __forceinline__ bool phase_dattn(const Params& P, int l, int j, int n
 
 // ------------------------------------------------------------------ S10
 
-__device__ __forceinline__ bool phase_final(const Params& P, int n, unsigned am_tag)
+// CTA 0: the argmax of the text head and of every depformer head, the token
+// chosen per stream (the supplied one, else that argmax), the history
+// write-back for frames p - delay[k] >= 0, and the outputs.
+__device__ __forceinline__ bool phase_final(const Params& P, int n, unsigned starts, const Smem& sm)
 {
     if (blockIdx.x != 0) return true;
     const StepDesc* D = P.desc;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int S = P.S;
-    for (int i = warp; i < n; i += NWARP) {
-        const int a = argmax_partials_warp(P, i, am_tag);
-        if (a < 0) return false;
-        const int p = D->pos[i], slot = D->slot[i];
-        if (lane < NSTREAM) {
-            const int k = lane;
-            const int f = p - P.delays[k];
-            int c;
-            if (k == S) {
-                int forced = -1;
-                if (f == p) forced = D->codes[i][S];
-                else if (f >= 0) forced = ld_cg_int(P.hist + ((size_t)slot * NSTREAM + S) * HIST + f % HIST);
-                c = forced >= 0 ? forced : a;
-                P.code_argmax[i * 16 + (S - 1)] = a;
-            } else {
-                c = P.chosen[i * NSTREAM + k];
-            }
-            if (f >= 0) P.hist[((size_t)slot * NSTREAM + k) * HIST + f % HIST] = c;
-            if (k == 0) P.text_out[i] = c;
-            else P.codes_out[i * 16 + (k - 1)] = f >= 0 ? c : -1;
+    const int S = P.S, G = P.G;
+    int* am = sm.X;  // [n][S + 1]: text head, then the head of substep 0 .. S-1
+    int ok = 1;
+    for (int it = warp; it < n * (S + 1) && ok; it += NWARP) {
+        const int i = it / (S + 1), t = it % (S + 1) - 1;
+        int a;
+        if (t < 0) {
+            a = argmax_partials_warp(P, P.amax + (size_t)i * G * 2, G, phase_tag(D, P.dep_ph0 - 1));
+        } else {
+            const int g = group_of(starts, t);
+            int j0, nj, b0, b1;
+            group_bounds(starts, S, g, j0, nj);
+            substep_ctas(G, nj, t - j0, b0, b1);
+            a = argmax_partials_warp(P, P.damax + ((size_t)i * S + t) * G * 2, b1 - b0,
+                                     phase_tag(D, P.dep_ph0 + (g + 1) * P.dep_ph_stride - 1));
         }
+        ok = a >= 0;
+        if (lane == 0) am[it] = a;
+    }
+    if (!csync_and(ok)) return false;
+    for (int it = threadIdx.x; it < n * NSTREAM; it += NT) {
+        const int i = it / NSTREAM, k = it % NSTREAM;
+        const int p = D->pos[i], slot = D->slot[i];
+        const int f = p - P.delays[k];
+        const int a = am[i * (S + 1) + k];  // stream k's head: the text head, or substep k-1's
+        const int sup = supplied_token(P, i, k);
+        const int c = sup >= 0 ? sup : a;
+        if (k == 0) P.text_argmax[i] = a;
+        else P.code_argmax[i * 16 + (k - 1)] = a;
+        if (f >= 0) P.hist[((size_t)slot * NSTREAM + k) * HIST + f % HIST] = c;
+        if (k == 0) P.text_out[i] = c;
+        else P.codes_out[i * 16 + (k - 1)] = f >= 0 ? c : -1;
     }
     return true;
 }
@@ -1427,57 +1507,78 @@ __device__ __forceinline__ bool phase_final(const Params& P, int n, unsigned am_
 // ------------------------------------------------------------------ phase dispatch
 
 template <typename TW, typename TKV, int BG>
-__device__ __forceinline__ bool run_phase(const Params& P, const Phase ph, int phi, int n, const Smem& sm, unsigned& stage)
+__device__ __forceinline__ bool run_phase(const Params& P, Phase ph, int phi, int n, unsigned starts, const Smem& sm,
+                                          unsigned& stage)
 {
-    const int d = P.d, F = P.F, dd = P.dd, dF = P.dF;
+    const int d = P.d, F = P.F, dd = P.dd, dF = P.dF, S = P.S;
     const StepDesc* D = P.desc;
     const unsigned tag = phase_tag(D, phi);
     const unsigned in_tag = ph.in_ph >= 0 ? phase_tag(D, ph.in_ph) : 0u;
     const unsigned res_tag = ph.res_ph >= 0 ? phase_tag(D, ph.res_ph) : 0u;
+    int c, cnt;
+    if (!resolve(P, starts, ph, c, cnt)) return true;
+    const int j = ph.j;  // depformer: this CTA's substep
     switch (ph.type) {
         case PH_EMBED: phase_embed<TW>(P, n, tag, sm); return true;
         case PH_QKV:
             prefetch_kv_windows<TKV>(P, ph.l, n);
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, in_tag, P.attn_norm + (size_t)ph.l * d, nullptr, 0, nullptr, 0},
+            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.x, d, in_tag, P.attn_norm + (size_t)ph.l * d},
                                       n, sm, stage, EpiQKV<TKV>{ph.l, tag});
         case PH_ATTN: return phase_attn<TKV>(P, ph.l, n, in_tag, tag, sm);
         case PH_O:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.o, d, in_tag, nullptr, nullptr, 0, nullptr, 0}, n, sm, stage,
-                                      EpiResid{P.x, d, res_tag, tag});
+            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.o, d, in_tag}, n, sm, stage, EpiResid{P.x, d, res_tag, tag});
         case PH_GU:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, in_tag, P.ffn_norm + (size_t)ph.l * d, nullptr, 0, nullptr, 0},
+            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.x, d, in_tag, P.ffn_norm + (size_t)ph.l * d},
                                       n, sm, stage, EpiSwiglu{P.s, F, tag});
         case PH_DOWN:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.s, F, in_tag, nullptr, nullptr, 0, nullptr, 0}, n, sm, stage,
-                                      EpiResid{P.x, d, res_tag, tag});
+            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.s, F, in_tag}, n, sm, stage, EpiResid{P.x, d, res_tag, tag});
         case PH_HEAD:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.x, d, in_tag, P.out_norm, nullptr, 0, nullptr, 0}, n, sm, stage,
-                                      EpiLogits{P.logits, P.V, P.V, P.yin, (long long)P.S * dd, tag});
+            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.x, d, in_tag, P.out_norm}, n, sm, stage,
+                                      EpiLogits{P.logits, P.V, P.V, P.yin, (long long)S * dd, tag, P.amax,
+                                                (long long)P.G * 2, (int)blockIdx.x});
         case PH_DQKV: {
+            const long long us = (long long)S * dd;
             XSrc xs;
             if (ph.l == 0) {
-                const void* add = ph.j == 0 ? P.dep_emb_text
-                                            : (const void*)((const TW*)P.dep_emb_audio + (size_t)(ph.j - 1) * P.C * dd);
-                xs = XSrc{P.yin + (size_t)ph.j * dd, (long long)P.S * dd, in_tag, P.dep_attn_norm, add, dd, P.u, tag};
+                // the residual starts as in-projection + embedding of the substep's input token
+                const void* add = j == 0 ? P.dep_emb_text : (const void*)((const TW*)P.dep_emb_audio + (size_t)(j - 1) * P.C * dd);
+                xs = XSrc{P.yin + (size_t)j * dd, us, in_tag, P.dep_attn_norm, add, dd, c == 0 ? P.u + (size_t)j * dd : nullptr,
+                          tag, us, j, ph.pad0, 0u, 0};
+                if (j == ph.pad0) {
+                    if (j == 0) {
+                        xs.am_tag = phase_tag(D, P.dep_ph0 - 1);  // the text head
+                        xs.am_cnt = P.G;
+                    } else {
+                        // the last substep of the group before: its head's partials
+                        const int g = group_of(starts, j);
+                        int pj0, pnj, b0, b1;
+                        group_bounds(starts, S, g - 1, pj0, pnj);
+                        substep_ctas(P.G, pnj, pnj - 1, b0, b1);
+                        xs.am_tag = phase_tag(D, P.dep_ph0 + g * P.dep_ph_stride - 1);
+                        xs.am_cnt = b1 - b0;
+                    }
+                }
             } else {
-                xs = XSrc{P.u, dd, in_tag, P.dep_attn_norm + (size_t)ph.l * dd, nullptr, 0, nullptr, 0};
+                xs = XSrc{P.u + (size_t)j * dd, us, in_tag, P.dep_attn_norm + (size_t)ph.l * dd};
             }
-            return gemv_phase<TW, BG>(P, ph, xs, n, sm, stage, EpiDQKV{ph.l, ph.j, tag});
+            return gemv_phase<TW, BG>(P, ph, c, cnt, xs, n, sm, stage, EpiDQKV{ph.l, j, tag});
         }
-        case PH_DATTN: return phase_dattn(P, ph.l, ph.j, n, in_tag, tag, sm);
+        case PH_DATTN: return phase_dattn(P, ph.l, ph.pad0, ph.pad1, starts, n, in_tag, tag, sm);
         case PH_DO:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.dat, dd, in_tag, nullptr, nullptr, 0, nullptr, 0}, n, sm, stage,
-                                      EpiResid{P.u, dd, res_tag, tag});
+            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.dat + (size_t)j * dd, (long long)S * dd, in_tag}, n, sm, stage,
+                                      EpiResid{P.u + (size_t)j * dd, (long long)S * dd, res_tag, tag});
         case PH_DGU:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.u, dd, in_tag, P.dep_ffn_norm + (size_t)ph.l * dd, nullptr, 0, nullptr, 0},
-                                      n, sm, stage, EpiSwiglu{P.ds, dF, tag});
+            return gemv_phase<TW, BG>(P, ph, c, cnt,
+                                      XSrc{P.u + (size_t)j * dd, (long long)S * dd, in_tag, P.dep_ffn_norm + (size_t)ph.l * dd},
+                                      n, sm, stage, EpiSwiglu{P.ds + (size_t)j * dF, (long long)S * dF, tag});
         case PH_DDOWN:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.ds, dF, in_tag, nullptr, nullptr, 0, nullptr, 0}, n, sm, stage,
-                                      EpiResid{P.u, dd, res_tag, tag});
+            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.ds + (size_t)j * dF, (long long)S * dF, in_tag}, n, sm, stage,
+                                      EpiResid{P.u + (size_t)j * dd, (long long)S * dd, res_tag, tag});
         case PH_DHEAD:
-            return gemv_phase<TW, BG>(P, ph, XSrc{P.u, dd, in_tag, P.dep_out_norm, nullptr, 0, nullptr, 0}, n, sm, stage,
-                                      EpiLogits{P.dlogits + (size_t)ph.j * P.C, (long long)P.S * P.C, P.C, nullptr, 0, tag});
-        case PH_FINAL: return phase_final(P, n, phase_tag(D, ph.am_ph));
+            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.u + (size_t)j * dd, (long long)S * dd, in_tag, P.dep_out_norm}, n, sm,
+                                      stage, EpiLogits{P.dlogits + (size_t)j * P.C, (long long)S * P.C, P.C, nullptr, 0, tag,
+                                                       P.damax + (size_t)j * P.G * 2, (long long)S * P.G * 2, c});
+        case PH_FINAL: return phase_final(P, n, starts, sm);
         default: return true;
     }
 }
@@ -1517,10 +1618,29 @@ __global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int
             bad = 1;
         }
     }
+    // depformer groups of this step: bit j of `known` stays set while every
+    // slot supplies stream j's input token (read before any history write of
+    // the step; the fence orders these reads before this CTA's later stores)
+    if (threadIdx.x == 0) sm.misc[1] = 0xFFFF;
+    __syncthreads();
+    if (ph1 > P.dep_ph0 && !bad) {
+        for (int it = threadIdx.x; it < n * (P.S - 1); it += blockDim.x) {
+            const int i = it / (P.S - 1), k = 1 + it % (P.S - 1);
+            if (supplied_token(P, i, k) < 0) atomicAnd((unsigned*)&sm.misc[1], ~(1u << k));
+        }
+    }
+    __threadfence();
     __syncthreads();  // barrier init visible to every thread; all threads agree on `bad`
     if (bad) return;
+    unsigned starts = 1u;
+    {
+        const unsigned known = (unsigned)sm.misc[1];
+        int j0 = 0;
+        for (int k = 1; k < P.S; ++k)
+            if (!((known >> k) & 1u) || k - j0 >= MAXGW) { starts |= 1u << k; j0 = k; }
+    }
     if ((threadIdx.x >> 5) == NWARP) {
-        if ((threadIdx.x & 31) == 0) producer<TW, BG>(P, ph0, ph1, n, sm);
+        if ((threadIdx.x & 31) == 0) producer<TW, BG>(P, ph0, ph1, n, starts, sm);
         return;
     }
     unsigned stage = 0;
@@ -1528,7 +1648,7 @@ __global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int
         if (threadIdx.x == 0) sm.misc[0] = ph;  // phase index for the in-phase stamps
         stamp(P, ph, 0);
         const Phase phs = P.phases[ph];
-        if (!run_phase<TW, TKV, BG>(P, phs, ph, n, sm, stage)) return;
+        if (!run_phase<TW, TKV, BG>(P, phs, ph, n, starts, sm, stage)) return;
         stamp(P, ph, 3);
         // diagnostics: the latest end of this phase over all CTAs
         if (P.ptime && threadIdx.x == 0) atomicMax(P.ptime + (size_t)ph * 8 + 6, globaltimer_ns());
