@@ -143,9 +143,18 @@ static int check_config(mfs_ctx* c, const mfs_config& g)
         return fail(c, MFS_E_ARG, "config: dep_head_dim must be 64 and dep_heads * 64 == dep_d");
     const int Ks[4] = {g.d, g.ffn, g.dep_d, g.dep_ffn};
     const int wbytes = g.weight_dtype == MFS_DTYPE_BF16 ? 2 : 4;
-    for (int K : Ks)
+    for (int K : Ks) {
         if (K % 8 != 0 || K > 12288 || K * wbytes > STAGE_BYTES)
             return fail(c, MFS_E_ARG, "config: K dimension %d not a multiple of 8, or a row exceeds %d bytes", K, STAGE_BYTES);
+        // every row of a stage must fit the registers of the warp that takes it
+        const int nwk = slice_warps(K), nwr = NWARP / nwk;
+        const int nvw = (K / 8 + nwk - 1) / nwk, vpl = (nvw + 31) / 32;
+        int rps = STAGE_BYTES / (K * wbytes);
+        rps = rps < RPS_MAX ? rps : RPS_MAX;
+        if ((rps + nwr - 1) / nwr > rows_per_warp_cap(vpl_class_of(vpl)))
+            return fail(c, MFS_E_ARG, "config: K dimension %d gives %d rows per warp and stage (at most %d)", K,
+                        (rps + nwr - 1) / nwr, rows_per_warp_cap(vpl_class_of(vpl)));
+    }
     if (g.text_vocab % 2 || g.card % 2) return fail(c, MFS_E_ARG, "config: vocabularies must be even");
     if (g.max_slots < 1 || g.max_slots > MFS_MAX_SLOTS) return fail(c, MFS_E_ARG, "config: max_slots out of range");
     if (g.weight_dtype != MFS_DTYPE_F32 && g.weight_dtype != MFS_DTYPE_BF16) return fail(c, MFS_E_ARG, "config: weight_dtype");

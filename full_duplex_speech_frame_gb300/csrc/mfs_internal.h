@@ -9,11 +9,28 @@ namespace mfs {
 
 constexpr int NT = 256;          // consumer threads per CTA (8 warps); one more warp produces
 constexpr int NWARP = NT / 32;
-constexpr int STAGE_BYTES = 24576;  // one weight ring stage
+// One weight ring stage.  Large stages amortise the consumers' per-stage cost
+// (barrier, copy to registers, row reductions); four of them keep 192 KB of
+// weights in flight per SM.
+constexpr int STAGE_BYTES = 49152;
 constexpr int RPS_MAX = 16;      // rows per stage at most
 // Ring depth per batch group: the per-row partial sums grow with the group, the ring shrinks.
-__host__ __device__ constexpr unsigned nstage_for(int bg) { return bg <= 2 ? 8u : 7u; }
+__host__ __device__ constexpr unsigned nstage_for(int bg) { return bg <= 2 ? 4u : 3u; }
 constexpr int SMEM_HEAD = 1024;  // mbarriers and scalars before the ring
+
+// Matrix-vector K-slicing, shared by the kernels and the host's config check:
+// nwk warps split K (the largest power of two <= NWARP that leaves >= 32
+// vectors of 8 weights per slice), NWARP / nwk warps split the rows of a stage.
+__host__ __device__ inline int slice_warps(int K)
+{
+    int nwk = NWARP;
+    while (nwk > 1 && (K / 8) / nwk < 32) nwk >>= 1;
+    return nwk;
+}
+// vectors per lane, rounded up to an instantiated width (1, 2 or 6)
+__host__ __device__ constexpr int vpl_class_of(int vpl) { return vpl <= 1 ? 1 : (vpl == 2 ? 2 : 6); }
+// rows of one stage a warp holds in registers at most, per width
+__host__ __device__ constexpr int rows_per_warp_cap(int vplc) { return vplc <= 2 ? 8 : 2; }
 constexpr int NSTREAM = MFS_N_STREAMS;
 constexpr int NCHUNK_MAX = 32;   // attention split over the window, per (slot, head)
 constexpr int HIST = 3;          // frames of token history per stream

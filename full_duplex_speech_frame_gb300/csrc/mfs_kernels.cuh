@@ -433,8 +433,7 @@ struct GemvCfg {
 __device__ __forceinline__ GemvCfg gemv_cfg(int K)
 {
     const int NV = K / 8;
-    int nwk = NWARP;
-    while (nwk > 1 && NV / nwk < 32) nwk >>= 1;
+    const int nwk = slice_warps(K);
     GemvCfg c;
     c.nwk = nwk;
     c.nwr = NWARP / nwk;
@@ -444,7 +443,7 @@ __device__ __forceinline__ GemvCfg gemv_cfg(int K)
 }
 
 // vectors per lane, rounded up to an instantiated width
-__device__ __forceinline__ int vpl_class(int vpl) { return vpl <= 1 ? 1 : (vpl == 2 ? 2 : 6); }
+__device__ __forceinline__ int vpl_class(int vpl) { return vpl_class_of(vpl); }
 
 // batch rows per pass: the input slice (8 * vpl * rows floats) stays in registers
 template <int BG>
@@ -807,7 +806,7 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
         const TW* ring = (const TW*)(sm.ring + (size_t)slot * STAGE_BYTES);
         // copy this warp's rows of the stage into registers, release the stage at
         // once (the producer refills it while the arithmetic runs), then compute
-        constexpr int RW = VPL <= 2 ? 8 : 2;   // rows per warp per stage, at most
+        constexpr int RW = rows_per_warp_cap(VPL);  // rows per warp per stage, at most (checked at create)
         constexpr int U4 = sizeof(TW) == 2 ? 1 : 2;  // 16-byte words per vector of 8 weights
         uint4 wv[RW][VPL][U4];
 #pragma unroll
