@@ -343,13 +343,12 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
     const size_t T8 = sizeof(uint2);  // tagged element
     const size_t a_x = areg(MS * d * T8), a_q = areg(MS * d * T8), a_kc = areg(MS * d * T8), a_vc = areg(MS * d * T8);
     const size_t a_o = areg(MS * d * T8), a_s = areg(MS * F * T8);
+    const size_t a_ap = areg(MS * H * NCHUNK_MAX * (hd + 2) * T8);
     const size_t a_lg = areg(MS * V * 4), a_yin = areg(MS * S * dd * T8), a_u = areg(MS * S * dd * T8);
     const size_t a_dq = areg(MS * S * dd * T8), a_dkv = areg(MS * dL * S * 2 * dd * T8), a_dat = areg(MS * S * dd * T8);
     const size_t a_ds = areg(MS * S * dF * T8), a_dlg = areg(MS * S * C * 4);
     const size_t a_am = areg(MS * c->G * 2 * T8), a_dam = areg(MS * S * c->G * 2 * T8);
     const size_t a_to = areg(MS * 4), a_co = areg(MS * 16 * 4), a_ta = areg(MS * 4), a_ca = areg(MS * 16 * 4);
-    (void)H;
-    (void)hd;
     CK(cudaMalloc((void**)&c->act, ao));
     CK(cudaMemset(c->act, 0, ao));
 
@@ -430,7 +429,7 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
     P.kc = c->kc; P.vc = c->vc; P.hist = c->hist; P.desc = c->d_desc;
     char* A = c->act;
     P.x = (uint2*)(A + a_x); P.q = (uint2*)(A + a_q); P.kcur = (uint2*)(A + a_kc); P.vcur = (uint2*)(A + a_vc);
-    P.o = (uint2*)(A + a_o); P.s = (uint2*)(A + a_s);
+    P.o = (uint2*)(A + a_o); P.s = (uint2*)(A + a_s); P.attp = (uint2*)(A + a_ap);
     P.logits = (float*)(A + a_lg); P.yin = (uint2*)(A + a_yin); P.u = (uint2*)(A + a_u);
     P.dq = (uint2*)(A + a_dq); P.dkv = (uint2*)(A + a_dkv); P.dat = (uint2*)(A + a_dat);
     P.ds = (uint2*)(A + a_ds); P.dlogits = (float*)(A + a_dlg); P.amax = (uint2*)(A + a_am);
@@ -447,7 +446,9 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
         // ring, then one region used as GEMV partials + row values, attention
         // partials, or the step's embedding rows, whichever phase runs
         const size_t gemv = (size_t)c->maxrows * bg * (NWARP + 1) * sizeof(float);
-        const size_t attn = (size_t)NWARP * (g.head_dim + 4) * sizeof(float);
+        const size_t attn_w = (size_t)NWARP * (g.head_dim + 4) * sizeof(float);
+        const size_t attn_m = (size_t)NCHUNK_MAX * (g.head_dim + 2) * sizeof(float);  // chunk merge
+        const size_t attn = attn_w > attn_m ? attn_w : attn_m;
         const size_t emb = (size_t)MFS_MAX_SLOTS * NSTREAM * sizeof(int);
         size_t region = gemv > attn ? gemv : attn;
         region = region > emb ? region : emb;

@@ -105,6 +105,7 @@ struct Params {
     uint2* kcur;     // [MS][d]  this step's rotated keys (rounded to the ring's type)
     uint2* vcur;     // [MS][d]  this step's values (rounded to the ring's type)
     uint2* o;        // [MS][d]  attention output
+    uint2* attp;     // [MS][H][NCHUNK_MAX][hd + 2] per-chunk attention partials: max, sum, outputs
     uint2* s;        // [MS][F]  SwiGLU output
     float* logits;   // [MS][V]  (diagnostics)
     uint2* yin;      // [MS][S][dd]  depformer in-projections

@@ -766,25 +766,14 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
         }
     }
     if (xs.g) {
-        // RMSNorm factor: sums of squares per K-slice, combined in slice order
+        // RMSNorm: sums of squares per K-slice; the factor (a scalar per batch
+        // row) multiplies the row sums after the weight stages, so no warp waits
+        // for the others' inputs before streaming
 #pragma unroll
         for (int b = 0; b < BGV; ++b) {
             const float q = warp_sum(ssq[b]);
             if (lane == 0 && rw == 0) sm.ssq[b * 16 + kw] = q;
         }
-        if (!csync_and(ok)) return false;
-#pragma unroll
-        for (int b = 0; b < BGV; ++b) {
-            float tot = 0.f;
-            for (int k = 0; k < c.nwk; ++k) tot += sm.ssq[b * 16 + k];
-            const float rb = rsqrtf(tot / (float)K + P.eps);
-#pragma unroll
-            for (int t = 0; t < VPL; ++t)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) xr[t][b][e] *= rb;
-        }
-    } else if (!csync_and(ok)) {
-        return false;
     }
     if (P.ptime) stamp(P, sm.misc[0], 1);
 
@@ -891,13 +880,19 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
         }
     }
     if (P.ptime) stamp(P, sm.misc[0], 2);
-    csync();
-    // sum the K-slices in slice order
+    if (!csync_and(ok)) return false;
+    // sum the K-slices in slice order; then the RMSNorm factor, its sums of
+    // squares also combined in slice order
     for (int it = tid; it < (r1 - r0) * nb; it += NT) {
         const int rl = it / nb, b = it % nb;
         const float* rp = sm.red + ((size_t)rl * BGV + b) * NWARP;
         float y = 0.f;
         for (int k = 0; k < c.nwk; ++k) y += rp[k];
+        if (xs.g) {
+            float tot = 0.f;
+            for (int k = 0; k < c.nwk; ++k) tot += sm.ssq[b * 16 + k];
+            y *= rsqrtf(tot / (float)K + P.eps);
+        }
         sm.yf[(size_t)rl * BGV + b] = y;
     }
     csync();
@@ -1247,9 +1242,41 @@ __device__ __forceinline__ void prefetch_kv_windows(const Params& P, int l, int 
     }
 }
 
-// One CTA per (batch row, head); its 16 warps split the window into 16
-// contiguous runs of keys (a split that depends on the window length only),
-// and the partial softmax states are merged in shared memory in warp order.
+// Chunks of a window of len keys: about 64 keys each, but no more than the
+// grid holds for one slot's heads at once (G / H), nor NCHUNK_MAX.  A function
+// of the slot's own window and the context's shape only, so a slot's result
+// never depends on the other slots of the step.
+__device__ __forceinline__ int attn_chunks(int len, int G, int H)
+{
+    int c = (len + 63) / 64;
+    const int cap = G / H > 1 ? G / H : 1;
+    c = c < cap ? c : cap;
+    return c < NCHUNK_MAX ? c : NCHUNK_MAX;
+}
+
+// Work items of the step's attention: (batch row i, head h, chunk c), row-major.
+__device__ __forceinline__ void attn_item(const StepDesc* D, int n, int H, int W, int G, int item, int& i, int& h,
+                                          int& c, int& nch, int& len)
+{
+    int base = 0;
+    for (i = 0; i < n; ++i) {
+        const int p = D->pos[i];
+        len = p + 1 < W ? p + 1 : W;
+        nch = attn_chunks(len, G, H);
+        if (item < base + nch * H) break;
+        base += nch * H;
+    }
+    const int r = item - base;
+    h = r / nch;
+    c = r % nch;
+}
+
+// One CTA per (batch row, head, chunk of the window): its warps split the
+// chunk into contiguous runs of keys, merged in shared memory in warp order.
+// A window of one chunk writes the output directly; otherwise each chunk
+// leaves {max, sum, unnormalised output} tagged in P.attp and the CTA that ran
+// chunk 0 merges the chunks in order once every CTA has run its chunks (no CTA
+// waits for another's chunk before finishing its own, so the waits end).
 // The newest key/value (this step's) comes from the tagged copy.
 template <typename TKV>
 __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsigned in_tag, unsigned tag, const Smem& sm)
@@ -1262,12 +1289,19 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
     const int grp = lane / LPP, gl = lane % LPP;
     const float scale = rsqrtf((float)hd);
     const int wstride = hd + 4;
-    for (int item = blockIdx.x; item < n * H; item += P.G) {
-        const int i = item / H, h = item % H;
+    const size_t pstride = (size_t)hd + 2;  // partial: max, sum, hd outputs
+    int total = 0;
+    for (int i = 0; i < n; ++i) {
+        const int p = D->pos[i];
+        total += attn_chunks(p + 1 < W ? p + 1 : W, P.G, H) * H;
+    }
+    for (int item = blockIdx.x; item < total; item += P.G) {
+        int i, h, c, nch, len;
+        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len);
         const int p = D->pos[i], slot = D->slot[i];
-        const int len = p + 1 < W ? p + 1 : W;
         const int start = p - len + 1;
-        const int j0 = (int)((long long)len * warp / NWARP), j1 = (int)((long long)len * (warp + 1) / NWARP);
+        const int k0 = (int)((long long)len * c / nch), k1 = (int)((long long)len * (c + 1) / nch);
+        const int j0 = k0 + (int)((long long)(k1 - k0) * warp / NWARP), j1 = k0 + (int)((long long)(k1 - k0) * (warp + 1) / NWARP);
         const long long kvbase = ((long long)slot * P.L + l) * (long long)W * d + h * hd + gl * 8;
         // the query and this step's key/value are polled while the first ring loads are in flight
         uint2 qt[8], kt[8], vt[8];
@@ -1357,10 +1391,11 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
             for (int e = 0; e < 8; ++e) wb[4 + gl * 8 + e] = acc[e];
         }
         if (!csync_and(ok)) return false;
-        // merge the 16 warps in warp order
+        // merge the warps in warp order
+        float M = -INFINITY;
+        for (int w = 0; w < NWARP; ++w) M = fmaxf(M, sm.wbuf[(size_t)w * wstride]);
+        uint2* part = P.attp + (((size_t)i * H + h) * NCHUNK_MAX + c) * pstride;
         for (int e = threadIdx.x; e < hd; e += NT) {
-            float M = -INFINITY;
-            for (int w = 0; w < NWARP; ++w) M = fmaxf(M, sm.wbuf[(size_t)w * wstride]);
             float L = 0.f, a = 0.f;
             for (int w = 0; w < NWARP; ++w) {
                 const float mw = sm.wbuf[(size_t)w * wstride];
@@ -1368,6 +1403,55 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
                 const float f = expf(mw - M);
                 L += sm.wbuf[(size_t)w * wstride + 1] * f;
                 a += sm.wbuf[(size_t)w * wstride + 4 + e] * f;
+            }
+            if (nch == 1) {
+                st_tag1(P.o + (size_t)i * d + h * hd + e, __float_as_uint(a / L), tag);
+            } else {
+                st_tag1(part + 2 + e, __float_as_uint(a), tag);
+                if (e == 0) {
+                    st_tag1(part, __float_as_uint(M), tag);
+                    st_tag1(part + 1, __float_as_uint(L), tag);
+                }
+            }
+        }
+        csync();
+    }
+    // merges: the CTA that ran chunk 0 of a split window combines its chunks in order
+    for (int item = blockIdx.x; item < total; item += P.G) {
+        int i, h, c, nch, len;
+        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len);
+        if (c != 0 || nch == 1) continue;
+        const uint2* part = P.attp + ((size_t)i * H + h) * NCHUNK_MAX * pstride;
+        // every chunk's partial into shared memory, four loads in flight per thread
+        float* mb = sm.wbuf;  // [nch][hd + 2]
+        const int cnt = nch * (int)pstride;
+        int ok = 1;
+        for (int x0 = threadIdx.x; x0 < cnt && ok; x0 += 4 * NT) {
+            uint2 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int x = x0 + u * NT;
+                v[u] = x < cnt ? ld_tag1(part + (x / pstride) * pstride + x % pstride) : make_uint2(0u, tag);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int x = x0 + u * NT;
+                unsigned bits = v[u].x;
+                if (x < cnt && v[u].y != tag && ok) ok = wait_tag1(part + (x / pstride) * pstride + x % pstride, tag, bits, P.err);
+                if (x < cnt) mb[x] = __uint_as_float(bits);
+            }
+        }
+        if (!csync_and(ok)) return false;
+        for (int e = threadIdx.x; e < hd; e += NT) {
+            float M = -INFINITY;
+            for (int k = 0; k < nch; ++k) M = fmaxf(M, mb[k * pstride]);
+            float L = 0.f, a = 0.f;
+            for (int k = 0; k < nch; ++k) {
+                const float mk = mb[k * pstride];
+                if (mk == -INFINITY) continue;
+                const float f = expf(mk - M);
+                L += mb[k * pstride + 1] * f;
+                a += mb[k * pstride + 2 + e] * f;
             }
             st_tag1(P.o + (size_t)i * d + h * hd + e, __float_as_uint(a / L), tag);
         }

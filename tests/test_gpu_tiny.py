@@ -69,6 +69,35 @@ def test_tiny_free_running_config(mfs):
     assert compared >= 16, f"only {compared} frames matched token for token"
 
 
+def test_tiny_long_window_split_attention(mfs):
+    """W = 200 with two slots at different positions (a 150-frame prompt on one): windows
+    of more than 64 keys are split into chunks and merged; one slot wraps a W = 200 ring
+    after a 190-frame prompt.  Compared with the oracle, and slot 1 alone is bit-identical."""
+    s = tiny(window=200, max_slots=3)
+    w = synth.make_weights(s, 6, gain_std=0.1)
+    ctx = H.gpu_context(s, w)
+    orc = oracle.Oracle(s, w)
+    pr0 = synth.forced_frames(s, 6, synth.STREAM_PROMPT, 150, 1)[:, 0]
+    pr1 = synth.forced_frames(s, 7, synth.STREAM_PROMPT, 190, 1)[:, 0]
+    mfs.mfs_prefill(ctx, [0], pr0[None])
+    mfs.mfs_prefill(ctx, [1], pr1[None])
+    mfs.mfs_prefill(ctx, [2], pr1[None])
+    orc.prefill(0, pr0)
+    orc.prefill(1, pr1)
+    z = synth.forced_frames(s, 8, synth.STREAM_FORCED, 16, 2)
+    for p in range(16):
+        text, codes = mfs.mfs_step(ctx, [0, 1], z[p])
+        dbg = mfs.mfs_read_debug(ctx)
+        ref = orc.step([0, 1], z[p], want_logits=True)
+        H.check_logits(dbg["text_logits"], ref["text_logits"], f"text logits, frame {p}")
+        H.check_logits(dbg["dep_logits"], ref["dep_logits"], f"depformer logits, frame {p}")
+        np.testing.assert_array_equal(codes, ref["codes"])
+        t2, c2 = mfs.mfs_step(ctx, [2], z[p][1:2])
+        d2 = mfs.mfs_read_debug(ctx)
+        assert np.array_equal(d2["text_logits"][0], dbg["text_logits"][1])
+        assert np.array_equal(d2["dep_logits"][0], dbg["dep_logits"][1])
+
+
 def test_tiny_ring_wraps(mfs):
     """W = 8 over 40 frames: every step after the 8th wraps the ring."""
     s = tiny(window=8)
