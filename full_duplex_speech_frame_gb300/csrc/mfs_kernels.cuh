@@ -563,7 +563,13 @@ __device__ __forceinline__ void producer(const Params& P, int ph0, int ph1, int 
     const uint64_t pol = l2_evict_first();
     unsigned s = 0;
     bool ok = true;
+    const int dep_end = P.dep_ph0 + n_groups(starts) * P.dep_ph_stride;
+    const int dep_all = P.dep_ph0 + P.S * P.dep_ph_stride;
     for (int ph = ph0; ph < ph1 && ok; ++ph) {
+        if (ph == dep_end && dep_end < dep_all) {
+            ph = dep_all - 1;  // nothing to stream for absent groups
+            continue;
+        }
         const TW* W;
         int N, K, c, cnt;
         Phase q = P.phases[ph];
@@ -1215,30 +1221,35 @@ __device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes, uint6
     asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(p), "r"(bytes), "l"(pol) : "memory");
 }
 
-// While the QKV phase of layer l runs, the CTAs that will run that layer's
-// attention pull the older keys/values of their (row, head) windows into L2,
-// so the attention reads hit L2 instead of queueing behind the weight stream.
-// Only for windows small enough to sit in L2 (at most 32 MB per layer).
+// While the QKV phase of layer l runs, the older keys/values of every slot's
+// window are pulled into L2, one whole ring row (all heads, d elements) per
+// prefetch, spread evenly over the CTAs of the grid, so that the attention reads
+// hit L2 instead of queueing behind the weight stream.  Only for windows small
+// enough to sit in L2 (at most 32 MB per layer).
 template <typename TKV>
 __device__ __forceinline__ void prefetch_kv_windows(const Params& P, int l, int n)
 {
     const StepDesc* D = P.desc;
-    const int H = P.H, hd = P.hd, d = P.d, W = P.W;
+    const int d = P.d, W = P.W;
     long long total = 0;
-    for (int i = 0; i < n; ++i) total += (long long)(D->pos[i] + 1 < W ? D->pos[i] + 1 : W);
-    if (total * H * hd * (long long)sizeof(TKV) * 2 > (32ll << 20)) return;
+    for (int i = 0; i < n; ++i) total += (long long)(D->pos[i] + 1 < W ? D->pos[i] : W - 1);
+    if (total * d * (long long)sizeof(TKV) * 2 > (32ll << 20)) return;
     const uint64_t pol = l2_evict_last();
-    for (int item = blockIdx.x; item < n * H; item += P.G) {
-        const int i = item / H, h = item % H;
-        const int p = D->pos[i], slot = D->slot[i];
-        const int len = p + 1 < W ? p + 1 : W;
-        const int start = p - len + 1;
-        const long long base = ((long long)slot * P.L + l) * (long long)W * d + h * hd;
-        for (int k = threadIdx.x; k < 2 * (len - 1); k += NT) {
-            const int j = k >> 1;
-            const long long off = base + (long long)((start + j) % W) * d;
-            prefetch_l2((const TKV*)((k & 1) ? P.vc : P.kc) + off, (unsigned)(hd * sizeof(TKV)), pol);
+    const unsigned row_bytes = (unsigned)(d * sizeof(TKV));
+    int i = 0, base = 0;
+    // row k goes to CTA k mod G, so that no SM's copy engine queues more than a few rows
+    for (long long k = blockIdx.x + (long long)P.G * threadIdx.x; k < 2 * total; k += (long long)P.G * NT) {
+        const int j = (int)(k >> 1);  // older position j of the concatenated windows
+        int len = D->pos[i] + 1 < W ? D->pos[i] : W - 1;
+        while (j >= base + len) {  // k only grows: walk the slots forward
+            base += len;
+            ++i;
+            len = D->pos[i] + 1 < W ? D->pos[i] : W - 1;
         }
+        const int p = D->pos[i];
+        const int q = p - len + (j - base);  // absolute position, p - len .. p - 1
+        const long long off = (((long long)D->slot[i] * P.L + l) * (long long)W + q % W) * d;
+        prefetch_l2((const TKV*)((k & 1) ? P.vc : P.kc) + off, row_bytes, pol);
     }
 }
 
@@ -1727,7 +1738,14 @@ __global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int
         return;
     }
     unsigned stage = 0;
+    // depformer phases of groups that do not exist this step are skipped as a block
+    const int dep_end = P.dep_ph0 + n_groups(starts) * P.dep_ph_stride;
+    const int dep_all = P.dep_ph0 + P.S * P.dep_ph_stride;
     for (int ph = ph0; ph < ph1; ++ph) {
+        if (ph == dep_end && dep_end < dep_all) {
+            ph = dep_all;
+            if (ph >= ph1) break;
+        }
         if (threadIdx.x == 0) sm.misc[0] = ph;  // phase index for the in-phase stamps
         stamp(P, ph, 0);
         const Phase phs = P.phases[ph];
