@@ -173,15 +173,18 @@ def max_over_ranks(v, world):
     return float(t.item())
 
 
-def cpu_oracle_sample(frames=6, prompt=8):
+def cpu_oracle_sample(frames=6, prompt=8, warmup=0):
     """Time the CPU oracle on a bounded sample of the workload: a short forced
-    prompt (untimed), then `frames` decode frames (timed)."""
+    prompt and `warmup` decode frames (untimed), then `frames` decode frames (timed)."""
     import oracle
     s = WORKLOAD.shape
     w = synth.make_weights(s, WORKLOAD.weight_seed)
     orc = oracle.Oracle(s, w)
     orc.prefill(0, synth.forced_frames(s, WORKLOAD.input_seed, synth.STREAM_PROMPT, prompt, 1)[:, 0])
-    u = synth.user_frames(s, WORKLOAD.input_seed, frames, 1)
+    u = synth.user_frames(s, WORKLOAD.input_seed, warmup + frames, 1)
+    for p in range(warmup):
+        orc.step([0], u[p])
+    u = u[warmup:]
     t0 = time.perf_counter()
     for p in range(frames):
         orc.step([0], u[p])
@@ -196,9 +199,10 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     frames = max(1, min(args.steps, 30))
-    cb = cpu_oracle_sample(frames=frames)
+    cb = cpu_oracle_sample(frames=frames, warmup=min(args.warmup, 3))
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": UNIT, "n_gpus": args.gpus,
-            "steps": frames, "warmup": 0, "ms_per_step": 1000.0 / cb["value"], "higher_is_better": True,
+            "steps": frames, "warmup": min(args.warmup, 3), "ms_per_step": 1000.0 / cb["value"],
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": "full_b1: full PersonaPlex shape, bf16 weights N(0,0.02) seed 0, B=1, "
                                    "forced prompt then decode frames, greedy", "batch": 1},
