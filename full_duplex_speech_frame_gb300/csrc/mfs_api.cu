@@ -876,6 +876,14 @@ extern "C" int mfs_set_mode(mfs_ctx* c, int mode)
     return MFS_OK;
 }
 
+extern "C" int mfs_set_skip_settled(mfs_ctx* c, int on)
+{
+    if (!c) return MFS_E_ARG;
+    if (on != 0 && on != 1) return fail(c, MFS_E_ARG, "skip_settled must be 0 or 1");
+    c->P.skip_settled = on;
+    return MFS_OK;
+}
+
 extern "C" int mfs_launches_per_step(const mfs_ctx* c)
 {
     if (!c) return MFS_E_ARG;

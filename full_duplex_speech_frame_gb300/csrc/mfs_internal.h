@@ -121,6 +121,7 @@ struct Params {
     int* codes_out;  // [MS][16]
     int* text_argmax;  // [MS]
     int* code_argmax;  // [MS][16]
+    int skip_settled;  // skip trailing depformer substeps whose outputs are all settled
     int dep_ph0;       // index of the first depformer phase
     int dep_ph_stride; // phases per depformer group (dL x 5 + head)
     // control

@@ -499,13 +499,16 @@ __device__ __forceinline__ int supplied_token(const Params& P, int i, int k)
     return -1;
 }
 
-__device__ __forceinline__ int n_groups(unsigned starts) { return __popc(starts); }
-__device__ __forceinline__ int group_of(unsigned starts, int t) { return __popc(starts & ((2u << t) - 1u)) - 1; }
+// `starts` packs the group boundaries (bits 0..15: a group begins at substep j;
+// a set bit past the last group that runs marks where the run stops) and, in
+// bits 24..28, the number of groups that run this step.
+__device__ __forceinline__ int n_groups(unsigned starts) { return (int)((starts >> 24) & 31u); }
+__device__ __forceinline__ int group_of(unsigned starts, int t) { return __popc(starts & 0xFFFFu & ((2u << t) - 1u)) - 1; }
 
 // first substep j0 and width nj of group g
 __device__ __forceinline__ void group_bounds(unsigned starts, int S, int g, int& j0, int& nj)
 {
-    unsigned m = starts;
+    unsigned m = starts & 0xFFFFu;
     for (int k = 0; k < g; ++k) m &= m - 1u;
     j0 = __ffs(m) - 1;
     m &= m - 1u;
@@ -1570,6 +1573,8 @@ __device__ __forceinline__ bool phase_final(const Params& P, int n, unsigned sta
         int a;
         if (t < 0) {
             a = argmax_partials_warp(P, P.amax + (size_t)i * G * 2, G, phase_tag(D, P.dep_ph0 - 1));
+        } else if (group_of(starts, t) >= n_groups(starts)) {
+            a = -1;  // substep skipped: its stream's output is settled without it
         } else {
             const int g = group_of(starts, t);
             int j0, nj, b0, b1;
@@ -1578,7 +1583,7 @@ __device__ __forceinline__ bool phase_final(const Params& P, int n, unsigned sta
             a = argmax_partials_warp(P, P.damax + ((size_t)i * S + t) * G * 2, b1 - b0,
                                      phase_tag(D, P.dep_ph0 + (g + 1) * P.dep_ph_stride - 1));
         }
-        ok = a >= 0;
+        ok = a >= 0 || (t >= 0 && group_of(starts, t) >= n_groups(starts));
         if (lane == 0) am[it] = a;
     }
     if (!csync_and(ok)) return false;
@@ -1715,12 +1720,19 @@ __global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int
     // depformer groups of this step: bit j of `known` stays set while every
     // slot supplies stream j's input token (read before any history write of
     // the step; the fence orders these reads before this CTA's later stores)
-    if (threadIdx.x == 0) sm.misc[1] = 0xFFFF;
+    // Bit k of `given` stays set while every slot's output for stream k is
+    // settled without the depformer: supplied, or for a frame before 0.
+    if (threadIdx.x == 0) {
+        sm.misc[1] = 0xFFFF;
+        sm.misc[2] = 0x1FFFE;
+    }
     __syncthreads();
     if (ph1 > P.dep_ph0 && !bad) {
-        for (int it = threadIdx.x; it < n * (P.S - 1); it += blockDim.x) {
-            const int i = it / (P.S - 1), k = 1 + it % (P.S - 1);
-            if (supplied_token(P, i, k) < 0) atomicAnd((unsigned*)&sm.misc[1], ~(1u << k));
+        for (int it = threadIdx.x; it < n * P.S; it += blockDim.x) {
+            const int i = it / P.S, k = 1 + it % P.S;
+            const int t = supplied_token(P, i, k);
+            if (t < 0 && k < P.S) atomicAnd((unsigned*)&sm.misc[1], ~(1u << k));
+            if (t < 0 && D->pos[i] - P.delays[k] >= 0) atomicAnd((unsigned*)&sm.misc[2], ~(1u << k));
         }
     }
     __threadfence();
@@ -1728,10 +1740,16 @@ __global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int
     if (bad) return;
     unsigned starts = 1u;
     {
-        const unsigned known = (unsigned)sm.misc[1];
+        const unsigned known = (unsigned)sm.misc[1], given = (unsigned)sm.misc[2];
+        // substeps [jend, S) only produce settled outputs: skipped when the context allows
+        int jend = P.S;
+        if (P.skip_settled)
+            while (jend > 0 && ((given >> jend) & 1u)) --jend;
         int j0 = 0;
         for (int k = 1; k < P.S; ++k)
-            if (!((known >> k) & 1u) || k - j0 >= MAXGW) { starts |= 1u << k; j0 = k; }
+            if (k == jend || !((known >> k) & 1u) || k - j0 >= MAXGW) { starts |= 1u << k; j0 = k; }
+        const int ngr = jend == 0 ? 0 : __popc(starts & ((1u << jend) - 1u));
+        starts |= (unsigned)ngr << 24;
     }
     if ((threadIdx.x >> 5) == NWARP) {
         if ((threadIdx.x & 31) == 0) producer<TW, BG>(P, ph0, ph1, n, starts, sm);

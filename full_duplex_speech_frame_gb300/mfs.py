@@ -59,6 +59,7 @@ def _load_library():
         "mfs_read_debug": (ci, [vp, vp, vp, vp, vp]),
         "mfs_set_mode": (ci, [vp, ci]),
         "mfs_launches_per_step": (ci, [vp]),
+        "mfs_set_skip_settled": (ci, [vp, ci]),
         "mfs_set_timing": (ci, [vp, ci]),
         "mfs_kernel_time": (ci, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
         "mfs_phase_times": (ci, [vp, vp, ci]),
@@ -237,6 +238,11 @@ def mfs_read_debug(ctx: Ctx, n: Optional[int] = None) -> dict:
 
 def mfs_set_mode(ctx: Ctx, mode: int) -> None:
     _check(ctx, _lib.mfs_set_mode(ctx.handle, int(mode)))
+
+
+def mfs_set_skip_settled(ctx: Ctx, on: bool) -> None:
+    """Skip trailing depformer substeps whose outputs are all supplied (include/mfs.h)."""
+    _check(ctx, _lib.mfs_set_skip_settled(ctx.handle, int(bool(on))))
 
 
 def mfs_launches_per_step(ctx: Ctx) -> int:

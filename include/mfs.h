@@ -172,6 +172,18 @@ int mfs_read_debug(mfs_ctx* ctx, float* text_logits, float* dep_logits,
  * arithmetic, for diagnosis). */
 int mfs_set_mode(mfs_ctx* ctx, int mode);
 
+/* Depformer substeps whose every output is settled without them (mobius PR
+ * #368, "P3 - ONNX Runtime example": substep j yields the code of stream j+1;
+ * SGLang-Omni cookbook, PersonaPlex, "Known limitations": the depformer steps
+ * run after the backbone each frame).  With on = 1, a step skips the trailing
+ * substeps j..15 when, for every slot, the tokens of streams j+1..16 are
+ * supplied (or belong to frames before 0): the substeps are causal, so the
+ * earlier substeps and every output are unchanged.  In decode with the user
+ * streams supplied this skips substeps 8..15 (about 1.3 GB of weights per
+ * step).  Skipped substeps leave no logits and report argmax -1 in
+ * mfs_read_debug.  Default 0: all 16 substeps run. */
+int mfs_set_skip_settled(mfs_ctx* ctx, int on);
+
 /* Kernel launches made by the last step (for accounting). */
 int mfs_launches_per_step(const mfs_ctx* ctx);
 

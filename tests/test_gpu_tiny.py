@@ -282,3 +282,37 @@ def test_device_resident_step_and_deferred_token_error(mfs):
         tb, cb = mfs.mfs_step(b, [1, 0], u[p])
         np.testing.assert_array_equal(ta, tb)
         np.testing.assert_array_equal(ca, cb)
+
+
+def test_tiny_skip_settled_substeps(mfs):
+    """With trailing settled substeps skipped (user streams supplied in decode: substeps 8..15),
+    every output and the logits of the substeps that run are bit-identical to the full run;
+    a fully supplied frame skips the whole depformer.  The full run is checked against the oracle."""
+    s = tiny(max_slots=2)
+    w = synth.make_weights(s, 9, gain_std=0.1)
+    a, b = H.gpu_context(s, w), H.gpu_context(s, w)
+    mfs.mfs_set_skip_settled(b, True)
+    orc = oracle.Oracle(s, w)
+    u = synth.user_frames(s, 9, 12, 2)
+    z = synth.forced_frames(s, 9, synth.STREAM_FORCED, 3, 2)
+    frames = np.concatenate([u, z, u[:3]], axis=0)
+    for p in range(frames.shape[0]):
+        ta, ca = mfs.mfs_step(a, [0, 1], frames[p])
+        da = mfs.mfs_read_debug(a)
+        tb, cb = mfs.mfs_step(b, [0, 1], frames[p])
+        db = mfs.mfs_read_debug(b)
+        ref = orc.step([0, 1], frames[p], want_logits=True)
+        H.check_logits(da["dep_logits"], ref["dep_logits"], f"depformer logits, frame {p}")
+        np.testing.assert_array_equal(ta, tb)
+        np.testing.assert_array_equal(ca, cb)
+        np.testing.assert_array_equal(da["text_logits"], db["text_logits"])
+        ran = db["code_argmax"][0] >= 0
+        # stream k is settled when its token for frame p - delay[k] was supplied (or that frame is < 0)
+        settled = [all((frames[p][i][k] >= 0) if s.delays[k] == 0 else (p == 0 or frames[p - 1][i][k] >= 0)
+                       for i in range(2)) for k in range(17)]
+        jend = 16
+        while jend > 0 and settled[jend]:
+            jend -= 1
+        assert np.array_equal(ran, np.arange(16) < jend), f"frame {p}: substeps run {np.flatnonzero(ran)}, want < {jend}"
+        np.testing.assert_array_equal(da["dep_logits"][:, ran], db["dep_logits"][:, ran])
+        np.testing.assert_array_equal(da["code_argmax"][:, ran], db["code_argmax"][:, ran])
