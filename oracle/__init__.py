@@ -63,7 +63,10 @@ def _load():
         lib.orc_set_weight.argtypes = [vp, ctypes.c_char_p, vp, ctypes.c_longlong]
         lib.orc_reset_slot.argtypes = [vp, ci]
         lib.orc_position.argtypes = [vp, ci]
-        lib.orc_step.argtypes = [vp, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.orc_step.argtypes = [vp, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.orc_set_sampling.argtypes = [vp, ci, ctypes.c_double, ci, ctypes.c_double, ci]
+        lib.orc_sample_topk.restype = ci
+        lib.orc_sample_topk.argtypes = [vp, ci, ctypes.c_double, ci, ctypes.c_double]
         lib.orc_prefill.argtypes = [vp, ci, ci, vp]
         lib.orc_import_slot.argtypes = [vp, ci, vp, ctypes.c_longlong]
         lib.orc_export_slot.argtypes = [vp, ci, vp, ctypes.c_longlong]
@@ -161,8 +164,14 @@ class Oracle:
         if self._lib.orc_reset_slot(self._h, slot) != 0:
             raise ValueError("bad slot")
 
-    def step(self, slots, codes, want_logits: bool = False, want_tokens: bool = False):
-        """codes [n,17] int (-1 = generate).  Returns a dict of numpy arrays."""
+    def set_sampling(self, slot: int, text_temp: float, text_k: int, audio_temp: float, audio_k: int) -> None:
+        if self._lib.orc_set_sampling(self._h, slot, text_temp, text_k, audio_temp, audio_k) != 0:
+            raise ValueError("bad slot")
+
+    def step(self, slots, codes, want_logits: bool = False, want_tokens: bool = False, uniforms=None):
+        """codes [n,17] int (-1 = generate); uniforms [n,17] in [0, 1) switches on the
+        slots' sampling (stream k of row i draws with uniforms[i][k]).  Returns numpy arrays."""
+        unif = None if uniforms is None else np.ascontiguousarray(uniforms, np.float64).reshape(len(slots), 17)
         slots = np.ascontiguousarray(slots, np.int32)
         codes = np.ascontiguousarray(codes, np.int32).reshape(len(slots), 17)
         n, s = len(slots), self.shape
@@ -177,7 +186,7 @@ class Oracle:
                                 out["text"].ctypes.data, out["codes"].ctypes.data,
                                 _ptr(out.get("text_logits")), _ptr(out.get("dep_logits")),
                                 out["text_argmax"].ctypes.data, out["code_argmax"].ctypes.data,
-                                _ptr(out.get("x_tokens")))
+                                _ptr(out.get("x_tokens")), _ptr(unif))
         if rc != 0:
             raise ValueError(f"orc_step: {self._lib.orc_last_error(self._h).decode()} ({rc})")
         return out
@@ -187,3 +196,9 @@ class Oracle:
         rc = self._lib.orc_prefill(self._h, slot, codes.shape[0], codes.ctypes.data)
         if rc != 0:
             raise ValueError(f"orc_prefill: {self._lib.orc_last_error(self._h).decode()} ({rc})")
+
+
+def sample_topk(logits, temp: float, k: int, u: float) -> int:
+    """The oracle's temperature + top-k draw for one logit vector (fp64)."""
+    lg = np.ascontiguousarray(logits, np.float64).reshape(-1)
+    return int(_load().orc_sample_topk(lg.ctypes.data, lg.size, float(temp), int(k), float(u)))

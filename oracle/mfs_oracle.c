@@ -75,6 +75,9 @@ typedef struct {
     int hist[ORC_STREAMS][ORC_HIST];
     double* K; /* [n_layers][cap][d] */
     double* V;
+    /* sampling (k <= 1 or temperature <= 0: greedy) */
+    double text_temp, audio_temp;
+    int text_k, audio_k;
 } orc_slot;
 
 typedef struct {
@@ -249,6 +252,47 @@ static int argmax(const double* v, int n)
 
 static int mod(int a, int m) { int r = a % m; return r < 0 ? r + m : r; }
 
+/* Temperature + top-k sampling (mobius PR #368, commit note replacing greedy
+ * argmax: text temperature 0.7 / top_k 25, audio 0.8 / 250; SGLang-Omni
+ * cookbook, PersonaPlex, "Stage sampling": each request draws from its own
+ * generator).  The candidates are the k largest logits (ties: lower index
+ * first), weighted exp((logit - max) / temp).  With u in [0, 1) the token is
+ * the first candidate, in ascending index order, at which the running sum of
+ * weights exceeds u times their total; a draw from the candidates'
+ * distribution for uniform u.  k <= 1 or temp <= 0 is the argmax. */
+int orc_sample_topk(const double* lg, int n, double temp, int k, double u)
+{
+    if (k <= 1 || temp <= 0.0) return argmax(lg, n);
+    if (k > n) k = n;
+    /* membership: logit greater, or equal with a lower index, than fewer than k others */
+    unsigned char* in = (unsigned char*)calloc((size_t)n, 1);
+    /* partial selection sort on (value desc, index asc): k passes */
+    for (int r = 0; r < k; ++r) {
+        int best = -1;
+        for (int i = 0; i < n; ++i) {
+            if (in[i]) continue;
+            if (best < 0 || lg[i] > lg[best]) best = i;
+        }
+        in[best] = 1;
+    }
+    double mx = lg[argmax(lg, n)];
+    double tot = 0.0;
+    for (int i = 0; i < n; ++i)
+        if (in[i]) tot += exp((lg[i] - mx) / temp);
+    double target = u * tot, run = 0.0;
+    int tok = -1;
+    for (int i = 0; i < n && tok < 0; ++i) {
+        if (!in[i]) continue;
+        run += exp((lg[i] - mx) / temp);
+        if (run > target) tok = i;
+    }
+    if (tok < 0) /* u * tot rounded up to tot: the last candidate */
+        for (int i = n - 1; i >= 0 && tok < 0; --i)
+            if (in[i]) tok = i;
+    free(in);
+    return tok;
+}
+
 /* ------------------------------------------------------------------ lifecycle */
 
 orc* orc_create(const orc_config* c)
@@ -368,6 +412,17 @@ int orc_export_slot(orc* o, int slot, void* buf, long long nbytes)
             memcpy(vout + 4 * i, &vf, 4);
         }
     }
+    return 0;
+}
+
+/* Sampling parameters of a slot (k <= 1 or temp <= 0: greedy); used by
+ * orc_step when it is given uniforms. */
+int orc_set_sampling(orc* o, int slot, double text_temp, int text_k, double audio_temp, int audio_k)
+{
+    if (slot < 0 || slot >= o->c.max_slots) return -1;
+    orc_slot* s = &o->slots[slot];
+    s->text_temp = text_temp; s->text_k = text_k;
+    s->audio_temp = audio_temp; s->audio_k = audio_k;
     return 0;
 }
 
@@ -545,7 +600,7 @@ static void embed(orc* o, orc_slot* s, const int* codes, double* x, int* x_token
 
 /* depformer for one slot; h[d] is the temporal output, t the text token. */
 static void depformer(orc* o, orc_slot* s, const double* h, int t, int* codes_out,
-                      double* logits_out, int* argmax_out)
+                      double* logits_out, int* argmax_out, const double* unif)
 {
     const orc_config* c = &o->c;
     int p = s->pos, d = c->d, dd = c->dep_d, dF = c->dep_ffn, C = c->card, S = c->dep_steps;
@@ -597,7 +652,8 @@ static void depformer(orc* o, orc_slot* s, const double* h, int t, int* codes_ou
         if (argmax_out) argmax_out[j] = chat;
         int f = p - c->delays[k];
         int forced = f >= 0 ? s->hist[k][mod(f, ORC_HIST)] : -1;
-        int chosen = forced >= 0 ? forced : chat;
+        int drawn = unif ? orc_sample_topk(lg, C, s->audio_temp, s->audio_k, unif[k]) : chat;
+        int chosen = forced >= 0 ? forced : drawn;
         if (f >= 0) {
             s->hist[k][mod(f, ORC_HIST)] = chosen;
             codes_out[j] = chosen;
@@ -625,7 +681,7 @@ static int check_tokens(orc* o, const int* codes, int allow_generate)
  * code_argmax [n][16], x_tokens [n][17] (embedding rows read by S1). */
 int orc_step(orc* o, int n, const int* slots, const int* codes, int* text_out, int* codes_out,
              double* text_logits, double* dep_logits, int* text_argmax, int* code_argmax,
-             int* x_tokens)
+             int* x_tokens, const double* unif)
 {
     const orc_config* c = &o->c;
     if (!weights_ready(o)) { snprintf(o->err, sizeof o->err, "weights missing"); return -3; }
@@ -648,12 +704,14 @@ int orc_step(orc* o, int n, const int* slots, const int* codes, int* text_out, i
         if (text_logits) memcpy(text_logits + (size_t)i * V, lg, sizeof(double) * (size_t)V);
         int that = argmax(lg, V);
         if (text_argmax) text_argmax[i] = that;
-        int t = cd[0] >= 0 ? cd[0] : that;
+        const double* ui = unif ? unif + (size_t)i * ORC_STREAMS : NULL;
+        int tdraw = ui ? orc_sample_topk(lg, V, s->text_temp, s->text_k, ui[0]) : that;
+        int t = cd[0] >= 0 ? cd[0] : tdraw;
         s->hist[0][mod(s->pos, ORC_HIST)] = t;
         text_out[i] = t;
         depformer(o, s, h, t, codes_out + (size_t)i * (ORC_STREAMS - 1),
                   dep_logits ? dep_logits + (size_t)i * c->dep_steps * c->card : NULL,
-                  code_argmax ? code_argmax + (size_t)i * c->dep_steps : NULL);
+                  code_argmax ? code_argmax + (size_t)i * c->dep_steps : NULL, ui);
         s->pos += 1;
     }
     free(x); free(h); free(lg);

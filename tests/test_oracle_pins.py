@@ -354,3 +354,72 @@ def test_slot_state_import_continues_exactly():
     bad[4:8] = np.frombuffer(np.int32(s.max_pos + 1).tobytes(), np.uint8)
     with pytest.raises(ValueError):
         b.import_slot(1, bad)
+
+
+# ---------------------------------------------------------------- sampling heads
+
+def _topk_probs(lg, temp, k):
+    """Closed form: the k largest logits (ties to the lower index), softmax of logit / temp."""
+    order = sorted(range(len(lg)), key=lambda i: (-lg[i], i))[:k]
+    z = np.array([lg[i] for i in order]) / temp
+    p = np.exp(z - z.max())
+    return dict(zip(order, p / p.sum()))
+
+
+def test_sampler_greedy_limits():
+    rng = np.random.default_rng(1)
+    lg = rng.standard_normal(300)
+    for u in (0.0, 0.3, 0.999):
+        assert oracle.sample_topk(lg, 0.7, 1, u) == int(np.argmax(lg))
+        assert oracle.sample_topk(lg, 0.0, 25, u) == int(np.argmax(lg))
+        assert oracle.sample_topk(lg, 1e-9, 25, u) == int(np.argmax(lg))
+
+
+def test_sampler_equal_logits_ties_to_lower_indices():
+    lg = np.zeros(50)
+    for m in range(10):
+        assert oracle.sample_topk(lg, 0.8, 10, (m + 0.5) / 10) == m
+
+
+def test_sampler_matches_the_closed_form_distribution():
+    rng = np.random.default_rng(2)
+    lg = rng.standard_normal(40) * 2.0
+    lg[7] = lg[11]  # a tie inside the candidate set
+    for temp, k in ((0.8, 7), (0.7, 25), (1.3, 40)):
+        exact = _topk_probs(lg, temp, k)
+        grid = 20000
+        counts = {}
+        for g in range(grid):
+            t = oracle.sample_topk(lg, temp, k, (g + 0.5) / grid)
+            counts[t] = counts.get(t, 0) + 1
+        assert set(counts) <= set(exact)
+        for i, p in exact.items():
+            assert abs(counts.get(i, 0) / grid - p) <= 2.0 / grid, (temp, k, i)
+
+
+def test_sampler_temperature_scales_logits():
+    rng = np.random.default_rng(3)
+    lg = rng.standard_normal(200)
+    for u in np.linspace(0.01, 0.99, 60):
+        assert oracle.sample_topk(lg, 2.0, 30, u) == oracle.sample_topk(lg / 2.0, 1.0, 30, u)
+
+
+def test_sampled_step_draws_from_its_own_logits(tiny_w8):
+    """A sampled oracle step picks the text token and each generated code with the sampler
+    applied to that step's logits and the row's uniforms; k = 1 is the greedy step."""
+    s, w = tiny_w8
+    u = synth.user_frames(s, 51, 6, 1)
+    unif = (synth.uniform_int(51, 77, 6 * 17, 0, 1 << 24).reshape(6, 1, 17) + 0.5) / float(1 << 24)
+    a, b = oracle.Oracle(s, w), oracle.Oracle(s, w)
+    a.set_sampling(0, 0.7, 25, 0.8, 250)
+    b.set_sampling(0, 0.7, 1, 0.8, 1)
+    g = oracle.Oracle(s, w)
+    for p in range(6):
+        r = a.step([0], u[p], want_logits=True, uniforms=unif[p])
+        assert r["text"][0] == oracle.sample_topk(r["text_logits"][0], 0.7, 25, unif[p][0][0])
+        # substep 0 yields stream 1 (delay 0): drawn from its logits with stream 1's uniform
+        assert r["codes"][0][0] == oracle.sample_topk(r["dep_logits"][0][0], 0.8, 250, unif[p][0][1])
+        rb = b.step([0], u[p], want_logits=True, uniforms=unif[p])
+        rg = g.step([0], u[p], want_logits=True)
+        for key in ("text", "codes", "text_logits", "dep_logits"):
+            np.testing.assert_array_equal(rb[key], rg[key])
