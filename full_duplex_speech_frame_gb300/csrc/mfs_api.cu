@@ -69,6 +69,7 @@ struct mfs_ctx {
     int desc_next = 0;
     StepDesc* h_pref = nullptr;
     int* h_out = nullptr;        // text [MS] | codes [MS*16] | err | err_seq
+    float* h_unif = nullptr;     // pinned staging of a sampled step's uniforms [MS][17]
     // state
     Params P;
     int nphase = 0, nphase_prefill = 0;
@@ -349,6 +350,7 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
     const size_t a_ds = areg(MS * S * dF * T8), a_dlg = areg(MS * S * C * 4);
     const size_t a_am = areg(MS * c->G * 2 * T8), a_dam = areg(MS * S * c->G * 2 * T8);
     const size_t a_to = areg(MS * 4), a_co = areg(MS * 16 * 4), a_ta = areg(MS * 4), a_ca = areg(MS * 16 * 4);
+    const size_t a_sc = areg(MS * sizeof(SampleCfg)), a_un = areg(MS * NSTREAM * 4), a_dr = areg(MS * NSTREAM * 4);
     CK(cudaMalloc((void**)&c->act, ao));
     CK(cudaMemset(c->act, 0, ao));
 
@@ -412,6 +414,7 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
     for (int i = 0; i < DESC_RING; ++i) CK(cudaEventCreateWithFlags(&c->desc_ev[i], cudaEventDisableTiming));
     CK(cudaHostAlloc((void**)&c->h_pref, PREF_CHUNK * sizeof(StepDesc), cudaHostAllocDefault));
     CK(cudaHostAlloc((void**)&c->h_out, (MFS_MAX_SLOTS * 17 + 2) * sizeof(int), cudaHostAllocDefault));
+    CK(cudaHostAlloc((void**)&c->h_unif, MFS_MAX_SLOTS * NSTREAM * sizeof(float), cudaHostAllocDefault));
 
     Params& P = c->P;
     P.d = g.d; P.L = g.n_layers; P.H = g.n_heads; P.hd = g.head_dim; P.F = g.ffn; P.V = g.text_vocab;
@@ -435,6 +438,7 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
     P.ds = (uint2*)(A + a_ds); P.dlogits = (float*)(A + a_dlg); P.amax = (uint2*)(A + a_am);
     P.damax = (uint2*)(A + a_dam); P.text_out = (int*)(A + a_to); P.codes_out = (int*)(A + a_co);
     P.text_argmax = (int*)(A + a_ta); P.code_argmax = (int*)(A + a_ca);
+    P.samp = (const SampleCfg*)(A + a_sc); P.unif = (const float*)(A + a_un); P.drawn = (int*)(A + a_dr);
     P.err = c->d_err; P.err_seq = c->d_err + 1;
     P.phases = c->d_phases;
 
@@ -450,8 +454,10 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
         const size_t attn_m = (size_t)NCHUNK_MAX * (g.head_dim + 2) * sizeof(float);  // chunk merge
         const size_t attn = attn_w > attn_m ? attn_w : attn_m;
         const size_t emb = (size_t)MFS_MAX_SLOTS * NSTREAM * sizeof(int);
+        const size_t samp = (size_t)(2048 + MFS_MAX_SLOTS * NSTREAM) * sizeof(int);  // sampler histogram + final argmaxes
         size_t region = gemv > attn ? gemv : attn;
         region = region > emb ? region : emb;
+        region = region > samp ? region : samp;
         c->smem[i] = SMEM_HEAD + (size_t)nstage_for(bg) * STAGE_BYTES + region;
         if (c->smem[i] > 227 * 1024) return fail(c, MFS_E_ARG, "shape needs %zu B of shared memory", c->smem[i]);
         CK(cudaFuncSetAttribute(c->kfn[i], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c->smem[i]));
@@ -498,7 +504,7 @@ extern "C" void mfs_destroy(mfs_ctx* c)
     for (int i = 0; i < DESC_RING; ++i)
         if (c->desc_ev[i]) cudaEventDestroy(c->desc_ev[i]);
     for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
-    cudaFreeHost(c->h_desc); cudaFreeHost(c->h_pref); cudaFreeHost(c->h_out);
+    cudaFreeHost(c->h_desc); cudaFreeHost(c->h_pref); cudaFreeHost(c->h_out); cudaFreeHost(c->h_unif);
     if (c->own_stream && c->stream) cudaStreamDestroy(c->stream);
     delete c;
 }
@@ -659,6 +665,7 @@ static int fill_desc(mfs_ctx* c, StepDesc* h, int n, const int32_t* slots, const
 {
     h->n = n;
     h->seq = ++c->seq;
+    h->sampled = 0;
     for (int i = 0; i < n; ++i) {
         h->slot[i] = slots[i];
         h->pos[i] = c->pos[slots[i]] + frame_off;
@@ -667,8 +674,46 @@ static int fill_desc(mfs_ctx* c, StepDesc* h, int n, const int32_t* slots, const
     return MFS_OK;
 }
 
+static int step_host(mfs_ctx* c, int n, const int32_t* slots, const int32_t* in_codes, const float* uniforms,
+                     int32_t* text_tok, int32_t* codes);
+
 extern "C" int mfs_step(mfs_ctx* c, int n, const int32_t* slots, const int32_t* in_codes, int32_t* text_tok,
                         int32_t* codes)
+{
+    return step_host(c, n, slots, in_codes, nullptr, text_tok, codes);
+}
+
+extern "C" int mfs_step_sampled(mfs_ctx* c, int n, const int32_t* slots, const int32_t* in_codes, const float* uniforms,
+                                int32_t* text_tok, int32_t* codes)
+{
+    if (!c) return MFS_E_ARG;
+    if (!uniforms) return fail(c, MFS_E_ARG, "null uniforms");
+    for (int i = 0; i < n * NSTREAM; ++i)
+        if (!(uniforms[i] >= 0.f && uniforms[i] < 1.f)) return fail(c, MFS_E_ARG, "uniform %d outside [0, 1)", i);
+    return step_host(c, n, slots, in_codes, uniforms, text_tok, codes);
+}
+
+extern "C" int mfs_set_sampling(mfs_ctx* c, int slot, float text_temp, int text_topk, float audio_temp, int audio_topk)
+{
+    if (!c) return MFS_E_ARG;
+    if (slot < 0 || slot >= c->cfg.max_slots) return fail(c, MFS_E_SLOT, "slot %d outside [0, %d)", slot, c->cfg.max_slots);
+    if (text_topk < 0 || audio_topk < 0 || !(text_temp >= 0.f) || !(audio_temp >= 0.f))
+        return fail(c, MFS_E_ARG, "sampling: temperatures and top-k must be >= 0");
+    if (!c->pending.empty()) {
+        int rc = mfs_sync(c);
+        if (rc != MFS_OK) return rc;
+    }
+    SampleCfg cfg;
+    cfg.text_inv_t = text_temp > 0.f ? 1.f / text_temp : 0.f;
+    cfg.text_k = text_topk;
+    cfg.audio_inv_t = audio_temp > 0.f ? 1.f / audio_temp : 0.f;
+    cfg.audio_k = audio_topk;
+    CK(cudaMemcpy((SampleCfg*)c->P.samp + slot, &cfg, sizeof cfg, cudaMemcpyHostToDevice));
+    return MFS_OK;
+}
+
+static int step_host(mfs_ctx* c, int n, const int32_t* slots, const int32_t* in_codes, const float* uniforms,
+                     int32_t* text_tok, int32_t* codes)
 {
     if (!c) return MFS_E_ARG;
     if (!c->pending.empty()) {
@@ -683,6 +728,12 @@ extern "C" int mfs_step(mfs_ctx* c, int n, const int32_t* slots, const int32_t* 
     int di;
     StepDesc* h = next_desc(c, &di);
     fill_desc(c, h, n, slots, in_codes, 0);
+    if (uniforms) {
+        h->sampled = 1;
+        memcpy(c->h_unif, uniforms, (size_t)n * NSTREAM * sizeof(float));
+        CK(cudaMemcpyAsync((float*)c->P.unif, c->h_unif, (size_t)n * NSTREAM * sizeof(float), cudaMemcpyHostToDevice,
+                           c->stream));
+    }
     CK(cudaMemcpyAsync(c->d_desc, h, sizeof(StepDesc), cudaMemcpyHostToDevice, c->stream));
     CK(cudaEventRecord(c->desc_ev[di], c->stream));
     if ((rc = launch(c, n, c->nphase, c->d_desc))) return rc;

@@ -62,13 +62,23 @@ struct Phase {
 
 // Written by the host before each launch.
 struct StepDesc {
-    int n, seq, pad0, pad1;
+    int n, seq;
+    int sampled;  // 1: generated tokens of slots with sampling on are drawn with P.unif
+    int pad1;
     int slot[MFS_MAX_SLOTS];
     int pos[MFS_MAX_SLOTS];
     int codes[MFS_MAX_SLOTS][NSTREAM];
 };
 
 enum DeviceError : int { DERR_NONE = 0, DERR_TOKEN = 1, DERR_WAIT = 2 };
+
+// Per-slot sampling: temperature as its inverse, top-k (k <= 1 or inv_t <= 0: greedy).
+struct SampleCfg {
+    float text_inv_t;
+    int text_k;
+    float audio_inv_t;
+    int audio_k;
+};
 
 struct Params {
     // shape
@@ -117,6 +127,9 @@ struct Params {
     float* dlogits;  // [MS][S][C]  (diagnostics)
     uint2* amax;     // [MS][G][2] text head argmax partials per CTA: {value, tag}, {index, tag}
     uint2* damax;    // [MS][S][G][2] depformer head argmax partials per substep and CTA
+    const SampleCfg* samp;  // [max_slots] by slot
+    const float* unif;      // [MS][17] this step's uniforms in [0, 1), by row (sampled steps)
+    int* drawn;             // [MS][17] tokens drawn this step (CTA 0), by row
     int* text_out;   // [MS]
     int* codes_out;  // [MS][16]
     int* text_argmax;  // [MS]

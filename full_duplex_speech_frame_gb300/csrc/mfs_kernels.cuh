@@ -641,6 +641,174 @@ __device__ __forceinline__ int argmax_partials_warp(const Params& P, const uint2
     return ix == 0x7fffffff ? 0 : ix;
 }
 
+// ------------------------------------------------------------------ sampling heads
+// Temperature + top-k draw for one logit row, by every consumer thread of the
+// CTA: candidates are the k largest logits (ties to the lower index), weighted
+// exp((logit - max) / T); the token is the first candidate, in ascending index
+// order, at which the running sum of weights exceeds u times their total.  The
+// k-th largest key comes from a three-level radix select (11, 11, 10 bits);
+// each thread owns a contiguous run of indices, so thread order is index order.
+
+__device__ __forceinline__ unsigned order_key(float f)
+{
+    const unsigned b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// exclusive scan of one value per consumer thread, in thread order
+template <typename T>
+__device__ __forceinline__ T cta_exclusive_scan(T v, T& total, T* scratch)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    T x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const T y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) scratch[warp] = x;
+    csync();
+    T before = 0, tot = 0;
+    for (int w = 0; w < NWARP; ++w) {
+        const T sw = scratch[w];
+        if (w < warp) before += sw;
+        tot += sw;
+    }
+    csync();
+    total = tot;
+    return before + x - v;
+}
+
+// Among the keys whose bits above pre_shift equal `pre` (pre_shift 32: all),
+// the digit of width `bits` at `shift` holding the rank-th largest (1-based);
+// rank becomes the rank inside that digit.
+__device__ __forceinline__ int radix_level(const float* lg, int c0, int c1, unsigned pre, int pre_shift, int shift, int bits,
+                                           int& rank, unsigned* hist, unsigned* scratch, int* misc)
+{
+    const int nb = 1 << bits;
+    for (int b = threadIdx.x; b < nb; b += NT) hist[b] = 0u;
+    csync();
+    for (int i = c0; i < c1; ++i) {
+        const unsigned key = order_key(__ldcg(lg + i));
+        if (pre_shift >= 32 || (key >> pre_shift) == pre) atomicAdd(&hist[(key >> shift) & (unsigned)(nb - 1)], 1u);
+    }
+    csync();
+    const int per = nb / NT;                      // digits per thread; thread 0 owns the largest
+    const int d0 = nb - (threadIdx.x + 1) * per;
+    unsigned sum = 0u;
+    for (int q = 0; q < per; ++q) sum += hist[d0 + q];
+    unsigned total;
+    const unsigned above = cta_exclusive_scan(sum, total, scratch);
+    if (above < (unsigned)rank && (unsigned)rank <= above + sum) {
+        unsigned acc = above;
+        for (int q = per - 1; q >= 0; --q) {
+            const unsigned h = hist[d0 + q];
+            if ((unsigned)rank <= acc + h) {
+                misc[0] = d0 + q;
+                misc[1] = rank - (int)acc;
+                break;
+            }
+            acc += h;
+        }
+    }
+    csync();
+    rank = misc[1];
+    return misc[0];
+}
+
+__device__ __noinline__ int sample_topk_cta(const float* lg, int N, float inv_t, int k, float u, const Smem& sm)
+{
+    unsigned* hist = (unsigned*)sm.red;         // [2048]
+    unsigned* su = (unsigned*)sm.amv;           // [NWARP] scan scratch
+    float* sf = sm.amv;
+    int* misc = sm.misc + 4;                    // [4]
+    const int CH = (N + NT - 1) / NT;
+    const int c0 = min(N, (int)threadIdx.x * CH), c1 = min(N, c0 + CH);
+    if (k > N) k = N;
+    float mx = -INFINITY;
+    for (int i = c0; i < c1; ++i) mx = fmaxf(mx, __ldcg(lg + i));
+    mx = warp_max(mx);
+    if ((threadIdx.x & 31) == 0) sf[threadIdx.x >> 5] = mx;
+    csync();
+    mx = sf[0];
+    for (int w = 1; w < NWARP; ++w) mx = fmaxf(mx, sf[w]);
+    csync();
+    int rank = k;
+    const unsigned b1 = (unsigned)radix_level(lg, c0, c1, 0u, 32, 21, 11, rank, hist, su, misc);
+    const unsigned b2 = (unsigned)radix_level(lg, c0, c1, b1, 21, 10, 11, rank, hist, su, misc);
+    const unsigned b3 = (unsigned)radix_level(lg, c0, c1, (b1 << 11) | b2, 10, 0, 10, rank, hist, su, misc);
+    const unsigned kth = (b1 << 21) | (b2 << 10) | b3;
+    const unsigned need_eq = (unsigned)rank;    // candidates among the keys equal to kth, lowest indices first
+    unsigned ceq = 0u;
+    for (int i = c0; i < c1; ++i) ceq += order_key(__ldcg(lg + i)) == kth;
+    unsigned eq_tot;
+    const unsigned eq_before = cta_exclusive_scan(ceq, eq_tot, su);
+    float ws = 0.f;
+    int last = -1;
+    {
+        unsigned e = eq_before;
+        for (int i = c0; i < c1; ++i) {
+            const float v = __ldcg(lg + i);
+            const unsigned key = order_key(v);
+            bool in = key > kth;
+            if (key == kth) in = e++ < need_eq;
+            if (in) {
+                ws += expf((v - mx) * inv_t);
+                last = i;
+            }
+        }
+    }
+    float wtot;
+    const float wbefore = cta_exclusive_scan(ws, wtot, sf);
+    const float target = u * wtot;
+    if (threadIdx.x == 0) { misc[2] = 0x7fffffff; misc[3] = -1; }
+    csync();
+    if (last >= 0) atomicMax(&misc[3], last);
+    if (ws > 0.f && wbefore + ws > target) {
+        float run = wbefore;
+        unsigned e = eq_before;
+        for (int i = c0; i < c1; ++i) {
+            const float v = __ldcg(lg + i);
+            const unsigned key = order_key(v);
+            bool in = key > kth;
+            if (key == kth) in = e++ < need_eq;
+            if (in) {
+                run += expf((v - mx) * inv_t);
+                if (run > target) {
+                    atomicMin(&misc[2], i);
+                    break;
+                }
+            }
+        }
+    }
+    csync();
+    const int tok = misc[2] != 0x7fffffff ? misc[2] : misc[3];  // u * total rounded up to the total: the last candidate
+    csync();
+    return tok;
+}
+
+// Sampling of row i's head for stream k (0: text) in this step, or false for greedy.
+__device__ __forceinline__ bool sampling_on(const Params& P, int i, int k, float& inv_t, int& topk)
+{
+    const StepDesc* D = P.desc;
+    if (!D->sampled) return false;
+    const SampleCfg cfg = P.samp[D->slot[i]];
+    inv_t = k == 0 ? cfg.text_inv_t : cfg.audio_inv_t;
+    topk = k == 0 ? cfg.text_k : cfg.audio_k;
+    return topk > 1 && inv_t > 0.f;
+}
+
+// Logits of row i's head for stream k (0: the text head; k >= 1: substep k-1's head).
+__device__ __forceinline__ const float* head_logits(const Params& P, int i, int k, int& N)
+{
+    if (k == 0) {
+        N = P.V;
+        return P.logits + (size_t)i * P.V;
+    }
+    N = P.C;
+    return P.dlogits + ((size_t)i * P.S + (k - 1)) * P.C;
+}
+
 // Input token of depformer substep j for each batch row: the token supplied
 // for stream j (this frame, or the frame before for a delayed stream) if any,
 // else, at a group's first substep only, the argmax of the head before it (the
@@ -660,8 +828,30 @@ __device__ __forceinline__ bool dep_select_inputs(const Params& P, const XSrc& x
         }
         const int lim = j == 0 ? P.V : P.C;
         if (lane == 0) sm.prev[warp] = (chosen >= 0 && chosen < lim) ? chosen : 0;  // keeps the embedding read in range
+        float it_;
+        int ik_;
+        if (lane == 0) sm.misc[8 + warp] = j == xs.dj0 && supplied_token(P, i, j) < 0 && sampling_on(P, i, j, it_, ik_);
     }
-    return csync_and(ok);
+    if (!csync_and(ok)) return false;
+    // rows that draw their token: every CTA draws the same one from the head's logits
+    // (written before the partials were published, which the argmax wait saw)
+    for (int b = 0; b < nb; ++b) {
+        if (!sm.misc[8 + b]) continue;
+        __threadfence();
+        const int i = b0 + b;
+        float inv_t;
+        int topk, N;
+        sampling_on(P, i, j, inv_t, topk);
+        const float* lg = head_logits(P, i, j, N);
+        const int tok = sample_topk_cta(lg, N, inv_t, topk, P.unif[(size_t)i * NSTREAM + j], sm);
+        if (threadIdx.x == 0) {
+            const int lim = j == 0 ? P.V : P.C;
+            sm.prev[b] = (tok >= 0 && tok < lim) ? tok : 0;
+            if (blockIdx.x == 0) P.drawn[(size_t)i * NSTREAM + j] = tok;
+        }
+        csync();
+    }
+    return true;
 }
 
 // Consume one batch group [b0, b0+nb) of a matrix-vector phase: leaves the
@@ -1076,6 +1266,7 @@ struct EpiLogits {
             else if (extra) st_tag1(extra + (size_t)(b0 + b) * extra_stride + (r - nlog), __float_as_uint(y), tag);
         }
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        __threadfence();  // the logits are visible before the partials that announce them
         for (int b = 0; b < nb; ++b) {
             float bv = -INFINITY;
             int bi = 0x7fffffff;
@@ -1566,7 +1757,7 @@ __device__ __forceinline__ bool phase_final(const Params& P, int n, unsigned sta
     const StepDesc* D = P.desc;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = P.S, G = P.G;
-    int* am = sm.X;  // [n][S + 1]: text head, then the head of substep 0 .. S-1
+    int* am = sm.X + 2048;  // [n][S + 1]: text head, then the head of substep 0 .. S-1 (after the sampler's histogram)
     int ok = 1;
     for (int it = warp; it < n * (S + 1) && ok; it += NWARP) {
         const int i = it / (S + 1), t = it % (S + 1) - 1;
@@ -1587,15 +1778,41 @@ __device__ __forceinline__ bool phase_final(const Params& P, int n, unsigned sta
         if (lane == 0) am[it] = a;
     }
     if (!csync_and(ok)) return false;
+    // sampled rows: streams drawn at a group's first substep were recorded then; the
+    // stream of the last substep that ran (and the text when no substep ran) is drawn here
+    const int ngr = n_groups(starts);
+    int klast = 0;
+    if (ngr > 0) {
+        int j0, nj;
+        group_bounds(starts, S, ngr - 1, j0, nj);
+        klast = j0 + nj;
+    }
+    if (D->sampled) {
+        __threadfence();
+        for (int i = 0; i < n; ++i) {
+            float inv_t;
+            int topk, N;
+            if (klast <= S && supplied_token(P, i, klast) < 0 && sampling_on(P, i, klast, inv_t, topk)) {
+                const int tok = sample_topk_cta(head_logits(P, i, klast, N), N, inv_t, topk,
+                                                P.unif[(size_t)i * NSTREAM + klast], sm);
+                if (threadIdx.x == 0) P.drawn[(size_t)i * NSTREAM + klast] = tok;
+            }
+        }
+        csync();
+    }
     for (int it = threadIdx.x; it < n * NSTREAM; it += NT) {
         const int i = it / NSTREAM, k = it % NSTREAM;
         const int p = D->pos[i], slot = D->slot[i];
         const int f = p - P.delays[k];
-        const int a = am[i * (S + 1) + k];  // stream k's head: the text head, or substep k-1's
+        int a = am[i * (S + 1) + k];  // stream k's head: the text head, or substep k-1's
         const int sup = supplied_token(P, i, k);
+        float inv_t;
+        int topk;
+        if (sup < 0 && k <= klast && sampling_on(P, i, k, inv_t, topk)) a = P.drawn[(size_t)i * NSTREAM + k];
         const int c = sup >= 0 ? sup : a;
-        if (k == 0) P.text_argmax[i] = a;
-        else P.code_argmax[i * 16 + (k - 1)] = a;
+        const int raw = am[i * (S + 1) + k];
+        if (k == 0) P.text_argmax[i] = raw;
+        else P.code_argmax[i * 16 + (k - 1)] = raw;
         if (f >= 0) P.hist[((size_t)slot * NSTREAM + k) * HIST + f % HIST] = c;
         if (k == 0) P.text_out[i] = c;
         else P.codes_out[i * 16 + (k - 1)] = f >= 0 ? c : -1;

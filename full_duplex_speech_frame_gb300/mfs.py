@@ -60,6 +60,8 @@ def _load_library():
         "mfs_set_mode": (ci, [vp, ci]),
         "mfs_launches_per_step": (ci, [vp]),
         "mfs_set_skip_settled": (ci, [vp, ci]),
+        "mfs_set_sampling": (ci, [vp, ci, ctypes.c_float, ci, ctypes.c_float, ci]),
+        "mfs_step_sampled": (ci, [vp, ci, i32p, i32p, vp, i32p, i32p]),
         "mfs_set_timing": (ci, [vp, ci]),
         "mfs_kernel_time": (ci, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
         "mfs_phase_times": (ci, [vp, vp, ci]),
@@ -171,6 +173,26 @@ def mfs_step(ctx: Ctx, slots, in_codes):
     text = np.empty(n, np.int32)
     codes = np.empty((n, 16), np.int32)
     rc = _lib.mfs_step(ctx.handle, n, slots.ctypes.data, codes_in.ctypes.data, text.ctypes.data, codes.ctypes.data)
+    _check(ctx, rc)
+    ctx.last_n = n
+    return text, codes
+
+
+def mfs_set_sampling(ctx: Ctx, slot: int, text_temp: float, text_topk: int, audio_temp: float, audio_topk: int) -> None:
+    _check(ctx, _lib.mfs_set_sampling(ctx.handle, int(slot), float(text_temp), int(text_topk), float(audio_temp),
+                                      int(audio_topk)))
+
+
+def mfs_step_sampled(ctx: Ctx, slots, in_codes, uniforms):
+    """mfs_step with uniforms [n, 17] in [0, 1) for the slots' sampling heads."""
+    slots = _i32(slots).reshape(-1)
+    n = slots.size
+    codes_in = _i32(in_codes).reshape(n, 17)
+    unif = np.ascontiguousarray(uniforms, dtype=np.float32).reshape(n, 17)
+    text = np.empty(n, np.int32)
+    codes = np.empty((n, 16), np.int32)
+    rc = _lib.mfs_step_sampled(ctx.handle, n, slots.ctypes.data, codes_in.ctypes.data, unif.ctypes.data,
+                               text.ctypes.data, codes.ctypes.data)
     _check(ctx, rc)
     ctx.last_n = n
     return text, codes

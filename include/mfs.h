@@ -172,6 +172,24 @@ int mfs_read_debug(mfs_ctx* ctx, float* text_logits, float* dep_logits,
  * arithmetic, for diagnosis). */
 int mfs_set_mode(mfs_ctx* ctx, int mode);
 
+/* Sampling heads (mobius PR #368, commit note replacing greedy argmax with
+ * temperature + top-k sampling: text 0.7 / 25, audio 0.8 / 250; SGLang-Omni
+ * cookbook, PersonaPlex, "Stage sampling": every request draws from its own
+ * generator).  mfs_set_sampling sets a slot's temperatures and top-k (k <= 1
+ * or temperature 0: greedy, the default for every slot).  mfs_step_sampled is
+ * mfs_step plus uniforms [n, 17] in [0, 1) from the caller's per-session
+ * generator: row i's token of stream k (0: text) that is not supplied is drawn
+ * with uniforms[i][k] as follows.  The candidates are the k largest logits
+ * (ties: lower index first), weighted exp((logit - max) / temperature); the
+ * token is the first candidate, in ascending index order, at which the running
+ * sum of weights exceeds u times their total.  A drawn token feeds the next
+ * substep like a greedy one.  mfs_read_debug still reports the raw argmaxes.
+ * Uniforms outside [0, 1) give MFS_E_ARG.  mfs_step and mfs_step_device stay
+ * greedy. */
+int mfs_set_sampling(mfs_ctx* ctx, int slot, float text_temp, int text_topk, float audio_temp, int audio_topk);
+int mfs_step_sampled(mfs_ctx* ctx, int n, const int32_t* slots, const int32_t* in_codes, const float* uniforms,
+                     int32_t* text_tok, int32_t* codes);
+
 /* Depformer substeps whose every output is settled without them (mobius PR
  * #368, "P3 - ONNX Runtime example": substep j yields the code of stream j+1;
  * SGLang-Omni cookbook, PersonaPlex, "Known limitations": the depformer steps

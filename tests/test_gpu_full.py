@@ -195,3 +195,31 @@ def test_full_b16_prompts_then_decode(mfs, full_weights):
             ref = orc.step([k], u[p][i:i + 1], want_logits=True)
             _compare_rows(dbg, [i], ref, f"B=16 slot {i} frame {250 + p}")
             alive[k] = bool(text[i] == ref["text"][0] and np.array_equal(codes[i], ref["codes"][0]))
+
+
+def test_full_sampling_heads_draw_from_gpu_logits(mfs, full_weights):
+    """Full shape, B = 2 sampled slots (32000-word text head, top-25; audio top-250): every
+    generated token is the oracle sampler's draw from the GPU's own logits with the same
+    uniform, except at a CDF boundary where fp32 and fp64 may part."""
+    from tests.test_gpu_tiny import _near_cdf_boundary
+    s = synth.FULL.replace(max_slots=2)
+    ctx = H.gpu_context(s, full_weights)
+    mfs.mfs_prefill(ctx, [0, 1], synth.forced_frames(s, 5, synth.STREAM_PROMPT, 12, 2).transpose(1, 0, 2))
+    for slot in (0, 1):
+        mfs.mfs_set_sampling(ctx, slot, 0.7, 25, 0.8, 250)
+    u = synth.user_frames(s, 5, 3, 2)
+    unif = ((synth.uniform_int(5, 98, 3 * 2 * 17, 0, 1 << 24).reshape(3, 2, 17)) + 0.5) / float(1 << 24)
+    checked = 0
+    for p in range(3):
+        text, codes = mfs.mfs_step_sampled(ctx, [0, 1], u[p], unif[p])
+        dbg = mfs.mfs_read_debug(ctx)
+        for i in range(2):
+            for k in range(9):
+                lg = dbg["text_logits"][i] if k == 0 else dbg["dep_logits"][i][k - 1]
+                temp, topk = (0.7, 25) if k == 0 else (0.8, 250)
+                got = text[i] if k == 0 else codes[i][k - 1]
+                want = oracle.sample_topk(lg, temp, topk, unif[p][i][k])
+                if got != want:
+                    assert _near_cdf_boundary(lg, temp, topk, unif[p][i][k]), (p, i, k, got, want)
+                checked += 1
+    assert checked == 54

@@ -316,3 +316,60 @@ def test_tiny_skip_settled_substeps(mfs):
         assert np.array_equal(ran, np.arange(16) < jend), f"frame {p}: substeps run {np.flatnonzero(ran)}, want < {jend}"
         np.testing.assert_array_equal(da["dep_logits"][:, ran], db["dep_logits"][:, ran])
         np.testing.assert_array_equal(da["code_argmax"][:, ran], db["code_argmax"][:, ran])
+
+
+def _near_cdf_boundary(lg, temp, k, u, tol=1e-4):
+    """True when u * total lies within tol * total of a candidate's cumulative weight
+    (index order), where an fp32 and an fp64 evaluation may legitimately disagree."""
+    lg = np.asarray(lg, np.float64)
+    k = min(k, lg.size)
+    cand = sorted(sorted(range(lg.size), key=lambda i: (-lg[i], i))[:k])
+    wts = np.exp((lg[cand] - lg.max()) / temp)
+    cum = np.cumsum(wts)
+    return bool(np.min(np.abs(cum - u * cum[-1])) < tol * cum[-1])
+
+
+def test_tiny_sampling_heads(mfs):
+    """Two sampled slots (text 0.7 / top-25, audio 0.8 / top-250; and top-k past the
+    vocabularies, which keeps every candidate).  Every generated token equals the oracle's
+    sampler applied to the GPU's own logits with the same uniform (an fp32/fp64
+    disagreement is allowed only at a CDF boundary); logits follow the oracle, which
+    samples with the same uniforms, until a legal divergence."""
+    s = tiny(max_slots=2)
+    w = synth.make_weights(s, 11, gain_std=0.1)
+    ctx, orc = H.gpu_context(s, w), oracle.Oracle(s, w)
+    cfg = {0: (0.7, 25, 0.8, 250), 1: (1.0, 5000, 1.3, 2048)}
+    for slot, c in cfg.items():
+        mfs.mfs_set_sampling(ctx, slot, *c)
+        orc.set_sampling(slot, *c)
+    T = 16
+    u = synth.user_frames(s, 11, T, 2)
+    unif = ((synth.uniform_int(11, 99, T * 2 * 17, 0, 1 << 24).reshape(T, 2, 17)) + 0.5) / float(1 << 24)
+    checked = compared = 0
+    for p in range(T):
+        text, codes = mfs.mfs_step_sampled(ctx, [0, 1], u[p], unif[p])
+        dbg = mfs.mfs_read_debug(ctx)
+        ref = orc.step([0, 1], u[p], want_logits=True, uniforms=unif[p])
+        H.check_logits(dbg["text_logits"], ref["text_logits"], f"text logits, frame {p}")
+        H.check_logits(dbg["dep_logits"], ref["dep_logits"], f"depformer logits, frame {p}")
+        for i in range(2):
+            tt, tk, at, ak = cfg[i]
+            for k in range(9):  # text and agent streams 1..8 are generated
+                f = p - s.delays[k]
+                if f < 0:
+                    continue
+                lg = dbg["text_logits"][i] if k == 0 else dbg["dep_logits"][i][k - 1]
+                temp, topk = (tt, tk) if k == 0 else (at, ak)
+                got = text[i] if k == 0 else codes[i][k - 1]
+                want = oracle.sample_topk(lg, temp, topk, unif[p][i][k])
+                if got != want:
+                    assert _near_cdf_boundary(lg, temp, topk, unif[p][i][k]), (p, i, k, got, want)
+                checked += 1
+        compared += 1
+        if not (np.array_equal(text, ref["text"]) and np.array_equal(codes, ref["codes"])):
+            break  # a draw at a CDF boundary went the other way: histories diverge from here
+    assert checked >= 60 and compared >= 4, (checked, compared)
+    with pytest.raises(mfs.MfsError):
+        bad = unif[0].copy()
+        bad[0][3] = 1.0
+        mfs.mfs_step_sampled(ctx, [0, 1], u[0], bad)
