@@ -223,7 +223,7 @@ def run_gpu(args, rank, world):
     torch.cuda.set_stream(side)
     s = WORKLOAD.shape
     n = WORKLOAD.batch
-    need = 2 * args.warmup + 3 * args.steps
+    need = 3 * args.warmup + 4 * args.steps
     if PROMPT + need > s.max_pos:
         raise SystemExit("too many steps for the position range")
     w = synth.make_weights(s, WORKLOAD.weight_seed)
@@ -290,8 +290,24 @@ def run_gpu(args, rank, world):
     mfs.mfs_set_timing(ctx, 0)
     mfs.mfs_set_skip_settled(ctx, False)
 
+    # variant: sampling heads (text 0.7 / top-25, audio 0.8 / top-250), host-buffer calls
+    sb = vb + args.steps
+    mfs.mfs_set_sampling(ctx, 0, 0.7, 25, 0.8, 250)
+    unif = ((synth.uniform_int(WORKLOAD.input_seed, 97, (args.warmup + args.steps) * 17, 0, 1 << 24)
+             .reshape(-1, 1, 17)) + 0.5) / float(1 << 24)
+    for p in range(args.warmup):
+        mfs.mfs_step_sampled(ctx, slots, frames[sb + p], unif[p])
+    sb += args.warmup
+    mfs.mfs_set_timing(ctx, 1)
+    mfs.mfs_kernel_time(ctx)
+    for k in range(args.steps):
+        mfs.mfs_step_sampled(ctx, slots, frames[sb + k], unif[args.warmup + k])
+    skms, sks = mfs.mfs_kernel_time(ctx)
+    mfs.mfs_set_timing(ctx, 0)
+    mfs.mfs_set_sampling(ctx, 0, 0.0, 0, 0.0, 0)
+
     # end to end through the public host-buffer call
-    base2 = vb + args.steps
+    base2 = sb + args.steps
     pinned = torch.from_numpy(frames[base2:base2 + args.steps]).pin_memory().numpy()
     barrier(world)
     torch.cuda.synchronize()
@@ -335,6 +351,11 @@ def run_gpu(args, rank, world):
                         "supplied; outputs identical, weights streamed 1.25 GB less",
                 "value": n * args.steps * world / (ms_v / 1000.0), "unit": UNIT, "ms_per_step": ms_v / args.steps,
                 "kernel_ms": vkms / max(vks, 1),
+            },
+            "sampling_heads": {
+                "what": "mfs_step_sampled with text temperature 0.7 / top-25 and audio 0.8 / top-250 "
+                        "(uniforms supplied per step); device time of the step kernel",
+                "kernel_ms": skms / max(sks, 1), "value": 1000.0 / (skms / max(sks, 1)), "unit": UNIT,
             },
         },
     }

@@ -818,9 +818,11 @@ __device__ __forceinline__ bool dep_select_inputs(const Params& P, const XSrc& x
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j = xs.dj;
     int ok = 1;
+    const bool sampled = P.desc->sampled != 0;
     if (warp < nb) {
         const int i = b0 + warp;
         int chosen = supplied_token(P, i, j);
+        const bool generated = chosen < 0;
         if (chosen < 0 && j == xs.dj0) {
             const uint2* parts = j == 0 ? P.amax + (size_t)i * P.G * 2 : P.damax + ((size_t)i * P.S + (j - 1)) * P.G * 2;
             chosen = argmax_partials_warp(P, parts, xs.am_cnt, xs.am_tag);
@@ -830,12 +832,12 @@ __device__ __forceinline__ bool dep_select_inputs(const Params& P, const XSrc& x
         if (lane == 0) sm.prev[warp] = (chosen >= 0 && chosen < lim) ? chosen : 0;  // keeps the embedding read in range
         float it_;
         int ik_;
-        if (lane == 0) sm.misc[8 + warp] = j == xs.dj0 && supplied_token(P, i, j) < 0 && sampling_on(P, i, j, it_, ik_);
+        if (lane == 0) sm.misc[8 + warp] = sampled && generated && j == xs.dj0 && sampling_on(P, i, j, it_, ik_);
     }
     if (!csync_and(ok)) return false;
     // rows that draw their token: every CTA draws the same one from the head's logits
     // (written before the partials were published, which the argmax wait saw)
-    for (int b = 0; b < nb; ++b) {
+    for (int b = 0; b < nb && sampled; ++b) {
         if (!sm.misc[8 + b]) continue;
         __threadfence();
         const int i = b0 + b;
@@ -1266,7 +1268,7 @@ struct EpiLogits {
             else if (extra) st_tag1(extra + (size_t)(b0 + b) * extra_stride + (r - nlog), __float_as_uint(y), tag);
         }
         const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-        __threadfence();  // the logits are visible before the partials that announce them
+        if (P.desc->sampled) __threadfence();  // a sampled step reads the logits once the partials announce them
         for (int b = 0; b < nb; ++b) {
             float bv = -INFINITY;
             int bi = 0x7fffffff;
