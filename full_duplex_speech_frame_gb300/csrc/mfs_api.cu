@@ -648,7 +648,7 @@ static int collect_device_error(mfs_ctx* c)
                       sites[e[2] >= 1 && e[2] <= 6 ? e[2] : 0], want >> 10, want & 1023u, seen >> 10, seen & 1023u,
                       e[5], e[6]);
         }
-        CK(cudaMemset(c->d_err, 0, sizeof e));
+        CK(cudaMemset(c->d_err, 0, 7 * sizeof(int)));  // err[7] (the wait limit) stays
     }
     c->pending.clear();
     return rc;
@@ -925,6 +925,48 @@ extern "C" int mfs_set_mode(mfs_ctx* c, int mode)
     if (mode != 0 && mode != 1) return fail(c, MFS_E_ARG, "mode must be 0 or 1");
     c->mode = mode;
     return MFS_OK;
+}
+
+extern "C" int mfs_set_wait_limit(mfs_ctx* c, int ms)
+{
+    if (!c) return MFS_E_ARG;
+    if (ms < 1 || ms > 60000) return fail(c, MFS_E_ARG, "wait limit %d ms outside [1, 60000]", ms);
+    if (!c->pending.empty()) {
+        int rc = mfs_sync(c);
+        if (rc != MFS_OK) return rc;
+    }
+    const int us = ms * 1000;
+    CK(cudaMemcpy(c->d_err + 7, &us, sizeof us, cudaMemcpyHostToDevice));
+    return MFS_OK;
+}
+
+extern "C" int mfs_debug_stall(mfs_ctx* c, int slot)
+{
+    if (!c) return MFS_E_ARG;
+    int rc = weights_ready(c);
+    if (rc) return rc;
+    if (!c->pending.empty() && (rc = mfs_sync(c)) != MFS_OK) return rc;
+    if (slot < 0 || slot >= c->cfg.max_slots) return fail(c, MFS_E_SLOT, "slot %d outside [0, %d)", slot, c->cfg.max_slots);
+    if (c->pos[slot] >= c->cfg.max_pos) return fail(c, MFS_E_RANGE, "slot %d is at max_pos", slot);
+    int di;
+    StepDesc* h = next_desc(c, &di);
+    fill_desc(c, h, 1, &slot, nullptr, 0);
+    for (int k = 0; k < NSTREAM; ++k) h->codes[0][k] = -1;
+    CK(cudaMemcpyAsync(c->d_desc, h, sizeof(StepDesc), cudaMemcpyHostToDevice, c->stream));
+    CK(cudaEventRecord(c->desc_ev[di], c->stream));
+    // the first QKV phase alone: its input (this step's embedding sum) is never produced
+    Params P = c->P;
+    P.desc = c->d_desc;
+    P.ptime = nullptr;
+    int ph0 = 1, ph1 = 2, maxrows = c->maxrows;
+    void* args[] = {&P, &ph0, &ph1, &maxrows};
+    CK(cudaLaunchKernel(c->kfn[0], dim3(c->G), dim3(NT + 32), args, c->smem[0], c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+    int e0 = 0;
+    CK(cudaMemcpy(&e0, c->d_err, sizeof e0, cudaMemcpyDeviceToHost));
+    if (e0 == 0) return fail(c, MFS_E_STATE, "the stalled phase did not give up");
+    c->last_full = false;
+    return collect_device_error(c);
 }
 
 extern "C" int mfs_set_skip_settled(mfs_ctx* c, int on)

@@ -137,23 +137,29 @@ __device__ __forceinline__ unsigned long long globaltimer_ns()
     return t;
 }
 
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // every wait gives up after 2 s
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;  // every wait gives up after 2 s (default)
 
 // Spin bookkeeping: every 64 spins look at the clock and the error flag.
 // false: give up.  The first waiter to give up records where (err[2..6]:
-// wait site, expected and observed tag or parity, CTA, thread).
+// wait site, expected and observed tag or parity, CTA, thread).  err[7], when
+// positive, replaces the 2 s limit (microseconds).
 enum WaitSite : int { WS_TAG1 = 1, WS_TAG8 = 2, WS_FULL = 3, WS_EMPTY = 4, WS_DQ = 5, WS_DKV = 6 };
 
 struct Spin {
     unsigned n = 0;
-    unsigned long long t0 = 0;
+    unsigned long long t0 = 0, lim = WAIT_LIMIT_NS;
     __device__ __forceinline__ bool ok(int* err, int site, unsigned want, unsigned seen)
     {
         if ((++n & 63u) != 0u) return true;
         if (*(volatile int*)err != 0) return false;
         const unsigned long long t = globaltimer_ns();
-        if (t0 == 0) { t0 = t; return true; }
-        if (t - t0 > WAIT_LIMIT_NS) {
+        if (t0 == 0) {
+            t0 = t;
+            const int us = *(volatile int*)(err + 7);
+            if (us > 0) lim = (unsigned long long)us * 1000ull;
+            return true;
+        }
+        if (t - t0 > lim) {
             if (atomicCAS(err, 0, (int)DERR_WAIT) == 0) {
                 err[2] = site;
                 err[3] = (int)want;
@@ -986,7 +992,10 @@ __device__ __forceinline__ bool gemv_group(const Params& P, const Phase& ph, int
         const int nr = min(rps, r1 - ra);
         const int slot = (int)(stage % NS);
         const unsigned long long tw0 = P.ptime ? globaltimer_ns() : 0ull;
-        if (!mbar_wait(&sm.full[slot], (stage / NS) & 1u, P.err, WS_FULL)) return false;
+        if (!mbar_wait(&sm.full[slot], (stage / NS) & 1u, P.err, WS_FULL)) {
+            ok = 0;  // every thread leaves through the barrier below, whichever stage it reached
+            break;
+        }
         if (P.ptime && blockIdx.x == 0 && threadIdx.x == 0) {
             // diagnostics: time CTA 0 spent waiting for weight stages, and their count
             // (fire-and-forget reductions: the warp does not wait on them)

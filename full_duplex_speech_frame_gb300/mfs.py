@@ -60,6 +60,8 @@ def _load_library():
         "mfs_set_mode": (ci, [vp, ci]),
         "mfs_launches_per_step": (ci, [vp]),
         "mfs_set_skip_settled": (ci, [vp, ci]),
+        "mfs_set_wait_limit": (ci, [vp, ci]),
+        "mfs_debug_stall": (ci, [vp, ci]),
         "mfs_set_sampling": (ci, [vp, ci, ctypes.c_float, ci, ctypes.c_float, ci]),
         "mfs_step_sampled": (ci, [vp, ci, i32p, i32p, vp, i32p, i32p]),
         "mfs_set_timing": (ci, [vp, ci]),
@@ -265,6 +267,15 @@ def mfs_set_mode(ctx: Ctx, mode: int) -> None:
 def mfs_set_skip_settled(ctx: Ctx, on: bool) -> None:
     """Skip trailing depformer substeps whose outputs are all supplied (include/mfs.h)."""
     _check(ctx, _lib.mfs_set_skip_settled(ctx.handle, int(bool(on))))
+
+
+def mfs_set_wait_limit(ctx: Ctx, ms: int) -> None:
+    _check(ctx, _lib.mfs_set_wait_limit(ctx.handle, int(ms)))
+
+
+def mfs_debug_stall(ctx: Ctx, slot: int) -> None:
+    """Raises MfsError(MFS_E_DEVICE) when the device's bounded waits work (include/mfs.h)."""
+    _check(ctx, _lib.mfs_debug_stall(ctx.handle, int(slot)))
 
 
 def mfs_launches_per_step(ctx: Ctx) -> int:

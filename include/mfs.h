@@ -202,6 +202,18 @@ int mfs_step_sampled(mfs_ctx* ctx, int n, const int32_t* slots, const int32_t* i
  * mfs_read_debug.  Default 0: all 16 substeps run. */
 int mfs_set_skip_settled(mfs_ctx* ctx, int on);
 
+/* Failure detection.  Every wait inside the step kernel (on another CTA's
+ * tagged output, on a weight stage) gives up after a limit, records where,
+ * and the call returns MFS_E_DEVICE with that place in mfs_last_error; the
+ * context stays usable, the state of the step's slots is undefined (reset or
+ * import them).  mfs_set_wait_limit sets the limit (1 .. 60000 ms; default
+ * 2000).  mfs_debug_stall checks the mechanism: it launches the slot's first
+ * attention-projection phase alone, whose input is never produced, so its
+ * waits run out; it returns MFS_E_DEVICE (or MFS_E_STATE if nothing gave up)
+ * and leaves the slot's state undefined. */
+int mfs_set_wait_limit(mfs_ctx* ctx, int ms);
+int mfs_debug_stall(mfs_ctx* ctx, int slot);
+
 /* Kernel launches made by the last step (for accounting). */
 int mfs_launches_per_step(const mfs_ctx* ctx);
 

@@ -373,3 +373,27 @@ def test_tiny_sampling_heads(mfs):
         bad = unif[0].copy()
         bad[0][3] = 1.0
         mfs.mfs_step_sampled(ctx, [0, 1], u[0], bad)
+
+
+def test_tiny_device_wait_gives_up_and_context_recovers(mfs):
+    """A phase launched without its input waits, gives up after the (shortened) limit and
+    reports MFS_E_DEVICE with the wait site; the context then runs normal steps that match
+    the oracle (the stalled slot is reset first)."""
+    s = tiny(max_slots=2)
+    w = synth.make_weights(s, 12, gain_std=0.1)
+    ctx, orc = H.gpu_context(s, w), oracle.Oracle(s, w)
+    mfs.mfs_set_wait_limit(ctx, 50)
+    u = synth.user_frames(s, 12, 6, 2)
+    mfs.mfs_step(ctx, [0, 1], u[0])
+    orc.step([0, 1], u[0])
+    with pytest.raises(mfs.MfsError) as e:
+        mfs.mfs_debug_stall(ctx, 0)
+    assert e.value.status == "MFS_E_DEVICE" and "gave up" in str(e.value)
+    mfs.mfs_reset_slot(ctx, 0)
+    orc.reset_slot(0)
+    for p in range(1, 6):
+        text, codes = mfs.mfs_step(ctx, [0, 1], u[p])
+        dbg = mfs.mfs_read_debug(ctx)
+        ref = orc.step([0, 1], u[p], want_logits=True)
+        H.check_logits(dbg["text_logits"], ref["text_logits"], f"text logits, frame {p}")
+        H.check_logits(dbg["dep_logits"], ref["dep_logits"], f"depformer logits, frame {p}")
