@@ -13,7 +13,8 @@
  *     mobius PR #368, "P2 - Moshi LM"; 3000-frame ring window: vLLM-Omni
  *     PersonaPlex recipe, "Architecture" and "Notes") and a greedy text argmax;
  *   - the 16-substep autoregressive depformer with per-substep weights and a
- *     greedy code argmax per substep (mobius PR #368, "P2 - Moshi LM").
+ *     greedy code argmax per substep (mobius PR #368, "P2 - Moshi LM");
+ *     optionally temperature + top-k sampling instead of the argmaxes.
  *
  * Conventions for every entry point:
  *   - Return value: MFS_OK (0) or a negative MFS_E_* status.  An argument
@@ -167,9 +168,10 @@ int mfs_import_slot(mfs_ctx* ctx, int slot, const void* buf, size_t bytes);
 int mfs_read_debug(mfs_ctx* ctx, float* text_logits, float* dep_logits,
                    int32_t* text_argmax, int32_t* code_argmax);
 
-/* Execution mode: 0 (default) = one persistent cooperative launch per step
- * with grid-wide barriers between phases; 1 = one launch per phase (same
- * arithmetic, for diagnosis). */
+/* Execution mode: 0 (default) = one persistent cooperative launch per step,
+ * in which a phase waits for the tagged outputs of the phases it reads (no
+ * grid-wide barrier); 1 = one launch per phase (same arithmetic, bit for bit,
+ * for diagnosis). */
 int mfs_set_mode(mfs_ctx* ctx, int mode);
 
 /* Sampling heads (mobius PR #368, commit note replacing greedy argmax with
