@@ -397,3 +397,28 @@ def test_tiny_device_wait_gives_up_and_context_recovers(mfs):
         ref = orc.step([0, 1], u[p], want_logits=True)
         H.check_logits(dbg["text_logits"], ref["text_logits"], f"text logits, frame {p}")
         H.check_logits(dbg["dep_logits"], ref["dep_logits"], f"depformer logits, frame {p}")
+
+
+def test_tiny_session_priming(mfs):
+    """Priming (voice prompt, silence, persona text, silence) through the prompt path on the
+    GPU, then decode: logits follow the oracle primed with the same frames."""
+    from full_duplex_speech_frame_gb300.priming import priming_frames, prime_slot
+    s = tiny(max_slots=2)
+    w = synth.make_weights(s, 13, gain_std=0.1)
+    ctx, orc = H.gpu_context(s, w), oracle.Oracle(s, w)
+    voice = synth.uniform_int(13, 401, 6 * 8, 0, s.card).reshape(6, 8)
+    persona = synth.uniform_int(13, 402, 5, 0, s.text_vocab)
+    f = priming_frames(voice, persona, text_pad=3, agent_silence=[7] * 8, user_fill=[11] * 8,
+                       silence_after_voice=2, silence_after_persona=2)
+    prime_slot(ctx, 1, f)
+    orc.prefill(1, f)
+    assert mfs.mfs_position(ctx, 1) == orc.position(1) == f.shape[0]
+    u = synth.user_frames(s, 13, 4, 1)
+    for p in range(4):
+        text, codes = mfs.mfs_step(ctx, [1], u[p])
+        dbg = mfs.mfs_read_debug(ctx)
+        ref = orc.step([1], u[p], want_logits=True)
+        H.check_logits(dbg["text_logits"], ref["text_logits"], f"text logits, frame {p}")
+        H.check_logits(dbg["dep_logits"], ref["dep_logits"], f"depformer logits, frame {p}")
+        if not (np.array_equal(text, ref["text"]) and np.array_equal(codes, ref["codes"])):
+            break
