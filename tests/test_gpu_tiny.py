@@ -422,3 +422,47 @@ def test_tiny_session_priming(mfs):
         H.check_logits(dbg["dep_logits"], ref["dep_logits"], f"depformer logits, frame {p}")
         if not (np.array_equal(text, ref["text"]) and np.array_equal(codes, ref["codes"])):
             break
+
+
+def test_tiny_sampling_with_skipped_substeps(mfs):
+    """Sampling and skipped settled substeps together: every output equals a sampled run
+    without skipping (same uniforms), bit for bit."""
+    s = tiny(max_slots=2)
+    w = synth.make_weights(s, 14, gain_std=0.1)
+    a, b = H.gpu_context(s, w), H.gpu_context(s, w)
+    for ctx in (a, b):
+        for slot in (0, 1):
+            mfs.mfs_set_sampling(ctx, slot, 0.7, 25, 0.8, 250)
+    mfs.mfs_set_skip_settled(b, True)
+    u = synth.user_frames(s, 14, 8, 2)
+    unif = ((synth.uniform_int(14, 97, 8 * 2 * 17, 0, 1 << 24).reshape(8, 2, 17)) + 0.5) / float(1 << 24)
+    for p in range(8):
+        ta, ca = mfs.mfs_step_sampled(a, [0, 1], u[p], unif[p])
+        tb, cb = mfs.mfs_step_sampled(b, [0, 1], u[p], unif[p])
+        np.testing.assert_array_equal(ta, tb)
+        np.testing.assert_array_equal(ca, cb)
+
+
+def test_tiny_slot_state_import_rejects_bad_headers(mfs):
+    """Import checks the header against the context before touching the slot."""
+    s = tiny(max_slots=2, weight_dtype="bf16", kv_dtype="bf16", window=8)
+    w = synth.make_weights(s, 15, gain_std=0.1)
+    ctx = H.gpu_context(s, w)
+    good = synth.slot_state(s, 15, 0, 5)
+    mfs.mfs_import_slot(ctx, 1, good)
+    assert mfs.mfs_position(ctx, 1) == 5
+    cases = {"window": (8, 12), "dtype": (12, 16), "position": (4, 8)}
+    for what, (lo, hi) in cases.items():
+        bad = good.copy()
+        bad[lo:hi] = np.frombuffer(np.int32(99999).tobytes(), np.uint8)
+        with pytest.raises(mfs.MfsError) as e:
+            mfs.mfs_import_slot(ctx, 0, bad)
+        assert e.value.status == "MFS_E_ARG", what
+    bad = good.copy()
+    bad[16:20] = np.frombuffer(np.int32(s.text_vocab).tobytes(), np.uint8)  # history token out of range
+    with pytest.raises(mfs.MfsError):
+        mfs.mfs_import_slot(ctx, 0, bad)
+    with pytest.raises(mfs.MfsError):
+        mfs.mfs_import_slot(ctx, 0, good[:-16])
+    assert mfs.mfs_position(ctx, 0) == 0  # untouched
+    np.testing.assert_array_equal(mfs.mfs_export_slot(ctx, 1), good)
