@@ -65,6 +65,7 @@ def _load():
         lib.orc_position.argtypes = [vp, ci]
         lib.orc_step.argtypes = [vp, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.orc_set_sampling.argtypes = [vp, ci, ctypes.c_double, ci, ctypes.c_double, ci]
+        lib.orc_rvq_encode.argtypes = [vp, vp, ci, ci, vp, ci, vp, vp]
         lib.orc_sample_topk.restype = ci
         lib.orc_sample_topk.argtypes = [vp, ci, ctypes.c_double, ci, ctypes.c_double]
         lib.orc_prefill.argtypes = [vp, ci, ci, vp]
@@ -202,3 +203,17 @@ def sample_topk(logits, temp: float, k: int, u: float) -> int:
     """The oracle's temperature + top-k draw for one logit vector (fp64)."""
     lg = np.ascontiguousarray(logits, np.float64).reshape(-1)
     return int(_load().orc_sample_topk(lg.ctypes.data, lg.size, float(temp), int(k), float(u)))
+
+
+def rvq_encode(z_sem, z_ac, codebooks):
+    """The oracle's split RVQ encode: z_sem, z_ac [T, D], codebooks [8, Cb, D] (fp32 inputs).
+    Returns (codes [T, 8] int32, gap [T, 8] second-best minus best distance)."""
+    z_sem = np.ascontiguousarray(z_sem, np.float32)
+    z_ac = np.ascontiguousarray(z_ac, np.float32)
+    cb = np.ascontiguousarray(codebooks, np.float32)
+    T, D = z_sem.shape
+    codes = np.empty((T, 8), np.int32)
+    gap = np.empty((T, 8), np.float64)
+    _load().orc_rvq_encode(z_sem.ctypes.data, z_ac.ctypes.data, T, D, cb.ctypes.data, cb.shape[1],
+                           codes.ctypes.data, gap.ctypes.data)
+    return codes, gap

@@ -775,3 +775,46 @@ int orc_prefill(orc* o, int slot, int T, const int* codes)
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ Mimi split RVQ encode */
+
+/* The encoder-side argmin quantizer of Mimi's split residual VQ (mobius PR
+ * #368, "P1 - Mimi": SplitResidualVectorQuantizer, encoder-side argmin
+ * quantizer, 8 RVQ codes per 80 ms frame; kyutai-labs/moshi, "Mimi": the
+ * first codebook is semantic, the rest acoustic).  Frame t's semantic latent
+ * z_sem[t] takes the nearest codeword (squared Euclidean distance, ties to the
+ * lower index) of codebook 0; its acoustic latent z_ac[t] is quantized by
+ * codebooks 1..7 in turn, each on the residual the stage before left
+ * (r <- r - chosen codeword).  Codebooks cb [8][Cb][D] fp32; codes [T][8].
+ * gap (optional) [T][8]: second-best minus best distance of each stage, for
+ * comparisons with an implementation in another precision. */
+void orc_rvq_encode(const float* z_sem, const float* z_ac, int T, int D, const float* cb, int Cb, int* codes,
+                    double* gap)
+{
+    double* r = (double*)malloc(sizeof(double) * (size_t)D);
+    for (int t = 0; t < T; ++t) {
+        for (int q = 0; q < 8; ++q) {
+            if (q == 0)
+                for (int e = 0; e < D; ++e) r[e] = z_sem[(size_t)t * D + e];
+            else if (q == 1)
+                for (int e = 0; e < D; ++e) r[e] = z_ac[(size_t)t * D + e];
+            const float* book = cb + (size_t)q * Cb * D;
+            int best = 0;
+            double bd = INFINITY, second = INFINITY;
+            for (int c = 0; c < Cb; ++c) {
+                double dist = 0.0;
+                for (int e = 0; e < D; ++e) {
+                    const double diff = r[e] - (double)book[(size_t)c * D + e];
+                    dist += diff * diff;
+                }
+                if (dist < bd) { second = bd; bd = dist; best = c; }
+                else if (dist < second) second = dist;
+            }
+            codes[(size_t)t * 8 + q] = best;
+            if (gap) gap[(size_t)t * 8 + q] = second - bd;
+            if (q >= 1)
+                for (int e = 0; e < D; ++e) r[e] -= (double)book[(size_t)best * D + e];
+        }
+    }
+    free(r);
+}

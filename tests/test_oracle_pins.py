@@ -423,3 +423,39 @@ def test_sampled_step_draws_from_its_own_logits(tiny_w8):
         rg = g.step([0], u[p], want_logits=True)
         for key in ("text", "codes", "text_logits", "dep_logits"):
             np.testing.assert_array_equal(rb[key], rg[key])
+
+
+# ---------------------------------------------------------------- Mimi split RVQ encode
+
+def test_rvq_matches_library_nearest_neighbours():
+    """Each stage is the library's nearest neighbour (scipy cdist + argmin) on the residual
+    left by the stage before; the semantic codebook sees its own latent."""
+    cdist = pytest.importorskip("scipy.spatial.distance").cdist
+    rng = np.random.default_rng(5)
+    T, D, Cb = 12, 16, 64
+    zs, za = rng.standard_normal((T, D)).astype(np.float32), rng.standard_normal((T, D)).astype(np.float32)
+    cb = rng.standard_normal((8, Cb, D)).astype(np.float32)
+    codes, gap = oracle.rvq_encode(zs, za, cb)
+    assert (gap >= 0).all()
+    np.testing.assert_array_equal(codes[:, 0], np.argmin(cdist(zs.astype(np.float64), cb[0].astype(np.float64), "sqeuclidean"), axis=1))
+    r = za.astype(np.float64)
+    for q in range(1, 8):
+        want = np.argmin(cdist(r, cb[q].astype(np.float64), "sqeuclidean"), axis=1)
+        np.testing.assert_array_equal(codes[:, q], want)
+        r = r - cb[q][want].astype(np.float64)
+
+
+def test_rvq_exact_codewords_and_ties():
+    """A latent equal to a codeword picks it; a zero residual then picks the codeword of
+    least norm, the lower index on a tie."""
+    D, Cb = 8, 16
+    cb = np.zeros((8, Cb, D), np.float32)
+    rng = np.random.default_rng(6)
+    cb[:, 1:] = rng.standard_normal((8, Cb - 1, D)).astype(np.float32)
+    cb[:, 0] = 0.0
+    cb[:, 5] = 0.0  # same (zero) codeword at 0 and 5: the tie goes to 0
+    zs = cb[0, 9][None].copy()
+    za = cb[1, 7][None].copy()
+    codes, _ = oracle.rvq_encode(zs, za, cb)
+    assert codes[0, 0] == 9 and codes[0, 1] == 7
+    assert (codes[0, 2:] == 0).all()
