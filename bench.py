@@ -318,6 +318,21 @@ def run_gpu(args, rank, world):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     barrier(world)
 
+    # the Mimi split RVQ encoder on 152 x 16 frames (D 256, 2048 codewords per codebook)
+    Tq, Dq, Cq = 2432, 256, 2048
+    zq = torch.from_numpy(synth.normal_f32(WORKLOAD.input_seed, 501, 2 * Tq * Dq).reshape(2, Tq, Dq)).cuda()
+    cbq = torch.from_numpy(synth.normal_f32(WORKLOAD.input_seed, 503, 8 * Cq * Dq).reshape(8, Cq, Dq)).cuda()
+    cq = torch.empty(Tq, 8, dtype=torch.int32, device="cuda")
+    for _ in range(args.warmup):
+        mfs.mfs_rvq_encode(zq[0], zq[1], cbq, cq)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        mfs.mfs_rvq_encode(zq[0], zq[1], cbq, cq)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    rvq_ms = e0.elapsed_time(e1) / args.steps
+
     if rank != 0:
         return
     hbm, peak_kind = read_peaks()
@@ -351,6 +366,15 @@ def run_gpu(args, rank, world):
                         "supplied; outputs identical, weights streamed 1.25 GB less",
                 "value": n * args.steps * world / (ms_v / 1000.0), "unit": UNIT, "ms_per_step": ms_v / args.steps,
                 "kernel_ms": vkms / max(vks, 1),
+            },
+            "rvq_encode": {
+                "what": "mfs_rvq_encode, Mimi split RVQ argmin quantizer: 2432 frames, D 256, 8 codebooks of 2048",
+                "kernel_ms": rvq_ms, "value": Tq / (rvq_ms / 1000.0), "unit": "frames/s",
+                "roofline": {"bound": "alu", "unit": "distance terms/s",
+                             "achieved": Tq * 8 * Cq * Dq / (rvq_ms / 1000.0),
+                             "peak": 152 * 128 * 2.07e9 / 2,
+                             "frac": Tq * 8 * Cq * Dq / (rvq_ms / 1000.0) / (152 * 128 * 2.07e9 / 2),
+                             "peak_kind": "152 SMs x 128 fp32 lanes x 2.07 GHz, 2 instructions (subtract, fma) per term"},
             },
             "sampling_heads": {
                 "what": "mfs_step_sampled with text temperature 0.7 / top-25 and audio 0.8 / top-250 "

@@ -68,6 +68,7 @@ def _load_library():
         "mfs_kernel_time": (ci, [vp, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]),
         "mfs_phase_times": (ci, [vp, vp, ci]),
         "mfs_argmax_rows_noalloc": (ci, [vp, ci, ci, ctypes.c_longlong, vp, vp]),
+        "mfs_rvq_encode": (ci, [vp, vp, ci, ci, vp, ci, vp, vp]),
         "mfs_slot_state_bytes": (ctypes.c_size_t, [vp]),
         "mfs_export_slot": (ci, [vp, ci, vp, ctypes.c_size_t]),
         "mfs_import_slot": (ci, [vp, ci, vp, ctypes.c_size_t]),
@@ -313,4 +314,18 @@ def mfs_argmax_rows_noalloc(logits, out, stream=None) -> None:
     rows, cols = logits.shape
     st = _current_stream() if stream is None else ctypes.c_void_p(stream)
     rc = _lib.mfs_argmax_rows_noalloc(logits.data_ptr(), rows, cols, logits.stride(0), out.data_ptr(), st)
+    _check(None, rc)
+
+
+def mfs_rvq_encode(z_sem, z_ac, codebooks, codes, stream=None) -> None:
+    """Mimi split RVQ encode on CUDA tensors: z_sem, z_ac [T, D] fp32, codebooks [8, Cb, D]
+    fp32 -> codes [T, 8] int32 (see include/mfs.h); enqueued on `stream`."""
+    import torch
+    for t in (z_sem, z_ac, codebooks):
+        assert t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()
+    assert codes.is_cuda and codes.dtype == torch.int32 and codes.is_contiguous()
+    T, D = z_sem.shape
+    st = _current_stream() if stream is None else ctypes.c_void_p(stream)
+    rc = _lib.mfs_rvq_encode(z_sem.data_ptr(), z_ac.data_ptr(), T, D, codebooks.data_ptr(), codebooks.shape[1],
+                             codes.data_ptr(), st)
     _check(None, rc)

@@ -234,6 +234,25 @@ int mfs_set_timing(mfs_ctx* ctx, int flags);
 int mfs_kernel_time(mfs_ctx* ctx, double* total_ms, int* steps);
 int mfs_phase_times(mfs_ctx* ctx, uint64_t* ns, int cap);
 
+/* ---------------------------------------------------------------- Mimi RVQ
+ * Encoder-side argmin quantizer of Mimi's split residual vector quantizer
+ * (mobius PR #368, "P1 - Mimi": SplitResidualVectorQuantizer and the
+ * encoder-side argmin quantizer, 8 codes per 80 ms frame; kyutai-labs/moshi,
+ * "Mimi": the first codebook is semantic).  For each of T frames: codebook 0
+ * takes the nearest codeword to z_sem[t]; codebooks 1..7 quantize z_ac[t] and
+ * then, in turn, the residual the stage before leaves (r -= chosen codeword).
+ * Nearest = least squared Euclidean distance (fp32), ties to the lower index.
+ *   z_sem, z_ac  device, [T][D] fp32, 16-byte aligned (the quantizer's input
+ *                latents; the codec's trained projections are not part of it)
+ *   codebooks    device, [8][Cb][D] fp32, 16-byte aligned
+ *   codes        device, [T][8] int32 out
+ *   D            multiple of 4 in [4, MFS_RVQ_MAX_DIM]; stream as elsewhere
+ * Enqueues and returns; MFS_E_ARG on bad sizes, alignment or NULL pointers
+ * (mfs_last_error(NULL) gives the reason). */
+#define MFS_RVQ_MAX_DIM 1024
+int mfs_rvq_encode(const float* z_sem, const float* z_ac, int T, int D, const float* codebooks, int Cb,
+                   int32_t* codes, void* cuda_stream);
+
 /* ---------------------------------------------------------------- no-alloc
  * Greedy argmax over rows of fp32 logits that allocates no device memory.
  * The pages describe no such call: it exists for callers that cannot call
