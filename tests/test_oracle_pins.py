@@ -459,3 +459,16 @@ def test_rvq_exact_codewords_and_ties():
     codes, _ = oracle.rvq_encode(zs, za, cb)
     assert codes[0, 0] == 9 and codes[0, 1] == 7
     assert (codes[0, 2:] == 0).all()
+
+
+def test_synthetic_slot_state_round_trips_through_the_oracle():
+    """The synthetic state generator writes the documented slot-state layout: the oracle
+    reads it and writes back the same bytes (position, history, every ring row)."""
+    s = small_shape(weight_dtype="bf16", kv_dtype="bf16", window=6)
+    w = synth.make_weights(s, 9)
+    o = oracle.Oracle(s, w)
+    for pos in (0, 4, 23):
+        st = synth.slot_state(s, 9, pos, pos)
+        o.import_slot(1, st)
+        assert o.position(1) == pos
+        np.testing.assert_array_equal(o.export_slot(1), st)
