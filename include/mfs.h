@@ -103,7 +103,10 @@ const char* mfs_last_error(const mfs_ctx* ctx);
  * Blocking.  Returns MFS_E_STATE for an unknown name or a size mismatch. */
 int mfs_load_weights(mfs_ctx* ctx, const char* name, const void* src, size_t bytes, int on_device);
 
-/* One frame step for n slots (1 <= n <= max_slots).
+/* One frame step for n slots (1 <= n <= max_slots): the lockstep step with
+ * per-codebook delays and delayed output collection (mobius PR #368, "P3 -
+ * ONNX Runtime example"), all listed sessions advancing together in one 80 ms
+ * tick (vLLM-Omni PersonaPlex recipe, "Notes": batched ticks).
  *   slots    [n]      distinct slot ids (host)
  *   in_codes [n, 17]  frame p's tokens for each slot (host): -1 = generate,
  *                     else the token is forced (text < text_vocab, audio < card)
@@ -129,13 +132,16 @@ int mfs_step_device(mfs_ctx* ctx, int n, const int32_t* slots, const int32_t* d_
 int mfs_sync(mfs_ctx* ctx);
 
 /* Teacher-forced prompt of T frames for n slots: codes [n, T, 17] (host), every
- * token >= 0.  Runs the temporal stack only (the text head and depformer
+ * token >= 0 (persona and voice go in through the same lockstep step with their
+ * rows supplied: vLLM-Omni PersonaPlex recipe, "Architecture").  Runs the temporal stack only (the text head and depformer
  * cannot change a slot whose every stream is supplied) and advances each slot
  * by T frames.  Blocking. */
 int mfs_prefill(mfs_ctx* ctx, int n, const int32_t* slots, int T, const int32_t* codes);
 
-/* Return a slot to the fresh state: position 0, empty history.  Its ring is
- * not cleared: positions are only ever read after being rewritten. */
+/* Return a slot to the fresh state: position 0, empty history, so that a new
+ * session can take it (vLLM-Omni PersonaPlex recipe, "Notes": a recycled slot
+ * matches a fresh engine for the same inputs).  Its ring is not cleared:
+ * positions are only ever read after being rewritten. */
 int mfs_reset_slot(mfs_ctx* ctx, int slot);
 
 /* Frame count of a slot (its next position), or a negative status. */
@@ -204,7 +210,9 @@ int mfs_step_sampled(mfs_ctx* ctx, int n, const int32_t* slots, const int32_t* i
  * mfs_read_debug.  Default 0: all 16 substeps run. */
 int mfs_set_skip_settled(mfs_ctx* ctx, int on);
 
-/* Failure detection.  Every wait inside the step kernel (on another CTA's
+/* Failure detection (the pages detect failures on the host only, e.g. sessions
+ * beyond the batch size are refused: vLLM-Omni PersonaPlex recipe, "Notes";
+ * the device-side limit below has no counterpart there).  Every wait inside the step kernel (on another CTA's
  * tagged output, on a weight stage) gives up after a limit, records where,
  * and the call returns MFS_E_DEVICE with that place in mfs_last_error; the
  * context stays usable, the state of the step's slots is undefined (reset or
