@@ -3,7 +3,7 @@
 // One persistent cooperative kernel runs every phase of a step (embedding sum,
 // 32 temporal layers, text head, 16 depformer substeps, write-back); the same
 // kernel can also be launched once per phase for diagnosis.  One CTA per SM:
-// 16 consumer warps and one producer warp.
+// 8 consumer warps and one producer warp.
 //
 // Weights move by TMA bulk copies (cp.async.bulk) into a ring of shared-memory
 // stages guarded by mbarriers.  The producer walks the same phase schedule as
@@ -19,7 +19,7 @@
 // Buffers are reused only after every reader of the previous value has
 // produced an output that the next writer itself waits for.
 //
-// A CTA owns a contiguous block of row pairs of every matrix; its 16 consumer
+// A CTA owns a contiguous block of row pairs of every matrix; its 8 consumer
 // warps split K into contiguous slices and keep their slice of the
 // (normalised) activations in registers for the whole phase.  Partial dot
 // products are reduced with a fixed shuffle tree, then across K-slices in
@@ -400,7 +400,7 @@ struct Smem {
     float* red;       // [maxrows][BG][NWARP] per-K-slice partial sums of the CTA's rows
     float* yf;        // [maxrows][BG] final row values of the CTA
     int* X;           // embedding rows of this step (aliases red)
-    float* wbuf;      // attention partials of the 16 warps (aliases red)
+    float* wbuf;      // attention partials of the consumer warps (aliases red)
 };
 
 __device__ __forceinline__ Smem smem_map(char* base, int maxrows, int BG)

@@ -124,6 +124,26 @@ def make_config(d, n_layers, n_heads, head_dim, ffn, text_vocab, card, window, m
     return c
 
 
+def config_from_shape(shape) -> mfs_config:
+    """An mfs_config from any object with the config's field names as attributes
+    (dtypes as the strings "bf16" / "f32")."""
+    s = shape
+    return make_config(d=s.d, n_layers=s.n_layers, n_heads=s.n_heads, head_dim=s.head_dim, ffn=s.ffn,
+                       text_vocab=s.text_vocab, card=s.card, window=s.window, max_pos=s.max_pos,
+                       dep_d=s.dep_d, dep_layers=s.dep_layers, dep_heads=s.dep_heads,
+                       dep_head_dim=s.dep_head_dim, dep_ffn=s.dep_ffn, delays=s.delays,
+                       rope_theta=s.rope_theta, eps=s.eps, weight_dtype=s.weight_dtype,
+                       kv_dtype=s.kv_dtype, max_slots=s.max_slots, n_q=s.n_q, dep_steps=s.dep_steps)
+
+
+def context_with_weights(shape, weights) -> "Ctx":
+    """A context for `shape` with every named tensor of `weights` loaded."""
+    ctx = mfs_create(config_from_shape(shape))
+    for name, arr in weights.items():
+        mfs_load_weights(ctx, name, arr)
+    return ctx
+
+
 def _current_stream():
     try:
         import torch

@@ -286,11 +286,17 @@ int mfs_rvq_encode(const float* z_sem, const float* z_ac, int T, int D, const fl
  *           enqueues work and returns without waiting
  * Returns MFS_OK, MFS_E_ARG (bad sizes or NULL pointers), MFS_E_RANGE (sizes
  * beyond the fixed scratch), or MFS_E_CUDA; mfs_last_error(NULL) then gives
- * the reason.  Nothing is launched when an error is returned.
+ * the reason.  MFS_E_ARG and MFS_E_RANGE are found before anything is
+ * enqueued.  MFS_E_CUDA from the launch itself can come after the clear of the
+ * row counters (a memset of the scratch) was already enqueued on the stream;
+ * the argmax kernel then did not run and `out` is unchanged.
  *
  * The first call on each device looks up the device address of the scratch
  * array (cudaGetSymbolAddress) with that device current: make that first call
- * before any stream capture on the device.  Every call on a device shares the
+ * before any stream capture on the device.  The address is cached per device
+ * for the life of the process and is not looked up again: after a
+ * cudaDeviceReset of that device the cached address is stale, so do not call
+ * this entry point on a device that was reset.  Every call on a device shares the
  * one array; each call first clears the per-row counters that must start at
  * zero.  Calls whose work overlaps on the GPU (other streams, other host
  * threads) race on the array and may return wrong indices: order them on one

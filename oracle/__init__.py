@@ -63,7 +63,7 @@ def _load():
         lib.orc_set_weight.argtypes = [vp, ctypes.c_char_p, vp, ctypes.c_longlong]
         lib.orc_reset_slot.argtypes = [vp, ci]
         lib.orc_position.argtypes = [vp, ci]
-        lib.orc_step.argtypes = [vp, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.orc_step.argtypes = [vp, ci, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
         lib.orc_set_sampling.argtypes = [vp, ci, ctypes.c_double, ci, ctypes.c_double, ci]
         lib.orc_rvq_encode.argtypes = [vp, vp, ci, ci, vp, ci, vp, vp]
         lib.orc_sample_topk.restype = ci
@@ -169,10 +169,14 @@ class Oracle:
         if self._lib.orc_set_sampling(self._h, slot, text_temp, text_k, audio_temp, audio_k) != 0:
             raise ValueError("bad slot")
 
-    def step(self, slots, codes, want_logits: bool = False, want_tokens: bool = False, uniforms=None):
+    def step(self, slots, codes, want_logits: bool = False, want_tokens: bool = False, uniforms=None,
+             follow=None):
         """codes [n,17] int (-1 = generate); uniforms [n,17] in [0, 1) switches on the
-        slots' sampling (stream k of row i draws with uniforms[i][k]).  Returns numpy arrays."""
+        slots' sampling (stream k of row i draws with uniforms[i][k]).  follow [n,17]
+        (follow mode): the token adopted for stream k wherever the oracle would
+        generate it (-1: its own choice); supplied tokens still win.  Returns numpy arrays."""
         unif = None if uniforms is None else np.ascontiguousarray(uniforms, np.float64).reshape(len(slots), 17)
+        fol = None if follow is None else np.ascontiguousarray(follow, np.int32).reshape(len(slots), 17)
         slots = np.ascontiguousarray(slots, np.int32)
         codes = np.ascontiguousarray(codes, np.int32).reshape(len(slots), 17)
         n, s = len(slots), self.shape
@@ -187,7 +191,7 @@ class Oracle:
                                 out["text"].ctypes.data, out["codes"].ctypes.data,
                                 _ptr(out.get("text_logits")), _ptr(out.get("dep_logits")),
                                 out["text_argmax"].ctypes.data, out["code_argmax"].ctypes.data,
-                                _ptr(out.get("x_tokens")), _ptr(unif))
+                                _ptr(out.get("x_tokens")), _ptr(unif), _ptr(fol))
         if rc != 0:
             raise ValueError(f"orc_step: {self._lib.orc_last_error(self._h).decode()} ({rc})")
         return out

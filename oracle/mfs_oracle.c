@@ -36,6 +36,15 @@
  *  S10 outputs: the text token of frame p and, per audio stream, the code of
  *      frame p-delay[k] (-1 for frames before 0); p advances by one.
  *
+ * Follow mode (a test input, not part of the method): orc_step can be given,
+ * per slot and stream, a token to adopt in place of its own argmax (or draw)
+ * wherever that stream's token is generated this step.  A comparison with
+ * another implementation passes that implementation's chosen tokens, so the
+ * two keep the same token history after a legal flip at a near tie (greedy
+ * agreement is only required above a top-2 margin: SGLang-Omni cookbook,
+ * PersonaPlex, "Reference parity").  A supplied token still takes precedence,
+ * and the arithmetic of every logit is unchanged.
+ *
  * Keys (after rotation) and values are cached in the cache's dtype: fp64, or
  * bf16 (round to nearest even) as the model's own KV cache is held
  * (SGLang-Omni cookbook, PersonaPlex, "Known limitations": BF16 KV per request);
@@ -600,7 +609,7 @@ static void embed(orc* o, orc_slot* s, const int* codes, double* x, int* x_token
 
 /* depformer for one slot; h[d] is the temporal output, t the text token. */
 static void depformer(orc* o, orc_slot* s, const double* h, int t, int* codes_out,
-                      double* logits_out, int* argmax_out, const double* unif)
+                      double* logits_out, int* argmax_out, const double* unif, const int* follow)
 {
     const orc_config* c = &o->c;
     int p = s->pos, d = c->d, dd = c->dep_d, dF = c->dep_ffn, C = c->card, S = c->dep_steps;
@@ -653,6 +662,7 @@ static void depformer(orc* o, orc_slot* s, const double* h, int t, int* codes_ou
         int f = p - c->delays[k];
         int forced = f >= 0 ? s->hist[k][mod(f, ORC_HIST)] : -1;
         int drawn = unif ? orc_sample_topk(lg, C, s->audio_temp, s->audio_k, unif[k]) : chat;
+        if (follow && follow[k] >= 0) drawn = follow[k];  /* follow mode: adopt the given token */
         int chosen = forced >= 0 ? forced : drawn;
         if (f >= 0) {
             s->hist[k][mod(f, ORC_HIST)] = chosen;
@@ -678,16 +688,19 @@ static int check_tokens(orc* o, const int* codes, int allow_generate)
 /* One frame step for n slots (processed one after another).
  * codes [n][17] (-1 = generate); text_out [n]; codes_out [n][16];
  * optional: text_logits [n][V], dep_logits [n][16][C], text_argmax [n],
- * code_argmax [n][16], x_tokens [n][17] (embedding rows read by S1). */
+ * code_argmax [n][16], x_tokens [n][17] (embedding rows read by S1),
+ * unif [n][17] (sampling), follow [n][17] (follow mode: token adopted for a
+ * generated stream, -1 = the oracle's own choice). */
 int orc_step(orc* o, int n, const int* slots, const int* codes, int* text_out, int* codes_out,
              double* text_logits, double* dep_logits, int* text_argmax, int* code_argmax,
-             int* x_tokens, const double* unif)
+             int* x_tokens, const double* unif, const int* follow)
 {
     const orc_config* c = &o->c;
     if (!weights_ready(o)) { snprintf(o->err, sizeof o->err, "weights missing"); return -3; }
     for (int i = 0; i < n; ++i) {
         if (slots[i] < 0 || slots[i] >= c->max_slots) { snprintf(o->err, sizeof o->err, "bad slot"); return -1; }
         if (check_tokens(o, codes + (size_t)i * ORC_STREAMS, 1)) { snprintf(o->err, sizeof o->err, "bad token"); return -4; }
+        if (follow && check_tokens(o, follow + (size_t)i * ORC_STREAMS, 1)) { snprintf(o->err, sizeof o->err, "bad follow token"); return -4; }
         if (o->slots[slots[i]].pos >= c->max_pos) { snprintf(o->err, sizeof o->err, "position limit"); return -5; }
     }
     int d = c->d, V = c->text_vocab;
@@ -706,12 +719,14 @@ int orc_step(orc* o, int n, const int* slots, const int* codes, int* text_out, i
         if (text_argmax) text_argmax[i] = that;
         const double* ui = unif ? unif + (size_t)i * ORC_STREAMS : NULL;
         int tdraw = ui ? orc_sample_topk(lg, V, s->text_temp, s->text_k, ui[0]) : that;
+        const int* fi = follow ? follow + (size_t)i * ORC_STREAMS : NULL;
+        if (fi && fi[0] >= 0) tdraw = fi[0];  /* follow mode */
         int t = cd[0] >= 0 ? cd[0] : tdraw;
         s->hist[0][mod(s->pos, ORC_HIST)] = t;
         text_out[i] = t;
         depformer(o, s, h, t, codes_out + (size_t)i * (ORC_STREAMS - 1),
                   dep_logits ? dep_logits + (size_t)i * c->dep_steps * c->card : NULL,
-                  code_argmax ? code_argmax + (size_t)i * c->dep_steps : NULL, ui);
+                  code_argmax ? code_argmax + (size_t)i * c->dep_steps : NULL, ui, fi);
         s->pos += 1;
     }
     free(x); free(h); free(lg);

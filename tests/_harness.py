@@ -17,21 +17,12 @@ FLIP_MARGIN = 0.1       # argmax may differ only below this top-2 margin
 
 def config_of(shape):
     from full_duplex_speech_frame_gb300 import mfs
-    s = shape
-    return mfs.make_config(d=s.d, n_layers=s.n_layers, n_heads=s.n_heads, head_dim=s.head_dim, ffn=s.ffn,
-                           text_vocab=s.text_vocab, card=s.card, window=s.window, max_pos=s.max_pos,
-                           dep_d=s.dep_d, dep_layers=s.dep_layers, dep_heads=s.dep_heads,
-                           dep_head_dim=s.dep_head_dim, dep_ffn=s.dep_ffn, delays=s.delays,
-                           rope_theta=s.rope_theta, eps=s.eps, weight_dtype=s.weight_dtype,
-                           kv_dtype=s.kv_dtype, max_slots=s.max_slots, n_q=s.n_q, dep_steps=s.dep_steps)
+    return mfs.config_from_shape(shape)
 
 
 def gpu_context(shape, weights):
     from full_duplex_speech_frame_gb300 import mfs
-    ctx = mfs.mfs_create(config_of(shape))
-    for name, arr in weights.items():
-        mfs.mfs_load_weights(ctx, name, arr)
-    return ctx
+    return mfs.context_with_weights(shape, weights)
 
 
 def check_logits(gpu: np.ndarray, ref: np.ndarray, what: str) -> float:

@@ -180,6 +180,66 @@ def test_delay_schedule_free_running(tiny_w8):
     assert (X >= 0).all()
 
 
+def _chosen_as_follow(s, r):
+    """Follow-mode input from one step's results: the chosen token of every stream,
+    and for a frame before 0 (output -1) the raw argmax the substep chain used."""
+    f = np.empty((len(r["text"]), 17), np.int32)
+    f[:, 0] = r["text"]
+    f[:, 1:] = np.where(r["codes"] >= 0, r["codes"], r["code_argmax"])
+    return f
+
+
+def test_follow_with_own_choices_changes_nothing(tiny_w8):
+    """Follow mode fed the oracle's own chosen tokens reproduces every output and
+    logit bit for bit (it only replaces a choice by the same choice)."""
+    s, w = tiny_w8
+    T = 8
+    inp = synth.user_frames(s, 23, T, 2)
+    a, b = oracle.Oracle(s, w), oracle.Oracle(s, w)
+    for p in range(T):
+        ra = a.step([0, 1], inp[p], want_logits=True, want_tokens=True)
+        rb = b.step([0, 1], inp[p], want_logits=True, want_tokens=True, follow=_chosen_as_follow(s, ra))
+        for key in ra:
+            np.testing.assert_array_equal(ra[key], rb[key])
+
+
+def test_follow_equals_forcing_the_same_frame(tiny_w8):
+    """Adopting token v for a generated stream k is the same as the caller supplying v
+    for that stream's frame: at the same step for a stream without delay, at the step
+    before for a delayed one.  Outputs, logits and embedding rows agree bit for bit."""
+    s, w = tiny_w8
+    T = 9
+    inp = synth.user_frames(s, 24, T, 1)[:, 0]
+    toks = synth.uniform_int(24, 90, T * 17, 0, 1000).reshape(T, 17)
+    fol = np.full((T, 17), -1, np.int32)
+    forced = inp.copy()
+    for p in range(1, T - 1):
+        for k in (0, 1, 2, 5, 8):  # text, an undelayed and three delayed agent streams (generated)
+            v = int(toks[p, k]) % (s.text_vocab if k == 0 else s.card)
+            forced[p, k] = v                       # the caller supplies frame p
+            fol[p + s.delays[k], k] = v            # follow mode adopts it when frame p is generated
+    a, b, plain = oracle.Oracle(s, w), oracle.Oracle(s, w), oracle.Oracle(s, w)
+    changed = 0
+    for p in range(T):
+        ra = a.step([0], inp[p:p + 1], want_logits=True, want_tokens=True, follow=fol[p:p + 1])
+        rb = b.step([0], forced[p:p + 1], want_logits=True, want_tokens=True)
+        rp = plain.step([0], inp[p:p + 1], want_logits=True)
+        for key in ("text", "codes", "text_logits", "dep_logits", "x_tokens", "text_argmax", "code_argmax"):
+            np.testing.assert_array_equal(ra[key], rb[key], err_msg=f"step {p} {key}")
+        changed += int(not np.array_equal(ra["dep_logits"], rp["dep_logits"]))
+    assert changed >= T - 2  # the adopted tokens really changed the run (not a vacuous pin)
+
+
+def test_follow_rejects_out_of_range_tokens(tiny_w8):
+    s, w = tiny_w8
+    o = oracle.Oracle(s, w)
+    fol = np.full((1, 17), -1, np.int32)
+    fol[0, 4] = s.card
+    with pytest.raises(ValueError):
+        o.step([0], synth.user_frames(s, 25, 1, 1)[0], follow=fol)
+    assert o.position(0) == 0
+
+
 # ----------------------------------------------------------------------------- model
 
 @pytest.mark.parametrize("T", [20])
