@@ -225,7 +225,7 @@ def run_gpu(args, rank, world):
     # a stream of our own: the library enqueues on it and the events below time it
     side = torch.cuda.Stream()
     torch.cuda.set_stream(side)
-    s = WORKLOAD.shape
+    s = WORKLOAD.shape.replace(max_slots=32)  # slot 0 runs the B = 1 workload, all 32 the batched ones
     n = WORKLOAD.batch
     need = 3 * args.warmup + 4 * args.steps
     if PROMPT + need > s.max_pos:
@@ -322,6 +322,8 @@ def run_gpu(args, rank, world):
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     barrier(world)
 
+    batched = run_batched(args, mfs, ctx, s, stream, world) if not args.no_batched else {}
+
     # the Mimi split RVQ encoder on 152 x 16 frames (D 256, 2048 codewords per codebook)
     Tq, Dq, Cq = 2432, 256, 2048
     zq = torch.from_numpy(synth.normal_f32(WORKLOAD.input_seed, 501, 2 * Tq * Dq).reshape(2, Tq, Dq)).cuda()
@@ -380,6 +382,7 @@ def run_gpu(args, rank, world):
                              "frac": Tq * 8 * Cq * Dq / (rvq_ms / 1000.0) / (152 * 128 * 2.07e9 / 2),
                              "peak_kind": "152 SMs x 128 fp32 lanes x 2.07 GHz, 2 instructions (subtract, fma) per term"},
             },
+            **batched,
             "sampling_heads": {
                 "what": "mfs_step_sampled with text temperature 0.7 / top-25 and audio 0.8 / top-250 "
                         "(uniforms supplied per step); device time of the step kernel",
@@ -392,6 +395,85 @@ def run_gpu(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_batched(args, mfs, ctx, s, stream, world):
+    """The batched workloads on slots 0..B-1 of the same context, device-resident
+    (inputs in HBM, no host copies in the timed region).  Every step streams the
+    16.1 GB of weights once for all slots (the tensor-core pass) plus each slot's
+    key/value window, more than L2 holds, so no flush is needed.
+      B = 8:  per-slot windows uniform in [0, 3000] (synthetic ring states)
+      B = 16: 250-frame prompts for every slot (timed as well: the prompt path),
+              then decode frames from position 250
+      B = 32: every ring full (3000 keys, positions past 3000: every step wraps)
+    Returns {name: line}, each with aggregate frames/s, ms per step, algorithmic
+    bytes per step and the fraction of the measured HBM bandwidth."""
+    import torch
+    hbm, peak_kind = read_peaks()
+    shared = synth.slot_state(s, WORKLOAD.input_seed, 300, 0)
+    out = {}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def time_steps(B, lens_of_step, seed):
+        slots = list(range(B))
+        frames = torch.from_numpy(synth.user_frames(s, seed, args.warmup + args.steps, B)).cuda()
+        d_text = torch.empty(B, dtype=torch.int32, device="cuda")
+        d_out = torch.empty(B, 16, dtype=torch.int32, device="cuda")
+        for p in range(args.warmup):
+            mfs.mfs_step_device(ctx, slots, frames[p], d_text, d_out)
+        mfs.mfs_sync(ctx)
+        lens = [lens_of_step(args.warmup + k) for k in range(args.steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for k in range(args.steps):
+            mfs.mfs_step_device(ctx, slots, frames[args.warmup + k], d_text, d_out)
+        e1.record(stream)
+        mfs.mfs_sync(ctx)
+        torch.cuda.synchronize()
+        barrier(world)
+        ms = max_over_ranks(e0.elapsed_time(e1), world) / args.steps
+        byts = sum(algorithmic_bytes(s, l) for l in lens) / args.steps
+        return {"value": B * world / (ms / 1000.0), "unit": UNIT, "ms_per_step": ms, "batch": B,
+                "algorithmic_bytes_per_step": byts,
+                "roofline": {"bound": "hbm", "achieved": byts / (ms / 1000.0) / 1e9, "peak": hbm, "unit": "GB/s",
+                             "frac": byts / (ms / 1000.0) / 1e9 / hbm, "peak_kind": f"{peak_kind} hbm_gbs"},
+                "launches_per_step": mfs.mfs_launches_per_step(ctx)}
+
+    # B = 8: windows uniform in [0, 3000]
+    lens8 = synth.prefill_lengths(WORKLOAD.input_seed, 8, 0, 3000)
+    for i in range(8):
+        shared[4:8] = np.frombuffer(np.int32(lens8[i]).tobytes(), np.uint8)
+        mfs.mfs_import_slot(ctx, i, shared)
+    r = time_steps(8, lambda k: [min(int(lens8[i]) + k + 1, s.window) for i in range(8)], 11)
+    r["what"] = "B=8 decode, per-slot windows uniform in [0, 3000] (synthetic ring states), tensor-core weight pass"
+    out["batch_8"] = r
+
+    # B = 16: 250-frame prompts (timed), then decode
+    for i in range(16):
+        mfs.mfs_reset_slot(ctx, i)
+    prompt = torch.from_numpy(synth.forced_frames(s, WORKLOAD.input_seed, synth.STREAM_PROMPT, PROMPT, 16)
+                              .transpose(1, 0, 2).copy())
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    mfs.mfs_prefill(ctx, list(range(16)), prompt.numpy())
+    torch.cuda.synchronize()
+    pre_s = time.perf_counter() - t0
+    r = time_steps(16, lambda k: [min(PROMPT + k + 1, s.window)] * 16, 12)
+    r["what"] = "B=16 decode after 250-frame prompts, tensor-core weight pass"
+    r["prompt"] = {"frames": 16 * PROMPT, "seconds": pre_s, "value": 16 * PROMPT / pre_s, "unit": "prompt frames/s",
+                   "what": "mfs_prefill of 16 slots x 250 frames (host call, includes the token upload)"}
+    out["batch_16"] = r
+
+    # B = 32: full rings, every step wraps
+    pos32 = 3000 + synth.uniform_int(WORKLOAD.input_seed, synth.STREAM_LENGTHS + 1, 32, 0, 2000)
+    for i in range(32):
+        shared[4:8] = np.frombuffer(np.int32(pos32[i]).tobytes(), np.uint8)
+        mfs.mfs_import_slot(ctx, i, shared)
+    r = time_steps(32, lambda k: [s.window] * 32, 13)
+    r["what"] = "B=32 decode, every ring full (3000 keys, every step wraps), tensor-core weight pass"
+    out["batch_32"] = r
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -399,6 +481,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-batched", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

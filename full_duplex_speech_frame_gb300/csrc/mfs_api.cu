@@ -4,6 +4,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <cudaTypedefs.h>
+
 #include <map>
 #include <new>
 #include <cstddef>
@@ -74,8 +76,13 @@ struct mfs_ctx {
     Params P;
     int nphase = 0, nphase_prefill = 0;
     int maxrows = 0;
-    size_t smem[3] = {0, 0, 0};
-    const void* kfn[3] = {nullptr, nullptr, nullptr};
+    // kernels: batch groups of 1, 2, 4 slots (CUDA cores), then the tensor-core pass (bf16 weights only)
+    size_t smem[4] = {0, 0, 0, 0};
+    const void* kfn[4] = {nullptr, nullptr, nullptr, nullptr};
+    int threads[4] = {0, 0, 0, 0};
+    CUtensorMap* d_tmaps = nullptr;
+    int ntmaps = 0;
+    char* mma_buf = nullptr;      // tensor-core pass: partial tile sums, phase completion tags
     std::vector<int> pos;
     std::map<std::string, TensorInfo> tensors;
     int mode = 0;
@@ -126,7 +133,13 @@ const void* kernel_bf16(int bg) { return bg == 1 ? kernel_bf16_1() : bg == 2 ? k
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-static int bg_index(int n) { return n <= 1 ? 0 : (n == 2 ? 1 : 2); }
+// Kernel for a step of n slots: matrix-vector passes over groups of 1, 2 or 4
+// slots, or (bf16 weights, n >= 5) one tensor-core pass for all of them.
+static int kernel_index(const mfs_ctx* c, int n)
+{
+    if (n >= 5 && c->kfn[3]) return 3;
+    return n <= 1 ? 0 : (n == 2 ? 1 : 2);
+}
 static int bg_value(int idx) { return idx == 0 ? 1 : (idx == 1 ? 2 : 4); }
 
 // ------------------------------------------------------------------ create
@@ -301,6 +314,109 @@ static int max_rows(const mfs_config& g, int G)
 
 static thread_local std::string g_create_error;
 
+// Tiles of one matrix a CTA can touch in one phase, at most (cnt CTAs share it).
+static int tiles_touched(long long M, long long K, long long cnt)
+{
+    const long long KC = (K + MMA_KC - 1) / MMA_KC, T = (M + MMA_M - 1) / MMA_M;
+    const long long per = (T * KC + cnt - 1) / cnt;
+    return (int)((per + KC - 1) / KC + 1);
+}
+
+// Shared memory of the tensor-core instantiation: alignment slack, barriers,
+// stages, then one region for epilogue tile values, attention partials,
+// embedding rows or the sampler, whichever phase runs.
+static size_t mma_smem(const mfs_config& g)
+{
+    const size_t tile = (size_t)MMA_M * 32 * sizeof(float);
+    const size_t attn_w = (size_t)NWARP * (g.head_dim + 4) * sizeof(float);
+    const size_t attn_m = (size_t)NCHUNK_MAX * (g.head_dim + 2) * sizeof(float);
+    const size_t emb = (size_t)MFS_MAX_SLOTS * NSTREAM * sizeof(int);
+    const size_t samp = (size_t)(2048 + MFS_MAX_SLOTS * NSTREAM) * sizeof(int);
+    size_t region = tile;
+    for (size_t r : {attn_w, attn_m, emb, samp}) region = r > region ? r : region;
+    return 1024 + (size_t)MMA_HEAD + (size_t)MMA_NSTAGE * MMA_STAGE + region;
+}
+
+// One tensor map per weight matrix (tmap_index order): bf16 [rows][K], boxes of
+// 64 columns x 128 rows with the 128-byte swizzle the MMA operand layout expects.
+static int setup_tensor_core_pass(mfs_ctx* c)
+{
+    const mfs_config& g = c->cfg;
+    const long long d = g.d, F = g.ffn, dd = g.dep_d, dF = g.dep_ffn, V = g.text_vocab, C = g.card, S = g.dep_steps;
+    const int L = g.n_layers, dL = g.dep_layers;
+    // every matrix must leave a CTA at most MMA_MAX_TILES accumulator slots
+    struct Mat { long long M, K; };
+    const Mat tm[] = {{3 * d, d}, {d, d}, {2 * F, d}, {d, F}, {V + S * dd, d}};
+    const Mat dm[] = {{3 * dd, dd}, {dd, dd}, {2 * dF, dd}, {dd, dF}, {C, dd}};
+    for (const Mat& m : tm)
+        if (tiles_touched(m.M, m.K, c->G) > MMA_MAX_TILES) return MFS_OK;  // shape unsuited: batches stay on CUDA cores
+    for (const Mat& m : dm)
+        if (tiles_touched(m.M, m.K, c->G / MAXGW) > MMA_MAX_TILES) return MFS_OK;
+    const size_t smem = mma_smem(g);
+    if (smem > 227 * 1024) return MFS_OK;
+
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    CK(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q));
+    if (!fn || q != cudaDriverEntryPointSuccess) return fail(c, MFS_E_CUDA, "cuTensorMapEncodeTiled is not available");
+    auto encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    c->ntmaps = 4 * L + 1 + (int)S * (4 * dL + 1);
+    std::vector<CUtensorMap> maps((size_t)c->ntmaps);
+    auto make = [&](int idx, const void* base, long long M, long long K) -> int {
+        if (((uintptr_t)base & 15u) != 0 || (K * 2) % 16 != 0) return fail(c, MFS_E_ARG, "tensor map: misaligned matrix");
+        const cuuint64_t dim[2] = {(cuuint64_t)K, (cuuint64_t)M};
+        const cuuint64_t stride[1] = {(cuuint64_t)(K * 2)};
+        const cuuint32_t box[2] = {(cuuint32_t)MMA_KC, (cuuint32_t)MMA_M};
+        const cuuint32_t es[2] = {1, 1};
+        const CUresult r = encode(&maps[(size_t)idx], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dim,
+                                  stride, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return fail(c, MFS_E_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+        return MFS_OK;
+    };
+    const uint16_t* tw = (const uint16_t*)c->P.tw;
+    const size_t tl = (size_t)c->P.t_layer;
+    int rc = MFS_OK;
+    for (int l = 0; l < L && rc == MFS_OK; ++l) {
+        const uint16_t* b = tw + (size_t)l * tl;
+        if (!rc) rc = make(tmap_index(PH_QKV, l, 0, L, dL), b, 3 * d, d);
+        if (!rc) rc = make(tmap_index(PH_O, l, 0, L, dL), b + 3 * d * d, d, d);
+        if (!rc) rc = make(tmap_index(PH_GU, l, 0, L, dL), b + 4 * d * d, 2 * F, d);
+        if (!rc) rc = make(tmap_index(PH_DOWN, l, 0, L, dL), b + 4 * d * d + 2 * F * d, d, F);
+    }
+    if (!rc) rc = make(tmap_index(PH_HEAD, 0, 0, L, dL), c->P.head, V + S * dd, d);
+    const uint16_t* dw = (const uint16_t*)c->P.dw;
+    for (int j = 0; j < S && rc == MFS_OK; ++j)
+        for (int l = 0; l < dL && rc == MFS_OK; ++l) {
+            const uint16_t* b = dw + (size_t)j * c->P.d_sub + (size_t)l * c->P.d_layer;
+            if (!rc) rc = make(tmap_index(PH_DQKV, l, j, L, dL), b, 3 * dd, dd);
+            if (!rc) rc = make(tmap_index(PH_DO, l, j, L, dL), b + 3 * dd * dd, dd, dd);
+            if (!rc) rc = make(tmap_index(PH_DGU, l, j, L, dL), b + 4 * dd * dd, 2 * dF, dd);
+            if (!rc) rc = make(tmap_index(PH_DDOWN, l, j, L, dL), b + 4 * dd * dd + 2 * dF * dd, dd, dF);
+            if (!rc && l == dL - 1) rc = make(tmap_index(PH_DHEAD, 0, j, L, dL), dw + (size_t)j * c->P.d_sub + (size_t)dL * c->P.d_layer, C, dd);
+        }
+    if (rc != MFS_OK) return rc;
+    CK(cudaMalloc((void**)&c->d_tmaps, maps.size() * sizeof(CUtensorMap)));
+    CK(cudaMemcpy(c->d_tmaps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice));
+    c->P.tmaps = c->d_tmaps;
+    // partial tile sums and phase completion tags
+    const size_t part = (size_t)2 * c->G * MMA_M * 32 * sizeof(uint2), pssq = (size_t)2 * c->G * 32 * sizeof(uint2);
+    const size_t done = (size_t)c->nphase * c->G * sizeof(unsigned);
+    CK(cudaMalloc((void**)&c->mma_buf, part + pssq + done));
+    CK(cudaMemset(c->mma_buf, 0, part + pssq + done));
+    c->P.mpart = (uint2*)c->mma_buf;
+    c->P.mssq = (uint2*)(c->mma_buf + part);
+    c->P.done = (unsigned*)(c->mma_buf + part + pssq);
+    c->kfn[3] = kernel_bf16_mma();
+    c->threads[3] = MMA_THREADS;
+    c->smem[3] = smem;
+    CK(cudaFuncSetAttribute(c->kfn[3], cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    int per_sm = 0;
+    CK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, c->kfn[3], MMA_THREADS, smem));
+    if (per_sm < 1) return fail(c, MFS_E_CUDA, "tensor-core kernel does not fit on an SM");
+    return MFS_OK;
+}
+
 static int create_impl(mfs_ctx* c, void* cuda_stream)
 {
     int rc = check_config(c, c->cfg);
@@ -444,6 +560,11 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
 
     // kernels: one per batch group; shared memory for the largest row block
     c->maxrows = max_rows(g, c->G);
+    for (int i = 0; i < 4; ++i) c->threads[i] = NT + 32;
+    if (g.weight_dtype == MFS_DTYPE_BF16) {
+        int rc2 = setup_tensor_core_pass(c);
+        if (rc2 != MFS_OK) return rc2;
+    }
     for (int i = 0; i < 3; ++i) {
         const int bg = bg_value(i);
         c->kfn[i] = g.weight_dtype == MFS_DTYPE_BF16 ? kernel_bf16(bg) : kernel_f32(bg);
@@ -501,6 +622,8 @@ extern "C" void mfs_destroy(mfs_ctx* c)
     cudaFree(c->act); cudaFree(c->rope); cudaFree(c->d_phases); cudaFree(c->d_desc); cudaFree(c->d_pref);
     cudaFree(c->d_err);
     cudaFree(c->d_ptime);
+    cudaFree(c->d_tmaps);
+    cudaFree(c->mma_buf);
     for (int i = 0; i < DESC_RING; ++i)
         if (c->desc_ev[i]) cudaEventDestroy(c->desc_ev[i]);
     for (cudaEvent_t e : c->ev_pool) cudaEventDestroy(e);
@@ -584,7 +707,7 @@ static int launch(mfs_ctx* c, int n, int nph, const StepDesc* desc)
     P.desc = desc;
     P.ptime = c->stamps ? c->d_ptime : nullptr;
     c->last_nph = nph;
-    const int bi = bg_index(n);
+    const int bi = kernel_index(c, n);
     int maxrows = c->maxrows;
     cudaEvent_t ev1 = nullptr;
     if (c->timing) {
@@ -602,13 +725,13 @@ static int launch(mfs_ctx* c, int n, int nph, const StepDesc* desc)
     if (c->mode == 0) {
         int ph0 = 0, ph1 = nph;
         void* args[] = {&P, &ph0, &ph1, &maxrows};
-        CK(cudaLaunchCooperativeKernel(c->kfn[bi], dim3(c->G), dim3(NT + 32), args, c->smem[bi], c->stream));
+        CK(cudaLaunchCooperativeKernel(c->kfn[bi], dim3(c->G), dim3(c->threads[bi]), args, c->smem[bi], c->stream));
         c->launches = 1;
     } else {
         for (int ph = 0; ph < nph; ++ph) {
             int ph0 = ph, ph1 = ph + 1;
             void* args[] = {&P, &ph0, &ph1, &maxrows};
-            CK(cudaLaunchKernel(c->kfn[bi], dim3(c->G), dim3(NT + 32), args, c->smem[bi], c->stream));
+            CK(cudaLaunchKernel(c->kfn[bi], dim3(c->G), dim3(c->threads[bi]), args, c->smem[bi], c->stream));
         }
         c->launches = nph;
     }

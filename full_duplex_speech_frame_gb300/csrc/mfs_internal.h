@@ -1,6 +1,7 @@
 // Internal layout shared by the host side of the library and its kernels.
 #pragma once
 #include <stdint.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/mfs.h"
@@ -35,6 +36,46 @@ constexpr int NSTREAM = MFS_N_STREAMS;
 constexpr int NCHUNK_MAX = 32;   // attention split over the window, per (slot, head)
 constexpr int HIST = 3;          // frames of token history per stream
 constexpr int MAXGW = 8;         // depformer substeps run together as one group, at most
+
+// Tensor-core weight pass (batches of 5..32 slots, bf16 weights): a matrix is
+// cut into tiles of MMA_M rows and K-chunks of MMA_KC columns; one stage holds
+// a weight tile chunk (TMA, 128-byte swizzle) and the slots' activations as
+// bf16 high and low halves (up to 64 operand rows).
+constexpr int BG_MMA = 32;                            // instantiation marker: up to 32 slots per weight pass
+__host__ __device__ constexpr bool is_mma(int bg) { return bg >= 8; }
+constexpr int MMA_M = 128;
+constexpr int MMA_KC = 64;
+constexpr int MMA_W_BYTES = MMA_M * MMA_KC * 2;       // 16 KB
+constexpr int MMA_B_BYTES = 64 * MMA_KC * 2;          // 8 KB
+constexpr int MMA_STAGE = MMA_W_BYTES + MMA_B_BYTES;  // 24 KB
+constexpr int MMA_NSTAGE = 8;
+constexpr int MMA_HEAD = 3072;                        // barriers and scalars before the stages
+constexpr int MMA_TMEM_COLS = 512;
+constexpr int MMA_MAX_TILES = 8;                      // accumulator slots (tiles a CTA touches in one phase)
+constexpr int MMA_THREADS = 32 * (8 + 2);             // 8 consumer warps, the producer warp, the MMA warp
+// slots padded to 8, 16 or 32 (two operand rows each: N = 16, 32 or 64)
+__host__ __device__ constexpr int mma_nbp(int n) { return n <= 8 ? 8 : (n <= 16 ? 16 : 32); }
+
+// Weight matrices that have a tensor map (index into Params.tmaps): per
+// temporal layer QKV, O, GU, DOWN; the text head (+ depformer in-projections);
+// per depformer substep and layer DQKV, DO, DGU, DDOWN, then the substep's head.
+__host__ __device__ inline int tmap_index(int type, int l, int j, int L, int dL)
+{
+    // PhaseType values are below; kept as ints so the host can use this too
+    switch (type) {
+        case 1: return 4 * l + 0;   // PH_QKV
+        case 3: return 4 * l + 1;   // PH_O
+        case 4: return 4 * l + 2;   // PH_GU
+        case 5: return 4 * l + 3;   // PH_DOWN
+        case 6: return 4 * L;       // PH_HEAD
+        case 7: return 4 * L + 1 + j * (4 * dL + 1) + 4 * l + 0;  // PH_DQKV
+        case 9: return 4 * L + 1 + j * (4 * dL + 1) + 4 * l + 1;  // PH_DO
+        case 10: return 4 * L + 1 + j * (4 * dL + 1) + 4 * l + 2; // PH_DGU
+        case 11: return 4 * L + 1 + j * (4 * dL + 1) + 4 * l + 3; // PH_DDOWN
+        case 12: return 4 * L + 1 + j * (4 * dL + 1) + 4 * dL;    // PH_DHEAD
+        default: return -1;
+    }
+}
 
 enum PhaseType : int {
     PH_EMBED = 0,  // S0 + S1: record frame p's tokens, delayed embedding sum
@@ -142,11 +183,17 @@ struct Params {
     int* err_seq;    // step sequence number that raised it
     const Phase* phases;
     unsigned long long* ptime;  // optional: CTA 0 timer stamps and stage-wait sums, [nphase + 1][8]
+    // tensor-core path
+    const CUtensorMap* tmaps;   // per weight matrix (tmap_index), bf16 [rows][K], box 64 x 128, 128-byte swizzle
+    unsigned* done;             // [nphase][G] tag of the last phase each CTA finished
+    uint2* mpart;               // [2][G][MMA_M][32] partial tile sums a CTA leaves for a tile's owner (tagged)
+    uint2* mssq;                // [2][G][32] partial sums of squares of the inputs of that tile part (tagged)
 };
 
 // Kernel entry points, one per (weight dtype, batch group).  Defined in the
 // per-instantiation translation units.
 const void* kernel_f32(int bg);
 const void* kernel_bf16(int bg);
+const void* kernel_bf16_mma();
 
 }  // namespace mfs

@@ -30,6 +30,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "mfs_internal.h"
 
 namespace mfs {
@@ -392,7 +394,7 @@ struct Smem {
     uint64_t* full;   // [nstage] stage filled
     uint64_t* empty;  // [nstage] stage released
     float* ssq;       // [4][16] per-K-slice sums of squares
-    int* prev;        // [4] depformer input token per batch row
+    int* prev;        // [4] (tensor-core path: [32]) depformer input token per batch row
     float* amv;       // [NWARP]
     int* ami;         // [NWARP]
     int* misc;        // [0] phase index (diagnostic stamps)
@@ -401,6 +403,18 @@ struct Smem {
     float* yf;        // [maxrows][BG] final row values of the CTA
     int* X;           // embedding rows of this step (aliases red)
     float* wbuf;      // attention partials of the consumer warps (aliases red)
+    // tensor-core path (null in the matrix-vector instantiations)
+    uint64_t* wfull;  // [MMA_NSTAGE] weight chunk landed (TMA)
+    uint64_t* bfull;  // [MMA_NSTAGE] activation chunk written (one arrival per consumer warp)
+    uint64_t* sempty; // [MMA_NSTAGE] stage consumed by the MMAs (tcgen05.commit)
+    uint64_t* accf;   // [MMA_MAX_TILES] accumulator of a tile slot complete (tcgen05.commit)
+    uint64_t* accfree;  // the consumers have read every accumulator of the phase
+    uint64_t* mdone;  // every MMA the CTA issued has completed (before TMEM is freed)
+    uint32_t* tslot;  // TMEM base address from tcgen05.alloc
+    float* pssq;      // [MMA_MAX_TILES][32] this CTA's sums of squares of its inputs per tile part
+    float* bestv;     // [32] deferred argmax partials over the tiles a CTA owns
+    int* besti;       // [32]
+    char* mring;      // [MMA_NSTAGE][MMA_STAGE], 1024-byte aligned
 };
 
 __device__ __forceinline__ Smem smem_map(char* base, int maxrows, int BG)
@@ -416,6 +430,43 @@ __device__ __forceinline__ Smem smem_map(char* base, int maxrows, int BG)
     s.ring = base + SMEM_HEAD;
     s.red = (float*)(s.ring + (size_t)nstage_for(BG) * STAGE_BYTES);
     s.yf = s.red + (size_t)maxrows * BG * NWARP;
+    s.X = (int*)s.red;
+    s.wbuf = s.red;
+    s.wfull = s.bfull = s.sempty = s.accf = s.accfree = s.mdone = nullptr;
+    s.tslot = nullptr;
+    s.pssq = s.bestv = nullptr;
+    s.besti = nullptr;
+    s.mring = nullptr;
+    return s;
+}
+
+// Tensor-core instantiation: barriers and scalars in the first MMA_HEAD bytes
+// of a 1024-byte aligned base, then the stages, then one region shared by the
+// tile values of an epilogue, the attention partials, the embedding rows and
+// the sampler (never live at the same time).
+__device__ __forceinline__ Smem smem_map_mma(char* base)
+{
+    Smem s;
+    s.wfull = (uint64_t*)base;
+    s.bfull = s.wfull + 8;
+    s.sempty = s.wfull + 16;
+    s.accf = s.wfull + 24;
+    s.accfree = s.wfull + 32;
+    s.mdone = s.wfull + 33;
+    s.tslot = (uint32_t*)(base + 272);
+    s.full = s.empty = nullptr;
+    s.ssq = (float*)(base + 320);     // [4][16], unused here
+    s.prev = (int*)(base + 576);      // [32]
+    s.amv = (float*)(base + 704);     // [NWARP]
+    s.ami = (int*)(base + 736);       // [NWARP]
+    s.misc = (int*)(base + 768);      // [64]
+    s.pssq = (float*)(base + 1024);   // [MMA_MAX_TILES][32]
+    s.bestv = (float*)(base + 2048);  // [32]
+    s.besti = (int*)(base + 2176);    // [32]
+    s.mring = base + MMA_HEAD;
+    s.ring = nullptr;
+    s.red = (float*)(s.mring + (size_t)MMA_NSTAGE * MMA_STAGE);
+    s.yf = s.red;
     s.X = (int*)s.red;
     s.wbuf = s.red;
     return s;
@@ -818,8 +869,10 @@ __device__ __forceinline__ const float* head_logits(const Params& P, int i, int 
 // Input token of depformer substep j for each batch row: the token supplied
 // for stream j (this frame, or the frame before for a delayed stream) if any,
 // else, at a group's first substep only, the argmax of the head before it (the
-// text head for j = 0).  Every consumer thread calls it; false if a wait gave up.
-__device__ __forceinline__ bool dep_select_inputs(const Params& P, const XSrc& xs, int b0, int nb, const Smem& sm)
+// text head for j = 0).  Rows b0 .. b0+nb-1 (nb <= NWARP) land in
+// sm.prev[poff ..].  Every consumer thread calls it; false if a wait gave up.
+__device__ __forceinline__ bool dep_select_inputs(const Params& P, const XSrc& xs, int b0, int nb, const Smem& sm,
+                                                  int poff = 0)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int j = xs.dj;
@@ -835,16 +888,16 @@ __device__ __forceinline__ bool dep_select_inputs(const Params& P, const XSrc& x
             ok = chosen >= 0;
         }
         const int lim = j == 0 ? P.V : P.C;
-        if (lane == 0) sm.prev[warp] = (chosen >= 0 && chosen < lim) ? chosen : 0;  // keeps the embedding read in range
+        if (lane == 0) sm.prev[poff + warp] = (chosen >= 0 && chosen < lim) ? chosen : 0;  // keeps the embedding read in range
         float it_;
         int ik_;
-        if (lane == 0) sm.misc[8 + warp] = sampled && generated && j == xs.dj0 && sampling_on(P, i, j, it_, ik_);
+        if (lane == 0) sm.misc[8 + poff + warp] = sampled && generated && j == xs.dj0 && sampling_on(P, i, j, it_, ik_);
     }
     if (!csync_and(ok)) return false;
     // rows that draw their token: every CTA draws the same one from the head's logits
     // (written before the partials were published, which the argmax wait saw)
     for (int b = 0; b < nb && sampled; ++b) {
-        if (!sm.misc[8 + b]) continue;
+        if (!sm.misc[8 + poff + b]) continue;
         __threadfence();
         const int i = b0 + b;
         float inv_t;
@@ -854,7 +907,7 @@ __device__ __forceinline__ bool dep_select_inputs(const Params& P, const XSrc& x
         const int tok = sample_topk_cta(lg, N, inv_t, topk, P.unif[(size_t)i * NSTREAM + j], sm);
         if (threadIdx.x == 0) {
             const int lim = j == 0 ? P.V : P.C;
-            sm.prev[b] = (tok >= 0 && tok < lim) ? tok : 0;
+            sm.prev[poff + b] = (tok >= 0 && tok < lim) ? tok : 0;
             if (blockIdx.x == 0) P.drawn[(size_t)i * NSTREAM + j] = tok;
         }
         csync();
@@ -1255,7 +1308,14 @@ struct EpiLogits {
     uint2* am;            // argmax partials: batch row i, this CTA at am + i * am_stride + am_idx * 2
     long long am_stride;
     int am_idx;
+    float* dv = nullptr;  // deferred (several tiles per CTA): best value / index per batch row, published by flush()
+    int* di = nullptr;
     __device__ Pre pre(const Params&, int, int, int, int) const { return Pre{{0.f, 0.f}, {0.f, 0.f}, 1}; }
+    __device__ void flush(const Params& P, int b0, int nb) const
+    {
+        if (P.desc->sampled) __threadfence();
+        if (threadIdx.x < nb) publish(P, b0 + threadIdx.x, dv[threadIdx.x], di[threadIdx.x]);
+    }
     __device__ void publish(const Params& P, int i, float v, int ix) const
     {
         uint2* e = am + (size_t)i * am_stride + (size_t)am_idx * 2;
@@ -1296,7 +1356,11 @@ struct EpiLogits {
                 int ix = sm.ami[0];
                 for (int k = 1; k < NWARP; ++k)
                     if (am_better(sm.amv[k], sm.ami[k], v, ix)) { v = sm.amv[k]; ix = sm.ami[k]; }
-                publish(P, b0 + b, v, ix);
+                if (dv) {
+                    if (am_better(v, ix, dv[b], di[b])) { dv[b] = v; di[b] = ix; }
+                } else {
+                    publish(P, b0 + b, v, ix);
+                }
             }
         }
         return true;
@@ -1355,6 +1419,515 @@ __device__ __forceinline__ bool gemv_phase(const Params& P, const Phase& ph, int
             epi.empty(P, b0, nb);
         }
     }
+    return true;
+}
+
+// ------------------------------------------------------------------ tensor-core weight pass
+// Batches of 5..32 slots with bf16 weights: every matrix phase is a product of
+// the weight matrix (A, M rows x K) with the slots' activations (B, N rows x
+// K, N = 2 x slots padded to 8/16/32: each activation is split into a bf16
+// high half and the bf16 rounding of the remainder, so the product keeps
+// about 16 significant bits of the fp32 input and the weights are read once
+// for all slots).  tcgen05.mma accumulates in fp32 in tensor memory.
+//
+// A matrix is cut into units (tile of 128 rows, K-chunk of 64); CTA c of the
+// cnt sharing the matrix takes the contiguous units [U c / cnt, U (c+1) / cnt)
+// in tile-major order.  Per unit the producer warp loads the weight chunk with
+// a 2-D TMA copy (128-byte swizzle), the consumer warps write the activation
+// chunk (their tagged fp32 inputs, gain applied, split) into the stage in the
+// same swizzled layout, and the MMA warp issues 4 MMAs of K = 16.  A CTA owns
+// the tiles whose last chunk lies in its range; the CTAs before it that hold
+// earlier chunks of an owned tile leave partial sums (and partial sums of
+// squares of their inputs, for the RMSNorm factor) tagged in global memory,
+// and the owner adds them in K order before its epilogue.  The partition is a
+// function of the shapes and the grid only, so results never depend on data
+// outside the slot.
+//
+// Because a CTA reads only its own chunks of a phase's input, a buffer may be
+// rewritten while a slower CTA still reads an older value.  So before a CTA
+// writes anything in a tensor-core phase (partials or outputs), every CTA of
+// the grid must have finished the previous phase (P.done holds, per phase
+// and CTA, the tag of the phase once finished); every writer of a phase's
+// buffers comes after that point.
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// One warp, all lanes.
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, unsigned ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)), "r"(ncols) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, unsigned ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Shared-memory operand descriptor: K-major rows of 128 bytes with the 128-byte
+// swizzle, groups of 8 rows 1024 bytes apart (the layout a 2-D TMA copy of a
+// 64-wide bf16 box writes with CU_TENSOR_MAP_SWIZZLE_128B).
+__device__ __forceinline__ uint64_t sw128_desc(unsigned saddr)
+{
+    uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+    d |= (uint64_t)1 << 16;                             // leading byte offset (unused with this swizzle)
+    d |= (uint64_t)(1024 >> 4) << 32;                   // stride byte offset
+    d |= (uint64_t)1 << 46;                             // descriptor version
+    d |= (uint64_t)2 << 61;                             // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: bf16 x bf16 -> fp32, A and B K-major, M = 128, N = ncol.
+__device__ __forceinline__ uint32_t mma_idesc(int ncol)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(ncol >> 3) << 17) | ((uint32_t)(MMA_M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
+}
+
+// The barrier completes once every MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar, uint64_t pol)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1, {%2, %3}], [%4], %5;"
+                 ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol) : "memory");
+}
+
+// nc consecutive fp32 columns of this warp's 32 lanes (one lane per thread).
+template <int NC>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[NC]);
+
+template <>
+__device__ __forceinline__ void tmem_ld<4>(uint32_t taddr, float (&v)[4])
+{
+    uint32_t r[4];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = __uint_as_float(r[e]);
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld<8>(uint32_t taddr, float (&v)[8])
+{
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[e]);
+}
+
+template <>
+__device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+                 : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+}
+
+// This CTA's units of an M x K matrix.
+struct MmaPart {
+    int KC, T;
+    int u0, u1;        // units [u0, u1) of T * KC, tile-major
+    int t0, nt;        // first tile touched, tiles touched (0: none)
+    bool last_owned;   // the last tile touched ends inside the range
+};
+
+__device__ __forceinline__ int mma_unit0(long long U, int c, int cnt) { return (int)(U * c / cnt); }
+
+__device__ __forceinline__ MmaPart mma_part(int M, int K, int c, int cnt)
+{
+    MmaPart p;
+    p.KC = (K + MMA_KC - 1) / MMA_KC;
+    p.T = (M + MMA_M - 1) / MMA_M;
+    const long long U = (long long)p.T * p.KC;
+    p.u0 = mma_unit0(U, c, cnt);
+    p.u1 = mma_unit0(U, c + 1, cnt);
+    if (p.u1 > p.u0) {
+        p.t0 = p.u0 / p.KC;
+        const int tl = (p.u1 - 1) / p.KC;
+        p.nt = tl - p.t0 + 1;
+        p.last_owned = p.u1 == (tl + 1) * p.KC;
+    } else {
+        p.t0 = 0;
+        p.nt = 0;
+        p.last_owned = false;
+    }
+    return p;
+}
+
+// Producer warp (one lane), tensor-core instantiation: the weight chunk of every
+// unit of every matrix phase of the launch, in the consumers' order.
+template <typename TW>
+__device__ __forceinline__ void producer_mma(const Params& P, int ph0, int ph1, unsigned starts, const Smem& sm)
+{
+    const uint64_t pol = l2_evict_first();
+    unsigned s = 0;
+    bool ok = true;
+    const int dep_end = P.dep_ph0 + n_groups(starts) * P.dep_ph_stride;
+    const int dep_all = P.dep_ph0 + P.S * P.dep_ph_stride;
+    for (int ph = ph0; ph < ph1 && ok; ++ph) {
+        if (ph == dep_end && dep_end < dep_all) {
+            ph = dep_all - 1;
+            continue;
+        }
+        const TW* W;
+        int M, K, c, cnt;
+        Phase q = P.phases[ph];
+        if (!resolve(P, starts, q, c, cnt)) continue;
+        if (!phase_matrix<TW>(P, q, W, M, K)) continue;
+        const CUtensorMap* map = P.tmaps + tmap_index(q.type, q.l, q.j, P.L, P.dL);
+        const MmaPart mp = mma_part(M, K, c, cnt);
+        for (int u = mp.u0; u < mp.u1; ++u, ++s) {
+            const int slot = (int)(s % MMA_NSTAGE);
+            if (!mbar_wait(&sm.sempty[slot], ((s / MMA_NSTAGE) & 1u) ^ 1u, P.err, WS_EMPTY)) { ok = false; break; }
+            mbar_expect_tx(&sm.wfull[slot], MMA_W_BYTES);
+            tma_load_2d(sm.mring + (size_t)slot * MMA_STAGE, map, (u % mp.KC) * MMA_KC, (u / mp.KC) * MMA_M,
+                        &sm.wfull[slot], pol);
+        }
+    }
+    if (!ok) {
+        // the consumers stopped early: wait (bounded) until every issued copy has landed
+        for (unsigned k = s > MMA_NSTAGE ? s - MMA_NSTAGE : 0; k < s; ++k) {
+            uint64_t* b = &sm.wfull[k % MMA_NSTAGE];
+            const unsigned long long t0 = globaltimer_ns();
+            while (!mbar_try(b, (k / MMA_NSTAGE) & 1u))
+                if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
+        }
+    }
+}
+
+// MMA warp (one lane): per unit, wait for the weight and activation chunks,
+// issue the MMAs into the tile's accumulator slot, release the stage; when a
+// tile's last chunk of the range is in, signal its slot.  Before the first
+// unit of each matrix phase after the first, wait until the consumers have
+// read the previous phase's accumulators.
+template <typename TW>
+__device__ __forceinline__ void mma_issuer(const Params& P, int ph0, int ph1, int n, unsigned starts, const Smem& sm,
+                                           uint32_t tbase)
+{
+    const int ncol = 2 * mma_nbp(n);
+    const uint32_t idesc = mma_idesc(ncol);
+    unsigned s = 0, frees = 0;
+    bool first = true, ok = true;
+    const int dep_end = P.dep_ph0 + n_groups(starts) * P.dep_ph_stride;
+    const int dep_all = P.dep_ph0 + P.S * P.dep_ph_stride;
+    for (int ph = ph0; ph < ph1 && ok; ++ph) {
+        if (ph == dep_end && dep_end < dep_all) {
+            ph = dep_all - 1;
+            continue;
+        }
+        const TW* W;
+        int M, K, c, cnt;
+        Phase q = P.phases[ph];
+        if (!resolve(P, starts, q, c, cnt)) continue;
+        if (!phase_matrix<TW>(P, q, W, M, K)) continue;
+        if (!first) {
+            if (!mbar_wait(sm.accfree, frees & 1u, P.err, WS_FULL)) { ok = false; break; }
+            ++frees;
+        }
+        first = false;
+        const MmaPart mp = mma_part(M, K, c, cnt);
+        for (int u = mp.u0; u < mp.u1; ++u, ++s) {
+            const int slot = (int)(s % MMA_NSTAGE);
+            const unsigned par = (s / MMA_NSTAGE) & 1u;
+            if (!mbar_wait(&sm.wfull[slot], par, P.err, WS_FULL) || !mbar_wait(&sm.bfull[slot], par, P.err, WS_FULL)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int t = u / mp.KC, j = t - mp.t0;
+            const uint32_t d = tbase + (uint32_t)(j * ncol);
+            const unsigned sa = smem_u32(sm.mring + (size_t)slot * MMA_STAGE);
+            const uint64_t ad = sw128_desc(sa), bd = sw128_desc(sa + MMA_W_BYTES);
+            const int ufirst = max(mp.u0, t * mp.KC);
+#pragma unroll
+            for (int kk = 0; kk < MMA_KC / 16; ++kk)
+                mma_bf16(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, (u != ufirst || kk > 0) ? 1u : 0u);
+            mma_commit(&sm.sempty[slot]);
+            if (u == mp.u1 - 1 || (u + 1) % mp.KC == 0) mma_commit(&sm.accf[j]);
+        }
+    }
+    // every MMA issued has completed before tensor memory is freed
+    mma_commit(sm.mdone);
+    const unsigned long long t0 = globaltimer_ns();
+    while (!mbar_try(sm.mdone, 0u))
+        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
+}
+
+// Every CTA of the grid has finished phase ph (one warp polls, then the CTA meets).
+__device__ __forceinline__ bool wait_phase_done(const Params& P, int ph)
+{
+    const unsigned tag = phase_tag(P.desc, ph);
+    int ok = 1;
+    if ((threadIdx.x >> 5) == 0) {
+        for (int k = threadIdx.x; k < P.G && ok; k += 32) {
+            Spin sp;
+            for (;;) {
+                unsigned v;
+                asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(P.done + (size_t)ph * P.G + k) : "memory");
+                if (v == tag) break;
+                if (!sp.ok(P.err, WS_TAG1, tag, v)) { ok = 0; break; }
+            }
+        }
+        __threadfence();
+    }
+    return csync_and(ok);
+}
+
+__device__ __forceinline__ void mark_phase_done(const Params& P, int ph)
+{
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned tag = phase_tag(P.desc, ph);
+        asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(P.done + (size_t)ph * P.G + blockIdx.x), "r"(tag) : "memory");
+    }
+}
+
+// Per-thread state of the consumers across tensor-core phases.
+struct MmaState {
+    uint32_t tbase;
+    unsigned accpar;  // bit j: parity of the next completion of accumulator slot j
+    int ph0;          // first phase of the launch
+};
+
+// This warp's accumulator values of tile slot j: rows 32 (warp % 4) + lane,
+// batch rows [h * nbp / 2, (h + 1) * nbp / 2) with h = warp / 4 (high + low halves).
+template <int NC>
+__device__ __forceinline__ void mma_read_tile(uint32_t tbase, int j, int nbp, float (&y)[16])
+{
+    const int warp = threadIdx.x >> 5;
+    const uint32_t base = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(j * 2 * nbp) + (uint32_t)((warp >> 2) * NC);
+    float hi[NC], lo[NC];
+    tmem_ld<NC>(base, hi);
+    tmem_ld<NC>(base + (uint32_t)nbp, lo);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) y[e] = e < NC ? hi[e] + lo[e] : 0.f;
+}
+
+__device__ __forceinline__ void mma_read(uint32_t tbase, int j, int nbp, float (&y)[16])
+{
+    if (nbp == 8) mma_read_tile<4>(tbase, j, nbp, y);
+    else if (nbp == 16) mma_read_tile<8>(tbase, j, nbp, y);
+    else mma_read_tile<16>(tbase, j, nbp, y);
+}
+
+// Consumers of one tensor-core matrix phase: stage the activation chunks of
+// the CTA's units, then the partial of the tile it does not own, then, per
+// owned tile, the sum over the tile's contributors in K order, the RMSNorm
+// factor, and the epilogue.
+template <typename TW, class Epi>
+__device__ __forceinline__ bool mma_phase(const Params& P, const Phase& ph, int phi, int c, int cnt, const XSrc& xs, int n,
+                                          const Smem& sm, unsigned& stage, MmaState& ms, Epi epi)
+{
+    const TW* W;
+    int M, K;
+    phase_matrix<TW>(P, ph, W, M, K);
+    const MmaPart mp = mma_part(M, K, c, cnt);
+    const int nbp = mma_nbp(n);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cta0 = (int)blockIdx.x - c;  // first CTA of the set sharing this matrix
+    const unsigned tag = phase_tag(P.desc, phi);
+    const int par = phi & 1;
+    int ok = 1;
+    // depformer layer 0: the input token of every batch row (all CTAs take the same)
+    if (xs.add) {
+        for (int b0 = 0; b0 < n; b0 += NWARP)
+            if (!dep_select_inputs(P, xs, b0, min(NWARP, n - b0), sm, b0)) return false;
+    }
+    // activation chunks: thread (b, c16) writes 8 consecutive K of batch row b,
+    // high half in operand row b, low half in operand row nbp + b
+    const int b = tid >> 3, c16 = tid & 7;
+    const bool active = b < n;
+    float ssq = 0.f;
+    int cur = -1;
+    for (int u = mp.u0; u < mp.u1; ++u, ++stage) {
+        const int slot = (int)(stage % MMA_NSTAGE);
+        const int t = u / mp.KC, kc = u % mp.KC;
+        if (t != cur) {
+            if (cur >= 0) {  // flush the sums of squares of the previous tile part
+                float q = ssq;
+                q += __shfl_xor_sync(0xffffffffu, q, 1);
+                q += __shfl_xor_sync(0xffffffffu, q, 2);
+                q += __shfl_xor_sync(0xffffffffu, q, 4);
+                if (active && c16 == 0) sm.pssq[(cur - mp.t0) * 32 + b] = q;
+            }
+            cur = t;
+            ssq = 0.f;
+        }
+        if (lane == 0 && !mbar_wait(&sm.sempty[slot], ((stage / MMA_NSTAGE) & 1u) ^ 1u, P.err, WS_EMPTY)) ok = 0;
+        if (!__all_sync(0xffffffffu, ok)) break;
+        const int k0 = kc * MMA_KC + c16 * 8;
+        if (active) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = 0.f;
+            if (k0 < K) {
+                uint2 pend[8];
+                tag8_issue(xs.base + (size_t)b * xs.stride + k0, pend);
+                if (!tag8_take(pend, xs.base + (size_t)b * xs.stride + k0, xs.tag, f, P.err)) ok = 0;
+                if (xs.add) {
+                    float e8[8];
+                    WV<TW>::cvt(WV<TW>::load((const TW*)xs.add + (size_t)sm.prev[b] * (size_t)xs.add_stride + k0), e8);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] += e8[e];
+                    if (xs.store && t == 0) {
+                        uint2* dst = xs.store + (size_t)b * xs.store_stride + k0;
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) st_tag2(dst + e, f[e], f[e + 1], xs.store_tag);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ssq = fmaf(f[e], f[e], ssq);
+                if (xs.g) {
+                    const float4* gs = reinterpret_cast<const float4*>(xs.g + k0);
+                    const float4 g0 = __ldg(gs), g1 = __ldg(gs + 1);
+                    f[0] *= g0.x; f[1] *= g0.y; f[2] *= g0.z; f[3] *= g0.w;
+                    f[4] *= g1.x; f[5] *= g1.y; f[6] *= g1.z; f[7] *= g1.w;
+                }
+            }
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(f[e], f[e + 1]);
+                const float2 hf = __bfloat1622float2(h);
+                const __nv_bfloat162 l = __floats2bfloat162_rn(f[e] - hf.x, f[e + 1] - hf.y);
+                hi[e / 2] = *reinterpret_cast<const uint32_t*>(&h);
+                lo[e / 2] = *reinterpret_cast<const uint32_t*>(&l);
+            }
+            char* bs = sm.mring + (size_t)slot * MMA_STAGE + MMA_W_BYTES;
+            const int rh = b, rl = nbp + b;
+            *reinterpret_cast<uint4*>(bs + (rh >> 3) * 1024 + (rh & 7) * 128 + ((c16 ^ (rh & 7)) << 4)) =
+                make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(bs + (rl >> 3) * 1024 + (rl & 7) * 128 + ((c16 ^ (rl & 7)) << 4)) =
+                make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.bfull[slot]);
+    }
+    if (cur >= 0) {
+        float q = ssq;
+        q += __shfl_xor_sync(0xffffffffu, q, 1);
+        q += __shfl_xor_sync(0xffffffffu, q, 2);
+        q += __shfl_xor_sync(0xffffffffu, q, 4);
+        if (active && c16 == 0) sm.pssq[(cur - mp.t0) * 32 + b] = q;
+    }
+    if (!csync_and(ok)) return false;
+    // nothing is written before every CTA has finished the previous phase
+    if (phi - 1 >= ms.ph0 && !wait_phase_done(P, phi - 1)) return false;
+    const int row = 32 * (warp & 3) + lane;  // this thread's tile row
+    const int bh = (warp >> 2) * (nbp / 2);  // and its first batch row
+    // the partial of the tile this CTA does not own
+    if (mp.nt > 0 && !mp.last_owned) {
+        const int j = mp.nt - 1;
+        if (!mbar_wait(&sm.accf[j], (ms.accpar >> j) & 1u, P.err, WS_FULL)) ok = 0;
+        ms.accpar ^= 1u << j;
+        if (!csync_and(ok)) return false;
+        tc_fence_after();
+        float y[16];
+        mma_read(ms.tbase, j, nbp, y);
+        uint2* dst = P.mpart + (((size_t)par * P.G + blockIdx.x) * MMA_M + row) * 32;
+        for (int e = 0; e < nbp / 2; ++e)
+            if (bh + e < n) st_tag1(dst + bh + e, __float_as_uint(y[e]), tag);
+        if (tid < n) st_tag1(P.mssq + ((size_t)par * P.G + blockIdx.x) * 32 + tid, __float_as_uint(sm.pssq[j * 32 + tid]), tag);
+    }
+    // owned tiles
+    const int nown = mp.nt - (mp.last_owned ? 0 : 1);
+    constexpr bool is_logits = std::is_same<Epi, EpiLogits>::value;
+    if constexpr (is_logits) {
+        epi.dv = sm.bestv;
+        epi.di = sm.besti;
+    }
+    if (nown > 0) {
+        if (is_logits && tid < n) {
+            sm.bestv[tid] = -INFINITY;
+            sm.besti[tid] = 0x7fffffff;
+        }
+        for (int j = 0; j < nown && ok; ++j) {
+            const int t = mp.t0 + j;
+            if (!mbar_wait(&sm.accf[j], (ms.accpar >> j) & 1u, P.err, WS_FULL)) ok = 0;
+            ms.accpar ^= 1u << j;
+            if (!csync_and(ok)) return false;
+            tc_fence_after();
+            float y[16], acc[16];
+            mma_read(ms.tbase, j, nbp, y);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+            // contributors: the CTAs before this one whose ranges reach into tile t, in K order
+            const long long U = (long long)mp.T * mp.KC;
+            int cs = c;
+            while (cs > 0 && mma_unit0(U, cs, cnt) > t * mp.KC) --cs;  // cs: the CTA holding the tile's first unit
+            for (int cc = cs; cc < c; ++cc) {
+                if (mma_unit0(U, cc + 1, cnt) <= mma_unit0(U, cc, cnt)) continue;  // empty range
+                const uint2* src = P.mpart + (((size_t)par * P.G + cta0 + cc) * MMA_M + row) * 32;
+                for (int e = 0; e < nbp / 2; ++e) {
+                    if (bh + e >= n) break;
+                    unsigned bits = 0;
+                    if (!wait_tag1(src + bh + e, tag, bits, P.err)) { ok = 0; break; }
+                    acc[e] += __uint_as_float(bits);
+                }
+                if (!ok) break;
+            }
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[e] += y[e];
+            // RMSNorm factor per batch row from the tile's partial sums of squares, same order
+            if (xs.g && tid < n) {
+                float tot = 0.f;
+                for (int cc = cs; cc < c && ok; ++cc) {
+                    if (mma_unit0(U, cc + 1, cnt) <= mma_unit0(U, cc, cnt)) continue;
+                    unsigned bits = 0;
+                    if (!wait_tag1(P.mssq + ((size_t)par * P.G + cta0 + cc) * 32 + tid, tag, bits, P.err)) ok = 0;
+                    tot += __uint_as_float(bits);
+                }
+                tot += sm.pssq[j * 32 + tid];
+                sm.ssq[tid] = rsqrtf(tot / (float)K + P.eps);  // the factor of batch row tid
+            }
+            if (!csync_and(ok)) return false;
+            for (int e = 0; e < nbp / 2; ++e) {
+                const int bb = bh + e;
+                if (bb < n) {
+                    const float f = xs.g ? sm.ssq[bb] : 1.f;
+                    sm.yf[(size_t)row * nbp + bb] = acc[e] * f;
+                }
+            }
+            csync();
+            const int r0 = t * MMA_M, r1 = min(M, r0 + MMA_M);
+            const Pre pre = epi.pre(P, r0, r1, 0, n);
+            if (!csync_and(pre.ok)) return false;
+            if (!csync_and(epi.apply(P, sm, r0, r1, 0, n, nbp, pre))) return false;
+        }
+        if (!ok) return false;
+        if constexpr (is_logits) {
+            csync();
+            epi.flush(P, 0, n);
+        }
+    } else {
+        epi.empty(P, 0, n);
+    }
+    // the accumulators are free for the next phase
+    tc_fence_before();
+    csync();
+    if (tid == 0) mbar_arrive(sm.accfree);
     return true;
 }
 
@@ -1467,6 +2040,10 @@ __device__ __forceinline__ int attn_chunks(int len, int G, int H)
     int c = (len + 63) / 64;
     const int cap = G / H > 1 ? G / H : 1;
     c = c < cap ? c : cap;
+    // long windows: chunks of at most about 384 keys, so that the two items a CTA
+    // prefetches into L2 stay small next to L2 (see prefetch_attn_item)
+    const int clong = (len + 383) / 384;
+    c = c > clong ? c : clong;
     return c < NCHUNK_MAX ? c : NCHUNK_MAX;
 }
 
@@ -1485,6 +2062,26 @@ __device__ __forceinline__ void attn_item(const StepDesc* D, int n, int H, int W
     const int r = item - base;
     h = r / nch;
     c = r % nch;
+}
+
+// L2 prefetch of one attention item's keys and values (one 16-byte aligned run
+// of hd elements per position and tensor), for windows too large for the
+// whole-window prefetch during the QKV phase.
+template <typename TKV>
+__device__ __forceinline__ void prefetch_attn_item(const Params& P, int l, int n, int item, uint64_t pol)
+{
+    const StepDesc* D = P.desc;
+    int i, h, c, nch, len;
+    attn_item(D, n, P.H, P.W, P.G, item, i, h, c, nch, len);
+    const int p = D->pos[i], start = p - len + 1;
+    const int k0 = (int)((long long)len * c / nch), k1 = (int)((long long)len * (c + 1) / nch);
+    const long long base = ((long long)D->slot[i] * P.L + l) * (long long)P.W * P.d + (long long)h * P.hd;
+    const unsigned bytes = (unsigned)(P.hd * sizeof(TKV));
+    for (int j = k0 + (int)threadIdx.x; j < k1; j += NT) {
+        const long long off = base + (long long)((start + j) % P.W) * P.d;
+        prefetch_l2((const TKV*)P.kc + off, bytes, pol);
+        prefetch_l2((const TKV*)P.vc + off, bytes, pol);
+    }
 }
 
 // One CTA per (batch row, head, chunk of the window): its warps split the
@@ -1507,11 +2104,21 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
     const int wstride = hd + 4;
     const size_t pstride = (size_t)hd + 2;  // partial: max, sum, hd outputs
     int total = 0;
+    long long kvrows = 0;
     for (int i = 0; i < n; ++i) {
         const int p = D->pos[i];
         total += attn_chunks(p + 1 < W ? p + 1 : W, P.G, H) * H;
+        kvrows += p + 1 < W ? p : W - 1;
     }
+    // windows larger than the QKV-phase prefetch covers: each CTA pulls its current
+    // and its next item into L2 ahead of the loads
+    const bool big = kvrows * d * (long long)sizeof(TKV) * 2 > (32ll << 20);
+    const uint64_t pol = big ? l2_evict_last() : 0ull;
     for (int item = blockIdx.x; item < total; item += P.G) {
+        if (big) {
+            if (item == (int)blockIdx.x) prefetch_attn_item<TKV>(P, l, n, item, pol);
+            if (item + P.G < total) prefetch_attn_item<TKV>(P, l, n, item + P.G, pol);
+        }
         int i, h, c, nch, len;
         attn_item(D, n, H, W, P.G, item, i, h, c, nch, len);
         const int p = D->pos[i], slot = D->slot[i];
@@ -1833,9 +2440,19 @@ __device__ __forceinline__ bool phase_final(const Params& P, int n, unsigned sta
 
 // ------------------------------------------------------------------ phase dispatch
 
+// A matrix phase: tensor cores in the tensor-core instantiation, CUDA-core
+// matrix-vector passes otherwise.
+template <typename TW, int BG, class Epi>
+__device__ __forceinline__ bool matrix_phase(const Params& P, const Phase& ph, int phi, int c, int cnt, const XSrc& xs,
+                                             int n, const Smem& sm, unsigned& stage, MmaState& ms, const Epi& epi)
+{
+    if constexpr (is_mma(BG)) return mma_phase<TW>(P, ph, phi, c, cnt, xs, n, sm, stage, ms, epi);
+    else return gemv_phase<TW, BG>(P, ph, c, cnt, xs, n, sm, stage, epi);
+}
+
 template <typename TW, typename TKV, int BG>
 __device__ __forceinline__ bool run_phase(const Params& P, Phase ph, int phi, int n, unsigned starts, const Smem& sm,
-                                          unsigned& stage)
+                                          unsigned& stage, MmaState& ms)
 {
     const int d = P.d, F = P.F, dd = P.dd, dF = P.dF, S = P.S;
     const StepDesc* D = P.desc;
@@ -1849,18 +2466,18 @@ __device__ __forceinline__ bool run_phase(const Params& P, Phase ph, int phi, in
         case PH_EMBED: phase_embed<TW>(P, n, tag, sm); return true;
         case PH_QKV:
             prefetch_kv_windows<TKV>(P, ph.l, n);
-            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.x, d, in_tag, P.attn_norm + (size_t)ph.l * d},
-                                      n, sm, stage, EpiQKV<TKV>{ph.l, tag});
+            return matrix_phase<TW, BG>(P, ph, phi, c, cnt, XSrc{P.x, d, in_tag, P.attn_norm + (size_t)ph.l * d},
+                                      n, sm, stage, ms, EpiQKV<TKV>{ph.l, tag});
         case PH_ATTN: return phase_attn<TKV>(P, ph.l, n, in_tag, tag, sm);
         case PH_O:
-            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.o, d, in_tag}, n, sm, stage, EpiResid{P.x, d, res_tag, tag});
+            return matrix_phase<TW, BG>(P, ph, phi, c, cnt, XSrc{P.o, d, in_tag}, n, sm, stage, ms, EpiResid{P.x, d, res_tag, tag});
         case PH_GU:
-            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.x, d, in_tag, P.ffn_norm + (size_t)ph.l * d},
-                                      n, sm, stage, EpiSwiglu{P.s, F, tag});
+            return matrix_phase<TW, BG>(P, ph, phi, c, cnt, XSrc{P.x, d, in_tag, P.ffn_norm + (size_t)ph.l * d},
+                                      n, sm, stage, ms, EpiSwiglu{P.s, F, tag});
         case PH_DOWN:
-            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.s, F, in_tag}, n, sm, stage, EpiResid{P.x, d, res_tag, tag});
+            return matrix_phase<TW, BG>(P, ph, phi, c, cnt, XSrc{P.s, F, in_tag}, n, sm, stage, ms, EpiResid{P.x, d, res_tag, tag});
         case PH_HEAD:
-            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.x, d, in_tag, P.out_norm}, n, sm, stage,
+            return matrix_phase<TW, BG>(P, ph, phi, c, cnt, XSrc{P.x, d, in_tag, P.out_norm}, n, sm, stage, ms,
                                       EpiLogits{P.logits, P.V, P.V, P.yin, (long long)S * dd, tag, P.amax,
                                                 (long long)P.G * 2, (int)blockIdx.x});
         case PH_DQKV: {
@@ -1869,7 +2486,7 @@ __device__ __forceinline__ bool run_phase(const Params& P, Phase ph, int phi, in
             if (ph.l == 0) {
                 // the residual starts as in-projection + embedding of the substep's input token
                 const void* add = j == 0 ? P.dep_emb_text : (const void*)((const TW*)P.dep_emb_audio + (size_t)(j - 1) * P.C * dd);
-                xs = XSrc{P.yin + (size_t)j * dd, us, in_tag, P.dep_attn_norm, add, dd, c == 0 ? P.u + (size_t)j * dd : nullptr,
+                xs = XSrc{P.yin + (size_t)j * dd, us, in_tag, P.dep_attn_norm, add, dd, (c == 0 || is_mma(BG)) ? P.u + (size_t)j * dd : nullptr,
                           tag, us, j, ph.pad0, 0u, 0};
                 if (j == ph.pad0) {
                     if (j == 0) {
@@ -1888,22 +2505,22 @@ __device__ __forceinline__ bool run_phase(const Params& P, Phase ph, int phi, in
             } else {
                 xs = XSrc{P.u + (size_t)j * dd, us, in_tag, P.dep_attn_norm + (size_t)ph.l * dd};
             }
-            return gemv_phase<TW, BG>(P, ph, c, cnt, xs, n, sm, stage, EpiDQKV{ph.l, j, tag});
+            return matrix_phase<TW, BG>(P, ph, phi, c, cnt, xs, n, sm, stage, ms, EpiDQKV{ph.l, j, tag});
         }
         case PH_DATTN: return phase_dattn(P, ph.l, ph.pad0, ph.pad1, starts, n, in_tag, tag, sm);
         case PH_DO:
-            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.dat + (size_t)j * dd, (long long)S * dd, in_tag}, n, sm, stage,
-                                      EpiResid{P.u + (size_t)j * dd, (long long)S * dd, res_tag, tag});
+            return matrix_phase<TW, BG>(P, ph, phi, c, cnt, XSrc{P.dat + (size_t)j * dd, (long long)S * dd, in_tag}, n, sm, stage,
+                                      ms, EpiResid{P.u + (size_t)j * dd, (long long)S * dd, res_tag, tag});
         case PH_DGU:
-            return gemv_phase<TW, BG>(P, ph, c, cnt,
+            return matrix_phase<TW, BG>(P, ph, phi, c, cnt,
                                       XSrc{P.u + (size_t)j * dd, (long long)S * dd, in_tag, P.dep_ffn_norm + (size_t)ph.l * dd},
-                                      n, sm, stage, EpiSwiglu{P.ds + (size_t)j * dF, (long long)S * dF, tag});
+                                      n, sm, stage, ms, EpiSwiglu{P.ds + (size_t)j * dF, (long long)S * dF, tag});
         case PH_DDOWN:
-            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.ds + (size_t)j * dF, (long long)S * dF, in_tag}, n, sm, stage,
-                                      EpiResid{P.u + (size_t)j * dd, (long long)S * dd, res_tag, tag});
+            return matrix_phase<TW, BG>(P, ph, phi, c, cnt, XSrc{P.ds + (size_t)j * dF, (long long)S * dF, in_tag}, n, sm, stage,
+                                      ms, EpiResid{P.u + (size_t)j * dd, (long long)S * dd, res_tag, tag});
         case PH_DHEAD:
-            return gemv_phase<TW, BG>(P, ph, c, cnt, XSrc{P.u + (size_t)j * dd, (long long)S * dd, in_tag, P.dep_out_norm}, n, sm,
-                                      stage, EpiLogits{P.dlogits + (size_t)j * P.C, (long long)S * P.C, P.C, nullptr, 0, tag,
+            return matrix_phase<TW, BG>(P, ph, phi, c, cnt, XSrc{P.u + (size_t)j * dd, (long long)S * dd, in_tag, P.dep_out_norm}, n, sm,
+                                      stage, ms, EpiLogits{P.dlogits + (size_t)j * P.C, (long long)S * P.C, P.C, nullptr, 0, tag,
                                                        P.damax + (size_t)j * P.G * 2, (long long)S * P.G * 2, c});
         case PH_FINAL: return phase_final(P, n, starts, sm);
         default: return true;
@@ -1916,16 +2533,33 @@ __device__ __forceinline__ bool run_phase(const Params& P, Phase ph, int phi, in
 // every CTA must be resident at once (cooperative launch), because CTAs wait
 // for each other's tagged outputs.  maxrows sizes the shared memory.
 template <typename TW, typename TKV, int BG>
-__global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int ph1, int maxrows)
+__global__ void __launch_bounds__(is_mma(BG) ? MMA_THREADS : NT + 32, 1) step_kernel(Params P, int ph0, int ph1, int maxrows)
 {
     extern __shared__ __align__(1024) char smem_raw[];
-    const Smem sm = smem_map(smem_raw, maxrows, BG);
+    // the tensor-core stages need 1024-byte alignment (the host adds the slack)
+    char* abase = (char*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const Smem sm = is_mma(BG) ? smem_map_mma(abase) : smem_map(smem_raw, maxrows, BG);
+    const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int k = 0; k < (int)nstage_for(BG); ++k) {
-            mbar_init(&sm.full[k], 1);
-            mbar_init(&sm.empty[k], NWARP);  // every consumer warp releases every stage
+        if constexpr (is_mma(BG)) {
+            for (int k = 0; k < MMA_NSTAGE; ++k) {
+                mbar_init(&sm.wfull[k], 1);
+                mbar_init(&sm.bfull[k], NWARP);  // every consumer warp writes its part of every activation chunk
+                mbar_init(&sm.sempty[k], 1);
+            }
+            for (int k = 0; k < MMA_MAX_TILES; ++k) mbar_init(&sm.accf[k], 1);
+            mbar_init(sm.accfree, 1);
+            mbar_init(sm.mdone, 1);
+        } else {
+            for (int k = 0; k < (int)nstage_for(BG); ++k) {
+                mbar_init(&sm.full[k], 1);
+                mbar_init(&sm.empty[k], NWARP);  // every consumer warp releases every stage
+            }
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if constexpr (is_mma(BG)) {
+        if (warp == NWARP + 1) tmem_alloc(sm.tslot, MMA_TMEM_COLS);
     }
     const StepDesc* D = P.desc;
     const int n = D->n;
@@ -1964,8 +2598,15 @@ __global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int
         }
     }
     __threadfence();
-    __syncthreads();  // barrier init visible to every thread; all threads agree on `bad`
-    if (bad) return;
+    if constexpr (is_mma(BG)) tc_fence_before();
+    __syncthreads();  // barrier init and the TMEM address visible to every thread; all threads agree on `bad`
+    if constexpr (is_mma(BG)) tc_fence_after();
+    if (bad) {
+        if constexpr (is_mma(BG)) {
+            if (warp == NWARP + 1) tmem_dealloc(*sm.tslot, MMA_TMEM_COLS);
+        }
+        return;
+    }
     unsigned starts = 1u;
     {
         const unsigned known = (unsigned)sm.misc[1], given = (unsigned)sm.misc[2];
@@ -1979,9 +2620,39 @@ __global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int
         const int ngr = jend == 0 ? 0 : __popc(starts & ((1u << jend) - 1u));
         starts |= (unsigned)ngr << 24;
     }
-    if ((threadIdx.x >> 5) == NWARP) {
-        if ((threadIdx.x & 31) == 0) producer<TW, BG>(P, ph0, ph1, n, starts, sm);
+    if (warp == NWARP) {
+        if ((threadIdx.x & 31) == 0) {
+            if constexpr (is_mma(BG)) producer_mma<TW>(P, ph0, ph1, starts, sm);
+            else producer<TW, BG>(P, ph0, ph1, n, starts, sm);
+        }
         return;
+    }
+    MmaState ms;
+    ms.tbase = 0;
+    ms.accpar = 0;
+    ms.ph0 = ph0;
+    if constexpr (is_mma(BG)) {
+        const uint32_t tbase = *sm.tslot;
+        if (warp == NWARP + 1) {
+            if ((threadIdx.x & 31) == 0) mma_issuer<TW>(P, ph0, ph1, n, starts, sm, tbase);
+            __syncwarp();
+            // tensor memory is freed once the consumers have read their last accumulator
+            asm volatile("bar.sync 2, %0;" ::"n"(NT + 32) : "memory");
+            tc_fence_after();
+            tmem_dealloc(tbase, MMA_TMEM_COLS);
+            return;
+        }
+        ms.tbase = tbase;
+        // operand rows of padding batch rows stay zero in every stage
+        const int nbp = mma_nbp(n), npad = nbp - n;
+        for (int it = threadIdx.x; it < MMA_NSTAGE * 2 * npad * 8; it += NT) {
+            const int st = it / (2 * npad * 8), r = (it / 8) % (2 * npad), ch = it % 8;
+            const int row = r < npad ? n + r : nbp + n + (r - npad);
+            *reinterpret_cast<uint4*>(sm.mring + (size_t)st * MMA_STAGE + MMA_W_BYTES + (row >> 3) * 1024 + (row & 7) * 128 + ch * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        csync();
     }
     unsigned stage = 0;
     // depformer phases of groups that do not exist this step are skipped as a block
@@ -1995,10 +2666,18 @@ __global__ void __launch_bounds__(NT + 32, 1) step_kernel(Params P, int ph0, int
         if (threadIdx.x == 0) sm.misc[0] = ph;  // phase index for the in-phase stamps
         stamp(P, ph, 0);
         const Phase phs = P.phases[ph];
-        if (!run_phase<TW, TKV, BG>(P, phs, ph, n, starts, sm, stage)) return;
+        if (!run_phase<TW, TKV, BG>(P, phs, ph, n, starts, sm, stage, ms)) break;
+        if constexpr (is_mma(BG)) {
+            csync();  // every consumer thread of the CTA is done with the phase
+            mark_phase_done(P, ph);
+        }
         stamp(P, ph, 3);
         // diagnostics: the latest end of this phase over all CTAs
         if (P.ptime && threadIdx.x == 0) atomicMax(P.ptime + (size_t)ph * 8 + 6, globaltimer_ns());
+    }
+    if constexpr (is_mma(BG)) {
+        tc_fence_before();
+        asm volatile("bar.arrive 2, %0;" ::"n"(NT + 32) : "memory");
     }
     stamp(P, ph1, 0);
 }

@@ -51,3 +51,33 @@ def check_argmax(gpu_am, ref_logits, what: str) -> int:
     ok = argmax_agrees(np.asarray(gpu_am), np.asarray(ref_logits))
     assert ok.all(), f"{what}: greedy token differs with top-2 margin >= {FLIP_MARGIN} at {np.argwhere(~ok)[:5]}"
     return int((np.asarray(gpu_am) != np.argmax(ref_logits, axis=-1)).sum())
+
+
+def follow_tokens(text, codes, code_argmax) -> np.ndarray:
+    """Follow-mode input for the oracle from one GPU step: the GPU's chosen token per
+    stream, and for a frame before 0 (output -1) the raw argmax its substep chain used."""
+    text = np.asarray(text, np.int32)
+    codes = np.asarray(codes, np.int32)
+    f = np.empty((text.shape[0], 17), np.int32)
+    f[:, 0] = text
+    f[:, 1:] = np.where(codes >= 0, codes, np.asarray(code_argmax, np.int32))
+    return f
+
+
+class Tally:
+    """Frames compared, the worst |gpu - ref| / rms(ref) and the legal flips of a run."""
+
+    def __init__(self, what: str):
+        self.what, self.frames, self.worst, self.flips = what, 0, 0.0, 0
+
+    def step(self, dbg, rows, ref, label: str) -> None:
+        """Check GPU rows `rows` of one step against the oracle's results `ref`."""
+        self.worst = max(self.worst, check_logits(dbg["text_logits"][rows], ref["text_logits"], f"{label} text logits"))
+        self.worst = max(self.worst, check_logits(dbg["dep_logits"][rows], ref["dep_logits"], f"{label} depformer logits"))
+        self.flips += check_argmax(dbg["text_argmax"][rows], ref["text_logits"], f"{label} text argmax")
+        self.flips += check_argmax(dbg["code_argmax"][rows], ref["dep_logits"], f"{label} code argmax")
+        self.frames += len(rows)
+
+    def report(self) -> str:
+        return (f"{self.what}: {self.frames} slot-frames compared, worst |gpu-ref|/rms = {self.worst:.3e} "
+                f"(limit {LOGIT_RTOL}), {self.flips} legal flips")
