@@ -133,11 +133,12 @@ const void* kernel_bf16(int bg) { return bg == 1 ? kernel_bf16_1() : bg == 2 ? k
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Kernel for a step of n slots: matrix-vector passes over groups of 1, 2 or 4
-// slots, or (bf16 weights, n >= 5) one tensor-core pass for all of them.
+// Kernel for a step of n rows: matrix-vector passes over groups of 1, 2 or 4
+// rows, or (bf16 weights, 5 <= n <= 32) one tensor-core pass for all of them
+// (the pass holds at most 32 rows: 64 operand rows of high and low halves).
 static int kernel_index(const mfs_ctx* c, int n)
 {
-    if (n >= 5 && c->kfn[3]) return 3;
+    if (n >= 5 && n <= 32 && c->kfn[3]) return 3;
     return n <= 1 ? 0 : (n == 2 ? 1 : 2);
 }
 static int bg_value(int idx) { return idx == 0 ? 1 : (idx == 1 ? 2 : 4); }
@@ -450,7 +451,8 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
     CK(cudaMalloc((void**)&c->hist, MS * NSTREAM * HIST * sizeof(int)));
     CK(cudaMemset(c->hist, 0xFF, MS * NSTREAM * HIST * sizeof(int)));
 
-    // activations
+    // activations: one row per slot of a step, or per frame of a prompt chunk
+    const size_t AR = MS > (size_t)PROMPT_ROWS ? MS : (size_t)PROMPT_ROWS;
     size_t ao = 0;
     auto areg = [&](size_t bytes) {
         size_t o = ao;
@@ -458,9 +460,10 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
         return o;
     };
     const size_t T8 = sizeof(uint2);  // tagged element
-    const size_t a_x = areg(MS * d * T8), a_q = areg(MS * d * T8), a_kc = areg(MS * d * T8), a_vc = areg(MS * d * T8);
-    const size_t a_o = areg(MS * d * T8), a_s = areg(MS * F * T8);
-    const size_t a_ap = areg(MS * H * NCHUNK_MAX * (hd + 2) * T8);
+    const size_t a_x = areg(AR * d * T8), a_q = areg(AR * d * T8), a_kc = areg(AR * d * T8), a_vc = areg(AR * d * T8);
+    const size_t a_o = areg(AR * d * T8), a_s = areg(AR * F * T8);
+    const size_t a_ap = areg(AR * H * NCHUNK_MAX * (hd + 2) * T8);
+    const size_t a_xt = areg(AR * NSTREAM * T8);
     const size_t a_lg = areg(MS * V * 4), a_yin = areg(MS * S * dd * T8), a_u = areg(MS * S * dd * T8);
     const size_t a_dq = areg(MS * S * dd * T8), a_dkv = areg(MS * dL * S * 2 * dd * T8), a_dat = areg(MS * S * dd * T8);
     const size_t a_ds = areg(MS * S * dF * T8), a_dlg = areg(MS * S * C * 4);
@@ -548,7 +551,7 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
     P.kc = c->kc; P.vc = c->vc; P.hist = c->hist; P.desc = c->d_desc;
     char* A = c->act;
     P.x = (uint2*)(A + a_x); P.q = (uint2*)(A + a_q); P.kcur = (uint2*)(A + a_kc); P.vcur = (uint2*)(A + a_vc);
-    P.o = (uint2*)(A + a_o); P.s = (uint2*)(A + a_s); P.attp = (uint2*)(A + a_ap);
+    P.o = (uint2*)(A + a_o); P.s = (uint2*)(A + a_s); P.attp = (uint2*)(A + a_ap); P.xtok = (uint2*)(A + a_xt);
     P.logits = (float*)(A + a_lg); P.yin = (uint2*)(A + a_yin); P.u = (uint2*)(A + a_u);
     P.dq = (uint2*)(A + a_dq); P.dkv = (uint2*)(A + a_dkv); P.dat = (uint2*)(A + a_dat);
     P.ds = (uint2*)(A + a_ds); P.dlogits = (float*)(A + a_dlg); P.amax = (uint2*)(A + a_am);
@@ -789,6 +792,7 @@ static int fill_desc(mfs_ctx* c, StepDesc* h, int n, const int32_t* slots, const
     h->n = n;
     h->seq = ++c->seq;
     h->sampled = 0;
+    h->prompt_rows = 0;
     for (int i = 0; i < n; ++i) {
         h->slot[i] = slots[i];
         h->pos[i] = c->pos[slots[i]] + frame_off;
@@ -919,18 +923,42 @@ extern "C" int mfs_prefill(mfs_ctx* c, int n, const int32_t* slots, int T, const
     if (T == 0) return MFS_OK;
     if (!codes) return fail(c, MFS_E_ARG, "null codes");
     if ((rc = check_tokens(c, codes, n * T, 0))) return rc;
-    std::vector<int32_t> col((size_t)n * NSTREAM);
-    for (int t0 = 0; t0 < T; t0 += PREF_CHUNK) {
-        const int tn = T - t0 < PREF_CHUNK ? T - t0 : PREF_CHUNK;
+    // Launches of up to PROMPT_ROWS rows: a chunk takes tc consecutive frames of every
+    // slot (rows of a slot consecutive, in frame order) while every position of the
+    // chunk stays below the window, so that no ring row it writes is still read;
+    // otherwise one frame per launch.
+    int maxpos = 0;
+    for (int i = 0; i < n; ++i) maxpos = c->pos[slots[i]] > maxpos ? c->pos[slots[i]] : maxpos;
+    const int tc_max = n <= PROMPT_ROWS ? PROMPT_ROWS / n : 1;
+    std::vector<int> chunk_t0, chunk_tc;
+    for (int t0 = 0; t0 < T;) {
+        int tc = tc_max < T - t0 ? tc_max : T - t0;
+        if (maxpos + t0 + tc > c->cfg.window) tc = 1;
+        chunk_t0.push_back(t0);
+        chunk_tc.push_back(tc);
+        t0 += tc;
+    }
+    for (size_t q0 = 0; q0 < chunk_t0.size(); q0 += PREF_CHUNK) {
+        const size_t qn = chunk_t0.size() - q0 < (size_t)PREF_CHUNK ? chunk_t0.size() - q0 : (size_t)PREF_CHUNK;
         CK(cudaStreamSynchronize(c->stream));  // the pinned staging is reused
-        for (int t = 0; t < tn; ++t) {
+        for (size_t q = 0; q < qn; ++q) {
+            const int t0 = chunk_t0[q0 + q], tc = chunk_tc[q0 + q];
+            StepDesc* h = &c->h_pref[q];
+            h->n = n * tc;
+            h->seq = ++c->seq;
+            h->sampled = 0;
+            h->prompt_rows = tc > 1;
             for (int i = 0; i < n; ++i)
-                memcpy(&col[(size_t)i * NSTREAM], codes + ((size_t)i * T + t0 + t) * NSTREAM, NSTREAM * sizeof(int));
-            fill_desc(c, &c->h_pref[t], n, slots, col.data(), t0 + t);
+                for (int t = 0; t < tc; ++t) {
+                    const int r = i * tc + t;
+                    h->slot[r] = slots[i];
+                    h->pos[r] = c->pos[slots[i]] + t0 + t;
+                    memcpy(h->codes[r], codes + ((size_t)i * T + t0 + t) * NSTREAM, NSTREAM * sizeof(int));
+                }
         }
-        CK(cudaMemcpyAsync(c->d_pref, c->h_pref, tn * sizeof(StepDesc), cudaMemcpyHostToDevice, c->stream));
-        for (int t = 0; t < tn; ++t)
-            if ((rc = launch(c, n, c->nphase_prefill, c->d_pref + t))) return rc;
+        CK(cudaMemcpyAsync(c->d_pref, c->h_pref, qn * sizeof(StepDesc), cudaMemcpyHostToDevice, c->stream));
+        for (size_t q = 0; q < qn; ++q)
+            if ((rc = launch(c, n * chunk_tc[q0 + q], c->nphase_prefill, c->d_pref + q))) return rc;
     }
     CK(cudaMemcpyAsync(c->h_out + MFS_MAX_SLOTS * 17, c->d_err, 2 * sizeof(int), cudaMemcpyDeviceToHost, c->stream));
     CK(cudaStreamSynchronize(c->stream));

@@ -37,24 +37,25 @@ constexpr int NCHUNK_MAX = 32;   // attention split over the window, per (slot, 
 constexpr int HIST = 3;          // frames of token history per stream
 constexpr int MAXGW = 8;         // depformer substeps run together as one group, at most
 
-// Tensor-core weight pass (batches of 5..32 slots, bf16 weights): a matrix is
+// Tensor-core weight pass (batches of 5..32 rows, bf16 weights): a matrix is
 // cut into tiles of MMA_M rows and K-chunks of MMA_KC columns; one stage holds
-// a weight tile chunk (TMA, 128-byte swizzle) and the slots' activations as
-// bf16 high and low halves (up to 64 operand rows).
-constexpr int BG_MMA = 32;                            // instantiation marker: up to 32 slots per weight pass
+// a weight tile chunk (TMA, 128-byte swizzle) and the rows' activations split
+// into three bf16 parts (up to 96 operand rows).
+constexpr int BG_MMA = 32;                            // instantiation marker: up to 32 rows per weight pass
 __host__ __device__ constexpr bool is_mma(int bg) { return bg >= 8; }
 constexpr int MMA_M = 128;
 constexpr int MMA_KC = 64;
+constexpr int MMA_PARTS = 3;                          // bf16 parts of an activation (about 27 significant bits)
 constexpr int MMA_W_BYTES = MMA_M * MMA_KC * 2;       // 16 KB
-constexpr int MMA_B_BYTES = 64 * MMA_KC * 2;          // 8 KB
-constexpr int MMA_STAGE = MMA_W_BYTES + MMA_B_BYTES;  // 24 KB
-constexpr int MMA_NSTAGE = 8;
+constexpr int MMA_B_BYTES = MMA_PARTS * 32 * MMA_KC * 2;  // 12 KB
+constexpr int MMA_STAGE = MMA_W_BYTES + MMA_B_BYTES;  // 28 KB
+constexpr int MMA_NSTAGE = 7;
 constexpr int MMA_HEAD = 3072;                        // barriers and scalars before the stages
 constexpr int MMA_TMEM_COLS = 512;
-constexpr int MMA_MAX_TILES = 8;                      // accumulator slots (tiles a CTA touches in one phase)
+constexpr int MMA_MAX_TILES = 5;                      // accumulator slots (tiles a CTA touches in one phase)
 constexpr int MMA_THREADS = 32 * (8 + 2);             // 8 consumer warps, the producer warp, the MMA warp
-// slots padded to 8, 16 or 32 (two operand rows each: N = 16, 32 or 64)
-__host__ __device__ constexpr int mma_nbp(int n) { return n <= 8 ? 8 : (n <= 16 ? 16 : 32); }
+// rows padded to 16 or 32 (three operand rows each: N = 48 or 96)
+__host__ __device__ constexpr int mma_nbp(int n) { return n <= 16 ? 16 : 32; }
 
 // Weight matrices that have a tensor map (index into Params.tmaps): per
 // temporal layer QKV, O, GU, DOWN; the text head (+ depformer in-projections);
@@ -101,15 +102,20 @@ struct Phase {
     int type, l, j, in_ph, res_ph, am_ph, pad0, pad1;
 };
 
-// Written by the host before each launch.
+// Written by the host before each launch.  A row is one frame of one slot.  In
+// a normal step every row is a different slot.  In a prompt chunk
+// (prompt_rows = 1, temporal phases only, every token supplied) a slot may have
+// several rows, consecutive and in frame order, all at positions below the
+// window (no ring row a later row writes is still in an earlier row's window).
 struct StepDesc {
     int n, seq;
-    int sampled;  // 1: generated tokens of slots with sampling on are drawn with P.unif
-    int pad1;
+    int sampled;      // 1: generated tokens of slots with sampling on are drawn with P.unif
+    int prompt_rows;  // 1: rows may share a slot (prompt chunk)
     int slot[MFS_MAX_SLOTS];
     int pos[MFS_MAX_SLOTS];
     int codes[MFS_MAX_SLOTS][NSTREAM];
 };
+constexpr int PROMPT_ROWS = 32;  // rows of a prompt chunk at most (one tensor-core pass)
 
 enum DeviceError : int { DERR_NONE = 0, DERR_TOKEN = 1, DERR_WAIT = 2 };
 
@@ -149,8 +155,9 @@ struct Params {
     void* vc;                   // [MS][L][W][d] values
     int* hist;                  // [MS][17][3]
     const StepDesc* desc;
-    // activations, row = position in the step's slot list.  Elements that cross
-    // CTAs are tagged 64-bit words {float bits, tag}.
+    // activations, row = position in the step's row list (MS here: max(max_slots,
+    // PROMPT_ROWS) rows).  Elements that cross CTAs are tagged 64-bit words {float bits, tag}.
+    uint2* xtok;     // [MS][17] embedding rows of a prompt chunk, resolved by CTA 0 (tagged)
     uint2* x;        // [MS][d]  residual stream
     uint2* q;        // [MS][d]  rotated queries
     uint2* kcur;     // [MS][d]  this step's rotated keys (rounded to the ring's type)

@@ -1258,6 +1258,33 @@ struct EpiResid {
         return q;
     }
     __device__ void empty(const Params&, int, int) const {}
+    // Tensor-core tiles (up to MMA_M rows x 32 batch rows): every residual of the
+    // thread in flight at once, rows consecutive across threads.
+    __device__ bool apply_all(const Params& P, const Smem& sm, int r0, int r1, int nb, int bgv) const
+    {
+        constexpr int MAXI = MMA_M * 32 / NT;
+        const int rows = r1 - r0, items = rows * nb;
+        uint2 e[MAXI];
+#pragma unroll
+        for (int k = 0; k < MAXI; ++k) {
+            const int it = threadIdx.x + k * NT;
+            e[k] = make_uint2(0u, res_tag);
+            if (it < items) e[k] = ld_tag1(dst + (size_t)(it / rows) * stride + r0 + it % rows);
+        }
+        bool ok = true;
+#pragma unroll
+        for (int k = 0; k < MAXI; ++k) {
+            const int it = threadIdx.x + k * NT;
+            if (it < items) {
+                const int b = it / rows, rl = it % rows;
+                uint2* p = dst + (size_t)b * stride + r0 + rl;
+                unsigned bits = e[k].x;
+                if (e[k].y != res_tag && ok) ok = wait_tag1(p, res_tag, bits, P.err);
+                st_tag1(p, __float_as_uint(__uint_as_float(bits) + sm.yf[(size_t)rl * bgv + b]), tag);
+            }
+        }
+        return ok;
+    }
     __device__ bool apply(const Params& P, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre& q) const
     {
         bool ok = true;
@@ -1325,6 +1352,32 @@ struct EpiLogits {
     __device__ void empty(const Params& P, int b0, int nb) const
     {
         if (threadIdx.x < nb) publish(P, b0 + threadIdx.x, -INFINITY, 0x7fffffff);
+    }
+    // Tensor-core tile (deferred mode): store the tile's logits / extra rows, then
+    // warp w merges the tile's argmax of batch rows w, w + NWARP, ... into dv / di.
+    __device__ bool apply_tile(const Params& P, const Smem& sm, int r0, int r1, int nb, int bgv) const
+    {
+        const int rows = r1 - r0;
+        for (int it = threadIdx.x; it < rows * nb; it += NT) {
+            const int b = it / rows, rl = it % rows, r = r0 + rl;
+            const float y = sm.yf[(size_t)rl * bgv + b];
+            if (r < nlog) lg[(size_t)b * lg_stride + r] = y;
+            else if (extra) st_tag1(extra + (size_t)b * extra_stride + (r - nlog), __float_as_uint(y), tag);
+        }
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        for (int b = warp; b < nb; b += NWARP) {
+            float bv = -INFINITY;
+            int bi = 0x7fffffff;
+            for (int rl = lane; rl < rows; rl += 32) {
+                const int r = r0 + rl;
+                if (r >= nlog) break;
+                const float y = sm.yf[(size_t)rl * bgv + b];
+                if (am_better(y, r, bv, bi)) { bv = y; bi = r; }
+            }
+            warp_argmax(bv, bi);
+            if (lane == 0 && am_better(bv, bi, dv[b], di[b])) { dv[b] = bv; di[b] = bi; }
+        }
+        return true;
     }
     __device__ bool apply(const Params& P, const Smem& sm, int r0, int r1, int b0, int nb, int bgv, const Pre&) const
     {
@@ -1625,7 +1678,7 @@ template <typename TW>
 __device__ __forceinline__ void mma_issuer(const Params& P, int ph0, int ph1, int n, unsigned starts, const Smem& sm,
                                            uint32_t tbase)
 {
-    const int ncol = 2 * mma_nbp(n);
+    const int ncol = MMA_PARTS * mma_nbp(n);
     const uint32_t idesc = mma_idesc(ncol);
     unsigned s = 0, frees = 0;
     bool first = true, ok = true;
@@ -1680,13 +1733,23 @@ __device__ __forceinline__ bool wait_phase_done(const Params& P, int ph)
     const unsigned tag = phase_tag(P.desc, ph);
     int ok = 1;
     if ((threadIdx.x >> 5) == 0) {
-        for (int k = threadIdx.x; k < P.G && ok; k += 32) {
-            Spin sp;
-            for (;;) {
-                unsigned v;
-                asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(P.done + (size_t)ph * P.G + k) : "memory");
-                if (v == tag) break;
-                if (!sp.ok(P.err, WS_TAG1, tag, v)) { ok = 0; break; }
+        const unsigned* flags = P.done + (size_t)ph * P.G;
+        for (int k0 = 0; k0 < P.G && ok; k0 += 32 * 5) {
+            unsigned v[5];  // every flag of the batch in flight at once, then the stragglers
+#pragma unroll
+            for (int q = 0; q < 5; ++q) {
+                const int k = k0 + threadIdx.x + 32 * q;
+                v[q] = tag;
+                if (k < P.G) asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v[q]) : "l"(flags + k) : "memory");
+            }
+#pragma unroll
+            for (int q = 0; q < 5; ++q) {
+                const int k = k0 + threadIdx.x + 32 * q;
+                Spin sp;
+                while (ok && v[q] != tag) {
+                    if (!sp.ok(P.err, WS_TAG1, tag, v[q])) { ok = 0; break; }
+                    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v[q]) : "l"(flags + k) : "memory");
+                }
             }
         }
         __threadfence();
@@ -1711,33 +1774,42 @@ struct MmaState {
 };
 
 // This warp's accumulator values of tile slot j: rows 32 (warp % 4) + lane,
-// batch rows [h * nbp / 2, (h + 1) * nbp / 2) with h = warp / 4 (high + low halves).
+// batch rows [h * nbp / 2, (h + 1) * nbp / 2) with h = warp / 4; the products
+// of the three activation parts are added in part order.
 template <int NC>
 __device__ __forceinline__ void mma_read_tile(uint32_t tbase, int j, int nbp, float (&y)[16])
 {
     const int warp = threadIdx.x >> 5;
-    const uint32_t base = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(j * 2 * nbp) + (uint32_t)((warp >> 2) * NC);
-    float hi[NC], lo[NC];
-    tmem_ld<NC>(base, hi);
-    tmem_ld<NC>(base + (uint32_t)nbp, lo);
+    const uint32_t base = tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(j * MMA_PARTS * nbp) +
+                          (uint32_t)((warp >> 2) * NC);
+    float p0[NC], p1[NC], p2[NC];
+    tmem_ld<NC>(base, p0);
+    tmem_ld<NC>(base + (uint32_t)nbp, p1);
+    tmem_ld<NC>(base + (uint32_t)(2 * nbp), p2);
 #pragma unroll
-    for (int e = 0; e < 16; ++e) y[e] = e < NC ? hi[e] + lo[e] : 0.f;
+    for (int e = 0; e < 16; ++e) y[e] = e < NC ? (p0[e] + p1[e]) + p2[e] : 0.f;
 }
 
 __device__ __forceinline__ void mma_read(uint32_t tbase, int j, int nbp, float (&y)[16])
 {
-    if (nbp == 8) mma_read_tile<4>(tbase, j, nbp, y);
-    else if (nbp == 16) mma_read_tile<8>(tbase, j, nbp, y);
+    if (nbp == 16) mma_read_tile<8>(tbase, j, nbp, y);
     else mma_read_tile<16>(tbase, j, nbp, y);
 }
+
+// One unit's activation loads of one consumer thread, in flight ahead of their use.
+template <typename TW>
+struct ActLoad {
+    uint2 e[8];
+    typename WV<TW>::raw emb;
+};
 
 // Consumers of one tensor-core matrix phase: stage the activation chunks of
 // the CTA's units, then the partial of the tile it does not own, then, per
 // owned tile, the sum over the tile's contributors in K order, the RMSNorm
 // factor, and the epilogue.
 template <typename TW, class Epi>
-__device__ __forceinline__ bool mma_phase(const Params& P, const Phase& ph, int phi, int c, int cnt, const XSrc& xs, int n,
-                                          const Smem& sm, unsigned& stage, MmaState& ms, Epi epi)
+__device__ __noinline__ bool mma_phase(const Params& P, const Phase& ph, int phi, int c, int cnt, const XSrc& xs, int n,
+                                       const Smem& sm, unsigned& stage, MmaState& ms, Epi epi)
 {
     const TW* W;
     int M, K;
@@ -1754,40 +1826,53 @@ __device__ __forceinline__ bool mma_phase(const Params& P, const Phase& ph, int 
         for (int b0 = 0; b0 < n; b0 += NWARP)
             if (!dep_select_inputs(P, xs, b0, min(NWARP, n - b0), sm, b0)) return false;
     }
-    // activation chunks: thread (b, c16) writes 8 consecutive K of batch row b,
-    // high half in operand row b, low half in operand row nbp + b
+    // activation chunks: thread (b, c16) takes 8 consecutive K of batch row b and
+    // writes its three bf16 parts to operand rows b, nbp + b and 2 nbp + b; the
+    // loads of the next PD units are in flight while a unit is converted
     const int b = tid >> 3, c16 = tid & 7;
     const bool active = b < n;
+    const uint2* xrow = xs.base + (size_t)(active ? b : 0) * xs.stride + c16 * 8;
+    const TW* erow = xs.add ? (const TW*)xs.add + (size_t)sm.prev[active ? b : 0] * (size_t)xs.add_stride + c16 * 8 : nullptr;
+    auto issue = [&](int u) {
+        ActLoad<TW> a;
+        if (active && u < mp.u1) {
+            const int k0 = (u % mp.KC) * MMA_KC;
+            if (k0 + c16 * 8 < K) {
+                tag8_issue(xrow + k0, a.e);
+                if (xs.add) a.emb = WV<TW>::load(erow + k0);
+            }
+        }
+        return a;
+    };
     float ssq = 0.f;
     int cur = -1;
-    for (int u = mp.u0; u < mp.u1; ++u, ++stage) {
+    auto flush_ssq = [&]() {
+        float q = ssq;
+        q += __shfl_xor_sync(0xffffffffu, q, 1);
+        q += __shfl_xor_sync(0xffffffffu, q, 2);
+        q += __shfl_xor_sync(0xffffffffu, q, 4);
+        if (active && c16 == 0) sm.pssq[(cur - mp.t0) * 32 + b] = q;
+    };
+    auto convert = [&](int u, const ActLoad<TW> a) {
         const int slot = (int)(stage % MMA_NSTAGE);
         const int t = u / mp.KC, kc = u % mp.KC;
         if (t != cur) {
-            if (cur >= 0) {  // flush the sums of squares of the previous tile part
-                float q = ssq;
-                q += __shfl_xor_sync(0xffffffffu, q, 1);
-                q += __shfl_xor_sync(0xffffffffu, q, 2);
-                q += __shfl_xor_sync(0xffffffffu, q, 4);
-                if (active && c16 == 0) sm.pssq[(cur - mp.t0) * 32 + b] = q;
-            }
+            if (cur >= 0) flush_ssq();
             cur = t;
             ssq = 0.f;
         }
-        if (lane == 0 && !mbar_wait(&sm.sempty[slot], ((stage / MMA_NSTAGE) & 1u) ^ 1u, P.err, WS_EMPTY)) ok = 0;
-        if (!__all_sync(0xffffffffu, ok)) break;
+        if (lane == 0 && ok && !mbar_wait(&sm.sempty[slot], ((stage / MMA_NSTAGE) & 1u) ^ 1u, P.err, WS_EMPTY)) ok = 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
         const int k0 = kc * MMA_KC + c16 * 8;
-        if (active) {
+        if (active && ok) {
             float f[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) f[e] = 0.f;
             if (k0 < K) {
-                uint2 pend[8];
-                tag8_issue(xs.base + (size_t)b * xs.stride + k0, pend);
-                if (!tag8_take(pend, xs.base + (size_t)b * xs.stride + k0, xs.tag, f, P.err)) ok = 0;
+                if (!tag8_take(a.e, xrow + kc * MMA_KC, xs.tag, f, P.err)) ok = 0;
                 if (xs.add) {
                     float e8[8];
-                    WV<TW>::cvt(WV<TW>::load((const TW*)xs.add + (size_t)sm.prev[b] * (size_t)xs.add_stride + k0), e8);
+                    WV<TW>::cvt(a.emb, e8);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) f[e] += e8[e];
                     if (xs.store && t == 0) {
@@ -1805,38 +1890,54 @@ __device__ __forceinline__ bool mma_phase(const Params& P, const Phase& ph, int 
                     f[4] *= g1.x; f[5] *= g1.y; f[6] *= g1.z; f[7] *= g1.w;
                 }
             }
-            uint32_t hi[4], lo[4];
+            // f = p0 + p1 + p2 + r with bf16 parts and |r| <= 2^-27 |f| (each difference is exact in fp32)
+            uint32_t w0[4], w1[4], w2[4];
 #pragma unroll
             for (int e = 0; e < 8; e += 2) {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(f[e], f[e + 1]);
-                const float2 hf = __bfloat1622float2(h);
-                const __nv_bfloat162 l = __floats2bfloat162_rn(f[e] - hf.x, f[e + 1] - hf.y);
-                hi[e / 2] = *reinterpret_cast<const uint32_t*>(&h);
-                lo[e / 2] = *reinterpret_cast<const uint32_t*>(&l);
+                const __nv_bfloat162 h0 = __floats2bfloat162_rn(f[e], f[e + 1]);
+                const float2 g0 = __bfloat1622float2(h0);
+                const float r0 = f[e] - g0.x, r1 = f[e + 1] - g0.y;
+                const __nv_bfloat162 h1 = __floats2bfloat162_rn(r0, r1);
+                const float2 g1 = __bfloat1622float2(h1);
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(r0 - g1.x, r1 - g1.y);
+                w0[e / 2] = *reinterpret_cast<const uint32_t*>(&h0);
+                w1[e / 2] = *reinterpret_cast<const uint32_t*>(&h1);
+                w2[e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
             }
             char* bs = sm.mring + (size_t)slot * MMA_STAGE + MMA_W_BYTES;
-            const int rh = b, rl = nbp + b;
-            *reinterpret_cast<uint4*>(bs + (rh >> 3) * 1024 + (rh & 7) * 128 + ((c16 ^ (rh & 7)) << 4)) =
-                make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(bs + (rl >> 3) * 1024 + (rl & 7) * 128 + ((c16 ^ (rl & 7)) << 4)) =
-                make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            const int ra = b, rb = nbp + b, rc = 2 * nbp + b;
+            *reinterpret_cast<uint4*>(bs + (ra >> 3) * 1024 + (ra & 7) * 128 + ((c16 ^ (ra & 7)) << 4)) =
+                make_uint4(w0[0], w0[1], w0[2], w0[3]);
+            *reinterpret_cast<uint4*>(bs + (rb >> 3) * 1024 + (rb & 7) * 128 + ((c16 ^ (rb & 7)) << 4)) =
+                make_uint4(w1[0], w1[1], w1[2], w1[3]);
+            *reinterpret_cast<uint4*>(bs + (rc >> 3) * 1024 + (rc & 7) * 128 + ((c16 ^ (rc & 7)) << 4)) =
+                make_uint4(w2[0], w2[1], w2[2], w2[3]);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.bfull[slot]);
+        ++stage;
+    };
+    constexpr int PD = 2;
+    ActLoad<TW> pf[PD];
+#pragma unroll
+    for (int q = 0; q < PD; ++q) pf[q] = issue(mp.u0 + q);
+    for (int u = mp.u0; u < mp.u1 && __all_sync(0xffffffffu, ok); u += PD) {
+#pragma unroll
+        for (int q = 0; q < PD; ++q) {
+            if (u + q < mp.u1) {
+                convert(u + q, pf[q]);
+                pf[q] = issue(u + q + PD);
+            }
+        }
     }
-    if (cur >= 0) {
-        float q = ssq;
-        q += __shfl_xor_sync(0xffffffffu, q, 1);
-        q += __shfl_xor_sync(0xffffffffu, q, 2);
-        q += __shfl_xor_sync(0xffffffffu, q, 4);
-        if (active && c16 == 0) sm.pssq[(cur - mp.t0) * 32 + b] = q;
-    }
+    if (cur >= 0) flush_ssq();
     if (!csync_and(ok)) return false;
     // nothing is written before every CTA has finished the previous phase
     if (phi - 1 >= ms.ph0 && !wait_phase_done(P, phi - 1)) return false;
     const int row = 32 * (warp & 3) + lane;  // this thread's tile row
     const int bh = (warp >> 2) * (nbp / 2);  // and its first batch row
+    const int nh = nbp / 2;
     // the partial of the tile this CTA does not own
     if (mp.nt > 0 && !mp.last_owned) {
         const int j = mp.nt - 1;
@@ -1846,9 +1947,10 @@ __device__ __forceinline__ bool mma_phase(const Params& P, const Phase& ph, int 
         tc_fence_after();
         float y[16];
         mma_read(ms.tbase, j, nbp, y);
-        uint2* dst = P.mpart + (((size_t)par * P.G + blockIdx.x) * MMA_M + row) * 32;
-        for (int e = 0; e < nbp / 2; ++e)
-            if (bh + e < n) st_tag1(dst + bh + e, __float_as_uint(y[e]), tag);
+        uint2* dst = P.mpart + (((size_t)par * P.G + blockIdx.x) * MMA_M + row) * 32 + bh;
+#pragma unroll
+        for (int e = 0; e < 16; e += 2)
+            if (e < nh) st_tag2(dst + e, y[e], y[e + 1], tag);
         if (tid < n) st_tag1(P.mssq + ((size_t)par * P.G + blockIdx.x) * 32 + tid, __float_as_uint(sm.pssq[j * 32 + tid]), tag);
     }
     // owned tiles
@@ -1863,6 +1965,7 @@ __device__ __forceinline__ bool mma_phase(const Params& P, const Phase& ph, int 
             sm.bestv[tid] = -INFINITY;
             sm.besti[tid] = 0x7fffffff;
         }
+        const long long U = (long long)mp.T * mp.KC;
         for (int j = 0; j < nown && ok; ++j) {
             const int t = mp.t0 + j;
             if (!mbar_wait(&sm.accf[j], (ms.accpar >> j) & 1u, P.err, WS_FULL)) ok = 0;
@@ -1874,19 +1977,25 @@ __device__ __forceinline__ bool mma_phase(const Params& P, const Phase& ph, int 
 #pragma unroll
             for (int e = 0; e < 16; ++e) acc[e] = 0.f;
             // contributors: the CTAs before this one whose ranges reach into tile t, in K order
-            const long long U = (long long)mp.T * mp.KC;
             int cs = c;
             while (cs > 0 && mma_unit0(U, cs, cnt) > t * mp.KC) --cs;  // cs: the CTA holding the tile's first unit
-            for (int cc = cs; cc < c; ++cc) {
+            for (int cc = cs; cc < c && ok; ++cc) {
                 if (mma_unit0(U, cc + 1, cnt) <= mma_unit0(U, cc, cnt)) continue;  // empty range
-                const uint2* src = P.mpart + (((size_t)par * P.G + cta0 + cc) * MMA_M + row) * 32;
-                for (int e = 0; e < nbp / 2; ++e) {
-                    if (bh + e >= n) break;
-                    unsigned bits = 0;
-                    if (!wait_tag1(src + bh + e, tag, bits, P.err)) { ok = 0; break; }
-                    acc[e] += __uint_as_float(bits);
+                const uint2* src = P.mpart + (((size_t)par * P.G + cta0 + cc) * MMA_M + row) * 32 + bh;
+                uint2 v[16];
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {  // every element in flight at once, then the stragglers
+                    v[e] = v[e + 1] = make_uint2(0u, tag);
+                    if (e < nh) ld_tag2(src + e, v[e], v[e + 1]);
                 }
-                if (!ok) break;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    if (e < nh && bh + e < n) {
+                        unsigned bits = v[e].x;
+                        if (v[e].y != tag && ok) ok = wait_tag1(src + e, tag, bits, P.err);
+                        acc[e] += __uint_as_float(bits);
+                    }
+                }
             }
 #pragma unroll
             for (int e = 0; e < 16; ++e) acc[e] += y[e];
@@ -1903,18 +2012,22 @@ __device__ __forceinline__ bool mma_phase(const Params& P, const Phase& ph, int 
                 sm.ssq[tid] = rsqrtf(tot / (float)K + P.eps);  // the factor of batch row tid
             }
             if (!csync_and(ok)) return false;
-            for (int e = 0; e < nbp / 2; ++e) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
                 const int bb = bh + e;
-                if (bb < n) {
-                    const float f = xs.g ? sm.ssq[bb] : 1.f;
-                    sm.yf[(size_t)row * nbp + bb] = acc[e] * f;
-                }
+                if (e < nh && bb < n) sm.yf[(size_t)row * nbp + bb] = acc[e] * (xs.g ? sm.ssq[bb] : 1.f);
             }
             csync();
             const int r0 = t * MMA_M, r1 = min(M, r0 + MMA_M);
-            const Pre pre = epi.pre(P, r0, r1, 0, n);
-            if (!csync_and(pre.ok)) return false;
-            if (!csync_and(epi.apply(P, sm, r0, r1, 0, n, nbp, pre))) return false;
+            if constexpr (std::is_same<Epi, EpiResid>::value) {
+                if (!csync_and(epi.apply_all(P, sm, r0, r1, n, nbp))) return false;
+            } else if constexpr (is_logits) {
+                if (!csync_and(epi.apply_tile(P, sm, r0, r1, n, nbp))) return false;
+            } else {
+                const Pre pre = epi.pre(P, r0, r1, 0, n);
+                if (!csync_and(pre.ok)) return false;
+                if (!csync_and(epi.apply(P, sm, r0, r1, 0, n, nbp, pre))) return false;
+            }
         }
         if (!ok) return false;
         if constexpr (is_logits) {
@@ -1933,27 +2046,74 @@ __device__ __forceinline__ bool mma_phase(const Params& P, const Phase& ph, int 
 
 // ------------------------------------------------------------------ S0 + S1
 
+// First and last row of row i's slot (rows of a slot are consecutive).
+__device__ __forceinline__ int slot_first_row(const StepDesc* D, int i)
+{
+    while (i > 0 && D->slot[i - 1] == D->slot[i]) --i;
+    return i;
+}
+
+__device__ __forceinline__ int slot_last_row(const StepDesc* D, int n, int i)
+{
+    while (i + 1 < n && D->slot[i + 1] == D->slot[i]) ++i;
+    return i;
+}
+
 template <typename TW>
-__device__ __forceinline__ void phase_embed(const Params& P, int n, unsigned tag, const Smem& sm)
+__device__ __forceinline__ bool phase_embed(const Params& P, int n, unsigned tag, const Smem& sm)
 {
     const StepDesc* D = P.desc;
     const int d = P.d;
-    // embedding rows read by each stream: token of frame p-1-delay[k], or INIT
-    for (int it = threadIdx.x; it < n * NSTREAM; it += NT) {
-        const int i = it / NSTREAM, k = it % NSTREAM;
-        const int f = D->pos[i] - 1 - P.delays[k];
-        const int init = k == 0 ? P.V : P.C;
-        int tok = f < 0 ? init : ld_cg_int(P.hist + ((size_t)D->slot[i] * NSTREAM + k) * HIST + f % HIST);
-        if (tok < 0 || tok > init) tok = init;  // never taken for a consistent history; keeps reads in the table
-        sm.X[it] = tok;
-    }
-    csync();
-    // frame p's tokens into the history (column p mod 3, disjoint from the reads above)
-    if (blockIdx.x == 0) {
+    if (!D->prompt_rows) {
+        // embedding rows read by each stream: token of frame p-1-delay[k], or INIT
         for (int it = threadIdx.x; it < n * NSTREAM; it += NT) {
             const int i = it / NSTREAM, k = it % NSTREAM;
-            P.hist[((size_t)D->slot[i] * NSTREAM + k) * HIST + D->pos[i] % HIST] = D->codes[i][k];
+            const int f = D->pos[i] - 1 - P.delays[k];
+            const int init = k == 0 ? P.V : P.C;
+            int tok = f < 0 ? init : ld_cg_int(P.hist + ((size_t)D->slot[i] * NSTREAM + k) * HIST + f % HIST);
+            if (tok < 0 || tok > init) tok = init;  // never taken for a consistent history; keeps reads in the table
+            sm.X[it] = tok;
         }
+        csync();
+        // frame p's tokens into the history (column p mod 3, disjoint from the reads above)
+        if (blockIdx.x == 0) {
+            for (int it = threadIdx.x; it < n * NSTREAM; it += NT) {
+                const int i = it / NSTREAM, k = it % NSTREAM;
+                P.hist[((size_t)D->slot[i] * NSTREAM + k) * HIST + D->pos[i] % HIST] = D->codes[i][k];
+            }
+        }
+    } else if (blockIdx.x == 0) {
+        // prompt chunk: CTA 0 alone reads the history.  A frame of this chunk comes from
+        // its row's tokens, an earlier one from the history; the rows are published to
+        // the other CTAs, then the last three frames of each slot go into the history
+        // (their columns may hold frames other rows read: CTA 0 read them already).
+        for (int it = threadIdx.x; it < n * NSTREAM; it += NT) {
+            const int i = it / NSTREAM, k = it % NSTREAM;
+            const int f = D->pos[i] - 1 - P.delays[k];
+            const int init = k == 0 ? P.V : P.C;
+            const int r0 = slot_first_row(D, i);
+            int tok;
+            if (f < 0) tok = init;
+            else if (f >= D->pos[r0]) tok = D->codes[i - (D->pos[i] - f)][k];
+            else tok = ld_cg_int(P.hist + ((size_t)D->slot[i] * NSTREAM + k) * HIST + f % HIST);
+            if (tok < 0 || tok > init) tok = init;
+            sm.X[it] = tok;
+        }
+        csync();
+        for (int it = threadIdx.x; it < n * NSTREAM; it += NT) {
+            st_tag1(P.xtok + it, (unsigned)sm.X[it], tag);
+            const int i = it / NSTREAM, k = it % NSTREAM;
+            if (D->pos[i] >= D->pos[slot_last_row(D, n, i)] - (HIST - 1))
+                P.hist[((size_t)D->slot[i] * NSTREAM + k) * HIST + D->pos[i] % HIST] = D->codes[i][k];
+        }
+    } else {
+        int ok = 1;
+        for (int it = threadIdx.x; it < n * NSTREAM; it += NT) {
+            unsigned bits = 0;
+            if (ok) ok = wait_tag1(P.xtok + it, tag, bits, P.err);
+            sm.X[it] = ok ? (int)bits : 0;
+        }
+        if (!csync_and(ok)) return false;
     }
     // x[i] = sum over streams in stream order; rows loaded 6 at a time
     const int per = d / 8;
@@ -1990,6 +2150,7 @@ __device__ __forceinline__ void phase_embed(const Params& P, int n, unsigned tag
         for (int e = 0; e < 8; e += 2) st_tag2(dst + e, acc[e], acc[e + 1], tag);
     }
     csync();
+    return true;
 }
 
 // ------------------------------------------------------------------ S5 attention
@@ -2123,6 +2284,9 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
         attn_item(D, n, H, W, P.G, item, i, h, c, nch, len);
         const int p = D->pos[i], slot = D->slot[i];
         const int start = p - len + 1;
+        // keys of this launch: the last mcur of the window (the current one, and in a prompt
+        // chunk those of the slot's earlier rows), read from the tagged copies
+        const int mcur = p - D->pos[slot_first_row(D, i)] + 1;
         const int k0 = (int)((long long)len * c / nch), k1 = (int)((long long)len * (c + 1) / nch);
         const int j0 = k0 + (int)((long long)(k1 - k0) * warp / NWARP), j1 = k0 + (int)((long long)(k1 - k0) * (warp + 1) / NWARP);
         const long long kvbase = ((long long)slot * P.L + l) * (long long)W * d + h * hd + gl * 8;
@@ -2157,13 +2321,17 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
                 const int j = jj + u * PPI;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) { kf[u][e] = 0.f; vf[u][e] = 0.f; }
-                if (j < j1 && j != len - 1) {
+                if (j < j1 && j < len - mcur) {
                     const long long row = (long long)((start + j) % W) * d;
                     KV<TKV>::load8(P.kc, kvbase + row, kf[u]);
                     KV<TKV>::load8(P.vc, kvbase + row, vf[u]);
                 } else if (j == len - 1) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) { kf[u][e] = kcur[e]; vf[u][e] = vcur[e]; }
+                } else if (j < j1) {
+                    // an earlier frame of this prompt chunk: row i - (len - 1 - j)
+                    const size_t ro = (size_t)(i - (len - 1 - j)) * d + h * hd + gl * 8;
+                    if (ok) ok = wait_tag8(P.kcur + ro, in_tag, kf[u], P.err) && wait_tag8(P.vcur + ro, in_tag, vf[u], P.err);
                 }
             }
 #pragma unroll
@@ -2463,7 +2631,7 @@ __device__ __forceinline__ bool run_phase(const Params& P, Phase ph, int phi, in
     if (!resolve(P, starts, ph, c, cnt)) return true;
     const int j = ph.j;  // depformer: this CTA's substep
     switch (ph.type) {
-        case PH_EMBED: phase_embed<TW>(P, n, tag, sm); return true;
+        case PH_EMBED: return phase_embed<TW>(P, n, tag, sm);
         case PH_QKV:
             prefetch_kv_windows<TKV>(P, ph.l, n);
             return matrix_phase<TW, BG>(P, ph, phi, c, cnt, XSrc{P.x, d, in_tag, P.attn_norm + (size_t)ph.l * d},
@@ -2645,9 +2813,9 @@ __global__ void __launch_bounds__(is_mma(BG) ? MMA_THREADS : NT + 32, 1) step_ke
         ms.tbase = tbase;
         // operand rows of padding batch rows stay zero in every stage
         const int nbp = mma_nbp(n), npad = nbp - n;
-        for (int it = threadIdx.x; it < MMA_NSTAGE * 2 * npad * 8; it += NT) {
-            const int st = it / (2 * npad * 8), r = (it / 8) % (2 * npad), ch = it % 8;
-            const int row = r < npad ? n + r : nbp + n + (r - npad);
+        for (int it = threadIdx.x; it < MMA_NSTAGE * MMA_PARTS * npad * 8; it += NT) {
+            const int st = it / (MMA_PARTS * npad * 8), r = (it / 8) % (MMA_PARTS * npad), ch = it % 8;
+            const int row = (r / npad) * nbp + n + r % npad;
             *reinterpret_cast<uint4*>(sm.mring + (size_t)st * MMA_STAGE + MMA_W_BYTES + (row >> 3) * 1024 + (row & 7) * 128 + ch * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
         }

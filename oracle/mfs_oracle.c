@@ -549,12 +549,16 @@ static void attend(orc* o, orc_slot* s, int l, int p, double* q, double* k, cons
         for (int i = 0; i < d; ++i) Vl[(size_t)row * d + i] = round_bf16(Vl[(size_t)row * d + i]);
     double* Kw = (double*)malloc(sizeof(double) * (size_t)len * (size_t)d);
     double* Vw = (double*)malloc(sizeof(double) * (size_t)len * (size_t)d);
+    /* the window in ascending position; heads are independent (threads only share
+     * the work, each head's sums keep their order) */
+#pragma omp parallel for schedule(static)
     for (int j = 0; j < len; ++j) {
         int pos = start + j;
         int r = c->brute_force ? pos : mod(pos, W);
         memcpy(Kw + (size_t)j * d, Kl + (size_t)r * d, sizeof(double) * (size_t)d);
         memcpy(Vw + (size_t)j * d, Vl + (size_t)r * d, sizeof(double) * (size_t)d);
     }
+#pragma omp parallel for schedule(static)
     for (int hh = 0; hh < H; ++hh)
         orc_attention(q + hh * hd, Kw + hh * hd, Vw + hh * hd, len, hd, d, att + hh * hd);
     free(Kw); free(Vw);

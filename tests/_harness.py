@@ -81,3 +81,20 @@ class Tally:
     def report(self) -> str:
         return (f"{self.what}: {self.frames} slot-frames compared, worst |gpu-ref|/rms = {self.worst:.3e} "
                 f"(limit {LOGIT_RTOL}), {self.flips} legal flips")
+
+
+def nan_stale_rows(state: np.ndarray, shape, pos: int, all_rows: bool = False) -> np.ndarray:
+    """Set to NaN (bf16 0x7FC0) every key/value ring row of a slot state (slot-state
+    layout: 256-byte header, then keys and values [n_layers][W][d] bf16) that the next
+    step at position `pos` must not read: rows of positions never written (pos < W:
+    rows pos .. W-1) or outside the window (pos >= W: the row of position pos - W,
+    which the step overwrites before reading).  all_rows: every row."""
+    s = shape
+    kv = state[256:].view(np.uint16).reshape(2, s.n_layers, s.window, s.d)
+    if all_rows:
+        kv[...] = 0x7FC0
+    elif pos < s.window:
+        kv[:, :, pos:, :] = 0x7FC0
+    else:
+        kv[:, :, pos % s.window, :] = 0x7FC0
+    return state

@@ -83,7 +83,7 @@ def test_full_teacher_forced_wrap(mfs, full_weights):
 
 def test_full_b8_mixed_windows_125_frames(mfs, full_weights):
     """Config 3: B = 8, per-slot ring lengths uniform in [0, 3000] (synthetic states imported
-    into both sides), 125 decode frames for all eight slots in one call (the tensor-core
+    into both sides, NaN in every ring row outside the window), 125 decode frames for all eight slots in one call (the tensor-core
     pass).  The slots with the shortest and the longest window are followed by the oracle
     over all 125 frames.  Isolation: a copy of a sampled slot stepped in another batch of
     eight, beside other slots, gives bit-identical results.  A ninth slot two frames below
@@ -93,7 +93,8 @@ def test_full_b8_mixed_windows_125_frames(mfs, full_weights):
     lens = synth.prefill_lengths(1, 8, 0, 3000)
     states = {}
     for i in range(8):
-        st = synth.slot_state(s, 1, i, int(lens[i]))
+        # ring rows the window never reaches hold NaN: any read of one would show
+        st = H.nan_stale_rows(synth.slot_state(s, 1, i, int(lens[i])), s, int(lens[i]))
         mfs.mfs_import_slot(ctx, i, st)
         if i in (int(np.argmin(lens)), int(np.argmax(lens))):
             states[i] = st

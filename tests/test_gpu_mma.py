@@ -77,6 +77,25 @@ def test_mma_batched_prompt_then_decode(mfs):
     print(tally.report())
 
 
+@pytest.mark.parametrize("n,T", [(1, 40), (3, 21), (16, 5)])
+def test_mma_prompt_chunks(mfs, n, T):
+    """Prompt chunks of up to 32 rows through the tensor-core pass: 1 slot takes 32 frames
+    per launch, 3 slots 10, 16 slots 2 (the last frames of a short prompt run one per
+    launch).  Against the oracle's prompt path, then 6 decode frames followed."""
+    s = tiny_bf16(window=48, max_slots=n)
+    w = synth.make_weights(s, 70 + n, gain_std=0.1)
+    ctx, orc = H.gpu_context(s, w), oracle.Oracle(s, w)
+    pr = synth.forced_frames(s, 70 + n, synth.STREAM_PROMPT, T, n)  # [T, n, 17]
+    mfs.mfs_prefill(ctx, list(range(n)), pr.transpose(1, 0, 2))
+    for slot in range(n):
+        orc.prefill(slot, pr[:, slot])
+        assert mfs.mfs_position(ctx, slot) == T
+    u = synth.user_frames(s, 71 + n, 6, n)
+    tally = H.Tally(f"tensor-core prompt chunks, {n} slots x {T} frames")
+    followed_run(mfs, s, w, u, list(range(n)), ctx, orc, tally, f"prompt {n}x{T}")
+    print(tally.report())
+
+
 def test_mma_slot_isolation_bit_exact(mfs):
     """A slot's outputs and logits are bit-identical whatever the other slots of the
     batch hold (same batch size, other slots with other histories and tokens)."""

@@ -197,6 +197,9 @@ def test_reset_equals_fresh(mfs):
 
 
 def test_prompt_path_equals_forced_steps(mfs):
+    """The prompt path takes the first 16 frames of both slots as one chunk of 32 rows
+    (earlier frames of a slot read from the chunk's own rows), the rest one frame per
+    launch; it equals 30 forced steps bit for bit."""
     s = tiny(window=16)
     w = synth.make_weights(s, 8, gain_std=0.1)
     z = synth.forced_frames(s, 80, synth.STREAM_PROMPT, 30, 2)
