@@ -82,7 +82,7 @@ struct mfs_ctx {
     int threads[4] = {0, 0, 0, 0};
     CUtensorMap* d_tmaps = nullptr;
     int ntmaps = 0;
-    char* mma_buf = nullptr;      // tensor-core pass: partial tile sums, phase completion tags
+    char* mma_buf = nullptr;      // tensor-core pass: partial tile sums, activation panel
     std::vector<int> pos;
     std::map<std::string, TensorInfo> tensors;
     int mode = 0;
@@ -400,14 +400,25 @@ static int setup_tensor_core_pass(mfs_ctx* c)
     CK(cudaMalloc((void**)&c->d_tmaps, maps.size() * sizeof(CUtensorMap)));
     CK(cudaMemcpy(c->d_tmaps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice));
     c->P.tmaps = c->d_tmaps;
-    // partial tile sums and phase completion tags
-    const size_t part = (size_t)2 * c->G * MMA_M * 32 * sizeof(uint2), pssq = (size_t)2 * c->G * 32 * sizeof(uint2);
-    const size_t done = (size_t)c->nphase * c->G * sizeof(unsigned);
-    CK(cudaMalloc((void**)&c->mma_buf, part + pssq + done));
-    CK(cudaMemset(c->mma_buf, 0, part + pssq + done));
+    // partial tile sums, phase completion tags, and the activation panel (chunks
+    // of every matrix input in the operand layout, by phase parity and substep)
+    long long kmax = d > F ? d : F;
+    kmax = kmax > dd ? kmax : dd;
+    kmax = kmax > dF ? kmax : dF;
+    c->P.pchunks = (int)((kmax + MMA_KC - 1) / MMA_KC);
+    if (c->P.pchunks > MAX_PCHUNKS) return MFS_OK;  // (K <= 12288 is checked at create)
+    const size_t nch = (size_t)MMA_ROT * MAXGW * c->P.pchunks;
+    const size_t part = align_up((size_t)MMA_ROT * c->G * MMA_M * 32 * sizeof(uint2), 256);
+    const size_t panel = nch * MMA_B_BYTES, pssq = align_up(nch * 32 * sizeof(uint2), 256), pflag = nch * sizeof(unsigned);
+    const size_t done = align_up((size_t)c->nphase * c->G * sizeof(unsigned), 256);
+    const size_t total = part + panel + pssq + align_up(pflag, 256) + done;
+    CK(cudaMalloc((void**)&c->mma_buf, total));
+    CK(cudaMemset(c->mma_buf, 0, total));
     c->P.mpart = (uint2*)c->mma_buf;
-    c->P.mssq = (uint2*)(c->mma_buf + part);
-    c->P.done = (unsigned*)(c->mma_buf + part + pssq);
+    c->P.panel = c->mma_buf + part;
+    c->P.pssq = (uint2*)(c->mma_buf + part + panel);
+    c->P.pflag = (unsigned*)(c->mma_buf + part + panel + pssq);
+    c->P.done = (unsigned*)(c->mma_buf + part + panel + pssq + align_up(pflag, 256));
     c->kfn[3] = kernel_bf16_mma();
     c->threads[3] = MMA_THREADS;
     c->smem[3] = smem;
@@ -725,16 +736,27 @@ static int launch(mfs_ctx* c, int n, int nph, const StepDesc* desc)
         ev1 = c->ev_pool[c->ev_used + 1];
         c->ev_used += 2;
     }
+    // With the tensor-core pass, the depformer phases (small matrices, one dependent
+    // phase after another) run on the CUDA-core instantiation in groups of 4 rows, as a
+    // second launch: [0, dep_ph0) tensor cores, [dep_ph0, nph) CUDA cores.
+    const int split = (bi == 3 && nph > c->P.dep_ph0) ? c->P.dep_ph0 : nph;
     if (c->mode == 0) {
-        int ph0 = 0, ph1 = nph;
+        int ph0 = 0, ph1 = split;
         void* args[] = {&P, &ph0, &ph1, &maxrows};
         CK(cudaLaunchCooperativeKernel(c->kfn[bi], dim3(c->G), dim3(c->threads[bi]), args, c->smem[bi], c->stream));
         c->launches = 1;
+        if (split < nph) {
+            int q0 = split, q1 = nph;
+            void* args2[] = {&P, &q0, &q1, &maxrows};
+            CK(cudaLaunchCooperativeKernel(c->kfn[2], dim3(c->G), dim3(c->threads[2]), args2, c->smem[2], c->stream));
+            c->launches = 2;
+        }
     } else {
         for (int ph = 0; ph < nph; ++ph) {
+            const int k = ph < split ? bi : 2;
             int ph0 = ph, ph1 = ph + 1;
             void* args[] = {&P, &ph0, &ph1, &maxrows};
-            CK(cudaLaunchKernel(c->kfn[bi], dim3(c->G), dim3(c->threads[bi]), args, c->smem[bi], c->stream));
+            CK(cudaLaunchKernel(c->kfn[k], dim3(c->G), dim3(c->threads[k]), args, c->smem[k], c->stream));
         }
         c->launches = nph;
     }
@@ -989,6 +1011,36 @@ static size_t ring_bytes(const mfs_ctx* c)
     return (size_t)c->cfg.n_layers * c->cfg.window * c->cfg.d * c->kvb;
 }
 
+// A slot's key and value rings between the device layout [L][H][W][hd] and the
+// slot-state layout [L][W][d] (keys, then values) of a host buffer: one
+// contiguous host copy per tensor through a device staging buffer, transposed
+// there by pitched device copies (one per layer and head).  Exactly one of
+// out (export) and in (import) is set.
+static int ring_transfer(mfs_ctx* c, int slot, char* out, const char* in)
+{
+    const size_t L = c->cfg.n_layers, W = c->cfg.window, d = c->cfg.d, H = c->cfg.n_heads, hd = c->cfg.head_dim;
+    const size_t kvb = c->kvb, rb = ring_bytes(c);
+    char* stage = nullptr;
+    CK(cudaMalloc((void**)&stage, rb));
+    int rc = MFS_OK;
+    for (int t = 0; t < 2 && rc == MFS_OK; ++t) {
+        char* ring = (char*)(t == 0 ? c->kc : c->vc) + (size_t)slot * rb;
+        cudaError_t e = cudaSuccess;
+        if (in) e = cudaMemcpy(stage, in + (size_t)t * rb, rb, cudaMemcpyHostToDevice);
+        for (size_t l = 0; l < L && e == cudaSuccess; ++l)
+            for (size_t h = 0; h < H && e == cudaSuccess; ++h) {
+                char* dev = ring + ((l * H + h) * W * hd) * kvb;    // [W][hd], rows hd apart
+                char* flat = stage + (l * W * d + h * hd) * kvb;   // [W] rows of the head, d apart
+                e = in ? cudaMemcpy2D(dev, hd * kvb, flat, d * kvb, hd * kvb, W, cudaMemcpyDeviceToDevice)
+                       : cudaMemcpy2D(flat, d * kvb, dev, hd * kvb, hd * kvb, W, cudaMemcpyDeviceToDevice);
+            }
+        if (e == cudaSuccess && out) e = cudaMemcpy(out + (size_t)t * rb, stage, rb, cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) rc = fail(c, MFS_E_CUDA, "slot state copy: %s", cudaGetErrorString(e));
+    }
+    cudaFree(stage);
+    return rc;
+}
+
 extern "C" size_t mfs_slot_state_bytes(const mfs_ctx* c)
 {
     if (!c) return 0;
@@ -1011,10 +1063,7 @@ extern "C" int mfs_export_slot(mfs_ctx* c, int slot, void* buf, size_t bytes)
     memcpy(out, head, sizeof head);
     CK(cudaMemcpy(out + sizeof head, c->hist + (size_t)slot * NSTREAM * HIST, NSTREAM * HIST * sizeof(int),
                   cudaMemcpyDeviceToHost));
-    const size_t rb = ring_bytes(c);
-    CK(cudaMemcpy(out + MFS_SLOT_HEADER_BYTES, (const char*)c->kc + slot * rb, rb, cudaMemcpyDeviceToHost));
-    CK(cudaMemcpy(out + MFS_SLOT_HEADER_BYTES + rb, (const char*)c->vc + slot * rb, rb, cudaMemcpyDeviceToHost));
-    return MFS_OK;
+    return ring_transfer(c, slot, out + MFS_SLOT_HEADER_BYTES, nullptr);
 }
 
 extern "C" int mfs_import_slot(mfs_ctx* c, int slot, const void* buf, size_t bytes)
@@ -1041,10 +1090,9 @@ extern "C" int mfs_import_slot(mfs_ctx* c, int slot, const void* buf, size_t byt
         if (rc != MFS_OK) return rc;
     }
     CK(cudaStreamSynchronize(c->stream));
-    const size_t rb = ring_bytes(c);
     CK(cudaMemcpy(c->hist + (size_t)slot * NSTREAM * HIST, hist, sizeof hist, cudaMemcpyHostToDevice));
-    CK(cudaMemcpy((char*)c->kc + slot * rb, in + MFS_SLOT_HEADER_BYTES, rb, cudaMemcpyHostToDevice));
-    CK(cudaMemcpy((char*)c->vc + slot * rb, in + MFS_SLOT_HEADER_BYTES + rb, rb, cudaMemcpyHostToDevice));
+    const int rc = ring_transfer(c, slot, nullptr, in + MFS_SLOT_HEADER_BYTES);
+    if (rc != MFS_OK) return rc;
     c->pos[slot] = head[1];
     return MFS_OK;
 }

@@ -54,6 +54,8 @@ constexpr int MMA_HEAD = 3072;                        // barriers and scalars be
 constexpr int MMA_TMEM_COLS = 512;
 constexpr int MMA_MAX_TILES = 5;                      // accumulator slots (tiles a CTA touches in one phase)
 constexpr int MMA_THREADS = 32 * (8 + 2);             // 8 consumer warps, the producer warp, the MMA warp
+constexpr int MMA_ROT = 4;                            // phases a panel / partial buffer serves before its reuse
+constexpr int MAX_PCHUNKS = 192;                      // K-chunks of a matrix input at most (K <= 12288)
 // rows padded to 16 or 32 (three operand rows each: N = 48 or 96)
 __host__ __device__ constexpr int mma_nbp(int n) { return n <= 16 ? 16 : 32; }
 
@@ -151,8 +153,8 @@ struct Params {
     const float* dep_out_norm;  // [dd]
     const float2* rope;         // [max_pos][hd/2] (cos, sin)
     // per-slot state
-    void* kc;                   // [MS][L][W][d] keys (kv dtype)
-    void* vc;                   // [MS][L][W][d] values
+    void* kc;                   // [MS][L][H][W][hd] keys (kv dtype), head-major: a head's window is contiguous
+    void* vc;                   // [MS][L][H][W][hd] values
     int* hist;                  // [MS][17][3]
     const StepDesc* desc;
     // activations, row = position in the step's row list (MS here: max(max_slots,
@@ -192,9 +194,13 @@ struct Params {
     unsigned long long* ptime;  // optional: CTA 0 timer stamps and stage-wait sums, [nphase + 1][8]
     // tensor-core path
     const CUtensorMap* tmaps;   // per weight matrix (tmap_index), bf16 [rows][K], box 64 x 128, 128-byte swizzle
-    unsigned* done;             // [nphase][G] tag of the last phase each CTA finished
-    uint2* mpart;               // [2][G][MMA_M][32] partial tile sums a CTA leaves for a tile's owner (tagged)
-    uint2* mssq;                // [2][G][32] partial sums of squares of the inputs of that tile part (tagged)
+    unsigned* done;             // [nphase][G] tag of a depformer head phase each CTA finished
+    // the next four buffers rotate over MMA_ROT phases (phase index mod MMA_ROT)
+    uint2* mpart;               // [MMA_ROT][G][MMA_M][32] partial tile sums a CTA leaves for a tile's owner (tagged)
+    char* panel;                // [MMA_ROT][MAXGW][pchunks][MMA_B_BYTES] activation chunks in the operand layout (by substep)
+    uint2* pssq;                // [MMA_ROT][MAXGW][pchunks][32] sums of squares of a chunk's inputs per row (tagged)
+    unsigned* pflag;            // [MMA_ROT][MAXGW][pchunks] tag of the phase whose chunk is written
+    int pchunks;                // K-chunks of the widest matrix input
 };
 
 // Kernel entry points, one per (weight dtype, batch group).  Defined in the

@@ -102,6 +102,28 @@ struct KV;
 
 template <>
 struct KV<__nv_bfloat16> {
+    // 8 consecutive elements as loaded (kept packed in registers until used)
+    struct raw { uint4 a; };
+    static __device__ __forceinline__ raw load_raw(const void* base, long long i)
+    {
+        return {ld_cg16((const __nv_bfloat16*)base + i)};
+    }
+    static __device__ __forceinline__ void unpack(const raw& r, float f[8])
+    {
+        f[0] = bf_lo(r.a.x); f[1] = bf_hi(r.a.x); f[2] = bf_lo(r.a.y); f[3] = bf_hi(r.a.y);
+        f[4] = bf_lo(r.a.z); f[5] = bf_hi(r.a.z); f[6] = bf_lo(r.a.w); f[7] = bf_hi(r.a.w);
+    }
+    // values already rounded to bf16 pack exactly
+    static __device__ __forceinline__ raw pack(const float f[8])
+    {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+            const __nv_bfloat162 h = __floats2bfloat162_rn(f[e], f[e + 1]);
+            w[e / 2] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        return {make_uint4(w[0], w[1], w[2], w[3])};
+    }
     static __device__ __forceinline__ float round(float a) { return __bfloat162float(__float2bfloat16_rn(a)); }
     static __device__ __forceinline__ void store2(void* base, long long i, float a, float b)
     {
@@ -117,6 +139,21 @@ struct KV<__nv_bfloat16> {
 
 template <>
 struct KV<float> {
+    struct raw { uint4 a, b; };
+    static __device__ __forceinline__ raw load_raw(const void* base, long long i)
+    {
+        return {ld_cg16((const float*)base + i), ld_cg16((const float*)base + i + 4)};
+    }
+    static __device__ __forceinline__ void unpack(const raw& r, float f[8])
+    {
+        f[0] = __uint_as_float(r.a.x); f[1] = __uint_as_float(r.a.y); f[2] = __uint_as_float(r.a.z); f[3] = __uint_as_float(r.a.w);
+        f[4] = __uint_as_float(r.b.x); f[5] = __uint_as_float(r.b.y); f[6] = __uint_as_float(r.b.z); f[7] = __uint_as_float(r.b.w);
+    }
+    static __device__ __forceinline__ raw pack(const float f[8])
+    {
+        return {make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3])),
+                make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]), __float_as_uint(f[7]))};
+    }
     static __device__ __forceinline__ float round(float a) { return a; }
     static __device__ __forceinline__ void store2(void* base, long long i, float a, float b)
     {
@@ -1224,7 +1261,8 @@ struct EpiQKV {
                 // the ring keeps the key/value for later steps; this step's attention reads
                 // the same (rounded) numbers from the tagged copy
                 const int slot = D->slot[i];
-                const long long idx = (((long long)slot * P.L + l) * P.W + (p % P.W)) * (long long)d + e;
+                // ring [slot][layer][head][position mod W][hd]: a head's window is one contiguous run
+                const long long idx = ((((long long)slot * P.L + l) * P.H + e / hd) * P.W + (p % P.W)) * (long long)hd + e % hd;
                 KV<TKV>::store2(part == 1 ? P.kc : P.vc, idx, y0, y1);
                 st_tag2((part == 1 ? P.kcur : P.vcur) + (size_t)i * d + e, KV<TKV>::round(y0), KV<TKV>::round(y1), tag);
             }
@@ -1476,32 +1514,39 @@ __device__ __forceinline__ bool gemv_phase(const Params& P, const Phase& ph, int
 }
 
 // ------------------------------------------------------------------ tensor-core weight pass
-// Batches of 5..32 slots with bf16 weights: every matrix phase is a product of
-// the weight matrix (A, M rows x K) with the slots' activations (B, N rows x
-// K, N = 2 x slots padded to 8/16/32: each activation is split into a bf16
-// high half and the bf16 rounding of the remainder, so the product keeps
-// about 16 significant bits of the fp32 input and the weights are read once
-// for all slots).  tcgen05.mma accumulates in fp32 in tensor memory.
+// Batches of 5..32 rows with bf16 weights: every matrix phase is a product of
+// the weight matrix (A, M rows x K) with the rows' activations (B, N rows x K,
+// N = 3 x rows padded to 16 or 32: each activation is split into three bf16
+// parts, so the product keeps about 27 significant bits of the fp32 input and
+// the weights are read once for all rows).  tcgen05.mma accumulates in fp32 in
+// tensor memory.
+//
+// Activations: at the start of a phase the CTAs sharing the matrix convert the
+// input's 64-column K-chunks, each chunk once, into a global panel in the
+// operand layout (gain applied, split, 128-byte swizzle), with the chunk's
+// sums of squares per row, and publish a ready tag per chunk.
 //
 // A matrix is cut into units (tile of 128 rows, K-chunk of 64); CTA c of the
 // cnt sharing the matrix takes the contiguous units [U c / cnt, U (c+1) / cnt)
 // in tile-major order.  Per unit the producer warp loads the weight chunk with
-// a 2-D TMA copy (128-byte swizzle), the consumer warps write the activation
-// chunk (their tagged fp32 inputs, gain applied, split) into the stage in the
-// same swizzled layout, and the MMA warp issues 4 MMAs of K = 16.  A CTA owns
-// the tiles whose last chunk lies in its range; the CTAs before it that hold
-// earlier chunks of an owned tile leave partial sums (and partial sums of
-// squares of their inputs, for the RMSNorm factor) tagged in global memory,
-// and the owner adds them in K order before its epilogue.  The partition is a
-// function of the shapes and the grid only, so results never depend on data
-// outside the slot.
+// a 2-D TMA copy (128-byte swizzle) and the activation chunk with a 1-D bulk
+// copy from the panel once its tag is there; the MMA warp issues 4 MMAs of
+// K = 16.  A CTA owns the tiles whose last chunk lies in its range; the CTAs
+// before it that hold earlier chunks of an owned tile leave partial sums
+// tagged in global memory, and the owner adds them in K order, applies the
+// RMSNorm factor from the chunks' sums of squares, and runs the epilogue.  The
+// partition is a function of the shapes and the grid only, so results never
+// depend on data outside the row.
 //
-// Because a CTA reads only its own chunks of a phase's input, a buffer may be
-// rewritten while a slower CTA still reads an older value.  So before a CTA
-// writes anything in a tensor-core phase (partials or outputs), every CTA of
-// the grid must have finished the previous phase (P.done holds, per phase
-// and CTA, the tag of the phase once finished); every writer of a phase's
-// buffers comes after that point.
+// Buffer reuse: every chunk of a phase's input is converted once, and a tile's
+// owner needs all of K, so any output of a phase follows every read of its
+// input; each later writer of a buffer depends on such an output.  The panel
+// and partial buffers rotate over MMA_ROT = 4 phases: a phase's buffers are
+// rewritten four phases later, by which time every unit of the phase has
+// completed (the chain through the phases in between needs every tile of it,
+// attention phases included).  The one phase whose inputs need not depend on
+// the phase before, a depformer group's first layer after another group, first
+// waits until every CTA has finished that group's head (P.done).
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -1628,12 +1673,25 @@ __device__ __forceinline__ MmaPart mma_part(int M, int K, int c, int cnt)
     return p;
 }
 
-// Producer warp (one lane), tensor-core instantiation: the weight chunk of every
-// unit of every matrix phase of the launch, in the consumers' order.
-template <typename TW>
-__device__ __forceinline__ void producer_mma(const Params& P, int ph0, int ph1, unsigned starts, const Smem& sm)
+// Activation chunk kc of substep slot `sub` (0 for temporal phases) in the panel of parity par.
+__device__ __forceinline__ size_t panel_index(const Params& P, int par, int sub, int kc)
 {
-    const uint64_t pol = l2_evict_first();
+    return ((size_t)par * MAXGW + (size_t)sub) * (size_t)P.pchunks + (size_t)kc;
+}
+
+__device__ __forceinline__ int phase_sub(const Phase& q) { return q.type >= PH_DQKV && q.type <= PH_DHEAD ? q.j - q.pad0 : 0; }
+
+// Producer warp (one lane), tensor-core instantiation: for every unit of every
+// matrix phase of the launch, in the consumers' order, the weight chunk (2-D TMA
+// from the tensor map) and the activation chunk (1-D bulk copy from the panel,
+// once the CTA that converts it has published its tag).  Weights run ahead as
+// soon as a stage is free; activation copies follow as their chunks appear.
+template <typename TW>
+__device__ __forceinline__ void producer_mma(const Params& P, int ph0, int ph1, int n, unsigned starts, const Smem& sm)
+{
+    const uint64_t pol_w = l2_evict_first();
+    const uint64_t pol_b = l2_evict_last();  // a chunk serves every CTA whose range holds its K
+    const unsigned bbytes = (unsigned)(MMA_PARTS * mma_nbp(n) * MMA_KC * 2);
     unsigned s = 0;
     bool ok = true;
     const int dep_end = P.dep_ph0 + n_groups(starts) * P.dep_ph_stride;
@@ -1650,20 +1708,68 @@ __device__ __forceinline__ void producer_mma(const Params& P, int ph0, int ph1, 
         if (!phase_matrix<TW>(P, q, W, M, K)) continue;
         const CUtensorMap* map = P.tmaps + tmap_index(q.type, q.l, q.j, P.L, P.dL);
         const MmaPart mp = mma_part(M, K, c, cnt);
-        for (int u = mp.u0; u < mp.u1; ++u, ++s) {
-            const int slot = (int)(s % MMA_NSTAGE);
-            if (!mbar_wait(&sm.sempty[slot], ((s / MMA_NSTAGE) & 1u) ^ 1u, P.err, WS_EMPTY)) { ok = false; break; }
-            mbar_expect_tx(&sm.wfull[slot], MMA_W_BYTES);
-            tma_load_2d(sm.mring + (size_t)slot * MMA_STAGE, map, (u % mp.KC) * MMA_KC, (u / mp.KC) * MMA_M,
-                        &sm.wfull[slot], pol);
+        const size_t pbase = panel_index(P, ph % MMA_ROT, phase_sub(q), 0);
+        const unsigned* flags = P.pflag + pbase;
+        const char* chunks = P.panel + pbase * MMA_B_BYTES;
+        const unsigned tag = phase_tag(P.desc, ph);
+        int w = mp.u0, bq = mp.u0;  // next unit for the weights / for the activations
+        const unsigned s0 = s;
+        unsigned ready[(MAX_PCHUNKS + 31) / 32];  // bit kc: chunk kc seen ready in this phase
+#pragma unroll
+        for (int k = 0; k < (MAX_PCHUNKS + 31) / 32; ++k) ready[k] = 0u;
+        Spin sp;
+        while (bq < mp.u1) {
+            bool progress = false;
+            if (w < mp.u1 && w - bq < MMA_NSTAGE) {
+                const unsigned sw = s0 + (unsigned)(w - mp.u0);
+                const int slot = (int)(sw % MMA_NSTAGE);
+                if (mbar_try(&sm.sempty[slot], ((sw / MMA_NSTAGE) & 1u) ^ 1u)) {
+                    mbar_expect_tx(&sm.wfull[slot], MMA_W_BYTES);
+                    tma_load_2d(sm.mring + (size_t)slot * MMA_STAGE, map, (w % mp.KC) * MMA_KC, (w / mp.KC) * MMA_M,
+                                &sm.wfull[slot], pol_w);
+                    ++w;
+                    progress = true;
+                }
+            }
+            if (bq < w) {
+                const int kc = bq % mp.KC;
+                if (!((ready[kc >> 5] >> (kc & 31)) & 1u)) {
+                    // poll the 32 flags of kc's word at once (one round trip), then acquire
+                    const int k0 = kc & ~31;
+                    unsigned f[32], got = 0u;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        f[e] = 0u;
+                        if (k0 + e < mp.KC)
+                            asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(f[e]) : "l"(flags + k0 + e) : "memory");
+                    }
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) got |= (f[e] == tag ? 1u : 0u) << e;
+                    if (got & ~ready[kc >> 5]) {
+                        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        ready[kc >> 5] |= got;
+                    }
+                }
+                if ((ready[kc >> 5] >> (kc & 31)) & 1u) {
+                    const int slot = (int)((s0 + (unsigned)(bq - mp.u0)) % MMA_NSTAGE);
+                    mbar_expect_tx(&sm.bfull[slot], bbytes);
+                    bulk_g2s(sm.mring + (size_t)slot * MMA_STAGE + MMA_W_BYTES, chunks + (size_t)kc * MMA_B_BYTES, bbytes,
+                             &sm.bfull[slot], pol_b);
+                    ++bq;
+                    progress = true;
+                }
+            }
+            if (!progress && !sp.ok(P.err, WS_EMPTY, tag, 0)) { ok = false; break; }
         }
+        s = s0 + (unsigned)(w - mp.u0);
     }
     if (!ok) {
-        // the consumers stopped early: wait (bounded) until every issued copy has landed
+        // stopped early: wait (bounded) until every issued copy has landed
         for (unsigned k = s > MMA_NSTAGE ? s - MMA_NSTAGE : 0; k < s; ++k) {
-            uint64_t* b = &sm.wfull[k % MMA_NSTAGE];
             const unsigned long long t0 = globaltimer_ns();
-            while (!mbar_try(b, (k / MMA_NSTAGE) & 1u))
+            while (!mbar_try(&sm.wfull[k % MMA_NSTAGE], (k / MMA_NSTAGE) & 1u) ||
+                   !mbar_try(&sm.bfull[k % MMA_NSTAGE], (k / MMA_NSTAGE) & 1u))
                 if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
         }
     }
@@ -1703,9 +1809,14 @@ __device__ __forceinline__ void mma_issuer(const Params& P, int ph0, int ph1, in
         for (int u = mp.u0; u < mp.u1; ++u, ++s) {
             const int slot = (int)(s % MMA_NSTAGE);
             const unsigned par = (s / MMA_NSTAGE) & 1u;
-            if (!mbar_wait(&sm.wfull[slot], par, P.err, WS_FULL) || !mbar_wait(&sm.bfull[slot], par, P.err, WS_FULL)) {
-                ok = false;
-                break;
+            const unsigned long long tw0 = P.ptime ? globaltimer_ns() : 0ull;
+            if (!mbar_wait(&sm.wfull[slot], par, P.err, WS_FULL)) { ok = false; break; }
+            const unsigned long long tw1 = P.ptime ? globaltimer_ns() : 0ull;
+            if (!mbar_wait(&sm.bfull[slot], par, P.err, WS_FULL)) { ok = false; break; }
+            if (P.ptime && blockIdx.x == 0) {
+                // diagnostics: CTA 0's MMA warp waiting for weight chunks, then for activation chunks
+                P.ptime[(size_t)ph * 8 + 4] += tw1 - tw0;
+                P.ptime[(size_t)ph * 8 + 5] += globaltimer_ns() - tw1;
             }
             tc_fence_after();
             const int t = u / mp.KC, j = t - mp.t0;
@@ -1727,7 +1838,7 @@ __device__ __forceinline__ void mma_issuer(const Params& P, int ph0, int ph1, in
         if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) break;
 }
 
-// Every CTA of the grid has finished phase ph (one warp polls, then the CTA meets).
+// Every CTA of the grid has finished phase ph (one warp polls every flag, then the CTA meets).
 __device__ __forceinline__ bool wait_phase_done(const Params& P, int ph)
 {
     const unsigned tag = phase_tag(P.desc, ph);
@@ -1796,12 +1907,7 @@ __device__ __forceinline__ void mma_read(uint32_t tbase, int j, int nbp, float (
     else mma_read_tile<16>(tbase, j, nbp, y);
 }
 
-// One unit's activation loads of one consumer thread, in flight ahead of their use.
-template <typename TW>
-struct ActLoad {
-    uint2 e[8];
-    typename WV<TW>::raw emb;
-};
+
 
 // Consumers of one tensor-core matrix phase: stage the activation chunks of
 // the CTA's units, then the partial of the tile it does not own, then, per
@@ -1819,77 +1925,64 @@ __device__ __noinline__ bool mma_phase(const Params& P, const Phase& ph, int phi
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cta0 = (int)blockIdx.x - c;  // first CTA of the set sharing this matrix
     const unsigned tag = phase_tag(P.desc, phi);
-    const int par = phi & 1;
+    const int par = phi % MMA_ROT;
     int ok = 1;
+    // A group's first depformer layer after another group: its inputs need not depend
+    // on that group's last phases (supplied tokens), so every CTA must have left the
+    // previous group before this phase reuses its rotating buffers.
+    if (ph.type == PH_DQKV && ph.l == 0 && phi - 1 >= ms.ph0 && P.phases[phi - 1].type == PH_DHEAD &&
+        !wait_phase_done(P, phi - 1))
+        return false;
     // depformer layer 0: the input token of every batch row (all CTAs take the same)
     if (xs.add) {
         for (int b0 = 0; b0 < n; b0 += NWARP)
             if (!dep_select_inputs(P, xs, b0, min(NWARP, n - b0), sm, b0)) return false;
     }
-    // activation chunks: thread (b, c16) takes 8 consecutive K of batch row b and
-    // writes its three bf16 parts to operand rows b, nbp + b and 2 nbp + b; the
-    // loads of the next PD units are in flight while a unit is converted
+    // activation chunks of the panel: this CTA converts chunks c, c + cnt, ... of the
+    // phase's input (every CTA that shares the matrix does its share).  Thread
+    // (b, c16) takes 8 consecutive K of batch row b: waits for their tags, adds the
+    // depformer embedding (layer 0), applies the gain, splits each value into
+    // three bf16 parts and writes them to operand rows b, nbp + b and 2 nbp + b in
+    // the swizzled K-major layout; rows of padding batch rows are zero.  Then the
+    // chunk's sums of squares per row, a proxy fence, and the chunk's ready tag.
     const int b = tid >> 3, c16 = tid & 7;
     const bool active = b < n;
-    const uint2* xrow = xs.base + (size_t)(active ? b : 0) * xs.stride + c16 * 8;
-    const TW* erow = xs.add ? (const TW*)xs.add + (size_t)sm.prev[active ? b : 0] * (size_t)xs.add_stride + c16 * 8 : nullptr;
-    auto issue = [&](int u) {
-        ActLoad<TW> a;
-        if (active && u < mp.u1) {
-            const int k0 = (u % mp.KC) * MMA_KC;
-            if (k0 + c16 * 8 < K) {
-                tag8_issue(xrow + k0, a.e);
-                if (xs.add) a.emb = WV<TW>::load(erow + k0);
-            }
-        }
-        return a;
-    };
-    float ssq = 0.f;
-    int cur = -1;
-    auto flush_ssq = [&]() {
-        float q = ssq;
-        q += __shfl_xor_sync(0xffffffffu, q, 1);
-        q += __shfl_xor_sync(0xffffffffu, q, 2);
-        q += __shfl_xor_sync(0xffffffffu, q, 4);
-        if (active && c16 == 0) sm.pssq[(cur - mp.t0) * 32 + b] = q;
-    };
-    auto convert = [&](int u, const ActLoad<TW> a) {
-        const int slot = (int)(stage % MMA_NSTAGE);
-        const int t = u / mp.KC, kc = u % mp.KC;
-        if (t != cur) {
-            if (cur >= 0) flush_ssq();
-            cur = t;
-            ssq = 0.f;
-        }
-        if (lane == 0 && ok && !mbar_wait(&sm.sempty[slot], ((stage / MMA_NSTAGE) & 1u) ^ 1u, P.err, WS_EMPTY)) ok = 0;
-        ok = __shfl_sync(0xffffffffu, ok, 0);
+    const int sub = phase_sub(ph);
+    const size_t pbase = panel_index(P, par, sub, 0);
+    for (int kc = c; kc < mp.KC && ok; kc += cnt) {
         const int k0 = kc * MMA_KC + c16 * 8;
-        if (active && ok) {
-            float f[8];
+        float f[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = 0.f;
-            if (k0 < K) {
-                if (!tag8_take(a.e, xrow + kc * MMA_KC, xs.tag, f, P.err)) ok = 0;
-                if (xs.add) {
-                    float e8[8];
-                    WV<TW>::cvt(a.emb, e8);
+        for (int e = 0; e < 8; ++e) f[e] = 0.f;
+        float q = 0.f;
+        if (active && k0 < K) {
+            const uint2* src = xs.base + (size_t)b * xs.stride + k0;
+            uint2 pend[8];
+            tag8_issue(src, pend);
+            typename WV<TW>::raw er;
+            if (xs.add) er = WV<TW>::load((const TW*)xs.add + (size_t)sm.prev[b] * (size_t)xs.add_stride + k0);
+            if (!tag8_take(pend, src, xs.tag, f, P.err)) ok = 0;
+            if (xs.add) {
+                float e8[8];
+                WV<TW>::cvt(er, e8);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] += e8[e];
-                    if (xs.store && t == 0) {
-                        uint2* dst = xs.store + (size_t)b * xs.store_stride + k0;
+                for (int e = 0; e < 8; ++e) f[e] += e8[e];
+                if (xs.store) {
+                    uint2* dst = xs.store + (size_t)b * xs.store_stride + k0;
 #pragma unroll
-                        for (int e = 0; e < 8; e += 2) st_tag2(dst + e, f[e], f[e + 1], xs.store_tag);
-                    }
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ssq = fmaf(f[e], f[e], ssq);
-                if (xs.g) {
-                    const float4* gs = reinterpret_cast<const float4*>(xs.g + k0);
-                    const float4 g0 = __ldg(gs), g1 = __ldg(gs + 1);
-                    f[0] *= g0.x; f[1] *= g0.y; f[2] *= g0.z; f[3] *= g0.w;
-                    f[4] *= g1.x; f[5] *= g1.y; f[6] *= g1.z; f[7] *= g1.w;
+                    for (int e = 0; e < 8; e += 2) st_tag2(dst + e, f[e], f[e + 1], xs.store_tag);
                 }
             }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) q = fmaf(f[e], f[e], q);
+            if (xs.g) {
+                const float4* gs = reinterpret_cast<const float4*>(xs.g + k0);
+                const float4 g0 = __ldg(gs), g1 = __ldg(gs + 1);
+                f[0] *= g0.x; f[1] *= g0.y; f[2] *= g0.z; f[3] *= g0.w;
+                f[4] *= g1.x; f[5] *= g1.y; f[6] *= g1.z; f[7] *= g1.w;
+            }
+        }
+        if (b < nbp) {
             // f = p0 + p1 + p2 + r with bf16 parts and |r| <= 2^-27 |f| (each difference is exact in fp32)
             uint32_t w0[4], w1[4], w2[4];
 #pragma unroll
@@ -1904,37 +1997,60 @@ __device__ __noinline__ bool mma_phase(const Params& P, const Phase& ph, int phi
                 w1[e / 2] = *reinterpret_cast<const uint32_t*>(&h1);
                 w2[e / 2] = *reinterpret_cast<const uint32_t*>(&h2);
             }
-            char* bs = sm.mring + (size_t)slot * MMA_STAGE + MMA_W_BYTES;
+            char* ch = P.panel + (pbase + (size_t)kc) * MMA_B_BYTES;
             const int ra = b, rb = nbp + b, rc = 2 * nbp + b;
-            *reinterpret_cast<uint4*>(bs + (ra >> 3) * 1024 + (ra & 7) * 128 + ((c16 ^ (ra & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(ch + (ra >> 3) * 1024 + (ra & 7) * 128 + ((c16 ^ (ra & 7)) << 4)) =
                 make_uint4(w0[0], w0[1], w0[2], w0[3]);
-            *reinterpret_cast<uint4*>(bs + (rb >> 3) * 1024 + (rb & 7) * 128 + ((c16 ^ (rb & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(ch + (rb >> 3) * 1024 + (rb & 7) * 128 + ((c16 ^ (rb & 7)) << 4)) =
                 make_uint4(w1[0], w1[1], w1[2], w1[3]);
-            *reinterpret_cast<uint4*>(bs + (rc >> 3) * 1024 + (rc & 7) * 128 + ((c16 ^ (rc & 7)) << 4)) =
+            *reinterpret_cast<uint4*>(ch + (rc >> 3) * 1024 + (rc & 7) * 128 + ((c16 ^ (rc & 7)) << 4)) =
                 make_uint4(w2[0], w2[1], w2[2], w2[3]);
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.bfull[slot]);
-        ++stage;
-    };
-    constexpr int PD = 2;
-    ActLoad<TW> pf[PD];
-#pragma unroll
-    for (int q = 0; q < PD; ++q) pf[q] = issue(mp.u0 + q);
-    for (int u = mp.u0; u < mp.u1 && __all_sync(0xffffffffu, ok); u += PD) {
-#pragma unroll
-        for (int q = 0; q < PD; ++q) {
-            if (u + q < mp.u1) {
-                convert(u + q, pf[q]);
-                pf[q] = issue(u + q + PD);
-            }
+        q += __shfl_xor_sync(0xffffffffu, q, 1);
+        q += __shfl_xor_sync(0xffffffffu, q, 2);
+        q += __shfl_xor_sync(0xffffffffu, q, 4);
+        if (active && c16 == 0) st_tag1(P.pssq + (pbase + (size_t)kc) * 32 + b, __float_as_uint(q), tag);
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // the chunk is read by bulk copies (async proxy)
+        if (!csync_and(ok)) return false;
+        if (tid == 0) {
+            __threadfence();
+            asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(P.pflag + pbase + kc), "r"(tag) : "memory");
         }
     }
-    if (cur >= 0) flush_ssq();
     if (!csync_and(ok)) return false;
-    // nothing is written before every CTA has finished the previous phase
-    if (phi - 1 >= ms.ph0 && !wait_phase_done(P, phi - 1)) return false;
+    if (P.ptime) stamp(P, sm.misc[0], 1);
+    // RMSNorm factor per batch row from the chunks' sums of squares (8 threads per
+    // row take every 8th chunk, then a fixed reduction: the same for every tile)
+    if (xs.g) {
+        float tq = 0.f;
+        if (active) {
+            const uint2* ps = P.pssq + pbase * 32 + b;
+            for (int k0 = c16; k0 < mp.KC && ok; k0 += 64) {
+                uint2 v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int kc = k0 + 8 * e;
+                    v[e] = make_uint2(0u, tag);
+                    if (kc < mp.KC) v[e] = ld_tag1(ps + (size_t)kc * 32);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int kc = k0 + 8 * e;
+                    if (kc < mp.KC) {
+                        unsigned bits = v[e].x;
+                        if (v[e].y != tag && ok) ok = wait_tag1(ps + (size_t)kc * 32, tag, bits, P.err);
+                        tq += __uint_as_float(bits);
+                    }
+                }
+            }
+        }
+        tq += __shfl_xor_sync(0xffffffffu, tq, 1);
+        tq += __shfl_xor_sync(0xffffffffu, tq, 2);
+        tq += __shfl_xor_sync(0xffffffffu, tq, 4);
+        if (active && c16 == 0) sm.ssq[b] = rsqrtf(tq / (float)K + P.eps);
+    }
+    if (!csync_and(ok)) return false;
+    if (P.ptime) stamp(P, sm.misc[0], 2);
     const int row = 32 * (warp & 3) + lane;  // this thread's tile row
     const int bh = (warp >> 2) * (nbp / 2);  // and its first batch row
     const int nh = nbp / 2;
@@ -1947,11 +2063,10 @@ __device__ __noinline__ bool mma_phase(const Params& P, const Phase& ph, int phi
         tc_fence_after();
         float y[16];
         mma_read(ms.tbase, j, nbp, y);
-        uint2* dst = P.mpart + (((size_t)par * P.G + blockIdx.x) * MMA_M + row) * 32 + bh;
+        uint2* dst = P.mpart + (((size_t)par * P.G + blockIdx.x) * MMA_M + row) * 32 + bh;  // par: phase mod MMA_ROT
 #pragma unroll
         for (int e = 0; e < 16; e += 2)
             if (e < nh) st_tag2(dst + e, y[e], y[e + 1], tag);
-        if (tid < n) st_tag1(P.mssq + ((size_t)par * P.G + blockIdx.x) * 32 + tid, __float_as_uint(sm.pssq[j * 32 + tid]), tag);
     }
     // owned tiles
     const int nown = mp.nt - (mp.last_owned ? 0 : 1);
@@ -1999,18 +2114,6 @@ __device__ __noinline__ bool mma_phase(const Params& P, const Phase& ph, int phi
             }
 #pragma unroll
             for (int e = 0; e < 16; ++e) acc[e] += y[e];
-            // RMSNorm factor per batch row from the tile's partial sums of squares, same order
-            if (xs.g && tid < n) {
-                float tot = 0.f;
-                for (int cc = cs; cc < c && ok; ++cc) {
-                    if (mma_unit0(U, cc + 1, cnt) <= mma_unit0(U, cc, cnt)) continue;
-                    unsigned bits = 0;
-                    if (!wait_tag1(P.mssq + ((size_t)par * P.G + cta0 + cc) * 32 + tid, tag, bits, P.err)) ok = 0;
-                    tot += __uint_as_float(bits);
-                }
-                tot += sm.pssq[j * 32 + tid];
-                sm.ssq[tid] = rsqrtf(tot / (float)K + P.eps);  // the factor of batch row tid
-            }
             if (!csync_and(ok)) return false;
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
@@ -2161,34 +2264,45 @@ __device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes, uint6
 }
 
 // While the QKV phase of layer l runs, the older keys/values of every slot's
-// window are pulled into L2, one whole ring row (all heads, d elements) per
-// prefetch, spread evenly over the CTAs of the grid, so that the attention reads
-// hit L2 instead of queueing behind the weight stream.  Only for windows small
-// enough to sit in L2 (at most 32 MB per layer).
+// window are pulled into L2: per (slot, head, tensor) the window is one or two
+// contiguous runs of the head-major ring, prefetched 32 positions at a time and
+// spread evenly over the CTAs of the grid, so that the attention reads hit L2
+// instead of queueing behind the weight stream.  Only for windows small enough
+// to sit in L2 (at most 32 MB per layer).
 template <typename TKV>
 __device__ __forceinline__ void prefetch_kv_windows(const Params& P, int l, int n)
 {
     const StepDesc* D = P.desc;
-    const int d = P.d, W = P.W;
+    const int d = P.d, W = P.W, H = P.H, hd = P.hd;
+    constexpr int PCS = 32;  // positions per prefetch
     long long total = 0;
     for (int i = 0; i < n; ++i) total += (long long)(D->pos[i] + 1 < W ? D->pos[i] : W - 1);
     if (total * d * (long long)sizeof(TKV) * 2 > (32ll << 20)) return;
     const uint64_t pol = l2_evict_last();
-    const unsigned row_bytes = (unsigned)(d * sizeof(TKV));
-    int i = 0, base = 0;
-    // row k goes to CTA k mod G, so that no SM's copy engine queues more than a few rows
-    for (long long k = blockIdx.x + (long long)P.G * threadIdx.x; k < 2 * total; k += (long long)P.G * NT) {
-        const int j = (int)(k >> 1);  // older position j of the concatenated windows
-        int len = D->pos[i] + 1 < W ? D->pos[i] : W - 1;
-        while (j >= base + len) {  // k only grows: walk the slots forward
-            base += len;
-            ++i;
-            len = D->pos[i] + 1 < W ? D->pos[i] : W - 1;
+    // items (slot, head, piece, tensor), slot-major; item k goes to CTA k mod G
+    int i = 0;
+    long long base = 0;
+    auto older = [&](int ii) { return D->pos[ii] + 1 < W ? D->pos[ii] : W - 1; };
+    auto items = [&](int ii) { return (long long)H * ((older(ii) + PCS - 1) / PCS) * 2; };
+    long long cnt = n > 0 ? items(0) : 0;
+    for (long long k = blockIdx.x + (long long)P.G * threadIdx.x;; k += (long long)P.G * NT) {
+        while (i < n && k >= base + cnt) {  // k only grows: walk the slots forward
+            base += cnt;
+            if (++i < n) cnt = items(i);
         }
-        const int p = D->pos[i];
-        const int q = p - len + (j - base);  // absolute position, p - len .. p - 1
-        const long long off = (((long long)D->slot[i] * P.L + l) * (long long)W + q % W) * d;
-        prefetch_l2((const TKV*)((k & 1) ? P.vc : P.kc) + off, row_bytes, pol);
+        if (i >= n) break;
+        const long long r = k - base;
+        const int len = older(i), npc = (len + PCS - 1) / PCS;
+        const int h = (int)((r >> 1) / npc), pc = (int)((r >> 1) % npc);
+        const int q0 = D->pos[i] - len + pc * PCS, c = min(PCS, D->pos[i] - q0);  // positions [q0, q0 + c)
+        const TKV* run = (const TKV*)((r & 1) ? P.vc : P.kc) + (((long long)D->slot[i] * P.L + l) * H + h) * (long long)W * hd;
+        const int r0 = q0 % W;
+        if (r0 + c <= W) {
+            prefetch_l2(run + (long long)r0 * hd, (unsigned)(c * hd * sizeof(TKV)), pol);
+        } else {
+            prefetch_l2(run + (long long)r0 * hd, (unsigned)((W - r0) * hd * sizeof(TKV)), pol);
+            prefetch_l2(run, (unsigned)((r0 + c - W) * hd * sizeof(TKV)), pol);
+        }
     }
 }
 
@@ -2201,48 +2315,36 @@ __device__ __forceinline__ int attn_chunks(int len, int G, int H)
     int c = (len + 63) / 64;
     const int cap = G / H > 1 ? G / H : 1;
     c = c < cap ? c : cap;
-    // long windows: chunks of at most about 384 keys, so that the two items a CTA
-    // prefetches into L2 stay small next to L2 (see prefetch_attn_item)
+    // long windows: chunks of at most about 384 keys (more, shorter items keep
+    // every CTA busy when the windows of many slots are long)
     const int clong = (len + 383) / 384;
     c = c > clong ? c : clong;
     return c < NCHUNK_MAX ? c : NCHUNK_MAX;
 }
 
+// Chunks of a window when one warp takes an item (tensor-core instantiation):
+// about 128 keys each, at most NCHUNK_MAX.  A function of the window only.
+__device__ __forceinline__ int attn_chunks_warp(int len)
+{
+    const int c = (len + 127) / 128;
+    return c < NCHUNK_MAX ? c : NCHUNK_MAX;
+}
+
 // Work items of the step's attention: (batch row i, head h, chunk c), row-major.
 __device__ __forceinline__ void attn_item(const StepDesc* D, int n, int H, int W, int G, int item, int& i, int& h,
-                                          int& c, int& nch, int& len)
+                                          int& c, int& nch, int& len, bool per_warp = false)
 {
     int base = 0;
     for (i = 0; i < n; ++i) {
         const int p = D->pos[i];
         len = p + 1 < W ? p + 1 : W;
-        nch = attn_chunks(len, G, H);
+        nch = per_warp ? attn_chunks_warp(len) : attn_chunks(len, G, H);
         if (item < base + nch * H) break;
         base += nch * H;
     }
     const int r = item - base;
     h = r / nch;
     c = r % nch;
-}
-
-// L2 prefetch of one attention item's keys and values (one 16-byte aligned run
-// of hd elements per position and tensor), for windows too large for the
-// whole-window prefetch during the QKV phase.
-template <typename TKV>
-__device__ __forceinline__ void prefetch_attn_item(const Params& P, int l, int n, int item, uint64_t pol)
-{
-    const StepDesc* D = P.desc;
-    int i, h, c, nch, len;
-    attn_item(D, n, P.H, P.W, P.G, item, i, h, c, nch, len);
-    const int p = D->pos[i], start = p - len + 1;
-    const int k0 = (int)((long long)len * c / nch), k1 = (int)((long long)len * (c + 1) / nch);
-    const long long base = ((long long)D->slot[i] * P.L + l) * (long long)P.W * P.d + (long long)h * P.hd;
-    const unsigned bytes = (unsigned)(P.hd * sizeof(TKV));
-    for (int j = k0 + (int)threadIdx.x; j < k1; j += NT) {
-        const long long off = base + (long long)((start + j) % P.W) * P.d;
-        prefetch_l2((const TKV*)P.kc + off, bytes, pol);
-        prefetch_l2((const TKV*)P.vc + off, bytes, pol);
-    }
 }
 
 // One CTA per (batch row, head, chunk of the window): its warps split the
@@ -2252,6 +2354,102 @@ __device__ __forceinline__ void prefetch_attn_item(const Params& P, int l, int n
 // chunk 0 merges the chunks in order once every CTA has run its chunks (no CTA
 // waits for another's chunk before finishing its own, so the waits end).
 // The newest key/value (this step's) comes from the tagged copy.
+// Keys [j0, j1) of the window of batch row i, head h (len keys from absolute
+// position start; the last mcur of them are this launch's and come from the
+// tagged copies): scores in fp32, an online softmax over groups of PPI x UNR
+// keys, then the warp's key groups merged.  Every lane ends with the running
+// max m, the sum lsum and the unnormalised outputs acc of its 8 elements
+// (lanes gl, gl + LPP, ... hold the same values).  ok turns 0 if a wait gave up.
+template <typename TKV>
+__device__ __forceinline__ void attn_keys(const Params& P, int i, int h, int len, int start, int mcur, int j0, int j1,
+                                          long long kvbase, const float qv[8], const float kcur[8], const float vcur[8],
+                                          unsigned in_tag, int& ok, float& m, float& lsum, float acc[8])
+{
+    const int hd = P.hd, d = P.d, W = P.W;
+    const int lane = threadIdx.x & 31;
+    const int LPP = hd / 8;            // lanes per key
+    const int PPI = 32 / LPP;          // keys per warp iteration
+    const int grp = lane / LPP, gl = lane % LPP;
+    m = -INFINITY;
+    lsum = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    // keys in flight per lane: kept packed until used, so that bf16 rings keep 8
+    constexpr int UNR = sizeof(TKV) == 2 ? 8 : 4;
+    // warp-uniform trip count: every lane runs every iteration (shuffles below)
+    for (int jb = j0; jb < j1; jb += PPI * UNR) {
+        const int jj = jb + grp;
+        typename KV<TKV>::raw kr[UNR], vr[UNR];
+        float s[UNR];
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            const int j = jj + u * PPI;
+            if (j < j1 && j < len - mcur) {
+                const long long row = (long long)((start + j) % W) * hd;
+                kr[u] = KV<TKV>::load_raw(P.kc, kvbase + row);
+                vr[u] = KV<TKV>::load_raw(P.vc, kvbase + row);
+            } else {
+                float kf[8], vf[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { kf[e] = 0.f; vf[e] = 0.f; }
+                if (j == len - 1) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) { kf[e] = kcur[e]; vf[e] = vcur[e]; }
+                } else if (j < j1) {
+                    // an earlier frame of this prompt chunk: row i - (len - 1 - j)
+                    const size_t ro = (size_t)(i - (len - 1 - j)) * d + h * hd + gl * 8;
+                    if (ok) ok = wait_tag8(P.kcur + ro, in_tag, kf, P.err) && wait_tag8(P.vcur + ro, in_tag, vf, P.err);
+                }
+                kr[u] = KV<TKV>::pack(kf);
+                vr[u] = KV<TKV>::pack(vf);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            float kf[8];
+            KV<TKV>::unpack(kr[u], kf);
+            float t = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t = fmaf(qv[e], kf[e], t);
+            for (int o = LPP / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+            s[u] = (jj + u * PPI < j1) ? t : -INFINITY;
+        }
+        float mn = m;
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) mn = fmaxf(mn, s[u]);
+        if (mn == -INFINITY) continue;
+        const float corr = expf(m - mn);
+        lsum *= corr;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] *= corr;
+#pragma unroll
+        for (int u = 0; u < UNR; ++u) {
+            const float pu = expf(s[u] - mn);
+            lsum += pu;
+            float vf[8];
+            KV<TKV>::unpack(vr[u], vf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(pu, vf[e], acc[e]);
+        }
+        m = mn;
+    }
+    // merge the key groups of the warp (same bits on both partners)
+    for (int o = LPP; o < 32; o <<= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float l2 = __shfl_xor_sync(0xffffffffu, lsum, o);
+        float a2[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a2[e] = __shfl_xor_sync(0xffffffffu, acc[e], o);
+        const float M = fmaxf(m, m2);
+        const float c1 = m == -INFINITY ? 0.f : expf(m - M);
+        const float c2 = m2 == -INFINITY ? 0.f : expf(m2 - M);
+        lsum = lsum * c1 + l2 * c2;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = acc[e] * c1 + a2[e] * c2;
+        m = M;
+    }
+}
+
 template <typename TKV>
 __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsigned in_tag, unsigned tag, const Smem& sm)
 {
@@ -2265,21 +2463,11 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
     const int wstride = hd + 4;
     const size_t pstride = (size_t)hd + 2;  // partial: max, sum, hd outputs
     int total = 0;
-    long long kvrows = 0;
     for (int i = 0; i < n; ++i) {
         const int p = D->pos[i];
         total += attn_chunks(p + 1 < W ? p + 1 : W, P.G, H) * H;
-        kvrows += p + 1 < W ? p : W - 1;
     }
-    // windows larger than the QKV-phase prefetch covers: each CTA pulls its current
-    // and its next item into L2 ahead of the loads
-    const bool big = kvrows * d * (long long)sizeof(TKV) * 2 > (32ll << 20);
-    const uint64_t pol = big ? l2_evict_last() : 0ull;
     for (int item = blockIdx.x; item < total; item += P.G) {
-        if (big) {
-            if (item == (int)blockIdx.x) prefetch_attn_item<TKV>(P, l, n, item, pol);
-            if (item + P.G < total) prefetch_attn_item<TKV>(P, l, n, item + P.G, pol);
-        }
         int i, h, c, nch, len;
         attn_item(D, n, H, W, P.G, item, i, h, c, nch, len);
         const int p = D->pos[i], slot = D->slot[i];
@@ -2289,7 +2477,7 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
         const int mcur = p - D->pos[slot_first_row(D, i)] + 1;
         const int k0 = (int)((long long)len * c / nch), k1 = (int)((long long)len * (c + 1) / nch);
         const int j0 = k0 + (int)((long long)(k1 - k0) * warp / NWARP), j1 = k0 + (int)((long long)(k1 - k0) * (warp + 1) / NWARP);
-        const long long kvbase = ((long long)slot * P.L + l) * (long long)W * d + h * hd + gl * 8;
+        const long long kvbase = (((long long)slot * P.L + l) * H + h) * (long long)W * hd + gl * 8;
         // the query and this step's key/value are polled while the first ring loads are in flight
         uint2 qt[8], kt[8], vt[8];
         tag8_issue(P.q + (size_t)i * d + h * hd + gl * 8, qt);
@@ -2308,72 +2496,8 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
 #pragma unroll
         for (int e = 0; e < 8; ++e) qv[e] *= scale;
         if (P.ptime && item == blockIdx.x) stamp(P, sm.misc[0], 1);
-        float m = -INFINITY, lsum = 0.f, acc[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        constexpr int UNR = 4;
-        // warp-uniform trip count: every lane runs every iteration (shuffles below)
-        for (int jb = j0; jb < j1; jb += PPI * UNR) {
-            const int jj = jb + grp;
-            float kf[UNR][8], vf[UNR][8], s[UNR];
-#pragma unroll
-            for (int u = 0; u < UNR; ++u) {
-                const int j = jj + u * PPI;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) { kf[u][e] = 0.f; vf[u][e] = 0.f; }
-                if (j < j1 && j < len - mcur) {
-                    const long long row = (long long)((start + j) % W) * d;
-                    KV<TKV>::load8(P.kc, kvbase + row, kf[u]);
-                    KV<TKV>::load8(P.vc, kvbase + row, vf[u]);
-                } else if (j == len - 1) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) { kf[u][e] = kcur[e]; vf[u][e] = vcur[e]; }
-                } else if (j < j1) {
-                    // an earlier frame of this prompt chunk: row i - (len - 1 - j)
-                    const size_t ro = (size_t)(i - (len - 1 - j)) * d + h * hd + gl * 8;
-                    if (ok) ok = wait_tag8(P.kcur + ro, in_tag, kf[u], P.err) && wait_tag8(P.vcur + ro, in_tag, vf[u], P.err);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < UNR; ++u) {
-                float t = 0.f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) t = fmaf(qv[e], kf[u][e], t);
-                for (int o = LPP / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-                s[u] = (jj + u * PPI < j1) ? t : -INFINITY;
-            }
-            float mn = m;
-#pragma unroll
-            for (int u = 0; u < UNR; ++u) mn = fmaxf(mn, s[u]);
-            if (mn == -INFINITY) continue;
-            const float corr = expf(m - mn);
-            lsum *= corr;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] *= corr;
-#pragma unroll
-            for (int u = 0; u < UNR; ++u) {
-                const float pu = expf(s[u] - mn);
-                lsum += pu;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = fmaf(pu, vf[u][e], acc[e]);
-            }
-            m = mn;
-        }
-        // merge the key groups of the warp (same bits on both partners)
-        for (int o = LPP; o < 32; o <<= 1) {
-            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-            const float l2 = __shfl_xor_sync(0xffffffffu, lsum, o);
-            float a2[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) a2[e] = __shfl_xor_sync(0xffffffffu, acc[e], o);
-            const float M = fmaxf(m, m2);
-            const float c1 = m == -INFINITY ? 0.f : expf(m - M);
-            const float c2 = m2 == -INFINITY ? 0.f : expf(m2 - M);
-            lsum = lsum * c1 + l2 * c2;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = acc[e] * c1 + a2[e] * c2;
-            m = M;
-        }
+        float m, lsum, acc[8];
+        attn_keys<TKV>(P, i, h, len, start, mcur, j0, j1, kvbase, qv, kcur, vcur, in_tag, ok, m, lsum, acc);
         if (P.ptime && item == blockIdx.x) stamp(P, sm.misc[0], 2);
         float* wb = sm.wbuf + (size_t)warp * wstride;
         if (lane < LPP) {
@@ -2449,6 +2573,114 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
         csync();
     }
     return true;
+}
+
+// Attention of the tensor-core instantiation (many rows): one warp per item
+// (batch row, head, chunk of about 128 keys), with no block barrier, so a
+// CTA's eight warps keep eight items' loads in flight.  A window of one chunk
+// writes the output directly; otherwise each chunk leaves {max, sum,
+// unnormalised output} tagged in P.attp and the warp that ran chunk 0 merges
+// the chunks in order once it has run all of its own items (no warp waits for
+// another's chunk before finishing its own, so the waits end).
+template <typename TKV>
+__device__ __noinline__ bool phase_attn_warp(const Params& P, int l, int n, unsigned in_tag, unsigned tag)
+{
+    const StepDesc* D = P.desc;
+    const int H = P.H, hd = P.hd, d = P.d, W = P.W;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int LPP = hd / 8, gl = lane % LPP;
+    const float scale = rsqrtf((float)hd);
+    const size_t pstride = (size_t)hd + 2;  // partial: max, sum, hd outputs
+    const int gw = (int)blockIdx.x * NWARP + warp, GW = P.G * NWARP;
+    int total = 0;
+    for (int i = 0; i < n; ++i) {
+        const int p = D->pos[i];
+        total += attn_chunks_warp(p + 1 < W ? p + 1 : W) * H;
+    }
+    int ok = 1;
+    for (int item = gw; item < total && ok; item += GW) {
+        int i, h, c, nch, len;
+        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, true);
+        const int p = D->pos[i], slot = D->slot[i];
+        const int start = p - len + 1;
+        const int mcur = p - D->pos[slot_first_row(D, i)] + 1;
+        const int k0 = (int)((long long)len * c / nch), k1 = (int)((long long)len * (c + 1) / nch);
+        const long long kvbase = (((long long)slot * P.L + l) * H + h) * (long long)W * hd + gl * 8;
+        const size_t qo = (size_t)i * d + h * hd + gl * 8;
+        uint2 qt[8], kt[8], vt[8];
+        tag8_issue(P.q + qo, qt);
+        const bool has_cur = len - 1 >= k0 && len - 1 < k1;
+        if (has_cur) {
+            tag8_issue(P.kcur + qo, kt);
+            tag8_issue(P.vcur + qo, vt);
+        }
+        float qv[8], kcur[8], vcur[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { kcur[e] = 0.f; vcur[e] = 0.f; }
+        ok = tag8_take(qt, P.q + qo, in_tag, qv, P.err);
+        if (has_cur && ok) ok = tag8_take(kt, P.kcur + qo, in_tag, kcur, P.err) && tag8_take(vt, P.vcur + qo, in_tag, vcur, P.err);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qv[e] *= scale;
+        float m, lsum, acc[8];
+        attn_keys<TKV>(P, i, h, len, start, mcur, k0, k1, kvbase, qv, kcur, vcur, in_tag, ok, m, lsum, acc);
+        ok = __all_sync(0xffffffffu, ok);
+        if (lane < LPP) {
+            if (nch == 1) {
+                uint2* o = P.o + qo;
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) st_tag2(o + e, acc[e] / lsum, acc[e + 1] / lsum, tag);
+            } else {
+                uint2* part = P.attp + (((size_t)i * H + h) * NCHUNK_MAX + c) * pstride;
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) st_tag2(part + 2 + gl * 8 + e, acc[e], acc[e + 1], tag);
+                if (lane == 0) st_tag2(part, m, lsum, tag);
+            }
+        }
+    }
+    // merges: the warp that ran chunk 0 of a split window combines its chunks in order
+    for (int item = gw; item < total && ok; item += GW) {
+        int i, h, c, nch, len;
+        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, true);
+        if (c != 0 || nch == 1) continue;
+        const uint2* part = P.attp + ((size_t)i * H + h) * NCHUNK_MAX * pstride;
+        // lane takes elements lane, lane + 32, ... of the head; the chunk maxima and sums first
+        float mk = -INFINITY, lk = 0.f;
+        if (lane < nch) {
+            uint2 a, b;
+            ld_tag2(part + (size_t)lane * pstride, a, b);
+            unsigned ab = a.x, bb = b.x;
+            if (a.y != tag) ok = ok && wait_tag1(part + (size_t)lane * pstride, tag, ab, P.err);
+            if (b.y != tag) ok = ok && wait_tag1(part + (size_t)lane * pstride + 1, tag, bb, P.err);
+            mk = __uint_as_float(ab);
+            lk = __uint_as_float(bb);
+        }
+        float M = warp_max(mk);
+        const float f = (lane < nch && mk != -INFINITY) ? expf(mk - M) : 0.f;
+        const float L = warp_sum(lk * f);
+        // lane takes elements lane + 32 q of the head (hd <= 128); per chunk its loads
+        // are in flight together, and the chunks are added in order
+        constexpr int QE = 4;
+        float a[QE];
+#pragma unroll
+        for (int q = 0; q < QE; ++q) a[q] = 0.f;
+        for (int k = 0; k < nch && ok; ++k) {
+            const float fk = __shfl_sync(0xffffffffu, f, k);
+            const uint2* pk = part + (size_t)k * pstride + 2;
+            uint2 v[QE];
+#pragma unroll
+            for (int q = 0; q < QE; ++q) v[q] = lane + 32 * q < hd ? ld_tag1(pk + lane + 32 * q) : make_uint2(0u, tag);
+#pragma unroll
+            for (int q = 0; q < QE; ++q) {
+                unsigned bits = v[q].x;
+                if (lane + 32 * q < hd && v[q].y != tag && ok) ok = wait_tag1(pk + lane + 32 * q, tag, bits, P.err);
+                a[q] += __uint_as_float(bits) * fk;
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < QE; ++q)
+            if (lane + 32 * q < hd) st_tag1(P.o + (size_t)i * d + h * hd + lane + 32 * q, __float_as_uint(a[q] / L), tag);
+    }
+    return csync_and(ok);
 }
 
 // ------------------------------------------------------------------ S9 depformer attention
@@ -2636,7 +2868,9 @@ __device__ __forceinline__ bool run_phase(const Params& P, Phase ph, int phi, in
             prefetch_kv_windows<TKV>(P, ph.l, n);
             return matrix_phase<TW, BG>(P, ph, phi, c, cnt, XSrc{P.x, d, in_tag, P.attn_norm + (size_t)ph.l * d},
                                       n, sm, stage, ms, EpiQKV<TKV>{ph.l, tag});
-        case PH_ATTN: return phase_attn<TKV>(P, ph.l, n, in_tag, tag, sm);
+        case PH_ATTN:
+            if constexpr (is_mma(BG)) return phase_attn_warp<TKV>(P, ph.l, n, in_tag, tag);
+            else return phase_attn<TKV>(P, ph.l, n, in_tag, tag, sm);
         case PH_O:
             return matrix_phase<TW, BG>(P, ph, phi, c, cnt, XSrc{P.o, d, in_tag}, n, sm, stage, ms, EpiResid{P.x, d, res_tag, tag});
         case PH_GU:
@@ -2712,7 +2946,7 @@ __global__ void __launch_bounds__(is_mma(BG) ? MMA_THREADS : NT + 32, 1) step_ke
         if constexpr (is_mma(BG)) {
             for (int k = 0; k < MMA_NSTAGE; ++k) {
                 mbar_init(&sm.wfull[k], 1);
-                mbar_init(&sm.bfull[k], NWARP);  // every consumer warp writes its part of every activation chunk
+                mbar_init(&sm.bfull[k], 1);      // the producer's bulk copy of the activation chunk
                 mbar_init(&sm.sempty[k], 1);
             }
             for (int k = 0; k < MMA_MAX_TILES; ++k) mbar_init(&sm.accf[k], 1);
@@ -2790,7 +3024,7 @@ __global__ void __launch_bounds__(is_mma(BG) ? MMA_THREADS : NT + 32, 1) step_ke
     }
     if (warp == NWARP) {
         if ((threadIdx.x & 31) == 0) {
-            if constexpr (is_mma(BG)) producer_mma<TW>(P, ph0, ph1, starts, sm);
+            if constexpr (is_mma(BG)) producer_mma<TW>(P, ph0, ph1, n, starts, sm);
             else producer<TW, BG>(P, ph0, ph1, n, starts, sm);
         }
         return;
@@ -2811,16 +3045,6 @@ __global__ void __launch_bounds__(is_mma(BG) ? MMA_THREADS : NT + 32, 1) step_ke
             return;
         }
         ms.tbase = tbase;
-        // operand rows of padding batch rows stay zero in every stage
-        const int nbp = mma_nbp(n), npad = nbp - n;
-        for (int it = threadIdx.x; it < MMA_NSTAGE * MMA_PARTS * npad * 8; it += NT) {
-            const int st = it / (MMA_PARTS * npad * 8), r = (it / 8) % (MMA_PARTS * npad), ch = it % 8;
-            const int row = (r / npad) * nbp + n + r % npad;
-            *reinterpret_cast<uint4*>(sm.mring + (size_t)st * MMA_STAGE + MMA_W_BYTES + (row >> 3) * 1024 + (row & 7) * 128 + ch * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        csync();
     }
     unsigned stage = 0;
     // depformer phases of groups that do not exist this step are skipped as a block
@@ -2836,8 +3060,10 @@ __global__ void __launch_bounds__(is_mma(BG) ? MMA_THREADS : NT + 32, 1) step_ke
         const Phase phs = P.phases[ph];
         if (!run_phase<TW, TKV, BG>(P, phs, ph, n, starts, sm, stage, ms)) break;
         if constexpr (is_mma(BG)) {
-            csync();  // every consumer thread of the CTA is done with the phase
-            mark_phase_done(P, ph);
+            if (phs.type == PH_DHEAD) {  // the next group's first phase waits for every CTA to get here
+                csync();
+                mark_phase_done(P, ph);
+            }
         }
         stamp(P, ph, 3);
         // diagnostics: the latest end of this phase over all CTAs
