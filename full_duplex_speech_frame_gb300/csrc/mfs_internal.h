@@ -52,7 +52,8 @@ constexpr int MMA_STAGE = MMA_W_BYTES + MMA_B_BYTES;  // 28 KB
 constexpr int MMA_NSTAGE = 7;
 constexpr int MMA_HEAD = 3072;                        // barriers and scalars before the stages
 constexpr int MMA_TMEM_COLS = 512;
-constexpr int MMA_MAX_TILES = 5;                      // accumulator slots (tiles a CTA touches in one phase)
+constexpr int MMA_MAX_TILES = 5;                      // tile sums a CTA keeps (tiles it touches in one phase)
+constexpr int MMA_URING = 3;                          // tensor-memory slots of per-unit products (a ring)
 constexpr int MMA_THREADS = 32 * (8 + 2);             // 8 consumer warps, the producer warp, the MMA warp
 constexpr int MMA_ROT = 4;                            // phases a panel / partial buffer serves before its reuse
 constexpr int MAX_PCHUNKS = 192;                      // K-chunks of a matrix input at most (K <= 12288)

@@ -444,8 +444,9 @@ struct Smem {
     uint64_t* wfull;  // [MMA_NSTAGE] weight chunk landed (TMA)
     uint64_t* bfull;  // [MMA_NSTAGE] activation chunk written (one arrival per consumer warp)
     uint64_t* sempty; // [MMA_NSTAGE] stage consumed by the MMAs (tcgen05.commit)
-    uint64_t* accf;   // [MMA_MAX_TILES] accumulator of a tile slot complete (tcgen05.commit)
-    uint64_t* accfree;  // the consumers have read every accumulator of the phase
+    uint64_t* accf;   // [MMA_URING] (tdone) a unit's products are in its tensor-memory slot (tcgen05.commit)
+    uint64_t* tfree;  // [MMA_URING] the consumer warps have read that slot (one arrival per warp)
+    uint64_t* accfree;  // (unused)
     uint64_t* mdone;  // every MMA the CTA issued has completed (before TMEM is freed)
     uint32_t* tslot;  // TMEM base address from tcgen05.alloc
     float* pssq;      // [MMA_MAX_TILES][32] this CTA's sums of squares of its inputs per tile part
@@ -469,7 +470,7 @@ __device__ __forceinline__ Smem smem_map(char* base, int maxrows, int BG)
     s.yf = s.red + (size_t)maxrows * BG * NWARP;
     s.X = (int*)s.red;
     s.wbuf = s.red;
-    s.wfull = s.bfull = s.sempty = s.accf = s.accfree = s.mdone = nullptr;
+    s.wfull = s.bfull = s.sempty = s.accf = s.tfree = s.accfree = s.mdone = nullptr;
     s.tslot = nullptr;
     s.pssq = s.bestv = nullptr;
     s.besti = nullptr;
@@ -497,7 +498,8 @@ __device__ __forceinline__ Smem smem_map_mma(char* base)
     s.amv = (float*)(base + 704);     // [NWARP]
     s.ami = (int*)(base + 736);       // [NWARP]
     s.misc = (int*)(base + 768);      // [64]
-    s.pssq = (float*)(base + 1024);   // [MMA_MAX_TILES][32]
+    s.tfree = (uint64_t*)(base + 1024);  // [MMA_URING]
+    s.pssq = nullptr;
     s.bestv = (float*)(base + 2048);  // [32]
     s.besti = (int*)(base + 2176);    // [32]
     s.mring = base + MMA_HEAD;
@@ -1513,6 +1515,95 @@ __device__ __forceinline__ bool gemv_phase(const Params& P, const Phase& ph, int
     return true;
 }
 
+// ------------------------------------------------------------------ rows and attention items
+
+// First and last row of row i's slot (rows of a slot are consecutive).
+__device__ __forceinline__ int slot_first_row(const StepDesc* D, int i)
+{
+    while (i > 0 && D->slot[i - 1] == D->slot[i]) --i;
+    return i;
+}
+
+__device__ __forceinline__ int slot_last_row(const StepDesc* D, int n, int i)
+{
+    while (i + 1 < n && D->slot[i + 1] == D->slot[i]) ++i;
+    return i;
+}
+
+// Chunks of a window of len keys: about 64 keys each, but no more than the
+// grid holds for one slot's heads at once (G / H), nor NCHUNK_MAX.  A function
+// of the slot's own window and the context's shape only, so a slot's result
+// never depends on the other slots of the step.
+__device__ __forceinline__ int attn_chunks(int len, int G, int H)
+{
+    int c = (len + 63) / 64;
+    const int cap = G / H > 1 ? G / H : 1;
+    c = c < cap ? c : cap;
+    // long windows: chunks of at most about 384 keys (more, shorter items keep
+    // every CTA busy when the windows of many slots are long)
+    const int clong = (len + 383) / 384;
+    c = c > clong ? c : clong;
+    return c < NCHUNK_MAX ? c : NCHUNK_MAX;
+}
+
+// Chunks of a window when one warp takes an item: about 128 keys each, at most
+// NCHUNK_MAX.  A function of the window only.
+__device__ __forceinline__ int attn_chunks_warp(int len)
+{
+    const int c = (len + 127) / 128;
+    return c < NCHUNK_MAX ? c : NCHUNK_MAX;
+}
+
+// Keys per stage when the producer streams a head's keys and values through the
+// tensor-core stages (keys, then values, bf16), and stages per item.
+__device__ __forceinline__ int attn_stage_keys(int hd) { return MMA_STAGE / (2 * hd * 2); }
+constexpr int ATTN_STAGES_PER_ITEM = 7;
+
+// Chunks of a window when its keys are streamed through the stages: at most
+// ATTN_STAGES_PER_ITEM stages each, at most NCHUNK_MAX.  A function of the window only.
+__device__ __forceinline__ int attn_chunks_stream(int len, int hd)
+{
+    const int per = attn_stage_keys(hd) * ATTN_STAGES_PER_ITEM;
+    const int c = (len + per - 1) / per;
+    return c < NCHUNK_MAX ? c : NCHUNK_MAX;
+}
+
+enum AttnMode : int { ATTN_CTA = 0, ATTN_WARP = 1, ATTN_STREAM = 2 };
+
+// Work items of the step's attention: (batch row i, head h, chunk c), row-major.
+__device__ __forceinline__ int attn_nchunks(int mode, int len, int G, int H, int hd)
+{
+    return mode == ATTN_WARP ? attn_chunks_warp(len) : (mode == ATTN_STREAM ? attn_chunks_stream(len, hd) : attn_chunks(len, G, H));
+}
+
+__device__ __forceinline__ void attn_item(const StepDesc* D, int n, int H, int W, int G, int item, int& i, int& h,
+                                          int& c, int& nch, int& len, int mode = ATTN_CTA, int hd = 0)
+{
+    int base = 0;
+    for (i = 0; i < n; ++i) {
+        const int p = D->pos[i];
+        len = p + 1 < W ? p + 1 : W;
+        nch = attn_nchunks(mode, len, G, H, hd);
+        if (item < base + nch * H) break;
+        base += nch * H;
+    }
+    const int r = item - base;
+    h = r / nch;
+    c = r % nch;
+}
+
+// A key range of one attention item streamed through the stages: item's
+// chunk [k0, k1) minus this launch's keys (the last mcur of the window, which
+// come from the tagged copies).
+__device__ __forceinline__ void attn_stream_range(const StepDesc* D, int i, int len, int c, int nch, int& k0, int& k1,
+                                                  int& kend, int& mcur)
+{
+    mcur = D->pos[i] - D->pos[slot_first_row(D, i)] + 1;
+    k0 = (int)((long long)len * c / nch);
+    k1 = (int)((long long)len * (c + 1) / nch);
+    kend = min(k1, len - mcur);
+}
+
 // ------------------------------------------------------------------ tensor-core weight pass
 // Batches of 5..32 rows with bf16 weights: every matrix phase is a product of
 // the weight matrix (A, M rows x K) with the rows' activations (B, N rows x K,
@@ -1642,6 +1733,31 @@ __device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, float (&v)[16])
     for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
 }
 
+// nc fp32 columns into this warp's 32 lanes of tensor memory.
+template <int NC>
+__device__ __forceinline__ void tmem_st(uint32_t taddr, const float (&v)[16]);
+
+template <>
+__device__ __forceinline__ void tmem_st<8>(uint32_t taddr, const float (&v)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                   "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                   "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])) : "memory");
+}
+
+template <>
+__device__ __forceinline__ void tmem_st<16>(uint32_t taddr, const float (&v)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+                 ::"r"(taddr), "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                   "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                   "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+                   "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+                   "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+                   "r"(__float_as_uint(v[15])) : "memory");
+}
+
 // This CTA's units of an M x K matrix.
 struct MmaPart {
     int KC, T;
@@ -1705,6 +1821,40 @@ __device__ __forceinline__ void producer_mma(const Params& P, int ph0, int ph1, 
         int M, K, c, cnt;
         Phase q = P.phases[ph];
         if (!resolve(P, starts, q, c, cnt)) continue;
+        if (q.type == PH_ATTN) {
+            // keys then values of every item of this CTA, one stage per attn_stage_keys positions
+            // (read once: evict-first, like the weights)
+            const StepDesc* D = P.desc;
+            const int H = P.H, hd = P.hd, Wn = P.W, KPS = attn_stage_keys(hd);
+            int total = 0;
+            for (int i = 0; i < n; ++i) total += attn_chunks_stream(D->pos[i] + 1 < Wn ? D->pos[i] + 1 : Wn, hd) * H;
+            for (int item = blockIdx.x; item < total && ok; item += P.G) {
+                int i, h, ci, nch, len, k0, k1, kend, mcur;
+                attn_item(D, n, H, Wn, P.G, item, i, h, ci, nch, len, ATTN_STREAM, hd);
+                attn_stream_range(D, i, len, ci, nch, k0, k1, kend, mcur);
+                const int start = D->pos[i] - len + 1;
+                const size_t hbase = (((size_t)D->slot[i] * P.L + q.l) * H + h) * (size_t)Wn * hd;
+                for (int kb = k0; kb < kend; kb += KPS, ++s) {
+                    const int nk = min(KPS, kend - kb);
+                    const int slot = (int)(s % MMA_NSTAGE);
+                    if (!mbar_wait(&sm.sempty[slot], ((s / MMA_NSTAGE) & 1u) ^ 1u, P.err, WS_EMPTY)) { ok = false; break; }
+                    const unsigned kbytes = (unsigned)(nk * hd * sizeof(TW));
+                    mbar_expect_tx(&sm.wfull[slot], 2 * kbytes);
+                    const int r0 = (start + kb) % Wn, n1 = min(nk, Wn - r0);
+                    char* dst = sm.mring + (size_t)slot * MMA_STAGE;
+                    for (int t = 0; t < 2; ++t) {  // keys, then values at KPS keys' offset
+                        const TW* ring = (const TW*)(t == 0 ? P.kc : P.vc) + hbase;
+                        char* dt = dst + (size_t)t * KPS * hd * sizeof(TW);
+                        bulk_g2s(dt, ring + (size_t)r0 * hd, (unsigned)(n1 * hd * sizeof(TW)), &sm.wfull[slot], pol_w);
+                        if (n1 < nk)
+                            bulk_g2s(dt + (size_t)n1 * hd * sizeof(TW), ring, (unsigned)((nk - n1) * hd * sizeof(TW)),
+                                     &sm.wfull[slot], pol_w);
+                    }
+                    mbar_arrive(&sm.bfull[slot]);  // the activation barrier's phase stays in step with the stage
+                }
+            }
+            continue;
+        }
         if (!phase_matrix<TW>(P, q, W, M, K)) continue;
         const CUtensorMap* map = P.tmaps + tmap_index(q.type, q.l, q.j, P.L, P.dL);
         const MmaPart mp = mma_part(M, K, c, cnt);
@@ -1775,19 +1925,18 @@ __device__ __forceinline__ void producer_mma(const Params& P, int ph0, int ph1, 
     }
 }
 
-// MMA warp (one lane): per unit, wait for the weight and activation chunks,
-// issue the MMAs into the tile's accumulator slot, release the stage; when a
-// tile's last chunk of the range is in, signal its slot.  Before the first
-// unit of each matrix phase after the first, wait until the consumers have
-// read the previous phase's accumulators.
+// MMA warp (one lane): per unit, wait for the weight and activation chunks and
+// for a free slot of the tensor-memory ring, issue the unit's four MMAs into
+// that slot (fresh: short fp32 chains on the tensor cores), release the stage
+// and signal the slot.
 template <typename TW>
 __device__ __forceinline__ void mma_issuer(const Params& P, int ph0, int ph1, int n, unsigned starts, const Smem& sm,
                                            uint32_t tbase)
 {
     const int ncol = MMA_PARTS * mma_nbp(n);
     const uint32_t idesc = mma_idesc(ncol);
-    unsigned s = 0, frees = 0;
-    bool first = true, ok = true;
+    unsigned s = 0, uc = 0;  // stages, units
+    bool ok = true;
     const int dep_end = P.dep_ph0 + n_groups(starts) * P.dep_ph_stride;
     const int dep_all = P.dep_ph0 + P.S * P.dep_ph_stride;
     for (int ph = ph0; ph < ph1 && ok; ++ph) {
@@ -1799,14 +1948,31 @@ __device__ __forceinline__ void mma_issuer(const Params& P, int ph0, int ph1, in
         int M, K, c, cnt;
         Phase q = P.phases[ph];
         if (!resolve(P, starts, q, c, cnt)) continue;
-        if (!phase_matrix<TW>(P, q, W, M, K)) continue;
-        if (!first) {
-            if (!mbar_wait(sm.accfree, frees & 1u, P.err, WS_FULL)) { ok = false; break; }
-            ++frees;
+        if (q.type == PH_ATTN) {
+            // attention stages go to the consumers; their barrier phases are waited
+            // out in order, so that a later parity wait cannot match an older phase
+            const StepDesc* D = P.desc;
+            const int H = P.H, hd = P.hd, Wn = P.W, KPS = attn_stage_keys(hd);
+            int total = 0;
+            for (int i = 0; i < n; ++i) total += attn_chunks_stream(D->pos[i] + 1 < Wn ? D->pos[i] + 1 : Wn, hd) * H;
+            for (int item = blockIdx.x; item < total && ok; item += P.G) {
+                int i, h, ci, nch, len, k0, k1, kend, mcur;
+                attn_item(D, n, H, Wn, P.G, item, i, h, ci, nch, len, ATTN_STREAM, hd);
+                attn_stream_range(D, i, len, ci, nch, k0, k1, kend, mcur);
+                for (int kb = k0; kb < kend; kb += KPS, ++s) {
+                    const int slot = (int)(s % MMA_NSTAGE);
+                    const unsigned par = (s / MMA_NSTAGE) & 1u;
+                    if (!mbar_wait(&sm.wfull[slot], par, P.err, WS_FULL) || !mbar_wait(&sm.bfull[slot], par, P.err, WS_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                }
+            }
+            continue;
         }
-        first = false;
+        if (!phase_matrix<TW>(P, q, W, M, K)) continue;
         const MmaPart mp = mma_part(M, K, c, cnt);
-        for (int u = mp.u0; u < mp.u1; ++u, ++s) {
+        for (int u = mp.u0; u < mp.u1; ++u, ++s, ++uc) {
             const int slot = (int)(s % MMA_NSTAGE);
             const unsigned par = (s / MMA_NSTAGE) & 1u;
             const unsigned long long tw0 = P.ptime ? globaltimer_ns() : 0ull;
@@ -1818,17 +1984,19 @@ __device__ __forceinline__ void mma_issuer(const Params& P, int ph0, int ph1, in
                 P.ptime[(size_t)ph * 8 + 4] += tw1 - tw0;
                 P.ptime[(size_t)ph * 8 + 5] += globaltimer_ns() - tw1;
             }
+            // the unit's products go to a fresh slot of the ring (K = 64: four MMAs);
+            // the consumers add them to the tile's sum in fp32 on the CUDA cores
+            const int r = (int)(uc % MMA_URING);
+            if (!mbar_wait(&sm.tfree[r], ((uc / MMA_URING) & 1u) ^ 1u, P.err, WS_FULL)) { ok = false; break; }
             tc_fence_after();
-            const int t = u / mp.KC, j = t - mp.t0;
-            const uint32_t d = tbase + (uint32_t)(j * ncol);
+            const uint32_t d = tbase + (uint32_t)(r * ncol);
             const unsigned sa = smem_u32(sm.mring + (size_t)slot * MMA_STAGE);
             const uint64_t ad = sw128_desc(sa), bd = sw128_desc(sa + MMA_W_BYTES);
-            const int ufirst = max(mp.u0, t * mp.KC);
 #pragma unroll
             for (int kk = 0; kk < MMA_KC / 16; ++kk)
-                mma_bf16(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, (u != ufirst || kk > 0) ? 1u : 0u);
+                mma_bf16(d, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, kk > 0 ? 1u : 0u);
             mma_commit(&sm.sempty[slot]);
-            if (u == mp.u1 - 1 || (u + 1) % mp.KC == 0) mma_commit(&sm.accf[j]);
+            mma_commit(&sm.accf[r]);
         }
     }
     // every MMA issued has completed before tensor memory is freed
@@ -1880,9 +2048,40 @@ __device__ __forceinline__ void mark_phase_done(const Params& P, int ph)
 // Per-thread state of the consumers across tensor-core phases.
 struct MmaState {
     uint32_t tbase;
-    unsigned accpar;  // bit j: parity of the next completion of accumulator slot j
+    unsigned uc;      // units read so far in this launch (position in the tensor-memory ring)
     int ph0;          // first phase of the launch
 };
+
+// Tile sum j of this warp's rows and batch rows (see mma_read_tile), stored in /
+// read from the columns after the ring: MMA_URING x 3 nbp, then nbp per tile.
+template <int NC>
+__device__ __forceinline__ uint32_t tile_sum_addr(uint32_t tbase, int j, int nbp)
+{
+    const int warp = threadIdx.x >> 5;
+    return tbase + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(MMA_URING * MMA_PARTS * nbp + j * nbp) +
+           (uint32_t)((warp >> 2) * NC);
+}
+
+__device__ __forceinline__ void tile_sum_store(uint32_t tbase, int j, int nbp, const float (&y)[16])
+{
+    if (nbp == 16) tmem_st<8>(tile_sum_addr<8>(tbase, j, nbp), y);
+    else tmem_st<16>(tile_sum_addr<16>(tbase, j, nbp), y);
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tile_sum_load(uint32_t tbase, int j, int nbp, float (&y)[16])
+{
+#pragma unroll
+    for (int e = 0; e < 16; ++e) y[e] = 0.f;
+    if (nbp == 16) {
+        float v[8];
+        tmem_ld<8>(tile_sum_addr<8>(tbase, j, nbp), v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = v[e];
+    } else {
+        tmem_ld<16>(tile_sum_addr<16>(tbase, j, nbp), y);
+    }
+}
 
 // This warp's accumulator values of tile slot j: rows 32 (warp % 4) + lane,
 // batch rows [h * nbp / 2, (h + 1) * nbp / 2) with h = warp / 4; the products
@@ -1945,6 +2144,7 @@ __device__ __noinline__ bool mma_phase(const Params& P, const Phase& ph, int phi
     // three bf16 parts and writes them to operand rows b, nbp + b and 2 nbp + b in
     // the swizzled K-major layout; rows of padding batch rows are zero.  Then the
     // chunk's sums of squares per row, a proxy fence, and the chunk's ready tag.
+    stage += (unsigned)(mp.u1 - mp.u0);  // the stages of this phase's units (the producer's and MMA warp's count)
     const int b = tid >> 3, c16 = tid & 7;
     const bool active = b < n;
     const int sub = phase_sub(ph);
@@ -2054,15 +2254,38 @@ __device__ __noinline__ bool mma_phase(const Params& P, const Phase& ph, int phi
     const int row = 32 * (warp & 3) + lane;  // this thread's tile row
     const int bh = (warp >> 2) * (nbp / 2);  // and its first batch row
     const int nh = nbp / 2;
+    // the units' products in order: each unit's slot of the ring is read, its three
+    // parts added, and the result added to the tile's sum in fp32 (round to
+    // nearest, K order); a finished tile's sum goes to its columns
+    {
+        float acc[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+        for (int u = mp.u0; u < mp.u1; ++u, ++ms.uc) {
+            const int r = (int)(ms.uc % MMA_URING);
+            if (ok && !mbar_wait(&sm.accf[r], (ms.uc / MMA_URING) & 1u, P.err, WS_FULL)) ok = 0;
+            if (!__all_sync(0xffffffffu, ok)) { ok = 0; break; }
+            tc_fence_after();
+            float y[16];
+            mma_read(ms.tbase, r, nbp, y);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.tfree[r]);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[e] += y[e];
+            if (u == mp.u1 - 1 || (u + 1) % mp.KC == 0) {
+                tile_sum_store(ms.tbase, u / mp.KC - mp.t0, nbp, acc);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+            }
+        }
+    }
+    if (!csync_and(ok)) return false;
     // the partial of the tile this CTA does not own
     if (mp.nt > 0 && !mp.last_owned) {
         const int j = mp.nt - 1;
-        if (!mbar_wait(&sm.accf[j], (ms.accpar >> j) & 1u, P.err, WS_FULL)) ok = 0;
-        ms.accpar ^= 1u << j;
-        if (!csync_and(ok)) return false;
-        tc_fence_after();
         float y[16];
-        mma_read(ms.tbase, j, nbp, y);
+        tile_sum_load(ms.tbase, j, nbp, y);
         uint2* dst = P.mpart + (((size_t)par * P.G + blockIdx.x) * MMA_M + row) * 32 + bh;  // par: phase mod MMA_ROT
 #pragma unroll
         for (int e = 0; e < 16; e += 2)
@@ -2083,12 +2306,8 @@ __device__ __noinline__ bool mma_phase(const Params& P, const Phase& ph, int phi
         const long long U = (long long)mp.T * mp.KC;
         for (int j = 0; j < nown && ok; ++j) {
             const int t = mp.t0 + j;
-            if (!mbar_wait(&sm.accf[j], (ms.accpar >> j) & 1u, P.err, WS_FULL)) ok = 0;
-            ms.accpar ^= 1u << j;
-            if (!csync_and(ok)) return false;
-            tc_fence_after();
             float y[16], acc[16];
-            mma_read(ms.tbase, j, nbp, y);
+            tile_sum_load(ms.tbase, j, nbp, y);
 #pragma unroll
             for (int e = 0; e < 16; ++e) acc[e] = 0.f;
             // contributors: the CTAs before this one whose ranges reach into tile t, in K order
@@ -2140,27 +2359,10 @@ __device__ __noinline__ bool mma_phase(const Params& P, const Phase& ph, int phi
     } else {
         epi.empty(P, 0, n);
     }
-    // the accumulators are free for the next phase
-    tc_fence_before();
-    csync();
-    if (tid == 0) mbar_arrive(sm.accfree);
     return true;
 }
 
 // ------------------------------------------------------------------ S0 + S1
-
-// First and last row of row i's slot (rows of a slot are consecutive).
-__device__ __forceinline__ int slot_first_row(const StepDesc* D, int i)
-{
-    while (i > 0 && D->slot[i - 1] == D->slot[i]) --i;
-    return i;
-}
-
-__device__ __forceinline__ int slot_last_row(const StepDesc* D, int n, int i)
-{
-    while (i + 1 < n && D->slot[i + 1] == D->slot[i]) ++i;
-    return i;
-}
 
 template <typename TW>
 __device__ __forceinline__ bool phase_embed(const Params& P, int n, unsigned tag, const Smem& sm)
@@ -2304,47 +2506,6 @@ __device__ __forceinline__ void prefetch_kv_windows(const Params& P, int l, int 
             prefetch_l2(run, (unsigned)((r0 + c - W) * hd * sizeof(TKV)), pol);
         }
     }
-}
-
-// Chunks of a window of len keys: about 64 keys each, but no more than the
-// grid holds for one slot's heads at once (G / H), nor NCHUNK_MAX.  A function
-// of the slot's own window and the context's shape only, so a slot's result
-// never depends on the other slots of the step.
-__device__ __forceinline__ int attn_chunks(int len, int G, int H)
-{
-    int c = (len + 63) / 64;
-    const int cap = G / H > 1 ? G / H : 1;
-    c = c < cap ? c : cap;
-    // long windows: chunks of at most about 384 keys (more, shorter items keep
-    // every CTA busy when the windows of many slots are long)
-    const int clong = (len + 383) / 384;
-    c = c > clong ? c : clong;
-    return c < NCHUNK_MAX ? c : NCHUNK_MAX;
-}
-
-// Chunks of a window when one warp takes an item (tensor-core instantiation):
-// about 128 keys each, at most NCHUNK_MAX.  A function of the window only.
-__device__ __forceinline__ int attn_chunks_warp(int len)
-{
-    const int c = (len + 127) / 128;
-    return c < NCHUNK_MAX ? c : NCHUNK_MAX;
-}
-
-// Work items of the step's attention: (batch row i, head h, chunk c), row-major.
-__device__ __forceinline__ void attn_item(const StepDesc* D, int n, int H, int W, int G, int item, int& i, int& h,
-                                          int& c, int& nch, int& len, bool per_warp = false)
-{
-    int base = 0;
-    for (i = 0; i < n; ++i) {
-        const int p = D->pos[i];
-        len = p + 1 < W ? p + 1 : W;
-        nch = per_warp ? attn_chunks_warp(len) : attn_chunks(len, G, H);
-        if (item < base + nch * H) break;
-        base += nch * H;
-    }
-    const int r = item - base;
-    h = r / nch;
-    c = r % nch;
 }
 
 // One CTA per (batch row, head, chunk of the window): its warps split the
@@ -2600,7 +2761,7 @@ __device__ __noinline__ bool phase_attn_warp(const Params& P, int l, int n, unsi
     int ok = 1;
     for (int item = gw; item < total && ok; item += GW) {
         int i, h, c, nch, len;
-        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, true);
+        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, ATTN_WARP);
         const int p = D->pos[i], slot = D->slot[i];
         const int start = p - len + 1;
         const int mcur = p - D->pos[slot_first_row(D, i)] + 1;
@@ -2640,7 +2801,7 @@ __device__ __noinline__ bool phase_attn_warp(const Params& P, int l, int n, unsi
     // merges: the warp that ran chunk 0 of a split window combines its chunks in order
     for (int item = gw; item < total && ok; item += GW) {
         int i, h, c, nch, len;
-        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, true);
+        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, ATTN_WARP);
         if (c != 0 || nch == 1) continue;
         const uint2* part = P.attp + ((size_t)i * H + h) * NCHUNK_MAX * pstride;
         // lane takes elements lane, lane + 32, ... of the head; the chunk maxima and sums first
@@ -2681,6 +2842,186 @@ __device__ __noinline__ bool phase_attn_warp(const Params& P, int l, int n, unsi
             if (lane + 32 * q < hd) st_tag1(P.o + (size_t)i * d + h * hd + lane + 32 * q, __float_as_uint(a[q] / L), tag);
     }
     return csync_and(ok);
+}
+
+// Attention of the tensor-core instantiation with keys and values streamed by the
+// producer warp: one CTA per item (batch row, head, chunk of up to 7 stages).
+// A stage holds up to attn_stage_keys(hd) keys, then as many values, bf16, copied
+// from the head-major ring; the eight warps take the stage's keys two at a time
+// (16 lanes per key), keep an online softmax per lane, release the stage, and at
+// the end of the item merge in warp order.  This launch's keys (the current one,
+// and a prompt chunk's earlier rows) come from the tagged copies.  Chunks merge
+// as in phase_attn.
+template <typename TKV>
+__device__ __noinline__ bool phase_attn_stream(const Params& P, int l, int n, unsigned in_tag, unsigned tag, const Smem& sm,
+                                               unsigned& stage)
+{
+    const StepDesc* D = P.desc;
+    const int H = P.H, hd = P.hd, d = P.d, W = P.W;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int LPP = hd / 8, PPI = 32 / LPP;
+    const int grp = lane / LPP, gl = lane % LPP;
+    const int KPS = attn_stage_keys(hd);
+    const float scale = rsqrtf((float)hd);
+    const int wstride = hd + 4;
+    const size_t pstride = (size_t)hd + 2;
+    int total = 0;
+    for (int i = 0; i < n; ++i) {
+        const int p = D->pos[i];
+        total += attn_chunks_stream(p + 1 < W ? p + 1 : W, hd) * H;
+    }
+    int ok = 1;
+    for (int item = blockIdx.x; item < total; item += P.G) {
+        int i, h, c, nch, len;
+        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, ATTN_STREAM, hd);
+        int k0, k1, kend, mcur;
+        attn_stream_range(D, i, len, c, nch, k0, k1, kend, mcur);
+        const size_t qo = (size_t)i * d + h * hd + gl * 8;
+        float qv[8];
+        uint2 qt[8];
+        tag8_issue(P.q + qo, qt);
+        if (!tag8_take(qt, P.q + qo, in_tag, qv, P.err)) ok = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) qv[e] *= scale;
+        float m = -INFINITY, lsum = 0.f, acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        // one key of the lane group: score, then the running softmax update
+        auto take = [&](const float kf[8], const float vf[8], bool valid) {
+            float t = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) t = fmaf(qv[e], kf[e], t);
+            for (int o = LPP / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+            if (!valid) return;
+            const float mn = fmaxf(m, t);
+            const float corr = expf(m - mn), pu = expf(t - mn);
+            lsum = lsum * corr + pu;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(pu, vf[e], acc[e] * corr);
+            m = mn;
+        };
+        // streamed keys, stage by stage (every warp passes every stage's barrier, also
+        // after a failed wait, so that no barrier waits for a warp that has left)
+        for (int kb = k0; kb < kend; kb += KPS, ++stage) {
+            const int nk = min(KPS, kend - kb);
+            const int slot = (int)(stage % MMA_NSTAGE);
+            if (ok && !mbar_wait(&sm.wfull[slot], (stage / MMA_NSTAGE) & 1u, P.err, WS_FULL)) ok = 0;
+            if (__all_sync(0xffffffffu, ok)) {
+                const __nv_bfloat16* ks = (const __nv_bfloat16*)(sm.mring + (size_t)slot * MMA_STAGE);
+                const __nv_bfloat16* vs = ks + (size_t)KPS * hd;
+                for (int kk0 = 0; kk0 < nk; kk0 += NWARP * PPI) {  // warp-uniform trip count
+                    const int kk = kk0 + warp * PPI + grp;
+                    float kf[8], vf[8];
+                    WV<__nv_bfloat16>::lds8(ks + (size_t)(kk < nk ? kk : 0) * hd + gl * 8, kf);
+                    WV<__nv_bfloat16>::lds8(vs + (size_t)(kk < nk ? kk : 0) * hd + gl * 8, vf);
+                    take(kf, vf, kk < nk);
+                }
+            } else {
+                ok = 0;
+            }
+            csync();  // every warp is done with the stage
+            if (threadIdx.x == 0) mbar_arrive(&sm.sempty[slot]);
+        }
+        // this launch's keys (from the tagged copies): key j is row i - (len - 1 - j)
+        const int jl0 = max(k0, len - mcur);
+        for (int jb = jl0; jb < k1; jb += NWARP * PPI) {
+            const int j = jb + warp * PPI + grp;
+            float kf[8], vf[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { kf[e] = 0.f; vf[e] = 0.f; }
+            if (j < k1 && ok) {
+                const size_t ro = (size_t)(i - (len - 1 - j)) * d + h * hd + gl * 8;
+                ok = wait_tag8(P.kcur + ro, in_tag, kf, P.err) && wait_tag8(P.vcur + ro, in_tag, vf, P.err);
+            }
+            take(kf, vf, j < k1);
+        }
+        // merge the key groups of the warp, then the warps in warp order
+        for (int o = LPP; o < 32; o <<= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+            const float l2 = __shfl_xor_sync(0xffffffffu, lsum, o);
+            float a2[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) a2[e] = __shfl_xor_sync(0xffffffffu, acc[e], o);
+            const float M = fmaxf(m, m2);
+            const float c1 = m == -INFINITY ? 0.f : expf(m - M);
+            const float c2 = m2 == -INFINITY ? 0.f : expf(m2 - M);
+            lsum = lsum * c1 + l2 * c2;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = acc[e] * c1 + a2[e] * c2;
+            m = M;
+        }
+        float* wb = sm.wbuf + (size_t)warp * wstride;
+        if (lane < LPP) {
+            if (lane == 0) { wb[0] = m; wb[1] = lsum; }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) wb[4 + gl * 8 + e] = acc[e];
+        }
+        if (!csync_and(ok)) return false;
+        float M = -INFINITY;
+        for (int w = 0; w < NWARP; ++w) M = fmaxf(M, sm.wbuf[(size_t)w * wstride]);
+        uint2* part = P.attp + (((size_t)i * H + h) * NCHUNK_MAX + c) * pstride;
+        for (int e = threadIdx.x; e < hd; e += NT) {
+            float L = 0.f, a = 0.f;
+            for (int w = 0; w < NWARP; ++w) {
+                const float mw = sm.wbuf[(size_t)w * wstride];
+                if (mw == -INFINITY) continue;
+                const float f = expf(mw - M);
+                L += sm.wbuf[(size_t)w * wstride + 1] * f;
+                a += sm.wbuf[(size_t)w * wstride + 4 + e] * f;
+            }
+            if (nch == 1) {
+                st_tag1(P.o + (size_t)i * d + h * hd + e, __float_as_uint(a / L), tag);
+            } else {
+                st_tag1(part + 2 + e, __float_as_uint(a), tag);
+                if (e == 0) {
+                    st_tag1(part, __float_as_uint(M), tag);
+                    st_tag1(part + 1, __float_as_uint(L), tag);
+                }
+            }
+        }
+        csync();
+    }
+    if (!csync_and(ok)) return false;
+    // merges: the CTA that ran chunk 0 of a split window combines its chunks in order
+    for (int item = blockIdx.x; item < total; item += P.G) {
+        int i, h, c, nch, len;
+        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, ATTN_STREAM, hd);
+        if (c != 0 || nch == 1) continue;
+        const uint2* part = P.attp + ((size_t)i * H + h) * NCHUNK_MAX * pstride;
+        float* mb = sm.wbuf;  // [nch][hd + 2]
+        const int cnt = nch * (int)pstride;
+        for (int x0 = threadIdx.x; x0 < cnt && ok; x0 += 4 * NT) {
+            uint2 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int x = x0 + u * NT;
+                v[u] = x < cnt ? ld_tag1(part + (x / pstride) * pstride + x % pstride) : make_uint2(0u, tag);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int x = x0 + u * NT;
+                unsigned bits = v[u].x;
+                if (x < cnt && v[u].y != tag && ok) ok = wait_tag1(part + (x / pstride) * pstride + x % pstride, tag, bits, P.err);
+                if (x < cnt) mb[x] = __uint_as_float(bits);
+            }
+        }
+        if (!csync_and(ok)) return false;
+        for (int e = threadIdx.x; e < hd; e += NT) {
+            float M = -INFINITY;
+            for (int k = 0; k < nch; ++k) M = fmaxf(M, mb[k * pstride]);
+            float L = 0.f, a = 0.f;
+            for (int k = 0; k < nch; ++k) {
+                const float mk = mb[k * pstride];
+                if (mk == -INFINITY) continue;
+                const float f = expf(mk - M);
+                L += mb[k * pstride + 1] * f;
+                a += mb[k * pstride + 2 + e] * f;
+            }
+            st_tag1(P.o + (size_t)i * d + h * hd + e, __float_as_uint(a / L), tag);
+        }
+        csync();
+    }
+    return true;
 }
 
 // ------------------------------------------------------------------ S9 depformer attention
@@ -2869,7 +3210,7 @@ __device__ __forceinline__ bool run_phase(const Params& P, Phase ph, int phi, in
             return matrix_phase<TW, BG>(P, ph, phi, c, cnt, XSrc{P.x, d, in_tag, P.attn_norm + (size_t)ph.l * d},
                                       n, sm, stage, ms, EpiQKV<TKV>{ph.l, tag});
         case PH_ATTN:
-            if constexpr (is_mma(BG)) return phase_attn_warp<TKV>(P, ph.l, n, in_tag, tag);
+            if constexpr (is_mma(BG)) return phase_attn_stream<TKV>(P, ph.l, n, in_tag, tag, sm, stage);
             else return phase_attn<TKV>(P, ph.l, n, in_tag, tag, sm);
         case PH_O:
             return matrix_phase<TW, BG>(P, ph, phi, c, cnt, XSrc{P.o, d, in_tag}, n, sm, stage, ms, EpiResid{P.x, d, res_tag, tag});
@@ -2949,8 +3290,10 @@ __global__ void __launch_bounds__(is_mma(BG) ? MMA_THREADS : NT + 32, 1) step_ke
                 mbar_init(&sm.bfull[k], 1);      // the producer's bulk copy of the activation chunk
                 mbar_init(&sm.sempty[k], 1);
             }
-            for (int k = 0; k < MMA_MAX_TILES; ++k) mbar_init(&sm.accf[k], 1);
-            mbar_init(sm.accfree, 1);
+            for (int k = 0; k < MMA_URING; ++k) {
+                mbar_init(&sm.accf[k], 1);      // the MMA warp's commit of a unit
+                mbar_init(&sm.tfree[k], NWARP);  // every consumer warp has read the unit's slot
+            }
             mbar_init(sm.mdone, 1);
         } else {
             for (int k = 0; k < (int)nstage_for(BG); ++k) {
@@ -3031,7 +3374,7 @@ __global__ void __launch_bounds__(is_mma(BG) ? MMA_THREADS : NT + 32, 1) step_ke
     }
     MmaState ms;
     ms.tbase = 0;
-    ms.accpar = 0;
+    ms.uc = 0;
     ms.ph0 = ph0;
     if constexpr (is_mma(BG)) {
         const uint32_t tbase = *sm.tslot;
