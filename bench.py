@@ -444,7 +444,8 @@ def run_batched(args, mfs, ctx, s, stream, world):
         shared[4:8] = np.frombuffer(np.int32(lens8[i]).tobytes(), np.uint8)
         mfs.mfs_import_slot(ctx, i, shared)
     r = time_steps(8, lambda k: [min(int(lens8[i]) + k + 1, s.window) for i in range(8)], 11)
-    r["what"] = "B=8 decode, per-slot windows uniform in [0, 3000] (synthetic ring states), tensor-core weight pass"
+    r["what"] = ("B=8 decode, per-slot windows uniform in [0, 3000] (synthetic ring states); temporal stack and text "
+                 "head on the tensor-core pass, depformer on the CUDA-core pass (two launches per step)")
     out["batch_8"] = r
 
     # B = 16: 250-frame prompts (timed), then decode
@@ -458,9 +459,11 @@ def run_batched(args, mfs, ctx, s, stream, world):
     torch.cuda.synchronize()
     pre_s = time.perf_counter() - t0
     r = time_steps(16, lambda k: [min(PROMPT + k + 1, s.window)] * 16, 12)
-    r["what"] = "B=16 decode after 250-frame prompts, tensor-core weight pass"
+    r["what"] = ("B=16 decode after 250-frame prompts; temporal stack and text head on the tensor-core pass, "
+                 "depformer on the CUDA-core pass (two launches per step)")
     r["prompt"] = {"frames": 16 * PROMPT, "seconds": pre_s, "value": 16 * PROMPT / pre_s, "unit": "prompt frames/s",
-                   "what": "mfs_prefill of 16 slots x 250 frames (host call, includes the token upload)"}
+                   "what": "mfs_prefill of 16 slots x 250 frames: 125 launches of 32 rows (two frames of every "
+                           "slot) on the tensor-core pass (host call, includes the token upload)"}
     out["batch_16"] = r
 
     # B = 32: full rings, every step wraps
@@ -469,7 +472,8 @@ def run_batched(args, mfs, ctx, s, stream, world):
         shared[4:8] = np.frombuffer(np.int32(pos32[i]).tobytes(), np.uint8)
         mfs.mfs_import_slot(ctx, i, shared)
     r = time_steps(32, lambda k: [s.window] * 32, 13)
-    r["what"] = "B=32 decode, every ring full (3000 keys, every step wraps), tensor-core weight pass"
+    r["what"] = ("B=32 decode, every ring full (3000 keys, every step wraps); temporal stack and text head on the "
+                 "tensor-core pass, depformer on the CUDA-core pass (two launches per step)")
     out["batch_32"] = r
     return out
 

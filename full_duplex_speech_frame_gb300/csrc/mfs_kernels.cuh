@@ -1558,6 +1558,7 @@ __device__ __forceinline__ int attn_chunks_warp(int len)
 // tensor-core stages (keys, then values, bf16), and stages per item.
 __device__ __forceinline__ int attn_stage_keys(int hd) { return MMA_STAGE / (2 * hd * 2); }
 constexpr int ATTN_STAGES_PER_ITEM = 7;
+constexpr int ATTN_R = 4;  // keys per lane group and pass in a streamed stage (4 passes cover one stage)
 
 // Chunks of a window when its keys are streamed through the stages: at most
 // ATTN_STAGES_PER_ITEM stages each, at most NCHUNK_MAX.  A function of the window only.
@@ -2909,12 +2910,45 @@ __device__ __noinline__ bool phase_attn_stream(const Params& P, int l, int n, un
             if (__all_sync(0xffffffffu, ok)) {
                 const __nv_bfloat16* ks = (const __nv_bfloat16*)(sm.mring + (size_t)slot * MMA_STAGE);
                 const __nv_bfloat16* vs = ks + (size_t)KPS * hd;
-                for (int kk0 = 0; kk0 < nk; kk0 += NWARP * PPI) {  // warp-uniform trip count
-                    const int kk = kk0 + warp * PPI + grp;
-                    float kf[8], vf[8];
-                    WV<__nv_bfloat16>::lds8(ks + (size_t)(kk < nk ? kk : 0) * hd + gl * 8, kf);
-                    WV<__nv_bfloat16>::lds8(vs + (size_t)(kk < nk ? kk : 0) * hd + gl * 8, vf);
-                    take(kf, vf, kk < nk);
+                // the lane group's keys of the stage (up to ATTN_R), loaded together; their
+                // scores, then one rescale of the running sums for the group
+                for (int kk0 = 0; kk0 < nk; kk0 += ATTN_R * NWARP * PPI) {  // warp-uniform trip count
+                    uint4 kr[ATTN_R], vr[ATTN_R];
+#pragma unroll
+                    for (int r = 0; r < ATTN_R; ++r) {
+                        const int kk = kk0 + r * NWARP * PPI + warp * PPI + grp;
+                        const size_t off = (size_t)(kk < nk ? kk : 0) * hd + gl * 8;
+                        kr[r] = *reinterpret_cast<const uint4*>(ks + off);
+                        vr[r] = *reinterpret_cast<const uint4*>(vs + off);
+                    }
+                    float sc[ATTN_R], mn = m;
+#pragma unroll
+                    for (int r = 0; r < ATTN_R; ++r) {
+                        const float kf[8] = {bf_lo(kr[r].x), bf_hi(kr[r].x), bf_lo(kr[r].y), bf_hi(kr[r].y),
+                                             bf_lo(kr[r].z), bf_hi(kr[r].z), bf_lo(kr[r].w), bf_hi(kr[r].w)};
+                        float t = 0.f;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) t = fmaf(qv[e], kf[e], t);
+                        for (int o = LPP / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+                        sc[r] = kk0 + r * NWARP * PPI + warp * PPI + grp < nk ? t : -INFINITY;
+                        mn = fmaxf(mn, sc[r]);
+                    }
+                    if (mn != -INFINITY) {
+                        const float corr = expf(m - mn);
+                        lsum *= corr;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[e] *= corr;
+#pragma unroll
+                        for (int r = 0; r < ATTN_R; ++r) {
+                            const float pu = expf(sc[r] - mn);
+                            lsum += pu;
+                            const float vf[8] = {bf_lo(vr[r].x), bf_hi(vr[r].x), bf_lo(vr[r].y), bf_hi(vr[r].y),
+                                                 bf_lo(vr[r].z), bf_hi(vr[r].z), bf_lo(vr[r].w), bf_hi(vr[r].w)};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) acc[e] = fmaf(pu, vf[e], acc[e]);
+                        }
+                        m = mn;
+                    }
                 }
             } else {
                 ok = 0;

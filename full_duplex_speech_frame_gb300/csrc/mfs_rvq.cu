@@ -4,7 +4,9 @@
 // residual each stage leaves.  Nearest codeword by squared Euclidean distance,
 // ties to the lower index.
 //
-// One CTA takes up to 16 frames and keeps their residuals in shared memory.
+// This file holds the CUDA-core form, used when D is not a multiple of 8 (the
+// tensor-core form in mfs_rvq_mma.cu takes the rest).  One CTA takes up to 16
+// frames and keeps their residuals in shared memory.
 // Each thread owns codewords c, c + 256, ...: it streams a codeword row once
 // (float4 loads, L1-resident while it is used) and accumulates its distance to
 // every frame of the tile, whose residual chunks all threads read at the same
@@ -18,6 +20,8 @@
 
 namespace mfs {
 void set_thread_error(const char* msg);  // defined with mfs_last_error
+int rvq_encode_mma(const float* z_sem, const float* z_ac, int T, int D, const float* codebooks, int Cb, int32_t* codes,
+                   cudaStream_t st);  // the tensor-core form (mfs_rvq_mma.cu)
 }
 
 namespace {
@@ -121,7 +125,8 @@ __global__ void __launch_bounds__(RV_THREADS, 2) rvq_kernel(const float* __restr
         if (q >= 1 && q < 7) {  // the residual for the next acoustic stage
             for (int k = threadIdx.x; k < nf * D4; k += RV_THREADS) {
                 const int f = k / D4, e = k % D4;
-                const float4 w = __ldg(book + (size_t)scode[f] * D4 + e);
+                const int cw = scode[f] < Cb ? scode[f] : 0;  // no codeword chosen: NaN distances
+                const float4 w = __ldg(book + (size_t)cw * D4 + e);
                 float4 x = rv_r[k];
                 x.x -= w.x;
                 x.y -= w.y;
@@ -151,6 +156,8 @@ extern "C" int mfs_rvq_encode(const float* z_sem, const float* z_ac, int T, int 
     if (!z_sem || !z_ac || !codebooks || !codes) return fail(MFS_E_ARG, "rvq: null pointer");
     if (((uintptr_t)z_sem | (uintptr_t)z_ac | (uintptr_t)codebooks) & 15u)
         return fail(MFS_E_ARG, "rvq: latents and codebooks must be 16-byte aligned");
+    if (D % 8 == 0 && 8LL * Cb <= 0x7fffffffLL)
+        return mfs::rvq_encode_mma(z_sem, z_ac, T, D, codebooks, Cb, codes, (cudaStream_t)cuda_stream);
     const size_t smem = (size_t)RV_FT * D * sizeof(float);
     if (smem > 48 * 1024) {  // the residual tile needs more than the default shared memory
         const cudaError_t a = cudaFuncSetAttribute(rvq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

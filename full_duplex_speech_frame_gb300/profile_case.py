@@ -33,6 +33,8 @@ def main() -> None:
     ap.add_argument("--dep-layers", type=int, default=1)
     ap.add_argument("--steps", type=int, default=4)
     ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--full-rings", action="store_true",
+                    help="start every slot from a synthetic state with a full ring (positions past the window)")
     a = ap.parse_args()
     import torch
     torch.cuda.set_stream(torch.cuda.Stream())
@@ -40,11 +42,19 @@ def main() -> None:
     s = synth.FULL.replace(n_layers=a.layers, dep_layers=a.dep_layers, max_slots=B)
     ctx = mfs.context_with_weights(s, synth.make_weights(s, 0))
     slots = list(range(B))
-    mfs.mfs_prefill(ctx, slots, synth.forced_frames(s, 1, synth.STREAM_PROMPT, PROMPT, B).transpose(1, 0, 2))
+    if a.full_rings:
+        import numpy as np
+        st = synth.slot_state(s, 1, 300, 0)
+        for i in slots:
+            st[4:8] = np.frombuffer(np.int32(s.window + 7 * i).tobytes(), np.uint8)
+            mfs.mfs_import_slot(ctx, i, st)
+    else:
+        mfs.mfs_prefill(ctx, slots, synth.forced_frames(s, 1, synth.STREAM_PROMPT, PROMPT, B).transpose(1, 0, 2))
     u = synth.user_frames(s, 1, a.steps, B)
     for p in range(a.steps):
         text, codes = mfs.mfs_step(ctx, slots, u[p])
-    print(f"profile case: {a.layers} temporal / {a.dep_layers} depformer layers, B = {B}, {PROMPT}-frame prompt, "
+    start = "full rings" if a.full_rings else f"{PROMPT}-frame prompt"
+    print(f"profile case: {a.layers} temporal / {a.dep_layers} depformer layers, B = {B}, {start}, "
           f"{a.steps} steps; last text token {int(text[0])}")
 
 

@@ -255,8 +255,19 @@ int mfs_phase_times(mfs_ctx* ctx, uint64_t* ns, int cap);
  *   codebooks    device, [8][Cb][D] fp32, 16-byte aligned
  *   codes        device, [T][8] int32 out
  *   D            multiple of 4 in [4, MFS_RVQ_MAX_DIM]; stream as elsewhere
- * Enqueues and returns; MFS_E_ARG on bad sizes, alignment or NULL pointers
- * (mfs_last_error(NULL) gives the reason). */
+ * D a multiple of 8: the distances' cross terms r.c run on the tensor cores
+ * (bf16 high/low parts of r and c, fp32 accumulation, about 16 significant
+ * bits); each frame's 32 best codewords by that score are re-ranked by the
+ * exact fp32 distance, so the code is the exhaustive fp32 argmin unless more
+ * than 31 codewords score within that error (about 1e-5 of sum |r_i c_i|) of
+ * the nearest.  This form takes 4 * 8 * Cb * D + 32 * Cb bytes of scratch from
+ * the device's stream-ordered pool and frees it on the stream.  Otherwise every
+ * distance is computed exactly in fp32 on the CUDA cores.
+ * Enqueues and returns; MFS_E_ARG on bad sizes, alignment or NULL pointers;
+ * MFS_E_CUDA if the scratch or the launch fails (mfs_last_error(NULL) gives the
+ * reason).  A frame whose distances are all NaN gets code 0x7fffffff; on the
+ * tensor-core form, if one of the kernel's internal waits gives up (about 2 s:
+ * a stalled device), the frames of the CTAs that saw it get code -1. */
 #define MFS_RVQ_MAX_DIM 1024
 int mfs_rvq_encode(const float* z_sem, const float* z_ac, int T, int D, const float* codebooks, int Cb,
                    int32_t* codes, void* cuda_stream);
