@@ -446,7 +446,7 @@ struct Smem {
     uint64_t* sempty; // [MMA_NSTAGE] stage consumed by the MMAs (tcgen05.commit)
     uint64_t* accf;   // [MMA_URING] (tdone) a unit's products are in its tensor-memory slot (tcgen05.commit)
     uint64_t* tfree;  // [MMA_URING] the consumer warps have read that slot (one arrival per warp)
-    uint64_t* accfree;  // (unused)
+    uint64_t* adone;  // the consumers are past every stage of an attention phase (thread 0, once per phase)
     uint64_t* mdone;  // every MMA the CTA issued has completed (before TMEM is freed)
     uint32_t* tslot;  // TMEM base address from tcgen05.alloc
     float* pssq;      // [MMA_MAX_TILES][32] this CTA's sums of squares of its inputs per tile part
@@ -470,7 +470,7 @@ __device__ __forceinline__ Smem smem_map(char* base, int maxrows, int BG)
     s.yf = s.red + (size_t)maxrows * BG * NWARP;
     s.X = (int*)s.red;
     s.wbuf = s.red;
-    s.wfull = s.bfull = s.sempty = s.accf = s.tfree = s.accfree = s.mdone = nullptr;
+    s.wfull = s.bfull = s.sempty = s.accf = s.tfree = s.adone = s.mdone = nullptr;
     s.tslot = nullptr;
     s.pssq = s.bestv = nullptr;
     s.besti = nullptr;
@@ -489,7 +489,7 @@ __device__ __forceinline__ Smem smem_map_mma(char* base)
     s.bfull = s.wfull + 8;
     s.sempty = s.wfull + 16;
     s.accf = s.wfull + 24;
-    s.accfree = s.wfull + 32;
+    s.adone = s.wfull + 32;
     s.mdone = s.wfull + 33;
     s.tslot = (uint32_t*)(base + 272);
     s.full = s.empty = nullptr;
@@ -1558,13 +1558,12 @@ __device__ __forceinline__ int attn_chunks_warp(int len)
 // tensor-core stages (keys, then values, bf16), and stages per item.
 __device__ __forceinline__ int attn_stage_keys(int hd) { return MMA_STAGE / (2 * hd * 2); }
 constexpr int ATTN_STAGES_PER_ITEM = 7;
-constexpr int ATTN_R = 4;  // keys per lane group and pass in a streamed stage (4 passes cover one stage)
 
 // Chunks of a window when its keys are streamed through the stages: at most
 // ATTN_STAGES_PER_ITEM stages each, at most NCHUNK_MAX.  A function of the window only.
-__device__ __forceinline__ int attn_chunks_stream(int len, int hd)
+__device__ __forceinline__ int attn_chunks_stream(int len, int hd, int ipc)
 {
-    const int per = attn_stage_keys(hd) * ATTN_STAGES_PER_ITEM;
+    const int per = attn_stage_keys(hd) * ipc;
     const int c = (len + per - 1) / per;
     return c < NCHUNK_MAX ? c : NCHUNK_MAX;
 }
@@ -1572,19 +1571,34 @@ __device__ __forceinline__ int attn_chunks_stream(int len, int hd)
 enum AttnMode : int { ATTN_CTA = 0, ATTN_WARP = 1, ATTN_STREAM = 2 };
 
 // Work items of the step's attention: (batch row i, head h, chunk c), row-major.
-__device__ __forceinline__ int attn_nchunks(int mode, int len, int G, int H, int hd)
+__device__ __forceinline__ int attn_nchunks(int mode, int len, int G, int H, int hd, int ipc)
 {
-    return mode == ATTN_WARP ? attn_chunks_warp(len) : (mode == ATTN_STREAM ? attn_chunks_stream(len, hd) : attn_chunks(len, G, H));
+    return mode == ATTN_WARP ? attn_chunks_warp(len) : (mode == ATTN_STREAM ? attn_chunks_stream(len, hd, ipc) : attn_chunks(len, G, H));
+}
+
+// Stages per streamed attention item: the phase's stages spread over about six
+// items per CTA (fewer items, fewer per-item costs; enough of them to balance
+// the CTAs), at least ATTN_STAGES_PER_ITEM.  Every caller computes the same value.
+__device__ __forceinline__ int attn_stream_ipc(const StepDesc* D, int n, int W, int H, int hd, int G)
+{
+    const int kps = attn_stage_keys(hd);
+    long long st = 0;
+    for (int i = 0; i < n; ++i) {
+        const int p = D->pos[i];
+        st += ((p + 1 < W ? p + 1 : W) + kps - 1) / kps;
+    }
+    const long long want = (st * H + 6LL * G - 1) / (6LL * G);
+    return (int)(want < ATTN_STAGES_PER_ITEM ? ATTN_STAGES_PER_ITEM : (want > 4096 ? 4096 : want));
 }
 
 __device__ __forceinline__ void attn_item(const StepDesc* D, int n, int H, int W, int G, int item, int& i, int& h,
-                                          int& c, int& nch, int& len, int mode = ATTN_CTA, int hd = 0)
+                                          int& c, int& nch, int& len, int mode = ATTN_CTA, int hd = 0, int ipc = 0)
 {
     int base = 0;
     for (i = 0; i < n; ++i) {
         const int p = D->pos[i];
         len = p + 1 < W ? p + 1 : W;
-        nch = attn_nchunks(mode, len, G, H, hd);
+        nch = attn_nchunks(mode, len, G, H, hd, ipc);
         if (item < base + nch * H) break;
         base += nch * H;
     }
@@ -1827,11 +1841,12 @@ __device__ __forceinline__ void producer_mma(const Params& P, int ph0, int ph1, 
             // (read once: evict-first, like the weights)
             const StepDesc* D = P.desc;
             const int H = P.H, hd = P.hd, Wn = P.W, KPS = attn_stage_keys(hd);
+            const int ipc = attn_stream_ipc(D, n, Wn, H, hd, P.G);
             int total = 0;
-            for (int i = 0; i < n; ++i) total += attn_chunks_stream(D->pos[i] + 1 < Wn ? D->pos[i] + 1 : Wn, hd) * H;
+            for (int i = 0; i < n; ++i) total += attn_chunks_stream(D->pos[i] + 1 < Wn ? D->pos[i] + 1 : Wn, hd, ipc) * H;
             for (int item = blockIdx.x; item < total && ok; item += P.G) {
                 int i, h, ci, nch, len, k0, k1, kend, mcur;
-                attn_item(D, n, H, Wn, P.G, item, i, h, ci, nch, len, ATTN_STREAM, hd);
+                attn_item(D, n, H, Wn, P.G, item, i, h, ci, nch, len, ATTN_STREAM, hd, ipc);
                 attn_stream_range(D, i, len, ci, nch, k0, k1, kend, mcur);
                 const int start = D->pos[i] - len + 1;
                 const size_t hbase = (((size_t)D->slot[i] * P.L + q.l) * H + h) * (size_t)Wn * hd;
@@ -1840,6 +1855,10 @@ __device__ __forceinline__ void producer_mma(const Params& P, int ph0, int ph1, 
                     const int slot = (int)(s % MMA_NSTAGE);
                     if (!mbar_wait(&sm.sempty[slot], ((s / MMA_NSTAGE) & 1u) ^ 1u, P.err, WS_EMPTY)) { ok = false; break; }
                     const unsigned kbytes = (unsigned)(nk * hd * sizeof(TW));
+                    // the activation barrier's phase stays in step with the stage; it completes
+                    // before the copies are issued, so the consumers that see the keys land have
+                    // passed a completed phase of it too
+                    mbar_arrive(&sm.bfull[slot]);
                     mbar_expect_tx(&sm.wfull[slot], 2 * kbytes);
                     const int r0 = (start + kb) % Wn, n1 = min(nk, Wn - r0);
                     char* dst = sm.mring + (size_t)slot * MMA_STAGE;
@@ -1851,7 +1870,6 @@ __device__ __forceinline__ void producer_mma(const Params& P, int ph0, int ph1, 
                             bulk_g2s(dt + (size_t)n1 * hd * sizeof(TW), ring, (unsigned)((nk - n1) * hd * sizeof(TW)),
                                      &sm.wfull[slot], pol_w);
                     }
-                    mbar_arrive(&sm.bfull[slot]);  // the activation barrier's phase stays in step with the stage
                 }
             }
             continue;
@@ -1936,7 +1954,7 @@ __device__ __forceinline__ void mma_issuer(const Params& P, int ph0, int ph1, in
 {
     const int ncol = MMA_PARTS * mma_nbp(n);
     const uint32_t idesc = mma_idesc(ncol);
-    unsigned s = 0, uc = 0;  // stages, units
+    unsigned s = 0, uc = 0, na = 0;  // stages, units, attention phases
     bool ok = true;
     const int dep_end = P.dep_ph0 + n_groups(starts) * P.dep_ph_stride;
     const int dep_all = P.dep_ph0 + P.S * P.dep_ph_stride;
@@ -1950,25 +1968,22 @@ __device__ __forceinline__ void mma_issuer(const Params& P, int ph0, int ph1, in
         Phase q = P.phases[ph];
         if (!resolve(P, starts, q, c, cnt)) continue;
         if (q.type == PH_ATTN) {
-            // attention stages go to the consumers; their barrier phases are waited
-            // out in order, so that a later parity wait cannot match an older phase
+            // attention stages go to the consumers: count them, then wait until the consumers
+            // are past all of them (every stage's barrier phases complete), so that the next
+            // parity wait on a slot cannot match an older phase
             const StepDesc* D = P.desc;
             const int H = P.H, hd = P.hd, Wn = P.W, KPS = attn_stage_keys(hd);
+            const int ipc = attn_stream_ipc(D, n, Wn, H, hd, P.G);
             int total = 0;
-            for (int i = 0; i < n; ++i) total += attn_chunks_stream(D->pos[i] + 1 < Wn ? D->pos[i] + 1 : Wn, hd) * H;
-            for (int item = blockIdx.x; item < total && ok; item += P.G) {
+            for (int i = 0; i < n; ++i) total += attn_chunks_stream(D->pos[i] + 1 < Wn ? D->pos[i] + 1 : Wn, hd, ipc) * H;
+            for (int item = blockIdx.x; item < total; item += P.G) {
                 int i, h, ci, nch, len, k0, k1, kend, mcur;
-                attn_item(D, n, H, Wn, P.G, item, i, h, ci, nch, len, ATTN_STREAM, hd);
+                attn_item(D, n, H, Wn, P.G, item, i, h, ci, nch, len, ATTN_STREAM, hd, ipc);
                 attn_stream_range(D, i, len, ci, nch, k0, k1, kend, mcur);
-                for (int kb = k0; kb < kend; kb += KPS, ++s) {
-                    const int slot = (int)(s % MMA_NSTAGE);
-                    const unsigned par = (s / MMA_NSTAGE) & 1u;
-                    if (!mbar_wait(&sm.wfull[slot], par, P.err, WS_FULL) || !mbar_wait(&sm.bfull[slot], par, P.err, WS_FULL)) {
-                        ok = false;
-                        break;
-                    }
-                }
+                if (kend > k0) s += (unsigned)((kend - k0 + KPS - 1) / KPS);
             }
+            if (!mbar_wait(sm.adone, na & 1u, P.err, WS_FULL)) ok = false;
+            ++na;
             continue;
         }
         if (!phase_matrix<TW>(P, q, W, M, K)) continue;
@@ -2846,13 +2861,18 @@ __device__ __noinline__ bool phase_attn_warp(const Params& P, int l, int n, unsi
 }
 
 // Attention of the tensor-core instantiation with keys and values streamed by the
-// producer warp: one CTA per item (batch row, head, chunk of up to 7 stages).
-// A stage holds up to attn_stage_keys(hd) keys, then as many values, bf16, copied
-// from the head-major ring; the eight warps take the stage's keys two at a time
-// (16 lanes per key), keep an online softmax per lane, release the stage, and at
-// the end of the item merge in warp order.  This launch's keys (the current one,
-// and a prompt chunk's earlier rows) come from the tagged copies.  Chunks merge
-// as in phase_attn.
+// producer warp: one CTA per item (batch row, head, chunk of the window; about six
+// items per CTA).  A stage holds up to attn_stage_keys(hd) keys, then as many values,
+// bf16, copied from the head-major ring.  A key belongs to a group of hd / 8 lanes
+// (8 elements each, so a warp reads 512 contiguous bytes at once); a stage is
+// ATTN_R passes, and a lane group's ATTN_R partial scores are reduced together
+// (each butterfly level halves the values a lane carries), then broadcast.  Scores
+// carry a factor log2(e), so the softmax runs on exp2; a group rescales its sums
+// only when a stage raises its maximum.  At the end of an item the groups, then the
+// warps, merge in order.  This launch's keys (the current one, and a prompt chunk's
+// earlier rows) come from the tagged copies.  Chunks merge as in phase_attn.
+constexpr int ATTN_R = 4;  // passes per stage: ATTN_R x NWARP x (256 / hd) >= attn_stage_keys(hd)
+
 template <typename TKV>
 __device__ __noinline__ bool phase_attn_stream(const Params& P, int l, int n, unsigned in_tag, unsigned tag, const Smem& sm,
                                                unsigned& stage)
@@ -2860,46 +2880,59 @@ __device__ __noinline__ bool phase_attn_stream(const Params& P, int l, int n, un
     const StepDesc* D = P.desc;
     const int H = P.H, hd = P.hd, d = P.d, W = P.W;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int LPP = hd / 8, PPI = 32 / LPP;
+    const int LPP = hd / 8, PPI = 32 / LPP;  // lanes per key, keys per warp and pass
     const int grp = lane / LPP, gl = lane % LPP;
     const int KPS = attn_stage_keys(hd);
-    const float scale = rsqrtf((float)hd);
+    const float scale = 1.4426950408889634f * rsqrtf((float)hd);  // log2(e) / sqrt(hd)
     const int wstride = hd + 4;
     const size_t pstride = (size_t)hd + 2;
+    const int ipc = attn_stream_ipc(D, n, W, H, hd, P.G);
     int total = 0;
     for (int i = 0; i < n; ++i) {
         const int p = D->pos[i];
-        total += attn_chunks_stream(p + 1 < W ? p + 1 : W, hd) * H;
+        total += attn_chunks_stream(p + 1 < W ? p + 1 : W, hd, ipc) * H;
     }
     int ok = 1;
     for (int item = blockIdx.x; item < total; item += P.G) {
         int i, h, c, nch, len;
-        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, ATTN_STREAM, hd);
+        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, ATTN_STREAM, hd, ipc);
         int k0, k1, kend, mcur;
         attn_stream_range(D, i, len, c, nch, k0, k1, kend, mcur);
-        const size_t qo = (size_t)i * d + h * hd + gl * 8;
-        float qv[8];
-        uint2 qt[8];
-        tag8_issue(P.q + qo, qt);
-        if (!tag8_take(qt, P.q + qo, in_tag, qv, P.err)) ok = 0;
+        float qv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (ok && !wait_tag8(P.q + (size_t)i * d + h * hd + gl * 8, in_tag, qv, P.err)) ok = 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e) qv[e] *= scale;
         float m = -INFINITY, lsum = 0.f, acc[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-        // one key of the lane group: score, then the running softmax update
-        auto take = [&](const float kf[8], const float vf[8], bool valid) {
-            float t = 0.f;
+        // the lane's 8-element share of q.k (two chains)
+        auto dot8 = [&](const uint4& k) {
+            float2 t2 = make_float2(0.f, 0.f);
+            ffma2(t2, qv[0], qv[1], bf_lo(k.x), bf_hi(k.x));
+            ffma2(t2, qv[2], qv[3], bf_lo(k.y), bf_hi(k.y));
+            ffma2(t2, qv[4], qv[5], bf_lo(k.z), bf_hi(k.z));
+            ffma2(t2, qv[6], qv[7], bf_lo(k.w), bf_hi(k.w));
+            return t2.x + t2.y;
+        };
+        auto addv = [&](float pu, const uint4& v) {
+            float2 a0 = make_float2(acc[0], acc[1]), a1 = make_float2(acc[2], acc[3]);
+            float2 a2 = make_float2(acc[4], acc[5]), a3 = make_float2(acc[6], acc[7]);
+            ffma2(a0, pu, pu, bf_lo(v.x), bf_hi(v.x));
+            ffma2(a1, pu, pu, bf_lo(v.y), bf_hi(v.y));
+            ffma2(a2, pu, pu, bf_lo(v.z), bf_hi(v.z));
+            ffma2(a3, pu, pu, bf_lo(v.w), bf_hi(v.w));
+            acc[0] = a0.x; acc[1] = a0.y; acc[2] = a1.x; acc[3] = a1.y;
+            acc[4] = a2.x; acc[5] = a2.y; acc[6] = a3.x; acc[7] = a3.y;
+        };
+        // raise the group's maximum to mn (rescaling its sums) if mn is above it
+        auto raise = [&](float mn) {
+            if (mn > m) {
+                const float corr = exp2f(m - mn);
+                lsum *= corr;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) t = fmaf(qv[e], kf[e], t);
-            for (int o = LPP / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-            if (!valid) return;
-            const float mn = fmaxf(m, t);
-            const float corr = expf(m - mn), pu = expf(t - mn);
-            lsum = lsum * corr + pu;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = fmaf(pu, vf[e], acc[e] * corr);
-            m = mn;
+                for (int e = 0; e < 8; ++e) acc[e] *= corr;
+                m = mn;
+            }
         };
         // streamed keys, stage by stage (every warp passes every stage's barrier, also
         // after a failed wait, so that no barrier waits for a warp that has left)
@@ -2910,45 +2943,38 @@ __device__ __noinline__ bool phase_attn_stream(const Params& P, int l, int n, un
             if (__all_sync(0xffffffffu, ok)) {
                 const __nv_bfloat16* ks = (const __nv_bfloat16*)(sm.mring + (size_t)slot * MMA_STAGE);
                 const __nv_bfloat16* vs = ks + (size_t)KPS * hd;
-                // the lane group's keys of the stage (up to ATTN_R), loaded together; their
-                // scores, then one rescale of the running sums for the group
-                for (int kk0 = 0; kk0 < nk; kk0 += ATTN_R * NWARP * PPI) {  // warp-uniform trip count
-                    uint4 kr[ATTN_R], vr[ATTN_R];
+                uint4 kr[ATTN_R], vr[ATTN_R];
+                float t[ATTN_R];
 #pragma unroll
-                    for (int r = 0; r < ATTN_R; ++r) {
-                        const int kk = kk0 + r * NWARP * PPI + warp * PPI + grp;
-                        const size_t off = (size_t)(kk < nk ? kk : 0) * hd + gl * 8;
-                        kr[r] = *reinterpret_cast<const uint4*>(ks + off);
-                        vr[r] = *reinterpret_cast<const uint4*>(vs + off);
-                    }
-                    float sc[ATTN_R], mn = m;
+                for (int r = 0; r < ATTN_R; ++r) {
+                    const int kk = r * NWARP * PPI + warp * PPI + grp;
+                    const size_t off = (size_t)(kk < nk ? kk : 0) * hd + gl * 8;
+                    kr[r] = *reinterpret_cast<const uint4*>(ks + off);
+                    vr[r] = *reinterpret_cast<const uint4*>(vs + off);
+                }
 #pragma unroll
-                    for (int r = 0; r < ATTN_R; ++r) {
-                        const float kf[8] = {bf_lo(kr[r].x), bf_hi(kr[r].x), bf_lo(kr[r].y), bf_hi(kr[r].y),
-                                             bf_lo(kr[r].z), bf_hi(kr[r].z), bf_lo(kr[r].w), bf_hi(kr[r].w)};
-                        float t = 0.f;
+                for (int r = 0; r < ATTN_R; ++r) t[r] = dot8(kr[r]);
+                // reduce the four partial scores over the group: lane gl ends with key
+                // 2 [gl & LPP/2] + [gl & LPP/4], then every lane takes all four
+                const bool hi1 = (gl & (LPP / 2)) != 0, hi2 = (gl & (LPP / 4)) != 0;
+                const float u0 = (hi1 ? t[2] : t[0]) + __shfl_xor_sync(0xffffffffu, hi1 ? t[0] : t[2], LPP / 2);
+                const float u1 = (hi1 ? t[3] : t[1]) + __shfl_xor_sync(0xffffffffu, hi1 ? t[1] : t[3], LPP / 2);
+                float sk = (hi2 ? u1 : u0) + __shfl_xor_sync(0xffffffffu, hi2 ? u0 : u1, LPP / 4);
+                for (int o = LPP / 8; o > 0; o >>= 1) sk += __shfl_xor_sync(0xffffffffu, sk, o);
+                float sc[ATTN_R], mn = m;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) t = fmaf(qv[e], kf[e], t);
-                        for (int o = LPP / 2; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-                        sc[r] = kk0 + r * NWARP * PPI + warp * PPI + grp < nk ? t : -INFINITY;
-                        mn = fmaxf(mn, sc[r]);
-                    }
-                    if (mn != -INFINITY) {
-                        const float corr = expf(m - mn);
-                        lsum *= corr;
+                for (int r = 0; r < ATTN_R; ++r) {
+                    const int src = grp * LPP + (r >> 1) * (LPP / 2) + (r & 1) * (LPP / 4);
+                    const float v = __shfl_sync(0xffffffffu, sk, src);
+                    sc[r] = r * NWARP * PPI + warp * PPI + grp < nk ? v : -INFINITY;
+                    mn = fmaxf(mn, sc[r]);
+                }
+                raise(mn);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[e] *= corr;
-#pragma unroll
-                        for (int r = 0; r < ATTN_R; ++r) {
-                            const float pu = expf(sc[r] - mn);
-                            lsum += pu;
-                            const float vf[8] = {bf_lo(vr[r].x), bf_hi(vr[r].x), bf_lo(vr[r].y), bf_hi(vr[r].y),
-                                                 bf_lo(vr[r].z), bf_hi(vr[r].z), bf_lo(vr[r].w), bf_hi(vr[r].w)};
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) acc[e] = fmaf(pu, vf[e], acc[e]);
-                        }
-                        m = mn;
-                    }
+                for (int r = 0; r < ATTN_R; ++r) {
+                    const float pu = sc[r] == -INFINITY ? 0.f : exp2f(sc[r] - m);  // a key past the stage adds 0
+                    lsum += pu;
+                    addv(pu, vr[r]);
                 }
             } else {
                 ok = 0;
@@ -2967,7 +2993,16 @@ __device__ __noinline__ bool phase_attn_stream(const Params& P, int l, int n, un
                 const size_t ro = (size_t)(i - (len - 1 - j)) * d + h * hd + gl * 8;
                 ok = wait_tag8(P.kcur + ro, in_tag, kf, P.err) && wait_tag8(P.vcur + ro, in_tag, vf, P.err);
             }
-            take(kf, vf, j < k1);
+            // the tagged copies hold values already rounded to bf16: they pack exactly
+            const uint4 kp = KV<__nv_bfloat16>::pack(kf).a, vp = KV<__nv_bfloat16>::pack(vf).a;
+            float tk = dot8(kp);
+            for (int o = LPP / 2; o > 0; o >>= 1) tk += __shfl_xor_sync(0xffffffffu, tk, o);
+            if (j < k1) {
+                raise(tk);
+                const float pu = exp2f(tk - m);
+                lsum += pu;
+                addv(pu, vp);
+            }
         }
         // merge the key groups of the warp, then the warps in warp order
         for (int o = LPP; o < 32; o <<= 1) {
@@ -2977,8 +3012,8 @@ __device__ __noinline__ bool phase_attn_stream(const Params& P, int l, int n, un
 #pragma unroll
             for (int e = 0; e < 8; ++e) a2[e] = __shfl_xor_sync(0xffffffffu, acc[e], o);
             const float M = fmaxf(m, m2);
-            const float c1 = m == -INFINITY ? 0.f : expf(m - M);
-            const float c2 = m2 == -INFINITY ? 0.f : expf(m2 - M);
+            const float c1 = m == -INFINITY ? 0.f : exp2f(m - M);
+            const float c2 = m2 == -INFINITY ? 0.f : exp2f(m2 - M);
             lsum = lsum * c1 + l2 * c2;
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[e] = acc[e] * c1 + a2[e] * c2;
@@ -2999,7 +3034,7 @@ __device__ __noinline__ bool phase_attn_stream(const Params& P, int l, int n, un
             for (int w = 0; w < NWARP; ++w) {
                 const float mw = sm.wbuf[(size_t)w * wstride];
                 if (mw == -INFINITY) continue;
-                const float f = expf(mw - M);
+                const float f = exp2f(mw - M);
                 L += sm.wbuf[(size_t)w * wstride + 1] * f;
                 a += sm.wbuf[(size_t)w * wstride + 4 + e] * f;
             }
@@ -3016,10 +3051,12 @@ __device__ __noinline__ bool phase_attn_stream(const Params& P, int l, int n, un
         csync();
     }
     if (!csync_and(ok)) return false;
+    // every stage of the phase is consumed: the MMA warp may go on to the next phase's stages
+    if (threadIdx.x == 0) mbar_arrive(sm.adone);
     // merges: the CTA that ran chunk 0 of a split window combines its chunks in order
     for (int item = blockIdx.x; item < total; item += P.G) {
         int i, h, c, nch, len;
-        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, ATTN_STREAM, hd);
+        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, ATTN_STREAM, hd, ipc);
         if (c != 0 || nch == 1) continue;
         const uint2* part = P.attp + ((size_t)i * H + h) * NCHUNK_MAX * pstride;
         float* mb = sm.wbuf;  // [nch][hd + 2]
@@ -3047,7 +3084,7 @@ __device__ __noinline__ bool phase_attn_stream(const Params& P, int l, int n, un
             for (int k = 0; k < nch; ++k) {
                 const float mk = mb[k * pstride];
                 if (mk == -INFINITY) continue;
-                const float f = expf(mk - M);
+                const float f = exp2f(mk - M);  // maxima carry the factor log2(e)
                 L += mb[k * pstride + 1] * f;
                 a += mb[k * pstride + 2 + e] * f;
             }
@@ -3329,6 +3366,7 @@ __global__ void __launch_bounds__(is_mma(BG) ? MMA_THREADS : NT + 32, 1) step_ke
                 mbar_init(&sm.tfree[k], NWARP);  // every consumer warp has read the unit's slot
             }
             mbar_init(sm.mdone, 1);
+            mbar_init(sm.adone, 1);
         } else {
             for (int k = 0; k < (int)nstage_for(BG); ++k) {
                 mbar_init(&sm.full[k], 1);

@@ -6,13 +6,14 @@
 // tensor cores (tcgen05.mma, bf16 operands, fp32 accumulation): the codebook
 // and the residuals are each split into a bf16 high part and the bf16 rounding
 // of the rest, and the products hi.hi + hi.lo + lo.hi + lo.lo keep about 16
-// significant bits, enough to pick candidates.  Each frame keeps its best 32
-// candidates by that score; their exact fp32 distances are then computed in
-// the order of the CUDA-core kernel (mfs_rvq.cu: float4 chunks, one fmaf per
-// component), and the smallest wins, lower index on ties.  So the code equals
-// the CUDA-core kernel's whenever the nearest codeword is among the 32, i.e.
-// unless more than 31 codewords lie within the score error (about 1e-4 of
-// |r| |c|) of the nearest.
+// significant bits (score error a few 1e-5 of sum_i |r_i c_i|), enough to pick
+// candidates.  Each frame's 8 best codewords by that score are then re-ranked
+// by their exact fp32 distances, computed in the order of the CUDA-core kernel
+// (mfs_rvq.cu: float4 chunks, one fmaf per component); the smallest wins,
+// lower index on ties.  So the code equals the CUDA-core kernel's whenever the
+// nearest codeword is among the 8, i.e. unless more than 7 codewords score
+// within that error of the nearest (identical codewords score identically and
+// keep the lower index first, so exact duplicates cannot push it out).
 //
 // A CTA takes 16 frames through all 8 stages.  Warp 4 (one lane) loads
 // codebook tiles (128 codewords x 64 dimensions, high and low parts) with 2-D
@@ -44,8 +45,12 @@ constexpr int RQ_TILE = RQ_CW * RQ_KC * 2;  // 16 KB: one part of a codebook til
 constexpr int RQ_STAGE = 2 * RQ_TILE;       // high and low parts
 constexpr int RQ_CONS = 128;         // consumer threads (warps 0-3)
 constexpr int RQ_THREADS = RQ_CONS + 64;
-constexpr int RQ_KEEP = 4;           // candidates per thread; 8 threads per frame: 32 per frame
-constexpr int RQ_NCOL = 64;          // accumulator columns: [A_hi x (B_hi | B_lo) | A_lo x (B_hi | B_lo)]
+constexpr int RQ_KEEP = 8;           // best codewords kept per sub-list (8 sub-lists, one thread each, per frame)
+constexpr int RQ_CAND = 8;           // of those, the frame's best 8 are re-ranked exactly (one per thread)
+constexpr int RQ_NCOL = 64;          // accumulator block: [A_hi x (B_hi | B_lo) | A_lo x (B_hi | B_lo)] columns
+constexpr int RQ_NSPLIT = 1;         // blocks per accumulator: chunk kc accumulates into block kc % RQ_NSPLIT
+constexpr int RQ_NACC = 2;           // accumulators (codeword tiles in flight between the MMAs and the consumers)
+constexpr int RQ_TMEM = RQ_NACC * RQ_NSPLIT * RQ_NCOL;  // tensor-memory columns (a power of 2, 32..512)
 constexpr int RQ_SCS = RQ_CW + 8;    // score row stride: the candidate scan's 32 lanes hit 32 banks
 constexpr int RQ_MAXST = 6;          // ring stages at most
 constexpr unsigned long long RQ_WAIT_NS = 2000000000ull;
@@ -75,16 +80,22 @@ __device__ __forceinline__ unsigned long long gtime()
 }
 
 // Bounded wait for the phase of parity `par`; false (and the error flag set) on timeout.
+// The error flag and the clock are looked at every 256 polls (a global load per poll
+// would put its latency on every hand-off).
 __device__ __forceinline__ bool bar_wait(uint64_t* b, unsigned par, int* flag)
 {
-    const unsigned long long t0 = gtime();
-    for (;;) {
+    unsigned long long t0 = 0;
+    for (unsigned n = 0;; ++n) {
         unsigned ok;
         asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
                      : "=r"(ok) : "r"(su32(b)), "r"(par) : "memory");
         if (ok) return true;
+        if ((n & 255u) != 255u) continue;
         if (*(volatile int*)flag) return false;
-        if (gtime() - t0 > RQ_WAIT_NS) {
+        const unsigned long long t = gtime();
+        if (t0 == 0) {
+            t0 = t;
+        } else if (t - t0 > RQ_WAIT_NS) {
             atomicExch(flag, 1);
             return false;
         }
@@ -155,7 +166,7 @@ __global__ void rq_split(const float* __restrict__ cb, long long n, int D, __nv_
 }
 
 struct RqSmem {
-    uint64_t full[RQ_MAXST], empty[RQ_MAXST], accf[2], accfree[2], bready, mdone;
+    uint64_t full[RQ_MAXST], empty[RQ_MAXST], accf[RQ_NACC], accfree[RQ_NACC], bready, mdone;
     uint32_t tslot;
 };
 
@@ -184,7 +195,7 @@ __global__ void __launch_bounds__(RQ_THREADS, 1) rq_kernel(const __grid_constant
             bar_init(&H->full[k], 1);
             bar_init(&H->empty[k], 1);
         }
-        for (int k = 0; k < 2; ++k) {
+        for (int k = 0; k < RQ_NACC; ++k) {
             bar_init(&H->accf[k], 1);
             bar_init(&H->accfree[k], 4);  // one arrival per consumer warp
         }
@@ -193,7 +204,7 @@ __global__ void __launch_bounds__(RQ_THREADS, 1) rq_kernel(const __grid_constant
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 5) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&H->tslot)), "r"(2u * RQ_NCOL) : "memory");
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(&H->tslot)), "r"((unsigned)RQ_TMEM) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
     fence_before();
@@ -233,7 +244,8 @@ __global__ void __launch_bounds__(RQ_THREADS, 1) rq_kernel(const __grid_constant
         return;
     }
     if (warp == 5) {
-        // MMA: per tile, two accumulators alternate; per chunk 4 K-steps x (A_hi, A_lo) x B (hi | lo rows)
+        // MMA: tiles take the accumulators in turn; per chunk 4 K-steps x (A_hi, A_lo) x B (hi | lo rows)
+        // into block kc % RQ_NSPLIT of the tile's accumulator
         if (lane == 0) {
             const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(32 >> 3) << 17) | ((uint32_t)(RQ_CW >> 4) << 24);
             unsigned s = 0, tcount = 0;
@@ -241,11 +253,11 @@ __global__ void __launch_bounds__(RQ_THREADS, 1) rq_kernel(const __grid_constant
             for (int q = 0; q < 8 && ok; ++q) {
                 if (!bar_wait(&H->bready, (unsigned)q & 1u, flag)) { ok = false; break; }
                 for (int ct = 0; ct < CT && ok; ++ct, ++tcount) {
-                    const int ab = (int)(tcount & 1u);
-                    if (!bar_wait(&H->accfree[ab], ((tcount >> 1) & 1u) ^ 1u, flag)) { ok = false; break; }
+                    const int ab = (int)(tcount % RQ_NACC);
+                    if (!bar_wait(&H->accfree[ab], ((tcount / RQ_NACC) & 1u) ^ 1u, flag)) { ok = false; break; }
                     fence_after();
-                    const uint32_t d = tbase + (uint32_t)(ab * RQ_NCOL);
                     for (int kc = 0; kc < KC; ++kc, ++s) {
+                        const uint32_t d = tbase + (uint32_t)((ab * RQ_NSPLIT + kc % RQ_NSPLIT) * RQ_NCOL);
                         const int slot = (int)(s % nst);
                         if (!bar_wait(&H->full[slot], (s / nst) & 1u, flag)) { ok = false; break; }
                         fence_after();
@@ -253,7 +265,7 @@ __global__ void __launch_bounds__(RQ_THREADS, 1) rq_kernel(const __grid_constant
                         const uint64_t ahi = sw128(sa), alo = sw128(sa + RQ_TILE), bd = sw128(su32(panel + (size_t)kc * 4096));
 #pragma unroll
                         for (int kk = 0; kk < RQ_KC / 16; ++kk) {
-                            const uint32_t acc = (kc > 0 || kk > 0) ? 1u : 0u;
+                            const uint32_t acc = (kc >= RQ_NSPLIT || kk > 0) ? 1u : 0u;
                             mma(d, ahi + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, acc);
                             mma(d + 32, alo + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, acc);
                         }
@@ -276,13 +288,14 @@ __global__ void __launch_bounds__(RQ_THREADS, 1) rq_kernel(const __grid_constant
         __syncwarp();
         asm volatile("bar.sync 1, %0;" ::"n"(RQ_CONS + 32) : "memory");
         fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(2u * RQ_NCOL) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"((unsigned)RQ_TMEM) : "memory");
         return;
     }
 
     // consumers (warps 0-3): tensor-memory lane = codeword of the tile = 32 warp + lane
     const int D4 = D / 4;
     const int f8 = tid >> 3, s8 = tid & 7;  // candidate lists: frame f8 (< 16), sub-list s8
+    const int nsb = KC < RQ_NSPLIT ? KC : RQ_NSPLIT;  // blocks of an accumulator in use
     unsigned tcount = 0;
     int ok = 1;
     for (int q = 0; q < 8; ++q) {
@@ -322,15 +335,30 @@ __global__ void __launch_bounds__(RQ_THREADS, 1) rq_kernel(const __grid_constant
 #pragma unroll
         for (int k = 0; k < RQ_KEEP; ++k) { cs[k] = INFINITY; ci[k] = 0x7fffffff; }
         for (int ct = 0; ct < CT; ++ct, ++tcount) {
-            const int ab = (int)(tcount & 1u);
-            if (ok && !bar_wait(&H->accf[ab], (tcount >> 1) & 1u, flag)) ok = 0;
+            const int ab = (int)(tcount % RQ_NACC);
+            if (ok && !bar_wait(&H->accf[ab], (tcount / RQ_NACC) & 1u, flag)) ok = 0;
             fence_after();
             float v0[16], v1[16], v2[16], v3[16];
-            const uint32_t ta = tbase + ((uint32_t)(32 * warp) << 16) + (uint32_t)(ab * RQ_NCOL);
+            const uint32_t ta = tbase + ((uint32_t)(32 * warp) << 16) + (uint32_t)(ab * RQ_NSPLIT * RQ_NCOL);
             tld16(ta, v0);       // A_hi x B_hi
             tld16(ta + 16, v1);  // A_hi x B_lo
             tld16(ta + 32, v2);  // A_lo x B_hi
             tld16(ta + 48, v3);  // A_lo x B_lo
+            for (int b = 1; b < nsb; ++b) {  // the other blocks of the tile's K
+                float w[16];
+                tld16(ta + b * RQ_NCOL, w);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v0[e] += w[e];
+                tld16(ta + b * RQ_NCOL + 16, w);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v1[e] += w[e];
+                tld16(ta + b * RQ_NCOL + 32, w);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v2[e] += w[e];
+                tld16(ta + b * RQ_NCOL + 48, w);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v3[e] += w[e];
+            }
             fence_before();
             __syncwarp();
             if (lane == 0) bar_arrive(&H->accfree[ab]);
@@ -356,39 +384,46 @@ __global__ void __launch_bounds__(RQ_THREADS, 1) rq_kernel(const __grid_constant
             }
             asm volatile("bar.sync 2, %0;" ::"n"(RQ_CONS) : "memory");
         }
-        // exact re-rank of the frame's 32 candidates (the CUDA-core kernel's arithmetic:
-        // float4 chunks in order, one fmaf per component); the four chains interleave
+        // the frame's best RQ_CAND codewords by score over its 8 sub-lists (a tournament over
+        // the lanes' sorted lists; codeword indices differ between sub-lists), one per lane
+        int mine = 0x7fffffff;
+#pragma unroll
+        for (int k = 0; k < RQ_CAND; ++k) {
+            float bv = cs[0];
+            int bx = ci[0];
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int i2 = __shfl_xor_sync(0xffffffffu, bx, o);
+                if (cbetter(v2, i2, bv, bx)) { bv = v2; bx = i2; }
+            }
+            if (s8 == k) mine = bx;
+            if (bx == ci[0] && bx != 0x7fffffff) {  // this lane's head won: pop it
+#pragma unroll
+                for (int m = 0; m < RQ_KEEP - 1; ++m) { cs[m] = cs[m + 1]; ci[m] = ci[m + 1]; }
+                cs[RQ_KEEP - 1] = INFINITY;
+                ci[RQ_KEEP - 1] = 0x7fffffff;
+            }
+        }
+        // exact fp32 distance of the lane's candidate (the CUDA-core kernel's arithmetic: float4
+        // chunks in order, one fmaf per component), then the least over the frame's lanes
         const float4* book = reinterpret_cast<const float4*>(cb + (size_t)q * Cb * D);
         const float4* r4 = reinterpret_cast<const float4*>(res + (size_t)f8 * D);
-        const float4* rows[RQ_KEEP];
-        float acc[RQ_KEEP];
-#pragma unroll
-        for (int k = 0; k < RQ_KEEP; ++k) {
-            rows[k] = book + (size_t)(ci[k] < Cb ? ci[k] : 0) * D4;
-            acc[k] = 0.f;
-        }
+        const float4* row = book + (size_t)(mine < Cb ? mine : 0) * D4;
+        float acc = 0.f;
+#pragma unroll 8
         for (int e = 0; e < D4; ++e) {
-            const float4 x = r4[e];
-#pragma unroll
-            for (int k = 0; k < RQ_KEEP; ++k) {
-                const float4 w = __ldg(rows[k] + e);
-                const float a = x.x - w.x, b = x.y - w.y, c2 = x.z - w.z, d2 = x.w - w.w;
-                acc[k] = fmaf(a, a, acc[k]);
-                acc[k] = fmaf(b, b, acc[k]);
-                acc[k] = fmaf(c2, c2, acc[k]);
-                acc[k] = fmaf(d2, d2, acc[k]);
-            }
+            const float4 w = __ldg(row + e), x = r4[e];
+            const float a = x.x - w.x, b = x.y - w.y, c2 = x.z - w.z, d2 = x.w - w.w;
+            acc = fmaf(a, a, acc);
+            acc = fmaf(b, b, acc);
+            acc = fmaf(c2, c2, acc);
+            acc = fmaf(d2, d2, acc);
         }
-        float bd = INFINITY;
-        int bi = 0x7fffffff;
+        float bd = mine < Cb ? acc : INFINITY;
+        int bi = mine < Cb ? mine : 0x7fffffff;
 #pragma unroll
-        for (int k = 0; k < RQ_KEEP; ++k)
-            if (ci[k] < Cb && cbetter(acc[k], ci[k], bd, bi)) {
-                bd = acc[k];
-                bi = ci[k];
-            }
-#pragma unroll
-        for (int o = 1; o < 8; o <<= 1) {  // the frame's 8 sub-lists (lanes of one 8-lane group)
+        for (int o = 1; o < 8; o <<= 1) {  // the frame's 8 lanes
             const float v2 = __shfl_xor_sync(0xffffffffu, bd, o);
             const int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
             if (cbetter(v2, i2, bd, bi)) { bd = v2; bi = i2; }

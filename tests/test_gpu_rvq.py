@@ -76,7 +76,7 @@ def test_rvq_matches_oracle(mfs, T, D, Cb):
 def test_rvq_clustered_codebooks(mfs):
     """Codebooks of 64 clusters of 48 close codewords (member m of cluster g at index 64 m + g, so
     a cluster spans every codeword tile and every candidate sub-list), latents near cluster
-    centres: the nearest codeword has 47 close rivals, more than the 32 candidates the
+    centres: the nearest codeword has 47 close rivals, more than the 8 candidates the
     tensor-core path re-ranks, yet it must still be found."""
     T, D, G, M = 64, 256, 64, 48
     Cb = G * M
