@@ -736,10 +736,12 @@ static int launch(mfs_ctx* c, int n, int nph, const StepDesc* desc)
         ev1 = c->ev_pool[c->ev_used + 1];
         c->ev_used += 2;
     }
-    // With the tensor-core pass, the depformer phases (small matrices, one dependent
-    // phase after another) run on the CUDA-core instantiation in groups of 4 rows, as a
-    // second launch: [0, dep_ph0) tensor cores, [dep_ph0, nph) CUDA cores.
-    const int split = (bi == 3 && nph > c->P.dep_ph0) ? c->P.dep_ph0 : nph;
+    // With the tensor-core pass and up to DEP_GEMV_MAX_ROWS rows, the depformer phases
+    // (small matrices, one dependent phase after another) run on the CUDA-core
+    // instantiation in groups of 4 rows, as a second launch: [0, dep_ph0) tensor cores,
+    // [dep_ph0, nph) CUDA cores.  Above that the groups of 4 cost more passes than the
+    // tensor-core phases' hand-offs, and one launch runs every phase.
+    const int split = (bi == 3 && nph > c->P.dep_ph0 && n <= DEP_GEMV_MAX_ROWS) ? c->P.dep_ph0 : nph;
     if (c->mode == 0) {
         int ph0 = 0, ph1 = split;
         void* args[] = {&P, &ph0, &ph1, &maxrows};

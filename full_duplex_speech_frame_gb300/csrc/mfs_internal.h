@@ -119,6 +119,9 @@ struct StepDesc {
     int codes[MFS_MAX_SLOTS][NSTREAM];
 };
 constexpr int PROMPT_ROWS = 32;  // rows of a prompt chunk at most (one tensor-core pass)
+// Batched steps of at most this many rows run the depformer on the CUDA-core
+// instantiation (second launch); larger ones keep it on the tensor-core pass.
+constexpr int DEP_GEMV_MAX_ROWS = 8;
 
 enum DeviceError : int { DERR_NONE = 0, DERR_TOKEN = 1, DERR_WAIT = 2 };
 

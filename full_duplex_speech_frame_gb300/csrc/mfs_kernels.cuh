@@ -385,10 +385,11 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* b)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(b)) : "memory");
 }
 
+// test_wait: a poll that never suspends the thread (waiters see a completed phase at once)
 __device__ __forceinline__ bool mbar_try(uint64_t* b, unsigned parity)
 {
     unsigned ok;
-    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+    asm volatile("{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
                  : "=r"(ok) : "r"(smem_u32(b)), "r"(parity) : "memory");
     return ok != 0;
 }
@@ -2235,38 +2236,6 @@ __device__ __noinline__ bool mma_phase(const Params& P, const Phase& ph, int phi
     }
     if (!csync_and(ok)) return false;
     if (P.ptime) stamp(P, sm.misc[0], 1);
-    // RMSNorm factor per batch row from the chunks' sums of squares (8 threads per
-    // row take every 8th chunk, then a fixed reduction: the same for every tile)
-    if (xs.g) {
-        float tq = 0.f;
-        if (active) {
-            const uint2* ps = P.pssq + pbase * 32 + b;
-            for (int k0 = c16; k0 < mp.KC && ok; k0 += 64) {
-                uint2 v[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int kc = k0 + 8 * e;
-                    v[e] = make_uint2(0u, tag);
-                    if (kc < mp.KC) v[e] = ld_tag1(ps + (size_t)kc * 32);
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int kc = k0 + 8 * e;
-                    if (kc < mp.KC) {
-                        unsigned bits = v[e].x;
-                        if (v[e].y != tag && ok) ok = wait_tag1(ps + (size_t)kc * 32, tag, bits, P.err);
-                        tq += __uint_as_float(bits);
-                    }
-                }
-            }
-        }
-        tq += __shfl_xor_sync(0xffffffffu, tq, 1);
-        tq += __shfl_xor_sync(0xffffffffu, tq, 2);
-        tq += __shfl_xor_sync(0xffffffffu, tq, 4);
-        if (active && c16 == 0) sm.ssq[b] = rsqrtf(tq / (float)K + P.eps);
-    }
-    if (!csync_and(ok)) return false;
-    if (P.ptime) stamp(P, sm.misc[0], 2);
     const int row = 32 * (warp & 3) + lane;  // this thread's tile row
     const int bh = (warp >> 2) * (nbp / 2);  // and its first batch row
     const int nh = nbp / 2;
@@ -2314,6 +2283,39 @@ __device__ __noinline__ bool mma_phase(const Params& P, const Phase& ph, int phi
         epi.dv = sm.bestv;
         epi.di = sm.besti;
     }
+    // RMSNorm factor per batch row from the chunks' sums of squares (8 threads per
+    // row take every 8th chunk, then a fixed reduction: the same for every tile).
+    // Only the owners of tiles need it, after their units: the MMAs do not wait for it.
+    if (xs.g && nown > 0) {
+        float tq = 0.f;
+        if (active) {
+            const uint2* ps = P.pssq + pbase * 32 + b;
+            for (int k0 = c16; k0 < mp.KC && ok; k0 += 64) {
+                uint2 v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int kc = k0 + 8 * e;
+                    v[e] = make_uint2(0u, tag);
+                    if (kc < mp.KC) v[e] = ld_tag1(ps + (size_t)kc * 32);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int kc = k0 + 8 * e;
+                    if (kc < mp.KC) {
+                        unsigned bits = v[e].x;
+                        if (v[e].y != tag && ok) ok = wait_tag1(ps + (size_t)kc * 32, tag, bits, P.err);
+                        tq += __uint_as_float(bits);
+                    }
+                }
+            }
+        }
+        tq += __shfl_xor_sync(0xffffffffu, tq, 1);
+        tq += __shfl_xor_sync(0xffffffffu, tq, 2);
+        tq += __shfl_xor_sync(0xffffffffu, tq, 4);
+        if (active && c16 == 0) sm.ssq[b] = rsqrtf(tq / (float)K + P.eps);
+    }
+    if (!csync_and(ok)) return false;
+    if (P.ptime) stamp(P, sm.misc[0], 2);
     if (nown > 0) {
         if (is_logits && tid < n) {
             sm.bestv[tid] = -INFINITY;

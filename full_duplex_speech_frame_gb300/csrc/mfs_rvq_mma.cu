@@ -335,6 +335,8 @@ __global__ void __launch_bounds__(RQ_THREADS, 1) rq_kernel(const __grid_constant
 #pragma unroll
         for (int k = 0; k < RQ_KEEP; ++k) { cs[k] = INFINITY; ci[k] = 0x7fffffff; }
         for (int ct = 0; ct < CT; ++ct, ++tcount) {
+            const int c = ct * RQ_CW + 32 * warp + lane;
+            const float nc = c < Cb ? __ldg(norm + (size_t)q * Cb + c) : 0.f;  // in flight during the wait
             const int ab = (int)(tcount % RQ_NACC);
             if (ok && !bar_wait(&H->accf[ab], (tcount / RQ_NACC) & 1u, flag)) ok = 0;
             fence_after();
@@ -362,8 +364,6 @@ __global__ void __launch_bounds__(RQ_THREADS, 1) rq_kernel(const __grid_constant
             fence_before();
             __syncwarp();
             if (lane == 0) bar_arrive(&H->accfree[ab]);
-            const int c = ct * RQ_CW + 32 * warp + lane;
-            const float nc = c < Cb ? __ldg(norm + (size_t)q * Cb + c) : 0.f;
 #pragma unroll
             for (int f = 0; f < RQ_NF; ++f)
                 sc[f * RQ_SCS + 32 * warp + lane] = c < Cb ? nc - 2.f * ((v0[f] + v1[f]) + (v2[f] + v3[f])) : INFINITY;
