@@ -87,7 +87,9 @@ struct mfs_ctx {
     std::map<std::string, TensorInfo> tensors;
     int mode = 0;
     int launches = 0;
-    int seq = 0;
+    unsigned seq = 0;            // step sequence number (tags use its low 22 bits)
+    size_t tag_off = 0, tag_bytes = 0;  // the tagged region of the activation arena
+    size_t mma_bytes = 0;        // the tensor-core pass's tagged buffers
     int last_n = 0;
     bool last_full = false;
     std::vector<Pending> pending;
@@ -412,6 +414,7 @@ static int setup_tensor_core_pass(mfs_ctx* c)
     const size_t panel = nch * MMA_B_BYTES, pssq = align_up(nch * 32 * sizeof(uint2), 256), pflag = nch * sizeof(unsigned);
     const size_t done = align_up((size_t)c->nphase * c->G * sizeof(unsigned), 256);
     const size_t total = part + panel + pssq + align_up(pflag, 256) + done;
+    c->mma_bytes = total;
     CK(cudaMalloc((void**)&c->mma_buf, total));
     CK(cudaMemset(c->mma_buf, 0, total));
     c->P.mpart = (uint2*)c->mma_buf;
@@ -481,6 +484,8 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
     const size_t a_am = areg(MS * c->G * 2 * T8), a_dam = areg(MS * S * c->G * 2 * T8);
     const size_t a_to = areg(MS * 4), a_co = areg(MS * 16 * 4), a_ta = areg(MS * 4), a_ca = areg(MS * 16 * 4);
     const size_t a_sc = areg(MS * sizeof(SampleCfg)), a_un = areg(MS * NSTREAM * 4), a_dr = areg(MS * NSTREAM * 4);
+    c->tag_off = a_x;  // [a_x, a_to): every tagged buffer (and the logits); a_to on are outputs and settings
+    c->tag_bytes = a_to - a_x;
     CK(cudaMalloc((void**)&c->act, ao));
     CK(cudaMemset(c->act, 0, ao));
 
@@ -811,10 +816,26 @@ extern "C" int mfs_sync(mfs_ctx* c)
     return collect_device_error(c);
 }
 
+// The next step's sequence number.  A tag is (seq << 10) | phase in 32 bits, so tags
+// repeat every 2^22 steps.  Before the step that starts a period, every tagged word is
+// set to 0xFFFFFFFF (phase 1023), which no step writes (at most 1023 phases), so no word
+// left from an earlier period can match a tag (the reset is ordered after every
+// launch of the earlier steps on the stream).
+static int next_seq(mfs_ctx* c, int& seq)
+{
+    ++c->seq;
+    if ((c->seq & 0x3FFFFFu) == 0u) {
+        CK(cudaMemsetAsync(c->act + c->tag_off, 0xFF, c->tag_bytes, c->stream));
+        if (c->mma_buf) CK(cudaMemsetAsync(c->mma_buf, 0xFF, c->mma_bytes, c->stream));
+    }
+    seq = (int)(c->seq & 0x7FFFFFFFu);
+    return MFS_OK;
+}
+
 static int fill_desc(mfs_ctx* c, StepDesc* h, int n, const int32_t* slots, const int32_t* codes, int frame_off)
 {
     h->n = n;
-    h->seq = ++c->seq;
+    if (next_seq(c, h->seq) != MFS_OK) return MFS_E_CUDA;
     h->sampled = 0;
     h->prompt_rows = 0;
     for (int i = 0; i < n; ++i) {
@@ -878,7 +899,7 @@ static int step_host(mfs_ctx* c, int n, const int32_t* slots, const int32_t* in_
     if ((rc = check_tokens(c, in_codes, n, -1))) return rc;
     int di;
     StepDesc* h = next_desc(c, &di);
-    fill_desc(c, h, n, slots, in_codes, 0);
+    if ((rc = fill_desc(c, h, n, slots, in_codes, 0))) return rc;
     if (uniforms) {
         h->sampled = 1;
         memcpy(c->h_unif, uniforms, (size_t)n * NSTREAM * sizeof(float));
@@ -912,7 +933,7 @@ extern "C" int mfs_step_device(mfs_ctx* c, int n, const int32_t* slots, const in
     if (!d_in_codes) return fail(c, MFS_E_ARG, "null device codes");
     int di;
     StepDesc* h = next_desc(c, &di);
-    fill_desc(c, h, n, slots, nullptr, 0);
+    if ((rc = fill_desc(c, h, n, slots, nullptr, 0))) return rc;
     const size_t head = offsetof(StepDesc, codes);
     CK(cudaMemcpyAsync(c->d_desc, h, head, cudaMemcpyHostToDevice, c->stream));
     CK(cudaEventRecord(c->desc_ev[di], c->stream));
@@ -969,7 +990,7 @@ extern "C" int mfs_prefill(mfs_ctx* c, int n, const int32_t* slots, int T, const
             const int t0 = chunk_t0[q0 + q], tc = chunk_tc[q0 + q];
             StepDesc* h = &c->h_pref[q];
             h->n = n * tc;
-            h->seq = ++c->seq;
+            if (next_seq(c, h->seq) != MFS_OK) return MFS_E_CUDA;
             h->sampled = 0;
             h->prompt_rows = tc > 1;
             for (int i = 0; i < n; ++i)
@@ -1120,6 +1141,14 @@ extern "C" int mfs_read_debug(mfs_ctx* c, float* text_logits, float* dep_logits,
     return MFS_OK;
 }
 
+extern "C" int mfs_debug_set_seq(mfs_ctx* c, uint32_t seq)
+{
+    if (!c) return MFS_E_ARG;
+    CK(cudaStreamSynchronize(c->stream));
+    c->seq = seq;
+    return MFS_OK;
+}
+
 extern "C" int mfs_set_mode(mfs_ctx* c, int mode)
 {
     if (!c) return MFS_E_ARG;
@@ -1151,7 +1180,7 @@ extern "C" int mfs_debug_stall(mfs_ctx* c, int slot)
     if (c->pos[slot] >= c->cfg.max_pos) return fail(c, MFS_E_RANGE, "slot %d is at max_pos", slot);
     int di;
     StepDesc* h = next_desc(c, &di);
-    fill_desc(c, h, 1, &slot, nullptr, 0);
+    if ((rc = fill_desc(c, h, 1, &slot, nullptr, 0))) return rc;
     for (int k = 0; k < NSTREAM; ++k) h->codes[0][k] = -1;
     CK(cudaMemcpyAsync(c->d_desc, h, sizeof(StepDesc), cudaMemcpyHostToDevice, c->stream));
     CK(cudaEventRecord(c->desc_ev[di], c->stream));

@@ -57,6 +57,7 @@ def _load_library():
         "mfs_reset_slot": (ci, [vp, ci]),
         "mfs_position": (ci, [vp, ci]),
         "mfs_read_debug": (ci, [vp, vp, vp, vp, vp]),
+        "mfs_debug_set_seq": (ci, [vp, ctypes.c_uint32]),
         "mfs_set_mode": (ci, [vp, ci]),
         "mfs_launches_per_step": (ci, [vp]),
         "mfs_set_skip_settled": (ci, [vp, ci]),
@@ -279,6 +280,11 @@ def mfs_read_debug(ctx: Ctx, n: Optional[int] = None) -> dict:
                              out["text_argmax"].ctypes.data, out["code_argmax"].ctypes.data)
     _check(ctx, rc)
     return out
+
+
+def mfs_debug_set_seq(ctx: Ctx, seq: int) -> None:
+    """Testing: the next step takes sequence number seq + 1 (see include/mfs.h)."""
+    _check(ctx, _lib.mfs_debug_set_seq(ctx.handle, int(seq) & 0xFFFFFFFF))
 
 
 def mfs_set_mode(ctx: Ctx, mode: int) -> None:

@@ -174,6 +174,14 @@ int mfs_import_slot(mfs_ctx* ctx, int slot, const void* buf, size_t bytes);
 int mfs_read_debug(mfs_ctx* ctx, float* text_logits, float* dep_logits,
                    int32_t* text_argmax, int32_t* code_argmax);
 
+/* Testing: the next step (or prompt launch) takes sequence number seq + 1.
+ * Phases hand values over as words tagged (sequence << 10) | phase in 32 bits,
+ * so tags repeat every 2^22 steps; before the step whose sequence number is a
+ * multiple of 2^22 the library sets every tagged word to a value no step
+ * writes.  This call lets a test cross that point without 4 million steps.
+ * Waits for the context's stream first; MFS_E_ARG on a null context. */
+int mfs_debug_set_seq(mfs_ctx* ctx, uint32_t seq);
+
 /* Execution mode: 0 (default) = one persistent cooperative launch per step,
  * in which a phase waits for the tagged outputs of the phases it reads (no
  * grid-wide barrier); 1 = one launch per phase (same arithmetic, bit for bit,

@@ -172,3 +172,31 @@ def test_mma_sampling_and_skipped_substeps(mfs):
         ta, ca = mfs.mfs_step(a, list(range(9)), u[p])
         tb, cb = mfs.mfs_step(b, list(range(9)), u[p])
         assert np.array_equal(ta, tb) and np.array_equal(ca, cb)
+
+
+@pytest.mark.parametrize("n", [2, 5])
+def test_tag_period_wrap_is_invisible(mfs, n):
+    """Phases hand values over as words tagged (sequence << 10) | phase, which repeat every
+    2^22 steps; the library resets its tagged buffers before the step that starts a period.
+    Steps across that point (sequence numbers 2^22 - 3 .. 2^22 + 4, on the CUDA-core pass
+    for 2 slots and the tensor-core pass for 5) give outputs and logits bit-identical to the
+    same steps at small sequence numbers."""
+    s = tiny_bf16(window=24, max_slots=n)
+    w = synth.make_weights(s, 77, gain_std=0.1)
+    pr = synth.forced_frames(s, 78, synth.STREAM_PROMPT, 6, n).transpose(1, 0, 2)
+    u = synth.user_frames(s, 79, 7, n)
+    runs = []
+    for start in (None, (1 << 22) - 4):
+        ctx = H.gpu_context(s, w)
+        mfs.mfs_prefill(ctx, list(range(n)), pr)
+        if start is not None:
+            mfs.mfs_debug_set_seq(ctx, start)
+        res = []
+        for p in range(u.shape[0]):
+            text, codes = mfs.mfs_step(ctx, list(range(n)), u[p])
+            dbg = mfs.mfs_read_debug(ctx)
+            res.append([text.copy(), codes.copy(), dbg["text_logits"], dbg["dep_logits"]])
+        runs.append(res)
+    for a, b in zip(*runs):
+        for x, y in zip(a, b):
+            np.testing.assert_array_equal(x, y)
