@@ -554,6 +554,7 @@ static int create_impl(mfs_ctx* c, void* cuda_stream)
     Params& P = c->P;
     P.d = g.d; P.L = g.n_layers; P.H = g.n_heads; P.hd = g.head_dim; P.F = g.ffn; P.V = g.text_vocab;
     P.C = g.card; P.W = g.window; P.dd = g.dep_d; P.dL = g.dep_layers; P.dH = g.dep_heads;
+    P.Wa = g.window;
     P.dhd = g.dep_head_dim; P.dF = g.dep_ffn; P.S = g.dep_steps;
     for (int k = 0; k < NSTREAM; ++k) P.delays[k] = g.delays[k];
     P.eps = (float)g.eps;
@@ -1138,6 +1139,16 @@ extern "C" int mfs_read_debug(mfs_ctx* c, float* text_logits, float* dep_logits,
     if (dep_logits) CK(cudaMemcpy(dep_logits, c->P.dlogits, n * 16 * c->cfg.card * 4, cudaMemcpyDeviceToHost));
     if (text_argmax) CK(cudaMemcpy(text_argmax, c->P.text_argmax, n * 4, cudaMemcpyDeviceToHost));
     if (code_argmax) CK(cudaMemcpy(code_argmax, c->P.code_argmax, n * 16 * 4, cudaMemcpyDeviceToHost));
+    return MFS_OK;
+}
+
+extern "C" int mfs_set_ring_mask_oldest(mfs_ctx* c, int on)
+{
+    if (!c) return MFS_E_ARG;
+    if (on != 0 && on != 1) return fail(c, MFS_E_ARG, "on must be 0 or 1");
+    if (on && c->cfg.window < 2) return fail(c, MFS_E_ARG, "masking the oldest slot needs a window of at least 2");
+    CK(cudaStreamSynchronize(c->stream));
+    c->P.Wa = on ? c->cfg.window - 1 : c->cfg.window;
     return MFS_OK;
 }
 

@@ -136,6 +136,7 @@ struct SampleCfg {
 struct Params {
     // shape
     int d, L, H, hd, F, V, C, W, dd, dL, dH, dhd, dF, S;
+    int Wa;                     // keys a step attends to at most: W, or W - 1 with the oldest ring slot masked
     int delays[NSTREAM];
     float eps;
     int G;  // CTAs in the grid

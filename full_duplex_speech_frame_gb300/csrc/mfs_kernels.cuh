@@ -1547,14 +1547,6 @@ __device__ __forceinline__ int attn_chunks(int len, int G, int H)
     return c < NCHUNK_MAX ? c : NCHUNK_MAX;
 }
 
-// Chunks of a window when one warp takes an item: about 128 keys each, at most
-// NCHUNK_MAX.  A function of the window only.
-__device__ __forceinline__ int attn_chunks_warp(int len)
-{
-    const int c = (len + 127) / 128;
-    return c < NCHUNK_MAX ? c : NCHUNK_MAX;
-}
-
 // Keys per stage when the producer streams a head's keys and values through the
 // tensor-core stages (keys, then values, bf16), and stages per item.
 __device__ __forceinline__ int attn_stage_keys(int hd) { return MMA_STAGE / (2 * hd * 2); }
@@ -1569,12 +1561,12 @@ __device__ __forceinline__ int attn_chunks_stream(int len, int hd, int ipc)
     return c < NCHUNK_MAX ? c : NCHUNK_MAX;
 }
 
-enum AttnMode : int { ATTN_CTA = 0, ATTN_WARP = 1, ATTN_STREAM = 2 };
+enum AttnMode : int { ATTN_CTA = 0, ATTN_STREAM = 2 };
 
 // Work items of the step's attention: (batch row i, head h, chunk c), row-major.
 __device__ __forceinline__ int attn_nchunks(int mode, int len, int G, int H, int hd, int ipc)
 {
-    return mode == ATTN_WARP ? attn_chunks_warp(len) : (mode == ATTN_STREAM ? attn_chunks_stream(len, hd, ipc) : attn_chunks(len, G, H));
+    return mode == ATTN_STREAM ? attn_chunks_stream(len, hd, ipc) : attn_chunks(len, G, H);
 }
 
 // Stages per streamed attention item: the phase's stages spread over about six
@@ -1842,12 +1834,12 @@ __device__ __forceinline__ void producer_mma(const Params& P, int ph0, int ph1, 
             // (read once: evict-first, like the weights)
             const StepDesc* D = P.desc;
             const int H = P.H, hd = P.hd, Wn = P.W, KPS = attn_stage_keys(hd);
-            const int ipc = attn_stream_ipc(D, n, Wn, H, hd, P.G);
+            const int ipc = attn_stream_ipc(D, n, P.Wa, H, hd, P.G);
             int total = 0;
-            for (int i = 0; i < n; ++i) total += attn_chunks_stream(D->pos[i] + 1 < Wn ? D->pos[i] + 1 : Wn, hd, ipc) * H;
+            for (int i = 0; i < n; ++i) total += attn_chunks_stream(D->pos[i] + 1 < P.Wa ? D->pos[i] + 1 : P.Wa, hd, ipc) * H;
             for (int item = blockIdx.x; item < total && ok; item += P.G) {
                 int i, h, ci, nch, len, k0, k1, kend, mcur;
-                attn_item(D, n, H, Wn, P.G, item, i, h, ci, nch, len, ATTN_STREAM, hd, ipc);
+                attn_item(D, n, H, P.Wa, P.G, item, i, h, ci, nch, len, ATTN_STREAM, hd, ipc);
                 attn_stream_range(D, i, len, ci, nch, k0, k1, kend, mcur);
                 const int start = D->pos[i] - len + 1;
                 const size_t hbase = (((size_t)D->slot[i] * P.L + q.l) * H + h) * (size_t)Wn * hd;
@@ -1974,12 +1966,12 @@ __device__ __forceinline__ void mma_issuer(const Params& P, int ph0, int ph1, in
             // parity wait on a slot cannot match an older phase
             const StepDesc* D = P.desc;
             const int H = P.H, hd = P.hd, Wn = P.W, KPS = attn_stage_keys(hd);
-            const int ipc = attn_stream_ipc(D, n, Wn, H, hd, P.G);
+            const int ipc = attn_stream_ipc(D, n, P.Wa, H, hd, P.G);
             int total = 0;
-            for (int i = 0; i < n; ++i) total += attn_chunks_stream(D->pos[i] + 1 < Wn ? D->pos[i] + 1 : Wn, hd, ipc) * H;
+            for (int i = 0; i < n; ++i) total += attn_chunks_stream(D->pos[i] + 1 < P.Wa ? D->pos[i] + 1 : P.Wa, hd, ipc) * H;
             for (int item = blockIdx.x; item < total; item += P.G) {
                 int i, h, ci, nch, len, k0, k1, kend, mcur;
-                attn_item(D, n, H, Wn, P.G, item, i, h, ci, nch, len, ATTN_STREAM, hd, ipc);
+                attn_item(D, n, H, P.Wa, P.G, item, i, h, ci, nch, len, ATTN_STREAM, hd, ipc);
                 attn_stream_range(D, i, len, ci, nch, k0, k1, kend, mcur);
                 if (kend > k0) s += (unsigned)((kend - k0 + KPS - 1) / KPS);
             }
@@ -2496,13 +2488,13 @@ __device__ __forceinline__ void prefetch_kv_windows(const Params& P, int l, int 
     const int d = P.d, W = P.W, H = P.H, hd = P.hd;
     constexpr int PCS = 32;  // positions per prefetch
     long long total = 0;
-    for (int i = 0; i < n; ++i) total += (long long)(D->pos[i] + 1 < W ? D->pos[i] : W - 1);
+    for (int i = 0; i < n; ++i) total += (long long)(D->pos[i] + 1 < P.Wa ? D->pos[i] : P.Wa - 1);
     if (total * d * (long long)sizeof(TKV) * 2 > (32ll << 20)) return;
     const uint64_t pol = l2_evict_last();
     // items (slot, head, piece, tensor), slot-major; item k goes to CTA k mod G
     int i = 0;
     long long base = 0;
-    auto older = [&](int ii) { return D->pos[ii] + 1 < W ? D->pos[ii] : W - 1; };
+    auto older = [&](int ii) { return D->pos[ii] + 1 < P.Wa ? D->pos[ii] : P.Wa - 1; };
     auto items = [&](int ii) { return (long long)H * ((older(ii) + PCS - 1) / PCS) * 2; };
     long long cnt = n > 0 ? items(0) : 0;
     for (long long k = blockIdx.x + (long long)P.G * threadIdx.x;; k += (long long)P.G * NT) {
@@ -2644,11 +2636,11 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
     int total = 0;
     for (int i = 0; i < n; ++i) {
         const int p = D->pos[i];
-        total += attn_chunks(p + 1 < W ? p + 1 : W, P.G, H) * H;
+        total += attn_chunks(p + 1 < P.Wa ? p + 1 : P.Wa, P.G, H) * H;
     }
     for (int item = blockIdx.x; item < total; item += P.G) {
         int i, h, c, nch, len;
-        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len);
+        attn_item(D, n, H, P.Wa, P.G, item, i, h, c, nch, len);
         const int p = D->pos[i], slot = D->slot[i];
         const int start = p - len + 1;
         // keys of this launch: the last mcur of the window (the current one, and in a prompt
@@ -2713,7 +2705,7 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
     // merges: the CTA that ran chunk 0 of a split window combines its chunks in order
     for (int item = blockIdx.x; item < total; item += P.G) {
         int i, h, c, nch, len;
-        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len);
+        attn_item(D, n, H, P.Wa, P.G, item, i, h, c, nch, len);
         if (c != 0 || nch == 1) continue;
         const uint2* part = P.attp + ((size_t)i * H + h) * NCHUNK_MAX * pstride;
         // every chunk's partial into shared memory, four loads in flight per thread
@@ -2754,114 +2746,6 @@ __device__ __forceinline__ bool phase_attn(const Params& P, int l, int n, unsign
     return true;
 }
 
-// Attention of the tensor-core instantiation (many rows): one warp per item
-// (batch row, head, chunk of about 128 keys), with no block barrier, so a
-// CTA's eight warps keep eight items' loads in flight.  A window of one chunk
-// writes the output directly; otherwise each chunk leaves {max, sum,
-// unnormalised output} tagged in P.attp and the warp that ran chunk 0 merges
-// the chunks in order once it has run all of its own items (no warp waits for
-// another's chunk before finishing its own, so the waits end).
-template <typename TKV>
-__device__ __noinline__ bool phase_attn_warp(const Params& P, int l, int n, unsigned in_tag, unsigned tag)
-{
-    const StepDesc* D = P.desc;
-    const int H = P.H, hd = P.hd, d = P.d, W = P.W;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int LPP = hd / 8, gl = lane % LPP;
-    const float scale = rsqrtf((float)hd);
-    const size_t pstride = (size_t)hd + 2;  // partial: max, sum, hd outputs
-    const int gw = (int)blockIdx.x * NWARP + warp, GW = P.G * NWARP;
-    int total = 0;
-    for (int i = 0; i < n; ++i) {
-        const int p = D->pos[i];
-        total += attn_chunks_warp(p + 1 < W ? p + 1 : W) * H;
-    }
-    int ok = 1;
-    for (int item = gw; item < total && ok; item += GW) {
-        int i, h, c, nch, len;
-        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, ATTN_WARP);
-        const int p = D->pos[i], slot = D->slot[i];
-        const int start = p - len + 1;
-        const int mcur = p - D->pos[slot_first_row(D, i)] + 1;
-        const int k0 = (int)((long long)len * c / nch), k1 = (int)((long long)len * (c + 1) / nch);
-        const long long kvbase = (((long long)slot * P.L + l) * H + h) * (long long)W * hd + gl * 8;
-        const size_t qo = (size_t)i * d + h * hd + gl * 8;
-        uint2 qt[8], kt[8], vt[8];
-        tag8_issue(P.q + qo, qt);
-        const bool has_cur = len - 1 >= k0 && len - 1 < k1;
-        if (has_cur) {
-            tag8_issue(P.kcur + qo, kt);
-            tag8_issue(P.vcur + qo, vt);
-        }
-        float qv[8], kcur[8], vcur[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) { kcur[e] = 0.f; vcur[e] = 0.f; }
-        ok = tag8_take(qt, P.q + qo, in_tag, qv, P.err);
-        if (has_cur && ok) ok = tag8_take(kt, P.kcur + qo, in_tag, kcur, P.err) && tag8_take(vt, P.vcur + qo, in_tag, vcur, P.err);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qv[e] *= scale;
-        float m, lsum, acc[8];
-        attn_keys<TKV>(P, i, h, len, start, mcur, k0, k1, kvbase, qv, kcur, vcur, in_tag, ok, m, lsum, acc);
-        ok = __all_sync(0xffffffffu, ok);
-        if (lane < LPP) {
-            if (nch == 1) {
-                uint2* o = P.o + qo;
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) st_tag2(o + e, acc[e] / lsum, acc[e + 1] / lsum, tag);
-            } else {
-                uint2* part = P.attp + (((size_t)i * H + h) * NCHUNK_MAX + c) * pstride;
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) st_tag2(part + 2 + gl * 8 + e, acc[e], acc[e + 1], tag);
-                if (lane == 0) st_tag2(part, m, lsum, tag);
-            }
-        }
-    }
-    // merges: the warp that ran chunk 0 of a split window combines its chunks in order
-    for (int item = gw; item < total && ok; item += GW) {
-        int i, h, c, nch, len;
-        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, ATTN_WARP);
-        if (c != 0 || nch == 1) continue;
-        const uint2* part = P.attp + ((size_t)i * H + h) * NCHUNK_MAX * pstride;
-        // lane takes elements lane, lane + 32, ... of the head; the chunk maxima and sums first
-        float mk = -INFINITY, lk = 0.f;
-        if (lane < nch) {
-            uint2 a, b;
-            ld_tag2(part + (size_t)lane * pstride, a, b);
-            unsigned ab = a.x, bb = b.x;
-            if (a.y != tag) ok = ok && wait_tag1(part + (size_t)lane * pstride, tag, ab, P.err);
-            if (b.y != tag) ok = ok && wait_tag1(part + (size_t)lane * pstride + 1, tag, bb, P.err);
-            mk = __uint_as_float(ab);
-            lk = __uint_as_float(bb);
-        }
-        float M = warp_max(mk);
-        const float f = (lane < nch && mk != -INFINITY) ? expf(mk - M) : 0.f;
-        const float L = warp_sum(lk * f);
-        // lane takes elements lane + 32 q of the head (hd <= 128); per chunk its loads
-        // are in flight together, and the chunks are added in order
-        constexpr int QE = 4;
-        float a[QE];
-#pragma unroll
-        for (int q = 0; q < QE; ++q) a[q] = 0.f;
-        for (int k = 0; k < nch && ok; ++k) {
-            const float fk = __shfl_sync(0xffffffffu, f, k);
-            const uint2* pk = part + (size_t)k * pstride + 2;
-            uint2 v[QE];
-#pragma unroll
-            for (int q = 0; q < QE; ++q) v[q] = lane + 32 * q < hd ? ld_tag1(pk + lane + 32 * q) : make_uint2(0u, tag);
-#pragma unroll
-            for (int q = 0; q < QE; ++q) {
-                unsigned bits = v[q].x;
-                if (lane + 32 * q < hd && v[q].y != tag && ok) ok = wait_tag1(pk + lane + 32 * q, tag, bits, P.err);
-                a[q] += __uint_as_float(bits) * fk;
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < QE; ++q)
-            if (lane + 32 * q < hd) st_tag1(P.o + (size_t)i * d + h * hd + lane + 32 * q, __float_as_uint(a[q] / L), tag);
-    }
-    return csync_and(ok);
-}
-
 // Attention of the tensor-core instantiation with keys and values streamed by the
 // producer warp: one CTA per item (batch row, head, chunk of the window; about six
 // items per CTA).  A stage holds up to attn_stage_keys(hd) keys, then as many values,
@@ -2888,16 +2772,16 @@ __device__ __noinline__ bool phase_attn_stream(const Params& P, int l, int n, un
     const float scale = 1.4426950408889634f * rsqrtf((float)hd);  // log2(e) / sqrt(hd)
     const int wstride = hd + 4;
     const size_t pstride = (size_t)hd + 2;
-    const int ipc = attn_stream_ipc(D, n, W, H, hd, P.G);
+    const int ipc = attn_stream_ipc(D, n, P.Wa, H, hd, P.G);
     int total = 0;
     for (int i = 0; i < n; ++i) {
         const int p = D->pos[i];
-        total += attn_chunks_stream(p + 1 < W ? p + 1 : W, hd, ipc) * H;
+        total += attn_chunks_stream(p + 1 < P.Wa ? p + 1 : P.Wa, hd, ipc) * H;
     }
     int ok = 1;
     for (int item = blockIdx.x; item < total; item += P.G) {
         int i, h, c, nch, len;
-        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, ATTN_STREAM, hd, ipc);
+        attn_item(D, n, H, P.Wa, P.G, item, i, h, c, nch, len, ATTN_STREAM, hd, ipc);
         int k0, k1, kend, mcur;
         attn_stream_range(D, i, len, c, nch, k0, k1, kend, mcur);
         float qv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -3058,7 +2942,7 @@ __device__ __noinline__ bool phase_attn_stream(const Params& P, int l, int n, un
     // merges: the CTA that ran chunk 0 of a split window combines its chunks in order
     for (int item = blockIdx.x; item < total; item += P.G) {
         int i, h, c, nch, len;
-        attn_item(D, n, H, W, P.G, item, i, h, c, nch, len, ATTN_STREAM, hd, ipc);
+        attn_item(D, n, H, P.Wa, P.G, item, i, h, c, nch, len, ATTN_STREAM, hd, ipc);
         if (c != 0 || nch == 1) continue;
         const uint2* part = P.attp + ((size_t)i * H + h) * NCHUNK_MAX * pstride;
         float* mb = sm.wbuf;  // [nch][hd + 2]

@@ -57,6 +57,7 @@ def _load_library():
         "mfs_reset_slot": (ci, [vp, ci]),
         "mfs_position": (ci, [vp, ci]),
         "mfs_read_debug": (ci, [vp, vp, vp, vp, vp]),
+        "mfs_set_ring_mask_oldest": (ci, [vp, ci]),
         "mfs_debug_set_seq": (ci, [vp, ctypes.c_uint32]),
         "mfs_set_mode": (ci, [vp, ci]),
         "mfs_launches_per_step": (ci, [vp]),
@@ -280,6 +281,11 @@ def mfs_read_debug(ctx: Ctx, n: Optional[int] = None) -> dict:
                              out["text_argmax"].ctypes.data, out["code_argmax"].ctypes.data)
     _check(ctx, rc)
     return out
+
+
+def mfs_set_ring_mask_oldest(ctx: Ctx, on: bool) -> None:
+    """Attend to W - 1 keys once the ring is full (the masked-oldest-slot window variant)."""
+    _check(ctx, _lib.mfs_set_ring_mask_oldest(ctx.handle, 1 if on else 0))
 
 
 def mfs_debug_set_seq(ctx: Ctx, seq: int) -> None:

@@ -174,6 +174,15 @@ int mfs_import_slot(mfs_ctx* ctx, int slot, const void* buf, size_t bytes);
 int mfs_read_debug(mfs_ctx* ctx, float* text_logits, float* dep_logits,
                    int32_t* text_argmax, int32_t* code_argmax);
 
+/* Ring window variant (SGLang-Omni cookbook, PersonaPlex, "Known limitations":
+ * the window follows the streaming ring, including the masked oldest slot once
+ * the ring fills).  on = 1: a step at position p attends to positions
+ * max(0, p - W + 2) .. p, i.e. W - 1 keys once the ring holds W; the ring keeps
+ * its capacity W.  on = 0 (default): positions max(0, p - W + 1) .. p.  Applies
+ * from the next step on; waits for the context's stream.  MFS_E_ARG if on is not
+ * 0 or 1, or W < 2. */
+int mfs_set_ring_mask_oldest(mfs_ctx* ctx, int on);
+
 /* Testing: the next step (or prompt launch) takes sequence number seq + 1.
  * Phases hand values over as words tagged (sequence << 10) | phase in 32 bits,
  * so tags repeat every 2^22 steps; before the step whose sequence number is a

@@ -46,7 +46,7 @@ class _Cfg(ctypes.Structure):
         "max_pos", "dep_d", "dep_layers", "dep_heads", "dep_head_dim", "dep_ffn", "dep_steps")] + [
         ("delays", ctypes.c_int * 17), ("rope_theta", ctypes.c_double), ("eps", ctypes.c_double),
         ("weight_dtype", ctypes.c_int), ("max_slots", ctypes.c_int), ("brute_force", ctypes.c_int),
-        ("kv_dtype", ctypes.c_int)]
+        ("kv_dtype", ctypes.c_int), ("mask_oldest", ctypes.c_int)]
 
 
 def _load():
@@ -110,7 +110,7 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
 class Oracle:
     """One oracle instance: slots, token histories and fp64 key/value rings."""
 
-    def __init__(self, shape, weights: Dict[str, np.ndarray], brute_force: bool = False):
+    def __init__(self, shape, weights: Dict[str, np.ndarray], brute_force: bool = False, mask_oldest: bool = False):
         s = shape
         c = _Cfg()
         for f in ("d", "n_layers", "n_heads", "head_dim", "ffn", "text_vocab", "card", "n_q",
@@ -123,6 +123,7 @@ class Oracle:
         c.weight_dtype = 1 if s.weight_dtype == "bf16" else 0
         c.brute_force = 1 if brute_force else 0
         c.kv_dtype = 1 if s.kv_dtype == "bf16" else 0
+        c.mask_oldest = 1 if mask_oldest else 0
         self.shape = s
         self._lib = _load()
         self._h = self._lib.orc_create(ctypes.byref(c))

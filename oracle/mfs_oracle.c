@@ -19,7 +19,9 @@
  *      RMSNorm eps 1e-8): a = rmsnorm(x); q|k|v = Wqkv a; q and k rotated by
  *      the absolute frame position p (interleaved pairs, theta 10000); keys and
  *      values of positions max(0, p-W+1) .. p (W = 3000 window, vLLM-Omni
- *      PersonaPlex recipe, "Architecture") with a max-subtracted softmax at
+ *      PersonaPlex recipe, "Architecture"; with mask_oldest W-1 positions,
+ *      the masked oldest slot of SGLang-Omni cookbook, PersonaPlex, "Known
+ *      limitations") with a max-subtracted softmax at
  *      scale 1/sqrt(hd); x += Wo o; a = rmsnorm(x); gate|up = Wgu a;
  *      x += Wdown (silu(gate) * up).
  *  S4  h = rmsnorm(x, out_norm); text logits = Wtext h; greedy argmax (lowest
@@ -72,6 +74,7 @@ typedef struct {
     int max_slots;
     int brute_force;  /* 1: keep every position, mask to the last W */
     int kv_dtype;     /* 0 = fp64 cache, 1 = keys and values rounded to bf16 when cached */
+    int mask_oldest;  /* 1: once the ring holds W positions its oldest is masked (W - 1 keys) */
 } orc_config;
 
 typedef struct {
@@ -306,6 +309,7 @@ int orc_sample_topk(const double* lg, int n, double temp, int k, double u)
 
 orc* orc_create(const orc_config* c)
 {
+    if (c->mask_oldest && c->window < 2) return NULL;
     orc* o = (orc*)calloc(1, sizeof(orc));
     if (!o) return NULL;
     o->c = *c;
@@ -523,12 +527,15 @@ static int input_token(const orc* o, const orc_slot* s, int k, int p)
 }
 
 /* Rotate q and k of one position, store k and v at the ring row of position p,
- * and attend over the window of p (keys in ascending absolute position). */
+ * and attend over the window of p (keys in ascending absolute position): the last
+ * W positions, or with mask_oldest the last W - 1 (SGLang-Omni cookbook,
+ * PersonaPlex, "Known limitations": the oldest slot of a full ring is masked). */
 static void attend(orc* o, orc_slot* s, int l, int p, double* q, double* k, const double* v, double* att)
 {
     const orc_config* c = &o->c;
     int d = c->d, H = c->n_heads, hd = c->head_dim, W = c->window;
-    int len = p + 1 < W ? p + 1 : W;
+    int Wa = c->mask_oldest ? W - 1 : W;
+    int len = p + 1 < Wa ? p + 1 : Wa;
     int start = p - len + 1;
     size_t layer_stride = (size_t)o->cap * (size_t)d;
     for (int hh = 0; hh < H; ++hh) {

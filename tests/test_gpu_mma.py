@@ -200,3 +200,41 @@ def test_tag_period_wrap_is_invisible(mfs, n):
     for a, b in zip(*runs):
         for x, y in zip(a, b):
             np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("n", [2, 6])
+def test_ring_mask_oldest(mfs, n):
+    """The masked-oldest-slot window (W - 1 keys once the ring of capacity W is full), on the
+    CUDA-core pass (2 slots) and the tensor-core pass (6 slots), W = 8, 20 steps from
+    position 0 (two wraps): the oracle with the same flag follows the GPU, and the GPU
+    matches, bit for bit, a context with a plain window of 7."""
+    s = tiny_bf16(window=8, max_slots=n)
+    w = synth.make_weights(s, 90 + n, gain_std=0.1)
+    ctx, orc = H.gpu_context(s, w), oracle.Oracle(s, w, mask_oldest=True)
+    mfs.mfs_set_ring_mask_oldest(ctx, True)
+    ctx7 = H.gpu_context(s.replace(window=7), w)
+    u = synth.user_frames(s, 91 + n, 20, n)
+    tally = H.Tally(f"masked oldest ring slot, W=8, B={n}")
+    slots = list(range(n))
+    for p in range(u.shape[0]):
+        text, codes = mfs.mfs_step(ctx, slots, u[p])
+        dbg = mfs.mfs_read_debug(ctx)
+        text7, codes7 = mfs.mfs_step(ctx7, slots, u[p])
+        dbg7 = mfs.mfs_read_debug(ctx7)
+        np.testing.assert_array_equal(text, text7)
+        np.testing.assert_array_equal(codes, codes7)
+        np.testing.assert_array_equal(dbg["text_logits"], dbg7["text_logits"])
+        np.testing.assert_array_equal(dbg["dep_logits"], dbg7["dep_logits"])
+        fol = H.follow_tokens(text, codes, dbg["code_argmax"])
+        ref = orc.step(slots, u[p], want_logits=True, follow=fol)
+        np.testing.assert_array_equal(text, ref["text"])
+        np.testing.assert_array_equal(codes, ref["codes"])
+        tally.step(dbg, slots, ref, f"frame {p}")
+    print(tally.report())
+
+
+def test_ring_mask_oldest_rejects_bad_flag(mfs):
+    s = tiny_bf16(window=8, max_slots=2)
+    ctx = H.gpu_context(s, synth.make_weights(s, 5, gain_std=0.1))
+    with pytest.raises(mfs.MfsError):
+        mfs._check(ctx, mfs._lib.mfs_set_ring_mask_oldest(ctx.handle, 2))

@@ -289,6 +289,30 @@ def test_ring_equals_brute_force_history(tiny_w8):
             np.testing.assert_array_equal(ra[key], rb[key])
 
 
+def test_masked_oldest_slot_is_a_window_of_w_minus_1(tiny_w8):
+    """The masked-oldest-slot variant (a ring of capacity W whose oldest slot is masked once
+    full) attends exactly like the plain window of W - 1: same outputs and logits at every
+    step, including the steps before the ring fills and after it wraps; with the flag off
+    it differs once the ring holds W positions."""
+    s, w = tiny_w8
+    T = 3 * s.window + 5
+    inp = synth.user_frames(s, 24, T, 1)[:, 0]
+    a = oracle.Oracle(s, w, mask_oldest=True)
+    b = oracle.Oracle(s.replace(window=s.window - 1), w)
+    c = oracle.Oracle(s, w)
+    differs = False
+    for p in range(T):
+        ra = a.step([0], inp[p:p + 1], want_logits=True)
+        rb = b.step([0], inp[p:p + 1], want_logits=True)
+        rc = c.step([0], inp[p:p + 1], want_logits=True)
+        for key in ra:
+            np.testing.assert_array_equal(ra[key], rb[key])
+        if p < s.window - 1:
+            np.testing.assert_array_equal(ra["text_logits"], rc["text_logits"])
+        differs |= not np.array_equal(ra["text_logits"], rc["text_logits"])
+    assert differs
+
+
 def test_window_actually_limits_context(tiny_w8):
     """Tokens older than the window (through every layer) cannot change the output."""
     s, w = tiny_w8
