@@ -7,21 +7,22 @@
 // and the residuals are each split into a bf16 high part and the bf16 rounding
 // of the rest, and the products hi.hi + hi.lo + lo.hi + lo.lo keep about 16
 // significant bits (score error a few 1e-5 of sum_i |r_i c_i|), enough to pick
-// candidates.  Each frame's 8 best codewords by that score are then re-ranked
-// by their exact fp32 distances, computed in the order of the CUDA-core kernel
-// (mfs_rvq.cu: float4 chunks, one fmaf per component); the smallest wins,
-// lower index on ties.  So the code equals the CUDA-core kernel's whenever the
-// nearest codeword is among the 8, i.e. unless more than 7 codewords score
-// within that error of the nearest (identical codewords score identically and
-// keep the lower index first, so exact duplicates cannot push it out).
+// candidates.  A frame's codewords fall into 8 classes by index mod 8; the best
+// 2 of each class by that score (16 per frame) are then re-ranked by their
+// exact fp32 distances, computed in the order of the CUDA-core kernel
+// (mfs_rvq.cu: float4 chunks, one fmaf per component); the smallest wins, lower
+// index on ties.  So the code equals the CUDA-core kernel's whenever the
+// nearest codeword is among the 16, i.e. unless two codewords of its class score
+// within that error of it (identical codewords score identically and keep the
+// lower index first, so exact duplicates cannot push it out).
 //
 // A CTA takes 16 frames through all 8 stages.  Warp 4 (one lane) loads
 // codebook tiles (128 codewords x 64 dimensions, high and low parts) with 2-D
 // TMA copies into a ring of stages; warp 5 (one lane) issues the MMAs into one
 // of two tensor-memory accumulators per codeword tile; warps 0-3 build the
 // residuals' operand panel in shared memory, read each tile's scores (one
-// codeword per thread), keep per-frame candidate lists, re-rank them exactly,
-// and update the residuals.
+// codeword per thread), keep the best two of each class per frame, re-rank
+// them exactly, and update the residuals.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -45,8 +46,7 @@ constexpr int RQ_TILE = RQ_CW * RQ_KC * 2;  // 16 KB: one part of a codebook til
 constexpr int RQ_STAGE = 2 * RQ_TILE;       // high and low parts
 constexpr int RQ_CONS = 128;         // consumer threads (warps 0-3)
 constexpr int RQ_THREADS = RQ_CONS + 64;
-constexpr int RQ_KEEP = 8;           // best codewords kept per sub-list (8 sub-lists, one thread each, per frame)
-constexpr int RQ_CAND = 8;           // of those, the frame's best 8 are re-ranked exactly (one per thread)
+constexpr int RQ_KEEP = 2;           // best codewords kept per sub-list (8 sub-lists, one thread each, per frame)
 constexpr int RQ_NCOL = 64;          // accumulator block: [A_hi x (B_hi | B_lo) | A_lo x (B_hi | B_lo)] columns
 constexpr int RQ_NSPLIT = 1;         // blocks per accumulator: chunk kc accumulates into block kc % RQ_NSPLIT
 constexpr int RQ_NACC = 2;           // accumulators (codeword tiles in flight between the MMAs and the consumers)
@@ -368,60 +368,45 @@ __global__ void __launch_bounds__(RQ_THREADS, 1) rq_kernel(const __grid_constant
             for (int f = 0; f < RQ_NF; ++f)
                 sc[f * RQ_SCS + 32 * warp + lane] = c < Cb ? nc - 2.f * ((v0[f] + v1[f]) + (v2[f] + v3[f])) : INFINITY;
             asm volatile("bar.sync 2, %0;" ::"n"(RQ_CONS) : "memory");
-            for (int k = s8; k < RQ_CW; k += 8) {
+            for (int k = s8; k < RQ_CW; k += 8) {  // keep the sub-list's best two (cs[0] <= cs[1])
                 const float v = sc[f8 * RQ_SCS + k];
                 const int ix = ct * RQ_CW + k;
-                if (cbetter(v, ix, cs[RQ_KEEP - 1], ci[RQ_KEEP - 1])) {
-                    cs[RQ_KEEP - 1] = v;
-                    ci[RQ_KEEP - 1] = ix;
-#pragma unroll
-                    for (int m = RQ_KEEP - 1; m > 0; --m)
-                        if (cbetter(cs[m], ci[m], cs[m - 1], ci[m - 1])) {
-                            const float ts = cs[m]; cs[m] = cs[m - 1]; cs[m - 1] = ts;
-                            const int ti = ci[m]; ci[m] = ci[m - 1]; ci[m - 1] = ti;
-                        }
+                if (cbetter(v, ix, cs[1], ci[1])) {
+                    const bool first = cbetter(v, ix, cs[0], ci[0]);
+                    cs[1] = first ? cs[0] : v;
+                    ci[1] = first ? ci[0] : ix;
+                    cs[0] = first ? v : cs[0];
+                    ci[0] = first ? ix : ci[0];
                 }
             }
             asm volatile("bar.sync 2, %0;" ::"n"(RQ_CONS) : "memory");
         }
-        // the frame's best RQ_CAND codewords by score over its 8 sub-lists (a tournament over
-        // the lanes' sorted lists; codeword indices differ between sub-lists), one per lane
-        int mine = 0x7fffffff;
-#pragma unroll
-        for (int k = 0; k < RQ_CAND; ++k) {
-            float bv = cs[0];
-            int bx = ci[0];
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) {
-                const float v2 = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int i2 = __shfl_xor_sync(0xffffffffu, bx, o);
-                if (cbetter(v2, i2, bv, bx)) { bv = v2; bx = i2; }
-            }
-            if (s8 == k) mine = bx;
-            if (bx == ci[0] && bx != 0x7fffffff) {  // this lane's head won: pop it
-#pragma unroll
-                for (int m = 0; m < RQ_KEEP - 1; ++m) { cs[m] = cs[m + 1]; ci[m] = ci[m + 1]; }
-                cs[RQ_KEEP - 1] = INFINITY;
-                ci[RQ_KEEP - 1] = 0x7fffffff;
-            }
-        }
-        // exact fp32 distance of the lane's candidate (the CUDA-core kernel's arithmetic: float4
-        // chunks in order, one fmaf per component), then the least over the frame's lanes
+        // exact fp32 distances of the lane's two candidates (the CUDA-core kernel's arithmetic:
+        // float4 chunks in order, one fmaf per component; the two chains interleave), then the
+        // least over the frame's 16 candidates (8 lanes)
         const float4* book = reinterpret_cast<const float4*>(cb + (size_t)q * Cb * D);
         const float4* r4 = reinterpret_cast<const float4*>(res + (size_t)f8 * D);
-        const float4* row = book + (size_t)(mine < Cb ? mine : 0) * D4;
-        float acc = 0.f;
+        const float4* row0 = book + (size_t)(ci[0] < Cb ? ci[0] : 0) * D4;
+        const float4* row1 = book + (size_t)(ci[1] < Cb ? ci[1] : 0) * D4;
+        float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll 8
         for (int e = 0; e < D4; ++e) {
-            const float4 w = __ldg(row + e), x = r4[e];
-            const float a = x.x - w.x, b = x.y - w.y, c2 = x.z - w.z, d2 = x.w - w.w;
-            acc = fmaf(a, a, acc);
-            acc = fmaf(b, b, acc);
-            acc = fmaf(c2, c2, acc);
-            acc = fmaf(d2, d2, acc);
+            const float4 x = r4[e], w0 = __ldg(row0 + e), w1 = __ldg(row1 + e);
+            const float a0 = x.x - w0.x, b0 = x.y - w0.y, c0 = x.z - w0.z, d0 = x.w - w0.w;
+            const float a1 = x.x - w1.x, b1 = x.y - w1.y, c1 = x.z - w1.z, d1 = x.w - w1.w;
+            acc0 = fmaf(a0, a0, acc0);
+            acc1 = fmaf(a1, a1, acc1);
+            acc0 = fmaf(b0, b0, acc0);
+            acc1 = fmaf(b1, b1, acc1);
+            acc0 = fmaf(c0, c0, acc0);
+            acc1 = fmaf(c1, c1, acc1);
+            acc0 = fmaf(d0, d0, acc0);
+            acc1 = fmaf(d1, d1, acc1);
         }
-        float bd = mine < Cb ? acc : INFINITY;
-        int bi = mine < Cb ? mine : 0x7fffffff;
+        float bd = INFINITY;
+        int bi = 0x7fffffff;
+        if (ci[0] < Cb && cbetter(acc0, ci[0], bd, bi)) { bd = acc0; bi = ci[0]; }
+        if (ci[1] < Cb && cbetter(acc1, ci[1], bd, bi)) { bd = acc1; bi = ci[1]; }
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) {  // the frame's 8 lanes
             const float v2 = __shfl_xor_sync(0xffffffffu, bd, o);

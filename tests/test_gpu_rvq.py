@@ -74,10 +74,10 @@ def test_rvq_matches_oracle(mfs, T, D, Cb):
 
 
 def test_rvq_clustered_codebooks(mfs):
-    """Codebooks of 64 clusters of 48 close codewords (member m of cluster g at index 64 m + g, so
-    a cluster spans every codeword tile and every candidate sub-list), latents near cluster
-    centres: the nearest codeword has 47 close rivals, more than the 8 candidates the
-    tensor-core path re-ranks, yet it must still be found."""
+    """Codebooks of 64 clusters of 48 close codewords (member m of cluster g at index 64 m + g:
+    a cluster spans every codeword tile but lies in one class of indices mod 8), latents near
+    cluster centres: the nearest codeword has 47 close rivals in its own class, of which the
+    tensor-core path keeps the best 2 by its approximate score, yet it must still be found."""
     T, D, G, M = 64, 256, 64, 48
     Cb = G * M
     centre = synth.normal_f32(7, 511, 8 * G * D).reshape(8, 1, G, D)
