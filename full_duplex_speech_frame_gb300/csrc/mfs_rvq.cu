@@ -156,7 +156,7 @@ extern "C" int mfs_rvq_encode(const float* z_sem, const float* z_ac, int T, int 
     if (!z_sem || !z_ac || !codebooks || !codes) return fail(MFS_E_ARG, "rvq: null pointer");
     if (((uintptr_t)z_sem | (uintptr_t)z_ac | (uintptr_t)codebooks) & 15u)
         return fail(MFS_E_ARG, "rvq: latents and codebooks must be 16-byte aligned");
-    if (D % 8 == 0 && 8LL * Cb <= 0x7fffffffLL)
+    if (D % 8 == 0 && Cb < (1 << 24))
         return mfs::rvq_encode_mma(z_sem, z_ac, T, D, codebooks, Cb, codes, (cudaStream_t)cuda_stream);
     const size_t smem = (size_t)RV_FT * D * sizeof(float);
     if (smem > 48 * 1024) {  // the residual tile needs more than the default shared memory

@@ -275,9 +275,11 @@ int mfs_phase_times(mfs_ctx* ctx, uint64_t* ns, int cap);
  * D a multiple of 8: the distances' cross terms r.c run on the tensor cores
  * (bf16 high/low parts of r and c, fp32 accumulation, about 16 significant
  * bits); per frame, the best 2 codewords by that score of each class of
- * indices mod 8 (16 candidates) are re-ranked by the exact fp32 distance, so
- * the code is the exhaustive fp32 argmin unless two codewords of the nearest's
- * class score within that error (a few 1e-5 of sum |r_i c_i|) of it.  This form takes 4 * 8 * Cb * D + 32 * Cb bytes of scratch from
+ * indices mod 8 are candidates, and those within a band of four times the
+ * score's error bound (2^-14 |r| |c|) of the best score are re-ranked by their
+ * fp32 distance (a fixed summation order), so the code is the exhaustive fp32
+ * argmin (up to that order's rounding) unless two codewords of the nearest's
+ * class score within that error of it.  This form takes 4 * 8 * Cb * D + 32 * Cb bytes of scratch from
  * the device's stream-ordered pool and frees it on the stream.  Otherwise every
  * distance is computed exactly in fp32 on the CUDA cores.
  * Enqueues and returns; MFS_E_ARG on bad sizes, alignment or NULL pointers;
