@@ -387,7 +387,7 @@ def run_gpu(args, rank, world):
             },
             "rvq_encode": {
                 "what": "mfs_rvq_encode, Mimi split RVQ argmin quantizer: 2432 frames, D 256, 8 codebooks of 2048; "
-                        "r.c on the tensor cores (bf16 high/low parts), exact fp32 re-rank of 16 candidates per frame",
+                        "r.c on the tensor cores (bf16 high/low parts) in CTA pairs of 32 frames, fp32 re-rank of the candidates near the best score",
                 "kernel_ms": rvq_ms, "value": Tq / (rvq_ms / 1000.0), "unit": "frames/s",
                 "roofline": {"bound": "tensor", "unit": "TFLOP/s",
                              "achieved": 2.0 * Tq * 8 * Cq * Dq / (rvq_ms / 1000.0) / 1e12,

@@ -47,11 +47,13 @@ def _compare(got, want, gap, T):
     assert compared >= 6 * T
 
 
-# D a multiple of 8 runs on the tensor cores (approximate scores, exact re-rank of 32
-# candidates); D = 12 and D = 36 on the CUDA cores (every distance exact).  2432 x 256 x 2048
-# is the timed workload; Cb = 300 and 5 leave ragged codeword tiles, T = 37 a ragged frame tile.
+# D a multiple of 8 runs on the tensor cores (approximate scores, fp32 re-rank of the candidates
+# near the best score): CTA pairs of 32 frames up to D = 520, one CTA per 16 frames for D = 1024;
+# D = 12 and D = 36 on the CUDA cores (every distance exact).  2432 x 256 x 2048 is the timed
+# workload; 2472 frames take two launches of CTA pairs; Cb = 300, 130 and 5 leave ragged codeword
+# tiles (Cb = 5: the second CTA of a pair has no tile), T = 37 a ragged frame group.
 @pytest.mark.parametrize("T,D,Cb", [(37, 256, 2048), (1, 1024, 300), (16, 8, 5), (2432, 256, 2048),
-                                    (23, 12, 100), (5, 36, 7), (40, 520, 130)])
+                                    (23, 12, 100), (5, 36, 7), (40, 520, 130), (2472, 64, 300)])
 def test_rvq_matches_oracle(mfs, T, D, Cb):
     """Codes equal the oracle's; a frame's chain is compared up to a stage whose best two
     distances lie within GAP (there fp32 may rank them the other way; later residuals differ)."""
