@@ -279,14 +279,20 @@ int mfs_phase_times(mfs_ctx* ctx, uint64_t* ns, int cap);
  * score's error bound (2^-14 |r| |c|) of the best score are re-ranked by their
  * fp32 distance (a fixed summation order), so the code is the exhaustive fp32
  * argmin (up to that order's rounding) unless two codewords of the nearest's
- * class score within that error of it.  This form takes 4 * 8 * Cb * D + 32 * Cb bytes of scratch from
- * the device's stream-ordered pool and frees it on the stream.  Otherwise every
- * distance is computed exactly in fp32 on the CUDA cores.
+ * class score within that error of it.  Up to D of about 520, CTAs work in
+ * pairs (32 frames per pair, every other codeword tile per CTA) that exchange
+ * each frame's winner through global memory, in cooperative launches of at
+ * most the device's co-resident grid (2432 frames per launch on 152 SMs); a
+ * larger D takes one CTA per 16 frames.  Codebooks of 2^24 or more codewords
+ * use the CUDA-core form.  The tensor-core form takes about 4 * 8 * Cb * D +
+ * 32 * Cb bytes of scratch (plus 1 KB per CTA pair) from the device's
+ * stream-ordered pool and frees it on the stream.  Otherwise every distance is
+ * computed exactly in fp32 on the CUDA cores.
  * Enqueues and returns; MFS_E_ARG on bad sizes, alignment or NULL pointers;
- * MFS_E_CUDA if the scratch or the launch fails (mfs_last_error(NULL) gives the
+ * MFS_E_CUDA if the scratch or a launch fails (mfs_last_error(NULL) gives the
  * reason).  A frame whose distances are all NaN gets code 0x7fffffff; on the
  * tensor-core form, if one of the kernel's internal waits gives up (about 2 s:
- * a stalled device), the frames of the CTAs that saw it get code -1. */
+ * a stalled device), the frames of the groups that saw it get code -1. */
 #define MFS_RVQ_MAX_DIM 1024
 int mfs_rvq_encode(const float* z_sem, const float* z_ac, int T, int D, const float* codebooks, int Cb,
                    int32_t* codes, void* cuda_stream);
